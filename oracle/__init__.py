@@ -1,0 +1,165 @@
+"""Python access to the plain-C fp64 oracle (``oracle/aq_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by ``__graft_entry__.smoke()``
+and by the CPU-baseline leg of ``bench.py``.  The product package never
+imports it.  It shares no code with the CUDA path; the only module both sides
+use is ``workloads`` (seeded inputs, no method arithmetic).
+
+Every function here is a thin ctypes call into the C file.  fp16 / bf16
+inputs are widened to float64 before the call (exactly, so the oracle sees the
+very values the GPU sees).  The definitions it follows are on the mlx-bun
+pages, @mlx-bun/inference 1.0.0, kernels/quantization/: the LSB-first bit
+stream of a 64-value group (affine-split-mma.ts, helper affine_unit), 2*B
+words per group (affine3-mma.ts / affine4-mma.ts), and w = scale*q + bias.
+
+Parity pins (tests/test_oracle_pins.py) tie every function to something
+other than itself: hand-derived packed words, a bit-by-bit brute force, round
+trips, closed forms and invariants.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "aq_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libaq_oracle.so")
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (plain C, -O2, no fast-math)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+           "-fno-fast-math", "-ffp-contract=off", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64, i32 = ctypes.c_int64, ctypes.c_int
+            p = ctypes.c_void_p
+            lib.oracle_words_per_row.argtypes = [i64, i32]
+            lib.oracle_words_per_row.restype = i64
+            lib.oracle_pack.argtypes = [p, i64, i64, i32, p]
+            lib.oracle_unpack.argtypes = [p, i64, i64, i32, p]
+            lib.oracle_dequant.argtypes = [p, p, p, i64, i64, i32, p]
+            lib.oracle_matmul.argtypes = [p, p, p, p, i64, i64, i64, i32, p, p]
+            lib.oracle_matmul_cols.argtypes = [p, p, p, p, i64, i64, i64, i32, p, i64, p, p]
+            lib.oracle_matmul_threads.argtypes = [p, p, p, p, i64, i64, i64, i32, p, p, i32]
+            for f in ("oracle_pack", "oracle_unpack", "oracle_dequant", "oracle_matmul",
+                      "oracle_matmul_cols", "oracle_matmul_threads"):
+                getattr(lib, f).restype = i32
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        raise ValueError(f"oracle {what}: invalid arguments")
+
+
+def words_per_row(K: int, bits: int) -> int:
+    return K * bits // 32
+
+
+def pack(codes: np.ndarray, bits: int) -> np.ndarray:
+    """codes uint8 [N, K] -> words uint32 [N, K*bits/32]."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    N, K = codes.shape
+    out = np.zeros((N, words_per_row(K, bits)), dtype=np.uint32)
+    _check(_load().oracle_pack(_ptr(codes), N, K, bits, _ptr(out)), "pack")
+    return out
+
+
+def unpack(words: np.ndarray, K: int, bits: int) -> np.ndarray:
+    """words uint32 [N, K*bits/32] -> codes uint8 [N, K]."""
+    words = np.ascontiguousarray(words, dtype=np.uint32)
+    N = words.shape[0]
+    if words.shape[1] != words_per_row(K, bits):
+        raise ValueError("words has the wrong row length for K and bits")
+    out = np.zeros((N, K), dtype=np.uint8)
+    _check(_load().oracle_unpack(_ptr(words), N, K, bits, _ptr(out)), "unpack")
+    return out
+
+
+def _f64(a: np.ndarray) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def dequant(words: np.ndarray, scales: np.ndarray, biases: np.ndarray, K: int,
+            bits: int) -> np.ndarray:
+    """Dense W [N, K] in float64.  scales/biases: any float dtype (widened)."""
+    words = np.ascontiguousarray(words, dtype=np.uint32)
+    s, b = _f64(scales), _f64(biases)
+    N = words.shape[0]
+    out = np.zeros((N, K), dtype=np.float64)
+    _check(_load().oracle_dequant(_ptr(words), _ptr(s), _ptr(b), N, K, bits, _ptr(out)),
+           "dequant")
+    return out
+
+
+def matmul(x: np.ndarray, words: np.ndarray, scales: np.ndarray, biases: np.ndarray,
+           bits: int, threads: int = 1):
+    """y = x . dequant(W)^T in float64, and bound = sum_k |x*w|.
+
+    x: float64 [M, K] (use workloads.to_f64 for fp16 / bf16 bit patterns).
+    Returns (y [M, N], bound [M, N]).
+    """
+    x = _f64(x)
+    words = np.ascontiguousarray(words, dtype=np.uint32)
+    s, b = _f64(scales), _f64(biases)
+    M, K = x.shape
+    N = words.shape[0]
+    y = np.zeros((M, N), dtype=np.float64)
+    bound = np.zeros((M, N), dtype=np.float64)
+    lib = _load()
+    if threads > 1:
+        rc = lib.oracle_matmul_threads(_ptr(x), _ptr(words), _ptr(s), _ptr(b), M, N, K, bits,
+                                       _ptr(y), _ptr(bound), threads)
+    else:
+        rc = lib.oracle_matmul(_ptr(x), _ptr(words), _ptr(s), _ptr(b), M, N, K, bits,
+                               _ptr(y), _ptr(bound))
+    _check(rc, "matmul")
+    return y, bound
+
+
+def matmul_cols(x: np.ndarray, words: np.ndarray, scales: np.ndarray, biases: np.ndarray,
+                bits: int, cols: Sequence[int]):
+    """Only output columns `cols`: returns (y [M, len(cols)], bound [M, len(cols)])."""
+    x = _f64(x)
+    words = np.ascontiguousarray(words, dtype=np.uint32)
+    s, b = _f64(scales), _f64(biases)
+    c = np.ascontiguousarray(cols, dtype=np.int64)
+    M, K = x.shape
+    N = words.shape[0]
+    y = np.zeros((M, len(c)), dtype=np.float64)
+    bound = np.zeros((M, len(c)), dtype=np.float64)
+    _check(_load().oracle_matmul_cols(_ptr(x), _ptr(words), _ptr(s), _ptr(b), M, N, K, bits,
+                                      _ptr(c), len(c), _ptr(y), _ptr(bound)), "matmul_cols")
+    return y, bound
+
+
+def tolerance(bound: np.ndarray) -> np.ndarray:
+    """Per-element acceptance bound |y - y_ref| <= 2e-3 * sum|x*w| + 1e-5."""
+    return 2e-3 * bound + 1e-5

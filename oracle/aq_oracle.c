@@ -1,0 +1,202 @@
+/*
+ * Reference oracle for the affine group-64 quantized matmul y = x . W^T.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is used by tests/, by the smoke check
+ * and by the CPU-baseline leg of bench.py.  The product library never links,
+ * loads or calls it, and it shares no code with the CUDA path.
+ *
+ * It is plain, slow and written to be checked by eye against the definition
+ * of the format on the mlx-bun pages (@mlx-bun/inference 1.0.0,
+ * kernels/quantization/*):
+ *
+ *  - affine-split-mma.ts, helper affine_unit: value v of a 64-value group is
+ *    bits [v*B, v*B + B) of the group's LSB-first bit stream, and may straddle
+ *    two 32-bit words;
+ *  - affine3-mma.ts / affine4-mma.ts (helpers affine_q3 / affine_q4): a group
+ *    is 2*B consecutive uint32 words, so a row of K values is K*B/32 words;
+ *  - affine3-rows.ts / affine4-rows.ts header comments: eight 3-bit values in
+ *    three little-endian bytes, eight 4-bit values per little-endian word;
+ *  - every kernel: scales and biases are [N, K/64], and a weight is
+ *    w = scale * q + bias (the mma kernels' fma(s, q, b)).
+ *
+ * All floating-point arithmetic is in double precision, summing over k in
+ * ascending order.  Inputs arrive as doubles: the fp16 / bf16 values of x,
+ * scales and biases widen to double exactly, so nothing is lost on the way in.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_GROUP 64
+
+static int valid_shape(int64_t N, int64_t K, int bits) {
+    if (N < 0 || K < 0) return 0;
+    if (K % ORACLE_GROUP != 0) return 0;
+    if (bits != 3 && bits != 4) return 0;
+    return 1;
+}
+
+/* Words per row: K values of B bits each, 32 bits per word. */
+int64_t oracle_words_per_row(int64_t K, int bits) { return K * bits / 32; }
+
+/*
+ * Pack: code v of a row becomes bits [v*B, v*B+B) of the row's bit stream;
+ * stream bit i lives in word i/32 at bit i%32 (least significant first).
+ * Only the low B bits of each code are used.
+ */
+int oracle_pack(const uint8_t *codes, int64_t N, int64_t K, int bits, uint32_t *words) {
+    if (!valid_shape(N, K, bits)) return 1;
+    const int64_t wpr = oracle_words_per_row(K, bits);
+    const uint32_t mask = (1u << bits) - 1u;
+    memset(words, 0, (size_t)(N * wpr) * sizeof(uint32_t));
+    for (int64_t n = 0; n < N; ++n) {
+        uint32_t *row = words + n * wpr;
+        for (int64_t v = 0; v < K; ++v) {
+            const uint32_t q = codes[n * K + v] & mask;
+            const int64_t bit = v * bits;
+            const int64_t w = bit / 32;
+            const int off = (int)(bit % 32);
+            row[w] |= q << off;
+            if (off + bits > 32) row[w + 1] |= q >> (32 - off);
+        }
+    }
+    return 0;
+}
+
+/* Code v of row n, read back from the bit stream (the inverse of pack). */
+static uint32_t oracle_code(const uint32_t *row, int64_t v, int bits) {
+    const int64_t bit = v * bits;
+    const int64_t w = bit / 32;
+    const int off = (int)(bit % 32);
+    uint32_t q = row[w] >> off;
+    if (off + bits > 32) q |= row[w + 1] << (32 - off);
+    return q & ((1u << bits) - 1u);
+}
+
+int oracle_unpack(const uint32_t *words, int64_t N, int64_t K, int bits, uint8_t *codes) {
+    if (!valid_shape(N, K, bits)) return 1;
+    const int64_t wpr = oracle_words_per_row(K, bits);
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t v = 0; v < K; ++v)
+            codes[n * K + v] = (uint8_t)oracle_code(words + n * wpr, v, bits);
+    return 0;
+}
+
+/* Dequantise: W[n][k] = scale[n][k/64] * q[n][k] + bias[n][k/64]. */
+int oracle_dequant(const uint32_t *words, const double *scales, const double *biases,
+                   int64_t N, int64_t K, int bits, double *W) {
+    if (!valid_shape(N, K, bits)) return 1;
+    const int64_t wpr = oracle_words_per_row(K, bits);
+    const int64_t G = K / ORACLE_GROUP;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k) {
+            const int64_t g = k / ORACLE_GROUP;
+            const double q = (double)oracle_code(words + n * wpr, k, bits);
+            W[n * K + k] = scales[n * G + g] * q + biases[n * G + g];
+        }
+    return 0;
+}
+
+/*
+ * One output element and its error scale:
+ *   y[m][n]     = sum_k x[m][k] * (scale[n][g(k)] * q[n][k] + bias[n][g(k)])
+ *   bound[m][n] = sum_k |x[m][k] * w[n][k]|
+ */
+static void oracle_element(const double *xrow, const uint32_t *wrow, const double *srow,
+                           const double *brow, int64_t K, int bits, double *y, double *bound) {
+    double acc = 0.0, mag = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        const int64_t g = k / ORACLE_GROUP;
+        const double w = srow[g] * (double)oracle_code(wrow, k, bits) + brow[g];
+        const double p = xrow[k] * w;
+        acc += p;
+        mag += fabs(p);
+    }
+    *y = acc;
+    if (bound) *bound = mag;
+}
+
+/* y[M][N] (and bound[M][N] if non-null) for all outputs, single-threaded. */
+int oracle_matmul(const double *x, const uint32_t *words, const double *scales,
+                  const double *biases, int64_t M, int64_t N, int64_t K, int bits,
+                  double *y, double *bound) {
+    if (!valid_shape(N, K, bits) || M < 0) return 1;
+    const int64_t wpr = oracle_words_per_row(K, bits);
+    const int64_t G = K / ORACLE_GROUP;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            oracle_element(x + m * K, words + n * wpr, scales + n * G, biases + n * G, K, bits,
+                           &y[m * N + n], bound ? &bound[m * N + n] : NULL);
+    return 0;
+}
+
+/*
+ * The same elements for a chosen list of output columns: y[m][j] is output
+ * column cols[j].  Used to check sampled outputs of full-size problems.
+ */
+int oracle_matmul_cols(const double *x, const uint32_t *words, const double *scales,
+                       const double *biases, int64_t M, int64_t N, int64_t K, int bits,
+                       const int64_t *cols, int64_t ncols, double *y, double *bound) {
+    if (!valid_shape(N, K, bits) || M < 0) return 1;
+    const int64_t wpr = oracle_words_per_row(K, bits);
+    const int64_t G = K / ORACLE_GROUP;
+    for (int64_t j = 0; j < ncols; ++j)
+        if (cols[j] < 0 || cols[j] >= N) return 1;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t j = 0; j < ncols; ++j) {
+            const int64_t n = cols[j];
+            oracle_element(x + m * K, words + n * wpr, scales + n * G, biases + n * G, K, bits,
+                           &y[m * ncols + j], bound ? &bound[m * ncols + j] : NULL);
+        }
+    return 0;
+}
+
+/*
+ * Row-parallel form of oracle_matmul: output columns are dealt out to
+ * nthreads POSIX threads in contiguous blocks.  Every element is computed by
+ * exactly the same oracle_element call, so the result is identical to the
+ * single-threaded one.  Used for large parity checks and the CPU baseline.
+ */
+struct oracle_job {
+    const double *x;
+    const uint32_t *words;
+    const double *scales, *biases;
+    int64_t M, N, K;
+    int bits;
+    int64_t n_begin, n_end;
+    double *y, *bound;
+};
+
+static void *oracle_worker(void *arg) {
+    const struct oracle_job *j = (const struct oracle_job *)arg;
+    const int64_t wpr = oracle_words_per_row(j->K, j->bits);
+    const int64_t G = j->K / ORACLE_GROUP;
+    for (int64_t m = 0; m < j->M; ++m)
+        for (int64_t n = j->n_begin; n < j->n_end; ++n)
+            oracle_element(j->x + m * j->K, j->words + n * wpr, j->scales + n * G,
+                           j->biases + n * G, j->K, j->bits, &j->y[m * j->N + n],
+                           j->bound ? &j->bound[m * j->N + n] : NULL);
+    return NULL;
+}
+
+int oracle_matmul_threads(const double *x, const uint32_t *words, const double *scales,
+                          const double *biases, int64_t M, int64_t N, int64_t K, int bits,
+                          double *y, double *bound, int nthreads) {
+    if (!valid_shape(N, K, bits) || M < 0) return 1;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    pthread_t tid[256];
+    int running[256];
+    struct oracle_job jobs[256];
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t] = (struct oracle_job){x, words, scales, biases, M, N, K, bits,
+                                      N * t / nthreads, N * (t + 1) / nthreads, y, bound};
+        running[t] = pthread_create(&tid[t], NULL, oracle_worker, &jobs[t]) == 0;
+        if (!running[t]) oracle_worker(&jobs[t]); /* no thread available: run it here */
+    }
+    for (int t = 0; t < nthreads; ++t)
+        if (running[t]) pthread_join(tid[t], NULL);
+    return 0;
+}
