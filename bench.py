@@ -1,0 +1,466 @@
+"""Benchmark: affine group-64 quantized matmul y = x . W^T on GB300.
+
+Default workload: the 4-bit decode GEMV (N=4096, K=4096, one bf16 activation
+row).  One step is one call of the library (one pass of the hot path over one
+activation batch).  The timed region holds exactly `--steps` calls, captured
+in CUDA graphs and cycling through enough copies of the weights that their
+total exceeds twice the L2 size (every call reads its weights from HBM).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decode|small|split3:I|layer:I|prefill:I] [--all]
+
+Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs an
+independent replica on its own GPU ("replicas only": the method needs no
+exchange between GPUs); the time is the maximum over ranks.
+
+--impl reference times the fp64 C oracle on the host cores instead (the
+reference arm of this method has no GPU implementation to run): each step is
+a bounded sample of output columns of the same workload, scaled to the
+metric's unit.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = ("µs/call and effective HBM GB/s (fraction of roofline), 3/4-bit group-64 "
+          "y=x·Wᵀ, M=1..512")
+DEFAULT_WORKLOAD = "decode"
+GRAPH_CHUNK = 1024
+
+
+def parse_workload(spec: str):
+    name, _, idx = spec.partition(":")
+    return name, int(idx or 0)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+def traffic_record():
+    """dram bytes per launch from the committed ncu summary, if the kernel
+    source it was taken on is unchanged (source hash recorded beside it)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        rec = {}
+        for line in open(path):
+            if "=" in line and not line.startswith("#"):
+                k, v = line.strip().split("=", 1)
+                rec[k.strip()] = v.strip()
+    except OSError:
+        return {}
+    src = os.path.join(ROOT, "quantized_matmul_affine_gb300", "csrc")
+    h = hashlib.sha256()
+    for fn in sorted(os.listdir(src)):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(src, fn), "rb").read())
+    if rec.get("csrc_sha256") != h.hexdigest():
+        return {}
+    return rec
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        t0, t1 = (self.marks + [0, 0])[:2] if len(self.marks) >= 2 else (0, time.time())
+        inside, near = [], []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            near.append(parts)
+            if t0 <= ts <= t1 + 0.2:
+                inside.append(parts)
+        use = inside or near[-3:]
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(p[1]) for p in use if p[1].replace(".", "").isdigit()]
+        mx = [float(p[2]) for p in use if p[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in use for i in range(4)
+                          if p[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside), "power_w_max": max(
+                    (float(p[3]) for p in use if p[3].replace(".", "").isdigit()), default=None)}
+
+
+def device_problem(p, copies, torch, aq):
+    """Pack the weights on the device and replicate them `copies` times."""
+    codes = torch.from_numpy(p.codes).cuda()
+    Wq = aq.aq_pack(codes, p.bits)
+    del codes
+    s = torch.from_numpy(p.scales).cuda()
+    b = torch.from_numpy(p.biases).cuda()
+    xt = torch.from_numpy(p.x_bits.view(np.int16)).cuda()
+    x = xt.view(torch.bfloat16 if p.x_dtype == "bf16" else torch.float16)
+    ws = [(Wq, s, b)] + [(Wq.clone(), s.clone(), b.clone()) for _ in range(copies - 1)]
+    return x, ws
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import quantized_matmul_affine_gb300 as aq
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.cuda.current_device()
+    props = torch.cuda.get_device_properties(dev)
+    name, idx = parse_workload(args.workload)
+    p = workloads.workload(name, idx)
+    bytes_call = workloads.algorithmic_bytes(p.M, p.N, p.K, p.bits)
+    flops_call = workloads.flops(p.M, p.N, p.K)
+    wbytes = p.N * p.K * p.bits // 8 + 4 * p.N * p.G
+    l2 = getattr(props, "L2_cache_size", 126 * 1024 * 1024)
+    copies = max(2, -(-2 * l2 // wbytes) + 1)
+    x, ws = device_problem(p, copies, torch, aq)
+    fn = aq.aq_matmul_bf16 if p.x_dtype == "bf16" else aq.aq_matmul
+    ys = [torch.empty((p.M, p.N), dtype=x.dtype, device="cuda") for _ in range(copies)]
+    variant = aq.aq_select(p.M, p.N, p.K, p.bits, aq.AQ_BF16 if p.x_dtype == "bf16" else aq.AQ_F16)
+    stream = torch.cuda.Stream()
+
+    def capture(ncalls, start):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(ncalls):
+                    c = (start + i) % copies
+                    Wq, s, b = ws[c]
+                    fn(x, Wq, s, b, p.bits, out=ys[c], stream=stream)
+        return g
+
+    # eager sanity call, then graphs: full chunks plus a remainder
+    with torch.cuda.stream(stream):
+        fn(x, *ws[0], p.bits, out=ys[0], stream=stream)
+    torch.cuda.synchronize()
+    chunk = min(GRAPH_CHUNK, max(1, args.steps))
+    g_chunk = capture(chunk, 0)
+    rem = args.steps % chunk
+    g_rem = capture(rem, 0) if rem else None
+    warm_chunk = min(chunk, max(1, args.warmup))
+    g_warm = capture(warm_chunk, 0)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    with torch.cuda.stream(stream):
+        done = 0
+        while done < args.warmup:
+            g_warm.replay()
+            done += warm_chunk
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(str(props.uuid) if hasattr(props, "uuid") else str(dev))
+    if not str(sampler.gpu_id).startswith("GPU-"):
+        sampler.gpu_id = "GPU-" + str(sampler.gpu_id)
+    sampler.start()
+    time.sleep(0.5)
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.mark()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps // chunk):
+            g_chunk.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark()
+    barrier()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    us_call = ms * 1e3 / args.steps  # per call on one GPU
+    value = us_call / world          # whole job: time per call across all replicas
+
+    # hot-L2 context: the same call on one weight copy, back to back
+    g_hot = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g_hot, stream=stream):
+            for _ in range(256):
+                fn(x, *ws[0], p.bits, out=ys[0], stream=stream)
+        g_hot.replay()
+        torch.cuda.synchronize()
+        h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        h0.record(stream)
+        for _ in range(8):
+            g_hot.replay()
+        h1.record(stream)
+    torch.cuda.synchronize()
+    us_hot = h0.elapsed_time(h1) * 1e3 / (8 * 256)
+
+    # end to end through the host entry point: pinned x in, pinned y out
+    e2e_steps = max(1, min(args.steps, 2000))
+    x_host = x.cpu().pin_memory()
+    y_host = torch.empty((p.M, p.N), dtype=x.dtype).pin_memory()
+    x_dev = torch.empty_like(x)
+    y_dev = torch.empty((p.M, p.N), dtype=x.dtype, device="cuda")
+    for _ in range(min(20, e2e_steps)):
+        aq.aq_matmul_host(x_host, *ws[0], p.bits, y_host, x_dev, y_dev, stream=stream)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        aq.aq_matmul_host(x_host, *ws[i % copies], p.bits, y_host, x_dev, y_dev, stream=stream)
+    torch.cuda.synchronize()
+    e2e_us = (time.perf_counter() - t0) * 1e6 / e2e_steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_us], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_us = float(t.item())
+
+    err = aq.aq_device_error()
+    hbm, tc, src = peaks()
+    t_s = us_call * 1e-6
+    bound = "hbm" if bytes_call / (hbm * 1e9) >= flops_call / (tc * 1e12) else "tensor"
+    if bound == "hbm":
+        achieved, peak, unit = bytes_call / t_s / 1e9, hbm, "GB/s"
+    else:
+        achieved, peak, unit = flops_call / t_s / 1e12, tc, "TFLOP/s"
+    rec = traffic_record()
+    traffic = None
+    if rec.get("workload") == args.workload and "dram_bytes_per_launch" in rec:
+        traffic = float(rec["dram_bytes_per_launch"])
+    t_roof = max(bytes_call / (hbm * 1e9), flops_call / (tc * 1e12))
+    line = {
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "us/call",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": us_call / 1e3,
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": p.x_dtype,
+        "data": "synthetic",
+        "config": {
+            "workload": f"{name}[{idx}]: {p.bits}-bit affine group-64, N={p.N}, K={p.K}, "
+                        f"M={p.M}, x {p.x_dtype}",
+            "M": p.M, "N": p.N, "K": p.K, "bits": p.bits, "x_dtype": p.x_dtype,
+            "variant": aq.aq_variant_name(variant),
+            "l2": f"cold: {copies} rotating weight copies, {copies * wbytes / 1e6:.0f} MB "
+                  f"> 2x L2 ({l2 / 1e6:.0f} MB)",
+            "timing": f"CUDA events on the launching stream around {args.steps} calls "
+                      f"replayed from CUDA graphs of {chunk}",
+            "parallelism": f"replicas x{world}",
+        },
+        "effective_gbs": round(bytes_call / t_s / 1e9, 1),
+        "tflops": round(flops_call / t_s / 1e12, 3),
+        "roofline_time_us": round(t_roof * 1e6, 3),
+        "roofline_frac_nominal_8tbs": round(bytes_call / t_s / 8e12, 4) if bound == "hbm" else None,
+        "hot_l2_us_per_call": round(us_hot, 4),
+        "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"{src} (MEASURED_PEAKS.json)" if src == "measured"
+                     else "fallback",
+                     "algorithmic_bytes_per_launch": bytes_call,
+                     "flops_per_launch": flops_call},
+        "e2e": {"value": round(e2e_us / world, 3), "unit": "us/call",
+                "h2d_bytes_per_step": p.M * p.K * 2, "d2h_bytes_per_step": p.M * p.N * 2,
+                "path": "aq_matmul_host (pinned x -> device, matmul, device -> pinned y, sync)"},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "device_error": err,
+    }
+    return line, p
+
+
+def cpu_sample_time(p, budget_s, threads):
+    """Time the oracle on a column sample of p; returns (us per full call, desc)."""
+    import oracle
+    words = oracle.pack(p.codes, p.bits)
+    x = p.x_f64()
+    cols = np.arange(min(p.N, 64))
+    t0 = time.perf_counter()
+    oracle.matmul_cols(x, words, p.scales, p.biases, p.bits, cols)
+    t_col = (time.perf_counter() - t0) / len(cols)
+    full = t_col * p.N / max(1, threads)
+    reps = max(1, int(budget_s / max(full, 1e-6)))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.matmul(x, words, p.scales, p.biases, p.bits, threads=threads)
+    dt = (time.perf_counter() - t0) / reps
+    return dt * 1e6, f"{reps} full calls of the workload ({p.M}x{p.N}x{p.K}) on {threads} threads"
+
+
+def run_reference(args, rank, world):
+    """The oracle on the host cores, as the reference arm."""
+    import oracle
+    oracle.build()
+    name, idx = parse_workload(args.workload)
+    p = workloads.workload(name, idx)
+    words = oracle.pack(p.codes, p.bits)
+    x = p.x_f64()
+    threads = os.cpu_count() or 1
+    # calibrate: seconds per output column on all threads
+    cols = np.arange(min(p.N, 256))
+    t0 = time.perf_counter()
+    oracle.matmul_cols(x, words, p.scales, p.biases, p.bits, cols)
+    t_col = (time.perf_counter() - t0) / len(cols) / threads
+    total = args.steps + args.warmup
+    per_step_budget = 90.0 / max(1, total)
+    ncols = int(min(p.N, max(threads, per_step_budget / max(t_col, 1e-9))))
+    rng = np.random.default_rng(0)
+    step_times = []
+    for i in range(total):
+        start = int(rng.integers(0, p.N - ncols + 1))
+        c = slice(start, start + ncols)  # a random window of output columns
+        sub_words = np.ascontiguousarray(words[c])
+        t0 = time.perf_counter()
+        oracle.matmul(x, sub_words, p.scales[c], p.biases[c], p.bits, threads=threads)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            step_times.append(dt * p.N / ncols)
+    us = statistics.mean(step_times) * 1e6
+    sample = (f"each step: {ncols} of {p.N} output columns (all {p.M} rows), scaled by "
+              f"N/{ncols}; {threads} threads")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(us, 3),
+        "unit": "us/call",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": us / 1e3,
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{name}[{idx}]: {p.bits}-bit affine group-64, N={p.N}, K={p.K}, "
+                               f"M={p.M}, x {p.x_dtype}",
+                   "M": p.M, "N": p.N, "K": p.K, "bits": p.bits, "x_dtype": p.x_dtype,
+                   "implementation": "fp64 C oracle (oracle/aq_oracle.c) on host cores"},
+        "cpu_baseline": {"value": round(us, 3), "unit": "us/call", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(us, 3), "unit": "us/call", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200000)
+    ap.add_argument("--warmup", type=int, default=2048)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of host time for the cpu_baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--all", action="store_true", help="one line per workload (not the default)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    specs = [args.workload]
+    if args.all:
+        specs = [f"{n}:{i}" for n, c in workloads.WORKLOADS.items() for i in range(len(c))]
+    for spec in specs:
+        args.workload = spec
+        line, p = run_ours(args, rank, world, local_rank)
+        if rank == 0:
+            if world == 1 and not args.no_cpu_baseline and not args.all:
+                import oracle
+                oracle.build()
+                threads = os.cpu_count() or 1
+                us, desc = cpu_sample_time(p, args.cpu_budget, threads)
+                line["cpu_baseline"] = {"value": round(us, 1), "unit": "us/call",
+                                        "cores": threads, "kind": "oracle", "sample": desc}
+            print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

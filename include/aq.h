@@ -1,0 +1,176 @@
+/*
+ * aq.h — C ABI of libaq: y = x . W^T over MLX-style affine group-64 weights
+ * at 3 or 4 bits, on one NVIDIA GB300 (sm_103a).
+ *
+ * Weight format (mlx-bun pages, @mlx-bun/inference 1.0.0,
+ * kernels/quantization/affine-split-mma.ts helper affine_unit and
+ * affine3-mma.ts / affine4-mma.ts helpers affine_q3 / affine_q4):
+ *   - W has N rows of K values; K is a multiple of 64 (one group = 64 values);
+ *   - a row's codes form one LSB-first bit stream: code v occupies bits
+ *     [v*bits, v*bits + bits); stream bit i is bit i%32 of uint32 word i/32;
+ *     so one group is 2*bits words and a row is K*bits/32 words (row-major
+ *     [N][K*bits/32]); 3-bit codes may straddle two words;
+ *   - scales and biases are fp16 [N][K/64]; a weight dequantises to
+ *     w[n][k] = scale[n][k/64] * q[n][k] + bias[n][k/64].
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named *_dev are DEVICE pointers (cudaMalloc / torch tensors);
+ *     pointers named *_host are HOST pointers.  The caller owns all memory;
+ *     the library borrows pointers until the work queued on `stream`
+ *     completes and never frees them.  Arrays are dense and row-major.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is queued asynchronously; no entry point synchronises
+ *     the device except aq_matmul_host (which synchronises `stream`) and
+ *     aq_device_error.
+ *   - The library allocates no device memory in any entry point.
+ *   - Arguments are validated before anything is queued; a bad argument
+ *     returns an error status and queues nothing.  Launch failures return
+ *     AQ_ERR_CUDA.  Faults that happen later on the device surface at the
+ *     caller's next synchronisation, as with any CUDA call.  Nothing prints.
+ *   - Entry points are thread-safe when different threads use different
+ *     streams; results do not depend on the thread or stream.
+ *   - Results are deterministic: the same inputs give bit-identical outputs,
+ *     call after call (fixed-order reductions, no atomics on data).
+ */
+#ifndef AQ_H
+#define AQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum aq_status {
+    AQ_OK = 0,
+    AQ_ERR_INVALID_ARG = 1, /* null pointer, negative size, bits not 3/4, K % 64 != 0 */
+    AQ_ERR_UNSUPPORTED = 2, /* valid but not served (e.g. an explicit variant that cannot run this shape) */
+    AQ_ERR_MISALIGNED = 3,  /* a pointer is not aligned to its element size */
+    AQ_ERR_CUDA = 4,        /* a CUDA runtime call failed (launch, copy, attribute) */
+    AQ_ERR_NOMEM = 5,       /* reserved: the library allocates nothing today */
+    AQ_ERR_DEVICE = 6       /* a kernel reported a device-side error (see aq_device_error) */
+} aq_status;
+
+/* Element type of x and y. */
+typedef enum aq_dtype { AQ_F16 = 0, AQ_BF16 = 1 } aq_dtype;
+
+/* Kernel variants, for aq_matmul_variant, aq_select and aq_stats. */
+typedef enum aq_variant {
+    AQ_VARIANT_AUTO = -1,   /* the dispatch rule picks */
+    AQ_VARIANT_GENERIC = 0, /* plain-load CUDA-core kernel: any K % 64 == 0, any alignment */
+    AQ_VARIANT_QMV = 1,     /* small-M: bulk-async staged weights, warp MMA, factored dequant */
+    AQ_VARIANT_TC = 2,      /* large-M: tcgen05 MMA with TMEM accumulators */
+    AQ_NUM_VARIANTS = 3
+} aq_variant;
+
+/*
+ * aq_pack — pack integer codes into the bit stream described above.
+ *   codes_dev  uint8 [N][K], device; only the low `bits` bits of each code
+ *              are used (higher bits are ignored).
+ *   words_dev  uint32 [N][K*bits/32], device, written entirely.
+ * Errors: AQ_ERR_INVALID_ARG if N < 0, K < 0, K % 64 != 0, bits not in {3,4},
+ * or a pointer is NULL while N*K > 0; AQ_ERR_MISALIGNED if words_dev is not
+ * 4-byte aligned.  N == 0 or K == 0 queues nothing and returns AQ_OK.
+ */
+aq_status aq_pack(const uint8_t *codes_dev, int64_t N, int64_t K, int bits,
+                  uint32_t *words_dev, void *stream);
+
+/*
+ * aq_matmul — y[M][N] = x[M][K] . dequant(W)^T with fp16 x and fp16 y.
+ * aq_matmul_bf16 — the same with bf16 x and bf16 y.
+ *   x_dev      [M][K] activations, device.
+ *   Wq_dev     uint32 [N][K*bits/32] packed codes, device.
+ *   scales_dev fp16 [N][K/64], device.   biases_dev fp16 [N][K/64], device.
+ *   out_dev    [M][N], device, caller-allocated; every element is written,
+ *              nothing outside it is.
+ * Accumulation is in fp32 and y is rounded to nearest even.  Any M >= 1,
+ * N >= 1 and K >= 64 with K % 64 == 0 is served; the fast kernels also want
+ * K % 512 == 0 and 16-byte aligned x, Wq, scales, biases and y (other
+ * shapes go to the generic kernel).
+ * Errors: AQ_ERR_INVALID_ARG if M < 1, N < 1, K < 64, K % 64 != 0, bits not
+ * in {3,4} or a pointer is NULL; AQ_ERR_MISALIGNED if a pointer is not
+ * aligned to its element size (2 bytes for x/y/scales/biases, 4 for Wq);
+ * AQ_ERR_CUDA if a launch fails.
+ * Follows affineSplitMma (affine-split-mma.ts): x of any row count times
+ * W^T, y in x's dtype, rows past M never written.
+ */
+aq_status aq_matmul(const void *x_dev, const uint32_t *Wq_dev, const void *scales_dev,
+                    const void *biases_dev, int64_t M, int64_t N, int64_t K, int bits,
+                    void *out_dev, void *stream);
+aq_status aq_matmul_bf16(const void *x_dev, const uint32_t *Wq_dev, const void *scales_dev,
+                         const void *biases_dev, int64_t M, int64_t N, int64_t K, int bits,
+                         void *out_dev, void *stream);
+
+/*
+ * aq_matmul_variant — aq_matmul / aq_matmul_bf16 with the element type as an
+ * argument and, optionally, an explicit kernel variant (AQ_VARIANT_AUTO lets
+ * the dispatch rule choose).  An explicit variant that cannot run the shape
+ * or alignment returns AQ_ERR_UNSUPPORTED and queues nothing.  Same
+ * arguments, ownership and errors as aq_matmul otherwise.
+ */
+aq_status aq_matmul_variant(int variant, int dtype, const void *x_dev, const uint32_t *Wq_dev,
+                            const void *scales_dev, const void *biases_dev, int64_t M,
+                            int64_t N, int64_t K, int bits, void *out_dev, void *stream);
+
+/*
+ * aq_matmul_host — the whole call from host memory: copies x_host to the
+ * caller's device buffer x_dev, runs the matmul (auto dispatch) into out_dev,
+ * copies the result back to out_host, and synchronises `stream`.
+ *   x_host   [M][K] of `dtype`, host (pinned memory makes the copies async).
+ *   x_dev    [M][K] device scratch owned by the caller.
+ *   out_dev  [M][N] device scratch owned by the caller.
+ *   out_host [M][N] of `dtype`, host, written on return.
+ * Weights (Wq_dev, scales_dev, biases_dev) stay resident on the device.
+ * Errors: as aq_matmul, plus AQ_ERR_CUDA if a copy or the synchronisation
+ * fails.
+ */
+aq_status aq_matmul_host(int dtype, const void *x_host, const uint32_t *Wq_dev,
+                         const void *scales_dev, const void *biases_dev, int64_t M, int64_t N,
+                         int64_t K, int bits, void *out_host, void *x_dev, void *out_dev,
+                         void *stream);
+
+/*
+ * aq_select — the variant the dispatch rule picks for a shape, without
+ * launching anything (host logic only; needs no GPU).  Alignment is assumed
+ * to be 16 bytes.  Returns an aq_variant value, or -1 for invalid arguments.
+ */
+int aq_select(int64_t M, int64_t N, int64_t K, int bits, int dtype);
+
+/*
+ * aq_stats — per-variant call counters since load (or the last reset).
+ *   calls  host array of n uint64; element v receives the number of calls
+ *          that launched variant v (n may be less than AQ_NUM_VARIANTS).
+ *   reset  non-zero: set the counters to zero after reading.
+ */
+aq_status aq_stats(uint64_t *calls, int n, int reset);
+
+/*
+ * aq_device_error — read the device-side error word that kernels set when a
+ * bounded wait gives up (a pipeline barrier not completing within its time
+ * limit).  Synchronises the device first.  *code receives 0 when no error
+ * was recorded; non-zero values identify the wait that gave up.  clear != 0
+ * resets the word to 0.
+ */
+aq_status aq_device_error(uint32_t *code, int clear);
+
+/*
+ * aq_free — release library-held resources (cached device attributes and
+ * kernel configuration state).  The library holds no device allocations;
+ * calling aq_free is optional and the library stays usable afterwards.
+ */
+void aq_free(void);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *aq_status_string(aq_status status);
+
+/* Human-readable name of a variant ("generic", "qmv", "tc"); "?" if unknown. */
+const char *aq_variant_name(int variant);
+
+/* Library version string. */
+const char *aq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AQ_H */

@@ -1,0 +1,198 @@
+"""Python binding of libaq (include/aq.h): affine group-64 3/4-bit matmul on GB300.
+
+Argument marshalling only.  Every function has the name of the C entry point
+it calls; tensors are torch tensors (device memory for ``*_dev`` arguments),
+``stream`` defaults to torch's current CUDA stream.  All the work runs in the
+library's CUDA kernels; there is no Python or CPU compute path, and importing
+this package fails if libaq.so cannot be loaded.
+
+    y = aq_matmul(x, Wq, scales, biases, bits)        # fp16 x -> fp16 y
+    y = aq_matmul_bf16(x, Wq, scales, biases, bits)   # bf16 x -> bf16 y
+    Wq = aq_pack(codes, bits)                         # uint8 codes -> uint32 words
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "AqError", "AQ_F16", "AQ_BF16", "AQ_VARIANT_AUTO", "AQ_VARIANT_GENERIC", "AQ_VARIANT_QMV",
+    "AQ_VARIANT_TC", "AQ_NUM_VARIANTS", "aq_pack", "aq_matmul", "aq_matmul_bf16",
+    "aq_matmul_variant", "aq_matmul_host", "aq_select", "aq_stats", "aq_device_error",
+    "aq_free", "aq_status_string", "aq_variant_name", "aq_version", "lib_path", "load",
+]
+
+AQ_OK = 0
+AQ_F16, AQ_BF16 = 0, 1
+AQ_VARIANT_AUTO, AQ_VARIANT_GENERIC, AQ_VARIANT_QMV, AQ_VARIANT_TC = -1, 0, 1, 2
+AQ_NUM_VARIANTS = 3
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+class AqError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {aq_status_string(status)} (status {status})")
+        self.status = status
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libaq.so (building it first if it is missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if build_if_missing and not _build.up_to_date():
+        _build.build()
+    if not os.path.exists(path):
+        raise ImportError(f"libaq.so not built at {path}")
+    lib = ctypes.CDLL(path)
+    p, i64, i32, u32p = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+    sig = {
+        "aq_pack": ([p, i64, i64, i32, p, p], i32),
+        "aq_matmul": ([p, p, p, p, i64, i64, i64, i32, p, p], i32),
+        "aq_matmul_bf16": ([p, p, p, p, i64, i64, i64, i32, p, p], i32),
+        "aq_matmul_variant": ([i32, i32, p, p, p, p, i64, i64, i64, i32, p, p], i32),
+        "aq_matmul_host": ([i32, p, p, p, p, i64, i64, i64, i32, p, p, p, p], i32),
+        "aq_select": ([i64, i64, i64, i32, i32], i32),
+        "aq_stats": ([p, i32, i32], i32),
+        "aq_device_error": ([u32p, i32], i32),
+        "aq_free": ([], None),
+        "aq_status_string": ([i32], ctypes.c_char_p),
+        "aq_variant_name": ([i32], ctypes.c_char_p),
+        "aq_version": ([], ctypes.c_char_p),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    _lib = lib
+    return lib
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(status: int, what: str) -> None:
+    if status != AQ_OK:
+        raise AqError(status, what)
+
+
+def _dev(t: torch.Tensor, name: str) -> int:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def aq_status_string(status: int) -> str:
+    return load().aq_status_string(status).decode()
+
+
+def aq_variant_name(variant: int) -> str:
+    return load().aq_variant_name(variant).decode()
+
+
+def aq_version() -> str:
+    return load().aq_version().decode()
+
+
+def aq_pack(codes: torch.Tensor, bits: int, words: Optional[torch.Tensor] = None,
+            stream=None) -> torch.Tensor:
+    """codes uint8 [N, K] (device) -> words uint32-as-int32 [N, K*bits/32]."""
+    N, K = codes.shape
+    if codes.dtype != torch.uint8:
+        raise ValueError("codes must be uint8")
+    if words is None:
+        words = torch.empty((N, K * bits // 32), dtype=torch.int32, device=codes.device)
+    _check(load().aq_pack(_dev(codes, "codes"), N, K, bits, _dev(words, "words"),
+                          _stream(stream)), "aq_pack")
+    return words
+
+
+def _mm(variant: int, dtype: int, x, Wq, scales, biases, bits, out, stream) -> torch.Tensor:
+    want = torch.float16 if dtype == AQ_F16 else torch.bfloat16
+    if x.dtype != want:
+        raise ValueError(f"x must be {want}")
+    if scales.dtype != torch.float16 or biases.dtype != torch.float16:
+        raise ValueError("scales and biases must be float16")
+    K = x.shape[-1]
+    M = x.numel() // K if K else 0
+    N = scales.shape[0]
+    if out is None:
+        out = torch.empty((*x.shape[:-1], N), dtype=x.dtype, device=x.device)
+    _check(load().aq_matmul_variant(variant, dtype, _dev(x, "x"), _dev(Wq, "Wq"),
+                                    _dev(scales, "scales"), _dev(biases, "biases"), M, N, K,
+                                    bits, _dev(out, "out"), _stream(stream)), "aq_matmul")
+    return out
+
+
+def aq_matmul(x, Wq, scales, biases, bits, out=None, stream=None) -> torch.Tensor:
+    """y = x . dequant(W)^T for fp16 x [..., K]; returns fp16 [..., N]."""
+    return _mm(AQ_VARIANT_AUTO, AQ_F16, x, Wq, scales, biases, bits, out, stream)
+
+
+def aq_matmul_bf16(x, Wq, scales, biases, bits, out=None, stream=None) -> torch.Tensor:
+    """y = x . dequant(W)^T for bf16 x [..., K]; returns bf16 [..., N]."""
+    return _mm(AQ_VARIANT_AUTO, AQ_BF16, x, Wq, scales, biases, bits, out, stream)
+
+
+def aq_matmul_variant(variant, x, Wq, scales, biases, bits, out=None, stream=None):
+    """Explicit kernel variant; the dtype follows x (fp16 or bf16)."""
+    dtype = AQ_BF16 if x.dtype == torch.bfloat16 else AQ_F16
+    return _mm(variant, dtype, x, Wq, scales, biases, bits, out, stream)
+
+
+def aq_matmul_host(x_host: torch.Tensor, Wq, scales, biases, bits, out_host: torch.Tensor,
+                   x_dev: torch.Tensor, out_dev: torch.Tensor, stream=None) -> torch.Tensor:
+    """Host x in, host y out (device staging buffers supplied); synchronises."""
+    dtype = AQ_BF16 if x_host.dtype == torch.bfloat16 else AQ_F16
+    if x_host.is_cuda or out_host.is_cuda:
+        raise ValueError("x_host and out_host must be host tensors")
+    K = x_host.shape[-1]
+    M = x_host.numel() // K
+    N = scales.shape[0]
+    _check(load().aq_matmul_host(dtype, x_host.data_ptr(), _dev(Wq, "Wq"),
+                                 _dev(scales, "scales"), _dev(biases, "biases"), M, N, K, bits,
+                                 out_host.data_ptr(), _dev(x_dev, "x_dev"),
+                                 _dev(out_dev, "out_dev"), _stream(stream)), "aq_matmul_host")
+    return out_host
+
+
+def aq_select(M: int, N: int, K: int, bits: int, dtype: int = AQ_F16) -> int:
+    return load().aq_select(M, N, K, bits, dtype)
+
+
+def aq_stats(reset: bool = False) -> List[int]:
+    buf = (ctypes.c_uint64 * AQ_NUM_VARIANTS)()
+    _check(load().aq_stats(ctypes.cast(buf, ctypes.c_void_p), AQ_NUM_VARIANTS, int(reset)),
+           "aq_stats")
+    return list(buf)
+
+
+def aq_device_error(clear: bool = False) -> int:
+    code = ctypes.c_uint32(0)
+    _check(load().aq_device_error(ctypes.addressof(code), int(clear)), "aq_device_error")
+    return code.value
+
+
+def aq_free() -> None:
+    load().aq_free()
+
+
+load()

@@ -1,0 +1,235 @@
+// C ABI of libaq: argument checks, the dispatch rule, counters, host I/O.
+//
+// The interface follows affineSplitMma on the mlx-bun pages (@mlx-bun/inference
+// 1.0.0, kernels/quantization/affine-split-mma.ts): x with any number of rows
+// times W^T, y in x's dtype, an error for no rows; plus the pack step and the
+// explicit-variant and host-memory entry points described in aq.h.
+#include "aq_internal.h"
+
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+
+namespace aq {
+
+namespace {
+
+std::atomic<uint64_t> g_calls[AQ_NUM_VARIANTS];
+std::atomic<int> g_sms_cache[64];
+
+// Largest M that the small-M kernel takes under the automatic rule, from
+// timings of both kernels on GB300 (see the dispatch table in the design
+// notes).  AQ_QMV_MAX_M overrides it for experiments.
+int qmv_max_m() {
+    static const int v = [] {
+        const char *e = std::getenv("AQ_QMV_MAX_M");
+        if (e && *e) return std::atoi(e);
+        return 32;
+    }();
+    return v;
+}
+
+}  // namespace
+
+int num_sms() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return 152;
+    }
+    int v = g_sms_cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+        cudaGetLastError();
+        return 152;
+    }
+    g_sms_cache[dev].store(v, std::memory_order_relaxed);
+    return v;
+}
+
+// The dispatch rule.  Returns the variant for the arguments (alignment
+// included), never AQ_VARIANT_AUTO.
+static int choose(const MatmulArgs &a) {
+    const bool qmv = qmv_supported(a);
+    const bool tc = tc_supported(a);
+    if (qmv && (a.M <= qmv_max_m() || !tc)) return AQ_VARIANT_QMV;
+    if (tc) return AQ_VARIANT_TC;
+    return AQ_VARIANT_GENERIC;
+}
+
+static aq_status check_args(const MatmulArgs &a) {
+    if (a.M < 1 || a.N < 1 || a.K < 64 || a.K % 64 != 0) return AQ_ERR_INVALID_ARG;
+    if (a.bits != 3 && a.bits != 4) return AQ_ERR_INVALID_ARG;
+    if (a.dtype != AQ_F16 && a.dtype != AQ_BF16) return AQ_ERR_INVALID_ARG;
+    if (!a.x || !a.Wq || !a.scales || !a.biases || !a.out) return AQ_ERR_INVALID_ARG;
+    if (a.M > (int64_t)1 << 31 || a.N > (int64_t)1 << 31 || a.K > (int64_t)1 << 31)
+        return AQ_ERR_UNSUPPORTED;
+    if (!aligned(a.x, 2) || !aligned(a.out, 2) || !aligned(a.scales, 2) || !aligned(a.biases, 2) ||
+        !aligned(a.Wq, 4))
+        return AQ_ERR_MISALIGNED;
+    return AQ_OK;
+}
+
+static aq_status run(int variant, const MatmulArgs &a) {
+    aq_status st = check_args(a);
+    if (st != AQ_OK) return st;
+    if (variant == AQ_VARIANT_AUTO) variant = choose(a);
+    cudaError_t err;
+    switch (variant) {
+        case AQ_VARIANT_GENERIC:
+            if (!generic_supported(a)) return AQ_ERR_UNSUPPORTED;
+            err = generic_launch(a);
+            break;
+        case AQ_VARIANT_QMV:
+            if (!qmv_supported(a)) return AQ_ERR_UNSUPPORTED;
+            err = qmv_launch(a);
+            break;
+        case AQ_VARIANT_TC:
+            if (!tc_supported(a)) return AQ_ERR_UNSUPPORTED;
+            err = tc_launch(a);
+            break;
+        default:
+            return AQ_ERR_INVALID_ARG;
+    }
+    if (err != cudaSuccess) return AQ_ERR_CUDA;
+    g_calls[variant].fetch_add(1, std::memory_order_relaxed);
+    return AQ_OK;
+}
+
+static MatmulArgs make_args(int dtype, const void *x, const uint32_t *Wq, const void *scales,
+                            const void *biases, int64_t M, int64_t N, int64_t K, int bits,
+                            void *out, void *stream) {
+    MatmulArgs a;
+    a.x = x;
+    a.Wq = Wq;
+    a.scales = scales;
+    a.biases = biases;
+    a.out = out;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.bits = bits;
+    a.dtype = dtype;
+    a.stream = static_cast<cudaStream_t>(stream);
+    return a;
+}
+
+}  // namespace aq
+
+using namespace aq;
+
+extern "C" {
+
+aq_status aq_pack(const uint8_t *codes_dev, int64_t N, int64_t K, int bits, uint32_t *words_dev,
+                  void *stream) {
+    if (N < 0 || K < 0 || K % 64 != 0 || (bits != 3 && bits != 4)) return AQ_ERR_INVALID_ARG;
+    if (N == 0 || K == 0) return AQ_OK;
+    if (!codes_dev || !words_dev) return AQ_ERR_INVALID_ARG;
+    if (!aligned(words_dev, 4)) return AQ_ERR_MISALIGNED;
+    if (pack_launch(codes_dev, N, K, bits, words_dev, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return AQ_ERR_CUDA;
+    return AQ_OK;
+}
+
+aq_status aq_matmul(const void *x_dev, const uint32_t *Wq_dev, const void *scales_dev,
+                    const void *biases_dev, int64_t M, int64_t N, int64_t K, int bits,
+                    void *out_dev, void *stream) {
+    return run(AQ_VARIANT_AUTO, make_args(AQ_F16, x_dev, Wq_dev, scales_dev, biases_dev, M, N, K,
+                                          bits, out_dev, stream));
+}
+
+aq_status aq_matmul_bf16(const void *x_dev, const uint32_t *Wq_dev, const void *scales_dev,
+                         const void *biases_dev, int64_t M, int64_t N, int64_t K, int bits,
+                         void *out_dev, void *stream) {
+    return run(AQ_VARIANT_AUTO, make_args(AQ_BF16, x_dev, Wq_dev, scales_dev, biases_dev, M, N, K,
+                                          bits, out_dev, stream));
+}
+
+aq_status aq_matmul_variant(int variant, int dtype, const void *x_dev, const uint32_t *Wq_dev,
+                            const void *scales_dev, const void *biases_dev, int64_t M, int64_t N,
+                            int64_t K, int bits, void *out_dev, void *stream) {
+    if (variant < AQ_VARIANT_AUTO || variant >= AQ_NUM_VARIANTS) return AQ_ERR_INVALID_ARG;
+    return run(variant, make_args(dtype, x_dev, Wq_dev, scales_dev, biases_dev, M, N, K, bits,
+                                  out_dev, stream));
+}
+
+aq_status aq_matmul_host(int dtype, const void *x_host, const uint32_t *Wq_dev,
+                         const void *scales_dev, const void *biases_dev, int64_t M, int64_t N,
+                         int64_t K, int bits, void *out_host, void *x_dev, void *out_dev,
+                         void *stream) {
+    MatmulArgs a = make_args(dtype, x_dev, Wq_dev, scales_dev, biases_dev, M, N, K, bits,
+                             out_dev, stream);
+    aq_status st = check_args(a);
+    if (st != AQ_OK) return st;
+    if (!x_host || !out_host) return AQ_ERR_INVALID_ARG;
+    const size_t xbytes = (size_t)M * (size_t)K * 2, ybytes = (size_t)M * (size_t)N * 2;
+    if (cudaMemcpyAsync(x_dev, x_host, xbytes, cudaMemcpyHostToDevice, a.stream) != cudaSuccess)
+        return AQ_ERR_CUDA;
+    st = run(AQ_VARIANT_AUTO, a);
+    if (st != AQ_OK) return st;
+    if (cudaMemcpyAsync(out_host, out_dev, ybytes, cudaMemcpyDeviceToHost, a.stream) !=
+        cudaSuccess)
+        return AQ_ERR_CUDA;
+    if (cudaStreamSynchronize(a.stream) != cudaSuccess) return AQ_ERR_CUDA;
+    return AQ_OK;
+}
+
+int aq_select(int64_t M, int64_t N, int64_t K, int bits, int dtype) {
+    // Placeholder addresses with 256-byte alignment: the plan only looks at
+    // their alignment, never dereferences them.
+    const uintptr_t fake = 0x100000;
+    MatmulArgs a = make_args(dtype, (const void *)fake, (const uint32_t *)fake, (const void *)fake,
+                             (const void *)fake, M, N, K, bits, (void *)fake, nullptr);
+    if (check_args(a) != AQ_OK) return -1;
+    return choose(a);
+}
+
+aq_status aq_stats(uint64_t *calls, int n, int reset) {
+    if (n < 0 || (n > 0 && !calls)) return AQ_ERR_INVALID_ARG;
+    for (int v = 0; v < AQ_NUM_VARIANTS; ++v) {
+        const uint64_t c = reset ? g_calls[v].exchange(0) : g_calls[v].load();
+        if (v < n) calls[v] = c;
+    }
+    return AQ_OK;
+}
+
+aq_status aq_device_error(uint32_t *code, int clear) {
+    if (!code) return AQ_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return AQ_ERR_CUDA;
+    uint32_t a = 0, b = 0;
+    if (qmv_read_error(&a, clear != 0) != cudaSuccess) return AQ_ERR_CUDA;
+    if (tc_read_error(&b, clear != 0) != cudaSuccess) return AQ_ERR_CUDA;
+    *code = a | b;
+    return AQ_OK;
+}
+
+void aq_free(void) {
+    for (auto &c : g_sms_cache) c.store(0);
+}
+
+const char *aq_status_string(aq_status status) {
+    switch (status) {
+        case AQ_OK: return "ok";
+        case AQ_ERR_INVALID_ARG: return "invalid argument";
+        case AQ_ERR_UNSUPPORTED: return "unsupported shape or variant";
+        case AQ_ERR_MISALIGNED: return "misaligned pointer";
+        case AQ_ERR_CUDA: return "CUDA runtime error";
+        case AQ_ERR_NOMEM: return "out of memory";
+        case AQ_ERR_DEVICE: return "device-side error";
+    }
+    return "unknown status";
+}
+
+const char *aq_variant_name(int variant) {
+    switch (variant) {
+        case AQ_VARIANT_GENERIC: return "generic";
+        case AQ_VARIANT_QMV: return "qmv";
+        case AQ_VARIANT_TC: return "tc";
+    }
+    return "?";
+}
+
+const char *aq_version(void) { return "aq 0.1.0 (sm_103a)"; }
+
+}  // extern "C"

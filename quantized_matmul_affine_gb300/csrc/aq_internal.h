@@ -1,0 +1,56 @@
+// Host-side declarations shared by the translation units of libaq.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/aq.h"
+
+namespace aq {
+
+struct MatmulArgs {
+    const void *x;
+    const uint32_t *Wq;
+    const void *scales;
+    const void *biases;
+    void *out;
+    int64_t M, N, K;
+    int bits;
+    int dtype;  // AQ_F16 / AQ_BF16
+    cudaStream_t stream;
+};
+
+// Device-side error codes (the word read by aq_device_error).  The low byte
+// names the kernel, the next byte the wait that gave up.
+enum : uint32_t {
+    ERR_QMV_FULL = 0x0101,
+    ERR_QMV_EMPTY = 0x0201,
+    ERR_TC_BASE = 0x0002,
+};
+
+// Each returns cudaSuccess, or the launch error.  `supported` reports
+// whether the variant can run the shape/alignment at all.
+bool generic_supported(const MatmulArgs &a);
+cudaError_t generic_launch(const MatmulArgs &a);
+
+bool qmv_supported(const MatmulArgs &a);
+cudaError_t qmv_launch(const MatmulArgs &a);
+
+bool tc_supported(const MatmulArgs &a);
+cudaError_t tc_launch(const MatmulArgs &a);
+
+cudaError_t pack_launch(const uint8_t *codes, int64_t N, int64_t K, int bits, uint32_t *words,
+                        cudaStream_t stream);
+
+// Device error words, one per translation unit that owns bounded waits.
+cudaError_t qmv_read_error(uint32_t *code, bool clear);
+cudaError_t tc_read_error(uint32_t *code, bool clear);
+
+// Number of streaming multiprocessors of the current device (cached).
+int num_sms();
+
+inline bool aligned(const void *p, uintptr_t a) {
+    return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+}  // namespace aq

@@ -1,0 +1,16 @@
+// Large-M kernel (tcgen05 + TMEM): not built yet; the dispatch rule sends
+// every shape to the small-M or generic kernels meanwhile.
+#include "aq_internal.h"
+
+namespace aq {
+
+bool tc_supported(const MatmulArgs &) { return false; }
+
+cudaError_t tc_launch(const MatmulArgs &) { return cudaErrorNotSupported; }
+
+cudaError_t tc_read_error(uint32_t *code, bool) {
+    *code = 0;
+    return cudaSuccess;
+}
+
+}  // namespace aq

@@ -1,0 +1,116 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+* libaq.so loads and exports every function that include/aq.h declares;
+* argument validation rejects bad calls before touching the GPU;
+* the dispatch rule (aq_select) picks the expected kernel per shape.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import quantized_matmul_affine_gb300 as aq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "aq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(aq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = header_functions()
+    for required in ("aq_pack", "aq_matmul", "aq_matmul_bf16", "aq_free", "aq_status_string",
+                     "aq_stats"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(aq.lib_path())
+    missing = [n for n in header_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_has_the_same_names():
+    for n in header_functions():
+        assert hasattr(aq, n), n
+
+
+def test_status_strings_and_version():
+    assert aq.aq_status_string(0) == "ok"
+    assert "invalid" in aq.aq_status_string(1)
+    assert aq.aq_status_string(99) == "unknown status"
+    assert aq.aq_variant_name(aq.AQ_VARIANT_QMV) == "qmv"
+    assert "sm_103a" in aq.aq_version()
+
+
+def _raw():
+    return aq.load()
+
+
+A = 0x100000  # a 256-byte-aligned placeholder address; validation never dereferences
+
+
+@pytest.mark.parametrize("M,N,K,bits,status", [
+    (0, 16, 512, 4, 1),      # no rows (affineSplitMma throws on M < 1)
+    (1, 0, 512, 4, 1),
+    (1, 16, 0, 4, 1),
+    (1, 16, 100, 4, 1),      # K not a multiple of 64
+    (1, 16, 512, 5, 1),      # bits not 3 or 4
+    (1, 16, 512, 2, 1),
+    (-1, 16, 512, 4, 1),
+])
+def test_matmul_rejects_bad_shapes(M, N, K, bits, status):
+    assert _raw().aq_matmul(A, A, A, A, M, N, K, bits, A, None) == status
+
+
+def test_matmul_rejects_null_and_misaligned():
+    lib = _raw()
+    assert lib.aq_matmul(None, A, A, A, 1, 16, 512, 4, A, None) == 1
+    assert lib.aq_matmul(A, A, A, A, 1, 16, 512, 4, None, None) == 1
+    assert lib.aq_matmul(A + 1, A, A, A, 1, 16, 512, 4, A, None) == 3   # x not 2-aligned
+    assert lib.aq_matmul(A, A + 2, A, A, 1, 16, 512, 4, A, None) == 3   # Wq not 4-aligned
+    assert lib.aq_matmul_bf16(A, A, A + 1, A, 1, 16, 512, 4, A, None) == 3
+    assert lib.aq_matmul_variant(7, 0, A, A, A, A, 1, 16, 512, 4, A, None) == 1
+    assert lib.aq_matmul_variant(0, 5, A, A, A, A, 1, 16, 512, 4, A, None) == 1  # bad dtype
+
+
+def test_pack_validation():
+    lib = _raw()
+    assert lib.aq_pack(A, 0, 512, 4, A, None) == 0       # empty: nothing to do
+    assert lib.aq_pack(A, 4, 0, 4, A, None) == 0
+    assert lib.aq_pack(A, 4, 100, 4, A, None) == 1
+    assert lib.aq_pack(A, 4, 64, 6, A, None) == 1
+    assert lib.aq_pack(None, 4, 64, 4, A, None) == 1
+    assert lib.aq_pack(A, 4, 64, 4, A + 2, None) == 3
+
+
+def test_stats_interface():
+    lib = _raw()
+    assert lib.aq_stats(None, -1, 0) == 1
+    assert lib.aq_stats(None, 0, 0) == 0
+    assert len(aq.aq_stats()) == aq.AQ_NUM_VARIANTS
+
+
+# The dispatch rule, on the shapes of the workloads (alignment assumed).
+@pytest.mark.parametrize("M,N,K,bits,variant", [
+    (1, 1024, 512, 4, aq.AQ_VARIANT_QMV),
+    (1, 4096, 4096, 4, aq.AQ_VARIANT_QMV),
+    (1, 10240, 5120, 3, aq.AQ_VARIANT_QMV),
+    (9, 10240, 5120, 3, aq.AQ_VARIANT_QMV),
+    (16, 10240, 5120, 3, aq.AQ_VARIANT_QMV),
+    (1, 5120, 13824, 4, aq.AQ_VARIANT_QMV),
+    (1, 13824, 5120, 4, aq.AQ_VARIANT_QMV),
+    (1, 100, 576, 4, aq.AQ_VARIANT_GENERIC),   # K % 512 != 0 -> generic
+    (3, 7, 64, 3, aq.AQ_VARIANT_GENERIC),
+])
+def test_select(M, N, K, bits, variant):
+    assert aq.aq_select(M, N, K, bits) == variant
+
+
+def test_select_invalid():
+    assert aq.aq_select(0, 16, 512, 4) == -1
+    assert aq.aq_select(1, 16, 512, 7) == -1
