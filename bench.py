@@ -242,6 +242,10 @@ def run_ours(args, rank, world, local_rank):
     value = us_call / world          # whole job: time per call across all replicas
 
     # hot-L2 context: the same call on one weight copy, back to back
+    us_hot, e2e_us = None, None
+    if args.quick:
+        return finish(args, p, name, idx, world, aq, variant, copies, wbytes, l2, chunk, us_call,
+                      value, us_hot, e2e_us, clocks, bytes_call, flops_call)
     g_hot = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         with torch.cuda.graph(g_hot, stream=stream):
@@ -277,7 +281,12 @@ def run_ours(args, rank, world, local_rank):
         t = torch.tensor([e2e_us], device="cuda", dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_us = float(t.item())
+    return finish(args, p, name, idx, world, aq, variant, copies, wbytes, l2, chunk, us_call,
+                  value, us_hot, e2e_us, clocks, bytes_call, flops_call)
 
+
+def finish(args, p, name, idx, world, aq, variant, copies, wbytes, l2, chunk, us_call, value,
+           us_hot, e2e_us, clocks, bytes_call, flops_call):
     err = aq.aq_device_error()
     hbm, tc, src = peaks()
     t_s = us_call * 1e-6
@@ -319,14 +328,15 @@ def run_ours(args, rank, world, local_rank):
         "tflops": round(flops_call / t_s / 1e12, 3),
         "roofline_time_us": round(t_roof * 1e6, 3),
         "roofline_frac_nominal_8tbs": round(bytes_call / t_s / 8e12, 4) if bound == "hbm" else None,
-        "hot_l2_us_per_call": round(us_hot, 4),
+        "hot_l2_us_per_call": round(us_hot, 4) if us_hot is not None else None,
         "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": f"{src} (MEASURED_PEAKS.json)" if src == "measured"
                      else "fallback",
                      "algorithmic_bytes_per_launch": bytes_call,
                      "flops_per_launch": flops_call},
-        "e2e": {"value": round(e2e_us / world, 3), "unit": "us/call",
+        "e2e": {"value": round(e2e_us / world, 3) if e2e_us is not None else None,
+                "unit": "us/call",
                 "h2d_bytes_per_step": p.M * p.K * 2, "d2h_bytes_per_step": p.M * p.N * 2,
                 "path": "aq_matmul_host (pinned x -> device, matmul, device -> pinned y, sync)"},
         "gpu_launches": args.steps,
@@ -421,6 +431,8 @@ def main():
                     help="seconds of host time for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--all", action="store_true", help="one line per workload (not the default)")
+    ap.add_argument("--quick", action="store_true",
+                    help="timed region only: skip the hot-L2, end-to-end and CPU legs")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -448,7 +460,7 @@ def main():
         args.workload = spec
         line, p = run_ours(args, rank, world, local_rank)
         if rank == 0:
-            if world == 1 and not args.no_cpu_baseline and not args.all:
+            if world == 1 and not args.no_cpu_baseline and not args.all and not args.quick:
                 import oracle
                 oracle.build()
                 threads = os.cpu_count() or 1

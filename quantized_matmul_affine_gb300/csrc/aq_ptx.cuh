@@ -147,3 +147,28 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 }
 
 }  // namespace aq
+
+namespace aq {
+
+// ---------------------------------------------------------------------------
+// cp.async (16-byte, L2-only) global -> shared, with commit/wait groups.
+// src_bytes == 0 writes zeros and reads nothing.  (The form with an L2
+// cache-policy operand faulted with an illegal instruction on GB300; the
+// plain zero-fill form is used.)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst_smem)),
+                 "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+}  // namespace aq

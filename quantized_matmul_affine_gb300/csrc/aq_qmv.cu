@@ -1,4 +1,4 @@
-// Small-M kernel ("qmv"): y = x . W^T for 1..32 activation rows per launch
+// Small-M kernel ("qmv"): y = x . W^T for up to 32 activation rows per launch
 // block, streaming the packed weights once per call.
 //
 // Method (mlx-bun pages, @mlx-bun/inference 1.0.0, kernels/quantization/):
@@ -6,34 +6,36 @@
 //     codes (affine-split-mma.ts affine_unit; affine3/4-mma.ts);
 //   * the factored form of the group dot product used by affine3-rows.ts /
 //     affine4-rows.ts: sum_g [ scale_g * sum_k q_k x_k + bias_g * sum_k x_k ],
-//     decoding each weight once and reusing it for every activation row;
+//     each weight decoded once and reused for every activation row;
 //   * the K-permuted operand layout of affine{3,4}-mma.ts (any permutation
 //     of k inside a group works, provided x is permuted the same way);
-//   * a deterministic split-K sum in a fixed order (affine-split-mma.ts
-//     adds its SPLITS partial tiles in index order, no atomics).
+//   * a deterministic split-K sum in a fixed order (affine-split-mma.ts adds
+//     its SPLITS partial tiles in index order, no atomics).
 //
 // GB300 design:
-//   * One CTA owns 16*RT weight rows and a contiguous range of 512-wide K
-//     stages.  A producer warp streams each stage's packed words, scales and
-//     biases into a ring of shared-memory buffers with bulk-async copies
-//     (cp.async.bulk, L2 evict-first), completion tracked by mbarriers; all
-//     of a CTA's stages are in flight at once when they fit in the ring.
-//   * Four consumer warps decode codes straight into fp16 MMA A-fragments:
-//     a code masked in place inside an fp16 with a zero exponent field is the
-//     exact subnormal q * 2^(p-24) (p = its bit position in the half), so the
-//     decode is one AND per two codes plus a shift or byte permute per word.
-//     x is pre-scaled by 2^-p for the matching k, making every product
-//     q * x * 2^-24 exactly; the per-group scale is applied to the fp32
-//     accumulator as scale * 2^24.  bf16 x is converted to fp16 once per CTA
-//     with a per-row power-of-two scale that keeps it in fp16 range.
-//   * mma.sync m16n8k16 (fp16 in, fp32 accumulate) does the multiply-adds:
-//     16 weight rows x 8 activation rows x 16 k per instruction.  Each
-//     thread holds 16 consecutive codes of a group for two rows, so one
-//     MMA k-step never mixes groups and the factored form applies per group.
-//   * Split-K across the CTAs of a thread-block cluster: partial tiles meet in
-//     distributed shared memory and are added in rank order.
-//   * Every mbarrier wait is bounded; a wait that gives up sets the kernel's
-//     error word and the CTA winds down without further waits.
+//   * A CTA is four warps; each warp owns 16 weight rows and streams them,
+//     512 K-values (8 groups) per stage, through its own ring of shared-memory
+//     stages with 16-byte cp.async copies (coalesced rows).
+//     There is no cross-warp hand-off in the main loop: a warp waits only on
+//     its own copies.
+//   * The four warps share the CTA's K range, so x is prepared once per CTA:
+//     permuted into MMA B-fragment order (fp16, pre-scaled per k as below)
+//     with per-group sums of x, in shared memory.
+//   * Codes decode straight into fp16 MMA A-fragments: a code masked in place
+//     inside an fp16 whose exponent field is zero is the exact subnormal
+//     q * 2^(p-24) (p = its bit position in the half), so decoding is one AND
+//     per two codes plus a shift or byte permute per word.  x is pre-scaled
+//     by 2^-p for the matching k, making every product q * x * 2^-24 exact;
+//     the group's scale is applied to the fp32 result as scale * 2^24.  bf16
+//     x is converted to fp16 once per CTA with a per-row power-of-two scale
+//     that keeps it inside the fp16 range.
+//   * mma.sync m16n8k16 (fp16 in, fp32 accumulate) does the multiply-adds.
+//     Each thread holds 16 consecutive codes of a group for two rows, so an
+//     MMA k-step never mixes groups; the 8 groups of a stage are independent
+//     MMA chains.
+//   * Narrow outputs split K over the CTAs of a thread-block cluster; their
+//     partial tiles meet in distributed shared memory and are added in rank
+//     order (deterministic).
 #include "aq_internal.h"
 #include "aq_ptx.cuh"
 
@@ -47,18 +49,23 @@ __device__ uint32_t g_qmv_error;
 
 namespace {
 
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kGroupsPerStage = 8;  // 512 values of K per stage
-constexpr int kGroupsPerWarp = kGroupsPerStage / kConsumerWarps;
-constexpr int kMaxStages = 8;
+constexpr int kWarps = 4;               // warps per CTA, 16 weight rows each
+constexpr int kThreads = kWarps * 32;
+constexpr int kRows = 16 * kWarps;      // weight rows per CTA
+constexpr int kGroupsPerStage = 8;      // 512 values of K per stage
+constexpr int kRing = 3;                // stages per warp ring
+constexpr int kMaxCluster = 16;
 
 template <int B>
 struct Fmt {
-    static constexpr int kGroupBytes = 8 * B;                        // 2*B words
+    static constexpr int kGroupBytes = 8 * B;                             // 2*B words
     static constexpr int kRowStageBytes = kGroupsPerStage * kGroupBytes;  // 256 / 192
-    // Row pitch in the stage buffer, padded against bank conflicts.
+    static constexpr int kChunksPerRow = kRowStageBytes / 16;             // 16 / 12
+    // Row pitch in a stage, padded so that the eight rows an MMA reads at
+    // once start in different bank groups.
     static constexpr int kRowPitch = kRowStageBytes + (B == 4 ? 32 : 16);
+    static constexpr int kScalesOff = 16 * kRowPitch;  // then scales[16][8], biases[16][8]
+    static constexpr int kStageBytes = kScalesOff + 2 * 16 * 16;
 };
 
 struct Params {
@@ -72,9 +79,8 @@ struct Params {
     int stages_total;  // K / 512
     int ks;            // CTAs per cluster splitting K
     int mc;            // activation rows per launch block (8*MB)
-    int nstage;        // ring depth
-    uint32_t stage_bytes, off_scales, off_biases;  // within one stage buffer
-    uint32_t off_bars, off_xfrag, off_xs, off_partial, off_escale, off_flag;
+    int slots;         // ring slots allocated per warp (<= kRing)
+    uint32_t off_xfrag, off_xs, off_scale, off_partial;
 };
 
 // Pair i of the 8 fp16 pairs decoded from a thread's 16 codes holds codes
@@ -83,17 +89,17 @@ template <int B>
 struct PairMap;
 template <>
 struct PairMap<4> {
-    static __device__ __forceinline__ int lo(int i) { return i < 4 ? i : i + 4; }
-    static __device__ __forceinline__ int hi(int i) { return lo(i) + 4; }
-    static __device__ __forceinline__ int p(int i) { return (i & 1) ? 4 : 0; }
+    static constexpr __device__ int lo(int i) { return i < 4 ? i : i + 4; }
+    static constexpr __device__ int hi(int i) { return lo(i) + 4; }
+    static constexpr __device__ int p(int i) { return (i & 1) ? 4 : 0; }
 };
 template <>
 struct PairMap<3> {
-    static __device__ __forceinline__ int lo(int i) { return i; }
-    static __device__ __forceinline__ int hi(int i) { return i + 8; }
-    static __device__ __forceinline__ int p(int i) {
-        // positions 0,3,6,0,3,0,3,6
-        return i == 2 || i == 7 ? 6 : (i == 1 || i == 4 || i == 6) ? 3 : 0;
+    static constexpr __device__ int lo(int i) { return i; }
+    static constexpr __device__ int hi(int i) { return i + 8; }
+    // positions 0,3,6,0,3,0,3,6
+    static constexpr __device__ int p(int i) {
+        return (i == 2 || i == 7) ? 6 : (i == 1 || i == 4 || i == 6) ? 3 : 0;
     }
 };
 
@@ -132,29 +138,6 @@ __device__ __forceinline__ void decode3(uint32_t wa, uint32_t wb, uint32_t sel0,
     P[7] = r3 & 0x01C001C0u;  // codes 7,15  p=6
 }
 
-__device__ __forceinline__ void record_error(volatile int *flag, uint32_t code) {
-    *flag = 1;
-    atomicOr(&g_qmv_error, code);
-}
-
-// Bounded wait that also gives up at once when another warp of the CTA has
-// already given up (so a failing CTA pays the time limit only once).
-__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *flag,
-                                              uint32_t code) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*flag) return false;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1; it < (1u << 31); ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0u) {
-            if (*flag) return false;
-            if (globaltimer_ns() - t0 > AQ_WAIT_LIMIT_NS) break;
-        }
-    }
-    record_error(flag, code);
-    return false;
-}
-
 template <typename T>
 __device__ __forceinline__ void load16(const T *src, float (&f)[16]) {
     const uint4 u0 = __ldg(reinterpret_cast<const uint4 *>(src));
@@ -162,9 +145,8 @@ __device__ __forceinline__ void load16(const T *src, float (&f)[16]) {
     const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        if constexpr (sizeof(T) == 2 && std::is_same<T, __half>::value) {
-            const __half2 h = *reinterpret_cast<const __half2 *>(&w[i]);
-            const float2 v = __half22float2(h);
+        if constexpr (std::is_same<T, __half>::value) {
+            const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
             f[2 * i] = v.x;
             f[2 * i + 1] = v.y;
         } else {
@@ -183,21 +165,33 @@ __device__ __forceinline__ void store_out<__nv_bfloat16>(__nv_bfloat16 *p, float
     *p = __float2bfloat16_rn(v);
 }
 
+__device__ __forceinline__ float half_lo(uint32_t v) {
+    return __half2float(__ushort_as_half((unsigned short)(v & 0xFFFFu)));
+}
+__device__ __forceinline__ float half_hi(uint32_t v) {
+    return __half2float(__ushort_as_half((unsigned short)(v >> 16)));
+}
+// element j (0..7) of 8 halves held in a uint4
+__device__ __forceinline__ float half_at(const uint4 &v, int j) {
+    const uint32_t w = j < 2 ? v.x : j < 4 ? v.y : j < 6 ? v.z : v.w;
+    return (j & 1) ? half_hi(w) : half_lo(w);
+}
+
 }  // namespace
 
-template <int B, typename T, int MB, int RT>
+template <int B, typename T, int MB>
 __global__ void __launch_bounds__(kThreads) qmv_kernel(const __grid_constant__ Params prm) {
     extern __shared__ __align__(128) uint8_t smem[];
-    constexpr int R = 16 * RT;   // weight rows per CTA
     constexpr int MCP = 8 * MB;  // padded activation rows per launch block
     using F = Fmt<B>;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int ct = threadIdx.x;
     const int ks = prm.ks;
     const int tile = blockIdx.x / ks;
     const int rank = blockIdx.x % ks;
-    const int64_t n0 = (int64_t)tile * R;
+    const int64_t n0 = (int64_t)tile * kRows;
     const int64_t m0 = (int64_t)blockIdx.y * prm.mc;
     const int Mc = (int)min((int64_t)prm.mc, prm.M - m0);  // valid activation rows here
     const int st_begin = (int)((int64_t)prm.stages_total * rank / ks);
@@ -206,250 +200,216 @@ __global__ void __launch_bounds__(kThreads) qmv_kernel(const __grid_constant__ P
     const int gb = st_begin * kGroupsPerStage;  // first group of this CTA
     const int gcta = nst * kGroupsPerStage;     // groups of this CTA
 
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + prm.off_bars);
-    uint64_t *empty = full + kMaxStages;
+    uint8_t *ring = smem + (size_t)warp * prm.slots * F::kStageBytes;
     uint8_t *xfrag = smem + prm.off_xfrag;
     float *xs = reinterpret_cast<float *>(smem + prm.off_xs);
+    float *escale = reinterpret_cast<float *>(smem + prm.off_scale);  // [MCP] x multiplier
+    float *oscale = escale + MCP;                                     // [MCP] y multiplier
+    unsigned *amax = reinterpret_cast<unsigned *>(oscale + MCP);      // [MCP]
     float *partial = reinterpret_cast<float *>(smem + prm.off_partial);
-    float *escale = reinterpret_cast<float *>(smem + prm.off_escale);  // [MCP] x multiplier
-    float *oscale = escale + MCP;                                      // [MCP] y multiplier
-    volatile int *flag = reinterpret_cast<volatile int *>(smem + prm.off_flag);
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < prm.nstage; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
+    // ----------------------------------------------------------------------
+    // Stage issue: 16 rows x 8 groups of packed words, plus the rows' 8
+    // scales and 8 biases, as 16-byte cp.async copies.
+    // ----------------------------------------------------------------------
+    const int64_t row_bytes = prm.K * B / 8;
+    const int64_t wrow0 = n0 + 16 * warp;  // first weight row of this warp
+    const uint8_t *wq8 = reinterpret_cast<const uint8_t *>(prm.Wq);
+    auto issue = [&](int s, int slot) {
+        uint8_t *dst = ring + slot * F::kStageBytes;
+        const int gs = gb + s * kGroupsPerStage;
+#pragma unroll
+        for (int i = 0; i < F::kChunksPerRow / 2; ++i) {
+            const int c = lane + 32 * i;
+            const int r = c / F::kChunksPerRow, col = c % F::kChunksPerRow;
+            const int64_t n = wrow0 + r;
+            const bool ok = n < prm.N;
+            const uint8_t *src = ok ? wq8 + n * row_bytes + (int64_t)gs * F::kGroupBytes + col * 16
+                                    : wq8;
+            cp_async16(dst + r * F::kRowPitch + col * 16, src, ok ? 16u : 0u);
         }
-        *flag = 0;
-        fence_mbar_init();
+        {
+            const int r = lane & 15;
+            const int64_t n = wrow0 + r;
+            const bool ok = n < prm.N;
+            const __half *base = (lane < 16) ? prm.scales : prm.biases;
+            const void *src = ok ? (const void *)(base + n * prm.G + gs) : (const void *)base;
+            cp_async16(dst + F::kScalesOff + (lane >> 4) * 256 + r * 16, src, ok ? 16u : 0u);
+        }
+    };
+    const int slots = prm.slots;
+#pragma unroll
+    for (int s = 0; s < kRing - 1; ++s) {
+        if (s < nst) issue(s, s);
+        cp_async_commit();
+    }
+
+    // ----------------------------------------------------------------------
+    // Prologue (all threads): x for this CTA's K range, permuted into
+    // B-fragment order, and per-group sums of x.
+    // ----------------------------------------------------------------------
+    const T *xg = static_cast<const T *>(prm.x);
+    if (ct < MCP) {
+        escale[ct] = 1.f;
+        oscale[ct] = 1.f;
+        amax[ct] = 0u;
     }
     __syncthreads();
-
-    if (warp == kConsumerWarps) {
-        // ------------------------------------------------------------------
-        // Producer: one lane per weight row issues that row's three copies.
-        // ------------------------------------------------------------------
-        const uint64_t pol = policy_evict_first();
-        const int64_t wpr = prm.K * B / 32;
-        const int valid_rows = (int)min((int64_t)R, prm.N - n0);
-        const uint32_t row_bytes = F::kRowStageBytes + 2 * 2 * kGroupsPerStage;
-        for (int si = 0; si < nst; ++si) {
-            const int slot = si % prm.nstage;
-            const uint32_t ph = (uint32_t)(si / prm.nstage) & 1u;
-            if (si >= prm.nstage && !wait_or_abort(&empty[slot], ph ^ 1u, flag, ERR_QMV_EMPTY))
-                break;
-            uint8_t *sb = smem + (size_t)slot * prm.stage_bytes;
-            if (lane == 0) mbar_arrive_expect_tx(&full[slot], row_bytes * valid_rows);
-            __syncwarp();
-            if (lane < valid_rows) {
-                const int64_t row = n0 + lane;
-                const int g0 = gb + si * kGroupsPerStage;
-                bulk_g2s(sb + lane * F::kRowPitch,
-                         prm.Wq + row * wpr + (int64_t)g0 * (2 * B), F::kRowStageBytes,
-                         &full[slot], pol);
-                bulk_g2s(sb + prm.off_scales + lane * 16, prm.scales + row * prm.G + g0, 16,
-                         &full[slot], pol);
-                bulk_g2s(sb + prm.off_biases + lane * 16, prm.biases + row * prm.G + g0, 16,
-                         &full[slot], pol);
-            }
-        }
-    } else {
-        // ------------------------------------------------------------------
-        // Consumers.  Prologue: x of this CTA's K range, permuted into
-        // B-fragment order, plus per-group sums of x.
-        // ------------------------------------------------------------------
-        const int ct = threadIdx.x;  // 0..127
-        const T *xg = static_cast<const T *>(prm.x);
-        if (ct < MCP) {
-            escale[ct] = 1.f;
-            oscale[ct] = 1.f;
-        }
-        if constexpr (std::is_same<T, __nv_bfloat16>::value) {
-            // Largest |x| per activation row over this CTA's K range, as
-            // ordered float bits; pick 2^-e so that the fp16 copy stays below
-            // 2^15 in magnitude.
-            unsigned *amax = reinterpret_cast<unsigned *>(partial);  // scratch before use
-            if (ct < MCP) amax[ct] = 0u;
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            for (int u = ct; u < gcta * Mc * 4; u += 128) {
-                const int j = u / (Mc * 4), m = (u >> 2) % Mc, t = u & 3;
+    if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+        // Largest |x| per activation row over this CTA's K range; pick 2^-e
+        // so that the fp16 copy stays below 2^15 in magnitude.
+        const int kc = gcta * 64;
+        for (int m = 0; m < Mc; ++m) {
+            float a = 0.f;
+            for (int k = 16 * ct; k < kc; k += 16 * kThreads) {
                 float f[16];
-                load16<T>(xg + (m0 + m) * prm.K + 64 * (gb + j) + 16 * t, f);
-                float a = 0.f;
+                load16<T>(xg + (m0 + m) * prm.K + 64 * gb + k, f);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(f[i]));
-                atomicMax(&amax[m], __float_as_uint(a));
             }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            if (ct < Mc) {
-                const int e = (int)((amax[ct] >> 23) & 0xFF) - 127;  // floor(log2 amax)
-                const int sh = e > 14 ? e - 14 : 0;
-                escale[ct] = exp2f((float)-sh);
-                oscale[ct] = exp2f((float)sh);
-            }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+#pragma unroll
+            for (int d = 16; d >= 1; d >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, d));
+            if (lane == 0) atomicMax(&amax[m], __float_as_uint(a));
+        }
+        __syncthreads();
+        if (ct < Mc) {
+            const int e = (int)((amax[ct] >> 23) & 0xFF) - 127;  // floor(log2 amax)
+            const int sh = e > 14 ? e - 14 : 0;
+            escale[ct] = __int_as_float((127 - sh) << 23);
+            oscale[ct] = __int_as_float((127 + sh) << 23);
+        }
+        __syncthreads();
+    }
+    for (int ub = 0; ub < gcta * Mc * 4; ub += kThreads) {
+        const int u = ub + ct;
+        const bool valid = u < gcta * Mc * 4;
+        const int j = valid ? u / (Mc * 4) : 0, m = valid ? (u >> 2) % Mc : 0, t = u & 3;
+        float f[16];
+        if (valid) {
+            load16<T>(xg + (m0 + m) * prm.K + 64 * (gb + j) + 16 * t, f);
         } else {
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+#pragma unroll
+            for (int i = 0; i < 16; ++i) f[i] = 0.f;
         }
-        for (int ub = 0; ub < gcta * Mc * 4; ub += 128) {
-            const int u = ub + ct;
-            const bool valid = u < gcta * Mc * 4;
-            const int j = valid ? u / (Mc * 4) : 0, m = valid ? (u >> 2) % Mc : 0, t = u & 3;
-            float f[16];
-            if (valid) {
-                load16<T>(xg + (m0 + m) * prm.K + 64 * (gb + j) + 16 * t, f);
+        const float es = valid ? escale[m] : 0.f;
+        float sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            f[i] *= es;
+            sum += f[i];
+        }
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        if (valid) {
+            uint32_t pr[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float sc = __int_as_float((127 - PairMap<B>::p(i)) << 23);  // 2^-p
+                pr[i] = pack_half2(f[PairMap<B>::lo(i)] * sc, f[PairMap<B>::hi(i)] * sc);
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(xfrag);
+            dst[((j * 2 + 0) * Mc + m) * 4 + t] = make_uint4(pr[0], pr[1], pr[2], pr[3]);
+            dst[((j * 2 + 1) * Mc + m) * 4 + t] = make_uint4(pr[4], pr[5], pr[6], pr[7]);
+            if (t == 0) xs[j * MCP + m] = sum;
+        }
+    }
+    for (int u = ct; u < gcta * MCP; u += kThreads)
+        if (u % MCP >= Mc) xs[u] = 0.f;
+    __syncthreads();
+
+    // ----------------------------------------------------------------------
+    // Main loop: each warp over its 16 rows and all stages of the CTA.
+    // ----------------------------------------------------------------------
+    const int g = lane >> 2, t = lane & 3;
+    uint32_t sel0 = 0, sel2 = 0;
+    int wi3 = 0;
+    if constexpr (B == 3) {
+        const uint32_t bo = 2u * (uint32_t)(t & 1);
+        sel0 = (bo + 0) | ((bo + 1) << 4) | ((bo + 3) << 8) | ((bo + 4) << 12);
+        sel2 = (bo + 1) | ((bo + 2) << 4) | ((bo + 4) << 8) | ((bo + 5) << 12);
+        wi3 = (3 * t) >> 1;
+    }
+    float acc[MB][4];
+#pragma unroll
+    for (int mb = 0; mb < MB; ++mb)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[mb][i] = 0.f;
+
+    const uint4 *xf4 = reinterpret_cast<const uint4 *>(xfrag);
+    for (int si = 0; si < nst; ++si) {
+        cp_async_wait<kRing - 2>();
+        __syncwarp();
+        const int slot = si % slots;
+        const uint8_t *sb = ring + slot * F::kStageBytes;
+        const uint4 sA = *reinterpret_cast<const uint4 *>(sb + F::kScalesOff + g * 16);
+        const uint4 sB = *reinterpret_cast<const uint4 *>(sb + F::kScalesOff + (g + 8) * 16);
+        const uint4 bA = *reinterpret_cast<const uint4 *>(sb + F::kScalesOff + 256 + g * 16);
+        const uint4 bB = *reinterpret_cast<const uint4 *>(sb + F::kScalesOff + 256 + (g + 8) * 16);
+#pragma unroll
+        for (int j = 0; j < kGroupsPerStage; ++j) {
+            const int grp = si * kGroupsPerStage + j;  // group within the CTA range
+            uint32_t PA[8], PB[8];
+            if constexpr (B == 4) {
+                const uint2 qa = *reinterpret_cast<const uint2 *>(sb + g * F::kRowPitch +
+                                                                  j * F::kGroupBytes + 8 * t);
+                const uint2 qb = *reinterpret_cast<const uint2 *>(sb + (g + 8) * F::kRowPitch +
+                                                                  j * F::kGroupBytes + 8 * t);
+                decode4(qa.x, qa.y, PA);
+                decode4(qb.x, qb.y, PB);
             } else {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) f[i] = 0.f;
+                const uint32_t *pa =
+                    reinterpret_cast<const uint32_t *>(sb + g * F::kRowPitch + j * F::kGroupBytes);
+                const uint32_t *pb = reinterpret_cast<const uint32_t *>(
+                    sb + (g + 8) * F::kRowPitch + j * F::kGroupBytes);
+                decode3(pa[wi3], pa[wi3 + 1], sel0, sel2, PA);
+                decode3(pb[wi3], pb[wi3 + 1], sel0, sel2, PB);
             }
-            const float es = valid ? escale[m] : 0.f;
-            float sum = 0.f;
+            const float sa = half_at(sA, j) * 16777216.f, sbb = half_at(sB, j) * 16777216.f;
+            const float ba = half_at(bA, j), bb = half_at(bB, j);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                f[i] *= es;
-                sum += f[i];
-            }
-            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-            if (valid) {
-                uint32_t pr[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float sc = __int_as_float((127 - PairMap<B>::p(i)) << 23);  // 2^-p
-                    pr[i] = pack_half2(f[PairMap<B>::lo(i)] * sc, f[PairMap<B>::hi(i)] * sc);
+            for (int mb = 0; mb < MB; ++mb) {
+                const int m = mb * 8 + g;
+                uint4 q0 = make_uint4(0, 0, 0, 0), q1 = make_uint4(0, 0, 0, 0);
+                if (m < Mc) {
+                    q0 = xf4[((grp * 2 + 0) * Mc + m) * 4 + t];
+                    q1 = xf4[((grp * 2 + 1) * Mc + m) * 4 + t];
                 }
-                uint4 *dst = reinterpret_cast<uint4 *>(xfrag);
-                dst[((j * 2 + 0) * Mc + m) * 4 + t] = make_uint4(pr[0], pr[1], pr[2], pr[3]);
-                dst[((j * 2 + 1) * Mc + m) * 4 + t] = make_uint4(pr[4], pr[5], pr[6], pr[7]);
-                if (t == 0) xs[j * MCP + m] = sum;
-            }
-        }
-        // zero the padding rows of xs
-        for (int u = ct; u < gcta * MCP; u += 128)
-            if (u % MCP >= Mc) xs[u] = 0.f;
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-
-        // ------------------------------------------------------------------
-        // Main loop.
-        // ------------------------------------------------------------------
-        const int g = lane >> 2, t = lane & 3;
-        uint32_t sel0 = 0, sel2 = 0;
-        int wi3 = 0;
-        if constexpr (B == 3) {
-            const uint32_t bo = 2u * (uint32_t)(t & 1);
-            sel0 = (bo + 0) | ((bo + 1) << 4) | ((bo + 3) << 8) | ((bo + 4) << 12);
-            sel2 = (bo + 1) | ((bo + 2) << 4) | ((bo + 4) << 8) | ((bo + 5) << 12);
-            wi3 = (3 * t) >> 1;
-        }
-        float acc[RT][MB][4];
-#pragma unroll
-        for (int rt = 0; rt < RT; ++rt)
-#pragma unroll
-            for (int mb = 0; mb < MB; ++mb)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) acc[rt][mb][i] = 0.f;
-
-        const uint4 *xf4 = reinterpret_cast<const uint4 *>(xfrag);
-        for (int si = 0; si < nst; ++si) {
-            const int slot = si % prm.nstage;
-            const uint32_t ph = (uint32_t)(si / prm.nstage) & 1u;
-            const bool ok = wait_or_abort(&full[slot], ph, flag, ERR_QMV_FULL);
-            const uint8_t *sb = smem + (size_t)slot * prm.stage_bytes;
-            const __half *ss = reinterpret_cast<const __half *>(sb + prm.off_scales);
-            const __half *sbias = reinterpret_cast<const __half *>(sb + prm.off_biases);
-            if (ok) {
-#pragma unroll
-                for (int jj = 0; jj < kGroupsPerWarp; ++jj) {
-                    const int jl = warp * kGroupsPerWarp + jj;  // group within the stage
-                    const int grp = si * kGroupsPerStage + jl;  // group within the CTA range
-                    uint4 bf[MB][2];
-                    float xs0[MB], xs1[MB];
-#pragma unroll
-                    for (int mb = 0; mb < MB; ++mb) {
-                        const int m = mb * 8 + g;
-                        if (m < Mc) {
-                            bf[mb][0] = xf4[((grp * 2 + 0) * Mc + m) * 4 + t];
-                            bf[mb][1] = xf4[((grp * 2 + 1) * Mc + m) * 4 + t];
-                        } else {
-                            bf[mb][0] = make_uint4(0, 0, 0, 0);
-                            bf[mb][1] = make_uint4(0, 0, 0, 0);
-                        }
-                        const float2 v =
-                            *reinterpret_cast<const float2 *>(&xs[grp * MCP + mb * 8 + 2 * t]);
-                        xs0[mb] = v.x;
-                        xs1[mb] = v.y;
-                    }
-#pragma unroll
-                    for (int rt = 0; rt < RT; ++rt) {
-                        const int ra = rt * 16 + g, rb = ra + 8;
-                        uint32_t PA[8], PB[8];
-                        if constexpr (B == 4) {
-                            const uint2 qa = *reinterpret_cast<const uint2 *>(
-                                sb + ra * F::kRowPitch + jl * F::kGroupBytes + 8 * t);
-                            const uint2 qb = *reinterpret_cast<const uint2 *>(
-                                sb + rb * F::kRowPitch + jl * F::kGroupBytes + 8 * t);
-                            decode4(qa.x, qa.y, PA);
-                            decode4(qb.x, qb.y, PB);
-                        } else {
-                            const uint32_t *pa = reinterpret_cast<const uint32_t *>(
-                                sb + ra * F::kRowPitch + jl * F::kGroupBytes);
-                            const uint32_t *pb = reinterpret_cast<const uint32_t *>(
-                                sb + rb * F::kRowPitch + jl * F::kGroupBytes);
-                            decode3(pa[wi3], pa[wi3 + 1], sel0, sel2, PA);
-                            decode3(pb[wi3], pb[wi3 + 1], sel0, sel2, PB);
-                        }
-                        const float sa = __half2float(ss[ra * kGroupsPerStage + jl]) * 16777216.f;
-                        const float sbb = __half2float(ss[rb * kGroupsPerStage + jl]) * 16777216.f;
-                        const float ba = __half2float(sbias[ra * kGroupsPerStage + jl]);
-                        const float bb = __half2float(sbias[rb * kGroupsPerStage + jl]);
-#pragma unroll
-                        for (int mb = 0; mb < MB; ++mb) {
-                            float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                            for (int s = 0; s < 4; ++s) {
-                                const uint32_t a[4] = {PA[2 * s], PB[2 * s], PA[2 * s + 1],
-                                                       PB[2 * s + 1]};
-                                const uint4 &q = bf[mb][s >> 1];
-                                const uint32_t b0 = (s & 1) ? q.z : q.x;
-                                const uint32_t b1 = (s & 1) ? q.w : q.y;
-                                mma_f16_16816(d, a, b0, b1, d);
-                            }
-                            acc[rt][mb][0] = fmaf(sa, d[0], fmaf(ba, xs0[mb], acc[rt][mb][0]));
-                            acc[rt][mb][1] = fmaf(sa, d[1], fmaf(ba, xs1[mb], acc[rt][mb][1]));
-                            acc[rt][mb][2] = fmaf(sbb, d[2], fmaf(bb, xs0[mb], acc[rt][mb][2]));
-                            acc[rt][mb][3] = fmaf(sbb, d[3], fmaf(bb, xs1[mb], acc[rt][mb][3]));
-                        }
-                    }
+                const float2 xv = *reinterpret_cast<const float2 *>(&xs[grp * MCP + mb * 8 + 2 * t]);
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                {
+                    const uint32_t a0[4] = {PA[0], PB[0], PA[1], PB[1]};
+                    mma_f16_16816(d, a0, q0.x, q0.y, d);
+                    const uint32_t a1[4] = {PA[2], PB[2], PA[3], PB[3]};
+                    mma_f16_16816(d, a1, q0.z, q0.w, d);
+                    const uint32_t a2[4] = {PA[4], PB[4], PA[5], PB[5]};
+                    mma_f16_16816(d, a2, q1.x, q1.y, d);
+                    const uint32_t a3[4] = {PA[6], PB[6], PA[7], PB[7]};
+                    mma_f16_16816(d, a3, q1.z, q1.w, d);
                 }
+                acc[mb][0] = fmaf(sa, d[0], fmaf(ba, xv.x, acc[mb][0]));
+                acc[mb][1] = fmaf(sa, d[1], fmaf(ba, xv.y, acc[mb][1]));
+                acc[mb][2] = fmaf(sbb, d[2], fmaf(bb, xv.x, acc[mb][2]));
+                acc[mb][3] = fmaf(sbb, d[3], fmaf(bb, xv.y, acc[mb][3]));
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
         }
+        __syncwarp();
+        if (si + kRing - 1 < nst) issue(si + kRing - 1, (si + kRing - 1) % slots);
+        cp_async_commit();
+    }
+    cp_async_wait<0>();
 
-        // ------------------------------------------------------------------
-        // Add the four warps' partial tiles in warp order.  The stage ring is
-        // idle now (every copy has landed and been read), so it holds them.
-        // ------------------------------------------------------------------
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        float *red = reinterpret_cast<float *>(smem);
-        constexpr int E = RT * MB * 32 * 4;  // elements per warp
+    // ----------------------------------------------------------------------
+    // Epilogue.
+    // ----------------------------------------------------------------------
+    T *y = static_cast<T *>(prm.y);
+    const int rowA = 16 * warp + g, rowB = rowA + 8;  // within the CTA
 #pragma unroll
-        for (int rt = 0; rt < RT; ++rt)
+    for (int mb = 0; mb < MB; ++mb) {
 #pragma unroll
-            for (int mb = 0; mb < MB; ++mb)
-                *reinterpret_cast<float4 *>(&red[warp * E + ((rt * MB + mb) * 32 + lane) * 4]) =
-                    make_float4(acc[rt][mb][0], acc[rt][mb][1], acc[rt][mb][2], acc[rt][mb][3]);
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        T *y = static_cast<T *>(prm.y);
-        for (int e = ct; e < E; e += 128) {
-            float v = 0.f;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) v += red[w * E + e];
-            const int i = e & 3, ln = (e >> 2) & 31, rm = e >> 7;
-            const int rt = rm / MB, mb = rm % MB;
-            const int row = rt * 16 + (ln >> 2) + 8 * (i >> 1);
-            const int col = mb * 8 + 2 * (ln & 3) + (i & 1);
-            v *= oscale[col];
+        for (int i = 0; i < 4; ++i) {
+            const int row = (i < 2) ? rowA : rowB;
+            const int col = mb * 8 + 2 * t + (i & 1);
+            const float v = acc[mb][i] * oscale[col];
             if (ks == 1) {
                 if (col < Mc && n0 + row < prm.N) store_out<T>(&y[(m0 + col) * prm.N + n0 + row], v);
             } else {
@@ -457,31 +417,20 @@ __global__ void __launch_bounds__(kThreads) qmv_kernel(const __grid_constant__ P
             }
         }
     }
-
     if (ks > 1) {
         // Split-K: CTA `rank` adds element e (e % ks == rank) over all ranks
         // of the cluster, rank 0 first.
         cluster_sync();
-        if (warp < kConsumerWarps) {
-            T *y = static_cast<T *>(prm.y);
-            const uint32_t base = smem_u32(partial);
-            for (int e = rank + ks * (int)threadIdx.x; e < R * MCP; e += ks * 128) {
-                const int row = e / MCP, col = e % MCP;
-                if (col >= Mc || n0 + row >= prm.N) continue;
-                float v = 0.f;
-                for (int r = 0; r < ks; ++r)
-                    v += ld_dsmem_f32(map_to_rank(base + 4u * (uint32_t)e, (uint32_t)r));
-                store_out<T>(&y[(m0 + col) * prm.N + n0 + row], v);
-            }
+        const uint32_t base = smem_u32(partial);
+        for (int e = rank + ks * ct; e < kRows * MCP; e += ks * kThreads) {
+            const int row = e / MCP, col = e % MCP;
+            if (col >= Mc || n0 + row >= prm.N) continue;
+            float v = 0.f;
+            for (int r = 0; r < ks; ++r)
+                v += ld_dsmem_f32(map_to_rank(base + 4u * (uint32_t)e, (uint32_t)r));
+            store_out<T>(&y[(m0 + col) * prm.N + n0 + row], v);
         }
         cluster_sync();
-    }
-    if (*flag) {
-        // A wait gave up.  Copies issued before that may still be landing in
-        // this CTA's shared memory: let them finish before the CTA exits.
-        const uint64_t t0 = globaltimer_ns();
-        while (globaltimer_ns() - t0 < 200000ull) {
-        }
     }
 }
 
@@ -491,7 +440,7 @@ __global__ void __launch_bounds__(kThreads) qmv_kernel(const __grid_constant__ P
 namespace {
 
 struct Plan {
-    int MB, RT, ks, mc, nstage, m_chunks, tiles;
+    int MB, ks, mc, m_chunks, tiles;
     size_t smem;
     Params prm;
 };
@@ -503,45 +452,35 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 bool make_plan(const MatmulArgs &a, Plan &p) {
     const int B = a.bits;
     if (a.K % 512 != 0 || a.M < 1 || a.N < 1) return false;
-    p.MB = a.M >= 25 ? 4 : a.M >= 17 ? 3 : a.M >= 9 ? 2 : 1;
-    if (p.MB == 3) p.MB = 4;
-    p.RT = 1;
+    p.MB = a.M > 16 ? 4 : a.M > 8 ? 2 : 1;
     p.mc = 8 * p.MB;
     p.m_chunks = (int)((a.M + p.mc - 1) / p.mc);
     if (p.m_chunks > 65535) return false;
-    const int R = 16 * p.RT;
-    const int64_t tiles = (a.N + R - 1) / R;
-    if (tiles * 8 > (int64_t)INT32_MAX) return false;
+    const int64_t tiles = (a.N + kRows - 1) / kRows;
+    if (tiles * kMaxCluster > (int64_t)INT32_MAX) return false;
     p.tiles = (int)tiles;
     const int stages_total = (int)(a.K / 512);
     const int mc_valid = (int)std::min<int64_t>(a.M, p.mc);
-    // Split K across a cluster until there are about two CTAs per SM, and
-    // until x for a CTA's K range fits comfortably in shared memory.
     const int sms = num_sms();
-    int ks = 1;
     auto xbytes = [&](int k) {
-        const int g = ((stages_total + k - 1) / k) * kGroupsPerStage;
-        return (size_t)g * mc_valid * 128 + (size_t)g * p.mc * 4;
+        const size_t g = (size_t)((stages_total + k - 1) / k) * kGroupsPerStage;
+        return g * mc_valid * 128 + g * p.mc * 4;
     };
-    while (ks < 8 && ks * 2 <= stages_total &&
-           ((int64_t)tiles * p.m_chunks * ks < 2 * sms || xbytes(ks) > 96 * 1024))
-        ks *= 2;
-    if (xbytes(ks) > 120 * 1024) return false;
+    // Split K over a cluster until there are about two CTAs per SM and x for
+    // a CTA's K range fits comfortably in shared memory.
+    int ks = 1;
+    const int ks_max = std::min(kMaxCluster, stages_total);
+    while (ks < ks_max &&
+           ((int64_t)tiles * p.m_chunks * ks < 2 * sms || xbytes(ks) > 64 * 1024))
+        ++ks;
+    if (xbytes(ks) > 100 * 1024) return false;
     p.ks = ks;
     const int st_cta = (stages_total + ks - 1) / ks;
-    p.nstage = std::min(kMaxStages, std::max(1, st_cta));
+    const int slots = std::min(kRing, st_cta);
+    const int stage_bytes = B == 4 ? Fmt<4>::kStageBytes : Fmt<3>::kStageBytes;
 
-    const int row_pitch = B == 4 ? Fmt<4>::kRowPitch : Fmt<3>::kRowPitch;
     Params &q = p.prm;
-    q.off_scales = (uint32_t)(R * row_pitch);
-    q.off_biases = q.off_scales + R * 16;
-    q.stage_bytes = (uint32_t)align_up(q.off_biases + R * 16, 128);
-    size_t off = (size_t)p.nstage * q.stage_bytes;
-    const size_t red_bytes = (size_t)kConsumerWarps * p.RT * p.MB * 32 * 4 * 4;
-    off = std::max(off, red_bytes);
-    off = align_up(off, 128);
-    q.off_bars = (uint32_t)off;
-    off += 2 * kMaxStages * 8;
+    size_t off = (size_t)kWarps * slots * stage_bytes;
     off = align_up(off, 128);
     q.off_xfrag = (uint32_t)off;
     const size_t gmax = (size_t)st_cta * kGroupsPerStage;
@@ -550,12 +489,11 @@ bool make_plan(const MatmulArgs &a, Plan &p) {
     q.off_xs = (uint32_t)off;
     off += gmax * p.mc * 4;
     off = align_up(off, 128);
+    q.off_scale = (uint32_t)off;
+    off += 3 * p.mc * 4;
+    off = align_up(off, 128);
     q.off_partial = (uint32_t)off;
-    off += (size_t)R * p.mc * 4;
-    q.off_escale = (uint32_t)off;
-    off += 2 * p.mc * 4;
-    q.off_flag = (uint32_t)off;
-    off += 16;
+    off += ks > 1 ? (size_t)kRows * p.mc * 4 : 0;
     p.smem = align_up(off, 128);
     if (p.smem > kSmemLimit) return false;
 
@@ -571,18 +509,20 @@ bool make_plan(const MatmulArgs &a, Plan &p) {
     q.stages_total = stages_total;
     q.ks = ks;
     q.mc = p.mc;
-    q.nstage = p.nstage;
+    q.slots = slots;
     return true;
 }
 
-template <int B, typename T, int MB, int RT>
+template <int B, typename T, int MB>
 cudaError_t launch_plan(const Plan &p, cudaStream_t stream) {
-    auto kern = qmv_kernel<B, T, MB, RT>;
+    auto kern = qmv_kernel<B, T, MB>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)kSmemLimit);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     });
     if (attr_err != cudaSuccess) return attr_err;
     cudaLaunchConfig_t cfg = {};
@@ -603,9 +543,9 @@ cudaError_t launch_plan(const Plan &p, cudaStream_t stream) {
 template <int B, typename T>
 cudaError_t launch_mb(const Plan &p, cudaStream_t s) {
     switch (p.MB) {
-        case 1: return launch_plan<B, T, 1, 1>(p, s);
-        case 2: return launch_plan<B, T, 2, 1>(p, s);
-        default: return launch_plan<B, T, 4, 1>(p, s);
+        case 1: return launch_plan<B, T, 1>(p, s);
+        case 2: return launch_plan<B, T, 2>(p, s);
+        default: return launch_plan<B, T, 4>(p, s);
     }
 }
 
