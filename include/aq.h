@@ -137,6 +137,15 @@ aq_status aq_matmul_host(int dtype, const void *x_host, const uint32_t *Wq_dev,
 int aq_select(int64_t M, int64_t N, int64_t K, int bits, int dtype);
 
 /*
+ * aq_describe — one line of text naming the kernel and launch geometry the
+ * dispatch rule picks for a shape (host logic only; needs no GPU).  Writes a
+ * NUL-terminated string of at most buflen bytes to the host buffer `buf` and
+ * returns the length it wanted (as snprintf), or -1 if buf is NULL or
+ * buflen < 1.
+ */
+int aq_describe(int64_t M, int64_t N, int64_t K, int bits, int dtype, char *buf, int buflen);
+
+/*
  * aq_stats — per-variant call counters since load (or the last reset).
  *   calls  host array of n uint64; element v receives the number of calls
  *          that launched variant v (n may be less than AQ_NUM_VARIANTS).

@@ -23,7 +23,7 @@ from . import build as _build
 __all__ = [
     "AqError", "AQ_F16", "AQ_BF16", "AQ_VARIANT_AUTO", "AQ_VARIANT_GENERIC", "AQ_VARIANT_QMV",
     "AQ_VARIANT_TC", "AQ_NUM_VARIANTS", "aq_pack", "aq_matmul", "aq_matmul_bf16",
-    "aq_matmul_variant", "aq_matmul_host", "aq_select", "aq_stats", "aq_device_error",
+    "aq_matmul_variant", "aq_matmul_host", "aq_select", "aq_describe", "aq_stats", "aq_device_error",
     "aq_free", "aq_status_string", "aq_variant_name", "aq_version", "lib_path", "load",
 ]
 
@@ -64,6 +64,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "aq_matmul_variant": ([i32, i32, p, p, p, p, i64, i64, i64, i32, p, p], i32),
         "aq_matmul_host": ([i32, p, p, p, p, i64, i64, i64, i32, p, p, p, p], i32),
         "aq_select": ([i64, i64, i64, i32, i32], i32),
+        "aq_describe": ([i64, i64, i64, i32, i32, p, i32], i32),
         "aq_stats": ([p, i32, i32], i32),
         "aq_device_error": ([u32p, i32], i32),
         "aq_free": ([], None),
@@ -176,6 +177,12 @@ def aq_matmul_host(x_host: torch.Tensor, Wq, scales, biases, bits, out_host: tor
 
 def aq_select(M: int, N: int, K: int, bits: int, dtype: int = AQ_F16) -> int:
     return load().aq_select(M, N, K, bits, dtype)
+
+
+def aq_describe(M: int, N: int, K: int, bits: int, dtype: int = AQ_F16) -> str:
+    buf = ctypes.create_string_buffer(256)
+    load().aq_describe(M, N, K, bits, dtype, ctypes.addressof(buf), 256)
+    return buf.value.decode()
 
 
 def aq_stats(reset: bool = False) -> List[int]:

@@ -7,6 +7,7 @@
 #include "aq_internal.h"
 
 #include <atomic>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 
@@ -183,6 +184,19 @@ int aq_select(int64_t M, int64_t N, int64_t K, int bits, int dtype) {
                              (const void *)fake, M, N, K, bits, (void *)fake, nullptr);
     if (check_args(a) != AQ_OK) return -1;
     return choose(a);
+}
+
+int aq_describe(int64_t M, int64_t N, int64_t K, int bits, int dtype, char *buf, int buflen) {
+    if (!buf || buflen < 1) return -1;
+    const uintptr_t fake = 0x100000;
+    MatmulArgs a = make_args(dtype, (const void *)fake, (const uint32_t *)fake, (const void *)fake,
+                             (const void *)fake, M, N, K, bits, (void *)fake, nullptr);
+    if (check_args(a) != AQ_OK) return snprintf(buf, buflen, "invalid arguments");
+    switch (choose(a)) {
+        case AQ_VARIANT_QMV: return qmv_describe(a, buf, buflen);
+        case AQ_VARIANT_TC: return tc_describe(a, buf, buflen);
+        default: return snprintf(buf, buflen, "generic");
+    }
 }
 
 aq_status aq_stats(uint64_t *calls, int n, int reset) {

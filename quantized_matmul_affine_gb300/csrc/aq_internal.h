@@ -35,9 +35,13 @@ cudaError_t generic_launch(const MatmulArgs &a);
 
 bool qmv_supported(const MatmulArgs &a);
 cudaError_t qmv_launch(const MatmulArgs &a);
+// Tuning hook: restrict the small-M kernel's geometry (0 = free choice).
+void qmv_force_geometry(int rows_tiles, int cluster_split, int ring_depth);
+int qmv_describe(const MatmulArgs &a, char *buf, int len);
 
 bool tc_supported(const MatmulArgs &a);
 cudaError_t tc_launch(const MatmulArgs &a);
+int tc_describe(const MatmulArgs &a, char *buf, int len);
 
 cudaError_t pack_launch(const uint8_t *codes, int64_t N, int64_t K, int bits, uint32_t *words,
                         cudaStream_t stream);

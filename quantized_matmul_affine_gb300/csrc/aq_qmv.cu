@@ -13,14 +13,16 @@
 //     its SPLITS partial tiles in index order, no atomics).
 //
 // GB300 design:
-//   * A CTA is four warps; each warp owns 16 weight rows and streams them,
-//     512 K-values (8 groups) per stage, through its own ring of shared-memory
-//     stages with 16-byte cp.async copies (coalesced rows).
-//     There is no cross-warp hand-off in the main loop: a warp waits only on
-//     its own copies.
-//   * The four warps share the CTA's K range, so x is prepared once per CTA:
+//   * A CTA is eight warps covering rt tiles of 16 weight rows, kw = 8/rt
+//     warps per tile splitting the CTA's K stages (512 K-values, 8 groups,
+//     each).  Every warp streams its tile's rows through its own two-stage
+//     ring in shared memory with 16-byte cp.async copies (coalesced rows),
+//     queuing the next stage before it waits on the current one.  There is
+//     no cross-warp hand-off in the main loop.
+//   * All warps share the CTA's K range, so x is prepared once per CTA:
 //     permuted into MMA B-fragment order (fp16, pre-scaled per k as below)
-//     with per-group sums of x, in shared memory.
+//     with per-group sums of x, in shared memory.  The kw partial tiles of a
+//     tile are added in warp order at the end.
 //   * Codes decode straight into fp16 MMA A-fragments: a code masked in place
 //     inside an fp16 whose exponent field is zero is the exact subnormal
 //     q * 2^(p-24) (p = its bit position in the half), so decoding is one AND
@@ -40,6 +42,8 @@
 #include "aq_ptx.cuh"
 
 #include <algorithm>
+#include <atomic>
+#include <cstdio>
 #include <mutex>
 #include <type_traits>
 
@@ -49,11 +53,10 @@ __device__ uint32_t g_qmv_error;
 
 namespace {
 
-constexpr int kWarps = 4;               // warps per CTA, 16 weight rows each
+constexpr int kWarps = 8;               // warps per CTA
 constexpr int kThreads = kWarps * 32;
-constexpr int kRows = 16 * kWarps;      // weight rows per CTA
 constexpr int kGroupsPerStage = 8;      // 512 values of K per stage
-constexpr int kRing = 3;                // stages per warp ring
+constexpr int kMaxSlots = 6;            // deepest per-warp ring
 constexpr int kMaxCluster = 16;
 
 template <int B>
@@ -78,9 +81,12 @@ struct Params {
     int G;             // groups per row
     int stages_total;  // K / 512
     int ks;            // CTAs per cluster splitting K
+    int rt;            // 16-row tiles per CTA
+    int kw;            // warps sharing one tile (splitting the CTA's stages)
     int mc;            // activation rows per launch block (8*MB)
-    int slots;         // ring slots allocated per warp (<= kRing)
-    uint32_t off_xfrag, off_xs, off_scale, off_partial;
+    int slots;         // ring depth per warp (stages; slots-1 in flight while computing)
+    uint32_t xpitch;   // bytes per activation row of x fragments
+    uint32_t off_xfrag, off_xs, off_scale, off_red, off_partial;
 };
 
 // Pair i of the 8 fp16 pairs decoded from a thread's 16 codes holds codes
@@ -102,6 +108,20 @@ struct PairMap<3> {
         return (i == 2 || i == 7) ? 6 : (i == 1 || i == 4 || i == 6) ? 3 : 0;
     }
 };
+
+// A-fragment registers of the four MMA k-steps of one group: step s takes
+// pairs 2s and 2s+1 of the row-g codes (PA) and of the row-(g+8) codes (PB)
+// as {PA[2s], PB[2s], PA[2s+1], PB[2s+1]}.
+__device__ __forceinline__ void to_frags(const uint32_t (&PA)[8], const uint32_t (&PB)[8],
+                                         uint32_t (&a)[4][4]) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        a[s][0] = PA[2 * s];
+        a[s][1] = PB[2 * s];
+        a[s][2] = PA[2 * s + 1];
+        a[s][3] = PB[2 * s + 1];
+    }
+}
 
 // 4-bit: words w0 (codes 0..7) and w1 (codes 8..15).  Masking nibble pairs
 // (j, j+4) in place gives two fp16 subnormals per AND.
@@ -139,24 +159,6 @@ __device__ __forceinline__ void decode3(uint32_t wa, uint32_t wb, uint32_t sel0,
 }
 
 template <typename T>
-__device__ __forceinline__ void load16(const T *src, float (&f)[16]) {
-    const uint4 u0 = __ldg(reinterpret_cast<const uint4 *>(src));
-    const uint4 u1 = __ldg(reinterpret_cast<const uint4 *>(src) + 1);
-    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        if constexpr (std::is_same<T, __half>::value) {
-            const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
-            f[2 * i] = v.x;
-            f[2 * i + 1] = v.y;
-        } else {
-            f[2 * i] = __uint_as_float(w[i] << 16);
-            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-        }
-    }
-}
-
-template <typename T>
 __device__ __forceinline__ void store_out(T *p, float v);
 template <>
 __device__ __forceinline__ void store_out<__half>(__half *p, float v) { *p = __float2half_rn(v); }
@@ -180,137 +182,183 @@ __device__ __forceinline__ float half_at(const uint4 &v, int j) {
 }  // namespace
 
 template <int B, typename T, int MB>
-__global__ void __launch_bounds__(kThreads) qmv_kernel(const __grid_constant__ Params prm) {
+__global__ void __launch_bounds__(kThreads, 2) qmv_kernel(const __grid_constant__ Params prm) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int MCP = 8 * MB;  // padded activation rows per launch block
     using F = Fmt<B>;
+    constexpr int kChunks = F::kChunksPerRow / 2;  // 16-byte copies per lane per stage
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int ct = threadIdx.x;
-    const int ks = prm.ks;
-    const int tile = blockIdx.x / ks;
+    const int ks = prm.ks, kw = prm.kw, rt = prm.rt;
+    const int tile = blockIdx.x / ks;  // CTA row block: rt tiles of 16 rows
     const int rank = blockIdx.x % ks;
-    const int64_t n0 = (int64_t)tile * kRows;
+    const int wt = warp / kw;          // this warp's tile within the CTA
+    const int kslot = warp % kw;       // this warp's share of the CTA's stages
+    const int64_t nb = (int64_t)tile * 16 * rt;  // first row of the CTA
     const int64_t m0 = (int64_t)blockIdx.y * prm.mc;
-    const int Mc = (int)min((int64_t)prm.mc, prm.M - m0);  // valid activation rows here
+    const int Mc = (int)min((int64_t)prm.mc, prm.M - m0);
     const int st_begin = (int)((int64_t)prm.stages_total * rank / ks);
     const int st_end = (int)((int64_t)prm.stages_total * (rank + 1) / ks);
-    const int nst = st_end - st_begin;
-    const int gb = st_begin * kGroupsPerStage;  // first group of this CTA
-    const int gcta = nst * kGroupsPerStage;     // groups of this CTA
+    const int nst = st_end - st_begin;                          // stages of the CTA
+    const int nw = kslot < nst ? (nst - kslot + kw - 1) / kw : 0;  // stages of this warp
+    const int gb = st_begin * kGroupsPerStage;
+    const int gcta = nst * kGroupsPerStage;
 
-    uint8_t *ring = smem + (size_t)warp * prm.slots * F::kStageBytes;
+    const int slots = prm.slots;
+    uint8_t *ring = smem + (size_t)warp * slots * F::kStageBytes;
     uint8_t *xfrag = smem + prm.off_xfrag;
     float *xs = reinterpret_cast<float *>(smem + prm.off_xs);
     float *escale = reinterpret_cast<float *>(smem + prm.off_scale);  // [MCP] x multiplier
     float *oscale = escale + MCP;                                     // [MCP] y multiplier
     unsigned *amax = reinterpret_cast<unsigned *>(oscale + MCP);      // [MCP]
+    float *red = reinterpret_cast<float *>(smem + prm.off_red);
     float *partial = reinterpret_cast<float *>(smem + prm.off_partial);
 
     // ----------------------------------------------------------------------
-    // Stage issue: 16 rows x 8 groups of packed words, plus the rows' 8
-    // scales and 8 biases, as 16-byte cp.async copies.
+    // Copy plan of this lane: kChunks 16-byte pieces of the warp's 16 rows
+    // per stage, plus one scale or bias row.  A row past N is read from row
+    // N-1 instead: it only feeds output rows that are never stored.
     // ----------------------------------------------------------------------
+    const int64_t wrow0 = nb + 16 * wt;
     const int64_t row_bytes = prm.K * B / 8;
-    const int64_t wrow0 = n0 + 16 * warp;  // first weight row of this warp
-    const uint8_t *wq8 = reinterpret_cast<const uint8_t *>(prm.Wq);
-    auto issue = [&](int s, int slot) {
-        uint8_t *dst = ring + slot * F::kStageBytes;
+    const int64_t nlast = prm.N - 1;
+    uint32_t soff[kChunks], doff[kChunks];
+#pragma unroll
+    for (int i = 0; i < kChunks; ++i) {
+        const int c = lane + 32 * i;
+        const int r = c / F::kChunksPerRow, col = c % F::kChunksPerRow;
+        const int64_t n = min(wrow0 + r, nlast) - min(wrow0, nlast);
+        soff[i] = (uint32_t)(n * row_bytes + col * 16);
+        doff[i] = (uint32_t)(r * F::kRowPitch + col * 16);
+    }
+    const uint8_t *wbase = reinterpret_cast<const uint8_t *>(prm.Wq) + min(wrow0, nlast) * row_bytes;
+    const int sbr = lane & 15;
+    const __half *sbbase = ((lane < 16) ? prm.scales : prm.biases) + min(wrow0 + sbr, nlast) * prm.G;
+    const uint32_t sbdoff = F::kScalesOff + (lane >> 4) * 256 + sbr * 16;
+    auto issue = [&](int i, int slot) {
+        const int s = kslot + i * kw;  // stage within the CTA range
         const int gs = gb + s * kGroupsPerStage;
+        uint8_t *dst = ring + slot * F::kStageBytes;
+        const uint8_t *src = wbase + (int64_t)gs * F::kGroupBytes;
 #pragma unroll
-        for (int i = 0; i < F::kChunksPerRow / 2; ++i) {
-            const int c = lane + 32 * i;
-            const int r = c / F::kChunksPerRow, col = c % F::kChunksPerRow;
-            const int64_t n = wrow0 + r;
-            const bool ok = n < prm.N;
-            const uint8_t *src = ok ? wq8 + n * row_bytes + (int64_t)gs * F::kGroupBytes + col * 16
-                                    : wq8;
-            cp_async16(dst + r * F::kRowPitch + col * 16, src, ok ? 16u : 0u);
-        }
-        {
-            const int r = lane & 15;
-            const int64_t n = wrow0 + r;
-            const bool ok = n < prm.N;
-            const __half *base = (lane < 16) ? prm.scales : prm.biases;
-            const void *src = ok ? (const void *)(base + n * prm.G + gs) : (const void *)base;
-            cp_async16(dst + F::kScalesOff + (lane >> 4) * 256 + r * 16, src, ok ? 16u : 0u);
-        }
+        for (int c = 0; c < kChunks; ++c) cp_async16(dst + doff[c], src + soff[c], 16u);
+        cp_async16(dst + sbdoff, sbbase + gs, 16u);
     };
-    const int slots = prm.slots;
-#pragma unroll
-    for (int s = 0; s < kRing - 1; ++s) {
-        if (s < nst) issue(s, s);
+    // Raw x of this CTA's K range goes to the fragment rows first (one group
+    // of copies, committed before the weight stages): one round trip that
+    // overlaps the weight copies.
+    {
+        const T *xg = static_cast<const T *>(prm.x);
+        const int per_row = gcta * 8;  // 16-byte chunks per activation row
+        for (int c = ct; c < Mc * per_row; c += kThreads) {
+            const int m = c / per_row, q = c - m * per_row;
+            cp_async16(xfrag + (size_t)m * prm.xpitch + q * 16,
+                       xg + (m0 + m) * prm.K + 64 * gb + 8 * q, 16u);
+        }
+        cp_async_commit();
+    }
+    for (int i = 0; i < slots - 1; ++i) {
+        if (i < nw) issue(i, i);
         cp_async_commit();
     }
 
     // ----------------------------------------------------------------------
-    // Prologue (all threads): x for this CTA's K range, permuted into
-    // B-fragment order, and per-group sums of x.
+    // Prologue (all threads): once the raw x has landed, rewrite it in place
+    // into B-fragment order and take per-group sums of x (times 2^-24, the
+    // scale of the MMA products).  The four quarters of a group belong to
+    // four adjacent lanes, which read the whole group before any writes.
     // ----------------------------------------------------------------------
-    const T *xg = static_cast<const T *>(prm.x);
     if (ct < MCP) {
         escale[ct] = 1.f;
-        oscale[ct] = 1.f;
+        oscale[ct] = 16777216.f;
         amax[ct] = 0u;
+    }
+    switch (slots) {  // the x group is complete once slots-1 younger groups may pend
+        case 2: cp_async_wait<1>(); break;
+        case 3: cp_async_wait<2>(); break;
+        case 4: cp_async_wait<3>(); break;
+        case 5: cp_async_wait<4>(); break;
+        default: cp_async_wait<5>(); break;
     }
     __syncthreads();
     if constexpr (std::is_same<T, __nv_bfloat16>::value) {
         // Largest |x| per activation row over this CTA's K range; pick 2^-e
         // so that the fp16 copy stays below 2^15 in magnitude.
-        const int kc = gcta * 64;
         for (int m = 0; m < Mc; ++m) {
-            float a = 0.f;
-            for (int k = 16 * ct; k < kc; k += 16 * kThreads) {
-                float f[16];
-                load16<T>(xg + (m0 + m) * prm.K + 64 * gb + k, f);
+            const uint4 *row = reinterpret_cast<const uint4 *>(xfrag + (size_t)m * prm.xpitch);
+            unsigned a = 0u;  // max of |x| as bits (bf16 in the high half)
+            for (int c = ct; c < gcta * 8; c += kThreads) {
+                const uint4 v = row[c];
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(f[i]));
+                for (int i = 0; i < 4; ++i) {
+                    a = max(a, (w[i] << 16) & 0x7FFF0000u);
+                    a = max(a, w[i] & 0x7FFF0000u);
+                }
             }
 #pragma unroll
-            for (int d = 16; d >= 1; d >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, d));
-            if (lane == 0) atomicMax(&amax[m], __float_as_uint(a));
+            for (int d = 16; d >= 1; d >>= 1) a = max(a, __shfl_xor_sync(0xffffffffu, a, d));
+            if (lane == 0) atomicMax(&amax[m], a);
         }
         __syncthreads();
         if (ct < Mc) {
             const int e = (int)((amax[ct] >> 23) & 0xFF) - 127;  // floor(log2 amax)
             const int sh = e > 14 ? e - 14 : 0;
             escale[ct] = __int_as_float((127 - sh) << 23);
-            oscale[ct] = __int_as_float((127 + sh) << 23);
+            oscale[ct] = __int_as_float((127 + 24 + sh) << 23);
         }
         __syncthreads();
     }
-    for (int ub = 0; ub < gcta * Mc * 4; ub += kThreads) {
-        const int u = ub + ct;
-        const bool valid = u < gcta * Mc * 4;
-        const int j = valid ? u / (Mc * 4) : 0, m = valid ? (u >> 2) % Mc : 0, t = u & 3;
-        float f[16];
-        if (valid) {
-            load16<T>(xg + (m0 + m) * prm.K + 64 * (gb + j) + 16 * t, f);
-        } else {
+    for (int m = 0; m < Mc; ++m) {
+        uint8_t *xrowp = xfrag + (size_t)m * prm.xpitch;
+        const float es = escale[m];
+        for (int vb = 0; vb < gcta * 4; vb += kThreads) {
+            const int v = vb + ct;  // (group j, quarter t) of row m
+            const bool valid = v < gcta * 4;
+            const int j = v >> 2, t = v & 3;
+            float f[16];
+            if (valid) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(xrowp + 32 * v);
+                const uint4 u0 = src[0], u1 = src[1];
+                const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
-            for (int i = 0; i < 16; ++i) f[i] = 0.f;
-        }
-        const float es = valid ? escale[m] : 0.f;
-        float sum = 0.f;
+                for (int i = 0; i < 8; ++i) {
+                    if constexpr (std::is_same<T, __half>::value) {
+                        const float2 fv = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+                        f[2 * i] = fv.x;
+                        f[2 * i + 1] = fv.y;
+                    } else {
+                        f[2 * i] = __uint_as_float(w[i] << 16);
+                        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+                    }
+                }
+            } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            f[i] *= es;
-            sum += f[i];
-        }
-        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-        if (valid) {
-            uint32_t pr[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float sc = __int_as_float((127 - PairMap<B>::p(i)) << 23);  // 2^-p
-                pr[i] = pack_half2(f[PairMap<B>::lo(i)] * sc, f[PairMap<B>::hi(i)] * sc);
+                for (int i = 0; i < 16; ++i) f[i] = 0.f;
             }
-            uint4 *dst = reinterpret_cast<uint4 *>(xfrag);
-            dst[((j * 2 + 0) * Mc + m) * 4 + t] = make_uint4(pr[0], pr[1], pr[2], pr[3]);
-            dst[((j * 2 + 1) * Mc + m) * 4 + t] = make_uint4(pr[4], pr[5], pr[6], pr[7]);
-            if (t == 0) xs[j * MCP + m] = sum;
+            float sum = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                f[i] *= es;
+                sum += f[i];
+            }
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            __syncwarp();  // the group's four quarters are read before they are overwritten
+            if (valid) {
+                uint32_t pr[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float sc = __int_as_float((127 - PairMap<B>::p(i)) << 23);  // 2^-p
+                    pr[i] = pack_half2(f[PairMap<B>::lo(i)] * sc, f[PairMap<B>::hi(i)] * sc);
+                }
+                uint4 *dst = reinterpret_cast<uint4 *>(xrowp) + j * 8 + t;
+                dst[0] = make_uint4(pr[0], pr[1], pr[2], pr[3]);
+                dst[4] = make_uint4(pr[4], pr[5], pr[6], pr[7]);
+                if (t == 0) xs[j * MCP + m] = sum * 5.9604644775390625e-08f;  // * 2^-24
+            }
         }
     }
     for (int u = ct; u < gcta * MCP; u += kThreads)
@@ -318,7 +366,8 @@ __global__ void __launch_bounds__(kThreads) qmv_kernel(const __grid_constant__ P
     __syncthreads();
 
     // ----------------------------------------------------------------------
-    // Main loop: each warp over its 16 rows and all stages of the CTA.
+    // Main loop: the warp's 16 rows over its stages.  The next stage is
+    // queued before waiting on the current one.
     // ----------------------------------------------------------------------
     const int g = lane >> 2, t = lane & 3;
     uint32_t sel0 = 0, sel2 = 0;
@@ -335,57 +384,69 @@ __global__ void __launch_bounds__(kThreads) qmv_kernel(const __grid_constant__ P
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[mb][i] = 0.f;
 
-    const uint4 *xf4 = reinterpret_cast<const uint4 *>(xfrag);
-    for (int si = 0; si < nst; ++si) {
-        cp_async_wait<kRing - 2>();
+    // x-fragment rows of this lane, clamped to the valid rows: a lane whose
+    // activation row does not exist reads row Mc-1 instead, which only feeds
+    // output columns that are never stored (MMA columns are independent).
+    const uint8_t *xrow[MB];
+#pragma unroll
+    for (int mb = 0; mb < MB; ++mb)
+        xrow[mb] = xfrag + (size_t)min(mb * 8 + g, Mc - 1) * prm.xpitch + 16 * t;
+    // this lane's first code word of row g in a stage
+    const int wlane_off = g * F::kRowPitch + (B == 4 ? 8 * t : 4 * wi3);
+
+    for (int i = 0; i < nw; ++i) {
+        if (i + slots - 1 < nw) issue(i + slots - 1, (i + slots - 1) % slots);
+        cp_async_commit();
+        // stage i has landed once at most slots-1 younger groups are pending
+        switch (slots) {
+            case 2: cp_async_wait<1>(); break;
+            case 3: cp_async_wait<2>(); break;
+            case 4: cp_async_wait<3>(); break;
+            case 5: cp_async_wait<4>(); break;
+            default: cp_async_wait<5>(); break;
+        }
         __syncwarp();
-        const int slot = si % slots;
-        const uint8_t *sb = ring + slot * F::kStageBytes;
+        const uint8_t *sb = ring + (i % slots) * F::kStageBytes;
+        const int s = kslot + i * kw;
         const uint4 sA = *reinterpret_cast<const uint4 *>(sb + F::kScalesOff + g * 16);
         const uint4 sB = *reinterpret_cast<const uint4 *>(sb + F::kScalesOff + (g + 8) * 16);
         const uint4 bA = *reinterpret_cast<const uint4 *>(sb + F::kScalesOff + 256 + g * 16);
         const uint4 bB = *reinterpret_cast<const uint4 *>(sb + F::kScalesOff + 256 + (g + 8) * 16);
+        const uint8_t *wa = sb + wlane_off;
+        const uint8_t *xst[MB];
+#pragma unroll
+        for (int mb = 0; mb < MB; ++mb) xst[mb] = xrow[mb] + (size_t)s * kGroupsPerStage * 128;
+        const float *xss = xs + s * kGroupsPerStage * MCP + 2 * t;
 #pragma unroll
         for (int j = 0; j < kGroupsPerStage; ++j) {
-            const int grp = si * kGroupsPerStage + j;  // group within the CTA range
             uint32_t PA[8], PB[8];
             if constexpr (B == 4) {
-                const uint2 qa = *reinterpret_cast<const uint2 *>(sb + g * F::kRowPitch +
-                                                                  j * F::kGroupBytes + 8 * t);
-                const uint2 qb = *reinterpret_cast<const uint2 *>(sb + (g + 8) * F::kRowPitch +
-                                                                  j * F::kGroupBytes + 8 * t);
+                const uint2 qa = *reinterpret_cast<const uint2 *>(wa + j * F::kGroupBytes);
+                const uint2 qb =
+                    *reinterpret_cast<const uint2 *>(wa + 8 * F::kRowPitch + j * F::kGroupBytes);
                 decode4(qa.x, qa.y, PA);
                 decode4(qb.x, qb.y, PB);
             } else {
-                const uint32_t *pa =
-                    reinterpret_cast<const uint32_t *>(sb + g * F::kRowPitch + j * F::kGroupBytes);
-                const uint32_t *pb = reinterpret_cast<const uint32_t *>(
-                    sb + (g + 8) * F::kRowPitch + j * F::kGroupBytes);
-                decode3(pa[wi3], pa[wi3 + 1], sel0, sel2, PA);
-                decode3(pb[wi3], pb[wi3 + 1], sel0, sel2, PB);
+                const uint32_t *pa = reinterpret_cast<const uint32_t *>(wa + j * F::kGroupBytes);
+                const uint32_t *pb =
+                    reinterpret_cast<const uint32_t *>(wa + 8 * F::kRowPitch + j * F::kGroupBytes);
+                decode3(pa[0], pa[1], sel0, sel2, PA);
+                decode3(pb[0], pb[1], sel0, sel2, PB);
             }
-            const float sa = half_at(sA, j) * 16777216.f, sbb = half_at(sB, j) * 16777216.f;
+            uint32_t a[4][4];
+            to_frags(PA, PB, a);
+            const float sa = half_at(sA, j), sbb = half_at(sB, j);
             const float ba = half_at(bA, j), bb = half_at(bB, j);
 #pragma unroll
             for (int mb = 0; mb < MB; ++mb) {
-                const int m = mb * 8 + g;
-                uint4 q0 = make_uint4(0, 0, 0, 0), q1 = make_uint4(0, 0, 0, 0);
-                if (m < Mc) {
-                    q0 = xf4[((grp * 2 + 0) * Mc + m) * 4 + t];
-                    q1 = xf4[((grp * 2 + 1) * Mc + m) * 4 + t];
-                }
-                const float2 xv = *reinterpret_cast<const float2 *>(&xs[grp * MCP + mb * 8 + 2 * t]);
+                const uint4 q0 = *reinterpret_cast<const uint4 *>(xst[mb] + j * 128);
+                const uint4 q1 = *reinterpret_cast<const uint4 *>(xst[mb] + j * 128 + 64);
+                const float2 xv = *reinterpret_cast<const float2 *>(&xss[j * MCP + mb * 8]);
                 float d[4] = {0.f, 0.f, 0.f, 0.f};
-                {
-                    const uint32_t a0[4] = {PA[0], PB[0], PA[1], PB[1]};
-                    mma_f16_16816(d, a0, q0.x, q0.y, d);
-                    const uint32_t a1[4] = {PA[2], PB[2], PA[3], PB[3]};
-                    mma_f16_16816(d, a1, q0.z, q0.w, d);
-                    const uint32_t a2[4] = {PA[4], PB[4], PA[5], PB[5]};
-                    mma_f16_16816(d, a2, q1.x, q1.y, d);
-                    const uint32_t a3[4] = {PA[6], PB[6], PA[7], PB[7]};
-                    mma_f16_16816(d, a3, q1.z, q1.w, d);
-                }
+                mma_f16_16816(d, a[0], q0.x, q0.y, d);
+                mma_f16_16816(d, a[1], q0.z, q0.w, d);
+                mma_f16_16816(d, a[2], q1.x, q1.y, d);
+                mma_f16_16816(d, a[3], q1.z, q1.w, d);
                 acc[mb][0] = fmaf(sa, d[0], fmaf(ba, xv.x, acc[mb][0]));
                 acc[mb][1] = fmaf(sa, d[1], fmaf(ba, xv.y, acc[mb][1]));
                 acc[mb][2] = fmaf(sbb, d[2], fmaf(bb, xv.x, acc[mb][2]));
@@ -393,28 +454,31 @@ __global__ void __launch_bounds__(kThreads) qmv_kernel(const __grid_constant__ P
             }
         }
         __syncwarp();
-        if (si + kRing - 1 < nst) issue(si + kRing - 1, (si + kRing - 1) % slots);
-        cp_async_commit();
     }
     cp_async_wait<0>();
 
     // ----------------------------------------------------------------------
-    // Epilogue.
+    // Epilogue: add the kw warps of each tile in warp order, then write y
+    // (or this CTA's partial tile when K is split over a cluster).
     // ----------------------------------------------------------------------
+#pragma unroll
+    for (int mb = 0; mb < MB; ++mb)
+        *reinterpret_cast<float4 *>(&red[((warp * MB + mb) * 32 + lane) * 4]) =
+            make_float4(acc[mb][0], acc[mb][1], acc[mb][2], acc[mb][3]);
+    __syncthreads();
     T *y = static_cast<T *>(prm.y);
-    const int rowA = 16 * warp + g, rowB = rowA + 8;  // within the CTA
-#pragma unroll
-    for (int mb = 0; mb < MB; ++mb) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int row = (i < 2) ? rowA : rowB;
-            const int col = mb * 8 + 2 * t + (i & 1);
-            const float v = acc[mb][i] * oscale[col];
-            if (ks == 1) {
-                if (col < Mc && n0 + row < prm.N) store_out<T>(&y[(m0 + col) * prm.N + n0 + row], v);
-            } else {
-                partial[row * MCP + col] = v;
-            }
+    for (int e = ct; e < rt * MB * 128; e += kThreads) {
+        const int tl = e / (MB * 128), rem = e % (MB * 128);
+        const int mb = rem / 128, ln = (rem / 4) % 32, i = rem % 4;
+        float v = 0.f;
+        for (int k = 0; k < kw; ++k) v += red[(((tl * kw + k) * MB + mb) * 32 + ln) * 4 + i];
+        const int row = 16 * tl + (ln >> 2) + 8 * (i >> 1);
+        const int col = mb * 8 + 2 * (ln & 3) + (i & 1);
+        v *= oscale[col];
+        if (ks == 1) {
+            if (col < Mc && nb + row < prm.N) store_out<T>(&y[(m0 + col) * prm.N + nb + row], v);
+        } else {
+            partial[row * MCP + col] = v;
         }
     }
     if (ks > 1) {
@@ -422,13 +486,13 @@ __global__ void __launch_bounds__(kThreads) qmv_kernel(const __grid_constant__ P
         // of the cluster, rank 0 first.
         cluster_sync();
         const uint32_t base = smem_u32(partial);
-        for (int e = rank + ks * ct; e < kRows * MCP; e += ks * kThreads) {
+        for (int e = rank + ks * ct; e < 16 * rt * MCP; e += ks * kThreads) {
             const int row = e / MCP, col = e % MCP;
-            if (col >= Mc || n0 + row >= prm.N) continue;
+            if (col >= Mc || nb + row >= prm.N) continue;
             float v = 0.f;
             for (int r = 0; r < ks; ++r)
                 v += ld_dsmem_f32(map_to_rank(base + 4u * (uint32_t)e, (uint32_t)r));
-            store_out<T>(&y[(m0 + col) * prm.N + n0 + row], v);
+            store_out<T>(&y[(m0 + col) * prm.N + nb + row], v);
         }
         cluster_sync();
     }
@@ -440,7 +504,7 @@ __global__ void __launch_bounds__(kThreads) qmv_kernel(const __grid_constant__ P
 namespace {
 
 struct Plan {
-    int MB, ks, mc, m_chunks, tiles;
+    int MB, ks, rt, kw, mc, m_chunks, blocks;
     size_t smem;
     Params prm;
 };
@@ -449,6 +513,50 @@ constexpr size_t kSmemLimit = 227 * 1024;
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+struct Layout {
+    size_t smem;
+    uint32_t xpitch, off_xfrag, off_xs, off_scale, off_red, off_partial;
+};
+
+Layout layout(int B, int MB, int mc_valid, int st_cta, int rt, int ks, int slots) {
+    Layout L;
+    const int mc = 8 * MB;
+    const int stage_bytes = B == 4 ? Fmt<4>::kStageBytes : Fmt<3>::kStageBytes;
+    size_t off = (size_t)kWarps * slots * stage_bytes;
+    off = align_up(off, 128);
+    L.off_xfrag = (uint32_t)off;
+    const size_t gmax = (size_t)st_cta * kGroupsPerStage;
+    // one row of fragments per activation row; the 64-byte pad puts
+    // consecutive rows in different halves of the banks
+    L.xpitch = (uint32_t)(gmax * 128 + 64);
+    off += (size_t)L.xpitch * mc_valid;
+    off = align_up(off, 128);
+    L.off_xs = (uint32_t)off;
+    off += gmax * mc * 4;
+    off = align_up(off, 128);
+    L.off_scale = (uint32_t)off;
+    off += 3 * mc * 4;
+    off = align_up(off, 128);
+    L.off_red = (uint32_t)off;
+    off += (size_t)kWarps * MB * 128 * 4;
+    L.off_partial = (uint32_t)off;
+    off += ks > 1 ? (size_t)16 * rt * mc * 4 : 0;
+    L.smem = align_up(off, 128);
+    return L;
+}
+
+std::atomic<int> g_force_rt{0}, g_force_ks{0}, g_force_slots{0};
+
+// Pick the CTA shape (rt row tiles x kw K-ways, rt*kw = 8 warps), the
+// cluster split ks and the ring depth.  Rule, from timing every (rt, ks) on
+// the workload shapes on GB300: every CTA pays a fixed x-preparation cost
+// (~2 us) and every cluster split a reduction (~1 us), so
+//   * use the largest row block whose CTA count still covers half the SMs,
+//     in a single resident wave, without a cluster split;
+//   * split K over a cluster only when even 16-row blocks leave half the SMs
+//     idle (narrow N), or when a warp would stream more than 12 stages;
+//   * a ring of three stages per warp (two in flight) when it fits; deeper
+//     rings only lowered occupancy.
 bool make_plan(const MatmulArgs &a, Plan &p) {
     const int B = a.bits;
     if (a.K % 512 != 0 || a.M < 1 || a.N < 1) return false;
@@ -456,47 +564,57 @@ bool make_plan(const MatmulArgs &a, Plan &p) {
     p.mc = 8 * p.MB;
     p.m_chunks = (int)((a.M + p.mc - 1) / p.mc);
     if (p.m_chunks > 65535) return false;
-    const int64_t tiles = (a.N + kRows - 1) / kRows;
-    if (tiles * kMaxCluster > (int64_t)INT32_MAX) return false;
-    p.tiles = (int)tiles;
-    const int stages_total = (int)(a.K / 512);
+    const int64_t tiles16 = (a.N + 15) / 16;
+    const int S = (int)(a.K / 512);
     const int mc_valid = (int)std::min<int64_t>(a.M, p.mc);
+    if (16 * (a.K * B / 8) >= ((int64_t)1 << 31)) return false;  // 32-bit copy offsets
     const int sms = num_sms();
-    auto xbytes = [&](int k) {
-        const size_t g = (size_t)((stages_total + k - 1) / k) * kGroupsPerStage;
-        return g * mc_valid * 128 + g * p.mc * 4;
-    };
-    // Split K over a cluster until there are about two CTAs per SM and x for
-    // a CTA's K range fits comfortably in shared memory.
+    const int frt = g_force_rt.load(), fks = g_force_ks.load(), fsl = g_force_slots.load();
+    const int64_t want = std::max<int64_t>(1, sms / 2);  // CTAs to cover half the SMs
+
+    int rt = 1;
+    for (int r = kWarps; r >= 1; r /= 2)
+        if ((tiles16 + r - 1) / r * p.m_chunks >= want) { rt = r; break; }
+    if (frt) rt = frt;
+    const int kw = kWarps / rt;
+    const int64_t blocks = (tiles16 + rt - 1) / rt;
     int ks = 1;
-    const int ks_max = std::min(kMaxCluster, stages_total);
-    while (ks < ks_max &&
-           ((int64_t)tiles * p.m_chunks * ks < 2 * sms || xbytes(ks) > 64 * 1024))
-        ++ks;
-    if (xbytes(ks) > 100 * 1024) return false;
-    p.ks = ks;
-    const int st_cta = (stages_total + ks - 1) / ks;
-    const int slots = std::min(kRing, st_cta);
-    const int stage_bytes = B == 4 ? Fmt<4>::kStageBytes : Fmt<3>::kStageBytes;
+    if (blocks * p.m_chunks < want) ks = (int)((int64_t)(sms * 4 / 5 + blocks * p.m_chunks - 1) / (blocks * p.m_chunks));
+    if ((S + kw - 1) / kw > 12) ks = std::max(ks, (S / kw + 5) / 6);
+    ks = std::max(1, std::min({ks, S, kMaxCluster}));
+    if (fks) ks = std::min(fks, S);
+    if (blocks * ks > (int64_t)INT32_MAX) return false;
 
+    bool found = false;
+    // the x fragments of the CTA's K range must fit: grow ks until they do
+    for (; ks <= std::min(S, kMaxCluster) && !found; ++ks) {
+        const int st_cta = (S + ks - 1) / ks;
+        const int per_warp_st = (st_cta + kw - 1) / kw;
+        int slots = fsl ? fsl : 3;
+        slots = std::max(2, std::min(slots, per_warp_st + 1));
+        Layout L = layout(B, p.MB, mc_valid, st_cta, rt, ks, slots);
+        while (!fsl && L.smem > kSmemLimit && slots > 2)
+            L = layout(B, p.MB, mc_valid, st_cta, rt, ks, --slots);
+        if (L.smem > kSmemLimit || (L.off_scale - L.off_xfrag) > 120 * 1024) {
+            if (fks) break;
+            continue;
+        }
+        found = true;
+        p.rt = rt;
+        p.kw = kw;
+        p.ks = ks;
+        p.prm.slots = slots;
+        p.blocks = (int)blocks;
+        p.smem = L.smem;
+        p.prm.xpitch = L.xpitch;
+        p.prm.off_xfrag = L.off_xfrag;
+        p.prm.off_xs = L.off_xs;
+        p.prm.off_scale = L.off_scale;
+        p.prm.off_red = L.off_red;
+        p.prm.off_partial = L.off_partial;
+    }
+    if (!found) return false;
     Params &q = p.prm;
-    size_t off = (size_t)kWarps * slots * stage_bytes;
-    off = align_up(off, 128);
-    q.off_xfrag = (uint32_t)off;
-    const size_t gmax = (size_t)st_cta * kGroupsPerStage;
-    off += gmax * mc_valid * 128;
-    off = align_up(off, 128);
-    q.off_xs = (uint32_t)off;
-    off += gmax * p.mc * 4;
-    off = align_up(off, 128);
-    q.off_scale = (uint32_t)off;
-    off += 3 * p.mc * 4;
-    off = align_up(off, 128);
-    q.off_partial = (uint32_t)off;
-    off += ks > 1 ? (size_t)kRows * p.mc * 4 : 0;
-    p.smem = align_up(off, 128);
-    if (p.smem > kSmemLimit) return false;
-
     q.x = a.x;
     q.Wq = a.Wq;
     q.scales = static_cast<const __half *>(a.scales);
@@ -506,10 +624,11 @@ bool make_plan(const MatmulArgs &a, Plan &p) {
     q.N = a.N;
     q.K = a.K;
     q.G = (int)(a.K / 64);
-    q.stages_total = stages_total;
-    q.ks = ks;
+    q.stages_total = S;
+    q.ks = p.ks;
+    q.rt = p.rt;
+    q.kw = p.kw;
     q.mc = p.mc;
-    q.slots = slots;
     return true;
 }
 
@@ -526,7 +645,7 @@ cudaError_t launch_plan(const Plan &p, cudaStream_t stream) {
     });
     if (attr_err != cudaSuccess) return attr_err;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(p.tiles * p.ks), (unsigned)p.m_chunks, 1);
+    cfg.gridDim = dim3((unsigned)(p.blocks * p.ks), (unsigned)p.m_chunks, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = stream;
@@ -567,6 +686,19 @@ cudaError_t qmv_launch(const MatmulArgs &a) {
                                   : launch_mb<3, __half>(p, a.stream);
     return a.dtype == AQ_BF16 ? launch_mb<4, __nv_bfloat16>(p, a.stream)
                               : launch_mb<4, __half>(p, a.stream);
+}
+
+void qmv_force_geometry(int rt, int ks, int slots) {
+    g_force_rt.store(rt);
+    g_force_ks.store(ks);
+    g_force_slots.store(slots);
+}
+
+int qmv_describe(const MatmulArgs &a, char *buf, int len) {
+    Plan p;
+    if (!make_plan(a, p)) return snprintf(buf, len, "qmv: unsupported");
+    return snprintf(buf, len, "qmv rows/cta=%d kways=%d cluster=%d ring=%d grid=%dx%d smem=%zu mb=%d",
+                    16 * p.rt, p.kw, p.ks, p.prm.slots, p.blocks * p.ks, p.m_chunks, p.smem, p.MB);
 }
 
 cudaError_t qmv_read_error(uint32_t *code, bool clear) {
