@@ -1,22 +1,540 @@
-// Large-M kernel (tcgen05 + TMEM): not built yet; the dispatch rule sends
-// every shape to the small-M or generic kernels meanwhile.
+// Large-M kernel ("tc"): y = x . W^T on the 5th-generation tensor cores
+// (tcgen05, accumulators in tensor memory), for M large enough that the
+// product is a dense contraction.
+//
+// Method (mlx-bun pages, @mlx-bun/inference 1.0.0, kernels/quantization/):
+// affine-split-mma.ts computes any number of activation rows with the
+// weights as the A operand (8 weight rows per simdgroup tile) and x^T as B,
+// dequantising each weight as fma(q, scale, bias) right before the matrix
+// product; the trellis prefill kernels on the same site reconstruct a weight
+// tile into threadgroup memory and then run matrix products on it.  Here:
+//
+//   * A = 128 weight rows x 64 k (one group) per stage, dequantised by eight
+//     warps into shared memory as bf16 (x bf16) or fp16 (x fp16) in the
+//     128-byte-swizzled K-major layout the tensor core reads directly;
+//   * B = BM activation rows x 64 k of x, loaded by TMA (tensor map, 128-byte
+//     swizzle) - x is never converted;
+//   * one thread issues tcgen05.mma (M=128, N=BM, K=16) x4 per stage into an
+//     fp32 accumulator in tensor memory; two accumulators alternate so the
+//     epilogue of one tile overlaps the main loop of the next;
+//   * four epilogue warps read the accumulator with tcgen05.ld, round to the
+//     output type and store y; persistent CTAs (one per SM) walk the tiles.
+//
+// Roles (448 threads): warp 0 TMA producer, warp 1 MMA issuer and tensor
+// memory owner, warps 2-5 epilogue, warps 6-13 dequantisation (each streams
+// its 16 weight rows through a two-slot cp.async ring).  Every mbarrier wait
+// is bounded; a wait that gives up records an error and the CTA winds down.
 #include "aq_internal.h"
+#include "aq_ptx.cuh"
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
 #include <cstdio>
+#include <mutex>
 
 namespace aq {
 
-bool tc_supported(const MatmulArgs &) { return false; }
+__device__ uint32_t g_tc_error;
 
-cudaError_t tc_launch(const MatmulArgs &) { return cudaErrorNotSupported; }
+namespace {
 
-int tc_describe(const MatmulArgs &, char *buf, int len) {
-    return snprintf(buf, len, "tc: not built");
+constexpr int kThreadsTc = 14 * 32;
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpDq = 6, kDqWarps = 8;  // warps 2-5: epilogue
+constexpr int kStages = 3;    // A/B stages (one 64-wide group each)
+constexpr int kRawSlots = 2;  // raw super-stages per dequant warp
+constexpr int kGroups = 8;    // groups per raw super-stage (512 k)
+constexpr int kATileBytes = 128 * 128;
+
+template <int B>
+struct Raw {
+    static constexpr int kGroupBytes = 8 * B;
+    static constexpr int kRowBytes = kGroups * kGroupBytes;  // 256 / 192
+    static constexpr int kChunksPerRow = kRowBytes / 16;    // 16 / 12
+    static constexpr int kRowPitch = kRowBytes + (B == 4 ? 32 : 16);
+    static constexpr int kSbOff = 16 * kRowPitch;  // scales[16][8] then biases[16][8]
+    static constexpr int kSlotBytes = kSbOff + 2 * 16 * 16;
+};
+
+struct TcParams {
+    const uint32_t *Wq;
+    const __half *scales;
+    const __half *biases;
+    void *y;
+    int M, N, K, G;
+    int n_tiles, m_tiles;
+    uint32_t off_b, off_raw, off_bar, tmem_cols;
+};
+
+__device__ __forceinline__ void tc_record(volatile int *flag, uint32_t code) {
+    *flag = 1;
+    atomicOr(&g_tc_error, code);
 }
 
-cudaError_t tc_read_error(uint32_t *code, bool) {
-    *code = 0;
-    return cudaSuccess;
+// Bounded mbarrier wait; gives up at once if another role already gave up.
+__device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile int *flag,
+                                        uint32_t code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*flag) return false;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1; it < (1u << 31); ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0u) {
+            if (*flag) return false;
+            if (globaltimer_ns() - t0 > AQ_WAIT_LIMIT_NS) break;
+        }
+    }
+    tc_record(flag, code);
+    return false;
+}
+
+__device__ __forceinline__ float h_at(const uint4 &v, int j) {
+    const uint32_t w = j < 2 ? v.x : j < 4 ? v.y : j < 6 ? v.z : v.w;
+    return __half2float(__ushort_as_half((unsigned short)((j & 1) ? (w >> 16) : (w & 0xFFFFu))));
+}
+__device__ __forceinline__ uint32_t h2_at(const uint4 &v, int j) {  // (h_j, h_j) as half2 bits
+    const uint32_t w = j < 2 ? v.x : j < 4 ? v.y : j < 6 ? v.z : v.w;
+    return prmt(w, 0u, (j & 1) ? 0x3232u : 0x1010u);
+}
+
+__device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// 8 codes (code i at bit bi*i of u) -> 8 dequantised values as 4 packed pairs.
+// bf16: w = fma(128 + q, s, b - 128 s) in fp32 (the code placed in the
+// mantissa of 128.0f), rounded once to bf16.  fp16: (q_lo, q_hi) exact as
+// halves, then one half2 fma with (s, s) and (b, b).
+template <int BITS, bool BF16>
+__device__ __forceinline__ uint4 dequant8(uint32_t u, float s, float bb, uint32_t s2, uint32_t b2) {
+    uint32_t out[4];
+    if constexpr (BF16) {
+        float f[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int sh = 16 - BITS * i;  // move code i to bit 16
+            const uint32_t t = sh >= 0 ? (u << sh) : (u >> (-sh));
+            const uint32_t m = ((1u << BITS) - 1u) << 16;
+            f[i] = fmaf(__uint_as_float((t & m) | 0x43000000u), s, bb);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) out[i] = bf16x2(f[2 * i], f[2 * i + 1]);
+    } else {
+        const __half2 magic = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            // code 2i to bit 0, code 2i+1 to bit 16
+            const uint32_t v = u >> (2 * BITS * i);
+            const uint32_t msk = (1u << BITS) - 1u;
+            const uint32_t pr = (v & msk) | ((v << (16 - BITS)) & (msk << 16));
+            const uint32_t qq = pr | 0x64006400u;  // halves 1024 + code
+            __half2 q = __hsub2(*reinterpret_cast<const __half2 *>(&qq), magic);
+            __half2 w = __hfma2(q, *reinterpret_cast<const __half2 *>(&s2),
+                                *reinterpret_cast<const __half2 *>(&b2));
+            out[i] = *reinterpret_cast<uint32_t *>(&w);
+        }
+    }
+    return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+template <typename T>
+__device__ __forceinline__ T cvt_out(float v);
+template <>
+__device__ __forceinline__ __half cvt_out<__half>(float v) { return __float2half_rn(v); }
+template <>
+__device__ __forceinline__ __nv_bfloat16 cvt_out<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+}  // namespace
+
+template <int B, bool BF16, int BM>
+__global__ void __launch_bounds__(kThreadsTc, 1)
+    tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tmap_x) {
+    using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+    using R = Raw<B>;
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    uint8_t *a_ring = smem;
+    uint8_t *b_ring = smem + p.off_b;
+    uint8_t *raw = smem + p.off_raw;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.off_bar);
+    uint64_t *a_full = bars;
+    uint64_t *b_full = bars + kStages;
+    uint64_t *ab_empty = bars + 2 * kStages;
+    uint64_t *acc_full = bars + 3 * kStages;
+    uint64_t *acc_empty = acc_full + 2;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(acc_empty + 2);
+    volatile int *flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int total = p.n_tiles * p.m_tiles;
+    const int G = p.G;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&a_full[s], kDqWarps);
+            mbar_init(&b_full[s], 1);
+            mbar_init(&ab_empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 4);
+        }
+        *flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(tmem_holder, p.tmem_cols);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == kWarpTma) {
+        // ------------------------------------------------------------------
+        // x tiles: BM rows x 64 k per stage, 128-byte swizzled, by TMA.
+        // ------------------------------------------------------------------
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+                const int m0 = (tile % p.m_tiles) * BM;
+                for (int g = 0; g < G; ++g, ++it) {
+                    const int slot = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1u;
+                    if (it >= kStages && !tc_wait(&ab_empty[slot], ph ^ 1u, flag, 0x0102)) goto tma_done;
+                    mbar_arrive_expect_tx(&b_full[slot], BM * 128);
+                    tma_load_2d(b_ring + slot * (BM * 128), &tmap_x, 64 * g, m0, &b_full[slot]);
+                }
+            }
+        tma_done:;
+        }
+    } else if (warp == kWarpMma) {
+        // ------------------------------------------------------------------
+        // MMA issue: 4 x (128 x BM x 16) per stage into accumulator b.
+        // ------------------------------------------------------------------
+        if (lane == 0) {
+            const uint32_t idesc = (1u << 4) | ((BF16 ? 1u : 0u) << 7) | ((BF16 ? 1u : 0u) << 10) |
+                                   ((uint32_t)(BM >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+            uint32_t it = 0, ti = 0;
+            for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++ti) {
+                const uint32_t b = ti & 1u, use = ti >> 1;
+                if (ti >= 2 && !tc_wait(&acc_empty[b], (use & 1u) ^ 1u, flag, 0x0202)) break;
+                tc_fence_after();
+                const uint32_t d = tmem + b * BM;
+                bool ok = true;
+                for (int g = 0; g < G; ++g, ++it) {
+                    const int slot = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1u;
+                    if (!tc_wait(&a_full[slot], ph, flag, 0x0302) ||
+                        !tc_wait(&b_full[slot], ph, flag, 0x0402)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_base = smem_u32(a_ring + slot * kATileBytes);
+                    const uint32_t b_base = smem_u32(b_ring + slot * (BM * 128));
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma_f16(d, sw128_desc(a_base + 32 * kk), sw128_desc(b_base + 32 * kk),
+                                   idesc, (g | kk) != 0);
+                    tc_commit(&ab_empty[slot]);
+                }
+                if (!ok) break;
+                tc_commit(&acc_full[b]);
+            }
+        }
+    } else if (warp < kWarpDq) {
+        // ------------------------------------------------------------------
+        // Epilogue: TMEM lanes 32q..32q+31 (weight rows), BM columns (x rows).
+        // ------------------------------------------------------------------
+        const int q = warp & 3;
+        T *y = static_cast<T *>(p.y);
+        uint32_t ti = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++ti) {
+            const uint32_t b = ti & 1u, use = ti >> 1;
+            if (!tc_wait(&acc_full[b], use & 1u, flag, 0x0502)) break;
+            tc_fence_after();
+            const int n = (tile / p.m_tiles) * 128 + 32 * q + lane;
+            const int m0 = (tile % p.m_tiles) * BM;
+            for (int c0 = 0; c0 < BM && m0 + c0 < p.M; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + b * BM + c0, v);
+                tmem_wait_ld();
+                if (n < p.N) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int m = m0 + c0 + i;
+                        if (m < p.M) y[(size_t)m * p.N + n] = cvt_out<T>(__uint_as_float(v[i]));
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[b]);
+        }
+    } else {
+        // ------------------------------------------------------------------
+        // Dequantisation: this warp's 16 rows of each 128-row weight tile.
+        // ------------------------------------------------------------------
+        const int dw = warp - kWarpDq;
+        uint8_t *ring = raw + dw * kRawSlots * R::kSlotBytes;
+        const int64_t row_bytes = (int64_t)p.K * B / 8;
+        const int nss = G / kGroups;  // super-stages per tile
+        // copy plan: kChunks 16-byte pieces of 16 rows per super-stage + s/b
+        constexpr int kChunks = R::kChunksPerRow / 2;
+        uint32_t roff[kChunks], doff[kChunks];
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i) {
+            const int c = lane + 32 * i;
+            const int r = c / R::kChunksPerRow, col = c % R::kChunksPerRow;
+            roff[i] = (uint32_t)r;
+            doff[i] = (uint32_t)(r * R::kRowPitch + col * 16);
+            roff[i] |= (uint32_t)col << 8;
+        }
+        const int nlast = p.N - 1;
+        auto issue = [&](int tile, int ss, int slot) {
+            const int n0 = (tile / p.m_tiles) * 128 + 16 * dw;
+            uint8_t *dst = ring + slot * R::kSlotBytes;
+            const int64_t kb = (int64_t)ss * kGroups * R::kGroupBytes;
+#pragma unroll
+            for (int i = 0; i < kChunks; ++i) {
+                const int r = roff[i] & 0xFF, col = roff[i] >> 8;
+                const int64_t n = min(n0 + r, nlast);
+                cp_async16(dst + doff[i],
+                           reinterpret_cast<const uint8_t *>(p.Wq) + n * row_bytes + kb + col * 16, 16u);
+            }
+            const int sr = lane & 15;
+            const int64_t n = min(n0 + sr, nlast);
+            const __half *base = (lane < 16) ? p.scales : p.biases;
+            cp_async16(dst + R::kSbOff + (lane >> 4) * 256 + sr * 16, base + n * p.G + ss * kGroups, 16u);
+        };
+        // flat sequence of (tile, super-stage) for this CTA
+        int tile = blockIdx.x, ss = 0;
+        int ntile = tile, nss_next = 0;  // next to issue
+        auto advance = [&](int &t, int &s) {
+            if (++s == nss) {
+                s = 0;
+                t += gridDim.x;
+            }
+        };
+        uint32_t it = 0;  // A-stage counter (matches the MMA's)
+        int iss = 0;      // super-stages issued
+        if (ntile < total) {
+            issue(ntile, nss_next, 0);
+            ++iss;
+            advance(ntile, nss_next);
+        }
+        cp_async_commit();
+        const int rl = lane >> 1, h = lane & 1;
+        const int arow = 16 * dw + rl;  // row within the 128-row A tile
+        bool ok = true;
+        for (int cnt = 0; tile < total && ok; ++cnt) {
+            if (ntile < total) {
+                issue(ntile, nss_next, iss % kRawSlots);
+                ++iss;
+                advance(ntile, nss_next);
+            }
+            cp_async_commit();
+            cp_async_wait<1>();
+            __syncwarp();
+            const uint8_t *slotp = ring + (cnt % kRawSlots) * R::kSlotBytes;
+            const uint4 sv = *reinterpret_cast<const uint4 *>(slotp + R::kSbOff + rl * 16);
+            const uint4 bv = *reinterpret_cast<const uint4 *>(slotp + R::kSbOff + 256 + rl * 16);
+            const uint8_t *rowp = slotp + rl * R::kRowPitch;
+#pragma unroll 1
+            for (int j = 0; j < kGroups; ++j, ++it) {
+                const int slot = it % kStages;
+                const uint32_t ph = (it / kStages) & 1u;
+                if (it >= kStages && !tc_wait(&ab_empty[slot], ph ^ 1u, flag, 0x0602)) {
+                    ok = false;
+                    break;
+                }
+                const float s = h_at(sv, j), bsc = h_at(bv, j);
+                const float bb = fmaf(-128.f, s, bsc);
+                const uint32_t s2 = h2_at(sv, j), b2 = h2_at(bv, j);
+                uint32_t u[4];  // 8 codes per entry, this lane's chunks 4h..4h+3
+                if constexpr (B == 4) {
+                    const uint4 w = *reinterpret_cast<const uint4 *>(rowp + j * 32 + h * 16);
+                    u[0] = w.x;
+                    u[1] = w.y;
+                    u[2] = w.z;
+                    u[3] = w.w;
+                } else {
+                    const uint32_t *wp = reinterpret_cast<const uint32_t *>(rowp + j * 24 + h * 12);
+                    const uint32_t w0 = wp[0], w1 = wp[1], w2 = wp[2];
+                    u[0] = w0;
+                    u[1] = __funnelshift_r(w0, w1, 24);
+                    u[2] = __funnelshift_r(w1, w2, 16);
+                    u[3] = w2 >> 8;
+                }
+                uint8_t *arow_p = a_ring + slot * kATileBytes + arow * 128;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int chunk = 4 * h + c;  // k = 8*chunk .. 8*chunk+7
+                    const uint4 v = dequant8<B, BF16>(u[c], s, bb, s2, b2);
+                    *reinterpret_cast<uint4 *>(arow_p + ((chunk ^ (arow & 7)) << 4)) = v;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&a_full[slot]);
+            }
+            __syncwarp();
+            advance(tile, ss);
+        }
+        cp_async_wait<0>();
+    }
+
+    __syncthreads();
+    if (*flag) {
+        // A wait gave up: let copies and MMAs already issued finish before
+        // the tensor memory and shared memory are released.
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 1000000ull) {
+        }
+    }
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, p.tmem_cols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+constexpr size_t kSmemLimitTc = 227 * 1024;
+
+struct TcPlan {
+    int BM;
+    TcParams prm;
+    size_t smem;
+    int grid;
+};
+
+bool tc_plan(const MatmulArgs &a, TcPlan &pl) {
+    if (a.K % 512 != 0 || a.M < 1 || a.N < 1) return false;
+    if (a.M > INT32_MAX / 2 || a.N > INT32_MAX / 2 || a.K > INT32_MAX / 2) return false;
+    pl.BM = a.M <= 64 ? 64 : a.M <= 128 ? 128 : 256;
+    TcParams &q = pl.prm;
+    q.M = (int)a.M;
+    q.N = (int)a.N;
+    q.K = (int)a.K;
+    q.G = (int)(a.K / 64);
+    q.n_tiles = (int)((a.N + 127) / 128);
+    q.m_tiles = (int)((a.M + pl.BM - 1) / pl.BM);
+    if ((int64_t)q.n_tiles * q.m_tiles > INT32_MAX) return false;
+    const int raw_slot = a.bits == 4 ? Raw<4>::kSlotBytes : Raw<3>::kSlotBytes;
+    size_t off = (size_t)kStages * kATileBytes;
+    q.off_b = (uint32_t)off;
+    off += (size_t)kStages * pl.BM * 128;
+    q.off_raw = (uint32_t)off;
+    off += (size_t)kDqWarps * kRawSlots * raw_slot;
+    off = (off + 15) / 16 * 16;
+    q.off_bar = (uint32_t)off;
+    off += (3 * kStages + 4) * 8 + 16;
+    pl.smem = off + 1024;  // room to align the base to 1024 bytes
+    if (pl.smem > kSmemLimitTc) return false;
+    q.tmem_cols = pl.BM == 256 ? 512 : pl.BM == 128 ? 256 : 128;
+    q.Wq = a.Wq;
+    q.scales = static_cast<const __half *>(a.scales);
+    q.biases = static_cast<const __half *>(a.biases);
+    q.y = a.out;
+    const int total = q.n_tiles * q.m_tiles;
+    pl.grid = std::min(total, num_sms());
+    return true;
+}
+
+template <int B, bool BF16, int BM>
+cudaError_t tc_launch_t(const TcPlan &pl, const CUtensorMap &tm, cudaStream_t stream) {
+    auto kern = tc_kernel<B, BF16, BM>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)kSmemLimitTc);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    kern<<<pl.grid, kThreadsTc, pl.smem, stream>>>(pl.prm, tm);
+    return cudaGetLastError();
+}
+
+template <int B, bool BF16>
+cudaError_t tc_launch_bm(const TcPlan &pl, const CUtensorMap &tm, cudaStream_t s) {
+    switch (pl.BM) {
+        case 64: return tc_launch_t<B, BF16, 64>(pl, tm, s);
+        case 128: return tc_launch_t<B, BF16, 128>(pl, tm, s);
+        default: return tc_launch_t<B, BF16, 256>(pl, tm, s);
+    }
+}
+
+}  // namespace
+
+bool tc_supported(const MatmulArgs &a) {
+    if (!aligned(a.x, 16) || !aligned(a.Wq, 16) || !aligned(a.scales, 16) ||
+        !aligned(a.biases, 16))
+        return false;
+    TcPlan pl;
+    return tc_plan(a, pl);
+}
+
+cudaError_t tc_launch(const MatmulArgs &a) {
+    TcPlan pl;
+    if (!tc_plan(a, pl)) return cudaErrorInvalidValue;
+    auto enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    CUtensorMap tm;
+    const cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
+    const cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)pl.BM};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(&tm, a.dtype == AQ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                           2, const_cast<void *>(a.x), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (a.bits == 3)
+        return a.dtype == AQ_BF16 ? tc_launch_bm<3, true>(pl, tm, a.stream)
+                                  : tc_launch_bm<3, false>(pl, tm, a.stream);
+    return a.dtype == AQ_BF16 ? tc_launch_bm<4, true>(pl, tm, a.stream)
+                              : tc_launch_bm<4, false>(pl, tm, a.stream);
+}
+
+int tc_describe(const MatmulArgs &a, char *buf, int len) {
+    TcPlan pl;
+    if (!tc_plan(a, pl)) return snprintf(buf, len, "tc: unsupported");
+    return snprintf(buf, len, "tc bm=%d tiles=%dx%d grid=%d smem=%zu tmem=%u", pl.BM,
+                    pl.prm.n_tiles, pl.prm.m_tiles, pl.grid, pl.smem, pl.prm.tmem_cols);
+}
+
+cudaError_t tc_read_error(uint32_t *code, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(code, g_tc_error, sizeof(uint32_t));
+    if (e != cudaSuccess || !clear) return e;
+    const uint32_t zero = 0;
+    return cudaMemcpyToSymbol(g_tc_error, &zero, sizeof(uint32_t));
 }
 
 }  // namespace aq

@@ -104,6 +104,9 @@ def test_stats_interface():
     (16, 10240, 5120, 3, aq.AQ_VARIANT_QMV),
     (1, 5120, 13824, 4, aq.AQ_VARIANT_QMV),
     (1, 13824, 5120, 4, aq.AQ_VARIANT_QMV),
+    (64, 10240, 5120, 3, aq.AQ_VARIANT_TC),
+    (128, 28672, 8192, 4, aq.AQ_VARIANT_TC),
+    (512, 28672, 8192, 4, aq.AQ_VARIANT_TC),
     (1, 100, 576, 4, aq.AQ_VARIANT_GENERIC),   # K % 512 != 0 -> generic
     (3, 7, 64, 3, aq.AQ_VARIANT_GENERIC),
 ])

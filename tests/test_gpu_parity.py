@@ -64,7 +64,7 @@ def test_pack_bit_exact(bits, N, K):
 # --------------------------------------------------------------------------
 
 SHAPES = [
-    # (M, N, K)
+    # (M, N, K): one or several tiles of each kernel, with ragged N and M
     (1, 1024, 512),
     (1, 100, 512),
     (1, 37, 2048),
@@ -78,11 +78,13 @@ SHAPES = [
     (33, 40, 512),
     (64, 80, 1024),
     (100, 48, 512),
+    (130, 300, 1024),
+    (257, 200, 1536),
 ]
 
 
-@pytest.mark.parametrize("variant", [GENERIC, QMV, aq.AQ_VARIANT_AUTO],
-                         ids=["generic", "qmv", "auto"])
+@pytest.mark.parametrize("variant", [GENERIC, QMV, TC, aq.AQ_VARIANT_AUTO],
+                         ids=["generic", "qmv", "tc", "auto"])
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 @pytest.mark.parametrize("bits", [3, 4])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
@@ -113,7 +115,7 @@ def test_generic_ragged_k(shape, bits, dtype):
 # Closed forms (exact in fp32 up to the output rounding)
 # --------------------------------------------------------------------------
 
-@pytest.mark.parametrize("variant", [GENERIC, QMV], ids=["generic", "qmv"])
+@pytest.mark.parametrize("variant", [GENERIC, QMV, TC], ids=["generic", "qmv", "tc"])
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 @pytest.mark.parametrize("bits", [3, 4])
 def test_unit_rows_read_back_every_weight(bits, dtype, variant):
@@ -131,7 +133,7 @@ def test_unit_rows_read_back_every_weight(bits, dtype, variant):
     assert np.all(np.abs(y - w) <= ulp(w, dtype)), np.abs(y - w).max()
 
 
-@pytest.mark.parametrize("variant", [GENERIC, QMV], ids=["generic", "qmv"])
+@pytest.mark.parametrize("variant", [GENERIC, QMV, TC], ids=["generic", "qmv", "tc"])
 @pytest.mark.parametrize("bits", [3, 4])
 def test_zero_codes_and_zero_scales(bits, variant):
     p = workloads.make_problem("t", bits, 64, 1024, 4, "fp16", seed=11)
@@ -146,7 +148,7 @@ def test_zero_codes_and_zero_scales(bits, variant):
     assert_within_tolerance(run(ps, variant), expected, bound, "zero scales")
 
 
-@pytest.mark.parametrize("variant", [GENERIC, QMV], ids=["generic", "qmv"])
+@pytest.mark.parametrize("variant", [GENERIC, QMV, TC], ids=["generic", "qmv", "tc"])
 def test_ones_row(variant):
     bits, K, N = 4, 1024, 40
     p = workloads.make_problem("t", bits, N, K, 1, "bf16", seed=12)
@@ -160,7 +162,7 @@ def test_ones_row(variant):
 # Invariants and edge behaviour
 # --------------------------------------------------------------------------
 
-@pytest.mark.parametrize("variant", [GENERIC, QMV], ids=["generic", "qmv"])
+@pytest.mark.parametrize("variant", [GENERIC, QMV, TC], ids=["generic", "qmv", "tc"])
 def test_deterministic(variant):
     p = workloads.make_problem("t", 3, 1000, 2048, 5, "bf16", seed=13)
     codes, s, b, x = dev_tensors(p)
@@ -182,7 +184,7 @@ def test_rows_match_single_row_calls():
         assert np.all(np.abs(ym[0] - y[m]) <= 2 * oracle.tolerance(bound[m]))
 
 
-@pytest.mark.parametrize("variant", [GENERIC, QMV], ids=["generic", "qmv"])
+@pytest.mark.parametrize("variant", [GENERIC, QMV, TC], ids=["generic", "qmv", "tc"])
 def test_no_writes_outside_output(variant):
     M, N, K, bits = 3, 45, 1024, 4
     p = workloads.make_problem("t", bits, N, K, M, "fp16", seed=15)
