@@ -43,6 +43,25 @@ DEFAULT_WORKLOAD = "decode"
 GRAPH_CHUNK = 1024
 
 
+def reduce_max(value: float, device: str = "cpu") -> float:
+    """Maximum of `value` over all ranks (identity without a process group).
+    Replicas share nothing but this: the job's time is its slowest rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_us_per_call(us_per_call_slowest_rank: float, world: int) -> float:
+    """Time per call for the whole job: every rank ran the same number of
+    calls concurrently, so the job completes world x calls in the slowest
+    rank's time."""
+    return us_per_call_slowest_rank / max(1, world)
+
+
 def parse_workload(spec: str):
     name, _, idx = spec.partition(":")
     return name, int(idx or 0)
@@ -232,14 +251,9 @@ def run_ours(args, rank, world, local_rank):
     clocks = sampler.stop()
     ms = ev0.elapsed_time(ev1)
 
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-
-    us_call = ms * 1e3 / args.steps  # per call on one GPU
-    value = us_call / world          # whole job: time per call across all replicas
+    ms = reduce_max(ms, "cuda")
+    us_call = ms * 1e3 / args.steps  # per call on one GPU (slowest rank)
+    value = whole_job_us_per_call(us_call, world)
 
     # hot-L2 context: the same call on one weight copy, back to back
     us_hot, e2e_us = None, None
@@ -275,12 +289,7 @@ def run_ours(args, rank, world, local_rank):
     for i in range(e2e_steps):
         aq.aq_matmul_host(x_host, *ws[i % copies], p.bits, y_host, x_dev, y_dev, stream=stream)
     torch.cuda.synchronize()
-    e2e_us = (time.perf_counter() - t0) * 1e6 / e2e_steps
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_us], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_us = float(t.item())
+    e2e_us = reduce_max((time.perf_counter() - t0) * 1e6 / e2e_steps, "cuda")
     return finish(args, p, name, idx, world, aq, variant, copies, wbytes, l2, chunk, us_call,
                   value, us_hot, e2e_us, clocks, bytes_call, flops_call)
 
@@ -335,7 +344,8 @@ def finish(args, p, name, idx, world, aq, variant, copies, wbytes, l2, chunk, us
                      else "fallback",
                      "algorithmic_bytes_per_launch": bytes_call,
                      "flops_per_launch": flops_call},
-        "e2e": {"value": round(e2e_us / world, 3) if e2e_us is not None else None,
+        "e2e": {"value": round(whole_job_us_per_call(e2e_us, world), 3)
+                if e2e_us is not None else None,
                 "unit": "us/call",
                 "h2d_bytes_per_step": p.M * p.K * 2, "d2h_bytes_per_step": p.M * p.N * 2,
                 "path": "aq_matmul_host (pinned x -> device, matmul, device -> pinned y, sync)"},
