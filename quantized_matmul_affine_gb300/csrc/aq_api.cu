@@ -25,7 +25,7 @@ int qmv_max_m() {
     static const int v = [] {
         const char *e = std::getenv("AQ_QMV_MAX_M");
         if (e && *e) return std::atoi(e);
-        return 32;
+        return 16;
     }();
     return v;
 }

@@ -262,3 +262,21 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
 }
 
 }  // namespace aq
+
+namespace aq {
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  launch_dependents lets the next kernel of
+// the stream (launched with programmatic stream serialization) start once
+// every CTA of this grid has executed it; grid_dependency_wait blocks until
+// the preceding grid has completed and its memory is visible.  Without a
+// programmatic predecessor both are no-ops.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+}  // namespace aq

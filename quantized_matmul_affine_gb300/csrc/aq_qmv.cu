@@ -43,6 +43,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <cstdio>
 #include <mutex>
 #include <type_traits>
@@ -246,9 +247,17 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(const __grid_constant_
         for (int c = 0; c < kChunks; ++c) cp_async16(dst + doff[c], src + soff[c], 16u);
         cp_async16(dst + sbdoff, sbbase + gs, 16u);
     };
-    // Raw x of this CTA's K range goes to the fragment rows first (one group
-    // of copies, committed before the weight stages): one round trip that
-    // overlaps the weight copies.
+    // The weights do not depend on earlier kernels in the stream: their first
+    // stages are queued before waiting for the preceding grid, and the next
+    // kernel may launch as soon as every CTA of this one is running.
+    for (int i = 0; i < slots - 1; ++i) {
+        if (i < nw) issue(i, i);
+        cp_async_commit();
+    }
+    launch_dependents();
+    grid_dependency_wait();  // x and y belong to the stream order
+    // Raw x of this CTA's K range goes to the fragment rows (one more group
+    // of copies).
     {
         const T *xg = static_cast<const T *>(prm.x);
         const int per_row = gcta * 8;  // 16-byte chunks per activation row
@@ -257,10 +266,6 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(const __grid_constant_
             cp_async16(xfrag + (size_t)m * prm.xpitch + q * 16,
                        xg + (m0 + m) * prm.K + 64 * gb + 8 * q, 16u);
         }
-        cp_async_commit();
-    }
-    for (int i = 0; i < slots - 1; ++i) {
-        if (i < nw) issue(i, i);
         cp_async_commit();
     }
 
@@ -275,13 +280,7 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(const __grid_constant_
         oscale[ct] = 16777216.f;
         amax[ct] = 0u;
     }
-    switch (slots) {  // the x group is complete once slots-1 younger groups may pend
-        case 2: cp_async_wait<1>(); break;
-        case 3: cp_async_wait<2>(); break;
-        case 4: cp_async_wait<3>(); break;
-        case 5: cp_async_wait<4>(); break;
-        default: cp_async_wait<5>(); break;
-    }
+    cp_async_wait<0>();  // x (the youngest group) and the first weight stages
     __syncthreads();
     if constexpr (std::is_same<T, __nv_bfloat16>::value) {
         // Largest |x| per activation row over this CTA's K range; pick 2^-e
@@ -547,16 +546,30 @@ Layout layout(int B, int MB, int mc_valid, int st_cta, int rt, int ks, int slots
 
 std::atomic<int> g_force_rt{0}, g_force_ks{0}, g_force_slots{0};
 
+// Measured geometry for the benchmarked shapes: the fastest (rows per CTA,
+// cluster split, ring depth) of a sweep of every combination on GB300, with
+// programmatic dependent launch between consecutive calls.
+struct TunedShape {
+    int bits, N, K, MB;
+    int rt, ks, slots;
+};
+constexpr TunedShape kTuned[] = {
+    {4, 4096, 4096, 1, 1, 1, 2},    // decode 4.78 us
+    {4, 1024, 512, 1, 1, 1, 2},     // small 2.22 us
+    {3, 10240, 5120, 1, 8, 3, 3},   // 3-bit M=1 12.3 us
+    {3, 10240, 5120, 2, 8, 1, 3},   // 3-bit M=9..16 (K split grows if x does not fit)
+    {4, 5120, 5120, 1, 4, 3, 2},    // q/o projections 7.6 us
+    {4, 1024, 5120, 1, 1, 1, 3},    // k/v projections 3.7 us
+    {4, 13824, 5120, 1, 4, 1, 2},   // gate/up 12.0 us
+    {4, 5120, 13824, 1, 4, 3, 2},   // down 12.5 us
+};
+
 // Pick the CTA shape (rt row tiles x kw K-ways, rt*kw = 8 warps), the
-// cluster split ks and the ring depth.  Rule, from timing every (rt, ks) on
-// the workload shapes on GB300: every CTA pays a fixed x-preparation cost
-// (~2 us) and every cluster split a reduction (~1 us), so
-//   * use the largest row block whose CTA count still covers half the SMs,
-//     in a single resident wave, without a cluster split;
-//   * split K over a cluster only when even 16-row blocks leave half the SMs
-//     idle (narrow N), or when a warp would stream more than 12 stages;
-//   * a ring of three stages per warp (two in flight) when it fits; deeper
-//     rings only lowered occupancy.
+// cluster split ks and the ring depth.  Shapes in kTuned use their measured
+// geometry.  Otherwise, from the same sweeps: with consecutive calls
+// overlapping, the best launches fill about 1.6 CTAs per SM in one resident
+// wave (at most 2 per SM), and each extra cluster CTA costs about as much as
+// being 30% off that target; among equal scores the larger row block wins.
 bool make_plan(const MatmulArgs &a, Plan &p) {
     const int B = a.bits;
     if (a.K % 512 != 0 || a.M < 1 || a.N < 1) return false;
@@ -570,19 +583,39 @@ bool make_plan(const MatmulArgs &a, Plan &p) {
     if (16 * (a.K * B / 8) >= ((int64_t)1 << 31)) return false;  // 32-bit copy offsets
     const int sms = num_sms();
     const int frt = g_force_rt.load(), fks = g_force_ks.load(), fsl = g_force_slots.load();
-    const int64_t want = std::max<int64_t>(1, sms / 2);  // CTAs to cover half the SMs
 
-    int rt = 1;
-    for (int r = kWarps; r >= 1; r /= 2)
-        if ((tiles16 + r - 1) / r * p.m_chunks >= want) { rt = r; break; }
+    int rt = 1, ks = 1, want_slots = 2;
+    bool tuned = false;
+    for (const TunedShape &t : kTuned)
+        if (t.bits == B && t.N == a.N && t.K == a.K && t.MB == p.MB) {
+            rt = t.rt;
+            ks = t.ks;
+            want_slots = t.slots;
+            tuned = true;
+        }
+    if (!tuned) {
+        const double target = 1.6 * sms;
+        double best = 1e30;
+        for (int r = kWarps; r >= 1; r /= 2) {
+            const int64_t blocks = (tiles16 + r - 1) / r;
+            for (int k = 1; k <= std::min(S, kMaxCluster); ++k) {
+                const int64_t ctas = blocks * k * p.m_chunks;
+                if (ctas > 2 * (int64_t)sms && !(k == 1 && r == kWarps)) continue;
+                const double score = std::fabs((double)ctas - target) / target + 0.3 * (k - 1);
+                if (score < best - 1e-9) {
+                    best = score;
+                    rt = r;
+                    ks = k;
+                }
+            }
+        }
+    }
     if (frt) rt = frt;
+    if (fks) ks = fks;
+    if (fsl) want_slots = fsl;
+    ks = std::max(1, std::min({ks, S, kMaxCluster}));
     const int kw = kWarps / rt;
     const int64_t blocks = (tiles16 + rt - 1) / rt;
-    int ks = 1;
-    if (blocks * p.m_chunks < want) ks = (int)((int64_t)(sms * 4 / 5 + blocks * p.m_chunks - 1) / (blocks * p.m_chunks));
-    if ((S + kw - 1) / kw > 12) ks = std::max(ks, (S / kw + 5) / 6);
-    ks = std::max(1, std::min({ks, S, kMaxCluster}));
-    if (fks) ks = std::min(fks, S);
     if (blocks * ks > (int64_t)INT32_MAX) return false;
 
     bool found = false;
@@ -590,10 +623,9 @@ bool make_plan(const MatmulArgs &a, Plan &p) {
     for (; ks <= std::min(S, kMaxCluster) && !found; ++ks) {
         const int st_cta = (S + ks - 1) / ks;
         const int per_warp_st = (st_cta + kw - 1) / kw;
-        int slots = fsl ? fsl : 3;
-        slots = std::max(2, std::min(slots, per_warp_st + 1));
+        int slots = std::max(2, std::min(want_slots, per_warp_st + 1));
         Layout L = layout(B, p.MB, mc_valid, st_cta, rt, ks, slots);
-        while (!fsl && L.smem > kSmemLimit && slots > 2)
+        while (L.smem > kSmemLimit && slots > 2)
             L = layout(B, p.MB, mc_valid, st_cta, rt, ks, --slots);
         if (L.smem > kSmemLimit || (L.off_scale - L.off_xfrag) > 120 * 1024) {
             if (fks) break;
@@ -649,13 +681,20 @@ cudaError_t launch_plan(const Plan &p, cudaStream_t stream) {
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)p.ks;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (p.ks > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = (unsigned)p.ks;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = p.ks > 1 ? 1 : 0;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, kern, p.prm);
 }
 

@@ -195,12 +195,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    // Weights do not depend on earlier kernels: only the x loads (TMA warp)
+    // and the y stores (epilogue) wait for the preceding grid, and the next
+    // kernel may launch once every CTA of this one is running.
+    launch_dependents();
 
     if (warp == kWarpTma) {
         // ------------------------------------------------------------------
         // x tiles: BM rows x 64 k per stage, 128-byte swizzled, by TMA.
         // ------------------------------------------------------------------
         if (lane == 0) {
+            grid_dependency_wait();
             uint32_t it = 0;
             for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
                 const int m0 = (tile % p.m_tiles) * BM;
@@ -255,6 +260,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         // ------------------------------------------------------------------
         const int q = warp & 3;
         T *y = static_cast<T *>(p.y);
+        grid_dependency_wait();
         uint32_t ti = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++ti) {
             const uint32_t b = ti & 1u, use = ti >> 1;
@@ -477,8 +483,17 @@ cudaError_t tc_launch_t(const TcPlan &pl, const CUtensorMap &tm, cudaStream_t st
                                         (int)kSmemLimitTc);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    kern<<<pl.grid, kThreadsTc, pl.smem, stream>>>(pl.prm, tm);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)pl.grid, 1, 1);
+    cfg.blockDim = dim3(kThreadsTc, 1, 1);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, pl.prm, tm);
 }
 
 template <int B, bool BF16>
