@@ -280,3 +280,13 @@ __device__ __forceinline__ void grid_dependency_wait() {
 }
 
 }  // namespace aq
+
+namespace aq {
+
+// 8-byte cp.async (L1-allocating form; the 16-byte form bypasses L1).
+__device__ __forceinline__ void cp_async8(void *dst_smem, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst_smem)), "l"(src)
+                 : "memory");
+}
+
+}  // namespace aq

@@ -42,19 +42,22 @@ namespace {
 
 constexpr int kThreadsTc = 14 * 32;
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpDq = 6, kDqWarps = 8;  // warps 2-5: epilogue
-constexpr int kStages = 3;    // A/B stages (one 64-wide group each)
 constexpr int kRawSlots = 2;  // raw super-stages per dequant warp
-constexpr int kGroups = 8;    // groups per raw super-stage (512 k)
+constexpr int kGroups = 4;    // groups per raw super-stage (256 k)
 constexpr int kATileBytes = 128 * 128;
+
+// A/B pipeline depth by x tile width: as deep as shared memory allows.  The
+// ring has to cover the round trip dequantise -> MMA -> commit -> reuse.
+constexpr int stages_for(int BM) { return BM <= 64 ? 7 : BM <= 128 ? 5 : 3; }
 
 template <int B>
 struct Raw {
     static constexpr int kGroupBytes = 8 * B;
-    static constexpr int kRowBytes = kGroups * kGroupBytes;  // 256 / 192
-    static constexpr int kChunksPerRow = kRowBytes / 16;    // 16 / 12
-    static constexpr int kRowPitch = kRowBytes + (B == 4 ? 32 : 16);
-    static constexpr int kSbOff = 16 * kRowPitch;  // scales[16][8] then biases[16][8]
-    static constexpr int kSlotBytes = kSbOff + 2 * 16 * 16;
+    static constexpr int kRowBytes = kGroups * kGroupBytes;  // 128 / 96
+    static constexpr int kChunksPerRow = kRowBytes / 16;    // 8 / 6
+    static constexpr int kRowPitch = kRowBytes + 32;         // 160 / 128: rows in distinct banks
+    static constexpr int kSbOff = 16 * kRowPitch;  // scales[16][4] then biases[16][4]
+    static constexpr int kSlotBytes = kSbOff + 2 * 16 * 8;
 };
 
 struct TcParams {
@@ -155,6 +158,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tmap_x) {
     using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
     using R = Raw<B>;
+    constexpr int kStages = stages_for(BM);
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -318,7 +322,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             const int sr = lane & 15;
             const int64_t n = min(n0 + sr, nlast);
             const __half *base = (lane < 16) ? p.scales : p.biases;
-            cp_async16(dst + R::kSbOff + (lane >> 4) * 256 + sr * 16, base + n * p.G + ss * kGroups, 16u);
+            cp_async8(dst + R::kSbOff + (lane >> 4) * 128 + sr * 8, base + n * p.G + ss * kGroups);
         };
         // flat sequence of (tile, super-stage) for this CTA
         int tile = blockIdx.x, ss = 0;
@@ -350,8 +354,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             cp_async_wait<1>();
             __syncwarp();
             const uint8_t *slotp = ring + (cnt % kRawSlots) * R::kSlotBytes;
-            const uint4 sv = *reinterpret_cast<const uint4 *>(slotp + R::kSbOff + rl * 16);
-            const uint4 bv = *reinterpret_cast<const uint4 *>(slotp + R::kSbOff + 256 + rl * 16);
+            const uint2 sv2 = *reinterpret_cast<const uint2 *>(slotp + R::kSbOff + rl * 8);
+            const uint2 bv2 = *reinterpret_cast<const uint2 *>(slotp + R::kSbOff + 128 + rl * 8);
+            const uint4 sv = make_uint4(sv2.x, sv2.y, 0u, 0u);
+            const uint4 bv = make_uint4(bv2.x, bv2.y, 0u, 0u);
             const uint8_t *rowp = slotp + rl * R::kRowPitch;
 #pragma unroll 1
             for (int j = 0; j < kGroups; ++j, ++it) {
@@ -366,7 +372,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 const uint32_t s2 = h2_at(sv, j), b2 = h2_at(bv, j);
                 uint32_t u[4];  // 8 codes per entry, this lane's chunks 4h..4h+3
                 if constexpr (B == 4) {
-                    const uint4 w = *reinterpret_cast<const uint4 *>(rowp + j * 32 + h * 16);
+                    const uint4 w = *reinterpret_cast<const uint4 *>(rowp + j * 32 + h * 16);  // 4 words
                     u[0] = w.x;
                     u[1] = w.y;
                     u[2] = w.z;
@@ -453,6 +459,7 @@ bool tc_plan(const MatmulArgs &a, TcPlan &pl) {
     q.m_tiles = (int)((a.M + pl.BM - 1) / pl.BM);
     if ((int64_t)q.n_tiles * q.m_tiles > INT32_MAX) return false;
     const int raw_slot = a.bits == 4 ? Raw<4>::kSlotBytes : Raw<3>::kSlotBytes;
+    const int kStages = stages_for(pl.BM);
     size_t off = (size_t)kStages * kATileBytes;
     q.off_b = (uint32_t)off;
     off += (size_t)kStages * pl.BM * 128;
@@ -541,8 +548,9 @@ cudaError_t tc_launch(const MatmulArgs &a) {
 int tc_describe(const MatmulArgs &a, char *buf, int len) {
     TcPlan pl;
     if (!tc_plan(a, pl)) return snprintf(buf, len, "tc: unsupported");
-    return snprintf(buf, len, "tc bm=%d tiles=%dx%d grid=%d smem=%zu tmem=%u", pl.BM,
-                    pl.prm.n_tiles, pl.prm.m_tiles, pl.grid, pl.smem, pl.prm.tmem_cols);
+    return snprintf(buf, len, "tc bm=%d stages=%d tiles=%dx%d grid=%d smem=%zu tmem=%u", pl.BM,
+                    stages_for(pl.BM), pl.prm.n_tiles, pl.prm.m_tiles, pl.grid, pl.smem,
+                    pl.prm.tmem_cols);
 }
 
 cudaError_t tc_read_error(uint32_t *code, bool clear) {
