@@ -31,6 +31,12 @@
  *     streams; results do not depend on the thread or stream.
  *   - Results are deterministic: the same inputs give bit-identical outputs,
  *     call after call (fixed-order reductions, no atomics on data).
+ *   - Consecutive matmul calls on one stream overlap (programmatic dependent
+ *     launch): a call may start reading its Wq, scales and biases while the
+ *     previous matmul call on the stream is still running, and reads x and
+ *     writes out only after that call has finished.  So out_dev of a matmul
+ *     call must not alias Wq_dev, scales_dev or biases_dev of the next
+ *     matmul call on the same stream; everything else follows stream order.
  */
 #ifndef AQ_H
 #define AQ_H
@@ -60,7 +66,8 @@ typedef enum aq_variant {
     AQ_VARIANT_GENERIC = 0, /* plain-load CUDA-core kernel: any K % 64 == 0, any alignment */
     AQ_VARIANT_QMV = 1,     /* small-M: bulk-async staged weights, warp MMA, factored dequant */
     AQ_VARIANT_TC = 2,      /* large-M: tcgen05 MMA with TMEM accumulators */
-    AQ_NUM_VARIANTS = 3
+    AQ_VARIANT_GEMV = 3,    /* M <= 8: one resident CTA per SM, TMA weight ring, warp MMA */
+    AQ_NUM_VARIANTS = 4
 } aq_variant;
 
 /*
@@ -172,7 +179,7 @@ void aq_free(void);
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *aq_status_string(aq_status status);
 
-/* Human-readable name of a variant ("generic", "qmv", "tc"); "?" if unknown. */
+/* Human-readable name of a variant ("generic", "qmv", "tc", "gemv"); "?" if unknown. */
 const char *aq_variant_name(int variant);
 
 /* Library version string. */

@@ -6,8 +6,11 @@
 // explicit-variant and host-memory entry points described in aq.h.
 #include "aq_internal.h"
 
+#include <cudaTypedefs.h>
+
 #include <atomic>
 #include <cstdio>
+#include <mutex>
 #include <cstdlib>
 #include <cstring>
 
@@ -48,9 +51,50 @@ int num_sms() {
     return v;
 }
 
+bool tmap_encode(CUtensorMap *tm, CUtensorMapDataType type, int rank, const void *base,
+                 const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
+                 CUtensorMapSwizzle swizzle) {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        else
+            cudaGetLastError();
+    });
+    if (!fn || rank < 1 || rank > 5) return false;
+    cuuint64_t d[5], st[4];
+    cuuint32_t bx[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = (cuuint64_t)dims[i];
+        bx[i] = (cuuint32_t)box[i];
+        es[i] = 1;
+        if (i + 1 < rank) st[i] = (cuuint64_t)strides_bytes[i];
+    }
+    return fn(tm, type, (cuuint32_t)rank, const_cast<void *>(base), d, st, bx, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Largest M that the resident small-M kernel takes under the automatic rule
+// (AQ_GEMV_MAX_M overrides it for experiments).
+static int gemv_max_m() {
+    static const int v = [] {
+        const char *e = std::getenv("AQ_GEMV_MAX_M");
+        if (e && *e) return std::atoi(e);
+        return 8;
+    }();
+    return v;
+}
+
 // The dispatch rule.  Returns the variant for the arguments (alignment
 // included), never AQ_VARIANT_AUTO.
 static int choose(const MatmulArgs &a) {
+    if (a.M <= gemv_max_m() && gemv_supported(a)) return AQ_VARIANT_GEMV;
     const bool qmv = qmv_supported(a);
     const bool tc = tc_supported(a);
     if (qmv && (a.M <= qmv_max_m() || !tc)) return AQ_VARIANT_QMV;
@@ -88,6 +132,10 @@ static aq_status run(int variant, const MatmulArgs &a) {
         case AQ_VARIANT_TC:
             if (!tc_supported(a)) return AQ_ERR_UNSUPPORTED;
             err = tc_launch(a);
+            break;
+        case AQ_VARIANT_GEMV:
+            if (!gemv_supported(a)) return AQ_ERR_UNSUPPORTED;
+            err = gemv_launch(a);
             break;
         default:
             return AQ_ERR_INVALID_ARG;
@@ -193,6 +241,7 @@ int aq_describe(int64_t M, int64_t N, int64_t K, int bits, int dtype, char *buf,
                              (const void *)fake, M, N, K, bits, (void *)fake, nullptr);
     if (check_args(a) != AQ_OK) return snprintf(buf, buflen, "invalid arguments");
     switch (choose(a)) {
+        case AQ_VARIANT_GEMV: return gemv_describe(a, buf, buflen);
         case AQ_VARIANT_QMV: return qmv_describe(a, buf, buflen);
         case AQ_VARIANT_TC: return tc_describe(a, buf, buflen);
         default: return snprintf(buf, buflen, "generic");
@@ -211,10 +260,11 @@ aq_status aq_stats(uint64_t *calls, int n, int reset) {
 aq_status aq_device_error(uint32_t *code, int clear) {
     if (!code) return AQ_ERR_INVALID_ARG;
     if (cudaDeviceSynchronize() != cudaSuccess) return AQ_ERR_CUDA;
-    uint32_t a = 0, b = 0;
+    uint32_t a = 0, b = 0, c = 0;
     if (qmv_read_error(&a, clear != 0) != cudaSuccess) return AQ_ERR_CUDA;
     if (tc_read_error(&b, clear != 0) != cudaSuccess) return AQ_ERR_CUDA;
-    *code = a | b;
+    if (gemv_read_error(&c, clear != 0) != cudaSuccess) return AQ_ERR_CUDA;
+    *code = a | b | c;
     return AQ_OK;
 }
 
@@ -240,6 +290,7 @@ const char *aq_variant_name(int variant) {
         case AQ_VARIANT_GENERIC: return "generic";
         case AQ_VARIANT_QMV: return "qmv";
         case AQ_VARIANT_TC: return "tc";
+        case AQ_VARIANT_GEMV: return "gemv";
     }
     return "?";
 }

@@ -1,6 +1,7 @@
 // Host-side declarations shared by the translation units of libaq.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -26,12 +27,19 @@ enum : uint32_t {
     ERR_QMV_FULL = 0x0101,
     ERR_QMV_EMPTY = 0x0201,
     ERR_TC_BASE = 0x0002,
+    ERR_GEMV_FULL = 0x0103,
+    ERR_GEMV_EMPTY = 0x0203,
+    ERR_GEMV_DRAIN = 0x0303,
 };
 
 // Each returns cudaSuccess, or the launch error.  `supported` reports
 // whether the variant can run the shape/alignment at all.
 bool generic_supported(const MatmulArgs &a);
 cudaError_t generic_launch(const MatmulArgs &a);
+
+bool gemv_supported(const MatmulArgs &a);
+cudaError_t gemv_launch(const MatmulArgs &a);
+int gemv_describe(const MatmulArgs &a, char *buf, int len);
 
 bool qmv_supported(const MatmulArgs &a);
 cudaError_t qmv_launch(const MatmulArgs &a);
@@ -47,8 +55,25 @@ cudaError_t pack_launch(const uint8_t *codes, int64_t N, int64_t K, int bits, ui
                         cudaStream_t stream);
 
 // Device error words, one per translation unit that owns bounded waits.
+cudaError_t gemv_read_error(uint32_t *code, bool clear);
 cudaError_t qmv_read_error(uint32_t *code, bool clear);
 cudaError_t tc_read_error(uint32_t *code, bool clear);
+
+// A tiled TMA tensor map of `rank` dimensions (dims[0] innermost, strides
+// in bytes of dims 1..rank-1), box `box`, out-of-range elements read as
+// zero.  False if the driver entry point is missing or rejects the layout.
+bool tmap_encode(CUtensorMap *tm, CUtensorMapDataType type, int rank, const void *base,
+                 const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
+                 CUtensorMapSwizzle swizzle);
+// The 2-D case: a row-major [dim1][dim0] array.
+inline bool tmap_2d(CUtensorMap *tm, CUtensorMapDataType type, const void *base, uint64_t dim0,
+                    uint64_t dim1, uint64_t row_stride_bytes, uint32_t box0, uint32_t box1,
+                    CUtensorMapSwizzle swizzle) {
+    const uint64_t dims[2] = {dim0, dim1};
+    const uint64_t strides[1] = {row_stride_bytes};
+    const uint32_t box[2] = {box0, box1};
+    return tmap_encode(tm, type, 2, base, dims, strides, box, swizzle);
+}
 
 // Number of streaming multiprocessors of the current device (cached).
 int num_sms();

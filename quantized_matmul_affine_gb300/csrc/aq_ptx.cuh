@@ -61,6 +61,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the same condition (try_wait may suspend the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Gives up after
 // AQ_WAIT_LIMIT_NS (or 2^31 polls) and returns false; the caller records the
 // error and leaves its loop.
@@ -70,6 +83,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     for (uint32_t it = 1; it < (1u << 31); ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 255u) == 0u && globaltimer_ns() - t0 > AQ_WAIT_LIMIT_NS) return false;
+    }
+    return false;
+}
+
+// Like mbar_wait for a waiter off the critical path: sleeps between polls
+// so that it does not take issue slots from the warps doing the work.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity,
+                                                uint32_t sleep_ns) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1; it < (1u << 31); ++it) {
+        __nanosleep(sleep_ns);
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((it & 63u) == 0u && globaltimer_ns() - t0 > AQ_WAIT_LIMIT_NS) return false;
     }
     return false;
 }
@@ -91,6 +118,15 @@ __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, u
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
         "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst_smem)),
         "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s_plain(void *dst_smem, const void *src_gmem,
+                                               uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst_smem)),
+        "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
 
@@ -184,6 +220,15 @@ __device__ __forceinline__ void tma_load_2d(void *dst_smem, const void *tmap, in
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
         "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst_smem)),
         "l"(tmap), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void *dst_smem, const void *tmap, int c0, int c1,
+                                            int c2, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst_smem)),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
         : "memory");
 }
 

@@ -160,8 +160,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     using R = Raw<B>;
     constexpr int kStages = stages_for(BM);
     extern __shared__ uint8_t smem_dyn[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
-                                                ~static_cast<uintptr_t>(1023));
+    // Align to 1024 bytes by an offset from the __shared__ array itself, so
+    // that every access below stays a shared-memory access (32-bit address).
+    uint8_t *smem = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
     uint8_t *a_ring = smem;
     uint8_t *b_ring = smem + p.off_b;
     uint8_t *raw = smem + p.off_raw;
@@ -421,22 +422,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 // ---------------------------------------------------------------------------
 namespace {
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-        else
-            cudaGetLastError();
-    });
-    return fn;
-}
-
 constexpr size_t kSmemLimitTc = 227 * 1024;
 
 struct TcPlan {
@@ -525,19 +510,12 @@ bool tc_supported(const MatmulArgs &a) {
 cudaError_t tc_launch(const MatmulArgs &a) {
     TcPlan pl;
     if (!tc_plan(a, pl)) return cudaErrorInvalidValue;
-    auto enc = encode_fn();
-    if (!enc) return cudaErrorNotSupported;
     CUtensorMap tm;
-    const cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
-    const cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)pl.BM};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = enc(&tm, a.dtype == AQ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                           2, const_cast<void *>(a.x), dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (!tmap_2d(&tm, a.dtype == AQ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                 a.x, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.K * 2, 64u, (uint32_t)pl.BM,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
     if (a.bits == 3)
         return a.dtype == AQ_BF16 ? tc_launch_bm<3, true>(pl, tm, a.stream)
                                   : tc_launch_bm<3, false>(pl, tm, a.stream);

@@ -44,6 +44,7 @@ def test_status_strings_and_version():
     assert "invalid" in aq.aq_status_string(1)
     assert aq.aq_status_string(99) == "unknown status"
     assert aq.aq_variant_name(aq.AQ_VARIANT_QMV) == "qmv"
+    assert aq.aq_variant_name(aq.AQ_VARIANT_GEMV) == "gemv"
     assert "sm_103a" in aq.aq_version()
 
 
@@ -97,13 +98,15 @@ def test_stats_interface():
 
 # The dispatch rule, on the shapes of the workloads (alignment assumed).
 @pytest.mark.parametrize("M,N,K,bits,variant", [
-    (1, 1024, 512, 4, aq.AQ_VARIANT_QMV),
-    (1, 4096, 4096, 4, aq.AQ_VARIANT_QMV),
-    (1, 10240, 5120, 3, aq.AQ_VARIANT_QMV),
+    (1, 1024, 512, 4, aq.AQ_VARIANT_GEMV),
+    (1, 4096, 4096, 4, aq.AQ_VARIANT_GEMV),
+    (1, 10240, 5120, 3, aq.AQ_VARIANT_GEMV),
+    (8, 10240, 5120, 3, aq.AQ_VARIANT_GEMV),
     (9, 10240, 5120, 3, aq.AQ_VARIANT_QMV),
     (16, 10240, 5120, 3, aq.AQ_VARIANT_QMV),
-    (1, 5120, 13824, 4, aq.AQ_VARIANT_QMV),
-    (1, 13824, 5120, 4, aq.AQ_VARIANT_QMV),
+    (1, 5120, 13824, 4, aq.AQ_VARIANT_GEMV),
+    (1, 13824, 5120, 4, aq.AQ_VARIANT_GEMV),
+    (1, 28672, 8192, 4, aq.AQ_VARIANT_GEMV),   # two passes of 95 rows per CTA
     (64, 10240, 5120, 3, aq.AQ_VARIANT_TC),
     (128, 28672, 8192, 4, aq.AQ_VARIANT_TC),
     (512, 28672, 8192, 4, aq.AQ_VARIANT_TC),
@@ -117,3 +120,21 @@ def test_select(M, N, K, bits, variant):
 def test_select_invalid():
     assert aq.aq_select(0, 16, 512, 4) == -1
     assert aq.aq_select(1, 16, 512, 7) == -1
+
+
+@pytest.mark.parametrize("M,N,K,bits,want", [
+    (1, 4096, 4096, 4, "rows/cta=27 passes=1 tiles=2 groups/stage=32 stages=2 ring=2 x=whole grid=152"),
+    (1, 28672, 8192, 4, "rows/cta=190 passes=2"),
+    (8, 600, 13824, 4, "x=ring"),
+])
+def test_gemv_plan(M, N, K, bits, want):
+    # The resident kernel's plan on a 152-SM GB300 (the SM count the library
+    # assumes when no device is present): rows per CTA = ceil(N / SMs), whole
+    # K per CTA, at most 128 rows per pass, ring as deep as 112 KB allows.
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("plan depends on the device's SM count")
+    d = aq.aq_describe(M, N, K, bits)
+    assert d.startswith("gemv ") and want in d, d
+    smem = int(d.split("smem=")[1])
+    assert smem <= 112 * 1024

@@ -18,7 +18,10 @@ pytestmark = pytest.mark.gpu
 
 aq = pytest.importorskip("quantized_matmul_affine_gb300")
 
-GENERIC, QMV, TC = aq.AQ_VARIANT_GENERIC, aq.AQ_VARIANT_QMV, aq.AQ_VARIANT_TC
+GENERIC, QMV, TC, GEMV = (aq.AQ_VARIANT_GENERIC, aq.AQ_VARIANT_QMV, aq.AQ_VARIANT_TC,
+                          aq.AQ_VARIANT_GEMV)
+ALL = [GENERIC, QMV, TC, GEMV]
+ALL_IDS = ["generic", "qmv", "tc", "gemv"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -80,16 +83,25 @@ SHAPES = [
     (100, 48, 512),
     (130, 300, 1024),
     (257, 200, 1536),
+    # resident small-M kernel: several CTAs per partial tile, two passes per
+    # CTA, a ring that wraps many times, x through its 4-slot ring
+    (5, 1000, 1024),
+    (2, 20000, 512),
+    (1, 3000, 13824),
+    (8, 600, 13824),
 ]
 
+GEMV_MAX_M = 8
 
-@pytest.mark.parametrize("variant", [GENERIC, QMV, TC, aq.AQ_VARIANT_AUTO],
-                         ids=["generic", "qmv", "tc", "auto"])
+
+@pytest.mark.parametrize("variant", ALL + [aq.AQ_VARIANT_AUTO], ids=ALL_IDS + ["auto"])
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 @pytest.mark.parametrize("bits", [3, 4])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_matmul_parity(shape, bits, dtype, variant):
     M, N, K = shape
+    if variant == GEMV and M > GEMV_MAX_M:
+        pytest.skip("the resident kernel serves M <= 8")
     p = workloads.make_problem("t", bits, N, K, M, dtype, seed=M * 7 + N + K + bits)
     y = run(p, variant)
     y_ref, bound = reference(p)
@@ -133,7 +145,30 @@ def test_unit_rows_read_back_every_weight(bits, dtype, variant):
     assert np.all(np.abs(y - w) <= ulp(w, dtype)), np.abs(y - w).max()
 
 
-@pytest.mark.parametrize("variant", [GENERIC, QMV, TC], ids=["generic", "qmv", "tc"])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("bits", [3, 4])
+def test_gemv_unit_rows_read_back_every_weight(bits, dtype):
+    # The resident kernel takes at most 8 rows: 64 calls of 8 rows of the
+    # identity read back all 512 weights of every row.
+    K, N = 512, 300
+    p = workloads.make_problem("t", bits, N, K, 8, dtype, seed=4)
+    codes, s, b, _ = dev_tensors(p)
+    Wq = aq.aq_pack(codes, bits)
+    sf = p.scales.astype(np.float64)
+    bf = p.biases.astype(np.float64)
+    w = (sf[:, np.arange(K) // 64] * p.codes + bf[:, np.arange(K) // 64]).T  # [K, N]
+    conv = workloads.f32_to_bf16_bits if dtype == "bf16" else workloads.f32_to_fp16_bits
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+    for k0 in range(0, K, 8):
+        e = np.zeros((8, K), np.float32)
+        e[np.arange(8), k0 + np.arange(8)] = 1.0
+        x = torch.from_numpy(conv(e).view(np.int16)).view(tdt).cuda()
+        y = y_to_f64(aq.aq_matmul_variant(GEMV, x, Wq, s, b, bits), dtype)
+        ref = w[k0:k0 + 8]
+        assert np.all(np.abs(y - ref) <= ulp(ref, dtype)), (k0, np.abs(y - ref).max())
+
+
+@pytest.mark.parametrize("variant", ALL, ids=ALL_IDS)
 @pytest.mark.parametrize("bits", [3, 4])
 def test_zero_codes_and_zero_scales(bits, variant):
     p = workloads.make_problem("t", bits, 64, 1024, 4, "fp16", seed=11)
@@ -148,7 +183,7 @@ def test_zero_codes_and_zero_scales(bits, variant):
     assert_within_tolerance(run(ps, variant), expected, bound, "zero scales")
 
 
-@pytest.mark.parametrize("variant", [GENERIC, QMV, TC], ids=["generic", "qmv", "tc"])
+@pytest.mark.parametrize("variant", ALL, ids=ALL_IDS)
 def test_ones_row(variant):
     bits, K, N = 4, 1024, 40
     p = workloads.make_problem("t", bits, N, K, 1, "bf16", seed=12)
@@ -162,7 +197,7 @@ def test_ones_row(variant):
 # Invariants and edge behaviour
 # --------------------------------------------------------------------------
 
-@pytest.mark.parametrize("variant", [GENERIC, QMV, TC], ids=["generic", "qmv", "tc"])
+@pytest.mark.parametrize("variant", ALL, ids=ALL_IDS)
 def test_deterministic(variant):
     p = workloads.make_problem("t", 3, 1000, 2048, 5, "bf16", seed=13)
     codes, s, b, x = dev_tensors(p)
@@ -184,7 +219,7 @@ def test_rows_match_single_row_calls():
         assert np.all(np.abs(ym[0] - y[m]) <= 2 * oracle.tolerance(bound[m]))
 
 
-@pytest.mark.parametrize("variant", [GENERIC, QMV, TC], ids=["generic", "qmv", "tc"])
+@pytest.mark.parametrize("variant", ALL, ids=ALL_IDS)
 def test_no_writes_outside_output(variant):
     M, N, K, bits = 3, 45, 1024, 4
     p = workloads.make_problem("t", bits, N, K, M, "fp16", seed=15)
@@ -219,7 +254,7 @@ def test_dispatch_counters():
     aq.aq_matmul_variant(GENERIC, x, Wq, s, b, 4)
     torch.cuda.synchronize()
     calls = aq.aq_stats()
-    assert calls[QMV] == 1 and calls[GENERIC] == 1
+    assert calls[GEMV] == 1 and calls[GENERIC] == 1
 
 
 def test_host_entry_point():
