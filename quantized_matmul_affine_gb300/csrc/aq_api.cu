@@ -91,10 +91,19 @@ static int gemv_max_m() {
     return v;
 }
 
+// Single activation rows over more than this many bytes of packed weights
+// go to the streaming small-M kernel: there the resident kernel's per-SM
+// decode work outweighs its overlap of consecutive calls (measured on GB300:
+// 13824x5120 and 5120x13824 at 4 bits, 35 MB, are 4-15% faster on qmv; the
+// 20 MB 3-bit 10240x5120 layer is 22% faster on gemv).
+constexpr int64_t kGemvM1MaxWeightBytes = 24ll << 20;
+
 // The dispatch rule.  Returns the variant for the arguments (alignment
 // included), never AQ_VARIANT_AUTO.
 static int choose(const MatmulArgs &a) {
-    if (a.M <= gemv_max_m() && gemv_supported(a)) return AQ_VARIANT_GEMV;
+    const int64_t wbytes = a.N * a.K * a.bits / 8;
+    const bool gemv_first = a.M > 1 || wbytes <= kGemvM1MaxWeightBytes;
+    if (a.M <= gemv_max_m() && gemv_first && gemv_supported(a)) return AQ_VARIANT_GEMV;
     const bool qmv = qmv_supported(a);
     const bool tc = tc_supported(a);
     if (qmv && (a.M <= qmv_max_m() || !tc)) return AQ_VARIANT_QMV;

@@ -55,6 +55,7 @@
 
 #include <algorithm>
 #include <cstdio>
+#include <cstdlib>
 #include <mutex>
 #include <type_traits>
 
@@ -74,6 +75,18 @@ constexpr int kXPitch = 144;     // bytes per activation row in an x slot (128 +
 // for the 8 MMA columns (32 bytes).
 constexpr int kXRing = 4;        // x slots per warp when the warp's x is not kept whole
 constexpr size_t kSmemBudget = 112 * 1024;  // two CTAs (two calls) per SM
+constexpr size_t kSmemMax = 227 * 1024;     // one CTA per SM
+
+// Shared-memory budget of a plan (AQ_GEMV_SMEM_KB overrides it for
+// experiments).
+size_t smem_budget() {
+    static const size_t v = [] {
+        const char *e = std::getenv("AQ_GEMV_SMEM_KB");
+        const long kb = (e && *e) ? std::atol(e) : 0;
+        return kb > 0 ? std::min<size_t>((size_t)kb * 1024, kSmemMax) : kSmemBudget;
+    }();
+    return v;
+}
 
 struct GemvParams {
     const void *x;
@@ -138,6 +151,24 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
             : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// d = A * B (no accumulator input): the zero C comes from one register that
+// the compiler keeps for the whole loop, instead of four zeroed registers
+// per MMA chain.
+template <bool BF16>
+__device__ __forceinline__ void mma16816_first(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1, float zero) {
+    if constexpr (BF16)
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%10,%10,%10,%10};"
+            : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(zero));
+    else
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%10,%10,%10,%10};"
+            : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(zero));
+}
+
 // A thread holds 16 codes of a group for one row (codes 16c .. 16c+15 of the
 // group, c = lane % 4).  They decode into 8 registers P[i] of two 16-bit
 // halves holding codes (lo(i), hi(i)):
@@ -153,6 +184,14 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
 // 2^-20).  Otherwise every code is shifted to bit 0 of its half and or-ed
 // with `magic`: zero (fp16 subnormal q * 2^-24) or the bf16 exponent of 128
 // (the bf16 value 128 + q).
+// (a & b) | c in one LOP3.  Written out because with two immediate operands
+// the compiler splits it into two logic operations.
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
 template <bool kInPlace, uint32_t kMagic>
 __device__ __forceinline__ void decode4(uint32_t w0, uint32_t w1, uint32_t (&P)[8]) {
     constexpr uint32_t m = 0x000F000Fu;
@@ -167,14 +206,14 @@ __device__ __forceinline__ void decode4(uint32_t w0, uint32_t w1, uint32_t (&P)[
         P[6] = v1 & m;
         P[7] = v1 & (m << 4);
     } else {
-        P[0] = (w0 & m) | kMagic;
-        P[1] = ((w0 >> 4) & m) | kMagic;
-        P[2] = ((w0 >> 8) & m) | kMagic;
-        P[3] = ((w0 >> 12) & m) | kMagic;
-        P[4] = (w1 & m) | kMagic;
-        P[5] = ((w1 >> 4) & m) | kMagic;
-        P[6] = ((w1 >> 8) & m) | kMagic;
-        P[7] = ((w1 >> 12) & m) | kMagic;
+        P[0] = and_or(w0, m, kMagic);
+        P[1] = and_or(w0 >> 4, m, kMagic);
+        P[2] = and_or(w0 >> 8, m, kMagic);
+        P[3] = and_or(w0 >> 12, m, kMagic);
+        P[4] = and_or(w1, m, kMagic);
+        P[5] = and_or(w1 >> 4, m, kMagic);
+        P[6] = and_or(w1 >> 8, m, kMagic);
+        P[7] = and_or(w1 >> 12, m, kMagic);
     }
 }
 
@@ -188,14 +227,14 @@ __device__ __forceinline__ void decode3(uint32_t wa, uint32_t wb, uint32_t sel0,
     constexpr uint32_t m = 0x00070007u;
     const uint32_t r0 = prmt(wa, wb, sel0);
     const uint32_t r2 = prmt(wa, wb, sel2);
-    P[0] = (r0 & m) | kMagic;
-    P[1] = ((r0 >> 3) & m) | kMagic;
-    P[2] = ((r0 >> 6) & m) | kMagic;
-    P[3] = ((r0 >> 9) & m) | kMagic;
-    P[4] = ((r0 >> 12) & m) | kMagic;
-    P[5] = ((r2 >> 7) & m) | kMagic;
-    P[6] = ((r2 >> 10) & m) | kMagic;
-    P[7] = ((r2 >> 13) & m) | kMagic;
+    P[0] = and_or(r0, m, kMagic);
+    P[1] = and_or(r0 >> 3, m, kMagic);
+    P[2] = and_or(r0 >> 6, m, kMagic);
+    P[3] = and_or(r0 >> 9, m, kMagic);
+    P[4] = and_or(r0 >> 12, m, kMagic);
+    P[5] = and_or(r2 >> 7, m, kMagic);
+    P[6] = and_or(r2 >> 10, m, kMagic);
+    P[7] = and_or(r2 >> 13, m, kMagic);
 }
 
 // B fragments of the four k-steps from the thread's 16 raw x values
@@ -306,7 +345,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
                     launch_dependents();
                     triggered = true;
                 }
-                if (lap > 0 && !mbar_wait_sleep(&empty[slot], (lap - 1) & 1, 64)) {
+                if (lap > 0 && !mbar_wait_sleep(&empty[slot], (lap - 1) & 1, 128)) {
                     gemv_record(flag, ERR_GEMV_EMPTY);
                     break;
                 }
@@ -329,13 +368,13 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
                 }
             }
             if (!triggered) {
-                if (!mbar_wait_sleep(x_landed, 0, 256)) gemv_record(flag, ERR_GEMV_FULL);
+                if (!mbar_wait_sleep(x_landed, 0, 512)) gemv_record(flag, ERR_GEMV_FULL);
                 launch_dependents();
             }
             // Copies still in flight must land before the CTA may exit.
             if (lane == 0)
                 for (int j = std::max(0, it - p.ring); j < it; ++j)
-                    if (!mbar_wait_sleep(&full[j % p.ring], (j / p.ring) & 1, 256)) {
+                    if (!mbar_wait_sleep(&full[j % p.ring], (j / p.ring) & 1, 512)) {
                         gemv_record(flag, ERR_GEMV_DRAIN);
                         break;
                     }
@@ -426,30 +465,33 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
         if (lane == 0) mbar_arrive(x_landed);
         launch_dependents();
         const int G = (int)(K / 64);
-        for (int u = threadIdx.x; u < M * G * 4; u += kConsumers * 32) {
-            const int m = u / (G * 4), rem = u - m * (G * 4);
-            const int gg = rem >> 2, cq = rem & 3;
-            uint4 *q = reinterpret_cast<uint4 *>(xraw + m * p.x_row_pitch + gg * 128 + 32 * cq);
-            const uint4 u0 = q[0], u1 = q[1];
-            const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-            float sum = 0.f;
+        for (int m = 0; m < M; ++m) {
+            for (int u = threadIdx.x; u < G * 4; u += kConsumers * 32) {
+                const int gg = u >> 2, cq = u & 3;
+                uint4 *q = reinterpret_cast<uint4 *>(xraw + m * p.x_row_pitch + gg * 128 + 32 * cq);
+                const uint4 u0 = q[0], u1 = q[1];
+                const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+                float part[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                if constexpr (BF16) {
-                    sum += __uint_as_float(w[i] << 16) + __uint_as_float(w[i] & 0xFFFF0000u);
-                } else {
-                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
-                    sum += f.x + f.y;
+                for (int i = 0; i < 8; ++i) {
+                    if constexpr (BF16) {
+                        part[i] = __uint_as_float(w[i] << 16) + __uint_as_float(w[i] & 0xFFFF0000u);
+                    } else {
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+                        part[i] = f.x + f.y;
+                    }
                 }
+                float sum = ((part[0] + part[1]) + (part[2] + part[3])) +
+                            ((part[4] + part[5]) + (part[6] + part[7]));
+                uint32_t bx[4][2];
+                x_frags<B>(u0, u1, bx);
+                q[0] = make_uint4(bx[0][0], bx[0][1], bx[1][0], bx[1][1]);
+                q[1] = make_uint4(bx[2][0], bx[2][1], bx[3][0], bx[3][1]);
+                // the four quarters of a group are four adjacent lanes
+                sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+                if (cq == 0) xsg[gg * 8 + m] = sum * kXsScale;
             }
-            uint32_t bx[4][2];
-            x_frags<B>(u0, u1, bx);
-            q[0] = make_uint4(bx[0][0], bx[0][1], bx[1][0], bx[1][1]);
-            q[1] = make_uint4(bx[2][0], bx[2][1], bx[3][0], bx[3][1]);
-            // the four quarters of a group are four adjacent lanes
-            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-            if (cq == 0) xsg[gg * 8 + m] = sum * kXsScale;
         }
         consumers_sync();
     }
@@ -474,7 +516,8 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
         }
         for (int s = 0; s < p.n_stages; ++s) {
             const uint8_t *st = smem + (size_t)slot * p.slot_bytes;
-            gemv_wait(&full[slot], lap & 1, flag, ERR_GEMV_FULL);
+            // (no check of the error flag here: the wait is bounded by itself)
+            if (!mbar_wait(&full[slot], lap & 1)) gemv_record(flag, ERR_GEMV_FULL);
             // The warp's WPS groups of the stage sit in column block
             // (warp*WPS) >> 2 and scale block (warp*WPS) >> 3.
             const int j0 = warp * WPS;
@@ -635,6 +678,7 @@ bool gemv_plan(const MatmulArgs &a, GemvPlan &pl) {
     if (a.N > INT32_MAX / 2 || a.K > INT32_MAX / 2) return false;
     const int B = a.bits;
     const int G = (int)(a.K / 64);
+    const size_t budget = smem_budget();
     const int sms = num_sms();
     const int64_t per_sm = (a.N + sms - 1) / sms;
     const int passes = (int)((per_sm + kMaxPassRows - 1) / kMaxPassRows);
@@ -687,9 +731,9 @@ bool gemv_plan(const MatmulArgs &a, GemvPlan &pl) {
                 for (int alias = passes == 1 ? 1 : 0; alias >= 0; --alias) {
                     const size_t fixed =
                         x_bytes + (alias ? 0 : red_bytes) + bars + 1024 /* alignment */;
-                    if (fixed >= kSmemBudget) continue;
+                    if (fixed >= budget) continue;
                     const int ring =
-                        (int)std::min<size_t>((size_t)total, (kSmemBudget - fixed) / q.slot_bytes);
+                        (int)std::min<size_t>((size_t)total, (budget - fixed) / q.slot_bytes);
                     if (ring < std::min(want, total)) continue;
                     if (alias && (size_t)ring * q.slot_bytes < red_bytes) continue;
                     q.ring = ring;
@@ -705,7 +749,7 @@ bool gemv_plan(const MatmulArgs &a, GemvPlan &pl) {
                     pl.smem = off + 1024;
                     q.x = a.x;
                     q.y = a.out;
-                    if (pl.smem <= kSmemBudget) return true;
+                    if (pl.smem <= budget) return true;
                 }
             }
         }
@@ -721,7 +765,7 @@ cudaError_t gemv_launch_t(const GemvPlan &pl, const CUtensorMap &tw, const CUten
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)kSmemBudget);
+                                        (int)kSmemMax);
     });
     if (attr_err != cudaSuccess) return attr_err;
     cudaLaunchConfig_t cfg = {};

@@ -88,15 +88,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Like mbar_wait for a waiter off the critical path: sleeps between polls
-// so that it does not take issue slots from the warps doing the work.
+// (32 ns doubling up to max_sleep_ns) so that it does not take issue slots
+// from the warps doing the work.
 __device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity,
-                                                uint32_t sleep_ns) {
+                                                uint32_t max_sleep_ns) {
     if (mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
+    uint32_t ns = 32;
     for (uint32_t it = 1; it < (1u << 31); ++it) {
-        __nanosleep(sleep_ns);
+        __nanosleep(ns);
+        if (ns < max_sleep_ns) ns <<= 1;
         if (mbar_test_wait(bar, parity)) return true;
-        if ((it & 63u) == 0u && globaltimer_ns() - t0 > AQ_WAIT_LIMIT_NS) return false;
+        if ((it & 15u) == 0u && globaltimer_ns() - t0 > AQ_WAIT_LIMIT_NS) return false;
     }
     return false;
 }

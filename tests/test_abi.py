@@ -104,9 +104,10 @@ def test_stats_interface():
     (8, 10240, 5120, 3, aq.AQ_VARIANT_GEMV),
     (9, 10240, 5120, 3, aq.AQ_VARIANT_QMV),
     (16, 10240, 5120, 3, aq.AQ_VARIANT_QMV),
-    (1, 5120, 13824, 4, aq.AQ_VARIANT_GEMV),
-    (1, 13824, 5120, 4, aq.AQ_VARIANT_GEMV),
-    (1, 28672, 8192, 4, aq.AQ_VARIANT_GEMV),   # two passes of 95 rows per CTA
+    (1, 5120, 13824, 4, aq.AQ_VARIANT_QMV),    # 35 MB of weights at M = 1
+    (1, 13824, 5120, 4, aq.AQ_VARIANT_QMV),
+    (8, 13824, 5120, 4, aq.AQ_VARIANT_GEMV),
+    (2, 28672, 8192, 4, aq.AQ_VARIANT_GEMV),   # two passes of 95 rows per CTA
     (64, 10240, 5120, 3, aq.AQ_VARIANT_TC),
     (128, 28672, 8192, 4, aq.AQ_VARIANT_TC),
     (512, 28672, 8192, 4, aq.AQ_VARIANT_TC),
@@ -124,7 +125,7 @@ def test_select_invalid():
 
 @pytest.mark.parametrize("M,N,K,bits,want", [
     (1, 4096, 4096, 4, "rows/cta=27 passes=1 tiles=2 groups/stage=32 stages=2 ring=2 x=whole grid=152"),
-    (1, 28672, 8192, 4, "rows/cta=190 passes=2"),
+    (2, 28672, 8192, 4, "rows/cta=190 passes=2"),
     (8, 600, 13824, 4, "x=ring"),
 ])
 def test_gemv_plan(M, N, K, bits, want):
