@@ -66,7 +66,7 @@ typedef enum aq_variant {
     AQ_VARIANT_GENERIC = 0, /* plain-load CUDA-core kernel: any K % 64 == 0, any alignment */
     AQ_VARIANT_QMV = 1,     /* small-M: bulk-async staged weights, warp MMA, factored dequant */
     AQ_VARIANT_TC = 2,      /* large-M: tcgen05 MMA with TMEM accumulators */
-    AQ_VARIANT_GEMV = 3,    /* M <= 8: one resident CTA per SM, TMA weight ring, warp MMA */
+    AQ_VARIANT_GEMV = 3,    /* M <= 16: one resident CTA per SM, TMA weight ring, warp MMA */
     AQ_NUM_VARIANTS = 4
 } aq_variant;
 

@@ -81,12 +81,14 @@ bool tmap_encode(CUtensorMap *tm, CUtensorMapDataType type, int rank, const void
 }
 
 // Largest M that the resident small-M kernel takes under the automatic rule
-// (AQ_GEMV_MAX_M overrides it for experiments).
+// (AQ_GEMV_MAX_M overrides it for experiments): it serves up to two 8-column
+// blocks, and measured faster than qmv at every M from 1 to 16 but the
+// single-row case below.
 static int gemv_max_m() {
     static const int v = [] {
         const char *e = std::getenv("AQ_GEMV_MAX_M");
         if (e && *e) return std::atoi(e);
-        return 8;
+        return 16;
     }();
     return v;
 }

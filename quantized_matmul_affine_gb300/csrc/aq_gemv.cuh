@@ -1,0 +1,727 @@
+// Resident small-M kernel ("gemv"): y = x . W^T for 1 <= M <= 16 activation
+// rows (one or two 8-column MMA blocks), streaming the packed weights once
+// per call.  Kernel template and plan types, shared by the translation units
+// that instantiate it (aq_gemv.cu: one column block; aq_gemv16.cu: two).
+//
+// Method (mlx-bun pages, @mlx-bun/inference 1.0.0, kernels/quantization/):
+//   * the weight format: 64-value groups, 2*B uint32 words each, LSB-first
+//     codes (affine-split-mma.ts affine_unit; affine3/4-mma.ts);
+//   * the factored group dot product of affine3-rows.ts / affine4-rows.ts:
+//     sum_g [ scale_g * sum_k q_k x_k + bias_g * sum_k x_k ], each weight
+//     decoded once and reused for every activation row;
+//   * the K-permuted operand layout of affine{3,4}-mma.ts: inside a group
+//     any order of k serves, provided x takes the same order.
+//
+// GB300 design:
+//   * At most one CTA per SM.  CTA c owns a contiguous block of R weight
+//     rows over all of K, R = ceil(N / SMs), so every SM streams the same
+//     number of bytes; a block taller than 128 rows runs in passes.
+//   * A producer warp streams the block through a ring of stages in shared
+//     memory: one stage is SG groups of K (SG = 8, 16 or 32) for the R rows,
+//     loaded by three TMA boxes issued from three lanes at once - the codes
+//     as one 3-D box (SG/4 column blocks of 128 bytes, 96 at 3 bits, times R
+//     rows), the scales and the biases as one 3-D box each (blocks of 8
+//     groups times R rows, so a row's 8 scales are 16 bytes from the next
+//     row's and the loads of 8 rows never share a bank) - with completion
+//     counted on an mbarrier.  (On GB300 a TMA op costs ~75 ns of issue time
+//     whatever its size, so a stage is a few large boxes.)  The weights do
+//     not depend on the preceding kernel, so the producer fills the ring
+//     before the CTA waits on the preceding grid.
+//     A CTA takes at most 112 KB of shared memory and 288 threads, so it
+//     fits on an SM beside a CTA of the previous call: with programmatic
+//     dependent launch a call's weight stream overlaps the previous call's
+//     tail, and for weights of up to ~100 KB per SM the whole stream is in
+//     shared memory before the call's x is even ready.
+//   * Eight consumer warps.  Warp w takes SG/8 consecutive groups of every
+//     stage, for all the block's 16-row tiles (the tile count is a template
+//     parameter, so the tiles interleave freely).
+//   * x (one 8-column block): one bulk copy per activation row once the grid
+//     dependency resolves, rewritten in place into B-fragment order with the
+//     group sums; or per-warp cp.async rings when it does not fit.  x (two
+//     blocks): a fourth producer lane streams it with the weights, one
+//     3-D TMA box of the stage's groups x 16 rows per stage (rows past M read
+//     as zero), and each warp builds its fragments and sums per group.
+//   * Codes decode into MMA A fragments (weights are the 16-row A operand)
+//     with one shift and one LOP3 per two codes (4-bit fp16: one AND per
+//     two codes plus a shift per word, the codes staying in place), each
+//     code alone in the bits of a 16-bit half:
+//       fp16 x: the half is the subnormal q * 2^(p-24) (exact), so
+//               y_g = scale * 2^24 * D + bias * sum(x);
+//       bf16 x: under the exponent of 128 the half is the bf16 value 128 + q
+//               (exact), so y_g = scale * D + (bias - 128 * scale) * sum(x).
+//     x is the B operand in its own type; nothing is converted.  mma.sync
+//     m16n8k16 accumulates in fp32.
+//   * The group sums of x come from the same B fragments times an all-ones
+//     A operand: four more MMAs per group per warp, shared by every tile.
+//   * The eight warps' partial tiles meet in shared memory and are added in
+//     warp order (deterministic).
+#pragma once
+
+#include "aq_internal.h"
+#include "aq_ptx.cuh"
+
+#include <cuda.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+#include <type_traits>
+
+namespace aq {
+namespace gemv {
+
+constexpr int kConsumers = 8;                     // consumer warps
+constexpr int kGemvThreads = (kConsumers + 1) * 32;  // + one producer warp
+constexpr int kMaxTiles = 8;                      // 16-row tiles per pass
+constexpr int kMaxPassRows = 16 * kMaxTiles;
+constexpr int kXPitch = 144;     // bytes per activation row in an x slot (128 + 16: no bank conflicts)
+// An x slot holds one group of every activation row (M rows at kXPitch),
+// rewritten in place into MMA B-fragment order, then the group's sums of x
+// for the 8 MMA columns (32 bytes).
+constexpr int kXRing = 4;        // x slots per warp when the warp's x is not kept whole
+constexpr size_t kSmemBudget = 112 * 1024;  // two CTAs (two calls) per SM
+
+struct GemvParams {
+    const void *x;
+    void *y;
+    uint32_t *err;   // the device error word
+    int M, N, K;
+    int rows_cta;    // weight rows per CTA (passes * pass_rows)
+    int pass_rows;   // rows per pass = TMA box height (<= 128)
+    int passes;
+    int tiles;       // 16-row tiles per pass
+    int sg;          // groups per stage (8 x groups per warp)
+    int n_stages;    // G / sg
+    int ring;        // weight stages in the ring
+    int x_whole;     // 1: all of x in shared memory (one bulk copy per row); 0: per-warp rings
+    int red_alias;   // 1: the partial-tile buffer reuses the ring (single pass)
+    uint32_t slot_bytes, off_sc, off_bi;  // inside a ring slot (codes at 0)
+    uint32_t off_x, off_red, off_bar;
+    uint32_t x_warp_bytes;  // x region of one warp
+    uint32_t x_slot_bytes;  // one x slot (M rows + the 8 group sums)
+    uint32_t x_row_pitch;   // whole x: bytes per activation row (2K + 16)
+    uint32_t off_xs;        // whole x: group sums [G][8] floats
+    uint32_t off_xst;       // staged x (two column blocks): box inside a ring slot
+    uint32_t stage_tx;      // bytes one stage brings in
+};
+
+__device__ __forceinline__ void consumers_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void *tm) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tm) : "memory");
+}
+
+__device__ __forceinline__ void gemv_record(volatile int *flag, uint32_t *err, uint32_t code) {
+    *flag = 1;
+    atomicOr(err, code);
+}
+
+// Bounded mbarrier wait; gives up at once if another warp already gave up.
+__device__ __forceinline__ bool gemv_wait(uint64_t *bar, uint32_t parity, volatile int *flag,
+                                          uint32_t *err, uint32_t code) {
+    if (*flag) return false;
+    if (mbar_wait(bar, parity)) return true;
+    gemv_record(flag, err, code);
+    return false;
+}
+
+// (Not volatile: the MMA has no side effects, so independent ones may be
+// scheduled freely.)
+template <bool BF16>
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    if constexpr (BF16)
+        asm(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    else
+        asm(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// d = A * B (no accumulator input): the zero C comes from one register that
+// the compiler keeps for the whole loop, instead of four zeroed registers
+// per MMA chain.
+template <bool BF16>
+__device__ __forceinline__ void mma16816_first(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1, float zero) {
+    if constexpr (BF16)
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%10,%10,%10,%10};"
+            : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(zero));
+    else
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%10,%10,%10,%10};"
+            : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(zero));
+}
+
+// A thread holds 16 codes of a group for one row (codes 16c .. 16c+15 of the
+// group, c = lane % 4).  They decode into 8 registers P[i] of two 16-bit
+// halves holding codes (lo(i), hi(i)):
+//   4-bit: (0,4) (1,5) (2,6) (3,7) (8,12) (9,13) (10,14) (11,15)
+//   3-bit: (i, i+8)
+// The four MMA k-steps of the group take the register pairs
+//   4-bit: (P0,P2) (P4,P6) (P1,P3) (P5,P7);  3-bit: (P0,P1) (P2,P3) (P4,P5) (P6,P7).
+//
+// 4-bit with fp16 x: each code stays where it is inside its half, which is
+// then the exact fp16 subnormal q * 2^(p-24) with p = 0 for P0, P2, P4, P6
+// and p = 4 for P1, P3, P5, P7 (one shift and four ANDs per word).  Steps
+// 0-1 and steps 2-3 therefore accumulate separately (D0 at 2^-24, D4 at
+// 2^-20).  Otherwise every code is shifted to bit 0 of its half and or-ed
+// with `magic`: zero (fp16 subnormal q * 2^-24) or the bf16 exponent of 128
+// (the bf16 value 128 + q).
+// (a & b) | c in one LOP3.  Written out because with two immediate operands
+// the compiler splits it into two logic operations.
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+template <bool kInPlace, uint32_t kMagic>
+__device__ __forceinline__ void decode4(uint32_t w0, uint32_t w1, uint32_t (&P)[8]) {
+    constexpr uint32_t m = 0x000F000Fu;
+    if constexpr (kInPlace) {
+        const uint32_t v0 = w0 >> 8, v1 = w1 >> 8;
+        P[0] = w0 & m;
+        P[1] = w0 & (m << 4);
+        P[2] = v0 & m;
+        P[3] = v0 & (m << 4);
+        P[4] = w1 & m;
+        P[5] = w1 & (m << 4);
+        P[6] = v1 & m;
+        P[7] = v1 & (m << 4);
+    } else {
+        P[0] = and_or(w0, m, kMagic);
+        P[1] = and_or(w0 >> 4, m, kMagic);
+        P[2] = and_or(w0 >> 8, m, kMagic);
+        P[3] = and_or(w0 >> 12, m, kMagic);
+        P[4] = and_or(w1, m, kMagic);
+        P[5] = and_or(w1 >> 4, m, kMagic);
+        P[6] = and_or(w1 >> 8, m, kMagic);
+        P[7] = and_or(w1 >> 12, m, kMagic);
+    }
+}
+
+// 3-bit: the thread's 48-bit span (code j at bit 3j) starts at byte bo of
+// word wa.  r0 = span bytes {0,1,3,4} has codes 0..4 in its low half and
+// 8..12 in its high half, each half starting at bit 0; r2 = span bytes
+// {1,2,4,5} has codes 5..7 and 13..15 from bit 7 of each half.
+template <uint32_t kMagic>
+__device__ __forceinline__ void decode3(uint32_t wa, uint32_t wb, uint32_t sel0, uint32_t sel2,
+                                        uint32_t (&P)[8]) {
+    constexpr uint32_t m = 0x00070007u;
+    const uint32_t r0 = prmt(wa, wb, sel0);
+    const uint32_t r2 = prmt(wa, wb, sel2);
+    P[0] = and_or(r0, m, kMagic);
+    P[1] = and_or(r0 >> 3, m, kMagic);
+    P[2] = and_or(r0 >> 6, m, kMagic);
+    P[3] = and_or(r0 >> 9, m, kMagic);
+    P[4] = and_or(r0 >> 12, m, kMagic);
+    P[5] = and_or(r2 >> 7, m, kMagic);
+    P[6] = and_or(r2 >> 10, m, kMagic);
+    P[7] = and_or(r2 >> 13, m, kMagic);
+}
+
+// B fragments of the four k-steps from the thread's 16 raw x values
+// (r[j] = (x_2j, x_2j+1)), matching the code pairs of each step.
+template <int B>
+__device__ __forceinline__ void x_frags(const uint4 &u0, const uint4 &u1, uint32_t (&bx)[4][2]) {
+    const uint32_t r[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    if constexpr (B == 4) {
+        // (x0,x4)(x2,x6) | (x8,x12)(x10,x14) | (x1,x5)(x3,x7) | (x9,x13)(x11,x15)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int a = 4 * (q & 1);                     // 0, 4, 0, 4
+            const uint32_t sel = q < 2 ? 0x5410u : 0x7632u;  // low or high halves
+            bx[q][0] = prmt(r[a], r[a + 2], sel);
+            bx[q][1] = prmt(r[a + 1], r[a + 3], sel);
+        }
+    } else {
+        // (x0,x8)(x1,x9) | (x2,x10)(x3,x11) | (x4,x12)(x5,x13) | (x6,x14)(x7,x15)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            bx[q][0] = prmt(r[q], r[q + 4], 0x5410u);
+            bx[q][1] = prmt(r[q], r[q + 4], 0x7632u);
+        }
+    }
+}
+
+// Code registers of k-step q (see decode4 / decode3).
+template <int B>
+__device__ __forceinline__ void step_frags(const uint32_t (&PA)[8], const uint32_t (&PB)[8], int q,
+                                           uint32_t (&af)[4]) {
+    int i0, i1;
+    if constexpr (B == 4) {
+        i0 = (q & 1) * 4 + (q >> 1);  // 0, 4, 1, 5
+        i1 = i0 + 2;
+    } else {
+        i0 = 2 * q;
+        i1 = i0 + 1;
+    }
+    af[0] = PA[i0];
+    af[1] = PB[i0];
+    af[2] = PA[i1];
+    af[3] = PB[i1];
+}
+
+template <typename T>
+__device__ __forceinline__ void store_y(T *p, float v);
+template <>
+__device__ __forceinline__ void store_y<__half>(__half *p, float v) { *p = __float2half_rn(v); }
+template <>
+__device__ __forceinline__ void store_y<__nv_bfloat16>(__nv_bfloat16 *p, float v) {
+    *p = __float2bfloat16_rn(v);
+}
+
+template <int B, bool BF16, int TILES, int WPS, int MB>
+__global__ void __launch_bounds__(kGemvThreads, 2)
+    gemv_kernel(const __grid_constant__ GemvParams p, const __grid_constant__ CUtensorMap tm_w,
+                const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_b,
+                const __grid_constant__ CUtensorMap tm_x) {
+    constexpr bool kXStage = MB > 1;  // x streamed per stage by a fourth producer lane
+    using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+    constexpr int kBox = B == 4 ? 128 : 96;  // bytes of a row in one column block (4 groups)
+    constexpr uint32_t kMagic = BF16 ? 0x43004300u : 0u;
+    extern __shared__ uint8_t smem_raw[];
+    // Align to 1024 bytes by an offset from the __shared__ array itself, so
+    // that every access below stays a shared-memory access (32-bit address).
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);
+    uint64_t *empty = full + p.ring;
+    uint64_t *x_landed = empty + p.ring;  // one arrival per consumer warp
+    uint64_t *x_full = x_landed + 1;      // whole x: the bulk copies of x
+    volatile int *flag = reinterpret_cast<volatile int *>(x_full + 1);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < p.ring; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kConsumers);
+        }
+        mbar_init(x_landed, kConsumers);
+        mbar_init(x_full, 1);
+        *flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // The next call is allowed to launch (and start streaming its weights)
+    // only once this CTA's x has landed: launched earlier, its prefetch
+    // would queue in front of this call's x loads.  Every thread that stays
+    // alive triggers at that point (consumers after their copy, the
+    // producer lanes once x_landed completes).
+
+    const int row_cta = blockIdx.x * p.rows_cta;
+    const int total = p.passes * p.n_stages;
+    const int nb = p.sg / 4;  // column blocks per stage
+
+    if (warp == kConsumers) {
+        // ------------------------------------------------------------------
+        // Producer: lanes 0, 1, 2 issue the codes, scales and biases boxes of
+        // each (pass, stage) in order; lane 0 also posts the byte count.
+        // ------------------------------------------------------------------
+        if (lane < (kXStage ? 4 : 3)) {
+            const CUtensorMap *tm = lane == 0 ? &tm_w : lane == 1 ? &tm_s : lane == 2 ? &tm_b : &tm_x;
+            prefetch_tmap(tm);
+            if (lane == 3) grid_dependency_wait();  // x belongs to the stream order
+            bool triggered = false;
+            int it = 0, slot = 0, lap = 0, pass = 0, s = 0;
+            for (; it < total; ++it) {
+                if (!triggered && mbar_test_wait(x_landed, 0)) {
+                    launch_dependents();
+                    triggered = true;
+                }
+                if (lap > 0 && !mbar_wait_sleep(&empty[slot], (lap - 1) & 1, 128)) {
+                    gemv_record(flag, p.err, ERR_GEMV_EMPTY);
+                    break;
+                }
+                const int r0 = row_cta + pass * p.pass_rows;
+                uint8_t *dst = smem + (size_t)slot * p.slot_bytes;
+                if (lane == 3) {
+                    tma_load_3d(dst + p.off_xst, tm, 0, 0, s * p.sg, &full[slot]);
+                } else if (lane == 0) {
+                    mbar_arrive_expect_tx(&full[slot], p.stage_tx);
+                    tma_load_3d(dst, tm, 0, r0, s * nb, &full[slot]);
+                } else {
+                    tma_load_3d(dst + (lane == 1 ? p.off_sc : p.off_bi), tm, 0, r0, s * (p.sg / 8),
+                                &full[slot]);
+                }
+                if (++slot == p.ring) {
+                    slot = 0;
+                    ++lap;
+                }
+                if (++s == p.n_stages) {
+                    s = 0;
+                    ++pass;
+                }
+            }
+            if (!triggered) {
+                if (!mbar_wait_sleep(x_landed, 0, 512)) gemv_record(flag, p.err, ERR_GEMV_FULL);
+                launch_dependents();
+            }
+            // Copies still in flight must land before the CTA may exit.
+            if (lane == 0)
+                for (int j = std::max(0, it - p.ring); j < it; ++j)
+                    if (!mbar_wait_sleep(&full[j % p.ring], (j / p.ring) & 1, 512)) {
+                        gemv_record(flag, p.err, ERR_GEMV_DRAIN);
+                        break;
+                    }
+        }
+        return;
+    }
+
+    // ----------------------------------------------------------------------
+    // Consumers.  Warp w takes groups w*WPS .. w*WPS + WPS-1 of every stage
+    // (a stage is 8*WPS groups), for every 16-row tile of the pass; the
+    // WPS x TILES units of a stage are unrolled.
+    // ----------------------------------------------------------------------
+    constexpr bool kInPlace = (B == 4) && !BF16;
+    // fp16 x: the products carry 2^-24, which the group sums of x take too;
+    // y = 2^24 * acc.
+    constexpr float kXsScale = BF16 ? 1.f : 5.9604644775390625e-08f;
+    const int g = lane >> 2, c = lane & 3;
+    // MMA row g (and g + 8) reads tile row pg (and pg + 8): rows 0,2,4,6 for
+    // the lanes of one half-warp and 1,3,5,7 for the other, so that the
+    // 8-byte code loads of the 128-byte swizzle never share a bank.
+    const int pg = ((g & 3) << 1) | (g >> 2);
+    const int M = p.M;
+    const int64_t K = p.K;
+    const int n_wg = p.n_stages * WPS;  // groups of one warp over K
+    uint8_t *xw = smem + p.off_x + (size_t)warp * p.x_warp_bytes;
+    const uint32_t xsb = p.x_slot_bytes;
+    const int xrow = min(g, M - 1);     // columns past M repeat row M-1 (never stored)
+
+    // 3-bit: where this lane's 48-bit span starts (word, byte) in a group.
+    uint32_t sel0 = 0, sel2 = 0;
+    int wi3 = 0;
+    if constexpr (B == 3) {
+        const uint32_t bo = 2u * (uint32_t)(c & 1);
+        sel0 = bo | ((bo + 1) << 4) | ((bo + 3) << 8) | ((bo + 4) << 12);
+        sel2 = (bo + 1) | ((bo + 2) << 4) | ((bo + 4) << 8) | ((bo + 5) << 12);
+        wi3 = (3 * c) >> 1;
+    }
+
+    // x and y belong to the stream order: wait for the preceding grid.
+    grid_dependency_wait();
+
+    const T *xg = static_cast<const T *>(p.x);
+    // The warp's k-th group of every activation row: 128 bytes per row.
+    auto issue_x = [&](int k, int xslot) {
+        const int gg = (k / WPS) * (8 * WPS) + warp * WPS + (k % WPS);
+        uint8_t *dst = xw + (size_t)xslot * xsb;
+        const T *src = xg + (int64_t)gg * 64;
+        for (int q = lane; q < M * 8; q += 32) {
+            const int m = q >> 3, ch = q & 7;
+            cp_async16(dst + m * kXPitch + ch * 16, src + (int64_t)m * K + ch * 8, 16u);
+        }
+    };
+    const uint32_t one = BF16 ? 0x3F803F80u : 0x3C003C00u;
+    const uint32_t ones[4] = {one, one, one, one};
+    // Rewrite a landed x slot in place into B-fragment order and store the
+    // group sums of its 8 columns (the slot's tail).  A lane touches only
+    // its own 32 bytes of its own row, so slots need no warp barrier between
+    // them and consecutive ones overlap; lanes past row M-1 feed zeros.
+    auto prep_x = [&](int xslot) {
+        uint8_t *sl = xw + (size_t)xslot * xsb;
+        uint32_t bx[4][2] = {{0u, 0u}, {0u, 0u}, {0u, 0u}, {0u, 0u}};
+        uint4 *row = reinterpret_cast<uint4 *>(sl + g * kXPitch + 32 * c);
+        if (g < M) x_frags<B>(row[0], row[1], bx);
+        float xsum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) mma16816<BF16>(xsum, ones, bx[q][0], bx[q][1]);
+        if (g < M) {
+            row[0] = make_uint4(bx[0][0], bx[0][1], bx[1][0], bx[1][1]);
+            row[1] = make_uint4(bx[2][0], bx[2][1], bx[3][0], bx[3][1]);
+        }
+        if (g == 0)
+            *reinterpret_cast<float2 *>(sl + M * kXPitch + 8 * c) =
+                make_float2(xsum[0] * kXsScale, xsum[1] * kXsScale);
+    };
+    // Whole x: one bulk copy per activation row, then all consumer threads
+    // rewrite it in place into B-fragment order (one 32-byte quarter of a
+    // group each) and take the group sums, [G][8] floats.
+    uint8_t *xraw = smem + p.off_x;
+    float *xsg = reinterpret_cast<float *>(smem + p.off_xs);
+    if (!kXStage && p.x_whole) {
+        if (threadIdx.x == 0) {
+            mbar_arrive_expect_tx(x_full, (uint32_t)(M * K * 2));
+            for (int m = 0; m < M; ++m)
+                bulk_g2s_plain(xraw + m * p.x_row_pitch, xg + (int64_t)m * K, (uint32_t)(K * 2),
+                               x_full);
+        }
+        gemv_wait(x_full, 0, flag, p.err, ERR_GEMV_FULL);
+        if (lane == 0) mbar_arrive(x_landed);
+        launch_dependents();
+        const int G = (int)(K / 64);
+        for (int m = 0; m < M; ++m) {
+            for (int u = threadIdx.x; u < G * 4; u += kConsumers * 32) {
+                const int gg = u >> 2, cq = u & 3;
+                uint4 *q = reinterpret_cast<uint4 *>(xraw + m * p.x_row_pitch + gg * 128 + 32 * cq);
+                const uint4 u0 = q[0], u1 = q[1];
+                const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+                float part[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if constexpr (BF16) {
+                        part[i] = __uint_as_float(w[i] << 16) + __uint_as_float(w[i] & 0xFFFF0000u);
+                    } else {
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+                        part[i] = f.x + f.y;
+                    }
+                }
+                float sum = ((part[0] + part[1]) + (part[2] + part[3])) +
+                            ((part[4] + part[5]) + (part[6] + part[7]));
+                uint32_t bx[4][2];
+                x_frags<B>(u0, u1, bx);
+                q[0] = make_uint4(bx[0][0], bx[0][1], bx[1][0], bx[1][1]);
+                q[1] = make_uint4(bx[2][0], bx[2][1], bx[3][0], bx[3][1]);
+                // the four quarters of a group are four adjacent lanes
+                sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+                if (cq == 0) xsg[gg * 8 + m] = sum * kXsScale;
+            }
+        }
+        consumers_sync();
+    }
+
+    T *y = static_cast<T *>(p.y);
+    float *red = reinterpret_cast<float *>(smem + p.off_red);
+    const int pr = p.pass_rows;
+
+    int slot = 0, lap = 0;  // ring position of the current stage
+    for (int pass = 0; pass < p.passes; ++pass) {
+        float acc[TILES][MB][4];
+#pragma unroll
+        for (int t = 0; t < TILES; ++t)
+#pragma unroll
+            for (int mb = 0; mb < MB; ++mb)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[t][mb][i] = 0.f;
+
+        if (!kXStage && !p.x_whole) {
+            for (int k = 0; k < kXRing - 1; ++k) {
+                if (k < n_wg) issue_x(k, k);
+                cp_async_commit();
+            }
+        }
+        for (int s = 0; s < p.n_stages; ++s) {
+            const uint8_t *st = smem + (size_t)slot * p.slot_bytes;
+            // (no check of the error flag here: the wait is bounded by itself)
+            if (!mbar_wait(&full[slot], lap & 1)) gemv_record(flag, p.err, ERR_GEMV_FULL);
+            if (kXStage && pass == 0 && s == 0) {  // this call's x has started landing
+                if (lane == 0) mbar_arrive(x_landed);
+                launch_dependents();
+            }
+            // The warp's WPS groups of the stage sit in column block
+            // (warp*WPS) >> 2 and scale block (warp*WPS) >> 3.
+            const int j0 = warp * WPS;
+            const uint8_t *cb0 = st + (size_t)((j0 >> 2) * pr) * kBox;
+            const int q7 = ((j0 >> 2) * pr + pg) & 7;
+            const uint8_t *sc0 = st + p.off_sc + ((j0 >> 3) * pr) * 16 + (j0 & 7) * 2;
+            const uint8_t *bi0 = st + p.off_bi + ((j0 >> 3) * pr) * 16 + (j0 & 7) * 2;
+#pragma unroll
+            for (int i = 0; i < WPS; ++i) {
+                const int k = s * WPS + i;
+                int xslot = k;
+                if (!kXStage && !p.x_whole) {
+                    xslot = k % kXRing;
+                    if (k + kXRing - 1 < n_wg) issue_x(k + kXRing - 1, (k + kXRing - 1) % kXRing);
+                    cp_async_commit();
+                    cp_async_wait<kXRing - 1>();
+                    __syncwarp();
+                    if (pass == 0 && k == 0) {
+                        if (lane == 0) mbar_arrive(x_landed);
+                        launch_dependents();
+                    }
+                    prep_x(xslot);
+                    __syncwarp();
+                }
+                // B fragments and group sums of columns 2c, 2c+1 of each block
+                uint32_t bx[MB][4][2];
+                float xs0[MB], xs1[MB];
+                if constexpr (kXStage) {
+                    // raw x of the group: [8*MB rows][128 bytes], 128-byte swizzle
+#pragma unroll
+                    for (int mb = 0; mb < MB; ++mb) {
+                        const int seg = (j0 + i) * (8 * MB) + 8 * mb + g;
+                        const uint8_t *xr = st + p.off_xst + seg * 128;
+                        const uint4 u0 =
+                            *reinterpret_cast<const uint4 *>(xr + (((2 * c) ^ (seg & 7)) << 4));
+                        const uint4 u1 =
+                            *reinterpret_cast<const uint4 *>(xr + (((2 * c + 1) ^ (seg & 7)) << 4));
+                        x_frags<B>(u0, u1, bx[mb]);
+                        float xsum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            mma16816<BF16>(xsum, ones, bx[mb][q][0], bx[mb][q][1]);
+                        xs0[mb] = xsum[0] * kXsScale;
+                        xs1[mb] = xsum[1] * kXsScale;
+                    }
+                } else {
+                    const uint8_t *fr;
+                    const float *xsp;
+                    if (p.x_whole) {
+                        const int gg = s * (8 * WPS) + j0 + i;
+                        fr = xraw + xrow * p.x_row_pitch + gg * 128 + 32 * c;
+                        xsp = xsg + gg * 8 + 2 * c;
+                    } else {
+                        const uint8_t *sl = xw + (size_t)xslot * xsb;
+                        fr = sl + xrow * kXPitch + 32 * c;
+                        xsp = reinterpret_cast<const float *>(sl + M * kXPitch) + 2 * c;
+                    }
+                    const uint4 u0 = *reinterpret_cast<const uint4 *>(fr);
+                    const uint4 u1 = *reinterpret_cast<const uint4 *>(fr + 16);
+                    bx[0][0][0] = u0.x; bx[0][0][1] = u0.y; bx[0][1][0] = u0.z; bx[0][1][1] = u0.w;
+                    bx[0][2][0] = u1.x; bx[0][2][1] = u1.y; bx[0][3][0] = u1.z; bx[0][3][1] = u1.w;
+                    const float2 xs = *reinterpret_cast<const float2 *>(xsp);
+                    xs0[0] = xs.x;
+                    xs1[0] = xs.y;
+                }
+                const int gi = (j0 + i) & 3;  // group within its column block
+                // 128-byte swizzle: 16-byte chunk ch of a row segment q sits at
+                // ch ^ (q & 7); rows pg and pg + 8 of every tile share q & 7.
+                const int off4 = (((2 * gi + (c >> 1)) ^ q7) << 4) + 8 * (c & 1);
+#pragma unroll
+                for (int t = 0; t < TILES; ++t) {
+                    const int ra = 16 * t + pg, rb = ra + 8;
+                    uint32_t PA[8], PB[8];
+                    if constexpr (B == 4) {
+                        const uint2 qa = *reinterpret_cast<const uint2 *>(cb0 + ra * 128 + off4);
+                        const uint2 qb = *reinterpret_cast<const uint2 *>(cb0 + rb * 128 + off4);
+                        decode4<kInPlace, kMagic>(qa.x, qa.y, PA);
+                        decode4<kInPlace, kMagic>(qb.x, qb.y, PB);
+                    } else {
+                        const uint32_t *pa =
+                            reinterpret_cast<const uint32_t *>(cb0 + ra * 96 + 24 * gi) + wi3;
+                        const uint32_t *pb =
+                            reinterpret_cast<const uint32_t *>(cb0 + rb * 96 + 24 * gi) + wi3;
+                        decode3<kMagic>(pa[0], pa[1], sel0, sel2, PA);
+                        decode3<kMagic>(pb[0], pb[1], sel0, sel2, PB);
+                    }
+                    const float sa = __half2float(*reinterpret_cast<const __half *>(sc0 + ra * 16 + 2 * i));
+                    const float sb = __half2float(*reinterpret_cast<const __half *>(sc0 + rb * 16 + 2 * i));
+                    float ba = __half2float(*reinterpret_cast<const __half *>(bi0 + ra * 16 + 2 * i));
+                    float bb = __half2float(*reinterpret_cast<const __half *>(bi0 + rb * 16 + 2 * i));
+                    if constexpr (BF16 && !kInPlace) {
+                        ba = fmaf(-128.f, sa, ba);
+                        bb = fmaf(-128.f, sb, bb);
+                    }
+                    // steps 2-3 hold the codes at bit 4 (16 q * 2^-24) in the in-place decode
+                    const float sa4 = kInPlace ? sa * 0.0625f : sa, sb4 = kInPlace ? sb * 0.0625f : sb;
+#pragma unroll
+                    for (int mb = 0; mb < MB; ++mb) {
+                        // two independent MMA chains (steps 0-1 and 2-3)
+                        float da[4] = {0.f, 0.f, 0.f, 0.f}, db[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t af[4];
+                            step_frags<B>(PA, PB, q, af);
+                            if (q < 2)
+                                mma16816<BF16>(da, af, bx[mb][q][0], bx[mb][q][1]);
+                            else
+                                mma16816<BF16>(db, af, bx[mb][q][0], bx[mb][q][1]);
+                        }
+                        float *a4 = acc[t][mb];
+                        a4[0] = fmaf(sa, da[0], fmaf(sa4, db[0], fmaf(ba, xs0[mb], a4[0])));
+                        a4[1] = fmaf(sa, da[1], fmaf(sa4, db[1], fmaf(ba, xs1[mb], a4[1])));
+                        a4[2] = fmaf(sb, da[2], fmaf(sb4, db[2], fmaf(bb, xs0[mb], a4[2])));
+                        a4[3] = fmaf(sb, da[3], fmaf(sb4, db[3], fmaf(bb, xs1[mb], a4[3])));
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            if (++slot == p.ring) {
+                slot = 0;
+                ++lap;
+            }
+        }
+
+        // ------------------------------------------------------------------
+        // The eight warps' partial tiles, added in warp order.  With a single
+        // pass the buffer is the ring itself, free once every warp is done.
+        // ------------------------------------------------------------------
+        if (p.red_alias) consumers_sync();
+#pragma unroll
+        for (int t = 0; t < TILES; ++t)
+#pragma unroll
+            for (int mb = 0; mb < MB; ++mb)
+                *reinterpret_cast<float4 *>(&red[(((warp * TILES + t) * MB + mb) * 32 + lane) * 4]) =
+                    make_float4(acc[t][mb][0], acc[t][mb][1], acc[t][mb][2], acc[t][mb][3]);
+        consumers_sync();
+        const int r0 = row_cta + pass * pr;
+        const int rows = std::min(pr, p.N - r0);
+        for (int e = threadIdx.x; e < rows * M; e += kConsumers * 32) {
+            const int m = e / rows, r = e - m * rows;
+            const int t = r >> 4, rr = r & 15;
+            const int ph = rr & 7;                       // tile row within the half
+            const int gl = (ph >> 1) | ((ph & 1) << 2);  // the MMA row that read it
+            const int mb = m >> 3, mm = m & 7;           // column block, column in it
+            const int ln = 4 * gl + (mm >> 1), i = 2 * (rr >> 3) + (mm & 1);
+            float v = 0.f;
+            for (int w = 0; w < kConsumers; ++w)
+                v += red[(((w * TILES + t) * MB + mb) * 32 + ln) * 4 + i];
+            if constexpr (!BF16) v *= 16777216.f;  // 2^24
+            store_y<T>(&y[(int64_t)m * p.N + r0 + r], v);
+        }
+        consumers_sync();  // the buffer is rewritten by the next pass
+    }
+    cp_async_wait<0>();
+}
+
+// ---------------------------------------------------------------------------
+// Plan and launch (host)
+// ---------------------------------------------------------------------------
+struct GemvPlan {
+    GemvParams prm;
+    size_t smem;
+    int grid;
+    int mb;    // 8-column blocks of activation rows
+    int wps;   // groups per warp per stage
+    int bits;
+    bool bf16;
+};
+
+constexpr size_t kSmemMax = 227 * 1024;  // one CTA per SM at most
+
+template <int B, bool BF16, int TILES, int WPS, int MB>
+cudaError_t launch_t(const GemvPlan &pl, const CUtensorMap &tw, const CUtensorMap &ts,
+                     const CUtensorMap &tb, const CUtensorMap &tx, cudaStream_t stream) {
+    auto kern = gemv_kernel<B, BF16, TILES, WPS, MB>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)kSmemMax);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)pl.grid, 1, 1);
+    cfg.blockDim = dim3(kGemvThreads, 1, 1);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, pl.prm, tw, ts, tb, tx);
+}
+
+// Two column blocks (M = 9..16): defined in aq_gemv16.cu.
+cudaError_t launch_mb2(const GemvPlan &pl, const CUtensorMap &tw, const CUtensorMap &ts,
+                       const CUtensorMap &tb, const CUtensorMap &tx, cudaStream_t stream);
+
+}  // namespace gemv
+}  // namespace aq

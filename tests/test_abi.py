@@ -102,8 +102,9 @@ def test_stats_interface():
     (1, 4096, 4096, 4, aq.AQ_VARIANT_GEMV),
     (1, 10240, 5120, 3, aq.AQ_VARIANT_GEMV),
     (8, 10240, 5120, 3, aq.AQ_VARIANT_GEMV),
-    (9, 10240, 5120, 3, aq.AQ_VARIANT_QMV),
-    (16, 10240, 5120, 3, aq.AQ_VARIANT_QMV),
+    (9, 10240, 5120, 3, aq.AQ_VARIANT_GEMV),
+    (16, 10240, 5120, 3, aq.AQ_VARIANT_GEMV),
+    (17, 10240, 5120, 3, aq.AQ_VARIANT_TC),
     (1, 5120, 13824, 4, aq.AQ_VARIANT_QMV),    # 35 MB of weights at M = 1
     (1, 13824, 5120, 4, aq.AQ_VARIANT_QMV),
     (8, 13824, 5120, 4, aq.AQ_VARIANT_GEMV),
@@ -124,9 +125,10 @@ def test_select_invalid():
 
 
 @pytest.mark.parametrize("M,N,K,bits,want", [
-    (1, 4096, 4096, 4, "rows/cta=27 passes=1 tiles=2 groups/stage=32 stages=2 ring=2 x=whole grid=152"),
+    (1, 4096, 4096, 4, "rows/cta=27 passes=1 tiles=2 colblocks=1 groups/stage=32 stages=2 ring=2 x=whole grid=152"),
     (2, 28672, 8192, 4, "rows/cta=190 passes=2"),
     (8, 600, 13824, 4, "x=ring"),
+    (16, 10240, 5120, 3, "rows/cta=68 passes=2 tiles=3 colblocks=2"),
 ])
 def test_gemv_plan(M, N, K, bits, want):
     # The resident kernel's plan on a 152-SM GB300 (the SM count the library
