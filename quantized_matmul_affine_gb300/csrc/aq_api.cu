@@ -93,18 +93,18 @@ static int gemv_max_m() {
     return v;
 }
 
-// Single activation rows over more than this many bytes of packed weights
-// go to the streaming small-M kernel: there the resident kernel's per-SM
-// decode work outweighs its overlap of consecutive calls (measured on GB300:
-// 13824x5120 and 5120x13824 at 4 bits, 35 MB, are 4-15% faster on qmv; the
-// 20 MB 3-bit 10240x5120 layer is 22% faster on gemv).
-constexpr int64_t kGemvM1MaxWeightBytes = 24ll << 20;
+// A single activation row goes to the resident kernel only when its CTAs
+// take all their rows in one pass (N <= 128 rows x SMs); past that the
+// streaming small-M kernel keeps pace or wins (measured on GB300 at 4 bits,
+// M = 1: gemv is 11-29% faster on 13824x5120 and 4096x14336, within 1% on
+// 5120x13824; two passes: 5% faster on 28672x8192 but 8% slower on
+// 32000x4096; 128256x4096 and 57344x8192: 18-23% slower).
+static bool gemv_for_m1(const MatmulArgs &a) { return a.N <= 128ll * num_sms(); }
 
 // The dispatch rule.  Returns the variant for the arguments (alignment
 // included), never AQ_VARIANT_AUTO.
 static int choose(const MatmulArgs &a) {
-    const int64_t wbytes = a.N * a.K * a.bits / 8;
-    const bool gemv_first = a.M > 1 || wbytes <= kGemvM1MaxWeightBytes;
+    const bool gemv_first = a.M > 1 || gemv_for_m1(a);
     if (a.M <= gemv_max_m() && gemv_first && gemv_supported(a)) return AQ_VARIANT_GEMV;
     const bool qmv = qmv_supported(a);
     const bool tc = tc_supported(a);

@@ -12,6 +12,11 @@ namespace {
 
 uint32_t round_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
+// Largest whole-x footprint (rows of x, group sums and scales) kept in
+// shared memory; beyond it x is streamed with the weights.  A 13824-long
+// row (27.6 KB + 13.8 KB of sums and scales) still fits.
+constexpr size_t kXWholeMax = 48 * 1024;
+
 // Shared-memory budget of a plan (AQ_GEMV_SMEM_KB overrides it for
 // experiments).
 size_t smem_budget() {
@@ -71,66 +76,68 @@ bool gemv_plan(const MatmulArgs &a, GemvPlan &pl) {
     pl.bits = B;
     pl.bf16 = a.dtype == AQ_BF16;
     const uint32_t red_bytes = (uint32_t)kConsumers * q.tiles * MB * 32 * 4 * 4;
-    q.x_slot_bytes = round_up((uint32_t)a.M * kXPitch + 32u, 16u);
 
-    // The widest stage (most groups per warp) that divides K and keeps at
-    // least three stages in the ring (or the whole of K), else two.
+    // The widest stage (most groups per warp) that keeps at least three
+    // stages in the ring (or the whole of K), else two; x whole in shared
+    // memory (single column block only) before x staged with the weights.
     for (int want = 3; want >= 2; --want) {
-        for (int wps = max_wps(q.tiles, MB); wps >= 1; wps /= 2) {
-            const int sg = 8 * wps;
-            if (G % sg) continue;
-            q.sg = sg;
-            q.n_stages = G / sg;
-            const uint32_t nb = (uint32_t)sg / 4;
-            // codes [nb][pr][box] and scales, biases [sg/8][pr][8], each with
-            // room for the padded rows of the last block
-            const uint32_t wbytes = round_up((nb * (uint32_t)pr + rows_pad - (uint32_t)pr) * box,
-                                             B == 4 ? 1024u : 128u);
-            const uint32_t sbytes =
-                round_up(((nb / 2 - 1) * (uint32_t)pr + rows_pad) * 16u, 128u);
-            q.off_sc = wbytes;
-            q.off_bi = wbytes + sbytes;
-            // two column blocks: x of the stage, [sg][16 rows][128 B], 1024-aligned
-            const uint32_t xst = MB > 1 ? (uint32_t)sg * 16u * 128u : 0u;
-            q.off_xst = round_up(q.off_bi + sbytes, 1024u);
-            q.slot_bytes = round_up(q.off_xst + xst, 1024u);
-            q.stage_tx = nb * (uint32_t)pr * box + 2u * (uint32_t)pr * (uint32_t)sg * 2u + xst;
-            const int total = passes * q.n_stages;
-            for (int whole = MB > 1 ? 0 : 1; whole >= 0; --whole) {
-                q.x_whole = whole;
-                q.x_row_pitch = (uint32_t)a.K * 2u + 16u;
-                q.x_warp_bytes = round_up((uint32_t)kXRing * q.x_slot_bytes, 128u);
-                const size_t x_bytes =
-                    MB > 1  ? 0
-                    : whole ? round_up(q.x_row_pitch * (uint32_t)a.M, 128u) + (size_t)G * 32
-                            : (size_t)kConsumers * q.x_warp_bytes;
-                if (whole && x_bytes > 40 * 1024) continue;
-                const size_t bars = 2 * 8 * (size_t)total + 16 + 16;
-                // With one pass the partial tiles reuse the ring if it is large enough.
-                for (int alias = passes == 1 ? 1 : 0; alias >= 0; --alias) {
-                    const size_t fixed =
-                        x_bytes + (alias ? 0 : red_bytes) + bars + 1024 /* alignment */;
-                    if (fixed >= budget) continue;
-                    const int ring =
-                        (int)std::min<size_t>((size_t)total, (budget - fixed) / q.slot_bytes);
-                    if (ring < std::min(want, total)) continue;
-                    if (alias && (size_t)ring * q.slot_bytes < red_bytes) continue;
-                    q.ring = ring;
-                    q.red_alias = alias;
-                    size_t off = (size_t)ring * q.slot_bytes;
-                    q.off_x = (uint32_t)off;
-                    q.off_xs = (uint32_t)(off + round_up(q.x_row_pitch * (uint32_t)a.M, 128u));
-                    off += x_bytes;
-                    q.off_red = alias ? 0u : (uint32_t)off;
-                    off += alias ? 0 : red_bytes;
-                    q.off_bar = (uint32_t)off;
-                    off += 2 * 8 * (size_t)ring + 16 + 16;
-                    pl.smem = off + 1024;
-                    q.x = a.x;
-                    q.y = a.out;
-                    q.err = nullptr;
-                    pl.wps = wps;
-                    if (pl.smem <= budget) return true;
+        for (int whole = MB > 1 ? 0 : 1; whole >= 0; --whole) {
+            for (int wps = max_wps(q.tiles, MB); wps >= 1; wps /= 2) {
+                const int sg = 8 * wps;
+                // a last stage past the end of K reads zeros and its groups are skipped
+                q.sg = sg;
+                q.n_stages = (G + sg - 1) / sg;
+                const uint32_t nb = (uint32_t)sg / 4;
+                // codes [nb][pr][box] and scales, biases [sg/8][pr][8], each with
+                // room for the padded rows of the last block
+                const uint32_t wbytes = round_up((nb * (uint32_t)pr + rows_pad - (uint32_t)pr) * box,
+                                                 B == 4 ? 1024u : 128u);
+                const uint32_t sbytes =
+                    round_up(((nb / 2 - 1) * (uint32_t)pr + rows_pad) * 16u, 128u);
+                q.off_sc = wbytes;
+                q.off_bi = wbytes + sbytes;
+                const int total = passes * q.n_stages;
+                {
+                    q.x_whole = whole;
+                    q.x_row_pitch = (uint32_t)a.K * 2u + 16u;
+                    // staged x: the stage's groups x M rows x 128 B, 1024-aligned
+                    q.x_rows = (int)a.M;
+                    const uint32_t xst = whole ? 0u : (uint32_t)sg * (uint32_t)a.M * 128u;
+                    q.off_xst = round_up(q.off_bi + sbytes, 1024u);
+                    q.slot_bytes = round_up(q.off_xst + xst, 1024u);
+                    q.stage_tx =
+                        nb * (uint32_t)pr * box + 2u * (uint32_t)pr * (uint32_t)sg * 2u + xst;
+                    // whole x: rows at 2K + 16 bytes, then group sums and scales [2][G][8]
+                    const size_t x_bytes =
+                        whole ? round_up(q.x_row_pitch * (uint32_t)a.M, 128u) + (size_t)G * 64 : 0;
+                    if (whole && x_bytes > kXWholeMax) continue;
+                    const size_t bars = 2 * 8 * (size_t)total + 16 + 16;
+                    // With one pass the partial tiles reuse the ring if it is large enough.
+                    for (int alias = passes == 1 ? 1 : 0; alias >= 0; --alias) {
+                        const size_t fixed =
+                            x_bytes + (alias ? 0 : red_bytes) + bars + 1024 /* alignment */;
+                        if (fixed >= budget) continue;
+                        const int ring =
+                            (int)std::min<size_t>((size_t)total, (budget - fixed) / q.slot_bytes);
+                        if (ring < std::min(want, total)) continue;
+                        if (alias && (size_t)ring * q.slot_bytes < red_bytes) continue;
+                        q.ring = ring;
+                        q.red_alias = alias;
+                        size_t off = (size_t)ring * q.slot_bytes;
+                        q.off_x = (uint32_t)off;
+                        q.off_xs = (uint32_t)(off + round_up(q.x_row_pitch * (uint32_t)a.M, 128u));
+                        off += x_bytes;
+                        q.off_red = alias ? 0u : (uint32_t)off;
+                        off += alias ? 0 : red_bytes;
+                        q.off_bar = (uint32_t)off;
+                        off += 2 * 8 * (size_t)ring + 16 + 16;
+                        pl.smem = off + 1024;
+                        q.x = a.x;
+                        q.y = a.out;
+                        q.err = nullptr;
+                        pl.wps = wps;
+                        if (pl.smem <= budget) return true;
+                    }
                 }
             }
         }
@@ -142,10 +149,10 @@ template <int B, bool BF16, int TILES>
 cudaError_t launch_wps(const GemvPlan &pl, const CUtensorMap &tw, const CUtensorMap &ts,
                        const CUtensorMap &tb, const CUtensorMap &tx, cudaStream_t s) {
     if constexpr (TILES <= 2)
-        if (pl.wps == 4) return launch_t<B, BF16, TILES, 4, 1>(pl, tw, ts, tb, tx, s);
+        if (pl.wps == 4) return launch_t<B, BF16, TILES, 4, 1, false>(pl, tw, ts, tb, tx, s);
     if constexpr (TILES <= 4)
-        if (pl.wps == 2) return launch_t<B, BF16, TILES, 2, 1>(pl, tw, ts, tb, tx, s);
-    return launch_t<B, BF16, TILES, 1, 1>(pl, tw, ts, tb, tx, s);
+        if (pl.wps == 2) return launch_t<B, BF16, TILES, 2, 1, false>(pl, tw, ts, tb, tx, s);
+    return launch_t<B, BF16, TILES, 1, 1, false>(pl, tw, ts, tb, tx, s);
 }
 
 template <int B, bool BF16>
@@ -193,11 +200,12 @@ cudaError_t gemv_launch(const MatmulArgs &a) {
     const uint32_t sbox[3] = {8, pr, sg / 8};
     CUtensorMap tw, ts, tb;
     CUtensorMap tx = {};
-    if (pl.mb > 1) {
-        // x as [G][M][64] elements: one box = the stage's groups x 16 rows
+    const bool staged = !pl.prm.x_whole;
+    if (staged) {
+        // x as [G][M][64] elements: one box = the stage's groups x M rows
         const uint64_t xdims[3] = {64, (uint64_t)a.M, G};
         const uint64_t xstrides[2] = {(uint64_t)a.K * 2, 128};
-        const uint32_t xbox[3] = {64, 16, sg};
+        const uint32_t xbox[3] = {64, (uint32_t)a.M, sg};
         if (!tmap_encode(&tx, a.dtype == AQ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                          3, a.x, xdims, xstrides, xbox, CU_TENSOR_MAP_SWIZZLE_128B))
@@ -213,7 +221,8 @@ cudaError_t gemv_launch(const MatmulArgs &a) {
                      CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     if (pl.mb > 1) return gemv::launch_mb2(pl, tw, ts, tb, tx, a.stream);
-    if (pl.mb == 1) tx = tw;  // unused by one-column-block kernels
+    if (staged) return gemv::launch_staged1(pl, tw, ts, tb, tx, a.stream);
+    tx = tw;  // unused when x is whole
     const bool bf = a.dtype == AQ_BF16;
     if (a.bits == 3)
         return bf ? gemv::launch_tiles<3, true>(pl, tw, ts, tb, tx, a.stream)
@@ -230,7 +239,7 @@ int gemv_describe(const MatmulArgs &a, char *buf, int len) {
                     "gemv rows/cta=%d passes=%d tiles=%d colblocks=%d groups/stage=%d stages=%d "
                     "ring=%d x=%s grid=%d smem=%zu",
                     q.rows_cta, q.passes, q.tiles, pl.mb, q.sg, q.n_stages, q.ring,
-                    pl.mb > 1 ? "staged" : q.x_whole ? "whole" : "ring",
+                    q.x_whole ? "whole" : "staged",
                     pl.grid, pl.smem);
 }
 

@@ -35,12 +35,12 @@
 //   * Eight consumer warps.  Warp w takes SG/8 consecutive groups of every
 //     stage, for all the block's 16-row tiles (the tile count is a template
 //     parameter, so the tiles interleave freely).
-//   * x (one 8-column block): one bulk copy per activation row once the grid
-//     dependency resolves, rewritten in place into B-fragment order with the
-//     group sums; or per-warp cp.async rings when it does not fit.  x (two
-//     blocks): a fourth producer lane streams it with the weights, one
-//     3-D TMA box of the stage's groups x 16 rows per stage (rows past M read
-//     as zero), and each warp builds its fragments and sums per group.
+//   * x, when M x K fits in 40 KB: one bulk copy per activation row once the
+//     grid dependency resolves, rewritten in place into B-fragment order with
+//     the group sums.  Otherwise ("staged"): a fourth producer lane streams it
+//     with the weights, one 3-D TMA box of the stage's groups x 8 or 16 rows
+//     per stage (rows past M read as zero), and each warp builds its
+//     fragments and sums per group.
 //   * Codes decode into MMA A fragments (weights are the 16-row A operand)
 //     with one shift and one LOP3 per two codes (4-bit fp16: one AND per
 //     two codes plus a shift per word, the codes staying in place), each
@@ -79,7 +79,6 @@ constexpr int kXPitch = 144;     // bytes per activation row in an x slot (128 +
 // An x slot holds one group of every activation row (M rows at kXPitch),
 // rewritten in place into MMA B-fragment order, then the group's sums of x
 // for the 8 MMA columns (32 bytes).
-constexpr int kXRing = 4;        // x slots per warp when the warp's x is not kept whole
 constexpr size_t kSmemBudget = 112 * 1024;  // two CTAs (two calls) per SM
 
 struct GemvParams {
@@ -94,15 +93,14 @@ struct GemvParams {
     int sg;          // groups per stage (8 x groups per warp)
     int n_stages;    // G / sg
     int ring;        // weight stages in the ring
-    int x_whole;     // 1: all of x in shared memory (one bulk copy per row); 0: per-warp rings
+    int x_whole;     // 1: all of x in shared memory (one bulk copy per row); 0: staged per stage
     int red_alias;   // 1: the partial-tile buffer reuses the ring (single pass)
     uint32_t slot_bytes, off_sc, off_bi;  // inside a ring slot (codes at 0)
     uint32_t off_x, off_red, off_bar;
-    uint32_t x_warp_bytes;  // x region of one warp
-    uint32_t x_slot_bytes;  // one x slot (M rows + the 8 group sums)
     uint32_t x_row_pitch;   // whole x: bytes per activation row (2K + 16)
-    uint32_t off_xs;        // whole x: group sums [G][8] floats
-    uint32_t off_xst;       // staged x (two column blocks): box inside a ring slot
+    uint32_t off_xs;        // whole x: group sums [G][8] floats, then scale factors [G][8]
+    uint32_t off_xst;       // staged x: box inside a ring slot
+    int x_rows;             // staged x: rows per group in the box (= M)
     uint32_t stage_tx;      // bytes one stage brings in
 };
 
@@ -284,15 +282,14 @@ __device__ __forceinline__ void store_y<__nv_bfloat16>(__nv_bfloat16 *p, float v
     *p = __float2bfloat16_rn(v);
 }
 
-template <int B, bool BF16, int TILES, int WPS, int MB>
+template <int B, bool BF16, int TILES, int WPS, int MB, bool XST>
 __global__ void __launch_bounds__(kGemvThreads, 2)
     gemv_kernel(const __grid_constant__ GemvParams p, const __grid_constant__ CUtensorMap tm_w,
                 const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_b,
                 const __grid_constant__ CUtensorMap tm_x) {
-    constexpr bool kXStage = MB > 1;  // x streamed per stage by a fourth producer lane
+    constexpr bool kXStage = XST;  // x streamed per stage by a fourth producer lane
     using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
     constexpr int kBox = B == 4 ? 128 : 96;  // bytes of a row in one column block (4 groups)
-    constexpr uint32_t kMagic = BF16 ? 0x43004300u : 0u;
     extern __shared__ uint8_t smem_raw[];
     // Align to 1024 bytes by an offset from the __shared__ array itself, so
     // that every access below stays a shared-memory access (32-bit address).
@@ -386,10 +383,20 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
     // (a stage is 8*WPS groups), for every 16-row tile of the pass; the
     // WPS x TILES units of a stage are unrolled.
     // ----------------------------------------------------------------------
-    constexpr bool kInPlace = (B == 4) && !BF16;
-    // fp16 x: the products carry 2^-24, which the group sums of x take too;
-    // y = 2^24 * acc.
-    constexpr float kXsScale = BF16 ? 1.f : 5.9604644775390625e-08f;
+    // Whole x at 4 bits ("converted"): x is rewritten as fp16 with a
+    // power-of-two scale per (group, row), 2^(14 - floor(log2 max|x|)), and
+    // the x paired with codes at bit 4 carries a further 2^-4; the codes then
+    // stay in place (exact fp16 subnormals) and one MMA chain gives
+    // scale_x * 2^-24 * sum(q x); the epilogue multiplies by the group's
+    // scale times the inverse power of two.  Otherwise fp16 x is used as it
+    // is (codes at bit 4 in a second chain) and bf16 x with 128 + q codes.
+    constexpr bool kConv = (B == 4) && !XST;
+    constexpr bool kMmaBf16 = BF16 && !kConv;
+    constexpr bool kInPlace = (B == 4) && !kMmaBf16;
+    constexpr uint32_t kMagicDec = kMmaBf16 ? 0x43004300u : 0u;
+    // fp16 MMAs: the products carry 2^-24, which the group sums of x take
+    // too; y = 2^24 * acc.
+    constexpr float kXsScale = kMmaBf16 ? 1.f : 5.9604644775390625e-08f;
     const int g = lane >> 2, c = lane & 3;
     // MMA row g (and g + 8) reads tile row pg (and pg + 8): rows 0,2,4,6 for
     // the lanes of one half-warp and 1,3,5,7 for the other, so that the
@@ -397,9 +404,6 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
     const int pg = ((g & 3) << 1) | (g >> 2);
     const int M = p.M;
     const int64_t K = p.K;
-    const int n_wg = p.n_stages * WPS;  // groups of one warp over K
-    uint8_t *xw = smem + p.off_x + (size_t)warp * p.x_warp_bytes;
-    const uint32_t xsb = p.x_slot_bytes;
     const int xrow = min(g, M - 1);     // columns past M repeat row M-1 (never stored)
 
     // 3-bit: where this lane's 48-bit span starts (word, byte) in a group.
@@ -416,44 +420,17 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
     grid_dependency_wait();
 
     const T *xg = static_cast<const T *>(p.x);
-    // The warp's k-th group of every activation row: 128 bytes per row.
-    auto issue_x = [&](int k, int xslot) {
-        const int gg = (k / WPS) * (8 * WPS) + warp * WPS + (k % WPS);
-        uint8_t *dst = xw + (size_t)xslot * xsb;
-        const T *src = xg + (int64_t)gg * 64;
-        for (int q = lane; q < M * 8; q += 32) {
-            const int m = q >> 3, ch = q & 7;
-            cp_async16(dst + m * kXPitch + ch * 16, src + (int64_t)m * K + ch * 8, 16u);
-        }
-    };
-    const uint32_t one = BF16 ? 0x3F803F80u : 0x3C003C00u;
+    const uint32_t one = kMmaBf16 ? 0x3F803F80u : 0x3C003C00u;
     const uint32_t ones[4] = {one, one, one, one};
-    // Rewrite a landed x slot in place into B-fragment order and store the
-    // group sums of its 8 columns (the slot's tail).  A lane touches only
-    // its own 32 bytes of its own row, so slots need no warp barrier between
-    // them and consecutive ones overlap; lanes past row M-1 feed zeros.
-    auto prep_x = [&](int xslot) {
-        uint8_t *sl = xw + (size_t)xslot * xsb;
-        uint32_t bx[4][2] = {{0u, 0u}, {0u, 0u}, {0u, 0u}, {0u, 0u}};
-        uint4 *row = reinterpret_cast<uint4 *>(sl + g * kXPitch + 32 * c);
-        if (g < M) x_frags<B>(row[0], row[1], bx);
-        float xsum[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) mma16816<BF16>(xsum, ones, bx[q][0], bx[q][1]);
-        if (g < M) {
-            row[0] = make_uint4(bx[0][0], bx[0][1], bx[1][0], bx[1][1]);
-            row[1] = make_uint4(bx[2][0], bx[2][1], bx[3][0], bx[3][1]);
-        }
-        if (g == 0)
-            *reinterpret_cast<float2 *>(sl + M * kXPitch + 8 * c) =
-                make_float2(xsum[0] * kXsScale, xsum[1] * kXsScale);
-    };
     // Whole x: one bulk copy per activation row, then all consumer threads
     // rewrite it in place into B-fragment order (one 32-byte quarter of a
-    // group each) and take the group sums, [G][8] floats.
+    // group each) and take the group sums, [G][8] floats (and, converted,
+    // the inverse scales, [G][8] floats).
     uint8_t *xraw = smem + p.off_x;
     float *xsg = reinterpret_cast<float *>(smem + p.off_xs);
-    if (!kXStage && p.x_whole) {
+    const int G = (int)(K / 64);
+    float *xeg = xsg + G * 8;
+    if constexpr (!kXStage) {
         if (threadIdx.x == 0) {
             mbar_arrive_expect_tx(x_full, (uint32_t)(M * K * 2));
             for (int m = 0; m < M; ++m)
@@ -463,32 +440,56 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
         gemv_wait(x_full, 0, flag, p.err, ERR_GEMV_FULL);
         if (lane == 0) mbar_arrive(x_landed);
         launch_dependents();
-        const int G = (int)(K / 64);
         for (int m = 0; m < M; ++m) {
             for (int u = threadIdx.x; u < G * 4; u += kConsumers * 32) {
                 const int gg = u >> 2, cq = u & 3;
                 uint4 *q = reinterpret_cast<uint4 *>(xraw + m * p.x_row_pitch + gg * 128 + 32 * cq);
                 const uint4 u0 = q[0], u1 = q[1];
                 const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-                float part[8];
+                float f[16];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     if constexpr (BF16) {
-                        part[i] = __uint_as_float(w[i] << 16) + __uint_as_float(w[i] & 0xFFFF0000u);
+                        f[2 * i] = __uint_as_float(w[i] << 16);
+                        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
                     } else {
-                        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
-                        part[i] = f.x + f.y;
+                        const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+                        f[2 * i] = v.x;
+                        f[2 * i + 1] = v.y;
                     }
                 }
+                float part[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) part[i] = f[2 * i] + f[2 * i + 1];
                 float sum = ((part[0] + part[1]) + (part[2] + part[3])) +
                             ((part[4] + part[5]) + (part[6] + part[7]));
-                uint32_t bx[4][2];
-                x_frags<B>(u0, u1, bx);
-                q[0] = make_uint4(bx[0][0], bx[0][1], bx[1][0], bx[1][1]);
-                q[1] = make_uint4(bx[2][0], bx[2][1], bx[3][0], bx[3][1]);
                 // the four quarters of a group are four adjacent lanes
                 sum += __shfl_xor_sync(0xffffffffu, sum, 1);
                 sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+                if constexpr (kConv) {
+                    float mx = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) mx = fmaxf(mx, fabsf(f[i]));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                    // 2^sh with max|x| * 2^sh in [2^14, 2^15): exact, in range
+                    const int ex = mx > 0.f ? (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127 : 0;
+                    const int sh = 14 - ex;
+                    const float sc = __uint_as_float((uint32_t)(127 + sh) << 23);
+                    const float s4 = __uint_as_float((uint32_t)(127 + sh - 4) << 23);
+                    q[0] = make_uint4(pack_half2(f[0] * sc, f[4] * sc), pack_half2(f[2] * sc, f[6] * sc),
+                                      pack_half2(f[8] * sc, f[12] * sc),
+                                      pack_half2(f[10] * sc, f[14] * sc));
+                    q[1] = make_uint4(pack_half2(f[1] * s4, f[5] * s4), pack_half2(f[3] * s4, f[7] * s4),
+                                      pack_half2(f[9] * s4, f[13] * s4),
+                                      pack_half2(f[11] * s4, f[15] * s4));
+                    if (cq == 0) xeg[gg * 8 + m] = __uint_as_float((uint32_t)(127 - sh) << 23);
+                } else {
+                    uint32_t bx[4][2];
+                    x_frags<B>(u0, u1, bx);
+                    q[0] = make_uint4(bx[0][0], bx[0][1], bx[1][0], bx[1][1]);
+                    q[1] = make_uint4(bx[2][0], bx[2][1], bx[3][0], bx[3][1]);
+                }
                 if (cq == 0) xsg[gg * 8 + m] = sum * kXsScale;
             }
         }
@@ -509,12 +510,6 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) acc[t][mb][i] = 0.f;
 
-        if (!kXStage && !p.x_whole) {
-            for (int k = 0; k < kXRing - 1; ++k) {
-                if (k < n_wg) issue_x(k, k);
-                cp_async_commit();
-            }
-        }
         for (int s = 0; s < p.n_stages; ++s) {
             const uint8_t *st = smem + (size_t)slot * p.slot_bytes;
             // (no check of the error flag here: the wait is bounded by itself)
@@ -530,63 +525,51 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
             const int q7 = ((j0 >> 2) * pr + pg) & 7;
             const uint8_t *sc0 = st + p.off_sc + ((j0 >> 3) * pr) * 16 + (j0 & 7) * 2;
             const uint8_t *bi0 = st + p.off_bi + ((j0 >> 3) * pr) * 16 + (j0 & 7) * 2;
+            const int gg0 = s * (8 * WPS) + j0;  // global group of unit i = 0
 #pragma unroll
             for (int i = 0; i < WPS; ++i) {
-                const int k = s * WPS + i;
-                int xslot = k;
-                if (!kXStage && !p.x_whole) {
-                    xslot = k % kXRing;
-                    if (k + kXRing - 1 < n_wg) issue_x(k + kXRing - 1, (k + kXRing - 1) % kXRing);
-                    cp_async_commit();
-                    cp_async_wait<kXRing - 1>();
-                    __syncwarp();
-                    if (pass == 0 && k == 0) {
-                        if (lane == 0) mbar_arrive(x_landed);
-                        launch_dependents();
-                    }
-                    prep_x(xslot);
-                    __syncwarp();
-                }
+                if (WPS > 1 && gg0 + i >= G) continue;  // past the end of K (last stage)
                 // B fragments and group sums of columns 2c, 2c+1 of each block
                 uint32_t bx[MB][4][2];
                 float xs0[MB], xs1[MB];
+                float e0 = 1.f, e1 = 1.f;  // converted x: inverse scales of columns 2c, 2c+1
                 if constexpr (kXStage) {
-                    // raw x of the group: [8*MB rows][128 bytes], 128-byte swizzle
+                    // raw x of the group: [M rows][128 bytes], 128-byte swizzle; the
+                    // columns past M take zeros
 #pragma unroll
                     for (int mb = 0; mb < MB; ++mb) {
-                        const int seg = (j0 + i) * (8 * MB) + 8 * mb + g;
+                        const int row = 8 * mb + g;
+                        const int seg = (j0 + i) * p.x_rows + row;
                         const uint8_t *xr = st + p.off_xst + seg * 128;
-                        const uint4 u0 =
-                            *reinterpret_cast<const uint4 *>(xr + (((2 * c) ^ (seg & 7)) << 4));
-                        const uint4 u1 =
-                            *reinterpret_cast<const uint4 *>(xr + (((2 * c + 1) ^ (seg & 7)) << 4));
+                        uint4 u0 = make_uint4(0u, 0u, 0u, 0u), u1 = u0;
+                        if (row < p.x_rows) {
+                            u0 = *reinterpret_cast<const uint4 *>(xr + (((2 * c) ^ (seg & 7)) << 4));
+                            u1 = *reinterpret_cast<const uint4 *>(xr +
+                                                                  (((2 * c + 1) ^ (seg & 7)) << 4));
+                        }
                         x_frags<B>(u0, u1, bx[mb]);
                         float xsum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
-                            mma16816<BF16>(xsum, ones, bx[mb][q][0], bx[mb][q][1]);
+                            mma16816<kMmaBf16>(xsum, ones, bx[mb][q][0], bx[mb][q][1]);
                         xs0[mb] = xsum[0] * kXsScale;
                         xs1[mb] = xsum[1] * kXsScale;
                     }
                 } else {
-                    const uint8_t *fr;
-                    const float *xsp;
-                    if (p.x_whole) {
-                        const int gg = s * (8 * WPS) + j0 + i;
-                        fr = xraw + xrow * p.x_row_pitch + gg * 128 + 32 * c;
-                        xsp = xsg + gg * 8 + 2 * c;
-                    } else {
-                        const uint8_t *sl = xw + (size_t)xslot * xsb;
-                        fr = sl + xrow * kXPitch + 32 * c;
-                        xsp = reinterpret_cast<const float *>(sl + M * kXPitch) + 2 * c;
-                    }
+                    const int gg = gg0 + i;
+                    const uint8_t *fr = xraw + xrow * p.x_row_pitch + gg * 128 + 32 * c;
                     const uint4 u0 = *reinterpret_cast<const uint4 *>(fr);
                     const uint4 u1 = *reinterpret_cast<const uint4 *>(fr + 16);
                     bx[0][0][0] = u0.x; bx[0][0][1] = u0.y; bx[0][1][0] = u0.z; bx[0][1][1] = u0.w;
                     bx[0][2][0] = u1.x; bx[0][2][1] = u1.y; bx[0][3][0] = u1.z; bx[0][3][1] = u1.w;
-                    const float2 xs = *reinterpret_cast<const float2 *>(xsp);
+                    const float2 xs = *reinterpret_cast<const float2 *>(xsg + gg * 8 + 2 * c);
                     xs0[0] = xs.x;
                     xs1[0] = xs.y;
+                    if constexpr (kConv) {
+                        const float2 e = *reinterpret_cast<const float2 *>(xeg + gg * 8 + 2 * c);
+                        e0 = e.x;
+                        e1 = e.y;
+                    }
                 }
                 const int gi = (j0 + i) & 3;  // group within its column block
                 // 128-byte swizzle: 16-byte chunk ch of a row segment q sits at
@@ -599,44 +582,61 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
                     if constexpr (B == 4) {
                         const uint2 qa = *reinterpret_cast<const uint2 *>(cb0 + ra * 128 + off4);
                         const uint2 qb = *reinterpret_cast<const uint2 *>(cb0 + rb * 128 + off4);
-                        decode4<kInPlace, kMagic>(qa.x, qa.y, PA);
-                        decode4<kInPlace, kMagic>(qb.x, qb.y, PB);
+                        decode4<kInPlace, kMagicDec>(qa.x, qa.y, PA);
+                        decode4<kInPlace, kMagicDec>(qb.x, qb.y, PB);
                     } else {
                         const uint32_t *pa =
                             reinterpret_cast<const uint32_t *>(cb0 + ra * 96 + 24 * gi) + wi3;
                         const uint32_t *pb =
                             reinterpret_cast<const uint32_t *>(cb0 + rb * 96 + 24 * gi) + wi3;
-                        decode3<kMagic>(pa[0], pa[1], sel0, sel2, PA);
-                        decode3<kMagic>(pb[0], pb[1], sel0, sel2, PB);
+                        decode3<kMagicDec>(pa[0], pa[1], sel0, sel2, PA);
+                        decode3<kMagicDec>(pb[0], pb[1], sel0, sel2, PB);
                     }
                     const float sa = __half2float(*reinterpret_cast<const __half *>(sc0 + ra * 16 + 2 * i));
                     const float sb = __half2float(*reinterpret_cast<const __half *>(sc0 + rb * 16 + 2 * i));
                     float ba = __half2float(*reinterpret_cast<const __half *>(bi0 + ra * 16 + 2 * i));
                     float bb = __half2float(*reinterpret_cast<const __half *>(bi0 + rb * 16 + 2 * i));
-                    if constexpr (BF16 && !kInPlace) {
-                        ba = fmaf(-128.f, sa, ba);
-                        bb = fmaf(-128.f, sb, bb);
-                    }
-                    // steps 2-3 hold the codes at bit 4 (16 q * 2^-24) in the in-place decode
-                    const float sa4 = kInPlace ? sa * 0.0625f : sa, sb4 = kInPlace ? sb * 0.0625f : sb;
-#pragma unroll
-                    for (int mb = 0; mb < MB; ++mb) {
-                        // two independent MMA chains (steps 0-1 and 2-3)
-                        float da[4] = {0.f, 0.f, 0.f, 0.f}, db[4] = {0.f, 0.f, 0.f, 0.f};
+                    if constexpr (kConv) {
+                        // one chain: the x of codes at bit 4 already carries 2^-4
+                        float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             uint32_t af[4];
                             step_frags<B>(PA, PB, q, af);
-                            if (q < 2)
-                                mma16816<BF16>(da, af, bx[mb][q][0], bx[mb][q][1]);
-                            else
-                                mma16816<BF16>(db, af, bx[mb][q][0], bx[mb][q][1]);
+                            mma16816<false>(d, af, bx[0][q][0], bx[0][q][1]);
                         }
-                        float *a4 = acc[t][mb];
-                        a4[0] = fmaf(sa, da[0], fmaf(sa4, db[0], fmaf(ba, xs0[mb], a4[0])));
-                        a4[1] = fmaf(sa, da[1], fmaf(sa4, db[1], fmaf(ba, xs1[mb], a4[1])));
-                        a4[2] = fmaf(sb, da[2], fmaf(sb4, db[2], fmaf(bb, xs0[mb], a4[2])));
-                        a4[3] = fmaf(sb, da[3], fmaf(sb4, db[3], fmaf(bb, xs1[mb], a4[3])));
+                        float *a4 = acc[t][0];
+                        a4[0] = fmaf(sa * e0, d[0], fmaf(ba, xs0[0], a4[0]));
+                        a4[1] = fmaf(sa * e1, d[1], fmaf(ba, xs1[0], a4[1]));
+                        a4[2] = fmaf(sb * e0, d[2], fmaf(bb, xs0[0], a4[2]));
+                        a4[3] = fmaf(sb * e1, d[3], fmaf(bb, xs1[0], a4[3]));
+                    } else {
+                        if constexpr (kMmaBf16) {
+                            ba = fmaf(-128.f, sa, ba);
+                            bb = fmaf(-128.f, sb, bb);
+                        }
+                        // steps 2-3 hold the codes at bit 4 (16 q * 2^-24) in the in-place decode
+                        const float sa4 = kInPlace ? sa * 0.0625f : sa;
+                        const float sb4 = kInPlace ? sb * 0.0625f : sb;
+#pragma unroll
+                        for (int mb = 0; mb < MB; ++mb) {
+                            // two independent MMA chains (steps 0-1 and 2-3)
+                            float da[4] = {0.f, 0.f, 0.f, 0.f}, db[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                uint32_t af[4];
+                                step_frags<B>(PA, PB, q, af);
+                                if (q < 2)
+                                    mma16816<kMmaBf16>(da, af, bx[mb][q][0], bx[mb][q][1]);
+                                else
+                                    mma16816<kMmaBf16>(db, af, bx[mb][q][0], bx[mb][q][1]);
+                            }
+                            float *a4 = acc[t][mb];
+                            a4[0] = fmaf(sa, da[0], fmaf(sa4, db[0], fmaf(ba, xs0[mb], a4[0])));
+                            a4[1] = fmaf(sa, da[1], fmaf(sa4, db[1], fmaf(ba, xs1[mb], a4[1])));
+                            a4[2] = fmaf(sb, da[2], fmaf(sb4, db[2], fmaf(bb, xs0[mb], a4[2])));
+                            a4[3] = fmaf(sb, da[3], fmaf(sb4, db[3], fmaf(bb, xs1[mb], a4[3])));
+                        }
                     }
                 }
             }
@@ -672,12 +672,11 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
             float v = 0.f;
             for (int w = 0; w < kConsumers; ++w)
                 v += red[(((w * TILES + t) * MB + mb) * 32 + ln) * 4 + i];
-            if constexpr (!BF16) v *= 16777216.f;  // 2^24
+            if constexpr (!kMmaBf16) v *= 16777216.f;  // 2^24
             store_y<T>(&y[(int64_t)m * p.N + r0 + r], v);
         }
         consumers_sync();  // the buffer is rewritten by the next pass
     }
-    cp_async_wait<0>();
 }
 
 // ---------------------------------------------------------------------------
@@ -695,10 +694,10 @@ struct GemvPlan {
 
 constexpr size_t kSmemMax = 227 * 1024;  // one CTA per SM at most
 
-template <int B, bool BF16, int TILES, int WPS, int MB>
+template <int B, bool BF16, int TILES, int WPS, int MB, bool XST>
 cudaError_t launch_t(const GemvPlan &pl, const CUtensorMap &tw, const CUtensorMap &ts,
                      const CUtensorMap &tb, const CUtensorMap &tx, cudaStream_t stream) {
-    auto kern = gemv_kernel<B, BF16, TILES, WPS, MB>;
+    auto kern = gemv_kernel<B, BF16, TILES, WPS, MB, XST>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -719,7 +718,10 @@ cudaError_t launch_t(const GemvPlan &pl, const CUtensorMap &tw, const CUtensorMa
     return cudaLaunchKernelEx(&cfg, kern, pl.prm, tw, ts, tb, tx);
 }
 
-// Two column blocks (M = 9..16): defined in aq_gemv16.cu.
+// Staged x (x streamed with the weights): one column block in aq_gemv_xs.cu,
+// two (M = 9..16) in aq_gemv16.cu.
+cudaError_t launch_staged1(const GemvPlan &pl, const CUtensorMap &tw, const CUtensorMap &ts,
+                           const CUtensorMap &tb, const CUtensorMap &tx, cudaStream_t stream);
 cudaError_t launch_mb2(const GemvPlan &pl, const CUtensorMap &tw, const CUtensorMap &ts,
                        const CUtensorMap &tb, const CUtensorMap &tx, cudaStream_t stream);
 

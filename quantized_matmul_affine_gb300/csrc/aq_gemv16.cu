@@ -11,8 +11,8 @@ template <int B, bool BF16, int TILES>
 cudaError_t mb2_wps(const GemvPlan &pl, const CUtensorMap &tw, const CUtensorMap &ts,
                     const CUtensorMap &tb, const CUtensorMap &tx, cudaStream_t s) {
     if constexpr (TILES <= 2)
-        if (pl.wps == 2) return launch_t<B, BF16, TILES, 2, 2>(pl, tw, ts, tb, tx, s);
-    return launch_t<B, BF16, TILES, 1, 2>(pl, tw, ts, tb, tx, s);
+        if (pl.wps == 2) return launch_t<B, BF16, TILES, 2, 2, true>(pl, tw, ts, tb, tx, s);
+    return launch_t<B, BF16, TILES, 1, 2, true>(pl, tw, ts, tb, tx, s);
 }
 
 template <int B, bool BF16>

@@ -105,8 +105,12 @@ def test_stats_interface():
     (9, 10240, 5120, 3, aq.AQ_VARIANT_GEMV),
     (16, 10240, 5120, 3, aq.AQ_VARIANT_GEMV),
     (17, 10240, 5120, 3, aq.AQ_VARIANT_TC),
-    (1, 5120, 13824, 4, aq.AQ_VARIANT_QMV),    # 35 MB of weights at M = 1
-    (1, 13824, 5120, 4, aq.AQ_VARIANT_QMV),
+    (1, 5120, 13824, 4, aq.AQ_VARIANT_GEMV),
+    (1, 13824, 5120, 4, aq.AQ_VARIANT_GEMV),
+    (1, 19456, 4096, 4, aq.AQ_VARIANT_GEMV),   # one pass of 128 rows per SM at M = 1
+    (1, 19457, 4096, 4, aq.AQ_VARIANT_QMV),
+    (1, 28672, 8192, 4, aq.AQ_VARIANT_QMV),
+    (1, 128256, 4096, 4, aq.AQ_VARIANT_QMV),
     (8, 13824, 5120, 4, aq.AQ_VARIANT_GEMV),
     (2, 28672, 8192, 4, aq.AQ_VARIANT_GEMV),   # two passes of 95 rows per CTA
     (64, 10240, 5120, 3, aq.AQ_VARIANT_TC),
@@ -127,7 +131,7 @@ def test_select_invalid():
 @pytest.mark.parametrize("M,N,K,bits,want", [
     (1, 4096, 4096, 4, "rows/cta=27 passes=1 tiles=2 colblocks=1 groups/stage=32 stages=2 ring=2 x=whole grid=152"),
     (2, 28672, 8192, 4, "rows/cta=190 passes=2"),
-    (8, 600, 13824, 4, "x=ring"),
+    (8, 600, 13824, 4, "x=staged"),
     (16, 10240, 5120, 3, "rows/cta=68 passes=2 tiles=3 colblocks=2"),
 ])
 def test_gemv_plan(M, N, K, bits, want):
