@@ -42,13 +42,16 @@ namespace {
 
 constexpr int kThreadsTc = 14 * 32;
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpDq = 6, kDqWarps = 8;  // warps 2-5: epilogue
-constexpr int kRawSlots = 2;  // raw super-stages per dequant warp
 constexpr int kGroups = 4;    // groups per raw super-stage (256 k)
 constexpr int kATileBytes = 128 * 128;
 
-// A/B pipeline depth by x tile width: as deep as shared memory allows.  The
-// ring has to cover the round trip dequantise -> MMA -> commit -> reuse.
-constexpr int stages_for(int BM) { return BM <= 64 ? 7 : BM <= 128 ? 5 : 3; }
+// A/B pipeline depth by x tile width.  The ring has to cover the round trip
+// dequantise -> MMA -> commit -> reuse.
+constexpr int stages_for(int BM) { return BM <= 64 ? 5 : BM <= 128 ? 4 : 3; }
+// Raw super-stages per dequant warp; all but one are in flight while the
+// warp dequantises, so that the weight stream keeps enough bytes in flight
+// to cover the HBM latency (about 55 KB per SM at four slots).
+constexpr int raw_slots_for(int BM) { return BM <= 128 ? 4 : 3; }
 
 template <int B>
 struct Raw {
@@ -159,6 +162,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
     using R = Raw<B>;
     constexpr int kStages = stages_for(BM);
+    constexpr int kRawSlots = raw_slots_for(BM);
     extern __shared__ uint8_t smem_dyn[];
     // Align to 1024 bytes by an offset from the __shared__ array itself, so
     // that every access below stays a shared-memory access (32-bit address).
@@ -226,38 +230,46 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------------
-        // MMA issue: 4 x (128 x BM x 16) per stage into accumulator b.
+        // MMA issue: 4 x (128 x BM x 16) per stage into accumulator b.  The
+        // whole warp walks the stages (converged, waits taken by every lane
+        // and agreed on); lane 0 issues.  Descriptors: those of slot 0,
+        // k-step 0, plus the byte offset of the slot and k-step over 16.
         // ------------------------------------------------------------------
-        if (lane == 0) {
-            const uint32_t idesc = (1u << 4) | ((BF16 ? 1u : 0u) << 7) | ((BF16 ? 1u : 0u) << 10) |
-                                   ((uint32_t)(BM >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
-            uint32_t it = 0, ti = 0;
-            for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++ti) {
-                const uint32_t b = ti & 1u, use = ti >> 1;
-                if (ti >= 2 && !tc_wait(&acc_empty[b], (use & 1u) ^ 1u, flag, 0x0202)) break;
+        const uint32_t idesc = (1u << 4) | ((BF16 ? 1u : 0u) << 7) | ((BF16 ? 1u : 0u) << 10) |
+                               ((uint32_t)(BM >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+        const uint64_t a_desc0 = sw128_desc(smem_u32(a_ring));
+        const uint64_t b_desc0 = sw128_desc(smem_u32(b_ring));
+        uint32_t it = 0, ti = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++ti) {
+            const uint32_t b = ti & 1u, use = ti >> 1;
+            const bool free = ti < 2 || tc_wait(&acc_empty[b], (use & 1u) ^ 1u, flag, 0x0202);
+            if (!__all_sync(0xffffffffu, free)) break;
+            tc_fence_after();
+            const uint32_t d = tmem + b * BM;
+            bool ok = true;
+            for (int g = 0; g < G; ++g, ++it) {
+                const int slot = it % kStages;
+                const uint32_t ph = (it / kStages) & 1u;
+                const bool got = tc_wait(&a_full[slot], ph, flag, 0x0302) &&
+                                 tc_wait(&b_full[slot], ph, flag, 0x0402);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
-                const uint32_t d = tmem + b * BM;
-                bool ok = true;
-                for (int g = 0; g < G; ++g, ++it) {
-                    const int slot = it % kStages;
-                    const uint32_t ph = (it / kStages) & 1u;
-                    if (!tc_wait(&a_full[slot], ph, flag, 0x0302) ||
-                        !tc_wait(&b_full[slot], ph, flag, 0x0402)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t a_base = smem_u32(a_ring + slot * kATileBytes);
-                    const uint32_t b_base = smem_u32(b_ring + slot * (BM * 128));
+                if (lane == 0) {
+                    const uint64_t ad = a_desc0 + (uint64_t)((uint32_t)(slot * kATileBytes) >> 4);
+                    const uint64_t bd = b_desc0 + (uint64_t)((uint32_t)(slot * BM * 128) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        tc_mma_f16(d, sw128_desc(a_base + 32 * kk), sw128_desc(b_base + 32 * kk),
-                                   idesc, (g | kk) != 0);
+                        tc_mma_f16(d, ad + 2 * kk, bd + 2 * kk, idesc, (g | kk) != 0);
                     tc_commit(&ab_empty[slot]);
                 }
-                if (!ok) break;
-                tc_commit(&acc_full[b]);
+                __syncwarp();
             }
+            if (!ok) break;
+            if (lane == 0) tc_commit(&acc_full[b]);
+            __syncwarp();
         }
     } else if (warp < kWarpDq) {
         // ------------------------------------------------------------------
@@ -336,12 +348,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         };
         uint32_t it = 0;  // A-stage counter (matches the MMA's)
         int iss = 0;      // super-stages issued
-        if (ntile < total) {
-            issue(ntile, nss_next, 0);
-            ++iss;
-            advance(ntile, nss_next);
+        // kRawSlots - 1 super-stages ahead, one commit group each
+#pragma unroll 1
+        for (int pre = 0; pre < kRawSlots - 1; ++pre) {
+            if (ntile < total) {
+                issue(ntile, nss_next, iss % kRawSlots);
+                ++iss;
+                advance(ntile, nss_next);
+            }
+            cp_async_commit();
         }
-        cp_async_commit();
         const int rl = lane >> 1, h = lane & 1;
         const int arow = 16 * dw + rl;  // row within the 128-row A tile
         bool ok = true;
@@ -352,7 +368,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 advance(ntile, nss_next);
             }
             cp_async_commit();
-            cp_async_wait<1>();
+            cp_async_wait<kRawSlots - 1>();
             __syncwarp();
             const uint8_t *slotp = ring + (cnt % kRawSlots) * R::kSlotBytes;
             const uint2 sv2 = *reinterpret_cast<const uint2 *>(slotp + R::kSbOff + rl * 8);
@@ -445,6 +461,7 @@ bool tc_plan(const MatmulArgs &a, TcPlan &pl) {
     if ((int64_t)q.n_tiles * q.m_tiles > INT32_MAX) return false;
     const int raw_slot = a.bits == 4 ? Raw<4>::kSlotBytes : Raw<3>::kSlotBytes;
     const int kStages = stages_for(pl.BM);
+    const int kRawSlots = raw_slots_for(pl.BM);
     size_t off = (size_t)kStages * kATileBytes;
     q.off_b = (uint32_t)off;
     off += (size_t)kStages * pl.BM * 128;
