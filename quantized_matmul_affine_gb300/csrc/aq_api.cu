@@ -81,14 +81,15 @@ bool tmap_encode(CUtensorMap *tm, CUtensorMapDataType type, int rank, const void
 }
 
 // Largest M that the resident small-M kernel takes under the automatic rule
-// (AQ_GEMV_MAX_M overrides it for experiments): it serves up to two 8-column
+// (AQ_GEMV_MAX_M overrides it for experiments): it serves up to four 8-column
 // blocks, and measured faster than qmv at every M from 1 to 16 but the
-// single-row case below.
+// single-row case below, and 1.9-3.3x faster than tc from 17 to 32 (GB300:
+// 3-bit 10240x5120 at M = 32, 20.8 against 39.4 us).
 static int gemv_max_m() {
     static const int v = [] {
         const char *e = std::getenv("AQ_GEMV_MAX_M");
         if (e && *e) return std::atoi(e);
-        return 16;
+        return 32;
     }();
     return v;
 }

@@ -31,6 +31,7 @@ size_t smem_budget() {
 // Groups per warp per stage (the units of a stage are unrolled; this bounds
 // code and registers), by tiles per pass and column blocks.
 int max_wps(int tiles, int mb) {
+    if (mb > 2) return 1;
     if (mb > 1) return tiles <= 2 ? 2 : 1;
     return tiles <= 2 ? 4 : tiles <= 4 ? 2 : 1;
 }
@@ -49,13 +50,15 @@ uint32_t *error_word() {
 }
 
 bool gemv_plan(const MatmulArgs &a, GemvPlan &pl) {
-    if (a.M < 1 || a.M > 16 || a.N < 1 || a.K < 512 || a.K % 512 != 0) return false;
+    if (a.M < 1 || a.M > 32 || a.N < 1 || a.K < 512 || a.K % 512 != 0) return false;
     if (a.N > INT32_MAX / 2 || a.K > INT32_MAX / 2) return false;
     const int B = a.bits;
     const int G = (int)(a.K / 64);
-    const int MB = a.M > 8 ? 2 : 1;
-    const int max_tiles = MB == 1 ? kMaxTiles : 4;
-    const size_t budget = smem_budget();
+    const int MB = a.M > 16 ? 4 : a.M > 8 ? 2 : 1;
+    const int max_tiles = MB == 1 ? kMaxTiles : MB == 2 ? 4 : 6;
+    // Four column blocks take too many registers for two CTAs per SM: the
+    // CTA has the SM to itself and all of its shared memory.
+    const size_t budget = MB > 2 ? kSmemMax : smem_budget();
     const int sms = num_sms();
     const int64_t per_sm = (a.N + sms - 1) / sms;
     const int passes = (int)((per_sm + 16 * max_tiles - 1) / (16 * max_tiles));
@@ -220,6 +223,7 @@ cudaError_t gemv_launch(const MatmulArgs &a) {
         !tmap_encode(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, a.biases, sdims, sstrides, sbox,
                      CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
+    if (pl.mb > 2) return gemv::launch_mb4(pl, tw, ts, tb, tx, a.stream);
     if (pl.mb > 1) return gemv::launch_mb2(pl, tw, ts, tb, tx, a.stream);
     if (staged) return gemv::launch_staged1(pl, tw, ts, tb, tx, a.stream);
     tx = tw;  // unused when x is whole

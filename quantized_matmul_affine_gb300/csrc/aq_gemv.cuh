@@ -283,7 +283,7 @@ __device__ __forceinline__ void store_y<__nv_bfloat16>(__nv_bfloat16 *p, float v
 }
 
 template <int B, bool BF16, int TILES, int WPS, int MB, bool XST>
-__global__ void __launch_bounds__(kGemvThreads, 2)
+__global__ void __launch_bounds__(kGemvThreads, MB > 2 ? 1 : 2)
     gemv_kernel(const __grid_constant__ GemvParams p, const __grid_constant__ CUtensorMap tm_w,
                 const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_b,
                 const __grid_constant__ CUtensorMap tm_x) {
@@ -719,7 +719,9 @@ cudaError_t launch_t(const GemvPlan &pl, const CUtensorMap &tw, const CUtensorMa
 }
 
 // Staged x (x streamed with the weights): one column block in aq_gemv_xs.cu,
-// two (M = 9..16) in aq_gemv16.cu.
+// two (M = 9..16) in aq_gemv16.cu, four (M = 17..32) in aq_gemv32.cu.
+cudaError_t launch_mb4(const GemvPlan &pl, const CUtensorMap &tw, const CUtensorMap &ts,
+                       const CUtensorMap &tb, const CUtensorMap &tx, cudaStream_t stream);
 cudaError_t launch_staged1(const GemvPlan &pl, const CUtensorMap &tw, const CUtensorMap &ts,
                            const CUtensorMap &tb, const CUtensorMap &tx, cudaStream_t stream);
 cudaError_t launch_mb2(const GemvPlan &pl, const CUtensorMap &tw, const CUtensorMap &ts,
