@@ -63,8 +63,13 @@ def _load() -> ctypes.CDLL:
             lib.oracle_matmul.argtypes = [p, p, p, p, i64, i64, i64, i32, p, p]
             lib.oracle_matmul_cols.argtypes = [p, p, p, p, i64, i64, i64, i32, p, i64, p, p]
             lib.oracle_matmul_threads.argtypes = [p, p, p, p, i64, i64, i64, i32, p, p, i32]
+            lib.oracle_quantize.argtypes = [p, i64, i64, i32, p, p, p]
+            lib.oracle_f32_to_f16.argtypes = [ctypes.c_float]
+            lib.oracle_f32_to_f16.restype = ctypes.c_uint16
+            lib.oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
+            lib.oracle_f16_to_f32.restype = ctypes.c_float
             for f in ("oracle_pack", "oracle_unpack", "oracle_dequant", "oracle_matmul",
-                      "oracle_matmul_cols", "oracle_matmul_threads"):
+                      "oracle_matmul_cols", "oracle_matmul_threads", "oracle_quantize"):
                 getattr(lib, f).restype = i32
             _lib = lib
     return _lib
@@ -163,3 +168,32 @@ def matmul_cols(x: np.ndarray, words: np.ndarray, scales: np.ndarray, biases: np
 def tolerance(bound: np.ndarray) -> np.ndarray:
     """Per-element acceptance bound |y - y_ref| <= 2e-3 * sum|x*w| + 1e-5."""
     return 2e-3 * bound + 1e-5
+
+
+def f32_to_f16_bits(values) -> np.ndarray:
+    """float32 values -> binary16 bit patterns (the oracle's own RNE conversion)."""
+    v = np.asarray(values, dtype=np.float32).ravel()
+    lib = _load()
+    return np.array([lib.oracle_f32_to_f16(float(a)) for a in v], dtype=np.uint16)
+
+
+def f16_bits_to_f32(bits) -> np.ndarray:
+    """binary16 bit patterns -> float32 values (the oracle's own conversion)."""
+    b = np.asarray(bits, dtype=np.uint16).ravel()
+    lib = _load()
+    return np.array([lib.oracle_f16_to_f32(int(h)) for h in b], dtype=np.float32)
+
+
+def quantize(w: np.ndarray, bits: int):
+    """Float weights [N, K] (float32 holding fp16 / bf16 values) -> (codes uint8
+    [N, K], scale bits uint16 [N, K/64], bias bits uint16 [N, K/64]); pack the
+    codes with pack().  The quantiser's rule is in aq_oracle.c."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    N, K = w.shape
+    codes = np.zeros((N, K), dtype=np.uint8)
+    G = K // 64
+    sb = np.zeros((N, G), dtype=np.uint16)
+    bb = np.zeros((N, G), dtype=np.uint16)
+    _check(_load().oracle_quantize(_ptr(w), N, K, bits, _ptr(codes), _ptr(sb), _ptr(bb)),
+           "quantize")
+    return codes, sb, bb

@@ -200,3 +200,96 @@ int oracle_matmul_threads(const double *x, const uint32_t *words, const double *
         if (running[t]) pthread_join(tid[t], NULL);
     return 0;
 }
+
+/* ------------------------------------------------------------------------
+ * Quantiser: float weights -> (codes, fp16 scale, fp16 bias) per group.
+ *
+ * The pages fix the stored format and the dequantisation w = scale*q + bias,
+ * but not how a quantiser picks scale, bias and codes.  This is the plain
+ * reading, decided in single precision (the precision the GPU kernel decides
+ * the codes in, so both sides take the same integer decisions):
+ *
+ *   lo = min of the group's 64 values, hi = max           (exact)
+ *   scale = fp16( (hi - lo) / (2^B - 1) )                 (fp32 ops, RNE)
+ *   bias  = fp16( lo )                                    (RNE)
+ *   q = clamp( rint((w - bias) / scale), 0, 2^B - 1 )      (fp32 ops, rint
+ *                                                          ties to even;
+ *                                                          q = 0 if scale = 0)
+ *
+ * The fp16 conversions below are written from the IEEE 754 binary16
+ * definition (11-bit significand, exponent bias 15, subnormal step 2^-24,
+ * round to nearest with ties to even, overflow to infinity).
+ * ------------------------------------------------------------------------ */
+
+/* binary16 bits -> float (exact). */
+float oracle_f16_to_f32(uint16_t h) {
+    const int sign = (h >> 15) & 1;
+    const int e = (h >> 10) & 0x1F;
+    const int m = h & 0x3FF;
+    double v;
+    if (e == 0x1F)
+        v = m ? NAN : INFINITY;
+    else if (e == 0)
+        v = ldexp((double)m, -24); /* subnormal: m * 2^-24 */
+    else
+        v = ldexp((double)(1024 + m), e - 25); /* (1 + m/1024) * 2^(e-15) */
+    return (float)(sign ? -v : v);
+}
+
+/* float -> binary16 bits, round to nearest, ties to even. */
+uint16_t oracle_f32_to_f16(float f) {
+    const uint16_t sign = signbit(f) ? 0x8000u : 0u;
+    const double a = fabs((double)f);
+    if (isnan(f)) return (uint16_t)(sign | 0x7E00u);
+    /* 65520 lies halfway between 65504 (largest finite, odd significand) and
+       2^16, so it and everything above round to infinity */
+    if (a >= 65520.0) return (uint16_t)(sign | 0x7C00u);
+    if (a == 0.0) return sign;
+    int e2;
+    frexp(a, &e2);                    /* a = m * 2^e2, m in [0.5, 1) */
+    int e = e2 - 1;                   /* floor(log2 a) */
+    if (e < -14) e = -14;             /* subnormal range: fixed quantum 2^-24 */
+    const double quantum = ldexp(1.0, e - 10);
+    const double r = nearbyint(a / quantum); /* exact quotient; ties to even */
+    const double v = r * quantum;     /* the rounded magnitude (may reach 2^(e+1)) */
+    if (v < ldexp(1.0, -14)) return (uint16_t)(sign | (uint16_t)r); /* subnormal */
+    int ev2;
+    const double mv = frexp(v, &ev2); /* v = mv * 2^ev2 */
+    const int ev = ev2 - 1;
+    const uint16_t mant = (uint16_t)((mv * 2.0 - 1.0) * 1024.0);
+    return (uint16_t)(sign | (uint16_t)((ev + 15) << 10) | mant);
+}
+
+int oracle_quantize(const float *w, int64_t N, int64_t K, int bits, uint8_t *codes,
+                    uint16_t *scale_bits, uint16_t *bias_bits) {
+    if (!valid_shape(N, K, bits)) return 1;
+    const int64_t G = K / ORACLE_GROUP;
+    const int qmax = (1 << bits) - 1;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t g = 0; g < G; ++g) {
+            const float *wg = w + n * K + g * ORACLE_GROUP;
+            float lo = wg[0], hi = wg[0];
+            for (int v = 1; v < ORACLE_GROUP; ++v) {
+                if (wg[v] < lo) lo = wg[v];
+                if (wg[v] > hi) hi = wg[v];
+            }
+            const float range = hi - lo;
+            const float scale32 = range / (float)qmax;
+            const uint16_t sb = oracle_f32_to_f16(scale32);
+            const uint16_t bb = oracle_f32_to_f16(lo);
+            scale_bits[n * G + g] = sb;
+            bias_bits[n * G + g] = bb;
+            const float s = oracle_f16_to_f32(sb);
+            const float b = oracle_f16_to_f32(bb);
+            for (int v = 0; v < ORACLE_GROUP; ++v) {
+                int q = 0;
+                if (s != 0.0f) {
+                    const float t = (wg[v] - b) / s;
+                    const float r = rintf(t);
+                    q = r < 0.0f ? 0 : r > (float)qmax ? qmax : (int)r;
+                }
+                codes[n * K + g * ORACLE_GROUP + v] = (uint8_t)q;
+            }
+        }
+    return 0;
+}
