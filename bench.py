@@ -7,7 +7,10 @@ in CUDA graphs and cycling through enough copies of the weights that their
 total exceeds twice the L2 size (every call reads its weights from HBM).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode|small|split3:I|layer:I|prefill:I] [--all]
+                    [--workload decode|small|split3:I|layer:I|prefill:I|quantize:I] [--all]
+
+quantize:I times the float -> affine quantiser (aq_quantize) on the weight
+shapes of workloads.QUANTIZE_WORKLOADS instead of the matmul.
 
 Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs an
 independent replica on its own GPU ("replicas only": the method needs no
@@ -356,6 +359,133 @@ def finish(args, p, name, idx, world, aq, variant, copies, wbytes, l2, chunk, us
     return line, p
 
 
+QUANTIZE_METRIC = "µs/call and effective HBM GB/s (fraction of roofline), float -> affine group-64 quantiser"
+
+
+def run_quantize(args, rank, world, local_rank):
+    """The quantiser (aq_quantize / aq_quantize_bf16) on one of its workloads:
+    device-timed calls over rotating weight copies (> 2x L2), the same through
+    host buffers, and the oracle's quantiser on a row sample of the host."""
+    import torch
+    import quantized_matmul_affine_gb300 as aq
+
+    torch.cuda.set_device(local_rank)
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    name, idx = parse_workload(args.workload)
+    bits, N, K, dt, seed = workloads.QUANTIZE_WORKLOADS[name][idx]
+    b16, vals = workloads.make_weights(N, K, dt, seed)
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float16
+    w0 = torch.from_numpy(b16.view(np.int16)).cuda().view(tdt)
+    l2 = getattr(props, "L2_cache_size", 126 * 1024 * 1024)
+    copies = max(2, -(-2 * l2 // (2 * N * K)) + 1)
+    ws = [w0.clone() for _ in range(copies)]
+    q = aq.aq_quantize_bf16 if dt == "bf16" else aq.aq_quantize
+    outs = [q(w, bits) for w in ws]
+    stream = torch.cuda.Stream()
+
+    def capture(ncalls):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(ncalls):
+                    c = i % copies
+                    f = aq.load().aq_quantize_bf16 if dt == "bf16" else aq.load().aq_quantize
+                    Wq, sc, bi = outs[c]
+                    f(ws[c].data_ptr(), N, K, bits, Wq.data_ptr(), sc.data_ptr(), bi.data_ptr(),
+                      stream.cuda_stream)
+        return g
+
+    steps = max(1, min(args.steps, 2000))
+    chunk = min(256, steps)
+    g = capture(chunk)
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup // chunk)):
+            g.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(str(props.uuid) if hasattr(props, "uuid") else "0")
+    if not str(sampler.gpu_id).startswith("GPU-"):
+        sampler.gpu_id = "GPU-" + str(sampler.gpu_id)
+    sampler.start()
+    time.sleep(0.5)
+    torch.cuda.synchronize()
+    reps = max(1, steps // chunk)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.mark()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark()
+    clocks = sampler.stop()
+    us_call = reduce_max(ev0.elapsed_time(ev1) * 1e3 / (reps * chunk), "cuda")
+
+    # end to end: pinned weights in, packed codes, scales and biases out
+    w_host = w0.cpu().pin_memory()
+    Wq_h = torch.empty_like(outs[0][0], device="cpu").pin_memory()
+    s_h = torch.empty_like(outs[0][1], device="cpu").pin_memory()
+    b_h = torch.empty_like(outs[0][2], device="cpu").pin_memory()
+    n_e2e = 50
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(n_e2e):
+            ws[0].copy_(w_host, non_blocking=True)
+            Wq, sc, bi = q(ws[0], bits, stream=stream)
+            Wq_h.copy_(Wq, non_blocking=True)
+            s_h.copy_(sc, non_blocking=True)
+            b_h.copy_(bi, non_blocking=True)
+            stream.synchronize()
+    e2e_us = reduce_max((time.perf_counter() - t0) * 1e6 / n_e2e, "cuda")
+
+    hbm, _, src = peaks()
+    by = workloads.quantize_bytes(N, K, bits)
+    achieved = by / (us_call * 1e-6) / 1e9
+    line = {
+        "metric": QUANTIZE_METRIC,
+        "value": round(whole_job_us_per_call(us_call, world), 4),
+        "unit": "us/call",
+        "n_gpus": world, "steps": reps * chunk, "warmup": args.warmup,
+        "ms_per_step": us_call / 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": dt, "data": "synthetic",
+        "config": {"workload": f"{name}[{idx}]: quantise {N}x{K} {dt} weights to {bits}-bit "
+                               f"affine group-64",
+                   "N": N, "K": K, "bits": bits, "w_dtype": dt,
+                   "l2": f"cold: {copies} rotating weight copies > 2x L2 ({l2 / 1e6:.0f} MB)",
+                   "timing": f"CUDA events on the launching stream around {reps} replays of a "
+                             f"CUDA graph of {chunk} calls",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm,
+                     "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
+                     "peak_source": f"{src} (MEASURED_PEAKS.json)" if src == "measured"
+                     else "fallback",
+                     "algorithmic_bytes_per_launch": by},
+        "e2e": {"value": round(whole_job_us_per_call(e2e_us, world), 3), "unit": "us/call",
+                "h2d_bytes_per_step": 2 * N * K,
+                "d2h_bytes_per_step": N * K * bits // 8 + 4 * N * (K // 64),
+                "path": "pinned weights -> device, aq_quantize, codes/scales/biases -> pinned "
+                        "host, sync"},
+        "gpu_launches": reps * chunk,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:
+        import oracle
+        oracle.build()
+        rows = min(N, 512)
+        t0 = time.perf_counter()
+        n = 0
+        while time.perf_counter() - t0 < min(args.cpu_budget, 10.0) or n == 0:
+            oracle.quantize(vals[:rows], bits)
+            n += 1
+        us = (time.perf_counter() - t0) / n * (N / rows) * 1e6
+        line["cpu_baseline"] = {"value": round(us, 1), "unit": "us/call", "cores": 1,
+                                "kind": "oracle",
+                                "sample": f"{n} runs of the oracle quantiser on {rows} of {N} "
+                                          f"rows, scaled by N/{rows}; 1 thread"}
+    return line
+
+
 def cpu_sample_time(p, budget_s, threads):
     """Time the oracle on a column sample of p; returns (us per full call, desc)."""
     import oracle
@@ -468,6 +598,11 @@ def main():
         specs = [f"{n}:{i}" for n, c in workloads.WORKLOADS.items() for i in range(len(c))]
     for spec in specs:
         args.workload = spec
+        if parse_workload(spec)[0] in workloads.QUANTIZE_WORKLOADS:
+            line = run_quantize(args, rank, world, local_rank)
+            if rank == 0:
+                print(json.dumps(line), flush=True)
+            continue
         line, p = run_ours(args, rank, world, local_rank)
         if rank == 0:
             if world == 1 and not args.no_cpu_baseline and not args.all and not args.quick:

@@ -83,6 +83,30 @@ aq_status aq_pack(const uint8_t *codes_dev, int64_t N, int64_t K, int bits,
                   uint32_t *words_dev, void *stream);
 
 /*
+ * aq_quantize — quantise float weights W[N][K] (fp16) into the format above:
+ * packed codes, one fp16 scale and one fp16 bias per 64-value group.
+ * aq_quantize_bf16 — the same with bf16 weights.
+ *   w_dev       [N][K] weights, device, 16-byte aligned, row-major.
+ *   Wq_dev      uint32 [N][K*bits/32], device, caller-allocated, written entirely.
+ *   scales_dev  fp16 [N][K/64], device, caller-allocated, written entirely.
+ *   biases_dev  fp16 [N][K/64], device, caller-allocated, written entirely.
+ * The pages define the format and w = scale*q + bias (affine-split-mma.ts,
+ * helper affine_unit) but no quantiser; the rule here, decided in single
+ * precision per group, is: scale = fp16((max - min) / (2^bits - 1)),
+ * bias = fp16(min), q = clamp(rint((w - bias) / scale), 0, 2^bits - 1)
+ * (q = 0 when the scale is 0); fp16 rounding is to nearest even.  Weights
+ * must be finite and within fp16 range (the stored scale and bias are fp16).
+ * Errors: AQ_ERR_INVALID_ARG if N < 0, K < 0, K % 64 != 0, bits not in
+ * {3,4} or a pointer is NULL while N*K > 0; AQ_ERR_MISALIGNED if w_dev is not
+ * 16-byte aligned, Wq_dev not 4-byte or scales/biases not 2-byte aligned;
+ * AQ_ERR_CUDA if the launch fails.  N == 0 or K == 0 queues nothing.
+ */
+aq_status aq_quantize(const void *w_dev, int64_t N, int64_t K, int bits, uint32_t *Wq_dev,
+                      void *scales_dev, void *biases_dev, void *stream);
+aq_status aq_quantize_bf16(const void *w_dev, int64_t N, int64_t K, int bits,
+                           uint32_t *Wq_dev, void *scales_dev, void *biases_dev, void *stream);
+
+/*
  * aq_matmul — y[M][N] = x[M][K] . dequant(W)^T with fp16 x and fp16 y.
  * aq_matmul_bf16 — the same with bf16 x and bf16 y.
  *   x_dev      [M][K] activations, device.

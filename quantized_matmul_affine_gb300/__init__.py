@@ -22,7 +22,8 @@ from . import build as _build
 
 __all__ = [
     "AqError", "AQ_F16", "AQ_BF16", "AQ_VARIANT_AUTO", "AQ_VARIANT_GENERIC", "AQ_VARIANT_QMV",
-    "AQ_VARIANT_TC", "AQ_VARIANT_GEMV", "AQ_NUM_VARIANTS", "aq_pack", "aq_matmul", "aq_matmul_bf16",
+    "AQ_VARIANT_TC", "AQ_VARIANT_GEMV", "AQ_NUM_VARIANTS", "aq_pack", "aq_quantize",
+    "aq_quantize_bf16", "aq_matmul", "aq_matmul_bf16",
     "aq_matmul_variant", "aq_matmul_host", "aq_select", "aq_describe", "aq_stats", "aq_device_error",
     "aq_free", "aq_status_string", "aq_variant_name", "aq_version", "lib_path", "load",
 ]
@@ -60,6 +61,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     p, i64, i32, u32p = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
     sig = {
         "aq_pack": ([p, i64, i64, i32, p, p], i32),
+        "aq_quantize": ([p, i64, i64, i32, p, p, p, p], i32),
+        "aq_quantize_bf16": ([p, i64, i64, i32, p, p, p, p], i32),
         "aq_matmul": ([p, p, p, p, i64, i64, i64, i32, p, p], i32),
         "aq_matmul_bf16": ([p, p, p, p, i64, i64, i64, i32, p, p], i32),
         "aq_matmul_variant": ([i32, i32, p, p, p, p, i64, i64, i64, i32, p, p], i32),
@@ -125,6 +128,31 @@ def aq_pack(codes: torch.Tensor, bits: int, words: Optional[torch.Tensor] = None
     _check(load().aq_pack(_dev(codes, "codes"), N, K, bits, _dev(words, "words"),
                           _stream(stream)), "aq_pack")
     return words
+
+
+def _quantize(dtype, w: torch.Tensor, bits: int, stream) -> tuple:
+    want = torch.float16 if dtype == AQ_F16 else torch.bfloat16
+    if w.dtype != want:
+        raise ValueError(f"w must be {want}")
+    N, K = w.shape
+    Wq = torch.empty((N, K * bits // 32), dtype=torch.int32, device=w.device)
+    scales = torch.empty((N, K // 64), dtype=torch.float16, device=w.device)
+    biases = torch.empty((N, K // 64), dtype=torch.float16, device=w.device)
+    f = load().aq_quantize if dtype == AQ_F16 else load().aq_quantize_bf16
+    _check(f(_dev(w, "w"), N, K, bits, _dev(Wq, "Wq"), _dev(scales, "scales"),
+             _dev(biases, "biases"), _stream(stream)), "aq_quantize")
+    return Wq, scales, biases
+
+
+def aq_quantize(w: torch.Tensor, bits: int, stream=None) -> tuple:
+    """fp16 weights [N, K] (device) -> (Wq uint32-as-int32 [N, K*bits/32],
+    scales fp16 [N, K/64], biases fp16 [N, K/64])."""
+    return _quantize(AQ_F16, w, bits, stream)
+
+
+def aq_quantize_bf16(w: torch.Tensor, bits: int, stream=None) -> tuple:
+    """aq_quantize for bf16 weights."""
+    return _quantize(AQ_BF16, w, bits, stream)
 
 
 def _mm(variant: int, dtype: int, x, Wq, scales, biases, bits, out, stream) -> torch.Tensor:

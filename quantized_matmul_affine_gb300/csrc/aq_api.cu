@@ -193,6 +193,31 @@ aq_status aq_pack(const uint8_t *codes_dev, int64_t N, int64_t K, int bits, uint
     return AQ_OK;
 }
 
+static aq_status quantize_entry(int dtype, const void *w_dev, int64_t N, int64_t K, int bits,
+                                uint32_t *Wq_dev, void *scales_dev, void *biases_dev,
+                                void *stream) {
+    if (N < 0 || K < 0 || K % 64 != 0 || (bits != 3 && bits != 4)) return AQ_ERR_INVALID_ARG;
+    if (N == 0 || K == 0) return AQ_OK;
+    if (!w_dev || !Wq_dev || !scales_dev || !biases_dev) return AQ_ERR_INVALID_ARG;
+    if (!aligned(w_dev, 16) || !aligned(Wq_dev, 4) || !aligned(scales_dev, 2) ||
+        !aligned(biases_dev, 2))
+        return AQ_ERR_MISALIGNED;
+    if (quantize_launch(dtype, w_dev, N, K, bits, Wq_dev, scales_dev, biases_dev,
+                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return AQ_ERR_CUDA;
+    return AQ_OK;
+}
+
+aq_status aq_quantize(const void *w_dev, int64_t N, int64_t K, int bits, uint32_t *Wq_dev,
+                      void *scales_dev, void *biases_dev, void *stream) {
+    return quantize_entry(AQ_F16, w_dev, N, K, bits, Wq_dev, scales_dev, biases_dev, stream);
+}
+
+aq_status aq_quantize_bf16(const void *w_dev, int64_t N, int64_t K, int bits, uint32_t *Wq_dev,
+                           void *scales_dev, void *biases_dev, void *stream) {
+    return quantize_entry(AQ_BF16, w_dev, N, K, bits, Wq_dev, scales_dev, biases_dev, stream);
+}
+
 aq_status aq_matmul(const void *x_dev, const uint32_t *Wq_dev, const void *scales_dev,
                     const void *biases_dev, int64_t M, int64_t N, int64_t K, int bits,
                     void *out_dev, void *stream) {

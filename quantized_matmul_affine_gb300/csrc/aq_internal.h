@@ -51,6 +51,8 @@ bool tc_supported(const MatmulArgs &a);
 cudaError_t tc_launch(const MatmulArgs &a);
 int tc_describe(const MatmulArgs &a, char *buf, int len);
 
+cudaError_t quantize_launch(int dtype, const void *w, int64_t N, int64_t K, int bits,
+                            uint32_t *words, void *scales, void *biases, cudaStream_t stream);
 cudaError_t pack_launch(const uint8_t *codes, int64_t N, int64_t K, int bits, uint32_t *words,
                         cudaStream_t stream);
 

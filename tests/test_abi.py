@@ -125,6 +125,23 @@ def test_select(M, N, K, bits, variant):
     assert aq.aq_select(M, N, K, bits) == variant
 
 
+def test_quantize_rejects_bad_arguments_before_any_launch():
+    # validation happens on the host, before anything touches the device
+    lib = ctypes.CDLL(aq.lib_path())
+    for f in (lib.aq_quantize, lib.aq_quantize_bf16):
+        f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+        f.restype = ctypes.c_int
+        assert f(16, 2, 100, 4, 16, 16, 16, None) == 1   # K % 64 != 0
+        assert f(16, 2, 128, 5, 16, 16, 16, None) == 1   # bits
+        assert f(16, -1, 128, 4, 16, 16, 16, None) == 1  # N < 0
+        assert f(None, 2, 128, 4, 16, 16, 16, None) == 1  # NULL weights
+        assert f(8, 2, 128, 4, 16, 16, 16, None) == 3    # weights not 16-byte aligned
+        assert f(16, 2, 128, 4, 18, 16, 16, None) == 3   # words not 4-byte aligned
+        assert f(16, 2, 128, 4, 16, 17, 16, None) == 3   # scales not 2-byte aligned
+        assert f(16, 0, 128, 4, None, None, None, None) == 0  # empty: nothing queued
+
+
 def test_select_invalid():
     assert aq.aq_select(0, 16, 512, 4) == -1
     assert aq.aq_select(1, 16, 512, 7) == -1

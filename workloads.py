@@ -30,6 +30,11 @@ zero.  Activations are N(0,1), rounded to the x dtype.  The 3-bit
 rows); the layer shapes stand in for a 5120-hidden decoder layer with 40 x 128
 query heads, 8 KV heads and a 13824-wide MLP.  No dataset or trained weight is
 involved.
+
+Quantiser inputs (float weights for aq_quantize): N(0, 0.02) with a per-row
+spread factor |N(0,1)| + 0.25 (rows of different magnitude, as in trained
+projections), rounded to fp16 or bf16; shapes as the workloads above
+(QUANTIZE_WORKLOADS).
 """
 from __future__ import annotations
 
@@ -167,3 +172,27 @@ def algorithmic_bytes(M: int, N: int, K: int, bits: int, out_bytes: int = 2) -> 
 
 def flops(M: int, N: int, K: int) -> int:
     return 2 * M * N * K
+
+
+def make_weights(N: int, K: int, dtype: str, seed: int, std: float = 0.02):
+    """Float weights for the quantiser: (16-bit patterns uint16 [N, K], the same
+    values as float32 [N, K])."""
+    rng = np.random.default_rng(seed)
+    row = np.abs(rng.standard_normal((N, 1))) + 0.25
+    wf = (rng.standard_normal((N, K)) * std * row).astype(np.float32)
+    bits = f32_to_bf16_bits(wf) if dtype == "bf16" else f32_to_fp16_bits(wf)
+    vals = bf16_bits_to_f32(bits) if dtype == "bf16" else bits.view(np.float16).astype(np.float32)
+    return bits, vals
+
+
+# name -> list of (bits, N, K, w dtype, seed) for the quantiser
+QUANTIZE_WORKLOADS: Dict[str, List[Tuple[int, int, int, str, int]]] = {
+    "quantize": [(4, 4096, 4096, "bf16", 51), (3, 10240, 5120, "fp16", 52),
+                 (4, 13824, 5120, "bf16", 53), (4, 28672, 8192, "bf16", 54)],
+}
+
+
+def quantize_bytes(N: int, K: int, bits: int) -> int:
+    """Bytes one quantiser call must move at least: the 16-bit weights in,
+    packed codes and fp16 scales and biases out."""
+    return 2 * N * K + N * K * bits // 8 + 4 * N * (K // GROUP)
