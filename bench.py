@@ -7,9 +7,11 @@ in CUDA graphs and cycling through enough copies of the weights that their
 total exceeds twice the L2 size (every call reads its weights from HBM).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode|small|split3:I|layer:I|prefill:I|quantize:I] [--all]
+                    [--workload decode|small|split3:I|layer:I|prefill:I|quantize:I|
+                                layerstep:I] [--all]
 
-quantize:I times the float -> affine quantiser (aq_quantize) on the weight
+layerstep:I times one decoder-layer step (seven projections; I = 0/1 fused or
+not at M = 1, 2/3 at M = 8).  quantize:I times the float -> affine quantiser (aq_quantize) on the weight
 shapes of workloads.QUANTIZE_WORKLOADS instead of the matmul.
 
 Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs an
@@ -486,6 +488,136 @@ def run_quantize(args, rank, world, local_rank):
     return line
 
 
+LAYER_METRIC = ("µs per decoder-layer step and effective HBM GB/s (fraction of roofline), "
+                "7 affine group-64 projections at M rows")
+# name -> list of (M, fused)
+LAYER_STEPS = {"layerstep": [(1, True), (1, False), (8, True), (8, False)]}
+
+
+def run_layer_step(args, rank, world, local_rank):
+    """One decoder-layer step of the 5120-hidden layer workload (q, k, v, o,
+    gate, up, down at 4 bits, bf16): fused = q/k/v in one aq_matmul_multi
+    call, gate/up + SiLU in one aq_matmul_gate_up call, then o and down;
+    unfused = the seven projections as seven calls (no SiLU)."""
+    import torch
+    import quantized_matmul_affine_gb300 as aq
+
+    torch.cuda.set_device(local_rank)
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    name, idx = parse_workload(args.workload)
+    M, fused = LAYER_STEPS[name][idx]
+    l2 = getattr(props, "L2_cache_size", 126 * 1024 * 1024)
+    layer_bytes = sum(workloads.algorithmic_bytes(M, N, K, 4)
+                      for _, N, K in workloads.LAYER_PROJECTIONS)
+    wbytes = sum(N * K // 2 + 4 * N * (K // 64) for _, N, K in workloads.LAYER_PROJECTIONS)
+    copies = max(2, -(-2 * l2 // wbytes) + 1)
+    base = {}
+    for j, (n, N, K) in enumerate(workloads.LAYER_PROJECTIONS):
+        p = workloads.make_problem(n, 4, N, K, M, "bf16", seed=30 + j)
+        base[n] = (aq.aq_pack(torch.from_numpy(p.codes).cuda(), 4),
+                   torch.from_numpy(p.scales).cuda(), torch.from_numpy(p.biases).cuda())
+    W = [base] + [{n: tuple(t.clone() for t in w) for n, w in base.items()}
+                  for _ in range(copies - 1)]
+    xb = workloads.make_x(M, 5120, "bf16", seed=7)
+    x = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
+    xo = x.clone()
+    h = torch.empty((M, 13824), dtype=torch.bfloat16, device="cuda")
+    outs = {n: torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            for n, N, _ in workloads.LAYER_PROJECTIONS}
+    stream = torch.cuda.Stream()
+
+    def step(d, xin):
+        if fused:
+            aq.aq_matmul_multi(xin, [d["q"], d["k"], d["v"]], 4,
+                               outs=[outs["q"], outs["k"], outs["v"]], stream=stream)
+            aq.aq_matmul_bf16(xo, *d["o"], 4, out=outs["o"], stream=stream)
+            aq.aq_matmul_gate_up(xin, d["gate"], d["up"], 4, out=h, stream=stream)
+            aq.aq_matmul_bf16(h, *d["down"], 4, out=outs["down"], stream=stream)
+            return 4
+        for n in ("q", "k", "v"):
+            aq.aq_matmul_bf16(xin, *d[n], 4, out=outs[n], stream=stream)
+        aq.aq_matmul_bf16(xo, *d["o"], 4, out=outs["o"], stream=stream)
+        aq.aq_matmul_bf16(xin, *d["gate"], 4, out=outs["gate"], stream=stream)
+        aq.aq_matmul_bf16(xin, *d["up"], 4, out=outs["up"], stream=stream)
+        aq.aq_matmul_bf16(h, *d["down"], 4, out=outs["down"], stream=stream)
+        return 7
+
+    steps = max(1, min(args.steps, 4096))
+    chunk = min(64, steps)
+    with torch.cuda.stream(stream):
+        step(W[0], x)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            launches = sum(step(W[i % copies], x) for i in range(chunk))
+        for _ in range(max(1, args.warmup // chunk)):
+            g.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(str(props.uuid) if hasattr(props, "uuid") else "0")
+    if not str(sampler.gpu_id).startswith("GPU-"):
+        sampler.gpu_id = "GPU-" + str(sampler.gpu_id)
+    sampler.start()
+    time.sleep(0.5)
+    reps = max(1, steps // chunk)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.mark()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark()
+    clocks = sampler.stop()
+    us = reduce_max(ev0.elapsed_time(ev1) * 1e3 / (reps * chunk), "cuda")
+
+    # end to end: pinned x in, the layer's last output (down) back to the host
+    x_host = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory()
+    y_host = torch.empty((M, 5120), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(x)
+    n_e2e = 200
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(n_e2e):
+            x_dev.copy_(x_host, non_blocking=True)
+            step(W[i % copies], x_dev)
+            y_host.copy_(outs["down"], non_blocking=True)
+            stream.synchronize()
+    e2e_us = reduce_max((time.perf_counter() - t0) * 1e6 / n_e2e, "cuda")
+
+    hbm, _, src = peaks()
+    achieved = layer_bytes / (us * 1e-6) / 1e9
+    return {
+        "metric": LAYER_METRIC,
+        "value": round(whole_job_us_per_call(us, world), 3),
+        "unit": "us/step",
+        "n_gpus": world, "steps": reps * chunk, "warmup": args.warmup,
+        "ms_per_step": us / 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{name}[{idx}]: one 5120-hidden decoder layer (q,k,v,o,gate,up,"
+                               f"down), 4-bit, M={M}, "
+                               + ("fused: q/k/v multi, gate/up+SiLU" if fused
+                                  else "seven separate calls"),
+                   "M": M, "fused": fused,
+                   "l2": f"cold: {copies} rotating copies of the layer's weights "
+                         f"({copies * wbytes / 1e6:.0f} MB > 2x L2)",
+                   "timing": f"CUDA events on the launching stream around {reps} replays of a "
+                             f"CUDA graph of {chunk} steps",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm,
+                     "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
+                     "peak_source": f"{src} (MEASURED_PEAKS.json)" if src == "measured"
+                     else "fallback",
+                     "algorithmic_bytes_per_launch": layer_bytes},
+        "e2e": {"value": round(whole_job_us_per_call(e2e_us, world), 3), "unit": "us/step",
+                "h2d_bytes_per_step": M * 5120 * 2, "d2h_bytes_per_step": M * 5120 * 2,
+                "path": "pinned x -> device, the layer's calls, down output -> pinned host, sync"},
+        "gpu_launches": reps * launches,
+        "clocks": clocks,
+    }
+
+
 def cpu_sample_time(p, budget_s, threads):
     """Time the oracle on a column sample of p; returns (us per full call, desc)."""
     import oracle
@@ -598,6 +730,11 @@ def main():
         specs = [f"{n}:{i}" for n, c in workloads.WORKLOADS.items() for i in range(len(c))]
     for spec in specs:
         args.workload = spec
+        if parse_workload(spec)[0] in LAYER_STEPS:
+            line = run_layer_step(args, rank, world, local_rank)
+            if rank == 0:
+                print(json.dumps(line), flush=True)
+            continue
         if parse_workload(spec)[0] in workloads.QUANTIZE_WORKLOADS:
             line = run_quantize(args, rank, world, local_rank)
             if rank == 0:

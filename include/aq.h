@@ -132,6 +132,51 @@ aq_status aq_matmul_bf16(const void *x_dev, const uint32_t *Wq_dev, const void *
                          const void *biases_dev, int64_t M, int64_t N, int64_t K, int bits,
                          void *out_dev, void *stream);
 
+/* Largest number of projections aq_matmul_multi takes in one call. */
+#define AQ_MAX_PROJ 4
+
+/*
+ * aq_matmul_multi — several projections of the same activations in one call:
+ * y_j[M][N[j]] = x[M][K] . dequant(W_j)^T for j < nproj (1..AQ_MAX_PROJ),
+ * all with the same K and bits, e.g. the q, k and v projections of a
+ * decoder layer.  The small projections then share one launch instead of
+ * each paying its own (the pages' fused multi-projection decode idea).
+ *   dtype       AQ_F16 or AQ_BF16: the type of x and of every y_j.
+ *   Wq_dev, scales_dev, biases_dev, out_dev, N: host arrays of nproj
+ *               entries; entry j is projection j, laid out and owned as in
+ *               aq_matmul (device pointers, out caller-allocated).
+ * M <= 32 with K % 512 == 0 and 16-byte alignment runs as one launch of the
+ * resident small-M kernel; anything else runs one launch per projection
+ * under the usual dispatch rule, with the same results.  Outputs must not
+ * overlap each other, x or the weights.
+ * Errors: AQ_ERR_INVALID_ARG for a bad dtype, nproj outside 1..AQ_MAX_PROJ,
+ * a NULL array, or any projection that aq_matmul would reject; otherwise as
+ * aq_matmul.
+ */
+aq_status aq_matmul_multi(int dtype, const void *x_dev, int nproj,
+                          const uint32_t *const *Wq_dev, const void *const *scales_dev,
+                          const void *const *biases_dev, const int64_t *N, int64_t M,
+                          int64_t K, int bits, void *const *out_dev, void *stream);
+
+/*
+ * aq_matmul_gate_up — the gated MLP input of a decoder layer in one call:
+ * h[M][N] = silu(x . dequant(W_gate)^T) * (x . dequant(W_up)^T), with
+ * silu(g) = g / (1 + exp(-g)), both products accumulated in fp32 and h
+ * rounded once to x's dtype (the pages' fused gate/up + SiLU epilogue).
+ * Every CTA decodes the same rows of both projections, so the gate value
+ * never leaves the SM.  Both weight sets are [N][K] as in aq_matmul.
+ *   dtype    AQ_F16 or AQ_BF16 (x and h).
+ *   out_dev  h [M][N], device, caller-allocated.
+ * Served for M <= 32, K % 512 == 0, 16-byte alignment and N up to 128 rows
+ * per SM (19456 on 152 SMs); otherwise AQ_ERR_UNSUPPORTED and nothing is
+ * queued.  Errors otherwise as aq_matmul.
+ */
+aq_status aq_matmul_gate_up(int dtype, const void *x_dev, const uint32_t *Wg_dev,
+                            const void *scales_g_dev, const void *biases_g_dev,
+                            const uint32_t *Wu_dev, const void *scales_u_dev,
+                            const void *biases_u_dev, int64_t M, int64_t N, int64_t K,
+                            int bits, void *out_dev, void *stream);
+
 /*
  * aq_matmul_variant — aq_matmul / aq_matmul_bf16 with the element type as an
  * argument and, optionally, an explicit kernel variant (AQ_VARIANT_AUTO lets

@@ -23,7 +23,7 @@ from . import build as _build
 __all__ = [
     "AqError", "AQ_F16", "AQ_BF16", "AQ_VARIANT_AUTO", "AQ_VARIANT_GENERIC", "AQ_VARIANT_QMV",
     "AQ_VARIANT_TC", "AQ_VARIANT_GEMV", "AQ_NUM_VARIANTS", "aq_pack", "aq_quantize",
-    "aq_quantize_bf16", "aq_matmul", "aq_matmul_bf16",
+    "aq_quantize_bf16", "aq_matmul", "aq_matmul_bf16", "aq_matmul_multi", "aq_matmul_gate_up",
     "aq_matmul_variant", "aq_matmul_host", "aq_select", "aq_describe", "aq_stats", "aq_device_error",
     "aq_free", "aq_status_string", "aq_variant_name", "aq_version", "lib_path", "load",
 ]
@@ -62,6 +62,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     sig = {
         "aq_pack": ([p, i64, i64, i32, p, p], i32),
         "aq_quantize": ([p, i64, i64, i32, p, p, p, p], i32),
+        "aq_matmul_multi": ([i32, p, i32, p, p, p, p, i64, i64, i32, p, p], i32),
+        "aq_matmul_gate_up": ([i32, p, p, p, p, p, p, p, i64, i64, i64, i32, p, p], i32),
         "aq_quantize_bf16": ([p, i64, i64, i32, p, p, p, p], i32),
         "aq_matmul": ([p, p, p, p, i64, i64, i64, i32, p, p], i32),
         "aq_matmul_bf16": ([p, p, p, p, i64, i64, i64, i32, p, p], i32),
@@ -180,6 +182,47 @@ def aq_matmul(x, Wq, scales, biases, bits, out=None, stream=None) -> torch.Tenso
 def aq_matmul_bf16(x, Wq, scales, biases, bits, out=None, stream=None) -> torch.Tensor:
     """y = x . dequant(W)^T for bf16 x [..., K]; returns bf16 [..., N]."""
     return _mm(AQ_VARIANT_AUTO, AQ_BF16, x, Wq, scales, biases, bits, out, stream)
+
+
+def aq_matmul_multi(x, weights, bits, outs=None, stream=None) -> list:
+    """Several projections of the same x in one call: weights is a list of
+    (Wq, scales, biases) triples (1..4); returns [y_j] in x's dtype."""
+    dtype = AQ_BF16 if x.dtype == torch.bfloat16 else AQ_F16
+    P = len(weights)
+    K = x.shape[-1]
+    M = x.numel() // K if K else 0
+    Ns = [w[1].shape[0] for w in weights]
+    if outs is None:
+        outs = [torch.empty((*x.shape[:-1], n), dtype=x.dtype, device=x.device) for n in Ns]
+    ptr_arr = ctypes.c_void_p * max(P, 1)
+    Wp = ptr_arr(*[_dev(w[0], "Wq") for w in weights])
+    Sp = ptr_arr(*[_dev(w[1], "scales") for w in weights])
+    Bp = ptr_arr(*[_dev(w[2], "biases") for w in weights])
+    Op = ptr_arr(*[_dev(o, "out") for o in outs])
+    Na = (ctypes.c_int64 * max(P, 1))(*Ns)
+    _check(load().aq_matmul_multi(dtype, _dev(x, "x"), P, ctypes.cast(Wp, ctypes.c_void_p),
+                                  ctypes.cast(Sp, ctypes.c_void_p), ctypes.cast(Bp, ctypes.c_void_p),
+                                  ctypes.cast(Na, ctypes.c_void_p), M, K, bits,
+                                  ctypes.cast(Op, ctypes.c_void_p), _stream(stream)),
+           "aq_matmul_multi")
+    return outs
+
+
+def aq_matmul_gate_up(x, gate, up, bits, out=None, stream=None) -> torch.Tensor:
+    """h = silu(x . W_gate^T) * (x . W_up^T); gate and up are (Wq, scales,
+    biases) triples with the same N."""
+    dtype = AQ_BF16 if x.dtype == torch.bfloat16 else AQ_F16
+    K = x.shape[-1]
+    M = x.numel() // K if K else 0
+    N = gate[1].shape[0]
+    if out is None:
+        out = torch.empty((*x.shape[:-1], N), dtype=x.dtype, device=x.device)
+    _check(load().aq_matmul_gate_up(dtype, _dev(x, "x"), _dev(gate[0], "Wq"),
+                                    _dev(gate[1], "scales"), _dev(gate[2], "biases"),
+                                    _dev(up[0], "Wq"), _dev(up[1], "scales"),
+                                    _dev(up[2], "biases"), M, N, K, bits, _dev(out, "out"),
+                                    _stream(stream)), "aq_matmul_gate_up")
+    return out
 
 
 def aq_matmul_variant(variant, x, Wq, scales, biases, bits, out=None, stream=None):

@@ -232,6 +232,74 @@ aq_status aq_matmul_bf16(const void *x_dev, const uint32_t *Wq_dev, const void *
                                           bits, out_dev, stream));
 }
 
+aq_status aq_matmul_multi(int dtype, const void *x_dev, int nproj, const uint32_t *const *Wq_dev,
+                          const void *const *scales_dev, const void *const *biases_dev,
+                          const int64_t *N, int64_t M, int64_t K, int bits, void *const *out_dev,
+                          void *stream) {
+    if (dtype != AQ_F16 && dtype != AQ_BF16) return AQ_ERR_INVALID_ARG;
+    if (nproj < 1 || nproj > AQ_MAX_PROJ || !Wq_dev || !scales_dev || !biases_dev || !N ||
+        !out_dev)
+        return AQ_ERR_INVALID_ARG;
+    MultiArgs m{};
+    m.a = make_args(dtype, x_dev, nullptr, nullptr, nullptr, M, 0, K, bits, nullptr, stream);
+    m.nproj = nproj;
+    m.gate_up = false;
+    MatmulArgs each[AQ_MAX_PROJ];
+    for (int j = 0; j < nproj; ++j) {
+        each[j] = make_args(dtype, x_dev, Wq_dev[j], scales_dev[j], biases_dev[j], M, N[j], K,
+                            bits, out_dev[j], stream);
+        const aq_status st = check_args(each[j]);
+        if (st != AQ_OK) return st;
+        m.Wq[j] = Wq_dev[j];
+        m.scales[j] = scales_dev[j];
+        m.biases[j] = biases_dev[j];
+        m.out[j] = out_dev[j];
+        m.N[j] = N[j];
+    }
+    if (M <= gemv_max_m() && gemv_multi_supported(m)) {
+        if (gemv_launch_multi(m) != cudaSuccess) return AQ_ERR_CUDA;
+        g_calls[AQ_VARIANT_GEMV].fetch_add(1, std::memory_order_relaxed);
+        return AQ_OK;
+    }
+    // otherwise one launch per projection, each by the dispatch rule
+    for (int j = 0; j < nproj; ++j) {
+        const aq_status st = run(AQ_VARIANT_AUTO, each[j]);
+        if (st != AQ_OK) return st;
+    }
+    return AQ_OK;
+}
+
+aq_status aq_matmul_gate_up(int dtype, const void *x_dev, const uint32_t *Wg_dev,
+                            const void *scales_g_dev, const void *biases_g_dev,
+                            const uint32_t *Wu_dev, const void *scales_u_dev,
+                            const void *biases_u_dev, int64_t M, int64_t N, int64_t K, int bits,
+                            void *out_dev, void *stream) {
+    if (dtype != AQ_F16 && dtype != AQ_BF16) return AQ_ERR_INVALID_ARG;
+    const MatmulArgs g = make_args(dtype, x_dev, Wg_dev, scales_g_dev, biases_g_dev, M, N, K,
+                                   bits, out_dev, stream);
+    const MatmulArgs u = make_args(dtype, x_dev, Wu_dev, scales_u_dev, biases_u_dev, M, N, K,
+                                   bits, out_dev, stream);
+    aq_status st = check_args(g);
+    if (st == AQ_OK) st = check_args(u);
+    if (st != AQ_OK) return st;
+    MultiArgs m{};
+    m.a = g;
+    m.nproj = 2;
+    m.gate_up = true;
+    m.Wq[0] = Wg_dev;
+    m.scales[0] = scales_g_dev;
+    m.biases[0] = biases_g_dev;
+    m.Wq[1] = Wu_dev;
+    m.scales[1] = scales_u_dev;
+    m.biases[1] = biases_u_dev;
+    m.N[0] = m.N[1] = N;
+    m.out[0] = m.out[1] = out_dev;
+    if (!gemv_multi_supported(m)) return AQ_ERR_UNSUPPORTED;
+    if (gemv_launch_multi(m) != cudaSuccess) return AQ_ERR_CUDA;
+    g_calls[AQ_VARIANT_GEMV].fetch_add(1, std::memory_order_relaxed);
+    return AQ_OK;
+}
+
 aq_status aq_matmul_variant(int variant, int dtype, const void *x_dev, const uint32_t *Wq_dev,
                             const void *scales_dev, const void *biases_dev, int64_t M, int64_t N,
                             int64_t K, int bits, void *out_dev, void *stream) {

@@ -49,9 +49,24 @@ uint32_t *error_word() {
     return ptr;
 }
 
-bool gemv_plan(const MatmulArgs &a, GemvPlan &pl) {
-    if (a.M < 1 || a.M > 32 || a.N < 1 || a.K < 512 || a.K % 512 != 0) return false;
-    if (a.N > INT32_MAX / 2 || a.K > INT32_MAX / 2) return false;
+// The plan of a launch.  Several projections of the same x (n_proj[0..nproj),
+// a.N unused): their rows are split evenly over the SMs, each CTA within one
+// projection.  gate_up: two projections of a.N rows, every CTA the same rows
+// of both (two passes).
+bool gemv_plan(const MatmulArgs &a, GemvPlan &pl, const int64_t *n_proj, int nproj,
+               bool gate_up) {
+    if (nproj < 1 || nproj > kMaxProj || (gate_up && nproj != 2)) return false;
+    int64_t n_rows = a.N;
+    if (nproj > 1 && !gate_up) {
+        n_rows = 0;
+        for (int j = 0; j < nproj; ++j) {
+            if (n_proj[j] < 1 || n_proj[j] > INT32_MAX / 2) return false;
+            n_rows += n_proj[j];
+        }
+    }
+    if (a.M < 1 || a.M > 32 || n_rows < 1 || a.K < 512 || a.K % 512 != 0) return false;
+    if (n_rows > INT32_MAX / 2) return false;
+    if (a.K > INT32_MAX / 2) return false;
     const int B = a.bits;
     const int G = (int)(a.K / 64);
     const int MB = a.M > 16 ? 4 : a.M > 8 ? 2 : 1;
@@ -60,25 +75,48 @@ bool gemv_plan(const MatmulArgs &a, GemvPlan &pl) {
     // CTA has the SM to itself and all of its shared memory.
     const size_t budget = MB > 2 ? kSmemMax : smem_budget();
     const int sms = num_sms();
-    const int64_t per_sm = (a.N + sms - 1) / sms;
-    const int passes = (int)((per_sm + 16 * max_tiles - 1) / (16 * max_tiles));
-    const int pr = (int)((per_sm + passes - 1) / passes);
-    const int64_t rows_cta = (int64_t)pr * passes;
+    const int64_t per_sm = (n_rows + sms - 1) / sms;
+    int passes = (int)((per_sm + 16 * max_tiles - 1) / (16 * max_tiles));
+    int pr = (int)((per_sm + passes - 1) / passes);
+    int64_t rows_cta = (int64_t)pr * passes;
+    if (gate_up) {  // pass 0 the gate, pass 1 the up rows, the same rows
+        if (per_sm > 16 * max_tiles) return false;
+        passes = 2;
+        pr = (int)per_sm;
+        rows_cta = pr;
+    }
     GemvParams &q = pl.prm;
     q.M = (int)a.M;
-    q.N = (int)a.N;
+    q.N = (int)n_rows;
     q.K = (int)a.K;
     q.rows_cta = (int)rows_cta;
     q.pass_rows = pr;
     q.passes = passes;
     q.tiles = (pr + 15) / 16;
-    pl.grid = (int)((a.N + rows_cta - 1) / rows_cta);
+    q.nproj = nproj;
+    q.gate_up = gate_up ? 1 : 0;
+    if (nproj > 1 && !gate_up) {
+        int c = 0;
+        for (int j = 0; j < nproj; ++j) {
+            q.cta0[j] = c;
+            q.n_proj[j] = (int)n_proj[j];
+            c += (int)((n_proj[j] + rows_cta - 1) / rows_cta);
+        }
+        q.cta0[nproj] = c;
+        pl.grid = c;
+    } else {
+        pl.grid = (int)((a.N + rows_cta - 1) / rows_cta);
+        q.cta0[0] = 0;
+        q.cta0[1] = pl.grid;
+        q.n_proj[0] = q.n_proj[1] = (int)a.N;
+    }
     const uint32_t rows_pad = 16u * (uint32_t)q.tiles;
     const uint32_t box = B == 4 ? 128u : 96u;
     pl.mb = MB;
     pl.bits = B;
     pl.bf16 = a.dtype == AQ_BF16;
     const uint32_t red_bytes = (uint32_t)kConsumers * q.tiles * MB * 32 * 4 * 4;
+    const uint32_t gu_bytes = gate_up ? round_up((uint32_t)pr * (uint32_t)a.M * 4u, 128u) : 0u;
 
     // The widest stage (most groups per warp) that keeps at least three
     // stages in the ring (or the whole of K), else two; x whole in shared
@@ -117,8 +155,8 @@ bool gemv_plan(const MatmulArgs &a, GemvPlan &pl) {
                     const size_t bars = 2 * 8 * (size_t)total + 16 + 16;
                     // With one pass the partial tiles reuse the ring if it is large enough.
                     for (int alias = passes == 1 ? 1 : 0; alias >= 0; --alias) {
-                        const size_t fixed =
-                            x_bytes + (alias ? 0 : red_bytes) + bars + 1024 /* alignment */;
+                        const size_t fixed = x_bytes + (alias ? 0 : red_bytes) + gu_bytes + bars +
+                                             1024 /* alignment */;
                         if (fixed >= budget) continue;
                         const int ring =
                             (int)std::min<size_t>((size_t)total, (budget - fixed) / q.slot_bytes);
@@ -132,11 +170,14 @@ bool gemv_plan(const MatmulArgs &a, GemvPlan &pl) {
                         off += x_bytes;
                         q.off_red = alias ? 0u : (uint32_t)off;
                         off += alias ? 0 : red_bytes;
+                        q.off_gu = (uint32_t)off;
+                        off += gu_bytes;
                         q.off_bar = (uint32_t)off;
                         off += 2 * 8 * (size_t)ring + 16 + 16;
                         pl.smem = off + 1024;
                         q.x = a.x;
                         q.y = a.out;
+                        q.y_proj[0] = a.out;
                         q.err = nullptr;
                         pl.wps = wps;
                         if (pl.smem <= budget) return true;
@@ -149,27 +190,25 @@ bool gemv_plan(const MatmulArgs &a, GemvPlan &pl) {
 }
 
 template <int B, bool BF16, int TILES>
-cudaError_t launch_wps(const GemvPlan &pl, const CUtensorMap &tw, const CUtensorMap &ts,
-                       const CUtensorMap &tb, const CUtensorMap &tx, cudaStream_t s) {
+cudaError_t launch_wps(const GemvPlan &pl, const GemvMaps &m, cudaStream_t s) {
     if constexpr (TILES <= 2)
-        if (pl.wps == 4) return launch_t<B, BF16, TILES, 4, 1, false>(pl, tw, ts, tb, tx, s);
+        if (pl.wps == 4) return launch_t<B, BF16, TILES, 4, 1, false>(pl, m, s);
     if constexpr (TILES <= 4)
-        if (pl.wps == 2) return launch_t<B, BF16, TILES, 2, 1, false>(pl, tw, ts, tb, tx, s);
-    return launch_t<B, BF16, TILES, 1, 1, false>(pl, tw, ts, tb, tx, s);
+        if (pl.wps == 2) return launch_t<B, BF16, TILES, 2, 1, false>(pl, m, s);
+    return launch_t<B, BF16, TILES, 1, 1, false>(pl, m, s);
 }
 
 template <int B, bool BF16>
-cudaError_t launch_tiles(const GemvPlan &pl, const CUtensorMap &tw, const CUtensorMap &ts,
-                         const CUtensorMap &tb, const CUtensorMap &tx, cudaStream_t s) {
+cudaError_t launch_tiles(const GemvPlan &pl, const GemvMaps &m, cudaStream_t s) {
     switch (pl.prm.tiles) {
-        case 1: return launch_wps<B, BF16, 1>(pl, tw, ts, tb, tx, s);
-        case 2: return launch_wps<B, BF16, 2>(pl, tw, ts, tb, tx, s);
-        case 3: return launch_wps<B, BF16, 3>(pl, tw, ts, tb, tx, s);
-        case 4: return launch_wps<B, BF16, 4>(pl, tw, ts, tb, tx, s);
-        case 5: return launch_wps<B, BF16, 5>(pl, tw, ts, tb, tx, s);
-        case 6: return launch_wps<B, BF16, 6>(pl, tw, ts, tb, tx, s);
-        case 7: return launch_wps<B, BF16, 7>(pl, tw, ts, tb, tx, s);
-        default: return launch_wps<B, BF16, 8>(pl, tw, ts, tb, tx, s);
+        case 1: return launch_wps<B, BF16, 1>(pl, m, s);
+        case 2: return launch_wps<B, BF16, 2>(pl, m, s);
+        case 3: return launch_wps<B, BF16, 3>(pl, m, s);
+        case 4: return launch_wps<B, BF16, 4>(pl, m, s);
+        case 5: return launch_wps<B, BF16, 5>(pl, m, s);
+        case 6: return launch_wps<B, BF16, 6>(pl, m, s);
+        case 7: return launch_wps<B, BF16, 7>(pl, m, s);
+        default: return launch_wps<B, BF16, 8>(pl, m, s);
     }
 }
 
@@ -184,60 +223,102 @@ bool gemv_supported(const MatmulArgs &a) {
         !aligned(a.biases, 16))
         return false;
     GemvPlan pl;
-    return gemv_plan(a, pl);
+    return gemv_plan(a, pl, nullptr, 1, false);
 }
 
-cudaError_t gemv_launch(const MatmulArgs &a) {
-    GemvPlan pl;
-    if (!gemv_plan(a, pl)) return cudaErrorInvalidValue;
+namespace {
+
+// Tensor maps for the plan and launch.  Projection j's codes, scales and
+// biases are Wq[j], sc[j], bi[j] with n[j] rows.
+cudaError_t launch_plan(const MatmulArgs &a, GemvPlan &pl, const uint32_t *const *Wq,
+                        const void *const *sc, const void *const *bi, const int64_t *n,
+                        int nproj) {
     const uint64_t row_bytes = (uint64_t)a.K * a.bits / 8, G = (uint64_t)a.K / 64;
     const uint32_t pr = (uint32_t)pl.prm.pass_rows, sg = (uint32_t)pl.prm.sg;
     const uint64_t box = a.bits == 4 ? 128 : 96;
-    // codes as [row_bytes / box][N][box] bytes: one box = sg/4 column blocks x pr rows
-    const uint64_t wdims[3] = {box, (uint64_t)a.N, row_bytes / box};
-    const uint64_t wstrides[2] = {row_bytes, box};
-    const uint32_t wbox[3] = {(uint32_t)box, pr, sg / 4};
-    // scales, biases as [G / 8][N][8] halves: one box = sg/8 blocks of 8 groups x pr rows
-    const uint64_t sdims[3] = {8, (uint64_t)a.N, G / 8};
-    const uint64_t sstrides[2] = {2 * G, 16};
-    const uint32_t sbox[3] = {8, pr, sg / 8};
-    CUtensorMap tw, ts, tb;
-    CUtensorMap tx = {};
+    gemv::GemvMaps maps;
+    memset(&maps, 0, sizeof(maps));
     const bool staged = !pl.prm.x_whole;
     if (staged) {
         // x as [G][M][64] elements: one box = the stage's groups x M rows
         const uint64_t xdims[3] = {64, (uint64_t)a.M, G};
         const uint64_t xstrides[2] = {(uint64_t)a.K * 2, 128};
         const uint32_t xbox[3] = {64, (uint32_t)a.M, sg};
-        if (!tmap_encode(&tx, a.dtype == AQ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+        if (!tmap_encode(&maps.x, a.dtype == AQ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                          3, a.x, xdims, xstrides, xbox, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
+    for (int j = 0; j < nproj; ++j) {
+        // codes as [row_bytes / box][N][box] bytes: one box = sg/4 column blocks x pr rows
+        const uint64_t wdims[3] = {box, (uint64_t)n[j], row_bytes / box};
+        const uint64_t wstrides[2] = {row_bytes, box};
+        const uint32_t wbox[3] = {(uint32_t)box, pr, sg / 4};
+        // scales, biases as [G / 8][N][8] halves: one box = sg/8 blocks of 8 groups x pr rows
+        const uint64_t sdims[3] = {8, (uint64_t)n[j], G / 8};
+        const uint64_t sstrides[2] = {2 * G, 16};
+        const uint32_t sbox[3] = {8, pr, sg / 8};
+        if (!tmap_encode(&maps.w[j], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, Wq[j], wdims, wstrides,
+                         wbox,
+                         a.bits == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !tmap_encode(&maps.s[j], CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, sc[j], sdims, sstrides,
+                         sbox, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !tmap_encode(&maps.b[j], CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, bi[j], sdims, sstrides,
+                         sbox, CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     }
     pl.prm.err = gemv::error_word();
     if (!pl.prm.err) return cudaErrorInvalidValue;
-    if (!tmap_encode(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.Wq, wdims, wstrides, wbox,
-                     a.bits == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !tmap_encode(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, a.scales, sdims, sstrides, sbox,
-                     CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !tmap_encode(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, a.biases, sdims, sstrides, sbox,
-                     CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cudaErrorInvalidValue;
-    if (pl.mb > 2) return gemv::launch_mb4(pl, tw, ts, tb, tx, a.stream);
-    if (pl.mb > 1) return gemv::launch_mb2(pl, tw, ts, tb, tx, a.stream);
-    if (staged) return gemv::launch_staged1(pl, tw, ts, tb, tx, a.stream);
-    tx = tw;  // unused when x is whole
+    if (pl.mb > 2) return gemv::launch_mb4(pl, maps, a.stream);
+    if (pl.mb > 1) return gemv::launch_mb2(pl, maps, a.stream);
+    if (staged) return gemv::launch_staged1(pl, maps, a.stream);
     const bool bf = a.dtype == AQ_BF16;
     if (a.bits == 3)
-        return bf ? gemv::launch_tiles<3, true>(pl, tw, ts, tb, tx, a.stream)
-                  : gemv::launch_tiles<3, false>(pl, tw, ts, tb, tx, a.stream);
-    return bf ? gemv::launch_tiles<4, true>(pl, tw, ts, tb, tx, a.stream)
-              : gemv::launch_tiles<4, false>(pl, tw, ts, tb, tx, a.stream);
+        return bf ? gemv::launch_tiles<3, true>(pl, maps, a.stream)
+                  : gemv::launch_tiles<3, false>(pl, maps, a.stream);
+    return bf ? gemv::launch_tiles<4, true>(pl, maps, a.stream)
+              : gemv::launch_tiles<4, false>(pl, maps, a.stream);
+}
+
+}  // namespace
+
+cudaError_t gemv_launch(const MatmulArgs &a) {
+    GemvPlan pl;
+    if (!gemv_plan(a, pl, nullptr, 1, false)) return cudaErrorInvalidValue;
+    const int64_t n = a.N;
+    return launch_plan(a, pl, &a.Wq, &a.scales, &a.biases, &n, 1);
+}
+
+bool gemv_multi_supported(const MultiArgs &m) {
+    if (!aligned(m.a.x, 16)) return false;
+    for (int j = 0; j < m.nproj; ++j)
+        if (!aligned(m.Wq[j], 16) || !aligned(m.scales[j], 16) || !aligned(m.biases[j], 16))
+            return false;
+    GemvPlan pl;
+    return gemv_plan(m.a, pl, m.N, m.nproj, m.gate_up);
+}
+
+cudaError_t gemv_launch_multi(const MultiArgs &m) {
+    GemvPlan pl;
+    if (!gemv_plan(m.a, pl, m.N, m.nproj, m.gate_up)) return cudaErrorInvalidValue;
+    for (int j = 0; j < m.nproj; ++j) pl.prm.y_proj[j] = m.gate_up ? m.a.out : m.out[j];
+    return launch_plan(m.a, pl, m.Wq, m.scales, m.biases, m.N, m.nproj);
+}
+
+int gemv_describe_multi(const MultiArgs &m, char *buf, int len) {
+    GemvPlan pl;
+    if (!gemv_plan(m.a, pl, m.N, m.nproj, m.gate_up)) return snprintf(buf, len, "gemv: unsupported");
+    const gemv::GemvParams &q = pl.prm;
+    return snprintf(buf, len,
+                    "gemv %s projections=%d rows/cta=%d passes=%d tiles=%d colblocks=%d "
+                    "groups/stage=%d stages=%d ring=%d x=%s grid=%d smem=%zu",
+                    m.gate_up ? "gate_up" : "multi", m.nproj, q.rows_cta, q.passes, q.tiles, pl.mb,
+                    q.sg, q.n_stages, q.ring, q.x_whole ? "whole" : "staged", pl.grid, pl.smem);
 }
 
 int gemv_describe(const MatmulArgs &a, char *buf, int len) {
     GemvPlan pl;
-    if (!gemv_plan(a, pl)) return snprintf(buf, len, "gemv: unsupported");
+    if (!gemv_plan(a, pl, nullptr, 1, false)) return snprintf(buf, len, "gemv: unsupported");
     const gemv::GemvParams &q = pl.prm;
     return snprintf(buf, len,
                     "gemv rows/cta=%d passes=%d tiles=%d colblocks=%d groups/stage=%d stages=%d "

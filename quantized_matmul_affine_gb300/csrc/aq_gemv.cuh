@@ -73,7 +73,8 @@ namespace gemv {
 
 constexpr int kConsumers = 8;                     // consumer warps
 constexpr int kGemvThreads = (kConsumers + 1) * 32;  // + one producer warp
-constexpr int kMaxTiles = 8;                      // 16-row tiles per pass
+constexpr int kMaxTiles = 8;
+constexpr int kMaxProj = 4;       // projections of one x per launch                      // 16-row tiles per pass
 constexpr int kMaxPassRows = 16 * kMaxTiles;
 constexpr int kXPitch = 144;     // bytes per activation row in an x slot (128 + 16: no bank conflicts)
 // An x slot holds one group of every activation row (M rows at kXPitch),
@@ -102,6 +103,24 @@ struct GemvParams {
     uint32_t off_xst;       // staged x: box inside a ring slot
     int x_rows;             // staged x: rows per group in the box (= M)
     uint32_t stage_tx;      // bytes one stage brings in
+    // Several projections of the same x in one launch.  Independent outputs:
+    // CTAs cta0[j] .. cta0[j+1]-1 take projection j.  Gate/up (gate_up = 1,
+    // two projections of equal N): every CTA takes the same rows of both,
+    // pass 0 the gate and pass 1 the up projection, and writes
+    // silu(gate) * up; the gate's rows wait in shared memory at off_gu.
+    int nproj;
+    int gate_up;
+    int cta0[kMaxProj + 1];
+    int n_proj[kMaxProj];
+    void *y_proj[kMaxProj];
+    uint32_t off_gu;
+};
+
+// Tensor maps of one launch: x (staged x only) and the codes, scales and
+// biases of each projection.
+struct GemvMaps {
+    CUtensorMap x;
+    CUtensorMap w[kMaxProj], s[kMaxProj], b[kMaxProj];
 };
 
 __device__ __forceinline__ void consumers_sync() {
@@ -284,9 +303,7 @@ __device__ __forceinline__ void store_y<__nv_bfloat16>(__nv_bfloat16 *p, float v
 
 template <int B, bool BF16, int TILES, int WPS, int MB, bool XST>
 __global__ void __launch_bounds__(kGemvThreads, MB > 2 ? 1 : 2)
-    gemv_kernel(const __grid_constant__ GemvParams p, const __grid_constant__ CUtensorMap tm_w,
-                const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_b,
-                const __grid_constant__ CUtensorMap tm_x) {
+    gemv_kernel(const __grid_constant__ GemvParams p, const __grid_constant__ GemvMaps mp) {
     constexpr bool kXStage = XST;  // x streamed per stage by a fourth producer lane
     using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
     constexpr int kBox = B == 4 ? 128 : 96;  // bytes of a row in one column block (4 groups)
@@ -319,7 +336,10 @@ __global__ void __launch_bounds__(kGemvThreads, MB > 2 ? 1 : 2)
     // alive triggers at that point (consumers after their copy, the
     // producer lanes once x_landed completes).
 
-    const int row_cta = blockIdx.x * p.rows_cta;
+    int proj = 0;  // this CTA's projection (independent outputs)
+    if (!p.gate_up)
+        while (proj + 1 < p.nproj && (int)blockIdx.x >= p.cta0[proj + 1]) ++proj;
+    const int row_cta = ((int)blockIdx.x - p.cta0[proj]) * p.rows_cta;
     const int total = p.passes * p.n_stages;
     const int nb = p.sg / 4;  // column blocks per stage
 
@@ -329,8 +349,13 @@ __global__ void __launch_bounds__(kGemvThreads, MB > 2 ? 1 : 2)
         // each (pass, stage) in order; lane 0 also posts the byte count.
         // ------------------------------------------------------------------
         if (lane < (kXStage ? 4 : 3)) {
-            const CUtensorMap *tm = lane == 0 ? &tm_w : lane == 1 ? &tm_s : lane == 2 ? &tm_b : &tm_x;
+            // the lane's map for projection j (lane 3: x)
+            auto map_of = [&](int j) -> const CUtensorMap * {
+                return lane == 0 ? &mp.w[j] : lane == 1 ? &mp.s[j] : lane == 2 ? &mp.b[j] : &mp.x;
+            };
+            const CUtensorMap *tm = map_of(proj);
             prefetch_tmap(tm);
+            if (p.gate_up) prefetch_tmap(map_of(1));
             if (lane == 3) grid_dependency_wait();  // x belongs to the stream order
             bool triggered = false;
             int it = 0, slot = 0, lap = 0, pass = 0, s = 0;
@@ -343,7 +368,9 @@ __global__ void __launch_bounds__(kGemvThreads, MB > 2 ? 1 : 2)
                     gemv_record(flag, p.err, ERR_GEMV_EMPTY);
                     break;
                 }
-                const int r0 = row_cta + pass * p.pass_rows;
+                // gate/up: the same rows of projection `pass`
+                const int r0 = p.gate_up ? row_cta : row_cta + pass * p.pass_rows;
+                if (p.gate_up) tm = map_of(pass);
                 uint8_t *dst = smem + (size_t)slot * p.slot_bytes;
                 if (lane == 3) {
                     tma_load_3d(dst + p.off_xst, tm, 0, 0, s * p.sg, &full[slot]);
@@ -496,7 +523,9 @@ __global__ void __launch_bounds__(kGemvThreads, MB > 2 ? 1 : 2)
         consumers_sync();
     }
 
-    T *y = static_cast<T *>(p.y);
+    T *y = static_cast<T *>(p.y_proj[proj]);
+    const int Np = p.n_proj[proj];
+    float *gbuf = reinterpret_cast<float *>(smem + p.off_gu);  // gate/up: the gate's rows
     float *red = reinterpret_cast<float *>(smem + p.off_red);
     const int pr = p.pass_rows;
 
@@ -660,8 +689,8 @@ __global__ void __launch_bounds__(kGemvThreads, MB > 2 ? 1 : 2)
                 *reinterpret_cast<float4 *>(&red[(((warp * TILES + t) * MB + mb) * 32 + lane) * 4]) =
                     make_float4(acc[t][mb][0], acc[t][mb][1], acc[t][mb][2], acc[t][mb][3]);
         consumers_sync();
-        const int r0 = row_cta + pass * pr;
-        const int rows = std::min(pr, p.N - r0);
+        const int r0 = p.gate_up ? row_cta : row_cta + pass * pr;
+        const int rows = std::min(pr, Np - r0);
         for (int e = threadIdx.x; e < rows * M; e += kConsumers * 32) {
             const int m = e / rows, r = e - m * rows;
             const int t = r >> 4, rr = r & 15;
@@ -673,7 +702,15 @@ __global__ void __launch_bounds__(kGemvThreads, MB > 2 ? 1 : 2)
             for (int w = 0; w < kConsumers; ++w)
                 v += red[(((w * TILES + t) * MB + mb) * 32 + ln) * 4 + i];
             if constexpr (!kMmaBf16) v *= 16777216.f;  // 2^24
-            store_y<T>(&y[(int64_t)m * p.N + r0 + r], v);
+            if (p.gate_up) {
+                if (pass == 0) {  // the gate waits for the up projection
+                    gbuf[m * pr + r] = v;
+                    continue;
+                }
+                const float gt = gbuf[m * pr + r];
+                v = gt / (1.f + expf(-gt)) * v;  // silu(gate) * up
+            }
+            store_y<T>(&y[(int64_t)m * Np + r0 + r], v);
         }
         consumers_sync();  // the buffer is rewritten by the next pass
     }
@@ -695,8 +732,7 @@ struct GemvPlan {
 constexpr size_t kSmemMax = 227 * 1024;  // one CTA per SM at most
 
 template <int B, bool BF16, int TILES, int WPS, int MB, bool XST>
-cudaError_t launch_t(const GemvPlan &pl, const CUtensorMap &tw, const CUtensorMap &ts,
-                     const CUtensorMap &tb, const CUtensorMap &tx, cudaStream_t stream) {
+cudaError_t launch_t(const GemvPlan &pl, const GemvMaps &maps, cudaStream_t stream) {
     auto kern = gemv_kernel<B, BF16, TILES, WPS, MB, XST>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -715,17 +751,14 @@ cudaError_t launch_t(const GemvPlan &pl, const CUtensorMap &tw, const CUtensorMa
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, pl.prm, tw, ts, tb, tx);
+    return cudaLaunchKernelEx(&cfg, kern, pl.prm, maps);
 }
 
 // Staged x (x streamed with the weights): one column block in aq_gemv_xs.cu,
 // two (M = 9..16) in aq_gemv16.cu, four (M = 17..32) in aq_gemv32.cu.
-cudaError_t launch_mb4(const GemvPlan &pl, const CUtensorMap &tw, const CUtensorMap &ts,
-                       const CUtensorMap &tb, const CUtensorMap &tx, cudaStream_t stream);
-cudaError_t launch_staged1(const GemvPlan &pl, const CUtensorMap &tw, const CUtensorMap &ts,
-                           const CUtensorMap &tb, const CUtensorMap &tx, cudaStream_t stream);
-cudaError_t launch_mb2(const GemvPlan &pl, const CUtensorMap &tw, const CUtensorMap &ts,
-                       const CUtensorMap &tb, const CUtensorMap &tx, cudaStream_t stream);
+cudaError_t launch_mb4(const GemvPlan &pl, const GemvMaps &maps, cudaStream_t stream);
+cudaError_t launch_staged1(const GemvPlan &pl, const GemvMaps &maps, cudaStream_t stream);
+cudaError_t launch_mb2(const GemvPlan &pl, const GemvMaps &maps, cudaStream_t stream);
 
 }  // namespace gemv
 }  // namespace aq

@@ -8,28 +8,26 @@ namespace gemv {
 namespace {
 
 template <int B, bool BF16>
-cudaError_t mb4_tiles(const GemvPlan &pl, const CUtensorMap &tw, const CUtensorMap &ts,
-                      const CUtensorMap &tb, const CUtensorMap &tx, cudaStream_t s) {
+cudaError_t mb4_tiles(const GemvPlan &pl, const GemvMaps &m, cudaStream_t s) {
     switch (pl.prm.tiles) {
-        case 1: return launch_t<B, BF16, 1, 1, 4, true>(pl, tw, ts, tb, tx, s);
-        case 2: return launch_t<B, BF16, 2, 1, 4, true>(pl, tw, ts, tb, tx, s);
-        case 3: return launch_t<B, BF16, 3, 1, 4, true>(pl, tw, ts, tb, tx, s);
-        case 4: return launch_t<B, BF16, 4, 1, 4, true>(pl, tw, ts, tb, tx, s);
-        case 5: return launch_t<B, BF16, 5, 1, 4, true>(pl, tw, ts, tb, tx, s);
-        default: return launch_t<B, BF16, 6, 1, 4, true>(pl, tw, ts, tb, tx, s);
+        case 1: return launch_t<B, BF16, 1, 1, 4, true>(pl, m, s);
+        case 2: return launch_t<B, BF16, 2, 1, 4, true>(pl, m, s);
+        case 3: return launch_t<B, BF16, 3, 1, 4, true>(pl, m, s);
+        case 4: return launch_t<B, BF16, 4, 1, 4, true>(pl, m, s);
+        case 5: return launch_t<B, BF16, 5, 1, 4, true>(pl, m, s);
+        default: return launch_t<B, BF16, 6, 1, 4, true>(pl, m, s);
     }
 }
 
 }  // namespace
 
-cudaError_t launch_mb4(const GemvPlan &pl, const CUtensorMap &tw, const CUtensorMap &ts,
-                       const CUtensorMap &tb, const CUtensorMap &tx, cudaStream_t stream) {
+cudaError_t launch_mb4(const GemvPlan &pl, const GemvMaps &m, cudaStream_t stream) {
     if (pl.prm.tiles > 6) return cudaErrorInvalidValue;
     if (pl.bits == 3)
-        return pl.bf16 ? mb4_tiles<3, true>(pl, tw, ts, tb, tx, stream)
-                       : mb4_tiles<3, false>(pl, tw, ts, tb, tx, stream);
-    return pl.bf16 ? mb4_tiles<4, true>(pl, tw, ts, tb, tx, stream)
-                   : mb4_tiles<4, false>(pl, tw, ts, tb, tx, stream);
+        return pl.bf16 ? mb4_tiles<3, true>(pl, m, stream)
+                       : mb4_tiles<3, false>(pl, m, stream);
+    return pl.bf16 ? mb4_tiles<4, true>(pl, m, stream)
+                   : mb4_tiles<4, false>(pl, m, stream);
 }
 
 }  // namespace gemv

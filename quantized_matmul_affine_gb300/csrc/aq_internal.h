@@ -21,6 +21,21 @@ struct MatmulArgs {
     cudaStream_t stream;
 };
 
+// Several projections of one x in one launch (aq_matmul_multi) or the fused
+// gate/up pair (aq_matmul_gate_up: projection 0 the gate, 1 the up rows,
+// a.N rows each, y = silu(gate) * up in a.out).  a.Wq / a.scales / a.biases
+// are unused.
+struct MultiArgs {
+    MatmulArgs a;
+    int nproj;
+    bool gate_up;
+    const uint32_t *Wq[4];
+    const void *scales[4];
+    const void *biases[4];
+    void *out[4];
+    int64_t N[4];
+};
+
 // Device-side error codes (the word read by aq_device_error).  The low byte
 // names the kernel, the next byte the wait that gave up.
 enum : uint32_t {
@@ -39,6 +54,9 @@ cudaError_t generic_launch(const MatmulArgs &a);
 
 bool gemv_supported(const MatmulArgs &a);
 cudaError_t gemv_launch(const MatmulArgs &a);
+bool gemv_multi_supported(const MultiArgs &m);
+cudaError_t gemv_launch_multi(const MultiArgs &m);
+int gemv_describe_multi(const MultiArgs &m, char *buf, int len);
 int gemv_describe(const MatmulArgs &a, char *buf, int len);
 
 bool qmv_supported(const MatmulArgs &a);
