@@ -93,22 +93,25 @@ bool gemv_plan(const MatmulArgs &a, GemvPlan &pl, const int64_t *n_proj, int npr
     q.pass_rows = pr;
     q.passes = passes;
     q.tiles = (pr + 15) / 16;
-    q.nproj = nproj;
-    q.gate_up = gate_up ? 1 : 0;
+    GemvMulti &mx = pl.mx;
+    memset(&mx, 0, sizeof(mx));
+    pl.mp = nproj > 1 || gate_up;
+    mx.nproj = nproj;
+    mx.gate_up = gate_up ? 1 : 0;
     if (nproj > 1 && !gate_up) {
         int c = 0;
         for (int j = 0; j < nproj; ++j) {
-            q.cta0[j] = c;
-            q.n_proj[j] = (int)n_proj[j];
+            mx.cta0[j] = c;
+            mx.n_proj[j] = (int)n_proj[j];
             c += (int)((n_proj[j] + rows_cta - 1) / rows_cta);
         }
-        q.cta0[nproj] = c;
+        mx.cta0[nproj] = c;
         pl.grid = c;
     } else {
         pl.grid = (int)((a.N + rows_cta - 1) / rows_cta);
-        q.cta0[0] = 0;
-        q.cta0[1] = pl.grid;
-        q.n_proj[0] = q.n_proj[1] = (int)a.N;
+        mx.cta0[0] = 0;
+        mx.cta0[1] = pl.grid;
+        mx.n_proj[0] = mx.n_proj[1] = (int)a.N;
     }
     const uint32_t rows_pad = 16u * (uint32_t)q.tiles;
     const uint32_t box = B == 4 ? 128u : 96u;
@@ -170,14 +173,14 @@ bool gemv_plan(const MatmulArgs &a, GemvPlan &pl, const int64_t *n_proj, int npr
                         off += x_bytes;
                         q.off_red = alias ? 0u : (uint32_t)off;
                         off += alias ? 0 : red_bytes;
-                        q.off_gu = (uint32_t)off;
+                        mx.off_gu = (uint32_t)off;
                         off += gu_bytes;
                         q.off_bar = (uint32_t)off;
                         off += 2 * 8 * (size_t)ring + 16 + 16;
                         pl.smem = off + 1024;
                         q.x = a.x;
                         q.y = a.out;
-                        q.y_proj[0] = a.out;
+                        mx.y_proj[0] = a.out;
                         q.err = nullptr;
                         pl.wps = wps;
                         if (pl.smem <= budget) return true;
@@ -187,29 +190,6 @@ bool gemv_plan(const MatmulArgs &a, GemvPlan &pl, const int64_t *n_proj, int npr
         }
     }
     return false;
-}
-
-template <int B, bool BF16, int TILES>
-cudaError_t launch_wps(const GemvPlan &pl, const GemvMaps &m, cudaStream_t s) {
-    if constexpr (TILES <= 2)
-        if (pl.wps == 4) return launch_t<B, BF16, TILES, 4, 1, false>(pl, m, s);
-    if constexpr (TILES <= 4)
-        if (pl.wps == 2) return launch_t<B, BF16, TILES, 2, 1, false>(pl, m, s);
-    return launch_t<B, BF16, TILES, 1, 1, false>(pl, m, s);
-}
-
-template <int B, bool BF16>
-cudaError_t launch_tiles(const GemvPlan &pl, const GemvMaps &m, cudaStream_t s) {
-    switch (pl.prm.tiles) {
-        case 1: return launch_wps<B, BF16, 1>(pl, m, s);
-        case 2: return launch_wps<B, BF16, 2>(pl, m, s);
-        case 3: return launch_wps<B, BF16, 3>(pl, m, s);
-        case 4: return launch_wps<B, BF16, 4>(pl, m, s);
-        case 5: return launch_wps<B, BF16, 5>(pl, m, s);
-        case 6: return launch_wps<B, BF16, 6>(pl, m, s);
-        case 7: return launch_wps<B, BF16, 7>(pl, m, s);
-        default: return launch_wps<B, BF16, 8>(pl, m, s);
-    }
 }
 
 }  // namespace
@@ -267,17 +247,25 @@ cudaError_t launch_plan(const MatmulArgs &a, GemvPlan &pl, const uint32_t *const
                          sbox, CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     }
+    if (!staged) maps.x = maps.w[0];  // unused; any valid map
+    for (int j = nproj; j < gemv::kMaxProj; ++j) {  // unused projections
+        maps.w[j] = maps.w[0];
+        maps.s[j] = maps.s[0];
+        maps.b[j] = maps.b[0];
+    }
     pl.prm.err = gemv::error_word();
     if (!pl.prm.err) return cudaErrorInvalidValue;
-    if (pl.mb > 2) return gemv::launch_mb4(pl, maps, a.stream);
-    if (pl.mb > 1) return gemv::launch_mb2(pl, maps, a.stream);
-    if (staged) return gemv::launch_staged1(pl, maps, a.stream);
-    const bool bf = a.dtype == AQ_BF16;
-    if (a.bits == 3)
-        return bf ? gemv::launch_tiles<3, true>(pl, maps, a.stream)
-                  : gemv::launch_tiles<3, false>(pl, maps, a.stream);
-    return bf ? gemv::launch_tiles<4, true>(pl, maps, a.stream)
-              : gemv::launch_tiles<4, false>(pl, maps, a.stream);
+    using gemv::launch_blocks;
+    if (pl.mp) {
+        if (pl.mb > 2) return launch_blocks<4, true, true>(pl, maps, a.stream);
+        if (pl.mb > 1) return launch_blocks<2, true, true>(pl, maps, a.stream);
+        return staged ? launch_blocks<1, true, true>(pl, maps, a.stream)
+                      : launch_blocks<1, false, true>(pl, maps, a.stream);
+    }
+    if (pl.mb > 2) return launch_blocks<4, true, false>(pl, maps, a.stream);
+    if (pl.mb > 1) return launch_blocks<2, true, false>(pl, maps, a.stream);
+    return staged ? launch_blocks<1, true, false>(pl, maps, a.stream)
+                  : launch_blocks<1, false, false>(pl, maps, a.stream);
 }
 
 }  // namespace
@@ -301,7 +289,8 @@ bool gemv_multi_supported(const MultiArgs &m) {
 cudaError_t gemv_launch_multi(const MultiArgs &m) {
     GemvPlan pl;
     if (!gemv_plan(m.a, pl, m.N, m.nproj, m.gate_up)) return cudaErrorInvalidValue;
-    for (int j = 0; j < m.nproj; ++j) pl.prm.y_proj[j] = m.gate_up ? m.a.out : m.out[j];
+    for (int j = 0; j < m.nproj; ++j) pl.mx.y_proj[j] = m.gate_up ? m.a.out : m.out[j];
+    pl.prm.y = pl.mx.y_proj[0];  // one projection: the single-projection kernels
     return launch_plan(m.a, pl, m.Wq, m.scales, m.biases, m.N, m.nproj);
 }
 
@@ -335,4 +324,10 @@ cudaError_t gemv_read_error(uint32_t *code, bool clear) {
     return cudaMemcpyToSymbol(g_gemv_error, &zero, sizeof(uint32_t));
 }
 
+}  // namespace aq
+
+namespace aq {
+namespace gemv {
+template cudaError_t launch_blocks<1, false, false>(const GemvPlan &, const GemvMaps &, cudaStream_t);
+}  // namespace gemv
 }  // namespace aq

@@ -73,8 +73,8 @@ namespace gemv {
 
 constexpr int kConsumers = 8;                     // consumer warps
 constexpr int kGemvThreads = (kConsumers + 1) * 32;  // + one producer warp
-constexpr int kMaxTiles = 8;
-constexpr int kMaxProj = 4;       // projections of one x per launch                      // 16-row tiles per pass
+constexpr int kMaxTiles = 8;                      // 16-row tiles per pass
+constexpr int kMaxProj = 4;                       // projections of one x per launch
 constexpr int kMaxPassRows = 16 * kMaxTiles;
 constexpr int kXPitch = 144;     // bytes per activation row in an x slot (128 + 16: no bank conflicts)
 // An x slot holds one group of every activation row (M rows at kXPitch),
@@ -103,11 +103,15 @@ struct GemvParams {
     uint32_t off_xst;       // staged x: box inside a ring slot
     int x_rows;             // staged x: rows per group in the box (= M)
     uint32_t stage_tx;      // bytes one stage brings in
-    // Several projections of the same x in one launch.  Independent outputs:
-    // CTAs cta0[j] .. cta0[j+1]-1 take projection j.  Gate/up (gate_up = 1,
-    // two projections of equal N): every CTA takes the same rows of both,
-    // pass 0 the gate and pass 1 the up projection, and writes
-    // silu(gate) * up; the gate's rows wait in shared memory at off_gu.
+};
+
+// Several projections of the same x in one launch (kernels instantiated
+// with MP = true only).  Independent outputs: CTAs cta0[j] .. cta0[j+1]-1
+// take projection j.  Gate/up (gate_up = 1, two projections of equal N):
+// every CTA takes the same rows of both, pass 0 the gate and pass 1 the up
+// projection, and writes silu(gate) * up; the gate's rows wait in shared
+// memory at off_gu.
+struct GemvMulti {
     int nproj;
     int gate_up;
     int cta0[kMaxProj + 1];
@@ -116,8 +120,10 @@ struct GemvParams {
     uint32_t off_gu;
 };
 
-// Tensor maps of one launch: x (staged x only) and the codes, scales and
-// biases of each projection.
+// Tensor maps of one launch (host side): x (staged x only) and the codes,
+// scales and biases of each projection.  The kernel takes each map as a
+// parameter of its own, in the order w0, s0, b0, x, then the other
+// projections; the single-projection kernels carry no code for the others.
 struct GemvMaps {
     CUtensorMap x;
     CUtensorMap w[kMaxProj], s[kMaxProj], b[kMaxProj];
@@ -301,9 +307,16 @@ __device__ __forceinline__ void store_y<__nv_bfloat16>(__nv_bfloat16 *p, float v
     *p = __float2bfloat16_rn(v);
 }
 
-template <int B, bool BF16, int TILES, int WPS, int MB, bool XST>
+template <int B, bool BF16, int TILES, int WPS, int MB, bool XST, bool MP>
 __global__ void __launch_bounds__(kGemvThreads, MB > 2 ? 1 : 2)
-    gemv_kernel(const __grid_constant__ GemvParams p, const __grid_constant__ GemvMaps mp) {
+    gemv_kernel(const __grid_constant__ GemvParams p, const __grid_constant__ CUtensorMap tm_w0,
+                const __grid_constant__ CUtensorMap tm_s0, const __grid_constant__ CUtensorMap tm_b0,
+                const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w1,
+                const __grid_constant__ CUtensorMap tm_s1, const __grid_constant__ CUtensorMap tm_b1,
+                const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_s2,
+                const __grid_constant__ CUtensorMap tm_b2, const __grid_constant__ CUtensorMap tm_w3,
+                const __grid_constant__ CUtensorMap tm_s3, const __grid_constant__ CUtensorMap tm_b3,
+                const __grid_constant__ GemvMulti mx) {
     constexpr bool kXStage = XST;  // x streamed per stage by a fourth producer lane
     using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
     constexpr int kBox = B == 4 ? 128 : 96;  // bytes of a row in one column block (4 groups)
@@ -337,9 +350,12 @@ __global__ void __launch_bounds__(kGemvThreads, MB > 2 ? 1 : 2)
     // producer lanes once x_landed completes).
 
     int proj = 0;  // this CTA's projection (independent outputs)
-    if (!p.gate_up)
-        while (proj + 1 < p.nproj && (int)blockIdx.x >= p.cta0[proj + 1]) ++proj;
-    const int row_cta = ((int)blockIdx.x - p.cta0[proj]) * p.rows_cta;
+    int row_cta = blockIdx.x * p.rows_cta;
+    if constexpr (MP) {
+        if (!mx.gate_up)
+            while (proj + 1 < mx.nproj && (int)blockIdx.x >= mx.cta0[proj + 1]) ++proj;
+        row_cta = ((int)blockIdx.x - mx.cta0[proj]) * p.rows_cta;
+    }
     const int total = p.passes * p.n_stages;
     const int nb = p.sg / 4;  // column blocks per stage
 
@@ -351,11 +367,18 @@ __global__ void __launch_bounds__(kGemvThreads, MB > 2 ? 1 : 2)
         if (lane < (kXStage ? 4 : 3)) {
             // the lane's map for projection j (lane 3: x)
             auto map_of = [&](int j) -> const CUtensorMap * {
-                return lane == 0 ? &mp.w[j] : lane == 1 ? &mp.s[j] : lane == 2 ? &mp.b[j] : &mp.x;
+                if (lane == 3) return &tm_x;
+                if (j == 0) return lane == 0 ? &tm_w0 : lane == 1 ? &tm_s0 : &tm_b0;
+                if (j == 1) return lane == 0 ? &tm_w1 : lane == 1 ? &tm_s1 : &tm_b1;
+                if (j == 2) return lane == 0 ? &tm_w2 : lane == 1 ? &tm_s2 : &tm_b2;
+                return lane == 0 ? &tm_w3 : lane == 1 ? &tm_s3 : &tm_b3;
             };
-            const CUtensorMap *tm = map_of(proj);
+            const CUtensorMap *tm =
+                lane == 0 ? &tm_w0 : lane == 1 ? &tm_s0 : lane == 2 ? &tm_b0 : &tm_x;
+            if constexpr (MP) tm = map_of(proj);
             prefetch_tmap(tm);
-            if (p.gate_up) prefetch_tmap(map_of(1));
+            if constexpr (MP)
+                if (mx.gate_up) prefetch_tmap(map_of(1));
             if (lane == 3) grid_dependency_wait();  // x belongs to the stream order
             bool triggered = false;
             int it = 0, slot = 0, lap = 0, pass = 0, s = 0;
@@ -368,9 +391,12 @@ __global__ void __launch_bounds__(kGemvThreads, MB > 2 ? 1 : 2)
                     gemv_record(flag, p.err, ERR_GEMV_EMPTY);
                     break;
                 }
-                // gate/up: the same rows of projection `pass`
-                const int r0 = p.gate_up ? row_cta : row_cta + pass * p.pass_rows;
-                if (p.gate_up) tm = map_of(pass);
+                int r0 = row_cta + pass * p.pass_rows;
+                if constexpr (MP)
+                    if (mx.gate_up) {  // the same rows of projection `pass`
+                        r0 = row_cta;
+                        tm = map_of(pass);
+                    }
                 uint8_t *dst = smem + (size_t)slot * p.slot_bytes;
                 if (lane == 3) {
                     tma_load_3d(dst + p.off_xst, tm, 0, 0, s * p.sg, &full[slot]);
@@ -523,9 +549,14 @@ __global__ void __launch_bounds__(kGemvThreads, MB > 2 ? 1 : 2)
         consumers_sync();
     }
 
-    T *y = static_cast<T *>(p.y_proj[proj]);
-    const int Np = p.n_proj[proj];
-    float *gbuf = reinterpret_cast<float *>(smem + p.off_gu);  // gate/up: the gate's rows
+    T *y = static_cast<T *>(p.y);
+    int Np = p.N;
+    float *gbuf = nullptr;  // gate/up: the gate's rows
+    if constexpr (MP) {
+        y = static_cast<T *>(mx.y_proj[proj]);
+        Np = mx.n_proj[proj];
+        gbuf = reinterpret_cast<float *>(smem + mx.off_gu);
+    }
     float *red = reinterpret_cast<float *>(smem + p.off_red);
     const int pr = p.pass_rows;
 
@@ -689,7 +720,9 @@ __global__ void __launch_bounds__(kGemvThreads, MB > 2 ? 1 : 2)
                 *reinterpret_cast<float4 *>(&red[(((warp * TILES + t) * MB + mb) * 32 + lane) * 4]) =
                     make_float4(acc[t][mb][0], acc[t][mb][1], acc[t][mb][2], acc[t][mb][3]);
         consumers_sync();
-        const int r0 = p.gate_up ? row_cta : row_cta + pass * pr;
+        int r0 = row_cta + pass * pr;
+        if constexpr (MP)
+            if (mx.gate_up) r0 = row_cta;
         const int rows = std::min(pr, Np - r0);
         for (int e = threadIdx.x; e < rows * M; e += kConsumers * 32) {
             const int m = e / rows, r = e - m * rows;
@@ -702,14 +735,15 @@ __global__ void __launch_bounds__(kGemvThreads, MB > 2 ? 1 : 2)
             for (int w = 0; w < kConsumers; ++w)
                 v += red[(((w * TILES + t) * MB + mb) * 32 + ln) * 4 + i];
             if constexpr (!kMmaBf16) v *= 16777216.f;  // 2^24
-            if (p.gate_up) {
-                if (pass == 0) {  // the gate waits for the up projection
-                    gbuf[m * pr + r] = v;
-                    continue;
+            if constexpr (MP)
+                if (mx.gate_up) {
+                    if (pass == 0) {  // the gate waits for the up projection
+                        gbuf[m * pr + r] = v;
+                        continue;
+                    }
+                    const float gt = gbuf[m * pr + r];
+                    v = gt / (1.f + expf(-gt)) * v;  // silu(gate) * up
                 }
-                const float gt = gbuf[m * pr + r];
-                v = gt / (1.f + expf(-gt)) * v;  // silu(gate) * up
-            }
             store_y<T>(&y[(int64_t)m * Np + r0 + r], v);
         }
         consumers_sync();  // the buffer is rewritten by the next pass
@@ -721,6 +755,8 @@ __global__ void __launch_bounds__(kGemvThreads, MB > 2 ? 1 : 2)
 // ---------------------------------------------------------------------------
 struct GemvPlan {
     GemvParams prm;
+    GemvMulti mx;
+    bool mp;   // several projections or gate/up: the MP = true kernels
     size_t smem;
     int grid;
     int mb;    // 8-column blocks of activation rows
@@ -731,9 +767,9 @@ struct GemvPlan {
 
 constexpr size_t kSmemMax = 227 * 1024;  // one CTA per SM at most
 
-template <int B, bool BF16, int TILES, int WPS, int MB, bool XST>
+template <int B, bool BF16, int TILES, int WPS, int MB, bool XST, bool MP>
 cudaError_t launch_t(const GemvPlan &pl, const GemvMaps &maps, cudaStream_t stream) {
-    auto kern = gemv_kernel<B, BF16, TILES, WPS, MB, XST>;
+    auto kern = gemv_kernel<B, BF16, TILES, WPS, MB, XST, MP>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -751,14 +787,102 @@ cudaError_t launch_t(const GemvPlan &pl, const GemvMaps &maps, cudaStream_t stre
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, pl.prm, maps);
+    return cudaLaunchKernelEx(&cfg, kern, pl.prm, maps.w[0], maps.s[0], maps.b[0], maps.x,
+                              maps.w[1], maps.s[1], maps.b[1], maps.w[2], maps.s[2], maps.b[2],
+                              maps.w[3], maps.s[3], maps.b[3], pl.mx);
 }
 
-// Staged x (x streamed with the weights): one column block in aq_gemv_xs.cu,
-// two (M = 9..16) in aq_gemv16.cu, four (M = 17..32) in aq_gemv32.cu.
-cudaError_t launch_mb4(const GemvPlan &pl, const GemvMaps &maps, cudaStream_t stream);
-cudaError_t launch_staged1(const GemvPlan &pl, const GemvMaps &maps, cudaStream_t stream);
-cudaError_t launch_mb2(const GemvPlan &pl, const GemvMaps &maps, cudaStream_t stream);
+// Dispatch from the plan to an instantiation.  One 8-column block with x
+// whole (XST = false) or staged, two blocks (M = 9..16), four (M = 17..32);
+// groups per warp by tiles as max_wps allows.
+template <int B, bool BF16, int TILES, bool XST, bool MP>
+cudaError_t mb1_wps(const GemvPlan &pl, const GemvMaps &m, cudaStream_t s) {
+    if constexpr (TILES <= 2)
+        if (pl.wps == 4) return launch_t<B, BF16, TILES, 4, 1, XST, MP>(pl, m, s);
+    if constexpr (TILES <= 4)
+        if (pl.wps == 2) return launch_t<B, BF16, TILES, 2, 1, XST, MP>(pl, m, s);
+    return launch_t<B, BF16, TILES, 1, 1, XST, MP>(pl, m, s);
+}
+
+template <int B, bool BF16, bool XST, bool MP>
+cudaError_t mb1_tiles(const GemvPlan &pl, const GemvMaps &m, cudaStream_t s) {
+    switch (pl.prm.tiles) {
+        case 1: return mb1_wps<B, BF16, 1, XST, MP>(pl, m, s);
+        case 2: return mb1_wps<B, BF16, 2, XST, MP>(pl, m, s);
+        case 3: return mb1_wps<B, BF16, 3, XST, MP>(pl, m, s);
+        case 4: return mb1_wps<B, BF16, 4, XST, MP>(pl, m, s);
+        case 5: return mb1_wps<B, BF16, 5, XST, MP>(pl, m, s);
+        case 6: return mb1_wps<B, BF16, 6, XST, MP>(pl, m, s);
+        case 7: return mb1_wps<B, BF16, 7, XST, MP>(pl, m, s);
+        default: return mb1_wps<B, BF16, 8, XST, MP>(pl, m, s);
+    }
+}
+
+template <int B, bool BF16, int TILES, bool MP>
+cudaError_t mb2_wps(const GemvPlan &pl, const GemvMaps &m, cudaStream_t s) {
+    if constexpr (TILES <= 2)
+        if (pl.wps == 2) return launch_t<B, BF16, TILES, 2, 2, true, MP>(pl, m, s);
+    return launch_t<B, BF16, TILES, 1, 2, true, MP>(pl, m, s);
+}
+
+template <int B, bool BF16, bool MP>
+cudaError_t mb2_tiles(const GemvPlan &pl, const GemvMaps &m, cudaStream_t s) {
+    switch (pl.prm.tiles) {
+        case 1: return mb2_wps<B, BF16, 1, MP>(pl, m, s);
+        case 2: return mb2_wps<B, BF16, 2, MP>(pl, m, s);
+        case 3: return mb2_wps<B, BF16, 3, MP>(pl, m, s);
+        default: return mb2_wps<B, BF16, 4, MP>(pl, m, s);
+    }
+}
+
+template <int B, bool BF16, bool MP>
+cudaError_t mb4_tiles(const GemvPlan &pl, const GemvMaps &m, cudaStream_t s) {
+    switch (pl.prm.tiles) {
+        case 1: return launch_t<B, BF16, 1, 1, 4, true, MP>(pl, m, s);
+        case 2: return launch_t<B, BF16, 2, 1, 4, true, MP>(pl, m, s);
+        case 3: return launch_t<B, BF16, 3, 1, 4, true, MP>(pl, m, s);
+        case 4: return launch_t<B, BF16, 4, 1, 4, true, MP>(pl, m, s);
+        case 5: return launch_t<B, BF16, 5, 1, 4, true, MP>(pl, m, s);
+        default: return launch_t<B, BF16, 6, 1, 4, true, MP>(pl, m, s);
+    }
+}
+
+// One plan's launch for each (bits, dtype).  Column blocks: 1 (XST says
+// whether x is staged), 2 or 4.
+template <int MBLK, bool XST, bool MP>
+cudaError_t launch_blocks(const GemvPlan &pl, const GemvMaps &m, cudaStream_t s) {
+    if constexpr (MBLK == 1) {
+        if (pl.bits == 3)
+            return pl.bf16 ? mb1_tiles<3, true, XST, MP>(pl, m, s)
+                           : mb1_tiles<3, false, XST, MP>(pl, m, s);
+        return pl.bf16 ? mb1_tiles<4, true, XST, MP>(pl, m, s)
+                       : mb1_tiles<4, false, XST, MP>(pl, m, s);
+    } else if constexpr (MBLK == 2) {
+        if (pl.prm.tiles > 4) return cudaErrorInvalidValue;
+        if (pl.bits == 3)
+            return pl.bf16 ? mb2_tiles<3, true, MP>(pl, m, s) : mb2_tiles<3, false, MP>(pl, m, s);
+        return pl.bf16 ? mb2_tiles<4, true, MP>(pl, m, s) : mb2_tiles<4, false, MP>(pl, m, s);
+    } else {
+        if (pl.prm.tiles > 6) return cudaErrorInvalidValue;
+        if (pl.bits == 3)
+            return pl.bf16 ? mb4_tiles<3, true, MP>(pl, m, s) : mb4_tiles<3, false, MP>(pl, m, s);
+        return pl.bf16 ? mb4_tiles<4, true, MP>(pl, m, s) : mb4_tiles<4, false, MP>(pl, m, s);
+    }
+}
+
+// Each instantiation of launch_blocks lives in one translation unit (the
+// library builds in parallel): aq_gemv.cu (1 block, x whole), aq_gemv_xs.cu
+// (1 block, x staged), aq_gemv16.cu (2), aq_gemv32.cu (4); the
+// several-projection kernels in aq_gemv_mpw.cu (1 block, x whole),
+// aq_gemv_mps.cu (1 block, x staged) and aq_gemv_mp24.cu (2 and 4 blocks).
+extern template cudaError_t launch_blocks<1, false, false>(const GemvPlan &, const GemvMaps &, cudaStream_t);
+extern template cudaError_t launch_blocks<1, true, false>(const GemvPlan &, const GemvMaps &, cudaStream_t);
+extern template cudaError_t launch_blocks<2, true, false>(const GemvPlan &, const GemvMaps &, cudaStream_t);
+extern template cudaError_t launch_blocks<4, true, false>(const GemvPlan &, const GemvMaps &, cudaStream_t);
+extern template cudaError_t launch_blocks<1, false, true>(const GemvPlan &, const GemvMaps &, cudaStream_t);
+extern template cudaError_t launch_blocks<1, true, true>(const GemvPlan &, const GemvMaps &, cudaStream_t);
+extern template cudaError_t launch_blocks<2, true, true>(const GemvPlan &, const GemvMaps &, cudaStream_t);
+extern template cudaError_t launch_blocks<4, true, true>(const GemvPlan &, const GemvMaps &, cudaStream_t);
 
 }  // namespace gemv
 }  // namespace aq
