@@ -97,9 +97,15 @@ def traffic_record():
         return {}
     src = os.path.join(ROOT, "quantized_matmul_affine_gb300", "csrc")
     h = hashlib.sha256()
-    for fn in sorted(os.listdir(src)):
-        if fn.endswith((".cu", ".cuh", ".h")):
+    # the files that define the kernel (all kernel sources if not listed)
+    names = [n.strip() for n in rec.get("sources", "").split(",") if n.strip()]
+    if not names:
+        names = [fn for fn in sorted(os.listdir(src)) if fn.endswith((".cu", ".cuh", ".h"))]
+    for fn in names:
+        try:
             h.update(open(os.path.join(src, fn), "rb").read())
+        except OSError:
+            return {}
     if rec.get("csrc_sha256") != h.hexdigest():
         return {}
     return rec
