@@ -70,10 +70,10 @@ bool gemv_plan(const MatmulArgs &a, GemvPlan &pl, const int64_t *n_proj, int npr
     const int B = a.bits;
     const int G = (int)(a.K / 64);
     const int MB = a.M > 16 ? 4 : a.M > 8 ? 2 : 1;
-    const int max_tiles = MB == 1 ? kMaxTiles : MB == 2 ? 4 : 6;
-    // Four column blocks take too many registers for two CTAs per SM: the
-    // CTA has the SM to itself and all of its shared memory.
-    const size_t budget = MB > 2 ? kSmemMax : smem_budget();
+    const int max_tiles = MB == 1 ? kMaxTiles : 6;
+    // Two or four column blocks take too many registers for two CTAs per SM:
+    // the CTA has the SM to itself and all of its shared memory.
+    const size_t budget = MB > 1 ? kSmemMax : smem_budget();
     const int sms = num_sms();
     const int64_t per_sm = (n_rows + sms - 1) / sms;
     int passes = (int)((per_sm + 16 * max_tiles - 1) / (16 * max_tiles));

@@ -1,7 +1,8 @@
-// Resident small-M kernel ("gemv"): y = x . W^T for 1 <= M <= 16 activation
-// rows (one or two 8-column MMA blocks), streaming the packed weights once
-// per call.  Kernel template and plan types, shared by the translation units
-// that instantiate it (aq_gemv.cu: one column block; aq_gemv16.cu: two).
+// Resident small-M kernel ("gemv"): y = x . W^T for 1 <= M <= 32 activation
+// rows (one, two or four 8-column MMA blocks), streaming the packed weights
+// once per call; also several projections of one x per launch and the fused
+// gate/up + SiLU.  Kernel template, plan types and launch dispatch, shared by
+// the translation units that instantiate them (aq_gemv*.cu).
 //
 // Method (mlx-bun pages, @mlx-bun/inference 1.0.0, kernels/quantization/):
 //   * the weight format: 64-value groups, 2*B uint32 words each, LSB-first
@@ -10,12 +11,15 @@
 //     sum_g [ scale_g * sum_k q_k x_k + bias_g * sum_k x_k ], each weight
 //     decoded once and reused for every activation row;
 //   * the K-permuted operand layout of affine{3,4}-mma.ts: inside a group
-//     any order of k serves, provided x takes the same order.
+//     any order of k serves, provided x takes the same order;
+//   * the gate/up kernel of trellis-shared-m.ts: silu(gate) * up formed in
+//     the epilogue of the two products.
 //
 // GB300 design:
 //   * At most one CTA per SM.  CTA c owns a contiguous block of R weight
 //     rows over all of K, R = ceil(N / SMs), so every SM streams the same
-//     number of bytes; a block taller than 128 rows runs in passes.
+//     number of bytes; a block taller than 128 rows (96 with two or four
+//     column blocks) runs in passes.
 //   * A producer warp streams the block through a ring of stages in shared
 //     memory: one stage is SG groups of K (SG = 8, 16 or 32) for the R rows,
 //     loaded by three TMA boxes issued from three lanes at once - the codes
@@ -24,35 +28,36 @@
 //     groups times R rows, so a row's 8 scales are 16 bytes from the next
 //     row's and the loads of 8 rows never share a bank) - with completion
 //     counted on an mbarrier.  (On GB300 a TMA op costs ~75 ns of issue time
-//     whatever its size, so a stage is a few large boxes.)  The weights do
-//     not depend on the preceding kernel, so the producer fills the ring
-//     before the CTA waits on the preceding grid.
-//     A CTA takes at most 112 KB of shared memory and 288 threads, so it
-//     fits on an SM beside a CTA of the previous call: with programmatic
-//     dependent launch a call's weight stream overlaps the previous call's
-//     tail, and for weights of up to ~100 KB per SM the whole stream is in
-//     shared memory before the call's x is even ready.
+//     whatever its size, so a stage is a few large boxes.)  A last stage
+//     past the end of K reads zero fill and its groups are skipped.  The
+//     weights do not depend on the preceding kernel, so the producer fills
+//     the ring before the CTA waits on the preceding grid.
+//     With one column block a CTA takes at most 112 KB of shared memory and
+//     288 threads, so it fits on an SM beside a CTA of the previous call:
+//     with programmatic dependent launch a call's weight stream overlaps the
+//     previous call's tail.  With two or four blocks the CTA has the SM (and
+//     its 227 KB) to itself.
 //   * Eight consumer warps.  Warp w takes SG/8 consecutive groups of every
-//     stage, for all the block's 16-row tiles (the tile count is a template
-//     parameter, so the tiles interleave freely).
-//   * x, when M x K fits in 40 KB: one bulk copy per activation row once the
-//     grid dependency resolves, rewritten in place into B-fragment order with
-//     the group sums.  Otherwise ("staged"): a fourth producer lane streams it
-//     with the weights, one 3-D TMA box of the stage's groups x 8 or 16 rows
-//     per stage (rows past M read as zero), and each warp builds its
-//     fragments and sums per group.
+//     stage, for all the block's 16-row tiles and column blocks (template
+//     parameters, so the units interleave freely).
+//   * x whole (one column block, x and its sums within 48 KB): one bulk copy
+//     per activation row once the grid dependency resolves, rewritten in
+//     place into B-fragment order with the group sums.  Otherwise
+//     ("staged"): a fourth producer lane streams it with the weights, one
+//     3-D TMA box of the stage's groups x M rows per stage, and each warp
+//     builds its fragments and sums per group.
 //   * Codes decode into MMA A fragments (weights are the 16-row A operand)
 //     with one shift and one LOP3 per two codes (4-bit fp16: one AND per
 //     two codes plus a shift per word, the codes staying in place), each
 //     code alone in the bits of a 16-bit half:
-//       fp16 x: the half is the subnormal q * 2^(p-24) (exact), so
+//       fp16 MMA: the half is the subnormal q * 2^(p-24) (exact), so
 //               y_g = scale * 2^24 * D + bias * sum(x);
-//       bf16 x: under the exponent of 128 the half is the bf16 value 128 + q
-//               (exact), so y_g = scale * D + (bias - 128 * scale) * sum(x).
-//     x is the B operand in its own type; nothing is converted.  mma.sync
-//     m16n8k16 accumulates in fp32.
-//   * The group sums of x come from the same B fragments times an all-ones
-//     A operand: four more MMAs per group per warp, shared by every tile.
+//       bf16 MMA: under the exponent of 128 the half is the bf16 value
+//               128 + q (exact), so y_g = scale * D + (bias - 128 * scale) * sum(x).
+//     At 4 bits with x whole, x is rewritten as fp16 with a power-of-two
+//     scale per (group, row) and the fp16 MMA serves either x type; staged
+//     x is the B operand in its own type.  mma.sync m16n8k16 accumulates in
+//     fp32.
 //   * The eight warps' partial tiles meet in shared memory and are added in
 //     warp order (deterministic).
 #pragma once
@@ -308,7 +313,7 @@ __device__ __forceinline__ void store_y<__nv_bfloat16>(__nv_bfloat16 *p, float v
 }
 
 template <int B, bool BF16, int TILES, int WPS, int MB, bool XST, bool MP>
-__global__ void __launch_bounds__(kGemvThreads, MB > 2 ? 1 : 2)
+__global__ void __launch_bounds__(kGemvThreads, MB > 1 ? 1 : 2)
     gemv_kernel(const __grid_constant__ GemvParams p, const __grid_constant__ CUtensorMap tm_w0,
                 const __grid_constant__ CUtensorMap tm_s0, const __grid_constant__ CUtensorMap tm_b0,
                 const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w1,
@@ -831,7 +836,9 @@ cudaError_t mb2_tiles(const GemvPlan &pl, const GemvMaps &m, cudaStream_t s) {
         case 1: return mb2_wps<B, BF16, 1, MP>(pl, m, s);
         case 2: return mb2_wps<B, BF16, 2, MP>(pl, m, s);
         case 3: return mb2_wps<B, BF16, 3, MP>(pl, m, s);
-        default: return mb2_wps<B, BF16, 4, MP>(pl, m, s);
+        case 4: return mb2_wps<B, BF16, 4, MP>(pl, m, s);
+        case 5: return mb2_wps<B, BF16, 5, MP>(pl, m, s);
+        default: return mb2_wps<B, BF16, 6, MP>(pl, m, s);
     }
 }
 
@@ -858,7 +865,7 @@ cudaError_t launch_blocks(const GemvPlan &pl, const GemvMaps &m, cudaStream_t s)
         return pl.bf16 ? mb1_tiles<4, true, XST, MP>(pl, m, s)
                        : mb1_tiles<4, false, XST, MP>(pl, m, s);
     } else if constexpr (MBLK == 2) {
-        if (pl.prm.tiles > 4) return cudaErrorInvalidValue;
+        if (pl.prm.tiles > 6) return cudaErrorInvalidValue;
         if (pl.bits == 3)
             return pl.bf16 ? mb2_tiles<3, true, MP>(pl, m, s) : mb2_tiles<3, false, MP>(pl, m, s);
         return pl.bf16 ? mb2_tiles<4, true, MP>(pl, m, s) : mb2_tiles<4, false, MP>(pl, m, s);

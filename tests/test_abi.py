@@ -151,20 +151,20 @@ def test_select_invalid():
     (1, 4096, 4096, 4, "rows/cta=27 passes=1 tiles=2 colblocks=1 groups/stage=32 stages=2 ring=2 x=whole grid=152"),
     (2, 28672, 8192, 4, "rows/cta=190 passes=2"),
     (8, 600, 13824, 4, "x=staged"),
-    (16, 10240, 5120, 3, "rows/cta=68 passes=2 tiles=3 colblocks=2"),
+    (16, 10240, 5120, 3, "rows/cta=68 passes=1 tiles=5 colblocks=2"),
     (32, 10240, 5120, 3, "rows/cta=68 passes=1 tiles=5 colblocks=4 groups/stage=8 stages=10"),
     (32, 28672, 8192, 4, "rows/cta=190 passes=2 tiles=6 colblocks=4"),
 ])
 def test_gemv_plan(M, N, K, bits, want):
     # The resident kernel's plan on a 152-SM GB300 (the SM count the library
     # assumes when no device is present): rows per CTA = ceil(N / SMs), whole
-    # K per CTA, at most 128 rows per pass (96 with four column blocks), ring
-    # as deep as 112 KB allows (two CTAs per SM) or, with four column blocks
-    # (one CTA per SM), 227 KB.
+    # K per CTA, at most 128 rows per pass (96 with two or four column
+    # blocks), ring as deep as 112 KB allows (two CTAs per SM) or, with two or
+    # four column blocks (one CTA per SM), 227 KB.
     import torch
     if torch.cuda.is_available():
         pytest.skip("plan depends on the device's SM count")
     d = aq.aq_describe(M, N, K, bits)
     assert d.startswith("gemv ") and want in d, d
     smem = int(d.split("smem=")[1])
-    assert smem <= (112 if M <= 16 else 227) * 1024
+    assert smem <= (112 if M <= 8 else 227) * 1024
