@@ -66,8 +66,10 @@ typedef enum aq_variant {
     AQ_VARIANT_GENERIC = 0, /* plain-load CUDA-core kernel: any K % 64 == 0, any alignment */
     AQ_VARIANT_QMV = 1,     /* small-M: bulk-async staged weights, warp MMA, factored dequant */
     AQ_VARIANT_TC = 2,      /* large-M: tcgen05 MMA with TMEM accumulators */
-    AQ_VARIANT_GEMV = 3,    /* M <= 16: one resident CTA per SM, TMA weight ring, warp MMA */
-    AQ_NUM_VARIANTS = 4
+    AQ_VARIANT_GEMV = 3,    /* M <= 32: one resident CTA per SM, TMA weight ring, warp MMA */
+    AQ_VARIANT_TCW = 4,     /* M <= 128: tcgen05 MMA with x as the 128-row operand and 256-row
+                               weight tiles, K split over a cluster */
+    AQ_NUM_VARIANTS = 5
 } aq_variant;
 
 /*
@@ -248,7 +250,7 @@ void aq_free(void);
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *aq_status_string(aq_status status);
 
-/* Human-readable name of a variant ("generic", "qmv", "tc", "gemv"); "?" if unknown. */
+/* Human-readable name of a variant ("generic", "qmv", "tc", "gemv", "tcw"); "?" if unknown. */
 const char *aq_variant_name(int variant);
 
 /* Library version string. */

@@ -22,7 +22,7 @@ from . import build as _build
 
 __all__ = [
     "AqError", "AQ_F16", "AQ_BF16", "AQ_VARIANT_AUTO", "AQ_VARIANT_GENERIC", "AQ_VARIANT_QMV",
-    "AQ_VARIANT_TC", "AQ_VARIANT_GEMV", "AQ_NUM_VARIANTS", "aq_pack", "aq_quantize",
+    "AQ_VARIANT_TC", "AQ_VARIANT_GEMV", "AQ_VARIANT_TCW", "AQ_NUM_VARIANTS", "aq_pack", "aq_quantize",
     "aq_quantize_bf16", "aq_matmul", "aq_matmul_bf16", "aq_matmul_multi", "aq_matmul_gate_up",
     "aq_matmul_variant", "aq_matmul_host", "aq_select", "aq_describe", "aq_stats", "aq_device_error",
     "aq_free", "aq_status_string", "aq_variant_name", "aq_version", "lib_path", "load",
@@ -32,7 +32,8 @@ AQ_OK = 0
 AQ_F16, AQ_BF16 = 0, 1
 AQ_VARIANT_AUTO, AQ_VARIANT_GENERIC, AQ_VARIANT_QMV, AQ_VARIANT_TC = -1, 0, 1, 2
 AQ_VARIANT_GEMV = 3
-AQ_NUM_VARIANTS = 4
+AQ_VARIANT_TCW = 4
+AQ_NUM_VARIANTS = 5
 
 _lib: Optional[ctypes.CDLL] = None
 

@@ -102,11 +102,26 @@ static int gemv_max_m() {
 // 32000x4096; 128256x4096 and 57344x8192: 18-23% slower).
 static bool gemv_for_m1(const MatmulArgs &a) { return a.N <= 128ll * num_sms(); }
 
+// 33..128 activation rows go to the swapped-role tensor-core kernel when the
+// 128-row weight tiles of the tc kernel would leave the SMs short of work
+// (fewer than 0.6 x SMs tiles): its K split recruits the idle SMs.  Both are
+// bound by the dequantisation (~16-18 codes per ns per SM measured on
+// GB300), so with enough tiles tc's full grid wins (GB300, M = 64/128:
+// 10240x5120 3-bit 31.7 against 40.0 us, 5120x13824 72.5 against 101.6,
+// 4096x4096 25.2 against 30.7; 13824x5120 48.8 against 42.5, 28672x8192
+// 156 against 130).
+static bool tcw_first(const MatmulArgs &a) {
+    const int64_t tc_tiles = (a.N + 127) / 128;
+    return tc_tiles * 5 < (int64_t)num_sms() * 3;
+}
+
 // The dispatch rule.  Returns the variant for the arguments (alignment
 // included), never AQ_VARIANT_AUTO.
 static int choose(const MatmulArgs &a) {
     const bool gemv_first = a.M > 1 || gemv_for_m1(a);
     if (a.M <= gemv_max_m() && gemv_first && gemv_supported(a)) return AQ_VARIANT_GEMV;
+    if (a.M > gemv_max_m() && a.M <= 128 && tcw_first(a) && tcw_supported(a))
+        return AQ_VARIANT_TCW;
     const bool qmv = qmv_supported(a);
     const bool tc = tc_supported(a);
     if (qmv && (a.M <= qmv_max_m() || !tc)) return AQ_VARIANT_QMV;
@@ -148,6 +163,10 @@ static aq_status run(int variant, const MatmulArgs &a) {
         case AQ_VARIANT_GEMV:
             if (!gemv_supported(a)) return AQ_ERR_UNSUPPORTED;
             err = gemv_launch(a);
+            break;
+        case AQ_VARIANT_TCW:
+            if (!tcw_supported(a)) return AQ_ERR_UNSUPPORTED;
+            err = tcw_launch(a);
             break;
         default:
             return AQ_ERR_INVALID_ARG;
@@ -349,6 +368,7 @@ int aq_describe(int64_t M, int64_t N, int64_t K, int bits, int dtype, char *buf,
         case AQ_VARIANT_GEMV: return gemv_describe(a, buf, buflen);
         case AQ_VARIANT_QMV: return qmv_describe(a, buf, buflen);
         case AQ_VARIANT_TC: return tc_describe(a, buf, buflen);
+        case AQ_VARIANT_TCW: return tcw_describe(a, buf, buflen);
         default: return snprintf(buf, buflen, "generic");
     }
 }
@@ -396,6 +416,7 @@ const char *aq_variant_name(int variant) {
         case AQ_VARIANT_QMV: return "qmv";
         case AQ_VARIANT_TC: return "tc";
         case AQ_VARIANT_GEMV: return "gemv";
+        case AQ_VARIANT_TCW: return "tcw";
     }
     return "?";
 }

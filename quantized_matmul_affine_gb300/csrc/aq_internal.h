@@ -66,6 +66,9 @@ void qmv_force_geometry(int rows_tiles, int cluster_split, int ring_depth);
 int qmv_describe(const MatmulArgs &a, char *buf, int len);
 
 bool tc_supported(const MatmulArgs &a);
+bool tcw_supported(const MatmulArgs &a);
+cudaError_t tcw_launch(const MatmulArgs &a);
+int tcw_describe(const MatmulArgs &a, char *buf, int len);
 cudaError_t tc_launch(const MatmulArgs &a);
 int tc_describe(const MatmulArgs &a, char *buf, int len);
 

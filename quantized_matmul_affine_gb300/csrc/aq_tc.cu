@@ -434,6 +434,290 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 }
 
 // ---------------------------------------------------------------------------
+// "tcw": the same tensor-core path with the roles swapped, for M <= 128.
+//
+// A tcgen05.mma of kind::f16 costs about the same time for any N up to 256
+// (measured on GB300: ~118 cycles for N = 16..128, 128 for N = 256), so with
+// the weights as the 128-row A operand a narrow x tile leaves most of each
+// instruction unused.  Here the x tile is A (128 rows, rows past M read as
+// zero) and a 256-row weight tile is B (N = 256): twice the weights per
+// instruction.  A weight tile's K range is split over the CTAs of a cluster
+// (up to 8) so that narrow outputs still fill the SMs; the partial tiles are
+// added in rank order through distributed shared memory (deterministic).
+//
+// Roles (448 threads): warp 0 TMA producer of x tiles, warp 1 MMA issuer and
+// tensor memory owner, warps 2-5 epilogue, warps 6-13 dequantisation (each
+// streams 32 weight rows, one per lane, through a two-slot cp.async ring).
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kWRows = 256;                  // weight rows per tile (MMA N)
+constexpr int kWXRows = 128;                 // x rows per tile (MMA M)
+constexpr int kWStages = 3;                  // A/B ring depth
+constexpr int kWRawSlots = 2;                // raw super-stages per dequant warp
+constexpr int kWATile = kWXRows * 128;       // 16 KB
+constexpr int kWBTile = kWRows * 128;        // 32 KB
+constexpr int kWPitch = kWRows + 4;          // partial tile: floats per x row
+
+template <int B>
+struct RawW {
+    static constexpr int kGroupBytes = 8 * B;
+    static constexpr int kRowBytes = kGroups * kGroupBytes;  // 128 / 96
+    static constexpr int kRowPitch = kRowBytes + 16;         // 144 / 112: rows in distinct banks
+    static constexpr int kSbOff = 32 * kRowPitch;            // scales[32][4], then biases[32][4]
+    static constexpr int kSlotBytes = kSbOff + 2 * 32 * 8;
+};
+
+}  // namespace
+
+struct TcwParams {
+    const uint32_t *Wq;
+    const __half *scales;
+    const __half *biases;
+    void *y;
+    int M, N, K, G;
+    int splits;   // CTAs of a cluster sharing one weight tile's K range
+    int gps;      // groups per split (a multiple of 4)
+    uint32_t off_raw, off_bar;
+};
+
+template <int B, bool BF16>
+__global__ void __launch_bounds__(kThreadsTc, 1)
+    tcw_kernel(const __grid_constant__ TcwParams p, const __grid_constant__ CUtensorMap tmap_x) {
+    using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+    using R = RawW<B>;
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t *smem = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
+    uint8_t *a_ring = smem;                           // x tiles
+    uint8_t *b_ring = smem + kWStages * kWATile;      // weight tiles
+    uint8_t *raw = smem + p.off_raw;
+    float *partial = reinterpret_cast<float *>(smem);  // after the main loop
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.off_bar);
+    uint64_t *a_full = bars;
+    uint64_t *b_full = bars + kWStages;
+    uint64_t *ab_empty = bars + 2 * kWStages;
+    uint64_t *acc_full = bars + 3 * kWStages;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(acc_full + 1);
+    volatile int *flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = p.splits;
+    const int rank = (int)(blockIdx.x % (unsigned)S);
+    const int n0 = (int)(blockIdx.x / (unsigned)S) * kWRows;
+    const int g0 = rank * p.gps;
+    const int ns = min(p.G, g0 + p.gps) - g0;  // stages of this CTA (>= 4 by the plan)
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kWStages; ++s) {
+            mbar_init(&a_full[s], 1);
+            mbar_init(&b_full[s], kDqWarps);
+            mbar_init(&ab_empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        *flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(tmem_holder, kWRows);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    launch_dependents();
+
+    if (warp == kWarpTma) {
+        if (lane == 0) {
+            grid_dependency_wait();  // x belongs to the stream order
+            for (int i = 0; i < ns; ++i) {
+                const int slot = i % kWStages;
+                const uint32_t ph = (i / kWStages) & 1u;
+                if (i >= kWStages && !tc_wait(&ab_empty[slot], ph ^ 1u, flag, 0x0702)) break;
+                mbar_arrive_expect_tx(&a_full[slot], kWATile);
+                tma_load_2d(a_ring + slot * kWATile, &tmap_x, 64 * (g0 + i), 0, &a_full[slot]);
+            }
+        }
+    } else if (warp == kWarpMma) {
+        // D[x row][weight row] += x . W^T: 4 x (M=128, N=256, K=16) per stage
+        const uint32_t idesc = (1u << 4) | ((BF16 ? 1u : 0u) << 7) | ((BF16 ? 1u : 0u) << 10) |
+                               ((uint32_t)(kWRows >> 3) << 17) | ((uint32_t)(kWXRows >> 4) << 24);
+        const uint64_t a_desc0 = sw128_desc(smem_u32(a_ring));
+        const uint64_t b_desc0 = sw128_desc(smem_u32(b_ring));
+        bool ok = true;
+        for (int i = 0; i < ns; ++i) {
+            const int slot = i % kWStages;
+            const uint32_t ph = (i / kWStages) & 1u;
+            const bool got = tc_wait(&a_full[slot], ph, flag, 0x0802) &&
+                             tc_wait(&b_full[slot], ph, flag, 0x0802);
+            if (!__all_sync(0xffffffffu, got)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint64_t ad = a_desc0 + (uint64_t)((uint32_t)(slot * kWATile) >> 4);
+                const uint64_t bd = b_desc0 + (uint64_t)((uint32_t)(slot * kWBTile) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    tc_mma_f16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (i | kk) != 0);
+                tc_commit(&ab_empty[slot]);
+            }
+            __syncwarp();
+        }
+        if (ok && lane == 0) tc_commit(acc_full);
+        __syncwarp();
+    } else if (warp < kWarpDq) {
+        // Epilogue: TMEM lane = x row m = 32q + lane, column = weight row.
+        const int q = warp & 3;
+        const int m = 32 * q + lane;
+        T *y = static_cast<T *>(p.y);
+        grid_dependency_wait();  // y belongs to the stream order
+        const bool got = tc_wait(acc_full, 0, flag, 0x0902);
+        if (__all_sync(0xffffffffu, got)) {
+            tc_fence_after();
+            for (int c0 = 0; c0 < kWRows; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, v);
+                tmem_wait_ld();
+                if (m >= p.M) continue;
+                if (S > 1) {
+                    float4 *dst = reinterpret_cast<float4 *>(partial + m * kWPitch + c0);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                             __uint_as_float(v[4 * i + 2]),
+                                             __uint_as_float(v[4 * i + 3]));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int n = n0 + c0 + i;
+                        if (n < p.N) y[(size_t)m * p.N + n] = cvt_out<T>(__uint_as_float(v[i]));
+                    }
+                }
+            }
+            tc_fence_before();
+        }
+    } else {
+        // Dequantisation: lane = weight row 32*dw + lane of the tile.
+        const int dw = warp - kWarpDq;
+        uint8_t *ring = raw + dw * kWRawSlots * R::kSlotBytes;
+        const int64_t row_bytes = (int64_t)p.K * B / 8;
+        const int row = 32 * dw + lane;
+        const int64_t n = min(n0 + row, p.N - 1);  // rows past N repeat the last (never stored)
+        const uint8_t *wrow = reinterpret_cast<const uint8_t *>(p.Wq) + n * row_bytes;
+        const int nss = ns / kGroups;  // super-stages (4 groups each)
+        auto issue = [&](int ss, int slot) {
+            uint8_t *dst = ring + slot * R::kSlotBytes;
+            const int64_t kb = (int64_t)(g0 + ss * kGroups) * R::kGroupBytes;
+#pragma unroll
+            for (int c = 0; c < R::kRowBytes / 16; ++c)
+                cp_async16(dst + lane * R::kRowPitch + c * 16, wrow + kb + c * 16, 16u);
+            cp_async8(dst + R::kSbOff + lane * 8, p.scales + n * p.G + g0 + ss * kGroups);
+            cp_async8(dst + R::kSbOff + 256 + lane * 8, p.biases + n * p.G + g0 + ss * kGroups);
+        };
+        for (int pre = 0; pre < kWRawSlots - 1; ++pre) {
+            if (pre < nss) issue(pre, pre);
+            cp_async_commit();
+        }
+        int it = 0;  // stage counter (matches the MMA's)
+        bool ok = true;
+        for (int ss = 0; ss < nss && ok; ++ss) {
+            if (ss + kWRawSlots - 1 < nss) issue(ss + kWRawSlots - 1, (ss + kWRawSlots - 1) % kWRawSlots);
+            cp_async_commit();
+            cp_async_wait<kWRawSlots - 1>();
+            __syncwarp();
+            const uint8_t *slotp = ring + (ss % kWRawSlots) * R::kSlotBytes;
+            const uint2 sv2 = *reinterpret_cast<const uint2 *>(slotp + R::kSbOff + lane * 8);
+            const uint2 bv2 = *reinterpret_cast<const uint2 *>(slotp + R::kSbOff + 256 + lane * 8);
+            const uint4 sv = make_uint4(sv2.x, sv2.y, 0u, 0u);
+            const uint4 bv = make_uint4(bv2.x, bv2.y, 0u, 0u);
+            const uint8_t *rowp = slotp + lane * R::kRowPitch;
+#pragma unroll 1
+            for (int j = 0; j < kGroups; ++j, ++it) {
+                const int slot = it % kWStages;
+                const uint32_t ph = (it / kWStages) & 1u;
+                if (it >= kWStages) {
+                    const bool got = tc_wait(&ab_empty[slot], ph ^ 1u, flag, 0x0a02);
+                    if (!__all_sync(0xffffffffu, got)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                const float sc = h_at(sv, j), bsc = h_at(bv, j);
+                const float bb = fmaf(-128.f, sc, bsc);
+                const uint32_t s2 = h2_at(sv, j), b2 = h2_at(bv, j);
+                uint32_t u[8];  // 8 codes per entry
+                if constexpr (B == 4) {
+                    const uint4 w0 = *reinterpret_cast<const uint4 *>(rowp + j * 32);
+                    const uint4 w1 = *reinterpret_cast<const uint4 *>(rowp + j * 32 + 16);
+                    u[0] = w0.x; u[1] = w0.y; u[2] = w0.z; u[3] = w0.w;
+                    u[4] = w1.x; u[5] = w1.y; u[6] = w1.z; u[7] = w1.w;
+                } else {
+                    const uint32_t *wp = reinterpret_cast<const uint32_t *>(rowp + j * 24);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t w0 = wp[3 * h], w1 = wp[3 * h + 1], w2 = wp[3 * h + 2];
+                        u[4 * h] = w0;
+                        u[4 * h + 1] = __funnelshift_r(w0, w1, 24);
+                        u[4 * h + 2] = __funnelshift_r(w1, w2, 16);
+                        u[4 * h + 3] = w2 >> 8;
+                    }
+                }
+                uint8_t *brow = b_ring + slot * kWBTile + row * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {  // k = 8c .. 8c+7
+                    const uint4 v = dequant8<B, BF16>(u[c], sc, bb, s2, b2);
+                    *reinterpret_cast<uint4 *>(brow + ((c ^ (row & 7)) << 4)) = v;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&b_full[slot]);
+            }
+            __syncwarp();
+        }
+        cp_async_wait<0>();
+    }
+
+    __syncthreads();
+    if (*flag) {
+        // A wait gave up: let copies and MMAs already issued finish before
+        // the tensor memory and shared memory are released.
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 1000000ull) {
+        }
+    }
+    if (S > 1) {
+        // Every CTA of the cluster reaches both barriers, error or not.
+        // Rank r adds its share of the tile's M x 256 elements over all
+        // ranks, rank 0 first, and stores y (every storing thread has waited
+        // for the preceding grid).
+        grid_dependency_wait();
+        cluster_sync();
+        if (!*flag) {
+            T *y = static_cast<T *>(p.y);
+            const int total = p.M * kWRows;
+            const int chunk = (total + S - 1) / S;
+            const int e1 = min(total, (rank + 1) * chunk);
+            const uint32_t base = smem_u32(partial);
+            for (int e = rank * chunk + (int)threadIdx.x; e < e1; e += kThreadsTc) {
+                const int mm = e / kWRows, nn = e - mm * kWRows;
+                if (n0 + nn >= p.N) continue;
+                const uint32_t off = base + 4u * (uint32_t)(mm * kWPitch + nn);
+                float v = 0.f;
+                for (int r = 0; r < S; ++r) v += ld_dsmem_f32(map_to_rank(off, (uint32_t)r));
+                y[(size_t)mm * p.N + n0 + nn] = cvt_out<T>(v);
+            }
+        }
+        cluster_sync();
+    }
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kWRows);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 namespace {
@@ -514,7 +798,107 @@ cudaError_t tc_launch_bm(const TcPlan &pl, const CUtensorMap &tm, cudaStream_t s
     }
 }
 
+// The swapped-role kernel's plan: 256-row weight tiles; the K range of a
+// tile split over S CTAs of a cluster (S <= 8, groups per split a multiple
+// of 4) so that tiles x splits covers the SMs.
+struct TcwPlan {
+    TcwParams prm;
+    size_t smem;
+    int grid;
+};
+
+bool tcw_plan(const MatmulArgs &a, TcwPlan &pl) {
+    if (a.K % 512 != 0 || a.M < 1 || a.M > kWXRows || a.N < 1) return false;
+    if (a.N > INT32_MAX / 2 || a.K > INT32_MAX / 2) return false;
+    TcwParams &q = pl.prm;
+    q.M = (int)a.M;
+    q.N = (int)a.N;
+    q.K = (int)a.K;
+    q.G = (int)(a.K / 64);
+    const int tiles = (int)((a.N + kWRows - 1) / kWRows);
+    int S = std::max(1, std::min(8, num_sms() / tiles));
+    int gps = (q.G + S - 1) / S;
+    gps = (gps + kGroups - 1) / kGroups * kGroups;
+    S = (q.G + gps - 1) / gps;
+    q.splits = S;
+    q.gps = gps;
+    const int raw_slot = a.bits == 4 ? RawW<4>::kSlotBytes : RawW<3>::kSlotBytes;
+    size_t off = (size_t)kWStages * (kWATile + kWBTile);
+    q.off_raw = (uint32_t)off;
+    off += (size_t)kDqWarps * kWRawSlots * raw_slot;
+    off = (off + 15) / 16 * 16;
+    q.off_bar = (uint32_t)off;
+    off += (3 * kWStages + 1) * 8 + 16;
+    pl.smem = off + 1024;  // room to align the base to 1024 bytes
+    if (pl.smem > kSmemLimitTc) return false;
+    if ((size_t)kWXRows * kWPitch * 4 > (size_t)kWStages * (kWATile + kWBTile)) return false;
+    q.Wq = a.Wq;
+    q.scales = static_cast<const __half *>(a.scales);
+    q.biases = static_cast<const __half *>(a.biases);
+    q.y = a.out;
+    pl.grid = tiles * S;
+    return true;
+}
+
+template <int B, bool BF16>
+cudaError_t tcw_launch_t(const TcwPlan &pl, const CUtensorMap &tm, cudaStream_t stream) {
+    auto kern = tcw_kernel<B, BF16>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)kSmemLimitTc);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)pl.grid, 1, 1);
+    cfg.blockDim = dim3(kThreadsTc, 1, 1);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)pl.prm.splits;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kern, pl.prm, tm);
+}
+
 }  // namespace
+
+bool tcw_supported(const MatmulArgs &a) {
+    if (!aligned(a.x, 16) || !aligned(a.Wq, 16) || !aligned(a.scales, 16) ||
+        !aligned(a.biases, 16))
+        return false;
+    TcwPlan pl;
+    return tcw_plan(a, pl);
+}
+
+cudaError_t tcw_launch(const MatmulArgs &a) {
+    TcwPlan pl;
+    if (!tcw_plan(a, pl)) return cudaErrorInvalidValue;
+    CUtensorMap tm;
+    if (!tmap_2d(&tm, a.dtype == AQ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                 a.x, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.K * 2, 64u, (uint32_t)kWXRows,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    if (a.bits == 3)
+        return a.dtype == AQ_BF16 ? tcw_launch_t<3, true>(pl, tm, a.stream)
+                                  : tcw_launch_t<3, false>(pl, tm, a.stream);
+    return a.dtype == AQ_BF16 ? tcw_launch_t<4, true>(pl, tm, a.stream)
+                              : tcw_launch_t<4, false>(pl, tm, a.stream);
+}
+
+int tcw_describe(const MatmulArgs &a, char *buf, int len) {
+    TcwPlan pl;
+    if (!tcw_plan(a, pl)) return snprintf(buf, len, "tcw: unsupported");
+    return snprintf(buf, len, "tcw tiles=%d splits=%d groups/split=%d grid=%d smem=%zu",
+                    pl.grid / pl.prm.splits, pl.prm.splits, pl.prm.gps, pl.grid, pl.smem);
+}
 
 bool tc_supported(const MatmulArgs &a) {
     if (!aligned(a.x, 16) || !aligned(a.Wq, 16) || !aligned(a.scales, 16) ||

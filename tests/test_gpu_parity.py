@@ -18,10 +18,10 @@ pytestmark = pytest.mark.gpu
 
 aq = pytest.importorskip("quantized_matmul_affine_gb300")
 
-GENERIC, QMV, TC, GEMV = (aq.AQ_VARIANT_GENERIC, aq.AQ_VARIANT_QMV, aq.AQ_VARIANT_TC,
-                          aq.AQ_VARIANT_GEMV)
-ALL = [GENERIC, QMV, TC, GEMV]
-ALL_IDS = ["generic", "qmv", "tc", "gemv"]
+GENERIC, QMV, TC, GEMV, TCW = (aq.AQ_VARIANT_GENERIC, aq.AQ_VARIANT_QMV, aq.AQ_VARIANT_TC,
+                               aq.AQ_VARIANT_GEMV, aq.AQ_VARIANT_TCW)
+ALL = [GENERIC, QMV, TC, GEMV, TCW]
+ALL_IDS = ["generic", "qmv", "tc", "gemv", "tcw"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -97,6 +97,12 @@ SHAPES = [
     (24, 700, 1536),
     (32, 2100, 2048),
     (29, 15000, 512),
+    # swapped-role tensor-core kernel: K split over clusters of 2..8, a partial
+    # last weight tile, several tiles
+    (40, 300, 4096),
+    (64, 700, 2048),
+    (128, 1000, 1024),
+    (77, 3000, 1536),
 ]
 
 GEMV_MAX_M = 32
@@ -110,6 +116,8 @@ def test_matmul_parity(shape, bits, dtype, variant):
     M, N, K = shape
     if variant == GEMV and M > GEMV_MAX_M:
         pytest.skip("the resident kernel serves M <= 32")
+    if variant == TCW and M > 128:
+        pytest.skip("the swapped-role tensor-core kernel serves M <= 128")
     p = workloads.make_problem("t", bits, N, K, M, dtype, seed=M * 7 + N + K + bits)
     y = run(p, variant)
     y_ref, bound = reference(p)
