@@ -47,11 +47,11 @@ constexpr int kATileBytes = 128 * 128;
 
 // A/B pipeline depth by x tile width.  The ring has to cover the round trip
 // dequantise -> MMA -> commit -> reuse.
-constexpr int stages_for(int BM) { return BM <= 64 ? 5 : BM <= 128 ? 4 : 3; }
+constexpr int stages_for(int BM) { return BM <= 64 ? 5 : BM <= 128 ? 4 : BM <= 256 ? 3 : 2; }
 // Raw super-stages per dequant warp; all but one are in flight while the
 // warp dequantises, so that the weight stream keeps enough bytes in flight
 // to cover the HBM latency (about 55 KB per SM at four slots).
-constexpr int raw_slots_for(int BM) { return BM <= 128 ? 4 : 3; }
+constexpr int raw_slots_for(int BM) { return BM <= 128 ? 4 : BM <= 256 ? 3 : 2; }
 
 template <int B>
 struct Raw {
@@ -163,6 +163,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     using R = Raw<B>;
     constexpr int kStages = stages_for(BM);
     constexpr int kRawSlots = raw_slots_for(BM);
+    // A 512-row x tile is two N = 256 MMAs per k-step into one 512-column
+    // accumulator (each weight tile dequantised once for 512 x rows); the
+    // narrower tiles double-buffer their accumulator.
+    constexpr int kNI = BM > 256 ? 256 : BM;  // N of one MMA
+    constexpr int kAcc = BM > 256 ? 1 : 2;    // accumulators in tensor memory
     extern __shared__ uint8_t smem_dyn[];
     // Align to 1024 bytes by an offset from the __shared__ array itself, so
     // that every access below stays a shared-memory access (32-bit address).
@@ -223,7 +228,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     const uint32_t ph = (it / kStages) & 1u;
                     if (it >= kStages && !tc_wait(&ab_empty[slot], ph ^ 1u, flag, 0x0102)) goto tma_done;
                     mbar_arrive_expect_tx(&b_full[slot], BM * 128);
-                    tma_load_2d(b_ring + slot * (BM * 128), &tmap_x, 64 * g, m0, &b_full[slot]);
+#pragma unroll
+                    for (int h = 0; h < BM / kNI; ++h)
+                        tma_load_2d(b_ring + slot * (BM * 128) + h * kNI * 128, &tmap_x, 64 * g,
+                                    m0 + h * kNI, &b_full[slot]);
                 }
             }
         tma_done:;
@@ -236,13 +244,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         // k-step 0, plus the byte offset of the slot and k-step over 16.
         // ------------------------------------------------------------------
         const uint32_t idesc = (1u << 4) | ((BF16 ? 1u : 0u) << 7) | ((BF16 ? 1u : 0u) << 10) |
-                               ((uint32_t)(BM >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+                               ((uint32_t)(kNI >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
         const uint64_t a_desc0 = sw128_desc(smem_u32(a_ring));
         const uint64_t b_desc0 = sw128_desc(smem_u32(b_ring));
         uint32_t it = 0, ti = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++ti) {
-            const uint32_t b = ti & 1u, use = ti >> 1;
-            const bool free = ti < 2 || tc_wait(&acc_empty[b], (use & 1u) ^ 1u, flag, 0x0202);
+            const uint32_t b = ti % kAcc, use = ti / kAcc;
+            const bool free = ti < (uint32_t)kAcc ||
+                              tc_wait(&acc_empty[b], (use & 1u) ^ 1u, flag, 0x0202);
             if (!__all_sync(0xffffffffu, free)) break;
             tc_fence_after();
             const uint32_t d = tmem + b * BM;
@@ -262,7 +271,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     const uint64_t bd = b_desc0 + (uint64_t)((uint32_t)(slot * BM * 128) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        tc_mma_f16(d, ad + 2 * kk, bd + 2 * kk, idesc, (g | kk) != 0);
+#pragma unroll
+                        for (int h = 0; h < BM / kNI; ++h)
+                            tc_mma_f16(d + h * kNI, ad + 2 * kk,
+                                       bd + 2 * kk + (uint64_t)((uint32_t)(h * kNI * 128) >> 4),
+                                       idesc, (g | kk) != 0);
                     tc_commit(&ab_empty[slot]);
                 }
                 __syncwarp();
@@ -280,7 +293,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         grid_dependency_wait();
         uint32_t ti = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++ti) {
-            const uint32_t b = ti & 1u, use = ti >> 1;
+            const uint32_t b = ti % kAcc, use = ti / kAcc;
             if (!tc_wait(&acc_full[b], use & 1u, flag, 0x0502)) break;
             tc_fence_after();
             const int n = (tile / p.m_tiles) * 128 + 32 * q + lane;
@@ -734,7 +747,12 @@ struct TcPlan {
 bool tc_plan(const MatmulArgs &a, TcPlan &pl) {
     if (a.K % 512 != 0 || a.M < 1 || a.N < 1) return false;
     if (a.M > INT32_MAX / 2 || a.N > INT32_MAX / 2 || a.K > INT32_MAX / 2) return false;
-    pl.BM = a.M <= 64 ? 64 : a.M <= 128 ? 128 : 256;
+    // 512-row x tiles (each weight tile dequantised once for 512 rows) only
+    // past 512 rows: at M = 512 on GB300 they measured level with two
+    // 256-row tiles (218.7 against 217.8 us, 28672x8192), the two MMAs per
+    // k-step then setting the pace and 224 tiles leaving the second wave of
+    // 152 SMs half empty.
+    pl.BM = a.M <= 64 ? 64 : a.M <= 128 ? 128 : a.M <= 512 ? 256 : 512;
     TcParams &q = pl.prm;
     q.M = (int)a.M;
     q.N = (int)a.N;
@@ -756,7 +774,7 @@ bool tc_plan(const MatmulArgs &a, TcPlan &pl) {
     off += (3 * kStages + 4) * 8 + 16;
     pl.smem = off + 1024;  // room to align the base to 1024 bytes
     if (pl.smem > kSmemLimitTc) return false;
-    q.tmem_cols = pl.BM == 256 ? 512 : pl.BM == 128 ? 256 : 128;
+    q.tmem_cols = pl.BM >= 256 ? 512 : pl.BM == 128 ? 256 : 128;
     q.Wq = a.Wq;
     q.scales = static_cast<const __half *>(a.scales);
     q.biases = static_cast<const __half *>(a.biases);
@@ -794,7 +812,8 @@ cudaError_t tc_launch_bm(const TcPlan &pl, const CUtensorMap &tm, cudaStream_t s
     switch (pl.BM) {
         case 64: return tc_launch_t<B, BF16, 64>(pl, tm, s);
         case 128: return tc_launch_t<B, BF16, 128>(pl, tm, s);
-        default: return tc_launch_t<B, BF16, 256>(pl, tm, s);
+        case 256: return tc_launch_t<B, BF16, 256>(pl, tm, s);
+        default: return tc_launch_t<B, BF16, 512>(pl, tm, s);
     }
 }
 
@@ -914,7 +933,8 @@ cudaError_t tc_launch(const MatmulArgs &a) {
     CUtensorMap tm;
     if (!tmap_2d(&tm, a.dtype == AQ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                 a.x, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.K * 2, 64u, (uint32_t)pl.BM,
+                 a.x, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.K * 2, 64u,
+                 (uint32_t)std::min(pl.BM, 256),
                  CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     if (a.bits == 3)

@@ -103,6 +103,9 @@ SHAPES = [
     (64, 700, 2048),
     (128, 1000, 1024),
     (77, 3000, 1536),
+    # 512-row x tiles of the tc kernel (M > 512): two N = 256 MMAs per
+    # k-step, a second x tile, rows past M
+    (600, 300, 1024),
 ]
 
 GEMV_MAX_M = 32
