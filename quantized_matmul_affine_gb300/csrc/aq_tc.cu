@@ -70,6 +70,11 @@ struct TcParams {
     void *y;
     int M, N, K, G;
     int n_tiles, m_tiles;
+    // Work units: `rounds` rounds of whole tiles (tile = CTA + round * grid),
+    // then `tail` tiles split in two K halves between the two CTAs of a
+    // cluster (cluster c takes tile rounds * grid + c), added at the end
+    // through distributed shared memory.
+    int rounds, tail;
     uint32_t off_b, off_raw, off_bar, tmem_cols;
 };
 
@@ -187,6 +192,23 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int total = p.n_tiles * p.m_tiles;
     const int G = p.G;
+    // Unit u of this CTA: its tile and K range [gb, ge) in groups.
+    auto unit_of = [&](int u, int &tile, int &gb, int &ge) -> bool {
+        if (u < p.rounds) {
+            tile = (int)blockIdx.x + u * (int)gridDim.x;
+            gb = 0;
+            ge = G;
+            return tile < total;
+        }
+        if (u == p.rounds && p.tail > 0 && ((int)blockIdx.x >> 1) < p.tail) {
+            tile = p.rounds * (int)gridDim.x + ((int)blockIdx.x >> 1);
+            const int r = (int)blockIdx.x & 1;
+            gb = r ? G / 2 : 0;
+            ge = r ? G : G / 2;
+            return true;
+        }
+        return false;
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -221,9 +243,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         if (lane == 0) {
             grid_dependency_wait();
             uint32_t it = 0;
-            for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+            int tile, gb, ge;
+            for (int u = 0; unit_of(u, tile, gb, ge); ++u) {
                 const int m0 = (tile % p.m_tiles) * BM;
-                for (int g = 0; g < G; ++g, ++it) {
+                for (int g = gb; g < ge; ++g, ++it) {
                     const int slot = it % kStages;
                     const uint32_t ph = (it / kStages) & 1u;
                     if (it >= kStages && !tc_wait(&ab_empty[slot], ph ^ 1u, flag, 0x0102)) goto tma_done;
@@ -248,7 +271,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const uint64_t a_desc0 = sw128_desc(smem_u32(a_ring));
         const uint64_t b_desc0 = sw128_desc(smem_u32(b_ring));
         uint32_t it = 0, ti = 0;
-        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++ti) {
+        int tile, gb, ge;
+        for (int u = 0; unit_of(u, tile, gb, ge); ++u, ++ti) {
             const uint32_t b = ti % kAcc, use = ti / kAcc;
             const bool free = ti < (uint32_t)kAcc ||
                               tc_wait(&acc_empty[b], (use & 1u) ^ 1u, flag, 0x0202);
@@ -256,7 +280,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             tc_fence_after();
             const uint32_t d = tmem + b * BM;
             bool ok = true;
-            for (int g = 0; g < G; ++g, ++it) {
+            for (int g = gb; g < ge; ++g, ++it) {
                 const int slot = it % kStages;
                 const uint32_t ph = (it / kStages) & 1u;
                 const bool got = tc_wait(&a_full[slot], ph, flag, 0x0302) &&
@@ -275,7 +299,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                         for (int h = 0; h < BM / kNI; ++h)
                             tc_mma_f16(d + h * kNI, ad + 2 * kk,
                                        bd + 2 * kk + (uint64_t)((uint32_t)(h * kNI * 128) >> 4),
-                                       idesc, (g | kk) != 0);
+                                       idesc, (g != gb || kk != 0) ? 1u : 0u);
                     tc_commit(&ab_empty[slot]);
                 }
                 __syncwarp();
@@ -292,10 +316,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         T *y = static_cast<T *>(p.y);
         grid_dependency_wait();
         uint32_t ti = 0;
-        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++ti) {
+        int tile, gb, ge;
+        for (int u = 0; unit_of(u, tile, gb, ge); ++u, ++ti) {
             const uint32_t b = ti % kAcc, use = ti / kAcc;
             if (!tc_wait(&acc_full[b], use & 1u, flag, 0x0502)) break;
             tc_fence_after();
+            if (u >= p.rounds) break;  // a split tail tile: added at the end
             const int n = (tile / p.m_tiles) * 128 + 32 * q + lane;
             const int m0 = (tile % p.m_tiles) * BM;
             for (int c0 = 0; c0 < BM && m0 + c0 < p.M; c0 += 16) {
@@ -321,7 +347,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const int dw = warp - kWarpDq;
         uint8_t *ring = raw + dw * kRawSlots * R::kSlotBytes;
         const int64_t row_bytes = (int64_t)p.K * B / 8;
-        const int nss = G / kGroups;  // super-stages per tile
         // copy plan: kChunks 16-byte pieces of 16 rows per super-stage + s/b
         constexpr int kChunks = R::kChunksPerRow / 2;
         uint32_t roff[kChunks], doff[kChunks];
@@ -350,13 +375,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             const __half *base = (lane < 16) ? p.scales : p.biases;
             cp_async8(dst + R::kSbOff + (lane >> 4) * 128 + sr * 8, base + n * p.G + ss * kGroups);
         };
-        // flat sequence of (tile, super-stage) for this CTA
-        int tile = blockIdx.x, ss = 0;
-        int ntile = tile, nss_next = 0;  // next to issue
-        auto advance = [&](int &t, int &s) {
-            if (++s == nss) {
-                s = 0;
-                t += gridDim.x;
+        // flat sequence of (unit, super-stage) for this CTA: the one being
+        // dequantised (c...) and the next one to issue (n...)
+        int cu = 0, ctile = 0, cgb = 0, cge = 0, css = 0;
+        bool cvalid = unit_of(cu, ctile, cgb, cge);
+        int nu = 0, ntile = 0, ngb = 0, nge = 0, nss_next = 0;
+        bool nvalid = unit_of(nu, ntile, ngb, nge);
+        auto advance = [&](int &u, int &t, int &gbv, int &gev, bool &valid, int &ssv) {
+            if (++ssv == (gev - gbv) / kGroups) {
+                ssv = 0;
+                ++u;
+                valid = unit_of(u, t, gbv, gev);
             }
         };
         uint32_t it = 0;  // A-stage counter (matches the MMA's)
@@ -364,21 +393,21 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         // kRawSlots - 1 super-stages ahead, one commit group each
 #pragma unroll 1
         for (int pre = 0; pre < kRawSlots - 1; ++pre) {
-            if (ntile < total) {
-                issue(ntile, nss_next, iss % kRawSlots);
+            if (nvalid) {
+                issue(ntile, ngb / kGroups + nss_next, iss % kRawSlots);
                 ++iss;
-                advance(ntile, nss_next);
+                advance(nu, ntile, ngb, nge, nvalid, nss_next);
             }
             cp_async_commit();
         }
         const int rl = lane >> 1, h = lane & 1;
         const int arow = 16 * dw + rl;  // row within the 128-row A tile
         bool ok = true;
-        for (int cnt = 0; tile < total && ok; ++cnt) {
-            if (ntile < total) {
-                issue(ntile, nss_next, iss % kRawSlots);
+        for (int cnt = 0; cvalid && ok; ++cnt) {
+            if (nvalid) {
+                issue(ntile, ngb / kGroups + nss_next, iss % kRawSlots);
                 ++iss;
-                advance(ntile, nss_next);
+                advance(nu, ntile, ngb, nge, nvalid, nss_next);
             }
             cp_async_commit();
             cp_async_wait<kRawSlots - 1>();
@@ -427,7 +456,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 if (lane == 0) mbar_arrive(&a_full[slot]);
             }
             __syncwarp();
-            advance(tile, ss);
+            advance(cu, ctile, cgb, cge, cvalid, css);
         }
         cp_async_wait<0>();
     }
@@ -439,6 +468,66 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const uint64_t t0 = globaltimer_ns();
         while (globaltimer_ns() - t0 < 1000000ull) {
         }
+    }
+    if (p.tail > 0 && ((int)blockIdx.x >> 1) < p.tail) {
+        // The split tail tile: rank 1 hands its half of the accumulator to
+        // rank 0 through distributed shared memory, up to 256 columns at a
+        // time (the idle ring holds them); rank 0 adds it to its own half
+        // (rank 0 first) and stores y.  Both CTAs of the cluster take every
+        // barrier, error or not.
+        constexpr int kCh = BM < 256 ? BM : 256;  // columns per hand-over
+        constexpr int kXP = kCh + 4;              // floats per row of the buffer
+        static_assert(128 * kXP * 4 <= kStages * (kATileBytes + BM * 128), "hand-over buffer");
+        const int r = (int)blockIdx.x & 1;
+        const int tile = p.rounds * (int)gridDim.x + ((int)blockIdx.x >> 1);
+        int nfull = 0;  // whole tiles this CTA took before the tail
+        for (int u = 0; u < p.rounds; ++u)
+            nfull += ((int)blockIdx.x + u * (int)gridDim.x < total) ? 1 : 0;
+        const uint32_t b = (uint32_t)nfull % kAcc;
+        float *xbuf = reinterpret_cast<float *>(smem);  // [128][kXP] floats on rank 0
+        const bool epi = warp >= kWarpMma + 1 && warp < kWarpDq;
+        const int q = warp & 3;
+        const int row = 32 * q + lane;  // weight row of the tile
+        const int n = (tile / p.m_tiles) * 128 + row;
+        const int m0 = (tile % p.m_tiles) * BM;
+        T *y = static_cast<T *>(p.y);
+        const uint32_t rbuf = map_to_rank(smem_u32(xbuf), 0u) + 4u * (uint32_t)(row * kXP);
+        const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + b * BM;
+        tc_fence_after();
+        // rank 0's ring (the buffer) is idle only once its main loop is done
+        cluster_sync();
+        for (int c0 = 0; c0 < BM; c0 += kCh) {
+            if (epi && r == 1) {
+                for (int c1 = 0; c1 < kCh; c1 += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(ta + (uint32_t)(c0 + c1), v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4)
+                        st_dsmem_v4(rbuf + 4u * (uint32_t)(c1 + j), __uint_as_float(v[j]),
+                                    __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
+                                    __uint_as_float(v[j + 3]));
+                }
+            }
+            cluster_sync();
+            if (epi && r == 0) {
+                for (int c1 = 0; c1 < kCh; c1 += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(ta + (uint32_t)(c0 + c1), v);
+                    tmem_wait_ld();
+                    if (*flag || n >= p.N) continue;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int m = m0 + c0 + c1 + j;
+                        if (m < p.M)
+                            y[(size_t)m * p.N + n] =
+                                cvt_out<T>(__uint_as_float(v[j]) + xbuf[row * kXP + c1 + j]);
+                    }
+                }
+            }
+            cluster_sync();
+        }
+        tc_fence_before();
     }
     if (warp == kWarpMma) {
         tc_fence_after();
@@ -747,12 +836,9 @@ struct TcPlan {
 bool tc_plan(const MatmulArgs &a, TcPlan &pl) {
     if (a.K % 512 != 0 || a.M < 1 || a.N < 1) return false;
     if (a.M > INT32_MAX / 2 || a.N > INT32_MAX / 2 || a.K > INT32_MAX / 2) return false;
-    // 512-row x tiles (each weight tile dequantised once for 512 rows) only
-    // past 512 rows: at M = 512 on GB300 they measured level with two
-    // 256-row tiles (218.7 against 217.8 us, 28672x8192), the two MMAs per
-    // k-step then setting the pace and 224 tiles leaving the second wave of
-    // 152 SMs half empty.
-    pl.BM = a.M <= 64 ? 64 : a.M <= 128 ? 128 : a.M <= 512 ? 256 : 512;
+    // Past 256 rows, 512-row x tiles: each weight tile is dequantised once
+    // for 512 rows (two N = 256 MMAs per k-step).
+    pl.BM = a.M <= 64 ? 64 : a.M <= 128 ? 128 : a.M <= 256 ? 256 : 512;
     TcParams &q = pl.prm;
     q.M = (int)a.M;
     q.N = (int)a.N;
@@ -780,7 +866,22 @@ bool tc_plan(const MatmulArgs &a, TcPlan &pl) {
     q.biases = static_cast<const __half *>(a.biases);
     q.y = a.out;
     const int total = q.n_tiles * q.m_tiles;
-    pl.grid = std::min(total, num_sms());
+    int grid = std::min(total, num_sms());
+    q.rounds = (total + grid - 1) / grid;
+    q.tail = 0;
+    // Tiles left over after whole rounds, when they fill at most half of the
+    // grid, are split in two K halves over CTA pairs (clusters of two)
+    // instead of running a half-empty round.
+    const int g2 = grid & ~1;
+    if (g2 >= 2 && q.G % (2 * kGroups) == 0) {
+        const int full = total / g2, rem = total - full * g2;
+        if (rem > 0 && rem <= g2 / 2) {
+            grid = g2;
+            q.rounds = full;
+            q.tail = rem;
+        }
+    }
+    pl.grid = grid;
     return true;
 }
 
@@ -799,11 +900,15 @@ cudaError_t tc_launch_t(const TcPlan &pl, const CUtensorMap &tm, cudaStream_t st
     cfg.blockDim = dim3(kThreadsTc, 1, 1);
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = pl.prm.tail > 0 ? 2u : 1u;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, pl.prm, tm);
 }
 
@@ -947,9 +1052,10 @@ cudaError_t tc_launch(const MatmulArgs &a) {
 int tc_describe(const MatmulArgs &a, char *buf, int len) {
     TcPlan pl;
     if (!tc_plan(a, pl)) return snprintf(buf, len, "tc: unsupported");
-    return snprintf(buf, len, "tc bm=%d stages=%d tiles=%dx%d grid=%d smem=%zu tmem=%u", pl.BM,
-                    stages_for(pl.BM), pl.prm.n_tiles, pl.prm.m_tiles, pl.grid, pl.smem,
-                    pl.prm.tmem_cols);
+    return snprintf(buf, len,
+                    "tc bm=%d stages=%d tiles=%dx%d grid=%d rounds=%d split=%d smem=%zu tmem=%u",
+                    pl.BM, stages_for(pl.BM), pl.prm.n_tiles, pl.prm.m_tiles, pl.grid,
+                    pl.prm.rounds, pl.prm.tail, pl.smem, pl.prm.tmem_cols);
 }
 
 cudaError_t tc_read_error(uint32_t *code, bool clear) {
