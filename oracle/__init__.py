@@ -64,12 +64,19 @@ def _load() -> ctypes.CDLL:
             lib.oracle_matmul_cols.argtypes = [p, p, p, p, i64, i64, i64, i32, p, i64, p, p]
             lib.oracle_matmul_threads.argtypes = [p, p, p, p, i64, i64, i64, i32, p, p, i32]
             lib.oracle_quantize.argtypes = [p, i64, i64, i32, p, p, p]
+            lib.oracle_pack_g.argtypes = [p, i64, i64, i32, p]
+            lib.oracle_unpack_g.argtypes = [p, i64, i64, i32, p]
+            lib.oracle_dequant_g.argtypes = [p, p, p, i64, i64, i32, i32, p]
+            lib.oracle_matmul_g.argtypes = [p, p, p, p, i64, i64, i64, i32, i32, p, p, i32]
+            lib.oracle_quantize_g.argtypes = [p, i64, i64, i32, i32, p, p, p]
             lib.oracle_f32_to_f16.argtypes = [ctypes.c_float]
             lib.oracle_f32_to_f16.restype = ctypes.c_uint16
             lib.oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
             lib.oracle_f16_to_f32.restype = ctypes.c_float
             for f in ("oracle_pack", "oracle_unpack", "oracle_dequant", "oracle_matmul",
-                      "oracle_matmul_cols", "oracle_matmul_threads", "oracle_quantize"):
+                      "oracle_matmul_cols", "oracle_matmul_threads", "oracle_quantize",
+                      "oracle_pack_g", "oracle_unpack_g", "oracle_dequant_g", "oracle_matmul_g",
+                      "oracle_quantize_g"):
                 getattr(lib, f).restype = i32
             _lib = lib
     return _lib
@@ -196,4 +203,65 @@ def quantize(w: np.ndarray, bits: int):
     bb = np.zeros((N, G), dtype=np.uint16)
     _check(_load().oracle_quantize(_ptr(w), N, K, bits, _ptr(codes), _ptr(sb), _ptr(bb)),
            "quantize")
+    return codes, sb, bb
+
+
+# ---------------------------------------------------------------------------
+# Other code widths (2, 3, 4, 5, 6, 8 bits) and group sizes (32, 64, 128)
+# ---------------------------------------------------------------------------
+
+def pack_g(codes: np.ndarray, bits: int) -> np.ndarray:
+    """codes uint8 [N, K] -> words uint32 [N, K*bits/32], any width of the set,
+    K a multiple of 32."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    N, K = codes.shape
+    out = np.zeros((N, K * bits // 32), dtype=np.uint32)
+    _check(_load().oracle_pack_g(_ptr(codes), N, K, bits, _ptr(out)), "pack_g")
+    return out
+
+
+def unpack_g(words: np.ndarray, K: int, bits: int) -> np.ndarray:
+    words = np.ascontiguousarray(words, dtype=np.uint32)
+    N = words.shape[0]
+    if words.shape[1] != K * bits // 32:
+        raise ValueError("words has the wrong row length for K and bits")
+    out = np.zeros((N, K), dtype=np.uint8)
+    _check(_load().oracle_unpack_g(_ptr(words), N, K, bits, _ptr(out)), "unpack_g")
+    return out
+
+
+def dequant_g(words, scales, biases, K: int, bits: int, group: int) -> np.ndarray:
+    words = np.ascontiguousarray(words, dtype=np.uint32)
+    s, b = _f64(scales), _f64(biases)
+    N = words.shape[0]
+    out = np.zeros((N, K), dtype=np.float64)
+    _check(_load().oracle_dequant_g(_ptr(words), _ptr(s), _ptr(b), N, K, bits, group, _ptr(out)),
+           "dequant_g")
+    return out
+
+
+def matmul_g(x, words, scales, biases, bits: int, group: int, threads: int = 1):
+    """y = x . dequant(W)^T and bound = sum_k |x*w| for any width and group size."""
+    x = _f64(x)
+    words = np.ascontiguousarray(words, dtype=np.uint32)
+    s, b = _f64(scales), _f64(biases)
+    M, K = x.shape
+    N = words.shape[0]
+    y = np.zeros((M, N), dtype=np.float64)
+    bound = np.zeros((M, N), dtype=np.float64)
+    _check(_load().oracle_matmul_g(_ptr(x), _ptr(words), _ptr(s), _ptr(b), M, N, K, bits, group,
+                                   _ptr(y), _ptr(bound), threads), "matmul_g")
+    return y, bound
+
+
+def quantize_g(w: np.ndarray, bits: int, group: int):
+    """quantize() for any width and group size."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    N, K = w.shape
+    codes = np.zeros((N, K), dtype=np.uint8)
+    G = K // group
+    sb = np.zeros((N, G), dtype=np.uint16)
+    bb = np.zeros((N, G), dtype=np.uint16)
+    _check(_load().oracle_quantize_g(_ptr(w), N, K, bits, group, _ptr(codes), _ptr(sb), _ptr(bb)),
+           "quantize_g")
     return codes, sb, bb

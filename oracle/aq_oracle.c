@@ -38,6 +38,23 @@ static int valid_shape(int64_t N, int64_t K, int bits) {
     return 1;
 }
 
+/*
+ * Other code widths and group sizes (the "_g" functions below): B in
+ * {2,3,4,5,6,8} and groups of 32, 64 or 128 values.  The bit stream is the
+ * same LSB-first stream per row (code v at bits [v*B, v*B+B)), which needs
+ * K*B to be a multiple of 32; scales and biases are [N][K/group].  The pages'
+ * fused-decode kernel takes 4 and 8 bits with groups of 32, 64 and 128.
+ */
+static int valid_bits(int bits) {
+    return bits == 2 || bits == 3 || bits == 4 || bits == 5 || bits == 6 || bits == 8;
+}
+
+static int valid_shape_g(int64_t N, int64_t K, int bits, int group) {
+    if (N < 0 || K < 0 || !valid_bits(bits)) return 0;
+    if (group != 32 && group != 64 && group != 128) return 0;
+    return K % group == 0;
+}
+
 /* Words per row: K values of B bits each, 32 bits per word. */
 int64_t oracle_words_per_row(int64_t K, int bits) { return K * bits / 32; }
 
@@ -46,8 +63,7 @@ int64_t oracle_words_per_row(int64_t K, int bits) { return K * bits / 32; }
  * stream bit i lives in word i/32 at bit i%32 (least significant first).
  * Only the low B bits of each code are used.
  */
-int oracle_pack(const uint8_t *codes, int64_t N, int64_t K, int bits, uint32_t *words) {
-    if (!valid_shape(N, K, bits)) return 1;
+static void pack_rows(const uint8_t *codes, int64_t N, int64_t K, int bits, uint32_t *words) {
     const int64_t wpr = oracle_words_per_row(K, bits);
     const uint32_t mask = (1u << bits) - 1u;
     memset(words, 0, (size_t)(N * wpr) * sizeof(uint32_t));
@@ -62,6 +78,18 @@ int oracle_pack(const uint8_t *codes, int64_t N, int64_t K, int bits, uint32_t *
             if (off + bits > 32) row[w + 1] |= q >> (32 - off);
         }
     }
+}
+
+int oracle_pack(const uint8_t *codes, int64_t N, int64_t K, int bits, uint32_t *words) {
+    if (!valid_shape(N, K, bits)) return 1;
+    pack_rows(codes, N, K, bits, words);
+    return 0;
+}
+
+/* Any width of valid_bits, K a multiple of 32. */
+int oracle_pack_g(const uint8_t *codes, int64_t N, int64_t K, int bits, uint32_t *words) {
+    if (!valid_shape_g(N, K, bits, 32)) return 1;
+    pack_rows(codes, N, K, bits, words);
     return 0;
 }
 
@@ -75,28 +103,44 @@ static uint32_t oracle_code(const uint32_t *row, int64_t v, int bits) {
     return q & ((1u << bits) - 1u);
 }
 
-int oracle_unpack(const uint32_t *words, int64_t N, int64_t K, int bits, uint8_t *codes) {
-    if (!valid_shape(N, K, bits)) return 1;
+static void unpack_rows(const uint32_t *words, int64_t N, int64_t K, int bits, uint8_t *codes) {
     const int64_t wpr = oracle_words_per_row(K, bits);
     for (int64_t n = 0; n < N; ++n)
         for (int64_t v = 0; v < K; ++v)
             codes[n * K + v] = (uint8_t)oracle_code(words + n * wpr, v, bits);
+}
+
+int oracle_unpack(const uint32_t *words, int64_t N, int64_t K, int bits, uint8_t *codes) {
+    if (!valid_shape(N, K, bits)) return 1;
+    unpack_rows(words, N, K, bits, codes);
     return 0;
 }
 
-/* Dequantise: W[n][k] = scale[n][k/64] * q[n][k] + bias[n][k/64]. */
-int oracle_dequant(const uint32_t *words, const double *scales, const double *biases,
-                   int64_t N, int64_t K, int bits, double *W) {
-    if (!valid_shape(N, K, bits)) return 1;
+int oracle_unpack_g(const uint32_t *words, int64_t N, int64_t K, int bits, uint8_t *codes) {
+    if (!valid_shape_g(N, K, bits, 32)) return 1;
+    unpack_rows(words, N, K, bits, codes);
+    return 0;
+}
+
+/* Dequantise: W[n][k] = scale[n][k/group] * q[n][k] + bias[n][k/group]. */
+int oracle_dequant_g(const uint32_t *words, const double *scales, const double *biases,
+                     int64_t N, int64_t K, int bits, int group, double *W) {
+    if (!valid_shape_g(N, K, bits, group)) return 1;
     const int64_t wpr = oracle_words_per_row(K, bits);
-    const int64_t G = K / ORACLE_GROUP;
+    const int64_t G = K / group;
     for (int64_t n = 0; n < N; ++n)
         for (int64_t k = 0; k < K; ++k) {
-            const int64_t g = k / ORACLE_GROUP;
+            const int64_t g = k / group;
             const double q = (double)oracle_code(words + n * wpr, k, bits);
             W[n * K + k] = scales[n * G + g] * q + biases[n * G + g];
         }
     return 0;
+}
+
+int oracle_dequant(const uint32_t *words, const double *scales, const double *biases,
+                   int64_t N, int64_t K, int bits, double *W) {
+    if (!valid_shape(N, K, bits)) return 1;
+    return oracle_dequant_g(words, scales, biases, N, K, bits, ORACLE_GROUP, W);
 }
 
 /*
@@ -105,10 +149,11 @@ int oracle_dequant(const uint32_t *words, const double *scales, const double *bi
  *   bound[m][n] = sum_k |x[m][k] * w[n][k]|
  */
 static void oracle_element(const double *xrow, const uint32_t *wrow, const double *srow,
-                           const double *brow, int64_t K, int bits, double *y, double *bound) {
+                           const double *brow, int64_t K, int bits, int group, double *y,
+                           double *bound) {
     double acc = 0.0, mag = 0.0;
     for (int64_t k = 0; k < K; ++k) {
-        const int64_t g = k / ORACLE_GROUP;
+        const int64_t g = k / group;
         const double w = srow[g] * (double)oracle_code(wrow, k, bits) + brow[g];
         const double p = xrow[k] * w;
         acc += p;
@@ -128,7 +173,7 @@ int oracle_matmul(const double *x, const uint32_t *words, const double *scales,
     for (int64_t m = 0; m < M; ++m)
         for (int64_t n = 0; n < N; ++n)
             oracle_element(x + m * K, words + n * wpr, scales + n * G, biases + n * G, K, bits,
-                           &y[m * N + n], bound ? &bound[m * N + n] : NULL);
+                           ORACLE_GROUP, &y[m * N + n], bound ? &bound[m * N + n] : NULL);
     return 0;
 }
 
@@ -148,7 +193,7 @@ int oracle_matmul_cols(const double *x, const uint32_t *words, const double *sca
         for (int64_t j = 0; j < ncols; ++j) {
             const int64_t n = cols[j];
             oracle_element(x + m * K, words + n * wpr, scales + n * G, biases + n * G, K, bits,
-                           &y[m * ncols + j], bound ? &bound[m * ncols + j] : NULL);
+                           ORACLE_GROUP, &y[m * ncols + j], bound ? &bound[m * ncols + j] : NULL);
         }
     return 0;
 }
@@ -164,7 +209,7 @@ struct oracle_job {
     const uint32_t *words;
     const double *scales, *biases;
     int64_t M, N, K;
-    int bits;
+    int bits, group;
     int64_t n_begin, n_end;
     double *y, *bound;
 };
@@ -172,26 +217,27 @@ struct oracle_job {
 static void *oracle_worker(void *arg) {
     const struct oracle_job *j = (const struct oracle_job *)arg;
     const int64_t wpr = oracle_words_per_row(j->K, j->bits);
-    const int64_t G = j->K / ORACLE_GROUP;
+    const int64_t G = j->K / j->group;
     for (int64_t m = 0; m < j->M; ++m)
         for (int64_t n = j->n_begin; n < j->n_end; ++n)
             oracle_element(j->x + m * j->K, j->words + n * wpr, j->scales + n * G,
-                           j->biases + n * G, j->K, j->bits, &j->y[m * j->N + n],
+                           j->biases + n * G, j->K, j->bits, j->group, &j->y[m * j->N + n],
                            j->bound ? &j->bound[m * j->N + n] : NULL);
     return NULL;
 }
 
-int oracle_matmul_threads(const double *x, const uint32_t *words, const double *scales,
-                          const double *biases, int64_t M, int64_t N, int64_t K, int bits,
-                          double *y, double *bound, int nthreads) {
-    if (!valid_shape(N, K, bits) || M < 0) return 1;
+/* y and bound for any width and group size, on nthreads threads. */
+int oracle_matmul_g(const double *x, const uint32_t *words, const double *scales,
+                    const double *biases, int64_t M, int64_t N, int64_t K, int bits, int group,
+                    double *y, double *bound, int nthreads) {
+    if (!valid_shape_g(N, K, bits, group) || M < 0) return 1;
     if (nthreads < 1) nthreads = 1;
     if (nthreads > 256) nthreads = 256;
     pthread_t tid[256];
     int running[256];
     struct oracle_job jobs[256];
     for (int t = 0; t < nthreads; ++t) {
-        jobs[t] = (struct oracle_job){x, words, scales, biases, M, N, K, bits,
+        jobs[t] = (struct oracle_job){x, words, scales, biases, M, N, K, bits, group,
                                       N * t / nthreads, N * (t + 1) / nthreads, y, bound};
         running[t] = pthread_create(&tid[t], NULL, oracle_worker, &jobs[t]) == 0;
         if (!running[t]) oracle_worker(&jobs[t]); /* no thread available: run it here */
@@ -199,6 +245,14 @@ int oracle_matmul_threads(const double *x, const uint32_t *words, const double *
     for (int t = 0; t < nthreads; ++t)
         if (running[t]) pthread_join(tid[t], NULL);
     return 0;
+}
+
+int oracle_matmul_threads(const double *x, const uint32_t *words, const double *scales,
+                          const double *biases, int64_t M, int64_t N, int64_t K, int bits,
+                          double *y, double *bound, int nthreads) {
+    if (!valid_shape(N, K, bits) || M < 0) return 1;
+    return oracle_matmul_g(x, words, scales, biases, M, N, K, bits, ORACLE_GROUP, y, bound,
+                           nthreads);
 }
 
 /* ------------------------------------------------------------------------
@@ -260,16 +314,16 @@ uint16_t oracle_f32_to_f16(float f) {
     return (uint16_t)(sign | (uint16_t)((ev + 15) << 10) | mant);
 }
 
-int oracle_quantize(const float *w, int64_t N, int64_t K, int bits, uint8_t *codes,
-                    uint16_t *scale_bits, uint16_t *bias_bits) {
-    if (!valid_shape(N, K, bits)) return 1;
-    const int64_t G = K / ORACLE_GROUP;
+int oracle_quantize_g(const float *w, int64_t N, int64_t K, int bits, int group, uint8_t *codes,
+                      uint16_t *scale_bits, uint16_t *bias_bits) {
+    if (!valid_shape_g(N, K, bits, group)) return 1;
+    const int64_t G = K / group;
     const int qmax = (1 << bits) - 1;
     for (int64_t n = 0; n < N; ++n)
         for (int64_t g = 0; g < G; ++g) {
-            const float *wg = w + n * K + g * ORACLE_GROUP;
+            const float *wg = w + n * K + g * group;
             float lo = wg[0], hi = wg[0];
-            for (int v = 1; v < ORACLE_GROUP; ++v) {
+            for (int v = 1; v < group; ++v) {
                 if (wg[v] < lo) lo = wg[v];
                 if (wg[v] > hi) hi = wg[v];
             }
@@ -281,15 +335,21 @@ int oracle_quantize(const float *w, int64_t N, int64_t K, int bits, uint8_t *cod
             bias_bits[n * G + g] = bb;
             const float s = oracle_f16_to_f32(sb);
             const float b = oracle_f16_to_f32(bb);
-            for (int v = 0; v < ORACLE_GROUP; ++v) {
+            for (int v = 0; v < group; ++v) {
                 int q = 0;
                 if (s != 0.0f) {
                     const float t = (wg[v] - b) / s;
                     const float r = rintf(t);
                     q = r < 0.0f ? 0 : r > (float)qmax ? qmax : (int)r;
                 }
-                codes[n * K + g * ORACLE_GROUP + v] = (uint8_t)q;
+                codes[n * K + g * group + v] = (uint8_t)q;
             }
         }
     return 0;
+}
+
+int oracle_quantize(const float *w, int64_t N, int64_t K, int bits, uint8_t *codes,
+                    uint16_t *scale_bits, uint16_t *bias_bits) {
+    if (!valid_shape(N, K, bits)) return 1;
+    return oracle_quantize_g(w, N, K, bits, ORACLE_GROUP, codes, scale_bits, bias_bits);
 }

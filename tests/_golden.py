@@ -36,8 +36,8 @@ def codes_from_rule(rule: str, K: int) -> np.ndarray:
     raise ValueError(rule)
 
 
-def pack_vectors():
-    for name, bits, K, rule, words in _lines("pack_vectors.txt"):
+def pack_vectors(name_of_file="pack_vectors.txt"):
+    for name, bits, K, rule, words in _lines(name_of_file):
         K = int(K)
         yield (name, int(bits), K, codes_from_rule(rule, K),
                np.array([int(w, 16) for w in words.split()], dtype=np.uint32))
