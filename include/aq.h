@@ -77,9 +77,12 @@ typedef enum aq_variant {
  *   codes_dev  uint8 [N][K], device; only the low `bits` bits of each code
  *              are used (higher bits are ignored).
  *   words_dev  uint32 [N][K*bits/32], device, written entirely.
- * Errors: AQ_ERR_INVALID_ARG if N < 0, K < 0, K % 64 != 0, bits not in {3,4},
- * or a pointer is NULL while N*K > 0; AQ_ERR_MISALIGNED if words_dev is not
- * 4-byte aligned.  N == 0 or K == 0 queues nothing and returns AQ_OK.
+ * bits may be 2, 3, 4, 5, 6 or 8 (the same LSB-first stream; the matmul
+ * takes 3 and 4 at groups of 64 in aq_matmul and the others in
+ * aq_matmul_ex).
+ * Errors: AQ_ERR_INVALID_ARG if N < 0, K < 0, K % 32 != 0, bits outside that
+ * set, or a pointer is NULL while N*K > 0; AQ_ERR_MISALIGNED if words_dev is
+ * not 4-byte aligned.  N == 0 or K == 0 queues nothing and returns AQ_OK.
  */
 aq_status aq_pack(const uint8_t *codes_dev, int64_t N, int64_t K, int bits,
                   uint32_t *words_dev, void *stream);
@@ -133,6 +136,32 @@ aq_status aq_matmul(const void *x_dev, const uint32_t *Wq_dev, const void *scale
 aq_status aq_matmul_bf16(const void *x_dev, const uint32_t *Wq_dev, const void *scales_dev,
                          const void *biases_dev, int64_t M, int64_t N, int64_t K, int bits,
                          void *out_dev, void *stream);
+
+/*
+ * aq_matmul_ex — aq_matmul for other code widths and group sizes: bits in
+ * {2, 3, 4, 5, 6, 8}, groups of group_size in {32, 64, 128} values (the
+ * pages' fused-decode kernel takes 4 and 8 bits with groups of 32, 64 and
+ * 128).  Wq_dev is the same LSB-first stream (aq_pack), scales and biases
+ * fp16 [N][K/group_size]; dtype AQ_F16 or AQ_BF16 for x and y.  3 and 4 bits
+ * at groups of 64 run exactly as aq_matmul / aq_matmul_bf16 (the fast
+ * kernels); everything else runs the plain CUDA-core kernel
+ * (AQ_VARIANT_GENERIC).  Tolerance, ownership and errors as aq_matmul, with
+ * K % group_size == 0 in place of K % 64 == 0.
+ */
+aq_status aq_matmul_ex(int dtype, const void *x_dev, const uint32_t *Wq_dev,
+                       const void *scales_dev, const void *biases_dev, int64_t M, int64_t N,
+                       int64_t K, int bits, int group_size, void *out_dev, void *stream);
+
+/*
+ * aq_quantize_ex — aq_quantize / aq_quantize_bf16 (dtype AQ_F16 / AQ_BF16)
+ * for other code widths and group sizes (as aq_matmul_ex), with the same
+ * rule per group; codes decided with the IEEE quotient in single precision.
+ * w_dev 2-byte aligned; scales/biases fp16 [N][K/group_size].  Errors as
+ * aq_quantize with K % group_size == 0.
+ */
+aq_status aq_quantize_ex(int dtype, const void *w_dev, int64_t N, int64_t K, int bits,
+                         int group_size, uint32_t *Wq_dev, void *scales_dev, void *biases_dev,
+                         void *stream);
 
 /* Largest number of projections aq_matmul_multi takes in one call. */
 #define AQ_MAX_PROJ 4

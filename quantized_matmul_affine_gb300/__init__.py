@@ -24,6 +24,7 @@ __all__ = [
     "AqError", "AQ_F16", "AQ_BF16", "AQ_VARIANT_AUTO", "AQ_VARIANT_GENERIC", "AQ_VARIANT_QMV",
     "AQ_VARIANT_TC", "AQ_VARIANT_GEMV", "AQ_VARIANT_TCW", "AQ_NUM_VARIANTS", "aq_pack", "aq_quantize",
     "aq_quantize_bf16", "aq_matmul", "aq_matmul_bf16", "aq_matmul_multi", "aq_matmul_gate_up",
+    "aq_matmul_ex", "aq_quantize_ex",
     "aq_matmul_variant", "aq_matmul_host", "aq_select", "aq_describe", "aq_stats", "aq_device_error",
     "aq_free", "aq_status_string", "aq_variant_name", "aq_version", "lib_path", "load",
 ]
@@ -64,6 +65,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "aq_pack": ([p, i64, i64, i32, p, p], i32),
         "aq_quantize": ([p, i64, i64, i32, p, p, p, p], i32),
         "aq_matmul_multi": ([i32, p, i32, p, p, p, p, i64, i64, i32, p, p], i32),
+        "aq_matmul_ex": ([i32, p, p, p, p, i64, i64, i64, i32, i32, p, p], i32),
+        "aq_quantize_ex": ([i32, p, i64, i64, i32, i32, p, p, p, p], i32),
         "aq_matmul_gate_up": ([i32, p, p, p, p, p, p, p, i64, i64, i64, i32, p, p], i32),
         "aq_quantize_bf16": ([p, i64, i64, i32, p, p, p, p], i32),
         "aq_matmul": ([p, p, p, p, i64, i64, i64, i32, p, p], i32),
@@ -183,6 +186,34 @@ def aq_matmul(x, Wq, scales, biases, bits, out=None, stream=None) -> torch.Tenso
 def aq_matmul_bf16(x, Wq, scales, biases, bits, out=None, stream=None) -> torch.Tensor:
     """y = x . dequant(W)^T for bf16 x [..., K]; returns bf16 [..., N]."""
     return _mm(AQ_VARIANT_AUTO, AQ_BF16, x, Wq, scales, biases, bits, out, stream)
+
+
+def aq_matmul_ex(x, Wq, scales, biases, bits, group_size, out=None, stream=None):
+    """Any code width of 2/3/4/5/6/8 bits and group size of 32/64/128; the
+    dtype follows x (fp16 or bf16)."""
+    dtype = AQ_BF16 if x.dtype == torch.bfloat16 else AQ_F16
+    K = x.shape[-1]
+    M = x.numel() // K if K else 0
+    N = scales.shape[0]
+    if out is None:
+        out = torch.empty((*x.shape[:-1], N), dtype=x.dtype, device=x.device)
+    _check(load().aq_matmul_ex(dtype, _dev(x, "x"), _dev(Wq, "Wq"), _dev(scales, "scales"),
+                               _dev(biases, "biases"), M, N, K, bits, group_size,
+                               _dev(out, "out"), _stream(stream)), "aq_matmul_ex")
+    return out
+
+
+def aq_quantize_ex(w: torch.Tensor, bits: int, group_size: int, stream=None) -> tuple:
+    """aq_quantize for any code width and group size; w fp16 or bf16 [N, K]."""
+    dtype = AQ_BF16 if w.dtype == torch.bfloat16 else AQ_F16
+    N, K = w.shape
+    Wq = torch.empty((N, K * bits // 32), dtype=torch.int32, device=w.device)
+    scales = torch.empty((N, K // group_size), dtype=torch.float16, device=w.device)
+    biases = torch.empty((N, K // group_size), dtype=torch.float16, device=w.device)
+    _check(load().aq_quantize_ex(dtype, _dev(w, "w"), N, K, bits, group_size, _dev(Wq, "Wq"),
+                                 _dev(scales, "scales"), _dev(biases, "biases"), _stream(stream)),
+           "aq_quantize_ex")
+    return Wq, scales, biases
 
 
 def aq_matmul_multi(x, weights, bits, outs=None, stream=None) -> list:

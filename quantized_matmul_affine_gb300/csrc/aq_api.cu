@@ -200,9 +200,13 @@ using namespace aq;
 
 extern "C" {
 
+static bool valid_width(int bits) {
+    return bits == 2 || bits == 3 || bits == 4 || bits == 5 || bits == 6 || bits == 8;
+}
+
 aq_status aq_pack(const uint8_t *codes_dev, int64_t N, int64_t K, int bits, uint32_t *words_dev,
                   void *stream) {
-    if (N < 0 || K < 0 || K % 64 != 0 || (bits != 3 && bits != 4)) return AQ_ERR_INVALID_ARG;
+    if (N < 0 || K < 0 || K % 32 != 0 || !valid_width(bits)) return AQ_ERR_INVALID_ARG;
     if (N == 0 || K == 0) return AQ_OK;
     if (!codes_dev || !words_dev) return AQ_ERR_INVALID_ARG;
     if (!aligned(words_dev, 4)) return AQ_ERR_MISALIGNED;
@@ -223,6 +227,26 @@ static aq_status quantize_entry(int dtype, const void *w_dev, int64_t N, int64_t
         return AQ_ERR_MISALIGNED;
     if (quantize_launch(dtype, w_dev, N, K, bits, Wq_dev, scales_dev, biases_dev,
                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return AQ_ERR_CUDA;
+    return AQ_OK;
+}
+
+aq_status aq_quantize_ex(int dtype, const void *w_dev, int64_t N, int64_t K, int bits,
+                         int group_size, uint32_t *Wq_dev, void *scales_dev, void *biases_dev,
+                         void *stream) {
+    if (dtype != AQ_F16 && dtype != AQ_BF16) return AQ_ERR_INVALID_ARG;
+    if (bits == 3 || bits == 4)
+        if (group_size == 64)
+            return quantize_entry(dtype, w_dev, N, K, bits, Wq_dev, scales_dev, biases_dev, stream);
+    if (group_size != 32 && group_size != 64 && group_size != 128) return AQ_ERR_INVALID_ARG;
+    if (N < 0 || K < 0 || K % group_size != 0 || !valid_width(bits)) return AQ_ERR_INVALID_ARG;
+    if (N == 0 || K == 0) return AQ_OK;
+    if (!w_dev || !Wq_dev || !scales_dev || !biases_dev) return AQ_ERR_INVALID_ARG;
+    if (!aligned(w_dev, 2) || !aligned(Wq_dev, 4) || !aligned(scales_dev, 2) ||
+        !aligned(biases_dev, 2))
+        return AQ_ERR_MISALIGNED;
+    if (quantize_launch_g(dtype, w_dev, N, K, bits, group_size, Wq_dev, scales_dev, biases_dev,
+                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return AQ_ERR_CUDA;
     return AQ_OK;
 }
@@ -249,6 +273,26 @@ aq_status aq_matmul_bf16(const void *x_dev, const uint32_t *Wq_dev, const void *
                          void *out_dev, void *stream) {
     return run(AQ_VARIANT_AUTO, make_args(AQ_BF16, x_dev, Wq_dev, scales_dev, biases_dev, M, N, K,
                                           bits, out_dev, stream));
+}
+
+aq_status aq_matmul_ex(int dtype, const void *x_dev, const uint32_t *Wq_dev,
+                       const void *scales_dev, const void *biases_dev, int64_t M, int64_t N,
+                       int64_t K, int bits, int group_size, void *out_dev, void *stream) {
+    if (dtype != AQ_F16 && dtype != AQ_BF16) return AQ_ERR_INVALID_ARG;
+    MatmulArgs a = make_args(dtype, x_dev, Wq_dev, scales_dev, biases_dev, M, N, K, bits, out_dev,
+                             stream);
+    if ((bits == 3 || bits == 4) && group_size == 64) return run(AQ_VARIANT_AUTO, a);
+    if (group_size != 32 && group_size != 64 && group_size != 128) return AQ_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < group_size || K % group_size != 0 || !valid_width(bits))
+        return AQ_ERR_INVALID_ARG;
+    if (!x_dev || !Wq_dev || !scales_dev || !biases_dev || !out_dev) return AQ_ERR_INVALID_ARG;
+    if (!aligned(x_dev, 2) || !aligned(Wq_dev, 4) || !aligned(scales_dev, 2) ||
+        !aligned(biases_dev, 2) || !aligned(out_dev, 2))
+        return AQ_ERR_MISALIGNED;
+    if (!generic_supported_g(a, group_size)) return AQ_ERR_UNSUPPORTED;
+    if (generic_launch_g(a, group_size) != cudaSuccess) return AQ_ERR_CUDA;
+    g_calls[AQ_VARIANT_GENERIC].fetch_add(1, std::memory_order_relaxed);
+    return AQ_OK;
 }
 
 aq_status aq_matmul_multi(int dtype, const void *x_dev, int nproj, const uint32_t *const *Wq_dev,

@@ -1,4 +1,5 @@
-// Generic kernel: any K % 64 == 0, any N, any M, pointers aligned only to
+// Generic kernel: any K % 64 == 0 (any multiple of the group size for the
+// other code widths and group sizes), any N, any M, pointers aligned only to
 // their element size.  It serves the shapes and alignments the fast kernels
 // do not take, and is deliberately plain: one warp per (output column n,
 // block of up to 8 activation rows); lane l walks k = l, l+32, ...;
@@ -38,20 +39,20 @@ template <int B, typename T>
 __global__ void __launch_bounds__(kGenericWarps * 32)
     generic_kernel(const T *__restrict__ x, const uint32_t *__restrict__ Wq,
                    const __half *__restrict__ scales, const __half *__restrict__ biases, int64_t M,
-                   int64_t N, int64_t K, T *__restrict__ y) {
+                   int64_t N, int64_t K, int gshift, T *__restrict__ y) {
     const int lane = threadIdx.x & 31;
     const int64_t n = (int64_t)blockIdx.x * kGenericWarps + (threadIdx.x >> 5);
     const int64_t m0 = (int64_t)blockIdx.y * kGenericRows;
     if (n >= N) return;
     const int64_t wpr = K * B / 32;
-    const int64_t G = K / 64;
+    const int64_t G = K >> gshift;  // groups of 2^gshift values
     const uint32_t *row = Wq + n * wpr;
     const int rows = (int)((M - m0) < kGenericRows ? (M - m0) : kGenericRows);
     float acc[kGenericRows];
 #pragma unroll
     for (int r = 0; r < kGenericRows; ++r) acc[r] = 0.f;
     for (int64_t k = lane; k < K; k += 32) {
-        const int64_t g = k >> 6;
+        const int64_t g = k >> gshift;
         const int64_t bit = k * B;
         const int64_t wi = bit >> 5;
         const int off = (int)(bit & 31);
@@ -83,25 +84,41 @@ bool generic_supported(const MatmulArgs &a) {
            (a.M + kGenericRows - 1) / kGenericRows <= 65535;
 }
 
+bool generic_supported_g(const MatmulArgs &a, int group) {
+    const bool width = a.bits == 2 || a.bits == 3 || a.bits == 4 || a.bits == 5 || a.bits == 6 ||
+                       a.bits == 8;
+    const bool grp = group == 32 || group == 64 || group == 128;
+    return a.M >= 1 && a.N >= 1 && width && grp && a.K >= group && a.K % group == 0 &&
+           (a.M + kGenericRows - 1) / kGenericRows <= 65535;
+}
+
 template <typename T>
-static cudaError_t launch_t(const MatmulArgs &a) {
+static cudaError_t launch_t(const MatmulArgs &a, int group) {
     dim3 grid((unsigned)((a.N + kGenericWarps - 1) / kGenericWarps),
               (unsigned)((a.M + kGenericRows - 1) / kGenericRows));
     const T *x = static_cast<const T *>(a.x);
     const __half *s = static_cast<const __half *>(a.scales);
     const __half *b = static_cast<const __half *>(a.biases);
     T *y = static_cast<T *>(a.out);
-    if (a.bits == 3)
-        generic_kernel<3, T><<<grid, kGenericWarps * 32, 0, a.stream>>>(x, a.Wq, s, b, a.M, a.N,
-                                                                         a.K, y);
-    else
-        generic_kernel<4, T><<<grid, kGenericWarps * 32, 0, a.stream>>>(x, a.Wq, s, b, a.M, a.N,
-                                                                         a.K, y);
+    const int gs = group == 32 ? 5 : group == 64 ? 6 : 7;
+    const unsigned th = kGenericWarps * 32;
+    switch (a.bits) {
+        case 2: generic_kernel<2, T><<<grid, th, 0, a.stream>>>(x, a.Wq, s, b, a.M, a.N, a.K, gs, y); break;
+        case 3: generic_kernel<3, T><<<grid, th, 0, a.stream>>>(x, a.Wq, s, b, a.M, a.N, a.K, gs, y); break;
+        case 4: generic_kernel<4, T><<<grid, th, 0, a.stream>>>(x, a.Wq, s, b, a.M, a.N, a.K, gs, y); break;
+        case 5: generic_kernel<5, T><<<grid, th, 0, a.stream>>>(x, a.Wq, s, b, a.M, a.N, a.K, gs, y); break;
+        case 6: generic_kernel<6, T><<<grid, th, 0, a.stream>>>(x, a.Wq, s, b, a.M, a.N, a.K, gs, y); break;
+        default: generic_kernel<8, T><<<grid, th, 0, a.stream>>>(x, a.Wq, s, b, a.M, a.N, a.K, gs, y); break;
+    }
     return cudaGetLastError();
 }
 
 cudaError_t generic_launch(const MatmulArgs &a) {
-    return a.dtype == AQ_BF16 ? launch_t<__nv_bfloat16>(a) : launch_t<__half>(a);
+    return a.dtype == AQ_BF16 ? launch_t<__nv_bfloat16>(a, 64) : launch_t<__half>(a, 64);
+}
+
+cudaError_t generic_launch_g(const MatmulArgs &a, int group) {
+    return a.dtype == AQ_BF16 ? launch_t<__nv_bfloat16>(a, group) : launch_t<__half>(a, group);
 }
 
 }  // namespace aq

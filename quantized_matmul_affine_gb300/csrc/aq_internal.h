@@ -74,6 +74,10 @@ int tc_describe(const MatmulArgs &a, char *buf, int len);
 
 cudaError_t quantize_launch(int dtype, const void *w, int64_t N, int64_t K, int bits,
                             uint32_t *words, void *scales, void *biases, cudaStream_t stream);
+cudaError_t quantize_launch_g(int dtype, const void *w, int64_t N, int64_t K, int bits, int group,
+                              uint32_t *words, void *scales, void *biases, cudaStream_t stream);
+bool generic_supported_g(const MatmulArgs &a, int group);
+cudaError_t generic_launch_g(const MatmulArgs &a, int group);
 cudaError_t pack_launch(const uint8_t *codes, int64_t N, int64_t K, int bits, uint32_t *words,
                         cudaStream_t stream);
 

@@ -6,8 +6,9 @@
 // stream; stream bit i is bit i%32 of uint32 word i/32.  A 64-value group is
 // exactly 2*B words, so a row is K*B/32 words.
 //
-// One thread builds one output word from the (at most 12) codes that touch
-// it, so every word is written exactly once and no atomics are needed.
+// One thread builds one output word from the (at most 17, at 2 bits) codes
+// that touch it, so every word is written exactly once and no atomics are
+// needed.  Any width of 2, 3, 4, 5, 6 or 8 bits.
 #include "aq_internal.h"
 
 namespace aq {
@@ -47,10 +48,14 @@ cudaError_t pack_launch(const uint8_t *codes, int64_t N, int64_t K, int bits, ui
     int64_t blocks = (total + threads - 1) / threads;
     const int64_t cap = (int64_t)num_sms() * 16;
     if (blocks > cap) blocks = cap;
-    if (bits == 3)
-        pack_kernel<3><<<(unsigned)blocks, threads, 0, stream>>>(codes, N, K, words);
-    else
-        pack_kernel<4><<<(unsigned)blocks, threads, 0, stream>>>(codes, N, K, words);
+    switch (bits) {
+        case 2: pack_kernel<2><<<(unsigned)blocks, threads, 0, stream>>>(codes, N, K, words); break;
+        case 3: pack_kernel<3><<<(unsigned)blocks, threads, 0, stream>>>(codes, N, K, words); break;
+        case 4: pack_kernel<4><<<(unsigned)blocks, threads, 0, stream>>>(codes, N, K, words); break;
+        case 5: pack_kernel<5><<<(unsigned)blocks, threads, 0, stream>>>(codes, N, K, words); break;
+        case 6: pack_kernel<6><<<(unsigned)blocks, threads, 0, stream>>>(codes, N, K, words); break;
+        default: pack_kernel<8><<<(unsigned)blocks, threads, 0, stream>>>(codes, N, K, words); break;
+    }
     return cudaGetLastError();
 }
 

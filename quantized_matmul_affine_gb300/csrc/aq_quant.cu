@@ -122,7 +122,105 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint4 *__restrict__
     }
 }
 
+// Other widths and group sizes: one warp per group of 32, 64 or 128 values
+// (1, 2 or 4 per lane), min/max over the warp, the codes decided with the
+// IEEE quotient itself and rint (ties to even), packed through a per-warp
+// shared-memory word buffer (a group is group*B/32 words).
+template <int B, bool BF16, int VPL>
+__global__ void __launch_bounds__(256) quantize_g_kernel(const uint16_t *__restrict__ w,
+                                                         int64_t groups,
+                                                         uint32_t *__restrict__ words,
+                                                         __half *__restrict__ scales,
+                                                         __half *__restrict__ biases) {
+    constexpr int kQmax = (1 << B) - 1;
+    constexpr int kGroup = 32 * VPL;
+    constexpr int kWords = kGroup * B / 32;
+    __shared__ uint32_t buf[8][kWords];
+    const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
+    const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t gid = warp; gid < groups; gid += nwarps) {
+        float f[VPL];
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const uint16_t h = w[gid * kGroup + lane * VPL + i];
+            f[i] = BF16 ? __uint_as_float((uint32_t)h << 16)
+                        : __half2float(__ushort_as_half(h));
+        }
+        float lo = f[0], hi = f[0];
+#pragma unroll
+        for (int i = 1; i < VPL; ++i) {
+            lo = fminf(lo, f[i]);
+            hi = fmaxf(hi, f[i]);
+        }
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+            hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        }
+        const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), (float)kQmax));
+        const __half b16 = __float2half_rn(lo);
+        const float s = __half2float(s16), b = __half2float(b16);
+        for (int i = lane; i < kWords; i += 32) buf[wl][i] = 0u;
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            uint32_t q = 0;
+            if (s != 0.f)
+                q = (uint32_t)min(max(__float2int_rn(__fdiv_rn(__fsub_rn(f[i], b), s)), 0), kQmax);
+            const int bit = (lane * VPL + i) * B;
+            atomicOr(&buf[wl][bit >> 5], q << (bit & 31));
+            if ((bit & 31) + B > 32) atomicOr(&buf[wl][(bit >> 5) + 1], q >> (32 - (bit & 31)));
+        }
+        __syncwarp();
+        for (int i = lane; i < kWords; i += 32) words[gid * kWords + i] = buf[wl][i];
+        if (lane == 0) {
+            scales[gid] = s16;
+            biases[gid] = b16;
+        }
+        __syncwarp();
+    }
+}
+
+template <int B, bool BF16>
+cudaError_t quantize_g_group(int group, const uint16_t *w, int64_t groups, uint32_t *words,
+                             __half *s, __half *b, cudaStream_t stream) {
+    int64_t blocks = (groups + 7) / 8;
+    const int64_t cap = (int64_t)num_sms() * 8;
+    if (blocks > cap) blocks = cap;
+    if (group == 32)
+        quantize_g_kernel<B, BF16, 1><<<(unsigned)blocks, 256, 0, stream>>>(w, groups, words, s, b);
+    else if (group == 64)
+        quantize_g_kernel<B, BF16, 2><<<(unsigned)blocks, 256, 0, stream>>>(w, groups, words, s, b);
+    else
+        quantize_g_kernel<B, BF16, 4><<<(unsigned)blocks, 256, 0, stream>>>(w, groups, words, s, b);
+    return cudaGetLastError();
+}
+
+template <bool BF16>
+cudaError_t quantize_g_bits(int bits, int group, const uint16_t *w, int64_t groups,
+                            uint32_t *words, __half *s, __half *b, cudaStream_t stream) {
+    switch (bits) {
+        case 2: return quantize_g_group<2, BF16>(group, w, groups, words, s, b, stream);
+        case 3: return quantize_g_group<3, BF16>(group, w, groups, words, s, b, stream);
+        case 4: return quantize_g_group<4, BF16>(group, w, groups, words, s, b, stream);
+        case 5: return quantize_g_group<5, BF16>(group, w, groups, words, s, b, stream);
+        case 6: return quantize_g_group<6, BF16>(group, w, groups, words, s, b, stream);
+        default: return quantize_g_group<8, BF16>(group, w, groups, words, s, b, stream);
+    }
+}
+
 }  // namespace
+
+cudaError_t quantize_launch_g(int dtype, const void *w, int64_t N, int64_t K, int bits, int group,
+                              uint32_t *words, void *scales, void *biases, cudaStream_t stream) {
+    const int64_t groups = N * (K / group);
+    if (groups == 0) return cudaSuccess;
+    const uint16_t *wp = static_cast<const uint16_t *>(w);
+    __half *sp = static_cast<__half *>(scales), *bp = static_cast<__half *>(biases);
+    return dtype == AQ_BF16 ? quantize_g_bits<true>(bits, group, wp, groups, words, sp, bp, stream)
+                            : quantize_g_bits<false>(bits, group, wp, groups, words, sp, bp, stream);
+}
 
 cudaError_t quantize_launch(int dtype, const void *w, int64_t N, int64_t K, int bits,
                             uint32_t *words, void *scales, void *biases, cudaStream_t stream) {

@@ -84,7 +84,8 @@ def test_pack_validation():
     assert lib.aq_pack(A, 0, 512, 4, A, None) == 0       # empty: nothing to do
     assert lib.aq_pack(A, 4, 0, 4, A, None) == 0
     assert lib.aq_pack(A, 4, 100, 4, A, None) == 1
-    assert lib.aq_pack(A, 4, 64, 6, A, None) == 1
+    assert lib.aq_pack(A, 4, 64, 7, A, None) == 1        # width outside 2, 3, 4, 5, 6, 8
+    assert lib.aq_pack(A, 4, 48, 4, A, None) == 1        # K % 32 != 0
     assert lib.aq_pack(None, 4, 64, 4, A, None) == 1
     assert lib.aq_pack(A, 4, 64, 4, A + 2, None) == 3
 
