@@ -8,8 +8,9 @@ total exceeds twice the L2 size (every call reads its weights from HBM).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload decode|small|split3:I|layer:I|prefill:I|quantize:I|
-                                layerstep:I] [--all]
+                                layerstep:I|widths:I] [--all]
 
+widths:I times aq_matmul_ex on other code widths and group sizes.
 layerstep:I times one decoder-layer step (seven projections; I = 0/1 fused or
 not at M = 1, 2/3 at M = 8).  quantize:I times the float -> affine quantiser (aq_quantize) on the weight
 shapes of workloads.QUANTIZE_WORKLOADS instead of the matmul.
@@ -624,6 +625,115 @@ def run_layer_step(args, rank, world, local_rank):
     }
 
 
+WIDTHS_METRIC = ("µs/call and effective HBM GB/s (fraction of roofline), other code widths and "
+                 "group sizes, y=x·Wᵀ")
+# name -> list of (bits, group, N, K, M, x dtype)
+WIDTH_WORKLOADS = {"widths": [(8, 64, 4096, 4096, 1, "bf16"), (2, 32, 4096, 4096, 1, "bf16"),
+                              (6, 128, 4096, 4096, 1, "bf16"), (4, 128, 4096, 4096, 1, "bf16"),
+                              (8, 32, 4096, 4096, 16, "fp16")]}
+
+
+def run_widths(args, rank, world, local_rank):
+    """aq_matmul_ex on a width / group size other than the 3/4-bit group-64
+    format: device-timed calls over rotating weight copies (> 2x L2) and the
+    same through host buffers."""
+    import torch
+    import quantized_matmul_affine_gb300 as aq
+
+    torch.cuda.set_device(local_rank)
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    name, idx = parse_workload(args.workload)
+    bits, group, N, K, M, dt = WIDTH_WORKLOADS[name][idx]
+    rng = np.random.default_rng(60 + idx)
+    G = K // group
+    codes = rng.integers(0, 1 << bits, size=(N, K), dtype=np.uint8)
+    s = (np.abs(rng.standard_normal((N, G))) * (0.16 / (1 << bits)) + 1e-3).astype(np.float16)
+    b = (-(1 << (bits - 1)) * s.astype(np.float64)).astype(np.float16)
+    xb = workloads.make_x(M, K, dt, seed=61)
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float16
+    x = torch.from_numpy(xb.view(np.int16)).cuda().view(tdt)
+    Wq0 = aq.aq_pack(torch.from_numpy(codes).cuda(), bits)
+    s0, b0 = torch.from_numpy(s).cuda(), torch.from_numpy(b).cuda()
+    l2 = getattr(props, "L2_cache_size", 126 * 1024 * 1024)
+    wbytes = N * K * bits // 8 + 4 * N * G
+    copies = max(2, -(-2 * l2 // wbytes) + 1)
+    ws = [(Wq0.clone(), s0.clone(), b0.clone()) for _ in range(copies)]
+    ys = [torch.empty((M, N), dtype=tdt, device="cuda") for _ in range(copies)]
+    stream = torch.cuda.Stream()
+    steps = max(1, min(args.steps, 4096))
+    chunk = min(256, steps)
+    with torch.cuda.stream(stream):
+        aq.aq_matmul_ex(x, *ws[0], bits, group, out=ys[0], stream=stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(chunk):
+                c = i % copies
+                aq.aq_matmul_ex(x, *ws[c], bits, group, out=ys[c], stream=stream)
+        for _ in range(max(1, args.warmup // chunk)):
+            g.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(str(props.uuid) if hasattr(props, "uuid") else "0")
+    if not str(sampler.gpu_id).startswith("GPU-"):
+        sampler.gpu_id = "GPU-" + str(sampler.gpu_id)
+    sampler.start()
+    time.sleep(0.5)
+    reps = max(1, steps // chunk)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.mark()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark()
+    clocks = sampler.stop()
+    us = reduce_max(ev0.elapsed_time(ev1) * 1e3 / (reps * chunk), "cuda")
+    x_host = torch.from_numpy(xb.view(np.int16)).view(tdt).pin_memory()
+    y_host = torch.empty((M, N), dtype=tdt).pin_memory()
+    x_dev = torch.empty_like(x)
+    n_e2e = 200
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(n_e2e):
+            x_dev.copy_(x_host, non_blocking=True)
+            aq.aq_matmul_ex(x_dev, *ws[i % copies], bits, group, out=ys[0], stream=stream)
+            y_host.copy_(ys[0], non_blocking=True)
+            stream.synchronize()
+    e2e_us = reduce_max((time.perf_counter() - t0) * 1e6 / n_e2e, "cuda")
+    hbm, _, src = peaks()
+    by = wbytes + 2 * M * K + 2 * M * N
+    achieved = by / (us * 1e-6) / 1e9
+    return {
+        "metric": WIDTHS_METRIC,
+        "value": round(whole_job_us_per_call(us, world), 3),
+        "unit": "us/call",
+        "n_gpus": world, "steps": reps * chunk, "warmup": args.warmup,
+        "ms_per_step": us / 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": dt, "data": "synthetic",
+        "config": {"workload": f"{name}[{idx}]: {bits}-bit affine group-{group}, N={N}, K={K}, "
+                               f"M={M}, x {dt}",
+                   "bits": bits, "group": group, "M": M, "N": N, "K": K,
+                   "variant": aq.aq_variant_name(aq.AQ_VARIANT_GENERIC),
+                   "l2": f"cold: {copies} rotating weight copies > 2x L2 ({l2 / 1e6:.0f} MB)",
+                   "timing": f"CUDA events on the launching stream around {reps} replays of a "
+                             f"CUDA graph of {chunk} calls",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm,
+                     "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
+                     "peak_source": f"{src} (MEASURED_PEAKS.json)" if src == "measured"
+                     else "fallback",
+                     "algorithmic_bytes_per_launch": by},
+        "e2e": {"value": round(whole_job_us_per_call(e2e_us, world), 3), "unit": "us/call",
+                "h2d_bytes_per_step": 2 * M * K, "d2h_bytes_per_step": 2 * M * N,
+                "path": "pinned x -> device, aq_matmul_ex, y -> pinned host, sync"},
+        "gpu_launches": reps * chunk,
+        "clocks": clocks,
+    }
+
+
 def cpu_sample_time(p, budget_s, threads):
     """Time the oracle on a column sample of p; returns (us per full call, desc)."""
     import oracle
@@ -736,6 +846,11 @@ def main():
         specs = [f"{n}:{i}" for n, c in workloads.WORKLOADS.items() for i in range(len(c))]
     for spec in specs:
         args.workload = spec
+        if parse_workload(spec)[0] in WIDTH_WORKLOADS:
+            line = run_widths(args, rank, world, local_rank)
+            if rank == 0:
+                print(json.dumps(line), flush=True)
+            continue
         if parse_workload(spec)[0] in LAYER_STEPS:
             line = run_layer_step(args, rank, world, local_rank)
             if rank == 0:

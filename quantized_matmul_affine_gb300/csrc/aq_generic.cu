@@ -51,19 +51,37 @@ __global__ void __launch_bounds__(kGenericWarps * 32)
     float acc[kGenericRows];
 #pragma unroll
     for (int r = 0; r < kGenericRows; ++r) acc[r] = 0.f;
-    for (int64_t k = lane; k < K; k += 32) {
-        const int64_t g = k >> gshift;
-        const int64_t bit = k * B;
-        const int64_t wi = bit >> 5;
-        const int off = (int)(bit & 31);
-        uint32_t q = row[wi] >> off;
-        if (off + B > 32) q |= row[wi + 1] << (32 - off);
-        q &= (1u << B) - 1u;
-        const float w = fmaf(__half2float(scales[n * G + g]), (float)q,
-                             __half2float(biases[n * G + g]));
+    // four k per lane per step (k = lane + 32 j, j = 4i..4i+3): the loads of
+    // a step are independent and in flight together
+    constexpr int kU = 4;
+    for (int64_t k0 = lane; k0 < K; k0 += 32 * kU) {
+        float w[kU];
 #pragma unroll
-        for (int r = 0; r < kGenericRows; ++r)
-            if (r < rows) acc[r] = fmaf(w, to_f32<T>(x[(m0 + r) * K + k]), acc[r]);
+        for (int u = 0; u < kU; ++u) {
+            const int64_t k = k0 + 32 * u;
+            w[u] = 0.f;
+            if (k < K) {
+                const int64_t g = k >> gshift;
+                const int64_t bit = k * B;
+                const int64_t wi = bit >> 5;
+                const int off = (int)(bit & 31);
+                uint32_t q = row[wi] >> off;
+                if (off + B > 32) q |= row[wi + 1] << (32 - off);
+                q &= (1u << B) - 1u;
+                w[u] = fmaf(__half2float(scales[n * G + g]), (float)q,
+                            __half2float(biases[n * G + g]));
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kGenericRows; ++r) {
+            if (r < rows) {
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int64_t k = k0 + 32 * u;
+                    if (k < K) acc[r] = fmaf(w[u], to_f32<T>(x[(m0 + r) * K + k]), acc[r]);
+                }
+            }
+        }
     }
 #pragma unroll
     for (int r = 0; r < kGenericRows; ++r) {
