@@ -69,6 +69,8 @@ def _load() -> ctypes.CDLL:
             lib.oracle_dequant_g.argtypes = [p, p, p, i64, i64, i32, i32, p]
             lib.oracle_matmul_g.argtypes = [p, p, p, p, i64, i64, i64, i32, i32, p, p, i32]
             lib.oracle_quantize_g.argtypes = [p, i64, i64, i32, i32, p, p, p]
+            lib.oracle_attention.argtypes = [p, p, p, p, p, p, p, i64, i64, i64, i64, i32, i32,
+                                             p, p, p]
             lib.oracle_f32_to_f16.argtypes = [ctypes.c_float]
             lib.oracle_f32_to_f16.restype = ctypes.c_uint16
             lib.oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
@@ -76,7 +78,7 @@ def _load() -> ctypes.CDLL:
             for f in ("oracle_pack", "oracle_unpack", "oracle_dequant", "oracle_matmul",
                       "oracle_matmul_cols", "oracle_matmul_threads", "oracle_quantize",
                       "oracle_pack_g", "oracle_unpack_g", "oracle_dequant_g", "oracle_matmul_g",
-                      "oracle_quantize_g"):
+                      "oracle_quantize_g", "oracle_attention"):
                 getattr(lib, f).restype = i32
             _lib = lib
     return _lib
@@ -265,3 +267,27 @@ def quantize_g(w: np.ndarray, bits: int, group: int):
     _check(_load().oracle_quantize_g(_ptr(w), N, K, bits, group, _ptr(codes), _ptr(sb), _ptr(bb)),
            "quantize_g")
     return codes, sb, bb
+
+
+# ---------------------------------------------------------------------------
+# Decode attention over a quantised KV cache
+# ---------------------------------------------------------------------------
+
+def attention(q, kwords, kscales, kbiases, vwords, vscales, vbiases, KV: int, N: int,
+              bits: int, group: int):
+    """o = softmax(q . Kd^T) . Vd per query head (grouped-query: head h reads
+    KV head h / (H/KV)).  q float64 [H, D]; K/V words uint32 [KV*N, D*bits/32],
+    scales/biases [KV*N, D/group].  Returns (o [H, D], smag [H, N], vmag [H, D])
+    with smag = sum_d |q*k| and vmag = sum_n p*|v| (for the tolerance)."""
+    q = _f64(q)
+    H, D = q.shape
+    kw = np.ascontiguousarray(kwords, dtype=np.uint32)
+    vw = np.ascontiguousarray(vwords, dtype=np.uint32)
+    ks, kb, vs, vb = _f64(kscales), _f64(kbiases), _f64(vscales), _f64(vbiases)
+    o = np.zeros((H, D), np.float64)
+    smag = np.zeros((H, N), np.float64)
+    vmag = np.zeros((H, D), np.float64)
+    _check(_load().oracle_attention(_ptr(q), _ptr(kw), _ptr(ks), _ptr(kb), _ptr(vw), _ptr(vs),
+                                    _ptr(vb), H, KV, N, D, bits, group, _ptr(o), _ptr(smag),
+                                    _ptr(vmag)), "attention")
+    return o, smag, vmag

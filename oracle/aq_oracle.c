@@ -353,3 +353,69 @@ int oracle_quantize(const float *w, int64_t N, int64_t K, int bits, uint8_t *cod
     if (!valid_shape(N, K, bits)) return 1;
     return oracle_quantize_g(w, N, K, bits, ORACLE_GROUP, codes, scale_bits, bias_bits);
 }
+
+/* ------------------------------------------------------------------------
+ * Decode attention over a quantised KV cache (one query row per head):
+ *
+ *   s[h][n] = sum_d q[h][d] * Kd[kv][n][d],   kv = h / (H / KV)
+ *   p[h][n] = exp(s[h][n] - max_n s[h][n]) / sum_n exp(...)
+ *   o[h][d] = sum_n p[h][n] * Vd[kv][n][d]
+ *
+ * with Kd, Vd the caches dequantised as scale * q + bias per group of
+ * `group` values along d (rows [KV][N], D values each, packed as the weight
+ * format: K*B/32 words per row, LSB-first).  This is the operator of the
+ * pages' fused decode kernel (fused-decode-kernel.ts: L = 1, quantised K
+ * and V, grouped-query heads), taken as its plain definition in fp64; the
+ * query is used as given (any 1/sqrt(D) is the caller's).  Also returned,
+ * for the tolerance: smag[h][n] = sum_d |q*Kd| and vmag[h][d] =
+ * sum_n p * |Vd|.
+ * ------------------------------------------------------------------------ */
+int oracle_attention(const double *q, const uint32_t *kw, const double *ks, const double *kb,
+                     const uint32_t *vw, const double *vs, const double *vb, int64_t H,
+                     int64_t KV, int64_t N, int64_t D, int bits, int group, double *o,
+                     double *smag, double *vmag) {
+    if (H < 1 || KV < 1 || H % KV != 0 || N < 1 || !valid_shape_g(KV * N, D, bits, group))
+        return 1;
+    const int64_t wpr = oracle_words_per_row(D, bits);
+    const int64_t G = D / group;
+    double *s = (double *)malloc((size_t)N * sizeof(double));
+    if (!s) return 1;
+    for (int64_t h = 0; h < H; ++h) {
+        const int64_t kv = h / (H / KV);
+        const double *qh = q + h * D;
+        double mx = -INFINITY;
+        for (int64_t n = 0; n < N; ++n) {
+            const int64_t r = kv * N + n;
+            double acc = 0.0, mag = 0.0;
+            for (int64_t d = 0; d < D; ++d) {
+                const double kd = ks[r * G + d / group] * (double)oracle_code(kw + r * wpr, d, bits) +
+                                  kb[r * G + d / group];
+                acc += qh[d] * kd;
+                mag += fabs(qh[d] * kd);
+            }
+            s[n] = acc;
+            if (smag) smag[h * N + n] = mag;
+            if (acc > mx) mx = acc;
+        }
+        double den = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            s[n] = exp(s[n] - mx);
+            den += s[n];
+        }
+        for (int64_t d = 0; d < D; ++d) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                const int64_t r = kv * N + n;
+                const double vd = vs[r * G + d / group] * (double)oracle_code(vw + r * wpr, d, bits) +
+                                  vb[r * G + d / group];
+                const double p = s[n] / den;
+                acc += p * vd;
+                mag += p * fabs(vd);
+            }
+            o[h * D + d] = acc;
+            if (vmag) vmag[h * D + d] = mag;
+        }
+    }
+    free(s);
+    return 0;
+}
