@@ -163,6 +163,36 @@ aq_status aq_quantize_ex(int dtype, const void *w_dev, int64_t N, int64_t K, int
                          int group_size, uint32_t *Wq_dev, void *scales_dev, void *biases_dev,
                          void *stream);
 
+/*
+ * aq_attention_decode — decode attention over a quantised KV cache, one
+ * query row per head (grouped-query):
+ *   o[h] = softmax(q[h] . Kd[kv]^T) . Vd[kv],   kv = h / (H / KV),
+ * Kd, Vd the caches dequantised as scale * code + bias per group of
+ * group_size values along the head dimension.  This is the operator of the
+ * pages' fused decode kernel (fused-decode-kernel.ts); the query is used as
+ * given (a 1/sqrt(D) factor, if wanted, is folded into q by the caller).
+ *   dtype         AQ_F16 or AQ_BF16: the type of q and o.
+ *   q_dev         [H][D], device.
+ *   k_words_dev   uint32 [KV][N][D*bits/32], device, 16-byte aligned: row
+ *                 (kv, n) packed as aq_pack packs a weight row.
+ *   k_scales_dev, k_biases_dev  fp16 [KV][N][D/group_size], device.
+ *   v_words_dev, v_scales_dev, v_biases_dev  the same for V.
+ *   out_dev       o [H][D], device, caller-allocated.
+ * Served: bits 4 or 8, group_size 32/64/128 (D % group_size == 0,
+ * group_size >= D/32), D in {64, 128, 256}, H/KV in {1, 2, 4, 8}, any
+ * N >= 1.  Scores and probabilities are fp32; o is rounded once.  The rows
+ * of a KV head are split over the CTAs of one thread-block cluster and
+ * merged in rank order (deterministic); the library allocates nothing.
+ * Errors: AQ_ERR_INVALID_ARG for bad sizes, widths, group sizes or NULL
+ * pointers; AQ_ERR_MISALIGNED; AQ_ERR_UNSUPPORTED for valid arguments
+ * outside the served set (nothing queued); AQ_ERR_CUDA if the launch fails.
+ */
+aq_status aq_attention_decode(int dtype, const void *q_dev, const uint32_t *k_words_dev,
+                              const void *k_scales_dev, const void *k_biases_dev,
+                              const uint32_t *v_words_dev, const void *v_scales_dev,
+                              const void *v_biases_dev, int64_t H, int64_t KV, int64_t N,
+                              int64_t D, int bits, int group_size, void *out_dev, void *stream);
+
 /* Largest number of projections aq_matmul_multi takes in one call. */
 #define AQ_MAX_PROJ 4
 

@@ -24,7 +24,7 @@ __all__ = [
     "AqError", "AQ_F16", "AQ_BF16", "AQ_VARIANT_AUTO", "AQ_VARIANT_GENERIC", "AQ_VARIANT_QMV",
     "AQ_VARIANT_TC", "AQ_VARIANT_GEMV", "AQ_VARIANT_TCW", "AQ_NUM_VARIANTS", "aq_pack", "aq_quantize",
     "aq_quantize_bf16", "aq_matmul", "aq_matmul_bf16", "aq_matmul_multi", "aq_matmul_gate_up",
-    "aq_matmul_ex", "aq_quantize_ex",
+    "aq_matmul_ex", "aq_quantize_ex", "aq_attention_decode",
     "aq_matmul_variant", "aq_matmul_host", "aq_select", "aq_describe", "aq_stats", "aq_device_error",
     "aq_free", "aq_status_string", "aq_variant_name", "aq_version", "lib_path", "load",
 ]
@@ -66,6 +66,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "aq_quantize": ([p, i64, i64, i32, p, p, p, p], i32),
         "aq_matmul_multi": ([i32, p, i32, p, p, p, p, i64, i64, i32, p, p], i32),
         "aq_matmul_ex": ([i32, p, p, p, p, i64, i64, i64, i32, i32, p, p], i32),
+        "aq_attention_decode": ([i32, p, p, p, p, p, p, p, i64, i64, i64, i64, i32, i32, p, p],
+                                i32),
         "aq_quantize_ex": ([i32, p, i64, i64, i32, i32, p, p, p, p], i32),
         "aq_matmul_gate_up": ([i32, p, p, p, p, p, p, p, i64, i64, i64, i32, p, p], i32),
         "aq_quantize_bf16": ([p, i64, i64, i32, p, p, p, p], i32),
@@ -200,6 +202,23 @@ def aq_matmul_ex(x, Wq, scales, biases, bits, group_size, out=None, stream=None)
     _check(load().aq_matmul_ex(dtype, _dev(x, "x"), _dev(Wq, "Wq"), _dev(scales, "scales"),
                                _dev(biases, "biases"), M, N, K, bits, group_size,
                                _dev(out, "out"), _stream(stream)), "aq_matmul_ex")
+    return out
+
+
+def aq_attention_decode(q, k, v, bits, group_size, out=None, stream=None) -> torch.Tensor:
+    """Decode attention over a quantised KV cache.  q [H, D] (fp16 or bf16);
+    k and v are (words [KV, N, D*bits/32] int32, scales [KV, N, D/group] fp16,
+    biases [KV, N, D/group] fp16).  Returns o [H, D] in q's dtype."""
+    dtype = AQ_BF16 if q.dtype == torch.bfloat16 else AQ_F16
+    H, D = q.shape
+    KV, N = k[0].shape[0], k[0].shape[1]
+    if out is None:
+        out = torch.empty((H, D), dtype=q.dtype, device=q.device)
+    _check(load().aq_attention_decode(dtype, _dev(q, "q"), _dev(k[0], "k_words"),
+                                      _dev(k[1], "k_scales"), _dev(k[2], "k_biases"),
+                                      _dev(v[0], "v_words"), _dev(v[1], "v_scales"),
+                                      _dev(v[2], "v_biases"), H, KV, N, D, bits, group_size,
+                                      _dev(out, "out"), _stream(stream)), "aq_attention_decode")
     return out
 
 

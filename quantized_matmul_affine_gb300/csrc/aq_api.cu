@@ -295,6 +295,31 @@ aq_status aq_matmul_ex(int dtype, const void *x_dev, const uint32_t *Wq_dev,
     return AQ_OK;
 }
 
+aq_status aq_attention_decode(int dtype, const void *q_dev, const uint32_t *k_words_dev,
+                              const void *k_scales_dev, const void *k_biases_dev,
+                              const uint32_t *v_words_dev, const void *v_scales_dev,
+                              const void *v_biases_dev, int64_t H, int64_t KV, int64_t N,
+                              int64_t D, int bits, int group_size, void *out_dev, void *stream) {
+    if (dtype != AQ_F16 && dtype != AQ_BF16) return AQ_ERR_INVALID_ARG;
+    if (!q_dev || !k_words_dev || !k_scales_dev || !k_biases_dev || !v_words_dev ||
+        !v_scales_dev || !v_biases_dev || !out_dev)
+        return AQ_ERR_INVALID_ARG;
+    if (H < 1 || KV < 1 || N < 1 || D < 1 || H % KV != 0) return AQ_ERR_INVALID_ARG;
+    if ((bits != 4 && bits != 8) ||
+        (group_size != 32 && group_size != 64 && group_size != 128) || D % group_size != 0)
+        return AQ_ERR_INVALID_ARG;
+    if (!aligned(q_dev, 2) || !aligned(out_dev, 2) || !aligned(k_words_dev, 16) ||
+        !aligned(v_words_dev, 16) || !aligned(k_scales_dev, 2) || !aligned(k_biases_dev, 2) ||
+        !aligned(v_scales_dev, 2) || !aligned(v_biases_dev, 2))
+        return AQ_ERR_MISALIGNED;
+    if (!attention_supported(H, KV, N, D, bits, group_size)) return AQ_ERR_UNSUPPORTED;
+    if (attention_launch(dtype, q_dev, k_words_dev, k_scales_dev, k_biases_dev, v_words_dev,
+                         v_scales_dev, v_biases_dev, H, KV, N, D, bits, group_size, out_dev,
+                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return AQ_ERR_CUDA;
+    return AQ_OK;
+}
+
 aq_status aq_matmul_multi(int dtype, const void *x_dev, int nproj, const uint32_t *const *Wq_dev,
                           const void *const *scales_dev, const void *const *biases_dev,
                           const int64_t *N, int64_t M, int64_t K, int bits, void *const *out_dev,

@@ -77,6 +77,12 @@ cudaError_t quantize_launch(int dtype, const void *w, int64_t N, int64_t K, int 
 cudaError_t quantize_launch_g(int dtype, const void *w, int64_t N, int64_t K, int bits, int group,
                               uint32_t *words, void *scales, void *biases, cudaStream_t stream);
 bool generic_supported_g(const MatmulArgs &a, int group);
+bool attention_supported(int64_t H, int64_t KV, int64_t N, int64_t D, int bits, int group);
+int attention_cluster(int64_t KV, int64_t N);
+cudaError_t attention_launch(int dtype, const void *q, const uint32_t *kw, const void *ks,
+                             const void *kb, const uint32_t *vw, const void *vs, const void *vb,
+                             int64_t H, int64_t KV, int64_t N, int64_t D, int bits, int group,
+                             void *out, cudaStream_t stream);
 cudaError_t generic_launch_g(const MatmulArgs &a, int group);
 cudaError_t pack_launch(const uint8_t *codes, int64_t N, int64_t K, int bits, uint32_t *words,
                         cudaStream_t stream);

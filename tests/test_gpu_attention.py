@@ -1,0 +1,112 @@
+"""GPU parity of decode attention over a quantised KV cache
+(aq_attention_decode) against the fp64 oracle, through the C ABI.
+
+Tolerance per output element: the GPU keeps scores and probabilities in
+fp32, so a score is off by at most tau = 1e-4 * sum_d |q k| + 1e-5 (two
+orders above fp32 rounding); a softmax weight then moves by a factor within
+exp(+-2 tau), giving |o - o_ref| <= (exp(2 max tau) - 1) * sum_n p |v|, plus
+fp32 accumulation over the rows (2^-24 per row), plus one rounding of o to
+the output type (2^-8 relative bf16, 2^-11 fp16).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+aq = pytest.importorskip("quantized_matmul_affine_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    yield
+
+
+def _cache(rng, KV, N, D, bits, group):
+    R = KV * N
+    codes = rng.integers(0, 1 << bits, size=(R, D)).astype(np.uint8)
+    c = 0.16 / (1 << bits)
+    s = (np.abs(rng.standard_normal((R, D // group))) * c + 1e-3).astype(np.float16)
+    b = (-(1 << (bits - 1)) * s.astype(np.float64) + rng.standard_normal((R, D // group)) * 1e-3
+         ).astype(np.float16)
+    return codes, s, b
+
+
+def _dev_cache(codes, s, b, KV, N, D, bits):
+    words = aq.aq_pack(torch.from_numpy(codes).cuda(), bits).view(KV, N, D * bits // 32)
+    return (words, torch.from_numpy(s).cuda().view(KV, N, -1),
+            torch.from_numpy(b).cuda().view(KV, N, -1))
+
+
+def _case(H, KV, N, D, bits, group, dtype, seed, qscale=2.0):
+    rng = np.random.default_rng(seed)
+    kc, ks, kb = _cache(rng, KV, N, D, bits, group)
+    vc, vs, vb = _cache(rng, KV, N, D, bits, group)
+    qf = (rng.standard_normal((H, D)) * qscale).astype(np.float32)
+    q_bits = workloads.f32_to_bf16_bits(qf) if dtype == "bf16" else workloads.f32_to_fp16_bits(qf)
+    return (kc, ks, kb), (vc, vs, vb), q_bits
+
+
+def _check(H, KV, N, D, bits, group, dtype, seed, qscale=2.0):
+    (kc, ks, kb), (vc, vs, vb), q_bits = _case(H, KV, N, D, bits, group, dtype, seed, qscale)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+    q = torch.from_numpy(q_bits.view(np.int16)).cuda().view(tdt)
+    o = aq.aq_attention_decode(q, _dev_cache(kc, ks, kb, KV, N, D, bits),
+                               _dev_cache(vc, vs, vb, KV, N, D, bits), bits, group)
+    torch.cuda.synchronize()
+    got = workloads.to_f64(o.view(torch.int16).cpu().numpy().view(np.uint16), dtype)
+    ref, smag, vmag = oracle.attention(workloads.to_f64(q_bits, dtype), oracle.pack_g(kc, bits),
+                                       ks, kb, oracle.pack_g(vc, bits), vs, vb, KV, N, bits, group)
+    tau = (1e-4 * smag + 1e-5).max(axis=1, keepdims=True)
+    rnd = 2.0**-8 if dtype == "bf16" else 2.0**-11
+    tol = (np.expm1(2 * tau) + 2.0**-24 * N) * vmag + rnd * np.abs(ref) + 1e-6
+    bad = np.argwhere(~(np.abs(got - ref) <= tol))
+    assert bad.size == 0, [(int(h), int(d), float(got[h, d]), float(ref[h, d]), float(tol[h, d]))
+                           for h, d in bad[:4]]
+
+
+@pytest.mark.parametrize("H,KV,N,D,bits,group,dtype", [
+    (4, 4, 1, 64, 4, 32, "bf16"),         # one cached row
+    (8, 2, 100, 128, 4, 64, "bf16"),      # four query heads per KV head
+    (16, 8, 1000, 256, 8, 64, "bf16"),    # several CTAs per cluster
+    (8, 1, 777, 128, 8, 32, "fp16"),      # eight query heads, ragged blocks
+    (2, 2, 5000, 64, 4, 64, "fp16"),      # 16 blocks of a KV head
+    (32, 8, 4096, 128, 4, 128, "bf16"),
+    (6, 6, 70, 256, 4, 32, "bf16"),       # rows fewer than warps x blocks
+])
+def test_attention_parity(H, KV, N, D, bits, group, dtype):
+    _check(H, KV, N, D, bits, group, dtype, seed=H + KV + N + D + bits + group)
+
+
+def test_attention_sharp_softmax():
+    # large scores: one row dominates each head
+    _check(8, 4, 333, 128, 8, 64, "bf16", seed=9, qscale=40.0)
+
+
+def test_attention_workload_shape():
+    # 16 query heads over 8 KV heads of 256 dims, 8192 cached rows, 4-bit
+    _check(16, 8, 8192, 256, 4, 64, "bf16", seed=10)
+
+
+def test_attention_unsupported_head_dim():
+    (kc, ks, kb), (vc, vs, vb), q_bits = _case(2, 2, 10, 96, 4, 32, "bf16", seed=1)
+    q = torch.from_numpy(q_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    with pytest.raises(aq.AqError) as e:
+        aq.aq_attention_decode(q, _dev_cache(kc, ks, kb, 2, 10, 96, 4),
+                               _dev_cache(vc, vs, vb, 2, 10, 96, 4), 4, 32)
+    assert e.value.status == 2
+
+
+def test_attention_deterministic():
+    (kc, ks, kb), (vc, vs, vb), q_bits = _case(16, 8, 3000, 128, 4, 64, "bf16", seed=2)
+    q = torch.from_numpy(q_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    k = _dev_cache(kc, ks, kb, 8, 3000, 128, 4)
+    v = _dev_cache(vc, vs, vb, 8, 3000, 128, 4)
+    outs = [aq.aq_attention_decode(q, k, v, 4, 64).clone() for _ in range(3)]
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
