@@ -8,9 +8,11 @@ total exceeds twice the L2 size (every call reads its weights from HBM).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload decode|small|split3:I|layer:I|prefill:I|quantize:I|
-                                layerstep:I|widths:I] [--all]
+                                layerstep:I|widths:I|attention:I] [--all]
 
-widths:I times aq_matmul_ex on other code widths and group sizes.
+widths:I times aq_matmul_ex on other code widths and group sizes;
+attention:I times aq_attention_decode (decode attention over a quantised KV
+cache).
 layerstep:I times one decoder-layer step (seven projections; I = 0/1 fused or
 not at M = 1, 2/3 at M = 8).  quantize:I times the float -> affine quantiser (aq_quantize) on the weight
 shapes of workloads.QUANTIZE_WORKLOADS instead of the matmul.
@@ -734,6 +736,120 @@ def run_widths(args, rank, world, local_rank):
     }
 
 
+ATTN_METRIC = ("µs/call and effective HBM GB/s (fraction of roofline), decode attention over "
+               "an affine-quantised KV cache")
+# name -> list of (H, KV, N, D, bits, group, q dtype)
+ATTN_WORKLOADS = {"attention": [(16, 8, 8192, 256, 4, 64, "bf16"), (16, 8, 2048, 256, 4, 64, "bf16"),
+                                (16, 8, 32768, 256, 4, 64, "bf16"), (16, 8, 8192, 256, 8, 64, "bf16"),
+                                (32, 8, 8192, 128, 4, 64, "bf16")]}
+
+
+def run_attention(args, rank, world, local_rank):
+    """aq_attention_decode on one decode step of a quantised KV cache:
+    device-timed calls over rotating cache copies (> 2x L2) and the same
+    through host buffers (q in, o out)."""
+    import torch
+    import quantized_matmul_affine_gb300 as aq
+
+    torch.cuda.set_device(local_rank)
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    name, idx = parse_workload(args.workload)
+    H, KV, N, D, bits, group, dt = ATTN_WORKLOADS[name][idx]
+    rng = np.random.default_rng(70 + idx)
+    R = KV * N
+    G = D // group
+
+    def cache():
+        codes = rng.integers(0, 1 << bits, size=(R, D), dtype=np.uint8)
+        s = (np.abs(rng.standard_normal((R, G))) * (0.16 / (1 << bits)) + 1e-3).astype(np.float16)
+        b = (-(1 << (bits - 1)) * s.astype(np.float64)).astype(np.float16)
+        return (aq.aq_pack(torch.from_numpy(codes).cuda(), bits).view(KV, N, D * bits // 32),
+                torch.from_numpy(s).cuda().view(KV, N, G), torch.from_numpy(b).cuda().view(KV, N, G))
+
+    k0, v0 = cache(), cache()
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float16
+    qb = workloads.make_x(H, D, dt, seed=71)
+    q = torch.from_numpy(qb.view(np.int16)).cuda().view(tdt)
+    l2 = getattr(props, "L2_cache_size", 126 * 1024 * 1024)
+    cbytes = 2 * (R * D * bits // 8 + 4 * R * G)
+    copies = max(2, -(-2 * l2 // cbytes) + 1)
+    caches = [(tuple(t.clone() for t in k0), tuple(t.clone() for t in v0)) for _ in range(copies)]
+    outs = [torch.empty((H, D), dtype=tdt, device="cuda") for _ in range(copies)]
+    stream = torch.cuda.Stream()
+    steps = max(1, min(args.steps, 4096))
+    chunk = min(256, steps)
+    with torch.cuda.stream(stream):
+        aq.aq_attention_decode(q, *caches[0], bits, group, out=outs[0], stream=stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(chunk):
+                c = i % copies
+                aq.aq_attention_decode(q, *caches[c], bits, group, out=outs[c], stream=stream)
+        for _ in range(max(1, args.warmup // chunk)):
+            g.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(str(props.uuid) if hasattr(props, "uuid") else "0")
+    if not str(sampler.gpu_id).startswith("GPU-"):
+        sampler.gpu_id = "GPU-" + str(sampler.gpu_id)
+    sampler.start()
+    time.sleep(0.5)
+    reps = max(1, steps // chunk)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.mark()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark()
+    clocks = sampler.stop()
+    us = reduce_max(ev0.elapsed_time(ev1) * 1e3 / (reps * chunk), "cuda")
+    q_host = torch.from_numpy(qb.view(np.int16)).view(tdt).pin_memory()
+    o_host = torch.empty((H, D), dtype=tdt).pin_memory()
+    q_dev = torch.empty_like(q)
+    n_e2e = 200
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(n_e2e):
+            q_dev.copy_(q_host, non_blocking=True)
+            aq.aq_attention_decode(q_dev, *caches[i % copies], bits, group, out=outs[0],
+                                   stream=stream)
+            o_host.copy_(outs[0], non_blocking=True)
+            stream.synchronize()
+    e2e_us = reduce_max((time.perf_counter() - t0) * 1e6 / n_e2e, "cuda")
+    hbm, _, src = peaks()
+    by = cbytes + 2 * 2 * H * D
+    achieved = by / (us * 1e-6) / 1e9
+    return {
+        "metric": ATTN_METRIC,
+        "value": round(whole_job_us_per_call(us, world), 3),
+        "unit": "us/call",
+        "n_gpus": world, "steps": reps * chunk, "warmup": args.warmup,
+        "ms_per_step": us / 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": dt, "data": "synthetic",
+        "config": {"workload": f"{name}[{idx}]: {H} query heads over {KV} KV heads of {D}, "
+                               f"{N} cached rows, {bits}-bit group-{group} K and V, q {dt}",
+                   "H": H, "KV": KV, "N": N, "D": D, "bits": bits, "group": group,
+                   "l2": f"cold: {copies} rotating cache copies > 2x L2 ({l2 / 1e6:.0f} MB)",
+                   "timing": f"CUDA events on the launching stream around {reps} replays of a "
+                             f"CUDA graph of {chunk} calls",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm,
+                     "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
+                     "peak_source": f"{src} (MEASURED_PEAKS.json)" if src == "measured"
+                     else "fallback",
+                     "algorithmic_bytes_per_launch": by},
+        "e2e": {"value": round(whole_job_us_per_call(e2e_us, world), 3), "unit": "us/call",
+                "h2d_bytes_per_step": 2 * H * D, "d2h_bytes_per_step": 2 * H * D,
+                "path": "pinned q -> device, aq_attention_decode, o -> pinned host, sync"},
+        "gpu_launches": reps * chunk,
+        "clocks": clocks,
+    }
+
+
 def cpu_sample_time(p, budget_s, threads):
     """Time the oracle on a column sample of p; returns (us per full call, desc)."""
     import oracle
@@ -846,6 +962,11 @@ def main():
         specs = [f"{n}:{i}" for n, c in workloads.WORKLOADS.items() for i in range(len(c))]
     for spec in specs:
         args.workload = spec
+        if parse_workload(spec)[0] in ATTN_WORKLOADS:
+            line = run_attention(args, rank, world, local_rank)
+            if rank == 0:
+                print(json.dumps(line), flush=True)
+            continue
         if parse_workload(spec)[0] in WIDTH_WORKLOADS:
             line = run_widths(args, rank, world, local_rank)
             if rank == 0:

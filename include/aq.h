@@ -175,14 +175,16 @@ aq_status aq_quantize_ex(int dtype, const void *w_dev, int64_t N, int64_t K, int
  *   q_dev         [H][D], device.
  *   k_words_dev   uint32 [KV][N][D*bits/32], device, 16-byte aligned: row
  *                 (kv, n) packed as aq_pack packs a weight row.
- *   k_scales_dev, k_biases_dev  fp16 [KV][N][D/group_size], device.
+ *   k_scales_dev, k_biases_dev  fp16 [KV][N][D/group_size], device,
+ *                 16-byte aligned.
  *   v_words_dev, v_scales_dev, v_biases_dev  the same for V.
  *   out_dev       o [H][D], device, caller-allocated.
- * Served: bits 4 or 8, group_size 32/64/128 (D % group_size == 0,
- * group_size >= D/32), D in {64, 128, 256}, H/KV in {1, 2, 4, 8}, any
- * N >= 1.  Scores and probabilities are fp32; o is rounded once.  The rows
- * of a KV head are split over the CTAs of one thread-block cluster and
- * merged in rank order (deterministic); the library allocates nothing.
+ * Served: bits 4 or 8, group_size 32/64/128 (D % group_size == 0), D in
+ * {64, 128, 256}, H/KV in {1, 2, 4, 8}, any N >= 1.  Scores are fp32; the
+ * probabilities times the value scales enter the value product as fp16
+ * (relative error 2^-11 per term); o is rounded once.  The rows of a KV
+ * head are split over the CTAs of one thread-block cluster and merged in
+ * rank order (deterministic); the library allocates nothing.
  * Errors: AQ_ERR_INVALID_ARG for bad sizes, widths, group sizes or NULL
  * pointers; AQ_ERR_MISALIGNED; AQ_ERR_UNSUPPORTED for valid arguments
  * outside the served set (nothing queued); AQ_ERR_CUDA if the launch fails.

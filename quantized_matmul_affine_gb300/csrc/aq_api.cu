@@ -309,8 +309,8 @@ aq_status aq_attention_decode(int dtype, const void *q_dev, const uint32_t *k_wo
         (group_size != 32 && group_size != 64 && group_size != 128) || D % group_size != 0)
         return AQ_ERR_INVALID_ARG;
     if (!aligned(q_dev, 2) || !aligned(out_dev, 2) || !aligned(k_words_dev, 16) ||
-        !aligned(v_words_dev, 16) || !aligned(k_scales_dev, 2) || !aligned(k_biases_dev, 2) ||
-        !aligned(v_scales_dev, 2) || !aligned(v_biases_dev, 2))
+        !aligned(v_words_dev, 16) || !aligned(k_scales_dev, 16) || !aligned(k_biases_dev, 16) ||
+        !aligned(v_scales_dev, 16) || !aligned(v_biases_dev, 16))
         return AQ_ERR_MISALIGNED;
     if (!attention_supported(H, KV, N, D, bits, group_size)) return AQ_ERR_UNSUPPORTED;
     if (attention_launch(dtype, q_dev, k_words_dev, k_scales_dev, k_biases_dev, v_words_dev,
@@ -454,11 +454,12 @@ aq_status aq_stats(uint64_t *calls, int n, int reset) {
 aq_status aq_device_error(uint32_t *code, int clear) {
     if (!code) return AQ_ERR_INVALID_ARG;
     if (cudaDeviceSynchronize() != cudaSuccess) return AQ_ERR_CUDA;
-    uint32_t a = 0, b = 0, c = 0;
+    uint32_t a = 0, b = 0, c = 0, d = 0;
     if (qmv_read_error(&a, clear != 0) != cudaSuccess) return AQ_ERR_CUDA;
     if (tc_read_error(&b, clear != 0) != cudaSuccess) return AQ_ERR_CUDA;
     if (gemv_read_error(&c, clear != 0) != cudaSuccess) return AQ_ERR_CUDA;
-    *code = a | b | c;
+    if (attn_read_error(&d, clear != 0) != cudaSuccess) return AQ_ERR_CUDA;
+    *code = a | b | c | d;
     return AQ_OK;
 }
 

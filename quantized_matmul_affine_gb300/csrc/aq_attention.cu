@@ -9,20 +9,26 @@
 //
 // GB300 design:
 //   * One CTA per (KV head, block of cached rows) takes every query head of
-//     that KV head (NREP = H / KV of them), so each K and V row is read once.
-//     The blocks of a KV head form a thread-block cluster (up to 16 CTAs);
-//     their partial results are merged in rank order through distributed
-//     shared memory - no global scratch, no second launch.
-//   * 256 threads: lane l holds head-dimension elements [l*E, l*E + E),
-//     E = D / 32 (all inside one quantisation group); warp w takes rows
-//     w, w+8, ... of the block.  Per row: the lane's codes (one load of E
-//     codes), the factored partial score for each query head, a warp sum,
-//     the online softmax update, and the value row dequantised once and
-//     accumulated for every query head.
-//   * The eight warps' (max, sum, o) merge through shared memory in warp
-//     order; the cluster's CTAs then in rank order.  Scores and
-//     probabilities stay in fp32 (the pages round the scores to the input
-//     type; fp32 is the more exact reading); o is rounded once.
+//     that KV head (up to 8), so each K and V row is read once.  The blocks
+//     of a KV head form a thread-block cluster; their partial results are
+//     merged in rank order through distributed shared memory - no global
+//     scratch, no second launch.  The cluster size is picked from the
+//     driver's count of co-resident clusters.
+//   * A producer warp streams 128-row stages of K and V codes (2-D TMA,
+//     swizzled so that the fragment reads below are free of bank conflicts)
+//     and their scales and biases (1-D TMA) into a shared-memory ring.
+//   * Each of 8 consumer warps takes a 16-row tile of a stage.  Scores on the
+//     tensor cores: S^T-free form S[16 rows][8 heads] = codes x q', the codes
+//     as the exact fp16 subnormals code * 2^-24 (or 2^-20 where a nibble sits
+//     at bit 4), q' = q * 2^e per head in fp16; one m16n8k16 chain per group,
+//     then s = scale * sum(q code) + bias * sum(q) in fp32.
+//   * Online softmax in base 2 on the fragment; the probabilities, times the
+//     value scale of their row and group (and 2^ev, a per-CTA power of two
+//     that keeps them in the fp16 normal range), are transposed in registers
+//     (movmatrix) into the B operand of O^T[d][heads] += codes^T x P'; the
+//     value biases enter as sum(p * bias) per (head, group) in fp32.
+//   * The warps' (max, sum, o) merge through shared memory in warp order, the
+//     cluster's CTAs then in rank order; o is rounded once.
 #include "aq_internal.h"
 #include "aq_ptx.cuh"
 
@@ -31,150 +37,486 @@
 
 #include <algorithm>
 #include <mutex>
-#include <type_traits>
 
 namespace aq {
+
+__device__ uint32_t g_attn_error;
+
 namespace {
 
-constexpr int kAttnThreads = 256;
-constexpr int kAttnWarps = kAttnThreads / 32;
+constexpr int kCWarps = 8;                           // consumer warps
+constexpr int kAttnThreads = (kCWarps + 1) * 32;     // + the TMA producer warp
+constexpr int kTile = 16;                            // rows per warp tile
+constexpr int kStageRows = kTile * kCWarps;          // 128
+constexpr int kMaxStages = 8;
+constexpr int kRingBudget = 192 * 1024;
+constexpr float kLog2e = 1.4426950408889634f;
 
 struct AttnParams {
     const void *q;
-    const uint8_t *kw, *vw;       // packed rows [KV*N][D*bits/8] bytes
-    const __half *ks, *kb, *vs, *vb;  // [KV*N][D/group]
+    const __half *vs;   // value scales, read once for the CTA's power of two
     void *out;
-    int H, KV, N, D, group;
-    int block;     // cached rows per CTA
-    int csize;     // CTAs per cluster (one KV head)
-    int row_bytes;
+    uint32_t *err;
+    int KV, N, nrep;
+    int block;          // cached rows per CTA (multiple of 16)
+    int csize;          // CTAs per cluster (one KV head)
+    int stages;         // ring depth
+    int bf16;
 };
 
-template <typename T>
-__device__ __forceinline__ float ld_f(const T *p) {
-    if constexpr (std::is_same<T, __nv_bfloat16>::value)
-        return __bfloat162float(*p);
-    else
-        return __half2float(*p);
+template <int BITS, int D, int GROUP>
+struct Shape {
+    static constexpr int kRB = D * BITS / 8;            // bytes of one cached row
+    static constexpr int kW = kRB < 128 ? kRB : 128;    // TMA box width = swizzle span
+    static constexpr int kBoxes = kRB / kW;
+    static constexpr uint32_t kSwz = kW == 128 ? 7u : kW == 64 ? 3u : 1u;
+    static constexpr int kG = D / GROUP;                // groups per row
+    static constexpr int kGB = GROUP * BITS / 8;        // bytes of one group of a row
+    static constexpr int kCK = kGB / 4;                 // bytes a lane takes per row (scores)
+    static constexpr int kCV = kGB / 8;                 // bytes a lane takes per row (values)
+    static constexpr int kSteps = GROUP / 16;           // k-steps / M-tiles per group
+    static constexpr int kRegs = GROUP / 8;             // code registers per row per group
+    // scales: 128 rows x G halves from a 16-byte aligned start (up to 7
+    // before), in boxes of a multiple of 64 halves so that every box lands
+    // on a 128-byte boundary of shared memory (the tensor-copy rule)
+    static constexpr int kSH = kStageRows * kG + 8;
+    static constexpr int kSBoxes = (kSH + 255) / 256;
+    static constexpr int kSBox = ((kSH + kSBoxes - 1) / kSBoxes + 63) / 64 * 64;
+    static constexpr int kSArr = kSBoxes * kSBox;       // halves per scale array per stage
+    static constexpr int kCodeBytes = kStageRows * kRB; // K (or V) codes per stage
+    static constexpr int kTx = 2 * kCodeBytes + 4 * kSArr * 2;
+    static constexpr int kStageBytes = (kTx + 1023) / 1024 * 1024;
+    static_assert(kSBox <= 256 && (2 * kSBox) % 128 == 0 && (2 * kCodeBytes) % 1024 == 0,
+                  "tensor-copy boxes must land 128-byte aligned");
+};
+
+// Byte offset of (row, byte) inside a stage's K or V code region, with the
+// TMA swizzle of a box kW bytes wide (16-byte chunk index XOR row bits).
+template <class S>
+__device__ __forceinline__ uint32_t swz(int row, int byte) {
+    const uint32_t lin = (uint32_t)(row * S::kW + (byte % S::kW));
+    return (uint32_t)(byte / S::kW) * (kStageRows * S::kW) + (lin ^ (((lin >> 7) & S::kSwz) << 4));
 }
 
-// The lane's E codes as one 1/2/4/8-byte load.
-template <int BITS, int E>
-__device__ __forceinline__ void load_codes(const uint8_t *p, float (&c)[E]) {
-    constexpr int kBytes = E * BITS / 8;
-    uint64_t w;
-    if constexpr (kBytes == 1)
-        w = *p;
-    else if constexpr (kBytes == 2)
-        w = *reinterpret_cast<const uint16_t *>(p);
-    else if constexpr (kBytes == 4)
-        w = *reinterpret_cast<const uint32_t *>(p);
-    else
-        w = *reinterpret_cast<const uint64_t *>(p);
-#pragma unroll
-    for (int e = 0; e < E; ++e) c[e] = (float)((w >> (BITS * e)) & ((1u << BITS) - 1u));
+template <int NB>
+__device__ __forceinline__ void lds_words(const uint8_t *p, uint32_t (&w)[NB / 4 > 0 ? NB / 4 : 1]) {
+    if constexpr (NB == 2) {
+        w[0] = *reinterpret_cast<const uint16_t *>(p);
+    } else if constexpr (NB == 4) {
+        w[0] = *reinterpret_cast<const uint32_t *>(p);
+    } else if constexpr (NB == 8) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(p);
+        w[0] = v.x;
+        w[1] = v.y;
+    } else {
+        const uint4 v = *reinterpret_cast<const uint4 *>(p);
+        w[0] = v.x;
+        w[1] = v.y;
+        w[2] = v.z;
+        w[3] = v.w;
+    }
 }
 
-template <int BITS, int E, int NREP, bool BF16>
-__global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
-    using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-    constexpr int D = 32 * E;
-    extern __shared__ float sh[];
-    float *wm = sh;                              // [warps][NREP]
-    float *wl = wm + kAttnWarps * NREP;          // [warps][NREP]
-    float *wo = wl + kAttnWarps * NREP;          // [warps][NREP][D]
-    float *cm = wo + kAttnWarps * NREP * D;      // [NREP]   this CTA's merge
-    float *cl = cm + NREP;                       // [NREP]
-    float *co = cl + NREP;                       // [NREP][D]
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
+__device__ __forceinline__ void consumer_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kCWarps * 32) : "memory");
+}
+
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((127 + e) << 23); }
+
+// 15 - (the exponent of v as frexp gives it): v * 2^result lies in [2^14, 2^15)
+// (clamped to +-100 so that every power of two used stays a normal float).
+__device__ __forceinline__ int exp_for(float v) {
+    int ex;
+    frexpf(v, &ex);
+    return v > 0.f ? max(-100, min(100, 15 - ex)) : 0;
+}
+
+__device__ __forceinline__ void attn_record(volatile int *flag, uint32_t *err, uint32_t code) {
+    *flag = 1;
+    atomicOr(err, code);
+}
+
+template <int BITS, int D, int GROUP>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tm_kw,
+                const __grid_constant__ CUtensorMap tm_vw, const __grid_constant__ CUtensorMap tm_ks,
+                const __grid_constant__ CUtensorMap tm_kb, const __grid_constant__ CUtensorMap tm_vs,
+                const __grid_constant__ CUtensorMap tm_vb) {
+    using S = Shape<BITS, D, GROUP>;
+    constexpr int G = S::kG;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *ring = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int merge_bytes = 4 * ((kCWarps + 1) * p.nrep * (D + 2));
+    uint8_t *tail = ring + max(p.stages * S::kStageBytes, merge_bytes);
+    uint2 *qfrag = reinterpret_cast<uint2 *>(tail);                 // [D/16][32]
+    float *qf = reinterpret_cast<float *>(qfrag + (D / 16) * 32);   // [8][D]  q * 2^e
+    float *qs2 = qf + 8 * D;                                        // [8][G]  sum(q) log2 e
+    float *qsc = qs2 + 8 * G;                                       // [8]     2^(24-e) log2 e
+    float *red = qsc + 8;                                           // [8]
+    uint64_t *full = reinterpret_cast<uint64_t *>(red + 8);
+    uint64_t *empty = full + kMaxStages;
+    int *flag_s = reinterpret_cast<int *>(empty + kMaxStages);
+    volatile int *flag = flag_s;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gid = lane >> 2, t = lane & 3;
     const int kv = (int)blockIdx.x / p.csize;
     const int rank = (int)blockIdx.x % p.csize;
     const int n0 = rank * p.block;
     const int n1 = min(p.N, n0 + p.block);
-    const int gRow = D / p.group;
-    const int grp = lane * E / p.group;
+    const int nst = n1 > n0 ? (n1 - n0 + kStageRows - 1) / kStageRows : 0;
+    const int nrep = p.nrep;
+    const long long row_base = (long long)kv * p.N;
 
-    // the query heads of this KV head: the lane's elements and their sums
-    const T *q = static_cast<const T *>(p.q);
-    float qv[NREP][E], qsum[NREP];
-#pragma unroll
-    for (int j = 0; j < NREP; ++j) {
-        qsum[j] = 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-            qv[j][e] = ld_f<T>(q + (size_t)(kv * NREP + j) * D + lane * E + e);
-            qsum[j] += qv[j][e];
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < p.stages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kCWarps);
         }
-    }
-    float m[NREP], l[NREP], o[NREP][E];
-#pragma unroll
-    for (int j = 0; j < NREP; ++j) {
-        m[j] = -INFINITY;
-        l[j] = 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) o[j][e] = 0.f;
-    }
-
-    for (int n = n0 + warp; n < n1; n += kAttnWarps) {
-        const size_t r = (size_t)kv * p.N + n;
-        float c[E];
-        load_codes<BITS, E>(p.kw + r * p.row_bytes + lane * (E * BITS / 8), c);
-        const float ksc = __half2float(p.ks[r * gRow + grp]);
-        const float kbi = __half2float(p.kb[r * gRow + grp]);
-        float s[NREP];
-#pragma unroll
-        for (int j = 0; j < NREP; ++j) {
-            float dot = 0.f;
-#pragma unroll
-            for (int e = 0; e < E; ++e) dot = fmaf(qv[j][e], c[e], dot);
-            float part = fmaf(ksc, dot, kbi * qsum[j]);
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-            s[j] = part;
-        }
-        float cv[E];
-        load_codes<BITS, E>(p.vw + r * p.row_bytes + lane * (E * BITS / 8), cv);
-        const float vsc = __half2float(p.vs[r * gRow + grp]);
-        const float vbi = __half2float(p.vb[r * gRow + grp]);
-        float vd[E];
-#pragma unroll
-        for (int e = 0; e < E; ++e) vd[e] = fmaf(vsc, cv[e], vbi);
-#pragma unroll
-        for (int j = 0; j < NREP; ++j) {
-            const float mn = fmaxf(m[j], s[j]);
-            const float f = expf(m[j] - mn);  // 0 on the first row (m = -inf)
-            const float pj = expf(s[j] - mn);
-            l[j] = fmaf(l[j], f, pj);
-            m[j] = mn;
-#pragma unroll
-            for (int e = 0; e < E; ++e) o[j][e] = fmaf(o[j][e], f, pj * vd[e]);
-        }
-    }
-
-    // the eight warps, in warp order
-#pragma unroll
-    for (int j = 0; j < NREP; ++j) {
-        if (lane == 0) {
-            wm[warp * NREP + j] = m[j];
-            wl[warp * NREP + j] = l[j];
-        }
-#pragma unroll
-        for (int e = 0; e < E; ++e) wo[(warp * NREP + j) * D + lane * E + e] = o[j][e];
+        *flag_s = 0;
+        fence_mbar_init();
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < NREP * D; i += kAttnThreads) {
+
+    if (warp == kCWarps) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int st = 0; st < nst && !*flag; ++st) {
+                const int slot = st % p.stages, lap = st / p.stages;
+                if (lap > 0 && !mbar_wait(&empty[slot], (lap - 1) & 1)) {
+                    attn_record(flag, p.err, ERR_ATTN_EMPTY);
+                    break;
+                }
+                uint8_t *sb = ring + slot * S::kStageBytes;
+                const int row0 = (int)(row_base + n0 + st * kStageRows);
+                const int x0 = (row0 * G) & ~7;
+                mbar_arrive_expect_tx(&full[slot], (uint32_t)S::kTx);
+#pragma unroll
+                for (int b = 0; b < S::kBoxes; ++b) {
+                    tma_load_2d(sb + b * kStageRows * S::kW, &tm_kw, b * S::kW, row0, &full[slot]);
+                    tma_load_2d(sb + S::kCodeBytes + b * kStageRows * S::kW, &tm_vw, b * S::kW, row0,
+                                &full[slot]);
+                }
+                uint8_t *sc = sb + 2 * S::kCodeBytes;
+#pragma unroll
+                for (int b = 0; b < S::kSBoxes; ++b) {
+                    const int off = 2 * b * S::kSBox;
+                    tma_load_1d(sc + off, &tm_ks, x0 + b * S::kSBox, &full[slot]);
+                    tma_load_1d(sc + 2 * S::kSArr + off, &tm_kb, x0 + b * S::kSBox, &full[slot]);
+                    tma_load_1d(sc + 4 * S::kSArr + off, &tm_vs, x0 + b * S::kSBox, &full[slot]);
+                    tma_load_1d(sc + 6 * S::kSArr + off, &tm_vb, x0 + b * S::kSBox, &full[slot]);
+                }
+                issued = st + 1;
+            }
+            // copies still in flight land before the CTA moves on
+            for (int st = max(0, issued - p.stages); st < issued; ++st)
+                if (!mbar_wait(&full[st % p.stages], (st / p.stages) & 1)) {
+                    attn_record(flag, p.err, ERR_ATTN_FULL);
+                    break;
+                }
+        }
+    } else {
+        // ------------------------------------------------------------ prologue
+        {
+            // warp w: query head w of this KV head (zeros past nrep)
+            const int h = warp;
+            float qv[D / 32];
+            float mx = 0.f;
+#pragma unroll
+            for (int i = 0; i < D / 32; ++i) {
+                float v = 0.f;
+                if (h < nrep) {
+                    const size_t idx = (size_t)(kv * nrep + h) * D + lane + 32 * i;
+                    v = p.bf16 ? __bfloat162float(static_cast<const __nv_bfloat16 *>(p.q)[idx])
+                               : __half2float(static_cast<const __half *>(p.q)[idx]);
+                }
+                qv[i] = v;
+                mx = fmaxf(mx, fabsf(v));
+            }
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, off));
+            const int e = exp_for(mx);
+            const float sc = pow2i(e);
+#pragma unroll
+            for (int i = 0; i < D / 32; ++i) qf[h * D + lane + 32 * i] = qv[i] * sc;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float sum = 0.f;
+#pragma unroll
+                for (int i = 0; i < D / 32; ++i)
+                    if ((lane + 32 * i) / GROUP == g) sum += qv[i];
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(~0u, sum, off);
+                if (lane == 0) qs2[h * G + g] = sum * kLog2e;
+            }
+            if (lane == 0) qsc[h] = pow2i(24 - e) * kLog2e;
+
+            // the CTA's largest value scale
+            float vm = 0.f;
+            const long long v0 = (row_base + n0) * G, v1 = (row_base + n1) * G;
+            for (long long i = v0 + threadIdx.x; i < v1; i += kCWarps * 32)
+                vm = fmaxf(vm, fabsf(__half2float(p.vs[i])));
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) vm = fmaxf(vm, __shfl_xor_sync(~0u, vm, off));
+            if (lane == 0) red[warp] = vm;
+        }
+        consumer_sync();
+        // B fragments of q': k-step k of group g, lane (gid, t) = head gid,
+        // the k of thread t's registers 2s and 2s+1 (their two halves)
+        for (int k = 0; k < D / 16; ++k) {
+            const int g = k / S::kSteps, s2 = k % S::kSteps;
+            uint32_t r[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int i = 2 * s2 + j;
+                float v[2];
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    int d;
+                    float f = 1.f;
+                    if constexpr (BITS == 4) {
+                        d = g * GROUP + t * (GROUP / 4) + 8 * (i / 4) + (i % 4) + 4 * hf;
+                        if (i & 1) f = 0.0625f;
+                    } else {
+                        d = g * GROUP + t * (GROUP / 4) + 4 * (i / 2) + (i % 2) + 2 * hf;
+                    }
+                    v[hf] = gid < nrep ? qf[gid * D + d] * f : 0.f;
+                }
+                r[j] = pack_half2(v[0], v[1]);
+            }
+            qfrag[k * 32 + lane] = make_uint2(r[0], r[1]);
+        }
+        float vmax = 0.f;
+#pragma unroll
+        for (int w = 0; w < kCWarps; ++w) vmax = fmaxf(vmax, red[w]);
+        const int ev = exp_for(vmax);
+        const float vsc = pow2i(ev);
+        const float qsc0 = qsc[2 * t], qsc1 = qsc[2 * t + 1];
+        consumer_sync();
+
+        // ------------------------------------------------------------ main loop
+        float m2[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+        float bt[2][G];
+        float O[D / 16][4];
+#pragma unroll
+        for (int g = 0; g < G; ++g) bt[0][g] = bt[1][g] = 0.f;
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.f;
+
+        for (int st = 0; st < nst; ++st) {
+            const int slot = st % p.stages, lap = st / p.stages;
+            if (*flag) break;
+            if (!mbar_wait(&full[slot], lap & 1)) {
+                attn_record(flag, p.err, ERR_ATTN_FULL);
+                break;
+            }
+            const int r0 = n0 + st * kStageRows + warp * kTile;   // first row of the tile
+            if (r0 < n1) {
+                const uint8_t *kst = ring + slot * S::kStageBytes;
+                const uint8_t *vst = kst + S::kCodeBytes;
+                const int row0 = (int)(row_base + n0 + st * kStageRows);
+                const int soff = row0 * G - ((row0 * G) & ~7);
+                const __half *sks = reinterpret_cast<const __half *>(vst + S::kCodeBytes) + soff;
+                const __half *skb = sks + S::kSArr;
+                const __half *svs = sks + 2 * S::kSArr;
+                const __half *svb = sks + 3 * S::kSArr;
+                const int tr = warp * kTile;                       // tile row in the stage
+                const int ra = tr + gid, rb = tr + gid + 8;
+
+                // scores: rows (gid, gid+8) x heads (2t, 2t+1)
+                float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    uint32_t Ra[S::kRegs], Rb[S::kRegs];
+#pragma unroll
+                    for (int c = 0; c < (S::kCK + 15) / 16; ++c) {
+                        constexpr int NB = S::kCK < 16 ? S::kCK : 16;
+                        uint32_t wa[NB / 4], wb[NB / 4];
+                        const int byte = g * S::kGB + t * S::kCK + c * 16;
+                        lds_words<NB>(kst + swz<S>(ra, byte), wa);
+                        lds_words<NB>(kst + swz<S>(rb, byte), wb);
+#pragma unroll
+                        for (int j = 0; j < NB / 4; ++j) {
+                            const int base = (c * (NB / 4) + j) * (BITS == 4 ? 4 : 2);
+                            if constexpr (BITS == 4) {
+                                const uint32_t va = wa[j] >> 8, vb = wb[j] >> 8;
+                                Ra[base + 0] = wa[j] & 0x000F000Fu;
+                                Ra[base + 1] = wa[j] & 0x00F000F0u;
+                                Ra[base + 2] = va & 0x000F000Fu;
+                                Ra[base + 3] = va & 0x00F000F0u;
+                                Rb[base + 0] = wb[j] & 0x000F000Fu;
+                                Rb[base + 1] = wb[j] & 0x00F000F0u;
+                                Rb[base + 2] = vb & 0x000F000Fu;
+                                Rb[base + 3] = vb & 0x00F000F0u;
+                            } else {
+                                Ra[base + 0] = wa[j] & 0x00FF00FFu;
+                                Ra[base + 1] = (wa[j] >> 8) & 0x00FF00FFu;
+                                Rb[base + 0] = wb[j] & 0x00FF00FFu;
+                                Rb[base + 1] = (wb[j] >> 8) & 0x00FF00FFu;
+                            }
+                        }
+                    }
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int k = 0; k < S::kSteps; ++k) {
+                        const uint2 bq = qfrag[(g * S::kSteps + k) * 32 + lane];
+                        const uint32_t a[4] = {Ra[2 * k], Rb[2 * k], Ra[2 * k + 1], Rb[2 * k + 1]};
+                        mma_f16_16816(acc, a, bq.x, bq.y, acc);
+                    }
+                    const float ksa = __half2float(sks[ra * G + g]), ksb = __half2float(sks[rb * G + g]);
+                    const float kba = __half2float(skb[ra * G + g]), kbb = __half2float(skb[rb * G + g]);
+                    const float q0 = qs2[(2 * t) * G + g], q1 = qs2[(2 * t + 1) * G + g];
+                    s[0] = fmaf(ksa, acc[0] * qsc0, fmaf(kba, q0, s[0]));
+                    s[1] = fmaf(ksa, acc[1] * qsc1, fmaf(kba, q1, s[1]));
+                    s[2] = fmaf(ksb, acc[2] * qsc0, fmaf(kbb, q0, s[2]));
+                    s[3] = fmaf(ksb, acc[3] * qsc1, fmaf(kbb, q1, s[3]));
+                }
+                if (r0 + gid >= n1) s[0] = s[1] = -INFINITY;
+                if (r0 + gid + 8 >= n1) s[2] = s[3] = -INFINITY;
+
+                // online softmax (base 2) per head column
+                float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+                for (int off = 4; off <= 16; off <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(~0u, mx0, off));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(~0u, mx1, off));
+                }
+                const float mn0 = fmaxf(m2[0], mx0), mn1 = fmaxf(m2[1], mx1);
+                const float f0 = exp2f(m2[0] - mn0), f1 = exp2f(m2[1] - mn1);
+                m2[0] = mn0;
+                m2[1] = mn1;
+                const float pr[4] = {exp2f(s[0] - mn0), exp2f(s[1] - mn1), exp2f(s[2] - mn0),
+                                     exp2f(s[3] - mn1)};
+                l[0] = fmaf(l[0], f0, pr[0] + pr[2]);
+                l[1] = fmaf(l[1], f1, pr[1] + pr[3]);
+                if (__any_sync(~0u, f0 != 1.f || f1 != 1.f)) {
+#pragma unroll
+                    for (int i = 0; i < D / 16; ++i) {
+                        O[i][0] *= f0;
+                        O[i][1] *= f1;
+                        O[i][2] *= f0;
+                        O[i][3] *= f1;
+                    }
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        bt[0][g] *= f0;
+                        bt[1][g] *= f1;
+                    }
+                }
+
+                // values: O^T[d][heads] += codes^T x (p * scale * 2^ev)
+                const int va0 = tr + 2 * t, va1 = va0 + 1, va8 = va0 + 8, va9 = va0 + 9;
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float vsa = __half2float(svs[ra * G + g]) * vsc;
+                    const float vsb = __half2float(svs[rb * G + g]) * vsc;
+                    const float vba = __half2float(svb[ra * G + g]);
+                    const float vbb = __half2float(svb[rb * G + g]);
+                    bt[0][g] = fmaf(pr[0], vba, fmaf(pr[2], vbb, bt[0][g]));
+                    bt[1][g] = fmaf(pr[1], vba, fmaf(pr[3], vbb, bt[1][g]));
+                    const uint32_t b0 = movmatrix_t(pack_half2(pr[0] * vsa, pr[1] * vsa));
+                    const uint32_t b1 = movmatrix_t(pack_half2(pr[2] * vsb, pr[3] * vsb));
+                    constexpr int NW = S::kCV >= 4 ? S::kCV / 4 : 1;
+                    uint32_t w0[NW], w1[NW], w8[NW], w9[NW];
+                    const int byte = g * S::kGB + gid * S::kCV;
+                    lds_words<S::kCV>(vst + swz<S>(va0, byte), w0);
+                    lds_words<S::kCV>(vst + swz<S>(va1, byte), w1);
+                    lds_words<S::kCV>(vst + swz<S>(va8, byte), w8);
+                    lds_words<S::kCV>(vst + swz<S>(va9, byte), w9);
+#pragma unroll
+                    for (int m = 0; m < S::kSteps; ++m) {
+                        uint32_t a[4];
+                        if constexpr (BITS == 4) {
+                            const int wi = m / 4, bi = m % 4;
+                            const uint32_t sel = (uint32_t)bi | ((uint32_t)(4 + bi) << 8);
+                            const uint32_t x = prmt(w0[wi], w1[wi], sel);
+                            const uint32_t y = prmt(w8[wi], w9[wi], sel);
+                            a[0] = x & 0x000F000Fu;
+                            a[1] = x & 0x00F000F0u;
+                            a[2] = y & 0x000F000Fu;
+                            a[3] = y & 0x00F000F0u;
+                        } else {
+                            const int wi = (2 * m) / 4, bi = (2 * m) % 4;
+                            const uint32_t sl = (uint32_t)bi | ((uint32_t)(4 + bi) << 8);
+                            const uint32_t sh = sl + 0x101u;
+                            a[0] = prmt(w0[wi], w1[wi], sl) & 0x00FF00FFu;
+                            a[1] = prmt(w0[wi], w1[wi], sh) & 0x00FF00FFu;
+                            a[2] = prmt(w8[wi], w9[wi], sl) & 0x00FF00FFu;
+                            a[3] = prmt(w8[wi], w9[wi], sh) & 0x00FF00FFu;
+                        }
+                        mma_f16_16816(O[g * S::kSteps + m], a, b0, b1, O[g * S::kSteps + m]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+        }
+
+        // sums over the eight row lanes of each head column
+#pragma unroll
+        for (int off = 4; off <= 16; off <<= 1) {
+            l[0] += __shfl_xor_sync(~0u, l[0], off);
+            l[1] += __shfl_xor_sync(~0u, l[1], off);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                bt[0][g] += __shfl_xor_sync(~0u, bt[0][g], off);
+                bt[1][g] += __shfl_xor_sync(~0u, bt[1][g], off);
+            }
+        }
+        consumer_sync();  // every warp is done with the ring
+        float *wm = reinterpret_cast<float *>(ring);       // [warps][nrep]
+        float *wl = wm + kCWarps * nrep;                   // [warps][nrep]
+        float *wo = wl + kCWarps * nrep;                   // [warps][nrep][D]
+        const float fa = pow2i(24 - ev), fb = BITS == 4 ? pow2i(20 - ev) : fa;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int h = 2 * t + hh;
+            if (h < nrep) {
+                if (gid == 0) {
+                    wm[warp * nrep + h] = m2[hh];
+                    wl[warp * nrep + h] = l[hh];
+                }
+                float *o = wo + (warp * nrep + h) * D;
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+#pragma unroll
+                    for (int m = 0; m < S::kSteps; ++m) {
+                        const int d = g * GROUP + gid * (GROUP / 8) + 2 * m;
+                        o[d] = fmaf(O[g * S::kSteps + m][hh], fa, bt[hh][g]);
+                        o[d + 1] = fmaf(O[g * S::kSteps + m][2 + hh], fb, bt[hh][g]);
+                    }
+            }
+        }
+    }
+    __syncthreads();
+
+    // the eight warps, in warp order (log2 units)
+    const float *wm = reinterpret_cast<const float *>(ring);
+    const float *wl = wm + kCWarps * nrep;
+    const float *wo = wl + kCWarps * nrep;
+    float *cm = const_cast<float *>(wo) + kCWarps * nrep * D;   // [nrep]
+    float *cl = cm + nrep;                                      // [nrep]
+    float *co = cl + nrep;                                      // [nrep][D]
+    for (int i = threadIdx.x; i < nrep * D; i += kAttnThreads) {
         const int j = i / D, d = i - j * D;
         float M = -INFINITY;
-        for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, wm[w * NREP + j]);
-        float L = 0.f, O = 0.f;
-        for (int w = 0; w < kAttnWarps; ++w) {
-            const float mw = wm[w * NREP + j];
-            const float g = mw == -INFINITY ? 0.f : expf(mw - M);  // a warp with no rows
-            L = fmaf(wl[w * NREP + j], g, L);
-            O = fmaf(wo[(w * NREP + j) * D + d], g, O);
+        for (int w = 0; w < kCWarps; ++w) M = fmaxf(M, wm[w * nrep + j]);
+        float L = 0.f, Ov = 0.f;
+        for (int w = 0; w < kCWarps; ++w) {
+            const float mw = wm[w * nrep + j];
+            const float g = mw == -INFINITY ? 0.f : exp2f(mw - M);  // a warp with no rows
+            L = fmaf(wl[w * nrep + j], g, L);
+            Ov = fmaf(wo[(w * nrep + j) * D + d], g, Ov);
         }
-        co[j * D + d] = O;
+        co[j * D + d] = Ov;
         if (d == 0) {
             cm[j] = M;
             cl[j] = L;
@@ -183,10 +525,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     __syncthreads();
 
     // the cluster's CTAs, in rank order; rank r writes its share of o
-    T *out = static_cast<T *>(p.out);
     const int C = p.csize;
     if (C > 1) cluster_sync();
-    const int total = NREP * D;
+    const int total = nrep * D;
     const int chunk = (total + C - 1) / C;
     const uint32_t bm = smem_u32(cm), bl = smem_u32(cl), bo = smem_u32(co);
     for (int i = rank * chunk + (int)threadIdx.x; i < min(total, (rank + 1) * chunk);
@@ -195,127 +536,225 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         float M = -INFINITY;
         for (int rr = 0; rr < C; ++rr)
             M = fmaxf(M, C > 1 ? ld_dsmem_f32(map_to_rank(bm + 4u * j, (uint32_t)rr)) : cm[j]);
-        float L = 0.f, O = 0.f;
+        float L = 0.f, Ov = 0.f;
         for (int rr = 0; rr < C; ++rr) {
             const float mr = C > 1 ? ld_dsmem_f32(map_to_rank(bm + 4u * j, (uint32_t)rr)) : cm[j];
             if (mr == -INFINITY) continue;  // a block with no rows
-            const float g = expf(mr - M);
+            const float g = exp2f(mr - M);
             const float lr = C > 1 ? ld_dsmem_f32(map_to_rank(bl + 4u * j, (uint32_t)rr)) : cl[j];
             const float orr =
                 C > 1 ? ld_dsmem_f32(map_to_rank(bo + 4u * (uint32_t)i, (uint32_t)rr)) : co[i];
             L = fmaf(lr, g, L);
-            O = fmaf(orr, g, O);
+            Ov = fmaf(orr, g, Ov);
         }
-        const float v = O / L;
-        if constexpr (BF16)
-            out[(size_t)(kv * NREP + j) * D + d] = __float2bfloat16_rn(v);
+        const float v = Ov / L;
+        const size_t oi = (size_t)(kv * nrep + j) * D + d;
+        if (p.bf16)
+            static_cast<__nv_bfloat16 *>(p.out)[oi] = __float2bfloat16_rn(v);
         else
-            out[(size_t)(kv * NREP + j) * D + d] = __float2half_rn(v);
+            static_cast<__half *>(p.out)[oi] = __float2half_rn(v);
     }
     if (C > 1) cluster_sync();  // keep this CTA's results until every rank has read them
 }
 
-size_t attn_smem(int nrep, int D) {
-    return sizeof(float) * ((size_t)2 * kAttnWarps * nrep + (size_t)kAttnWarps * nrep * D +
-                            2 * (size_t)nrep + (size_t)nrep * D);
+template <int BITS, int D, int GROUP>
+size_t attn_smem_t(int stages, int nrep) {
+    using S = Shape<BITS, D, GROUP>;
+    const size_t merge = 4 * (size_t)((kCWarps + 1) * nrep * (D + 2));
+    const size_t ring = std::max((size_t)stages * S::kStageBytes, merge);
+    const size_t tail = (size_t)(D / 16) * 32 * 8 + 4 * (size_t)(8 * D + 8 * S::kG + 16) +
+                        16 * (size_t)kMaxStages + 16;
+    return 1024 + ring + tail;
 }
 
-template <int BITS, int E, int NREP, bool BF16>
-cudaError_t attn_launch_t(const AttnParams &prm, cudaStream_t stream) {
-    auto kern = attn_kernel<BITS, E, NREP, BF16>;
+template <int BITS, int D, int GROUP>
+int attn_max_stages() {
+    using S = Shape<BITS, D, GROUP>;
+    return std::max(1, std::min(kMaxStages, kRingBudget / S::kStageBytes));
+}
+
+// Co-resident clusters of each size 1..16 for this instantiation (queried once).
+template <int BITS, int D, int GROUP>
+const int *attn_active_clusters() {
+    static int n[17];
     static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    const size_t smem = attn_smem(NREP, 32 * E);
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)attn_smem(8, 256));
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    std::call_once(once, [] {
+        auto kern = attn_kernel<BITS, D, GROUP>;
+        const size_t smem = attn_smem_t<BITS, D, GROUP>(attn_max_stages<BITS, D, GROUP>(), 8);
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        for (int c = 1; c <= 16; ++c) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)(c * 8), 1, 1);
+            cfg.blockDim = dim3(kAttnThreads, 1, 1);
+            cfg.dynamicSmemBytes = smem;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = (unsigned)c;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int k = 0;
+            if (cudaOccupancyMaxActiveClusters(&k, kern, &cfg) != cudaSuccess) k = 0;
+            n[c] = k;
+        }
+        cudaGetLastError();
     });
-    if (attr_err != cudaSuccess) return attr_err;
+    return n;
+}
+
+// Cluster size: the c minimising (waves of clusters) x (stages per CTA),
+// the smaller c on ties.
+template <int BITS, int D, int GROUP>
+int attn_pick_cluster(int64_t KV, int64_t N) {
+    const int *n = attn_active_clusters<BITS, D, GROUP>();
+    const int64_t maxc = std::min<int64_t>(16, std::max<int64_t>(1, (N + kStageRows - 1) / kStageRows));
+    int best = 1;
+    int64_t best_cost = INT64_MAX;
+    for (int c = 1; c <= maxc; ++c) {
+        if (n[c] < 1) continue;
+        const int64_t waves = (KV + n[c] - 1) / n[c];
+        const int64_t block = ((N + c - 1) / c + kTile - 1) / kTile * kTile;
+        const int64_t cost = waves * ((block + kStageRows - 1) / kStageRows);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = c;
+        }
+    }
+    return best;
+}
+
+struct AttnLaunch {
+    int dtype;
+    const void *q;
+    const uint32_t *kw, *vw;
+    const void *ks, *kb, *vs, *vb;
+    void *out;
+    int64_t H, KV, N;
+    cudaStream_t stream;
+};
+
+template <int BITS, int D, int GROUP>
+cudaError_t attn_run(const AttnLaunch &L, int *cluster_out) {
+    using S = Shape<BITS, D, GROUP>;
+    const int C = attn_pick_cluster<BITS, D, GROUP>(L.KV, L.N);
+    if (cluster_out) {
+        *cluster_out = C;
+        return cudaSuccess;
+    }
+    AttnParams prm;
+    prm.q = L.q;
+    prm.vs = static_cast<const __half *>(L.vs);
+    prm.out = L.out;
+    void *err = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&err, g_attn_error);
+    if (e != cudaSuccess) return e;
+    prm.err = static_cast<uint32_t *>(err);
+    prm.KV = (int)L.KV;
+    prm.N = (int)L.N;
+    prm.nrep = (int)(L.H / L.KV);
+    prm.csize = C;
+    prm.block = (int)(((L.N + C - 1) / C + kTile - 1) / kTile * kTile);
+    const int nst = (prm.block + kStageRows - 1) / kStageRows;
+    prm.stages = std::max(1, std::min(attn_max_stages<BITS, D, GROUP>(), nst));
+    prm.bf16 = L.dtype == AQ_BF16;
+
+    const uint64_t rows = (uint64_t)(L.KV * L.N);
+    const CUtensorMapSwizzle swz = S::kW == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                   : S::kW == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                 : CU_TENSOR_MAP_SWIZZLE_32B;
+    CUtensorMap m[6];
+    if (!tmap_2d(&m[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, L.kw, S::kRB, rows, S::kRB, S::kW,
+                 kStageRows, swz) ||
+        !tmap_2d(&m[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, L.vw, S::kRB, rows, S::kRB, S::kW,
+                 kStageRows, swz))
+        return cudaErrorInvalidValue;
+    const void *sp[4] = {L.ks, L.kb, L.vs, L.vb};
+    for (int i = 0; i < 4; ++i) {
+        const uint64_t dims[1] = {rows * S::kG};
+        const uint32_t box[1] = {(uint32_t)S::kSBox};
+        if (!tmap_encode(&m[2 + i], CU_TENSOR_MAP_DATA_TYPE_UINT16, 1, sp[i], dims, nullptr, box,
+                         CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+    }
+    auto kern = attn_kernel<BITS, D, GROUP>;
+    attn_active_clusters<BITS, D, GROUP>();  // sets the kernel attributes
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(prm.KV * prm.csize), 1, 1);
+    cfg.gridDim = dim3((unsigned)(L.KV * C), 1, 1);
     cfg.blockDim = dim3(kAttnThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
+    cfg.dynamicSmemBytes = attn_smem_t<BITS, D, GROUP>(prm.stages, prm.nrep);
+    cfg.stream = L.stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)prm.csize;
+    attr[0].val.clusterDim.x = (unsigned)C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, prm);
+    return cudaLaunchKernelEx(&cfg, kern, prm, m[0], m[1], m[2], m[3], m[4], m[5]);
 }
 
-template <int BITS, int E, bool BF16>
-cudaError_t attn_nrep(int nrep, const AttnParams &prm, cudaStream_t s) {
-    switch (nrep) {
-        case 1: return attn_launch_t<BITS, E, 1, BF16>(prm, s);
-        case 2: return attn_launch_t<BITS, E, 2, BF16>(prm, s);
-        case 4: return attn_launch_t<BITS, E, 4, BF16>(prm, s);
-        default: return attn_launch_t<BITS, E, 8, BF16>(prm, s);
+template <int BITS, int D>
+cudaError_t attn_group(int group, const AttnLaunch &L, int *c) {
+    if constexpr (D == 64) {
+        return group == 32 ? attn_run<BITS, D, 32>(L, c) : attn_run<BITS, D, 64>(L, c);
+    } else {
+        return group == 32   ? attn_run<BITS, D, 32>(L, c)
+               : group == 64 ? attn_run<BITS, D, 64>(L, c)
+                             : attn_run<BITS, D, 128>(L, c);
     }
 }
 
-template <int BITS, bool BF16>
-cudaError_t attn_d(int D, int nrep, const AttnParams &prm, cudaStream_t s) {
+template <int BITS>
+cudaError_t attn_dim(int64_t D, int group, const AttnLaunch &L, int *c) {
     switch (D) {
-        case 64: return attn_nrep<BITS, 2, BF16>(nrep, prm, s);
-        case 128: return attn_nrep<BITS, 4, BF16>(nrep, prm, s);
-        default: return attn_nrep<BITS, 8, BF16>(nrep, prm, s);
+        case 64: return attn_group<BITS, 64>(group, L, c);
+        case 128: return attn_group<BITS, 128>(group, L, c);
+        default: return attn_group<BITS, 256>(group, L, c);
     }
+}
+
+cudaError_t attn_dispatch(int64_t D, int bits, int group, const AttnLaunch &L, int *c) {
+    return bits == 4 ? attn_dim<4>(D, group, L, c) : attn_dim<8>(D, group, L, c);
 }
 
 }  // namespace
 
 bool attention_supported(int64_t H, int64_t KV, int64_t N, int64_t D, int bits, int group) {
-    if (H < 1 || KV < 1 || H % KV != 0 || N < 1 || N > INT32_MAX / 2) return false;
+    if (H < 1 || KV < 1 || H % KV != 0 || N < 1) return false;
     const int64_t nrep = H / KV;
     if (nrep != 1 && nrep != 2 && nrep != 4 && nrep != 8) return false;
     if (D != 64 && D != 128 && D != 256) return false;
     if (bits != 4 && bits != 8) return false;
     if (group != 32 && group != 64 && group != 128) return false;
-    if (D % group != 0 || group < D / 32) return false;
-    return KV * N <= INT32_MAX / 2;
+    if (D % group != 0) return false;
+    // row and scale-element indices stay in int
+    return KV * N <= INT32_MAX / 16 && KV * N * (D / group) <= INT32_MAX / 2;
 }
 
-// Cluster size: enough CTAs to cover the SMs (one KV head per cluster, up to
-// 16 blocks of at least 64 rows).
-int attention_cluster(int64_t KV, int64_t N) {
-    const int64_t want = (num_sms() + KV - 1) / KV;
-    const int64_t by_rows = (N + 63) / 64;
-    return (int)std::max<int64_t>(1, std::min<int64_t>({16, want, by_rows}));
+int attention_cluster(int64_t KV, int64_t N, int64_t D, int bits, int group) {
+    AttnLaunch L = {};
+    L.KV = KV;
+    L.N = N;
+    int c = 0;
+    if (attn_dispatch(D, bits, group, L, &c) != cudaSuccess) return 0;
+    return c;
 }
 
 cudaError_t attention_launch(int dtype, const void *q, const uint32_t *kw, const void *ks,
                              const void *kb, const uint32_t *vw, const void *vs, const void *vb,
                              int64_t H, int64_t KV, int64_t N, int64_t D, int bits, int group,
                              void *out, cudaStream_t stream) {
-    AttnParams prm;
-    prm.q = q;
-    prm.kw = reinterpret_cast<const uint8_t *>(kw);
-    prm.vw = reinterpret_cast<const uint8_t *>(vw);
-    prm.ks = static_cast<const __half *>(ks);
-    prm.kb = static_cast<const __half *>(kb);
-    prm.vs = static_cast<const __half *>(vs);
-    prm.vb = static_cast<const __half *>(vb);
-    prm.out = out;
-    prm.H = (int)H;
-    prm.KV = (int)KV;
-    prm.N = (int)N;
-    prm.D = (int)D;
-    prm.group = group;
-    prm.csize = attention_cluster(KV, N);
-    prm.block = (int)((N + prm.csize - 1) / prm.csize);
-    prm.row_bytes = (int)(D * bits / 8);
-    const int nrep = (int)(H / KV);
-    const bool bf = dtype == AQ_BF16;
-    if (bits == 4)
-        return bf ? attn_d<4, true>((int)D, nrep, prm, stream)
-                  : attn_d<4, false>((int)D, nrep, prm, stream);
-    return bf ? attn_d<8, true>((int)D, nrep, prm, stream)
-              : attn_d<8, false>((int)D, nrep, prm, stream);
+    const AttnLaunch L = {dtype, q, kw, vw, ks, kb, vs, vb, out, H, KV, N, stream};
+    return attn_dispatch(D, bits, group, L, nullptr);
+}
+
+cudaError_t attn_read_error(uint32_t *code, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(code, g_attn_error, sizeof(uint32_t));
+    if (e != cudaSuccess || !clear) return e;
+    const uint32_t zero = 0;
+    return cudaMemcpyToSymbol(g_attn_error, &zero, sizeof(uint32_t));
 }
 
 }  // namespace aq

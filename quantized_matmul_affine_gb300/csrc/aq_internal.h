@@ -45,6 +45,8 @@ enum : uint32_t {
     ERR_GEMV_FULL = 0x0103,
     ERR_GEMV_EMPTY = 0x0203,
     ERR_GEMV_DRAIN = 0x0303,
+    ERR_ATTN_FULL = 0x0104,
+    ERR_ATTN_EMPTY = 0x0204,
 };
 
 // Each returns cudaSuccess, or the launch error.  `supported` reports
@@ -78,7 +80,8 @@ cudaError_t quantize_launch_g(int dtype, const void *w, int64_t N, int64_t K, in
                               uint32_t *words, void *scales, void *biases, cudaStream_t stream);
 bool generic_supported_g(const MatmulArgs &a, int group);
 bool attention_supported(int64_t H, int64_t KV, int64_t N, int64_t D, int bits, int group);
-int attention_cluster(int64_t KV, int64_t N);
+// Cluster size (CTAs per KV head) the launch would use; 0 if unsupported.
+int attention_cluster(int64_t KV, int64_t N, int64_t D, int bits, int group);
 cudaError_t attention_launch(int dtype, const void *q, const uint32_t *kw, const void *ks,
                              const void *kb, const uint32_t *vw, const void *vs, const void *vb,
                              int64_t H, int64_t KV, int64_t N, int64_t D, int bits, int group,
@@ -91,6 +94,7 @@ cudaError_t pack_launch(const uint8_t *codes, int64_t N, int64_t K, int bits, ui
 cudaError_t gemv_read_error(uint32_t *code, bool clear);
 cudaError_t qmv_read_error(uint32_t *code, bool clear);
 cudaError_t tc_read_error(uint32_t *code, bool clear);
+cudaError_t attn_read_error(uint32_t *code, bool clear);
 
 // A tiled TMA tensor map of `rank` dimensions (dims[0] innermost, strides
 // in bytes of dims 1..rank-1), box `box`, out-of-range elements read as

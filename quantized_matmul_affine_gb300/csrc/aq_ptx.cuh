@@ -227,6 +227,15 @@ namespace aq {
 // ---------------------------------------------------------------------------
 // TMA tiled loads (tensor map in kernel parameter space).
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void tma_load_1d(void *dst_smem, const void *tmap, int c0,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.1d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2}], [%3];" ::"r"(smem_u32(dst_smem)),
+        "l"(tmap), "r"(c0), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(void *dst_smem, const void *tmap, int c0, int c1,
                                             uint64_t *bar) {
     asm volatile(
