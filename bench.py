@@ -836,6 +836,7 @@ def run_attention(args, rank, world, local_rank):
                    "l2": f"cold: {copies} rotating cache copies > 2x L2 ({l2 / 1e6:.0f} MB)",
                    "timing": f"CUDA events on the launching stream around {reps} replays of a "
                              f"CUDA graph of {chunk} calls",
+                   "launch": aq.aq_attention_describe(H, KV, N, D, bits, group),
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm,
                      "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,

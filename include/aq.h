@@ -195,6 +195,19 @@ aq_status aq_attention_decode(int dtype, const void *q_dev, const uint32_t *k_wo
                               const void *v_biases_dev, int64_t H, int64_t KV, int64_t N,
                               int64_t D, int bits, int group_size, void *out_dev, void *stream);
 
+/*
+ * aq_attention_describe — one line naming the geometry aq_attention_decode
+ * launches for these sizes: "attn cluster=C block=R stages=S smem=B grid=G"
+ * (C CTAs per KV head, R cached rows per CTA, S stages in the shared-memory
+ * ring, B bytes of dynamic shared memory).  Queries the current device for
+ * co-resident clusters; "no device" without one, "unsupported" or "invalid
+ * arguments" for sizes aq_attention_decode would refuse.  Writes at most
+ * buflen bytes (NUL-terminated) to the host buffer and returns the length it
+ * wanted (as snprintf), or -1 if buf is NULL or buflen < 1.
+ */
+int aq_attention_describe(int64_t H, int64_t KV, int64_t N, int64_t D, int bits, int group_size,
+                          char *buf, int buflen);
+
 /* Largest number of projections aq_matmul_multi takes in one call. */
 #define AQ_MAX_PROJ 4
 

@@ -24,7 +24,7 @@ __all__ = [
     "AqError", "AQ_F16", "AQ_BF16", "AQ_VARIANT_AUTO", "AQ_VARIANT_GENERIC", "AQ_VARIANT_QMV",
     "AQ_VARIANT_TC", "AQ_VARIANT_GEMV", "AQ_VARIANT_TCW", "AQ_NUM_VARIANTS", "aq_pack", "aq_quantize",
     "aq_quantize_bf16", "aq_matmul", "aq_matmul_bf16", "aq_matmul_multi", "aq_matmul_gate_up",
-    "aq_matmul_ex", "aq_quantize_ex", "aq_attention_decode",
+    "aq_matmul_ex", "aq_quantize_ex", "aq_attention_decode", "aq_attention_describe",
     "aq_matmul_variant", "aq_matmul_host", "aq_select", "aq_describe", "aq_stats", "aq_device_error",
     "aq_free", "aq_status_string", "aq_variant_name", "aq_version", "lib_path", "load",
 ]
@@ -77,6 +77,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "aq_matmul_host": ([i32, p, p, p, p, i64, i64, i64, i32, p, p, p, p], i32),
         "aq_select": ([i64, i64, i64, i32, i32], i32),
         "aq_describe": ([i64, i64, i64, i32, i32, p, i32], i32),
+        "aq_attention_describe": ([i64, i64, i64, i64, i32, i32, p, i32], i32),
         "aq_stats": ([p, i32, i32], i32),
         "aq_device_error": ([u32p, i32], i32),
         "aq_free": ([], None),
@@ -305,6 +306,14 @@ def aq_select(M: int, N: int, K: int, bits: int, dtype: int = AQ_F16) -> int:
 def aq_describe(M: int, N: int, K: int, bits: int, dtype: int = AQ_F16) -> str:
     buf = ctypes.create_string_buffer(256)
     load().aq_describe(M, N, K, bits, dtype, ctypes.addressof(buf), 256)
+    return buf.value.decode()
+
+
+def aq_attention_describe(H: int, KV: int, N: int, D: int, bits: int, group_size: int) -> str:
+    """The launch geometry of aq_attention_decode for these sizes (needs the
+    device for its count of co-resident clusters)."""
+    buf = ctypes.create_string_buffer(256)
+    load().aq_attention_describe(H, KV, N, D, bits, group_size, ctypes.addressof(buf), 256)
     return buf.value.decode()
 
 

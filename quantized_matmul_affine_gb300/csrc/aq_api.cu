@@ -442,6 +442,15 @@ int aq_describe(int64_t M, int64_t N, int64_t K, int bits, int dtype, char *buf,
     }
 }
 
+int aq_attention_describe(int64_t H, int64_t KV, int64_t N, int64_t D, int bits, int group_size,
+                          char *buf, int buflen) {
+    if (!buf || buflen < 1) return -1;
+    if (H < 1 || KV < 1 || N < 1 || H % KV != 0) return snprintf(buf, buflen, "invalid arguments");
+    if (!attention_supported(H, KV, N, D, bits, group_size))
+        return snprintf(buf, buflen, "unsupported");
+    return attention_describe(H, KV, N, D, bits, group_size, buf, buflen);
+}
+
 aq_status aq_stats(uint64_t *calls, int n, int reset) {
     if (n < 0 || (n > 0 && !calls)) return AQ_ERR_INVALID_ARG;
     for (int v = 0; v < AQ_NUM_VARIANTS; ++v) {

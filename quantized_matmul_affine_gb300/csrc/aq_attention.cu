@@ -23,8 +23,9 @@
 //     at bit 4), q' = q * 2^e per head in fp16; one m16n8k16 chain per group,
 //     then s = scale * sum(q code) + bias * sum(q) in fp32.
 //   * Online softmax in base 2 on the fragment; the probabilities, times the
-//     value scale of their row and group (and 2^ev, a per-CTA power of two
-//     that keeps them in the fp16 normal range), are transposed in registers
+//     value scale of their row and group (and 2^ev, a per-warp power of two
+//     lowered as larger scales appear, which keeps them in the fp16 range
+//     and mostly out of its subnormals), are transposed in registers
 //     (movmatrix) into the B operand of O^T[d][heads] += codes^T x P'; the
 //     value biases enter as sum(p * bias) per (head, group) in fp32.
 //   * The warps' (max, sum, o) merge through shared memory in warp order, the
@@ -36,6 +37,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <cstdio>
 #include <mutex>
 
 namespace aq {
@@ -54,7 +56,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct AttnParams {
     const void *q;
-    const __half *vs;   // value scales, read once for the CTA's power of two
     void *out;
     uint32_t *err;
     int KV, N, nrep;
@@ -258,15 +259,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if (lane == 0) qs2[h * G + g] = sum * kLog2e;
             }
             if (lane == 0) qsc[h] = pow2i(24 - e) * kLog2e;
-
-            // the CTA's largest value scale
-            float vm = 0.f;
-            const long long v0 = (row_base + n0) * G, v1 = (row_base + n1) * G;
-            for (long long i = v0 + threadIdx.x; i < v1; i += kCWarps * 32)
-                vm = fmaxf(vm, fabsf(__half2float(p.vs[i])));
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) vm = fmaxf(vm, __shfl_xor_sync(~0u, vm, off));
-            if (lane == 0) red[warp] = vm;
         }
         consumer_sync();
         // B fragments of q': k-step k of group g, lane (gid, t) = head gid,
@@ -294,16 +286,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             qfrag[k * 32 + lane] = make_uint2(r[0], r[1]);
         }
-        float vmax = 0.f;
-#pragma unroll
-        for (int w = 0; w < kCWarps; ++w) vmax = fmaxf(vmax, red[w]);
-        const int ev = exp_for(vmax);
-        const float vsc = pow2i(ev);
         const float qsc0 = qsc[2 * t], qsc1 = qsc[2 * t + 1];
         consumer_sync();
 
         // ------------------------------------------------------------ main loop
         float m2[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+        // p * scale * 2^ev enters the value product: ev keeps the largest
+        // |scale| seen so far below 2^15 (fp16 range, few subnormals); it only
+        // decreases, and O is rescaled with it like with the running max
+        int ev = 127;
         float bt[2][G];
         float O[D / 16][4];
 #pragma unroll
@@ -397,13 +388,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                      exp2f(s[3] - mn1)};
                 l[0] = fmaf(l[0], f0, pr[0] + pr[2]);
                 l[1] = fmaf(l[1], f1, pr[1] + pr[3]);
-                if (__any_sync(~0u, f0 != 1.f || f1 != 1.f)) {
+                float vsa[G], vsb[G];
+                float vmx = 0.f;
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    vsa[g] = __half2float(svs[ra * G + g]);
+                    vsb[g] = __half2float(svs[rb * G + g]);
+                    vmx = fmaxf(vmx, fmaxf(fabsf(vsa[g]), fabsf(vsb[g])));
+                }
+#pragma unroll
+                for (int off = 4; off <= 16; off <<= 1)
+                    vmx = fmaxf(vmx, __shfl_xor_sync(~0u, vmx, off));
+                const int ev_new = min(ev, exp_for(vmx));
+                const float r = ev_new - ev < -126 ? 0.f : pow2i(ev_new - ev);
+                ev = ev_new;
+                const float vsc = pow2i(ev);
+                if (__any_sync(~0u, f0 != 1.f || f1 != 1.f || r != 1.f)) {
+                    const float o0 = f0 * r, o1 = f1 * r;
 #pragma unroll
                     for (int i = 0; i < D / 16; ++i) {
-                        O[i][0] *= f0;
-                        O[i][1] *= f1;
-                        O[i][2] *= f0;
-                        O[i][3] *= f1;
+                        O[i][0] *= o0;
+                        O[i][1] *= o1;
+                        O[i][2] *= o0;
+                        O[i][3] *= o1;
                     }
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
@@ -416,14 +423,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const int va0 = tr + 2 * t, va1 = va0 + 1, va8 = va0 + 8, va9 = va0 + 9;
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    const float vsa = __half2float(svs[ra * G + g]) * vsc;
-                    const float vsb = __half2float(svs[rb * G + g]) * vsc;
+                    const float vsa_ = vsa[g] * vsc, vsb_ = vsb[g] * vsc;
                     const float vba = __half2float(svb[ra * G + g]);
                     const float vbb = __half2float(svb[rb * G + g]);
                     bt[0][g] = fmaf(pr[0], vba, fmaf(pr[2], vbb, bt[0][g]));
                     bt[1][g] = fmaf(pr[1], vba, fmaf(pr[3], vbb, bt[1][g]));
-                    const uint32_t b0 = movmatrix_t(pack_half2(pr[0] * vsa, pr[1] * vsa));
-                    const uint32_t b1 = movmatrix_t(pack_half2(pr[2] * vsb, pr[3] * vsb));
+                    const uint32_t b0 = movmatrix_t(pack_half2(pr[0] * vsa_, pr[1] * vsa_));
+                    const uint32_t b1 = movmatrix_t(pack_half2(pr[2] * vsb_, pr[3] * vsb_));
                     constexpr int NW = S::kCV >= 4 ? S::kCV / 4 : 1;
                     uint32_t w0[NW], w1[NW], w8[NW], w9[NW];
                     const int byte = g * S::kGB + gid * S::kCV;
@@ -475,7 +481,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         float *wm = reinterpret_cast<float *>(ring);       // [warps][nrep]
         float *wl = wm + kCWarps * nrep;                   // [warps][nrep]
         float *wo = wl + kCWarps * nrep;                   // [warps][nrep][D]
-        const float fa = pow2i(24 - ev), fb = BITS == 4 ? pow2i(20 - ev) : fa;
+        const int evf = ev == 127 ? 0 : ev;  // a warp without rows holds zeros
+        const float fa = pow2i(24 - evf), fb = BITS == 4 ? pow2i(20 - evf) : fa;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             const int h = 2 * t + hh;
@@ -533,19 +540,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     for (int i = rank * chunk + (int)threadIdx.x; i < min(total, (rank + 1) * chunk);
          i += kAttnThreads) {
         const int j = i / D, d = i - j * D;
-        float M = -INFINITY;
-        for (int rr = 0; rr < C; ++rr)
-            M = fmaxf(M, C > 1 ? ld_dsmem_f32(map_to_rank(bm + 4u * j, (uint32_t)rr)) : cm[j]);
         float L = 0.f, Ov = 0.f;
-        for (int rr = 0; rr < C; ++rr) {
-            const float mr = C > 1 ? ld_dsmem_f32(map_to_rank(bm + 4u * j, (uint32_t)rr)) : cm[j];
-            if (mr == -INFINITY) continue;  // a block with no rows
-            const float g = exp2f(mr - M);
-            const float lr = C > 1 ? ld_dsmem_f32(map_to_rank(bl + 4u * j, (uint32_t)rr)) : cl[j];
-            const float orr =
-                C > 1 ? ld_dsmem_f32(map_to_rank(bo + 4u * (uint32_t)i, (uint32_t)rr)) : co[i];
-            L = fmaf(lr, g, L);
-            Ov = fmaf(orr, g, Ov);
+        if (C == 1) {
+            L = cl[j];
+            Ov = co[i];
+        } else {
+            // every rank's (max, sum, o) loaded at once, then folded in rank order
+            float mr[16], lr[16], orr[16];
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr)
+                if (rr < C) {
+                    mr[rr] = ld_dsmem_f32(map_to_rank(bm + 4u * j, (uint32_t)rr));
+                    lr[rr] = ld_dsmem_f32(map_to_rank(bl + 4u * j, (uint32_t)rr));
+                    orr[rr] = ld_dsmem_f32(map_to_rank(bo + 4u * (uint32_t)i, (uint32_t)rr));
+                }
+            float M = -INFINITY;
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr)
+                if (rr < C) M = fmaxf(M, mr[rr]);
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr)
+                if (rr < C && mr[rr] != -INFINITY) {  // a block with no rows adds nothing
+                    const float g = exp2f(mr[rr] - M);
+                    L = fmaf(lr[rr], g, L);
+                    Ov = fmaf(orr[rr], g, Ov);
+                }
         }
         const float v = Ov / L;
         const size_t oi = (size_t)(kv * nrep + j) * D + d;
@@ -625,6 +644,11 @@ int attn_pick_cluster(int64_t KV, int64_t N) {
     return best;
 }
 
+struct AttnPlan {
+    int cluster, block, stages;
+    size_t smem;
+};
+
 struct AttnLaunch {
     int dtype;
     const void *q;
@@ -636,16 +660,11 @@ struct AttnLaunch {
 };
 
 template <int BITS, int D, int GROUP>
-cudaError_t attn_run(const AttnLaunch &L, int *cluster_out) {
+cudaError_t attn_run(const AttnLaunch &L, AttnPlan *plan) {
     using S = Shape<BITS, D, GROUP>;
     const int C = attn_pick_cluster<BITS, D, GROUP>(L.KV, L.N);
-    if (cluster_out) {
-        *cluster_out = C;
-        return cudaSuccess;
-    }
     AttnParams prm;
     prm.q = L.q;
-    prm.vs = static_cast<const __half *>(L.vs);
     prm.out = L.out;
     void *err = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&err, g_attn_error);
@@ -659,6 +678,10 @@ cudaError_t attn_run(const AttnLaunch &L, int *cluster_out) {
     const int nst = (prm.block + kStageRows - 1) / kStageRows;
     prm.stages = std::max(1, std::min(attn_max_stages<BITS, D, GROUP>(), nst));
     prm.bf16 = L.dtype == AQ_BF16;
+    if (plan) {
+        *plan = {C, prm.block, prm.stages, attn_smem_t<BITS, D, GROUP>(prm.stages, prm.nrep)};
+        return cudaSuccess;
+    }
 
     const uint64_t rows = (uint64_t)(L.KV * L.N);
     const CUtensorMapSwizzle swz = S::kW == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
@@ -696,7 +719,7 @@ cudaError_t attn_run(const AttnLaunch &L, int *cluster_out) {
 }
 
 template <int BITS, int D>
-cudaError_t attn_group(int group, const AttnLaunch &L, int *c) {
+cudaError_t attn_group(int group, const AttnLaunch &L, AttnPlan *c) {
     if constexpr (D == 64) {
         return group == 32 ? attn_run<BITS, D, 32>(L, c) : attn_run<BITS, D, 64>(L, c);
     } else {
@@ -707,7 +730,7 @@ cudaError_t attn_group(int group, const AttnLaunch &L, int *c) {
 }
 
 template <int BITS>
-cudaError_t attn_dim(int64_t D, int group, const AttnLaunch &L, int *c) {
+cudaError_t attn_dim(int64_t D, int group, const AttnLaunch &L, AttnPlan *c) {
     switch (D) {
         case 64: return attn_group<BITS, 64>(group, L, c);
         case 128: return attn_group<BITS, 128>(group, L, c);
@@ -715,7 +738,7 @@ cudaError_t attn_dim(int64_t D, int group, const AttnLaunch &L, int *c) {
     }
 }
 
-cudaError_t attn_dispatch(int64_t D, int bits, int group, const AttnLaunch &L, int *c) {
+cudaError_t attn_dispatch(int64_t D, int bits, int group, const AttnLaunch &L, AttnPlan *c) {
     return bits == 4 ? attn_dim<4>(D, group, L, c) : attn_dim<8>(D, group, L, c);
 }
 
@@ -733,13 +756,16 @@ bool attention_supported(int64_t H, int64_t KV, int64_t N, int64_t D, int bits, 
     return KV * N <= INT32_MAX / 16 && KV * N * (D / group) <= INT32_MAX / 2;
 }
 
-int attention_cluster(int64_t KV, int64_t N, int64_t D, int bits, int group) {
+int attention_describe(int64_t H, int64_t KV, int64_t N, int64_t D, int bits, int group,
+                       char *buf, int len) {
     AttnLaunch L = {};
+    L.H = H;
     L.KV = KV;
     L.N = N;
-    int c = 0;
-    if (attn_dispatch(D, bits, group, L, &c) != cudaSuccess) return 0;
-    return c;
+    AttnPlan pl = {};
+    if (attn_dispatch(D, bits, group, L, &pl) != cudaSuccess) return snprintf(buf, len, "no device");
+    return snprintf(buf, len, "attn cluster=%d block=%d stages=%d smem=%zu grid=%lld", pl.cluster,
+                    pl.block, pl.stages, pl.smem, (long long)(KV * pl.cluster));
 }
 
 cudaError_t attention_launch(int dtype, const void *q, const uint32_t *kw, const void *ks,

@@ -80,8 +80,9 @@ cudaError_t quantize_launch_g(int dtype, const void *w, int64_t N, int64_t K, in
                               uint32_t *words, void *scales, void *biases, cudaStream_t stream);
 bool generic_supported_g(const MatmulArgs &a, int group);
 bool attention_supported(int64_t H, int64_t KV, int64_t N, int64_t D, int bits, int group);
-// Cluster size (CTAs per KV head) the launch would use; 0 if unsupported.
-int attention_cluster(int64_t KV, int64_t N, int64_t D, int bits, int group);
+// The launch geometry aq_attention_decode would use (snprintf semantics).
+int attention_describe(int64_t H, int64_t KV, int64_t N, int64_t D, int bits, int group,
+                       char *buf, int len);
 cudaError_t attention_launch(int dtype, const void *q, const uint32_t *kw, const void *ks,
                              const void *kb, const uint32_t *vw, const void *vs, const void *vb,
                              int64_t H, int64_t KV, int64_t N, int64_t D, int bits, int group,

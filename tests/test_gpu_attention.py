@@ -30,11 +30,13 @@ def _device():
     yield
 
 
-def _cache(rng, KV, N, D, bits, group):
+def _cache(rng, KV, N, D, bits, group, ramp=0.0):
     R = KV * N
     codes = rng.integers(0, 1 << bits, size=(R, D)).astype(np.uint8)
     c = 0.16 / (1 << bits)
-    s = (np.abs(rng.standard_normal((R, D // group))) * c + 1e-3).astype(np.float16)
+    # ramp > 0: scales grow by 2^ramp from the first cached row to the last
+    grow = 2.0 ** (ramp * (np.arange(R) % N) / max(1, N - 1))[:, None]
+    s = ((np.abs(rng.standard_normal((R, D // group))) * c + 1e-3) * grow).astype(np.float16)
     b = (-(1 << (bits - 1)) * s.astype(np.float64) + rng.standard_normal((R, D // group)) * 1e-3
          ).astype(np.float16)
     return codes, s, b
@@ -46,17 +48,18 @@ def _dev_cache(codes, s, b, KV, N, D, bits):
             torch.from_numpy(b).cuda().view(KV, N, -1))
 
 
-def _case(H, KV, N, D, bits, group, dtype, seed, qscale=2.0):
+def _case(H, KV, N, D, bits, group, dtype, seed, qscale=2.0, ramp=0.0):
     rng = np.random.default_rng(seed)
     kc, ks, kb = _cache(rng, KV, N, D, bits, group)
-    vc, vs, vb = _cache(rng, KV, N, D, bits, group)
+    vc, vs, vb = _cache(rng, KV, N, D, bits, group, ramp)
     qf = (rng.standard_normal((H, D)) * qscale).astype(np.float32)
     q_bits = workloads.f32_to_bf16_bits(qf) if dtype == "bf16" else workloads.f32_to_fp16_bits(qf)
     return (kc, ks, kb), (vc, vs, vb), q_bits
 
 
-def _check(H, KV, N, D, bits, group, dtype, seed, qscale=2.0):
-    (kc, ks, kb), (vc, vs, vb), q_bits = _case(H, KV, N, D, bits, group, dtype, seed, qscale)
+def _check(H, KV, N, D, bits, group, dtype, seed, qscale=2.0, ramp=0.0):
+    (kc, ks, kb), (vc, vs, vb), q_bits = _case(H, KV, N, D, bits, group, dtype, seed, qscale,
+                                               ramp)
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
     q = torch.from_numpy(q_bits.view(np.int16)).cuda().view(tdt)
     o = aq.aq_attention_decode(q, _dev_cache(kc, ks, kb, KV, N, D, bits),
@@ -98,6 +101,22 @@ def test_attention_parity(H, KV, N, D, bits, group, dtype):
 def test_attention_sharp_softmax():
     # large scores: one row dominates each head
     _check(8, 4, 333, 128, 8, 64, "bf16", seed=9, qscale=40.0)
+
+
+@pytest.mark.parametrize("ramp", [12.0, -12.0])
+def test_attention_value_scale_range(ramp):
+    # value scales over 4096x from the first row to the last (or back): the
+    # fp16 headroom exponent of each warp is lowered as larger scales appear
+    _check(8, 2, 3000, 128, 4, 64, "bf16", seed=11, ramp=ramp)
+
+
+def test_attention_describe():
+    d = aq.aq_attention_describe(16, 8, 8192, 256, 4, 64)
+    fields = dict(kv.split("=") for kv in d.split()[1:])
+    assert d.startswith("attn ") and 1 <= int(fields["cluster"]) <= 16
+    assert int(fields["block"]) * int(fields["cluster"]) >= 8192 and int(fields["block"]) % 16 == 0
+    assert int(fields["grid"]) == 8 * int(fields["cluster"])
+    assert aq.aq_attention_describe(16, 8, 8192, 96, 4, 32) == "unsupported"
 
 
 def test_attention_workload_shape():
