@@ -14,12 +14,14 @@
 //     merged in rank order through distributed shared memory - no global
 //     scratch, no second launch.  The cluster size is picked from the
 //     driver's count of co-resident clusters.
-//   * A producer warp streams 128-row stages of K and V codes (2-D TMA,
+//   * A producer warp streams 256-row stages (128 when a row is 256 bytes)
+//     of K and V codes (2-D TMA,
 //     swizzled so that the fragment reads below are free of bank conflicts)
 //     and their scales and biases (1-D TMA) into a shared-memory ring.
-//   * Each of 8 consumer warps takes a 16-row tile of a stage.  Scores on the
-//     tensor cores: S^T-free form S[16 rows][8 heads] = codes x q', the codes
-//     as the exact fp16 subnormals code * 2^-24 (or 2^-20 where a nibble sits
+//   * Each of 8 consumer warps takes a tile of two 16-row blocks of a stage
+//     (one block when a row is 256 bytes).  Scores on the tensor cores, per
+//     block S[16 rows][8 heads] = codes x q', the codes as the exact fp16
+//     subnormals code * 2^-24 (or 2^-20 where a nibble sits
 //     at bit 4), q' = q * 2^e per head in fp16; one m16n8k16 chain per group,
 //     then s = scale * sum(q code) + bias * sum(q) in fp32.
 //   * Online softmax in base 2 on the fragment; the probabilities, times the
@@ -30,6 +32,9 @@
 //     value biases enter as sum(p * bias) per (head, group) in fp32.
 //   * The warps' (max, sum, o) merge through shared memory in warp order, the
 //     cluster's CTAs then in rank order; o is rounded once.
+//   * Launched with programmatic stream serialisation: the next kernel may
+//     launch onto the SMs this grid leaves free, and this grid's first reads
+//     wait for the previous grid.
 #include "aq_internal.h"
 #include "aq_ptx.cuh"
 
@@ -46,12 +51,15 @@ __device__ uint32_t g_attn_error;
 
 namespace {
 
-constexpr int kCWarps = 8;                           // consumer warps
+// kSplit = 2 gives each tile to a pair of warps, each taking half of the head
+// dimension (more warps, but partial scores cross shared memory every tile);
+// measured slower on GB300 than one warp per tile, so kSplit = 1.
+constexpr int kSplit = 1;
+constexpr int kPairs = kSplit == 2 ? 6 : 8;          // warp tiles per stage
+constexpr int kCWarps = kSplit * kPairs;             // consumer warps
 constexpr int kAttnThreads = (kCWarps + 1) * 32;     // + the TMA producer warp
-constexpr int kTile = 16;                            // rows per warp tile
-constexpr int kStageRows = kTile * kCWarps;          // 128
 constexpr int kMaxStages = 8;
-constexpr int kRingBudget = 192 * 1024;
+constexpr int kRingBudget = 160 * 1024;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct AttnParams {
@@ -76,9 +84,19 @@ struct Shape {
     static constexpr int kCK = kGB / 4;                 // bytes a lane takes per row (scores)
     static constexpr int kCV = kGB / 8;                 // bytes a lane takes per row (values)
     static constexpr int kSteps = GROUP / 16;           // k-steps / M-tiles per group
-    static constexpr int kRegs = GROUP / 8;             // code registers per row per group
-    // scales: 128 rows x G halves from a 16-byte aligned start (up to 7
-    // before), in boxes of a multiple of 64 halves so that every box lands
+    // 16-row blocks a warp takes per stage: two (32 rows) unless a row is 256
+    // bytes, where a 256-row stage would leave room for only one in the ring
+    static constexpr int kRBk = kRB <= 128 ? 2 : 1;
+    static constexpr int kTileRows = 16 * kRBk;
+    static constexpr int kStageRows = kTileRows * kPairs;
+    // with kSplit = 2 each warp of a pair takes half of the head dimension's
+    // 16-wide units (k-steps of the scores, M-tiles of the values): whole
+    // groups when there are several, else half of the one group's steps
+    static constexpr int kGH = kSplit == 1 ? kG : kG >= 2 ? kG / 2 : 1;  // groups per warp
+    static constexpr int kHS = kSplit == 1 || kG >= 2 ? kSteps : kSteps / 2;  // steps per group
+    static constexpr int kHU = kGH * kHS;               // units per warp (D / 16 / kSplit)
+    // scales: kStageRows rows x G halves from a 16-byte aligned start (up to
+    // 7 before), in boxes of a multiple of 64 halves so that every box lands
     // on a 128-byte boundary of shared memory (the tensor-copy rule)
     static constexpr int kSH = kStageRows * kG + 8;
     static constexpr int kSBoxes = (kSH + 255) / 256;
@@ -96,7 +114,7 @@ struct Shape {
 template <class S>
 __device__ __forceinline__ uint32_t swz(int row, int byte) {
     const uint32_t lin = (uint32_t)(row * S::kW + (byte % S::kW));
-    return (uint32_t)(byte / S::kW) * (kStageRows * S::kW) + (lin ^ (((lin >> 7) & S::kSwz) << 4));
+    return (uint32_t)(byte / S::kW) * (S::kStageRows * S::kW) + (lin ^ (((lin >> 7) & S::kSwz) << 4));
 }
 
 template <int NB>
@@ -118,14 +136,34 @@ __device__ __forceinline__ void lds_words(const uint8_t *p, uint32_t (&w)[NB / 4
     }
 }
 
+// Neither has side effects, so neither is volatile: the compiler may then
+// interleave the independent MMA chains of a tile instead of issuing each
+// chain's dependent steps back to back.
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
     uint32_t d;
-    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
     return d;
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kCWarps * 32) : "memory");
+}
+
+__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
 }
 
 __device__ __forceinline__ float pow2i(int e) { return __int_as_float((127 + e) << 23); }
@@ -150,20 +188,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const __grid_constant__ CUtensorMap tm_kb, const __grid_constant__ CUtensorMap tm_vs,
                 const __grid_constant__ CUtensorMap tm_vb) {
     using S = Shape<BITS, D, GROUP>;
-    constexpr int G = S::kG;
+    constexpr int G = S::kG, RB = S::kRBk, SR = S::kStageRows;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *ring = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const int merge_bytes = 4 * ((kCWarps + 1) * p.nrep * (D + 2));
+    const int merge_bytes = (4 * p.nrep * ((kPairs + 1) * D + 3 * kPairs + 2) + 1023) & ~1023;
     uint8_t *tail = ring + max(p.stages * S::kStageBytes, merge_bytes);
-    uint2 *qfrag = reinterpret_cast<uint2 *>(tail);                 // [D/16][32]
+    float4 *exch = reinterpret_cast<float4 *>(tail);    // [pairs][2 slots][2 halves][32][RB]
+    uint2 *qfrag = reinterpret_cast<uint2 *>(exch + (kSplit == 2 ? kPairs * 2 * 2 * 32 * RB : 0));
     float *qf = reinterpret_cast<float *>(qfrag + (D / 16) * 32);   // [8][D]  q * 2^e
     float *qs2 = qf + 8 * D;                                        // [8][G]  sum(q) log2 e
     float *qsc = qs2 + 8 * G;                                       // [8]     2^(24-e) log2 e
-    float *red = qsc + 8;                                           // [8]
-    uint64_t *full = reinterpret_cast<uint64_t *>(red + 8);
+    uint64_t *full = reinterpret_cast<uint64_t *>(qsc + 16);
     uint64_t *empty = full + kMaxStages;
-    int *flag_s = reinterpret_cast<int *>(empty + kMaxStages);
+    uint64_t *xbar = empty + kMaxStages;     // [pairs][2 slots]: the score exchange
+    int *flag_s = reinterpret_cast<int *>(xbar + 2 * kPairs);
     volatile int *flag = flag_s;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -172,7 +211,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int rank = (int)blockIdx.x % p.csize;
     const int n0 = rank * p.block;
     const int n1 = min(p.N, n0 + p.block);
-    const int nst = n1 > n0 ? (n1 - n0 + kStageRows - 1) / kStageRows : 0;
+    const int nst = n1 > n0 ? (n1 - n0 + SR - 1) / SR : 0;
     const int nrep = p.nrep;
     const long long row_base = (long long)kv * p.N;
 
@@ -181,14 +220,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kCWarps);
         }
+        for (int i = 0; i < 2 * kPairs; ++i) mbar_init(&xbar[i], 64);
         *flag_s = 0;
         fence_mbar_init();
     }
     __syncthreads();
+    // the next kernel of the stream may launch now (onto SMs this grid does
+    // not hold); this grid's reads of q and the caches wait for the previous
+    // one to complete
+    launch_dependents();
 
     if (warp == kCWarps) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
+            grid_dependency_wait();
             int issued = 0;
             for (int st = 0; st < nst && !*flag; ++st) {
                 const int slot = st % p.stages, lap = st / p.stages;
@@ -197,13 +242,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     break;
                 }
                 uint8_t *sb = ring + slot * S::kStageBytes;
-                const int row0 = (int)(row_base + n0 + st * kStageRows);
+                const int row0 = (int)(row_base + n0 + st * SR);
                 const int x0 = (row0 * G) & ~7;
                 mbar_arrive_expect_tx(&full[slot], (uint32_t)S::kTx);
 #pragma unroll
                 for (int b = 0; b < S::kBoxes; ++b) {
-                    tma_load_2d(sb + b * kStageRows * S::kW, &tm_kw, b * S::kW, row0, &full[slot]);
-                    tma_load_2d(sb + S::kCodeBytes + b * kStageRows * S::kW, &tm_vw, b * S::kW, row0,
+                    tma_load_2d(sb + b * SR * S::kW, &tm_kw, b * S::kW, row0, &full[slot]);
+                    tma_load_2d(sb + S::kCodeBytes + b * SR * S::kW, &tm_vw, b * S::kW, row0,
                                 &full[slot]);
                 }
                 uint8_t *sc = sb + 2 * S::kCodeBytes;
@@ -226,7 +271,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ prologue
-        {
+        grid_dependency_wait();
+        if (warp < 8) {
             // warp w: query head w of this KV head (zeros past nrep)
             const int h = warp;
             float qv[D / 32];
@@ -261,9 +307,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (lane == 0) qsc[h] = pow2i(24 - e) * kLog2e;
         }
         consumer_sync();
-        // B fragments of q': k-step k of group g, lane (gid, t) = head gid,
-        // the k of thread t's registers 2s and 2s+1 (their two halves)
-        for (int k = 0; k < D / 16; ++k) {
+        // B fragments of q' for k-step k, lane (hg, tt): head hg, the k of
+        // thread tt's code registers 2s and 2s+1 (both halves)
+        for (int e = threadIdx.x; e < (D / 16) * 32; e += kCWarps * 32) {
+            const int k = e >> 5, hg = (e >> 2) & 7, tt = e & 3;
             const int g = k / S::kSteps, s2 = k % S::kSteps;
             uint32_t r[2];
 #pragma unroll
@@ -275,33 +322,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     int d;
                     float f = 1.f;
                     if constexpr (BITS == 4) {
-                        d = g * GROUP + t * (GROUP / 4) + 8 * (i / 4) + (i % 4) + 4 * hf;
+                        d = g * GROUP + tt * (GROUP / 4) + 8 * (i / 4) + (i % 4) + 4 * hf;
                         if (i & 1) f = 0.0625f;
                     } else {
-                        d = g * GROUP + t * (GROUP / 4) + 4 * (i / 2) + (i % 2) + 2 * hf;
+                        d = g * GROUP + tt * (GROUP / 4) + 4 * (i / 2) + (i % 2) + 2 * hf;
                     }
-                    v[hf] = gid < nrep ? qf[gid * D + d] * f : 0.f;
+                    v[hf] = hg < nrep ? qf[hg * D + d] * f : 0.f;
                 }
                 r[j] = pack_half2(v[0], v[1]);
             }
-            qfrag[k * 32 + lane] = make_uint2(r[0], r[1]);
+            qfrag[e] = make_uint2(r[0], r[1]);
         }
         const float qsc0 = qsc[2 * t], qsc1 = qsc[2 * t + 1];
         consumer_sync();
 
         // ------------------------------------------------------------ main loop
+        // warps w and w + kPairs share a tile when split
+        const int pw = warp % kPairs, half = kSplit == 2 ? warp / kPairs : 0;
+        const int g0 = G >= 2 ? half * S::kGH : 0;             // first group of this warp
+        const int ks0 = G >= 2 ? 0 : half * S::kHS;           // first step within a group
         float m2[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
         // p * scale * 2^ev enters the value product: ev keeps the largest
         // |scale| seen so far below 2^15 (fp16 range, few subnormals); it only
         // decreases, and O is rescaled with it like with the running max
         int ev = 127;
-        float bt[2][G];
-        float O[D / 16][4];
+        float bt[2][S::kGH];
+        float O[S::kHU][4];
 #pragma unroll
-        for (int g = 0; g < G; ++g) bt[0][g] = bt[1][g] = 0.f;
+        for (int g = 0; g < S::kGH; ++g) bt[0][g] = bt[1][g] = 0.f;
 #pragma unroll
-        for (int i = 0; i < D / 16; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.f;
+        for (int i = 0; i < S::kHU; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.f;
 
+        int tile = 0;
         for (int st = 0; st < nst; ++st) {
             const int slot = st % p.stages, lap = st / p.stages;
             if (*flag) break;
@@ -309,72 +361,132 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 attn_record(flag, p.err, ERR_ATTN_FULL);
                 break;
             }
-            const int r0 = n0 + st * kStageRows + warp * kTile;   // first row of the tile
+            const int r0 = n0 + st * SR + pw * S::kTileRows;   // first row of the tile
             if (r0 < n1) {
                 const uint8_t *kst = ring + slot * S::kStageBytes;
                 const uint8_t *vst = kst + S::kCodeBytes;
-                const int row0 = (int)(row_base + n0 + st * kStageRows);
+                const int row0 = (int)(row_base + n0 + st * SR);
                 const int soff = row0 * G - ((row0 * G) & ~7);
                 const __half *sks = reinterpret_cast<const __half *>(vst + S::kCodeBytes) + soff;
                 const __half *skb = sks + S::kSArr;
                 const __half *svs = sks + 2 * S::kSArr;
                 const __half *svb = sks + 3 * S::kSArr;
-                const int tr = warp * kTile;                       // tile row in the stage
-                const int ra = tr + gid, rb = tr + gid + 8;
+                const int tr = pw * S::kTileRows;                  // tile row in the stage
 
-                // scores: rows (gid, gid+8) x heads (2t, 2t+1)
-                float s[4] = {0.f, 0.f, 0.f, 0.f};
+                // this half's part of the scores of block b: rows (16b + gid,
+                // 16b + gid + 8) x heads (2t, 2t+1); t1 = sum scale * sum(q'
+                // code), t2 = sum bias * sum(q) log2 e (once per group)
+                float t1[RB][4], t2[RB][4];
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    uint32_t Ra[S::kRegs], Rb[S::kRegs];
+                for (int b = 0; b < RB; ++b)
 #pragma unroll
-                    for (int c = 0; c < (S::kCK + 15) / 16; ++c) {
-                        constexpr int NB = S::kCK < 16 ? S::kCK : 16;
-                        uint32_t wa[NB / 4], wb[NB / 4];
-                        const int byte = g * S::kGB + t * S::kCK + c * 16;
-                        lds_words<NB>(kst + swz<S>(ra, byte), wa);
-                        lds_words<NB>(kst + swz<S>(rb, byte), wb);
+                    for (int i = 0; i < 4; ++i) t1[b][i] = t2[b][i] = 0.f;
 #pragma unroll
-                        for (int j = 0; j < NB / 4; ++j) {
-                            const int base = (c * (NB / 4) + j) * (BITS == 4 ? 4 : 2);
-                            if constexpr (BITS == 4) {
-                                const uint32_t va = wa[j] >> 8, vb = wb[j] >> 8;
-                                Ra[base + 0] = wa[j] & 0x000F000Fu;
-                                Ra[base + 1] = wa[j] & 0x00F000F0u;
-                                Ra[base + 2] = va & 0x000F000Fu;
-                                Ra[base + 3] = va & 0x00F000F0u;
-                                Rb[base + 0] = wb[j] & 0x000F000Fu;
-                                Rb[base + 1] = wb[j] & 0x00F000F0u;
-                                Rb[base + 2] = vb & 0x000F000Fu;
-                                Rb[base + 3] = vb & 0x00F000F0u;
-                            } else {
-                                Ra[base + 0] = wa[j] & 0x00FF00FFu;
-                                Ra[base + 1] = (wa[j] >> 8) & 0x00FF00FFu;
-                                Rb[base + 0] = wb[j] & 0x00FF00FFu;
-                                Rb[base + 1] = (wb[j] >> 8) & 0x00FF00FFu;
+                for (int gg = 0; gg < S::kGH; ++gg) {
+                    const int g = g0 + gg;
+                    const float q0 = qs2[(2 * t) * G + g], q1 = qs2[(2 * t + 1) * G + g];
+#pragma unroll
+                    for (int b = 0; b < RB; ++b) {
+                        const int ra = tr + 16 * b + gid, rb = ra + 8;
+                        constexpr int NBY = S::kHS * BITS / 2;   // bytes of the half's steps
+                        uint32_t Ra[2 * S::kHS], Rb[2 * S::kHS];
+#pragma unroll
+                        for (int c = 0; c < (NBY + 15) / 16; ++c) {
+                            constexpr int NB = NBY < 16 ? NBY : 16;
+                            uint32_t wa[NB / 4], wb[NB / 4];
+                            const int byte = g * S::kGB + t * S::kCK + ks0 * (BITS / 2) + c * 16;
+                            lds_words<NB>(kst + swz<S>(ra, byte), wa);
+                            lds_words<NB>(kst + swz<S>(rb, byte), wb);
+#pragma unroll
+                            for (int j = 0; j < NB / 4; ++j) {
+                                const int base = (c * (NB / 4) + j) * (BITS == 4 ? 4 : 2);
+                                if constexpr (BITS == 4) {
+                                    const uint32_t va = wa[j] >> 8, vb = wb[j] >> 8;
+                                    Ra[base + 0] = wa[j] & 0x000F000Fu;
+                                    Ra[base + 1] = wa[j] & 0x00F000F0u;
+                                    Ra[base + 2] = va & 0x000F000Fu;
+                                    Ra[base + 3] = va & 0x00F000F0u;
+                                    Rb[base + 0] = wb[j] & 0x000F000Fu;
+                                    Rb[base + 1] = wb[j] & 0x00F000F0u;
+                                    Rb[base + 2] = vb & 0x000F000Fu;
+                                    Rb[base + 3] = vb & 0x00F000F0u;
+                                } else {
+                                    Ra[base + 0] = wa[j] & 0x00FF00FFu;
+                                    Ra[base + 1] = (wa[j] >> 8) & 0x00FF00FFu;
+                                    Rb[base + 0] = wb[j] & 0x00FF00FFu;
+                                    Rb[base + 1] = (wb[j] >> 8) & 0x00FF00FFu;
+                                }
                             }
                         }
-                    }
-                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int k = 0; k < S::kSteps; ++k) {
-                        const uint2 bq = qfrag[(g * S::kSteps + k) * 32 + lane];
-                        const uint32_t a[4] = {Ra[2 * k], Rb[2 * k], Ra[2 * k + 1], Rb[2 * k + 1]};
-                        mma_f16_16816(acc, a, bq.x, bq.y, acc);
+                        for (int k = 0; k < S::kHS; ++k) {
+                            const uint2 bq = qfrag[(g * S::kSteps + ks0 + k) * 32 + lane];
+                            const uint32_t a[4] = {Ra[2 * k], Rb[2 * k], Ra[2 * k + 1],
+                                                   Rb[2 * k + 1]};
+                            mma16816(acc, a, bq.x, bq.y);
+                        }
+                        const float ksa = __half2float(sks[ra * G + g]);
+                        const float ksb = __half2float(sks[rb * G + g]);
+                        t1[b][0] = fmaf(ksa, acc[0], t1[b][0]);
+                        t1[b][1] = fmaf(ksa, acc[1], t1[b][1]);
+                        t1[b][2] = fmaf(ksb, acc[2], t1[b][2]);
+                        t1[b][3] = fmaf(ksb, acc[3], t1[b][3]);
+                        if (ks0 == 0) {
+                            const float kba = __half2float(skb[ra * G + g]);
+                            const float kbb = __half2float(skb[rb * G + g]);
+                            t2[b][0] = fmaf(kba, q0, t2[b][0]);
+                            t2[b][1] = fmaf(kba, q1, t2[b][1]);
+                            t2[b][2] = fmaf(kbb, q0, t2[b][2]);
+                            t2[b][3] = fmaf(kbb, q1, t2[b][3]);
+                        }
                     }
-                    const float ksa = __half2float(sks[ra * G + g]), ksb = __half2float(sks[rb * G + g]);
-                    const float kba = __half2float(skb[ra * G + g]), kbb = __half2float(skb[rb * G + g]);
-                    const float q0 = qs2[(2 * t) * G + g], q1 = qs2[(2 * t + 1) * G + g];
-                    s[0] = fmaf(ksa, acc[0] * qsc0, fmaf(kba, q0, s[0]));
-                    s[1] = fmaf(ksa, acc[1] * qsc1, fmaf(kba, q1, s[1]));
-                    s[2] = fmaf(ksb, acc[2] * qsc0, fmaf(kbb, q0, s[2]));
-                    s[3] = fmaf(ksb, acc[3] * qsc1, fmaf(kbb, q1, s[3]));
                 }
-                if (r0 + gid >= n1) s[0] = s[1] = -INFINITY;
-                if (r0 + gid + 8 >= n1) s[2] = s[3] = -INFINITY;
+                // the pair's two parts, exchanged through shared memory: two
+                // slots by tile parity, each with an mbarrier that completes
+                // when all 64 lanes of the pair have written (a slot is written
+                // again only after the partner has passed the next exchange,
+                // so after it has read this one)
+                float s[RB][4];
+#pragma unroll
+                for (int b = 0; b < RB; ++b) {
+                    s[b][0] = fmaf(qsc0, t1[b][0], t2[b][0]);
+                    s[b][1] = fmaf(qsc1, t1[b][1], t2[b][1]);
+                    s[b][2] = fmaf(qsc0, t1[b][2], t2[b][2]);
+                    s[b][3] = fmaf(qsc1, t1[b][3], t2[b][3]);
+                }
+                if constexpr (kSplit == 2) {
+                    float4 *xs = exch + ((pw * 2 + (tile & 1)) * 2) * 32 * RB;
+                    uint64_t *xb = &xbar[pw * 2 + (tile & 1)];
+#pragma unroll
+                    for (int b = 0; b < RB; ++b)
+                        xs[(half * 32 + lane) * RB + b] =
+                            make_float4(s[b][0], s[b][1], s[b][2], s[b][3]);
+                    mbar_arrive(xb);
+                    if (!mbar_wait(xb, (tile >> 1) & 1)) attn_record(flag, p.err, ERR_ATTN_PAIR);
+#pragma unroll
+                    for (int b = 0; b < RB; ++b) {
+                        const float4 o = xs[((1 - half) * 32 + lane) * RB + b];
+                        s[b][0] += o.x;   // the same sums in both warps (a + b == b + a)
+                        s[b][1] += o.y;
+                        s[b][2] += o.z;
+                        s[b][3] += o.w;
+                    }
+                    ++tile;
+                }
+#pragma unroll
+                for (int b = 0; b < RB; ++b) {
+                    if (r0 + 16 * b + gid >= n1) s[b][0] = s[b][1] = -INFINITY;
+                    if (r0 + 16 * b + gid + 8 >= n1) s[b][2] = s[b][3] = -INFINITY;
+                }
 
-                // online softmax (base 2) per head column
-                float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+                // online softmax (base 2) per head column, once for the tile
+                float mx0 = fmaxf(s[0][0], s[0][2]), mx1 = fmaxf(s[0][1], s[0][3]);
+#pragma unroll
+                for (int b = 1; b < RB; ++b) {
+                    mx0 = fmaxf(mx0, fmaxf(s[b][0], s[b][2]));
+                    mx1 = fmaxf(mx1, fmaxf(s[b][1], s[b][3]));
+                }
 #pragma unroll
                 for (int off = 4; off <= 16; off <<= 1) {
                     mx0 = fmaxf(mx0, __shfl_xor_sync(~0u, mx0, off));
@@ -384,21 +496,33 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const float f0 = exp2f(m2[0] - mn0), f1 = exp2f(m2[1] - mn1);
                 m2[0] = mn0;
                 m2[1] = mn1;
-                const float pr[4] = {exp2f(s[0] - mn0), exp2f(s[1] - mn1), exp2f(s[2] - mn0),
-                                     exp2f(s[3] - mn1)};
-                l[0] = fmaf(l[0], f0, pr[0] + pr[2]);
-                l[1] = fmaf(l[1], f1, pr[1] + pr[3]);
-                float vsa[G], vsb[G];
+                float pr[RB][4];
+                float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+                for (int b = 0; b < RB; ++b) {
+                    pr[b][0] = exp2f(s[b][0] - mn0);
+                    pr[b][1] = exp2f(s[b][1] - mn1);
+                    pr[b][2] = exp2f(s[b][2] - mn0);
+                    pr[b][3] = exp2f(s[b][3] - mn1);
+                    ls0 += pr[b][0] + pr[b][2];
+                    ls1 += pr[b][1] + pr[b][3];
+                }
+                l[0] = fmaf(l[0], f0, ls0);
+                l[1] = fmaf(l[1], f1, ls1);
+
+                // value scales of the lane's rows in this half's groups; their
+                // largest |scale| sets ev
+                float vsa[RB][S::kGH], vsb[RB][S::kGH];
                 float vmx = 0.f;
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    vsa[g] = __half2float(svs[ra * G + g]);
-                    vsb[g] = __half2float(svs[rb * G + g]);
-                    vmx = fmaxf(vmx, fmaxf(fabsf(vsa[g]), fabsf(vsb[g])));
-                }
+                for (int b = 0; b < RB; ++b)
 #pragma unroll
-                for (int off = 4; off <= 16; off <<= 1)
-                    vmx = fmaxf(vmx, __shfl_xor_sync(~0u, vmx, off));
+                    for (int gg = 0; gg < S::kGH; ++gg) {
+                        vsa[b][gg] = __half2float(svs[(tr + 16 * b + gid) * G + g0 + gg]);
+                        vsb[b][gg] = __half2float(svs[(tr + 16 * b + gid + 8) * G + g0 + gg]);
+                        vmx = fmaxf(vmx, fmaxf(fabsf(vsa[b][gg]), fabsf(vsb[b][gg])));
+                    }
+                vmx = __uint_as_float(__reduce_max_sync(~0u, __float_as_uint(vmx)));
                 const int ev_new = min(ev, exp_for(vmx));
                 const float r = ev_new - ev < -126 ? 0.f : pow2i(ev_new - ev);
                 ev = ev_new;
@@ -406,59 +530,66 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if (__any_sync(~0u, f0 != 1.f || f1 != 1.f || r != 1.f)) {
                     const float o0 = f0 * r, o1 = f1 * r;
 #pragma unroll
-                    for (int i = 0; i < D / 16; ++i) {
+                    for (int i = 0; i < S::kHU; ++i) {
                         O[i][0] *= o0;
                         O[i][1] *= o1;
                         O[i][2] *= o0;
                         O[i][3] *= o1;
                     }
 #pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        bt[0][g] *= f0;
-                        bt[1][g] *= f1;
+                    for (int gg = 0; gg < S::kGH; ++gg) {
+                        bt[0][gg] *= f0;
+                        bt[1][gg] *= f1;
                     }
                 }
 
-                // values: O^T[d][heads] += codes^T x (p * scale * 2^ev)
-                const int va0 = tr + 2 * t, va1 = va0 + 1, va8 = va0 + 8, va9 = va0 + 9;
+                // values: O^T[d][heads] += codes^T x (p * scale * 2^ev), 16 rows per MMA
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float vsa_ = vsa[g] * vsc, vsb_ = vsb[g] * vsc;
-                    const float vba = __half2float(svb[ra * G + g]);
-                    const float vbb = __half2float(svb[rb * G + g]);
-                    bt[0][g] = fmaf(pr[0], vba, fmaf(pr[2], vbb, bt[0][g]));
-                    bt[1][g] = fmaf(pr[1], vba, fmaf(pr[3], vbb, bt[1][g]));
-                    const uint32_t b0 = movmatrix_t(pack_half2(pr[0] * vsa_, pr[1] * vsa_));
-                    const uint32_t b1 = movmatrix_t(pack_half2(pr[2] * vsb_, pr[3] * vsb_));
-                    constexpr int NW = S::kCV >= 4 ? S::kCV / 4 : 1;
-                    uint32_t w0[NW], w1[NW], w8[NW], w9[NW];
-                    const int byte = g * S::kGB + gid * S::kCV;
-                    lds_words<S::kCV>(vst + swz<S>(va0, byte), w0);
-                    lds_words<S::kCV>(vst + swz<S>(va1, byte), w1);
-                    lds_words<S::kCV>(vst + swz<S>(va8, byte), w8);
-                    lds_words<S::kCV>(vst + swz<S>(va9, byte), w9);
+                for (int gg = 0; gg < S::kGH; ++gg) {
+                    const int g = g0 + gg;
 #pragma unroll
-                    for (int m = 0; m < S::kSteps; ++m) {
-                        uint32_t a[4];
-                        if constexpr (BITS == 4) {
-                            const int wi = m / 4, bi = m % 4;
-                            const uint32_t sel = (uint32_t)bi | ((uint32_t)(4 + bi) << 8);
-                            const uint32_t x = prmt(w0[wi], w1[wi], sel);
-                            const uint32_t y = prmt(w8[wi], w9[wi], sel);
-                            a[0] = x & 0x000F000Fu;
-                            a[1] = x & 0x00F000F0u;
-                            a[2] = y & 0x000F000Fu;
-                            a[3] = y & 0x00F000F0u;
-                        } else {
-                            const int wi = (2 * m) / 4, bi = (2 * m) % 4;
-                            const uint32_t sl = (uint32_t)bi | ((uint32_t)(4 + bi) << 8);
-                            const uint32_t sh = sl + 0x101u;
-                            a[0] = prmt(w0[wi], w1[wi], sl) & 0x00FF00FFu;
-                            a[1] = prmt(w0[wi], w1[wi], sh) & 0x00FF00FFu;
-                            a[2] = prmt(w8[wi], w9[wi], sl) & 0x00FF00FFu;
-                            a[3] = prmt(w8[wi], w9[wi], sh) & 0x00FF00FFu;
+                    for (int b = 0; b < RB; ++b) {
+                        const int ra = tr + 16 * b + gid, rb = ra + 8;
+                        const float vsa_ = vsa[b][gg] * vsc, vsb_ = vsb[b][gg] * vsc;
+                        const float vba = __half2float(svb[ra * G + g]);
+                        const float vbb = __half2float(svb[rb * G + g]);
+                        bt[0][gg] = fmaf(pr[b][0], vba, fmaf(pr[b][2], vbb, bt[0][gg]));
+                        bt[1][gg] = fmaf(pr[b][1], vba, fmaf(pr[b][3], vbb, bt[1][gg]));
+                        const uint32_t b0 = movmatrix_t(pack_half2(pr[b][0] * vsa_, pr[b][1] * vsa_));
+                        const uint32_t b1 = movmatrix_t(pack_half2(pr[b][2] * vsb_, pr[b][3] * vsb_));
+                        // the half's M-tiles: 4-bit one byte each, 8-bit two
+                        constexpr int NV = S::kHS * BITS / 4;
+                        constexpr int NW = NV >= 4 ? NV / 4 : 1;
+                        uint32_t w0[NW], w1[NW], w8[NW], w9[NW];
+                        const int byte = g * S::kGB + gid * S::kCV + ks0 * (BITS / 4);
+                        const int v0 = tr + 16 * b + 2 * t;
+                        lds_words<NV>(vst + swz<S>(v0, byte), w0);
+                        lds_words<NV>(vst + swz<S>(v0 + 1, byte), w1);
+                        lds_words<NV>(vst + swz<S>(v0 + 8, byte), w8);
+                        lds_words<NV>(vst + swz<S>(v0 + 9, byte), w9);
+#pragma unroll
+                        for (int m = 0; m < S::kHS; ++m) {
+                            uint32_t a[4];
+                            if constexpr (BITS == 4) {
+                                const int wi = m / 4, bi = m % 4;
+                                const uint32_t sel = (uint32_t)bi | ((uint32_t)(4 + bi) << 8);
+                                const uint32_t x = prmt(w0[wi], w1[wi], sel);
+                                const uint32_t y = prmt(w8[wi], w9[wi], sel);
+                                a[0] = x & 0x000F000Fu;
+                                a[1] = x & 0x00F000F0u;
+                                a[2] = y & 0x000F000Fu;
+                                a[3] = y & 0x00F000F0u;
+                            } else {
+                                const int wi = (2 * m) / 4, bi = (2 * m) % 4;
+                                const uint32_t sl = (uint32_t)bi | ((uint32_t)(4 + bi) << 8);
+                                const uint32_t sh = sl + 0x101u;
+                                a[0] = prmt(w0[wi], w1[wi], sl) & 0x00FF00FFu;
+                                a[1] = prmt(w0[wi], w1[wi], sh) & 0x00FF00FFu;
+                                a[2] = prmt(w8[wi], w9[wi], sl) & 0x00FF00FFu;
+                                a[3] = prmt(w8[wi], w9[wi], sh) & 0x00FF00FFu;
+                            }
+                            mma16816(O[gg * S::kHS + m], a, b0, b1);
                         }
-                        mma_f16_16816(O[g * S::kSteps + m], a, b0, b1, O[g * S::kSteps + m]);
                     }
                 }
             }
@@ -472,87 +603,104 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             l[0] += __shfl_xor_sync(~0u, l[0], off);
             l[1] += __shfl_xor_sync(~0u, l[1], off);
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                bt[0][g] += __shfl_xor_sync(~0u, bt[0][g], off);
-                bt[1][g] += __shfl_xor_sync(~0u, bt[1][g], off);
+            for (int gg = 0; gg < S::kGH; ++gg) {
+                bt[0][gg] += __shfl_xor_sync(~0u, bt[0][gg], off);
+                bt[1][gg] += __shfl_xor_sync(~0u, bt[1][gg], off);
             }
         }
         consumer_sync();  // every warp is done with the ring
-        float *wm = reinterpret_cast<float *>(ring);       // [warps][nrep]
-        float *wl = wm + kCWarps * nrep;                   // [warps][nrep]
-        float *wo = wl + kCWarps * nrep;                   // [warps][nrep][D]
+        float *wm = reinterpret_cast<float *>(ring);       // [pairs][nrep]
+        float *wl = wm + kPairs * nrep;                    // [pairs][nrep]
+        float *wo = wl + kPairs * nrep;                    // [pairs][nrep][D]
         const int evf = ev == 127 ? 0 : ev;  // a warp without rows holds zeros
         const float fa = pow2i(24 - evf), fb = BITS == 4 ? pow2i(20 - evf) : fa;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             const int h = 2 * t + hh;
             if (h < nrep) {
-                if (gid == 0) {
-                    wm[warp * nrep + h] = m2[hh];
-                    wl[warp * nrep + h] = l[hh];
+                if (gid == 0 && half == 0) {
+                    wm[pw * nrep + h] = m2[hh];
+                    wl[pw * nrep + h] = l[hh];
                 }
-                float *o = wo + (warp * nrep + h) * D;
+                float *o = wo + (pw * nrep + h) * D;
 #pragma unroll
-                for (int g = 0; g < G; ++g)
+                for (int gg = 0; gg < S::kGH; ++gg)
 #pragma unroll
-                    for (int m = 0; m < S::kSteps; ++m) {
-                        const int d = g * GROUP + gid * (GROUP / 8) + 2 * m;
-                        o[d] = fmaf(O[g * S::kSteps + m][hh], fa, bt[hh][g]);
-                        o[d + 1] = fmaf(O[g * S::kSteps + m][2 + hh], fb, bt[hh][g]);
+                    for (int m = 0; m < S::kHS; ++m) {
+                        const int d = (g0 + gg) * GROUP + gid * (GROUP / 8) + 2 * (ks0 + m);
+                        *reinterpret_cast<float2 *>(o + d) =
+                            make_float2(fmaf(O[gg * S::kHS + m][hh], fa, bt[hh][gg]),
+                                        fmaf(O[gg * S::kHS + m][2 + hh], fb, bt[hh][gg]));
                     }
             }
         }
     }
     __syncthreads();
 
-    // the eight warps, in warp order (log2 units)
+    // the tiles, in tile order (log2 units): per-(tile, head) factors
+    // first, then o four elements at a time
     const float *wm = reinterpret_cast<const float *>(ring);
-    const float *wl = wm + kCWarps * nrep;
-    const float *wo = wl + kCWarps * nrep;
-    float *cm = const_cast<float *>(wo) + kCWarps * nrep * D;   // [nrep]
+    const float *wl = wm + kPairs * nrep;
+    const float *wo = wl + kPairs * nrep;
+    float *co = const_cast<float *>(wo) + kPairs * nrep * D;   // [nrep][D]
+    float *cm = co + nrep * D;                                  // [nrep]
     float *cl = cm + nrep;                                      // [nrep]
-    float *co = cl + nrep;                                      // [nrep][D]
-    for (int i = threadIdx.x; i < nrep * D; i += kAttnThreads) {
-        const int j = i / D, d = i - j * D;
+    float *wg = cl + nrep;                                      // [pairs][nrep]
+    if ((int)threadIdx.x < nrep) {
+        const int j = threadIdx.x;
         float M = -INFINITY;
-        for (int w = 0; w < kCWarps; ++w) M = fmaxf(M, wm[w * nrep + j]);
-        float L = 0.f, Ov = 0.f;
-        for (int w = 0; w < kCWarps; ++w) {
+        for (int w = 0; w < kPairs; ++w) M = fmaxf(M, wm[w * nrep + j]);
+        float L = 0.f;
+        for (int w = 0; w < kPairs; ++w) {
             const float mw = wm[w * nrep + j];
-            const float g = mw == -INFINITY ? 0.f : exp2f(mw - M);  // a warp with no rows
+            const float g = mw == -INFINITY ? 0.f : exp2f(mw - M);  // a tile with no rows
+            wg[w * nrep + j] = g;
             L = fmaf(wl[w * nrep + j], g, L);
-            Ov = fmaf(wo[(w * nrep + j) * D + d], g, Ov);
         }
-        co[j * D + d] = Ov;
-        if (d == 0) {
-            cm[j] = M;
-            cl[j] = L;
+        cm[j] = M;
+        cl[j] = L;
+    }
+    __syncthreads();
+    for (int i4 = threadIdx.x; i4 < nrep * D / 4; i4 += kAttnThreads) {
+        const int j = (4 * i4) / D;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kPairs; ++w) {
+            const float g = wg[w * nrep + j];
+            const float4 v = reinterpret_cast<const float4 *>(wo + w * nrep * D)[i4];
+            acc.x = fmaf(v.x, g, acc.x);
+            acc.y = fmaf(v.y, g, acc.y);
+            acc.z = fmaf(v.z, g, acc.z);
+            acc.w = fmaf(v.w, g, acc.w);
         }
+        reinterpret_cast<float4 *>(co)[i4] = acc;
     }
     __syncthreads();
 
     // the cluster's CTAs, in rank order; rank r writes its share of o
     const int C = p.csize;
     if (C > 1) cluster_sync();
-    const int total = nrep * D;
-    const int chunk = (total + C - 1) / C;
+    const int total4 = nrep * D / 4;
+    const int chunk4 = (total4 + C - 1) / C;
     const uint32_t bm = smem_u32(cm), bl = smem_u32(cl), bo = smem_u32(co);
-    for (int i = rank * chunk + (int)threadIdx.x; i < min(total, (rank + 1) * chunk);
-         i += kAttnThreads) {
-        const int j = i / D, d = i - j * D;
-        float L = 0.f, Ov = 0.f;
+    for (int i4 = rank * chunk4 + (int)threadIdx.x; i4 < min(total4, (rank + 1) * chunk4);
+         i4 += kAttnThreads) {
+        const int j = (4 * i4) / D, d = 4 * i4 - j * D;
+        float L = 0.f;
+        float4 Ov = make_float4(0.f, 0.f, 0.f, 0.f);
         if (C == 1) {
             L = cl[j];
-            Ov = co[i];
+            Ov = reinterpret_cast<const float4 *>(co)[i4];
         } else {
             // every rank's (max, sum, o) loaded at once, then folded in rank order
-            float mr[16], lr[16], orr[16];
+            float mr[16], lr[16];
+            float4 orr[16];
 #pragma unroll
             for (int rr = 0; rr < 16; ++rr)
                 if (rr < C) {
                     mr[rr] = ld_dsmem_f32(map_to_rank(bm + 4u * j, (uint32_t)rr));
                     lr[rr] = ld_dsmem_f32(map_to_rank(bl + 4u * j, (uint32_t)rr));
-                    orr[rr] = ld_dsmem_f32(map_to_rank(bo + 4u * (uint32_t)i, (uint32_t)rr));
+                    orr[rr] = ld_dsmem_v4(map_to_rank(bo + 16u * (uint32_t)i4, (uint32_t)rr));
                 }
             float M = -INFINITY;
 #pragma unroll
@@ -563,15 +711,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if (rr < C && mr[rr] != -INFINITY) {  // a block with no rows adds nothing
                     const float g = exp2f(mr[rr] - M);
                     L = fmaf(lr[rr], g, L);
-                    Ov = fmaf(orr[rr], g, Ov);
+                    Ov.x = fmaf(orr[rr].x, g, Ov.x);
+                    Ov.y = fmaf(orr[rr].y, g, Ov.y);
+                    Ov.z = fmaf(orr[rr].z, g, Ov.z);
+                    Ov.w = fmaf(orr[rr].w, g, Ov.w);
                 }
         }
-        const float v = Ov / L;
+        const float inv[4] = {Ov.x / L, Ov.y / L, Ov.z / L, Ov.w / L};
         const size_t oi = (size_t)(kv * nrep + j) * D + d;
-        if (p.bf16)
-            static_cast<__nv_bfloat16 *>(p.out)[oi] = __float2bfloat16_rn(v);
-        else
-            static_cast<__half *>(p.out)[oi] = __float2half_rn(v);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (p.bf16)
+                static_cast<__nv_bfloat16 *>(p.out)[oi + k] = __float2bfloat16_rn(inv[k]);
+            else
+                static_cast<__half *>(p.out)[oi + k] = __float2half_rn(inv[k]);
+        }
     }
     if (C > 1) cluster_sync();  // keep this CTA's results until every rank has read them
 }
@@ -579,10 +733,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 template <int BITS, int D, int GROUP>
 size_t attn_smem_t(int stages, int nrep) {
     using S = Shape<BITS, D, GROUP>;
-    const size_t merge = 4 * (size_t)((kCWarps + 1) * nrep * (D + 2));
+    const size_t merge =
+        (4 * (size_t)nrep * ((kPairs + 1) * D + 3 * kPairs + 2) + 1023) & ~(size_t)1023;
     const size_t ring = std::max((size_t)stages * S::kStageBytes, merge);
-    const size_t tail = (size_t)(D / 16) * 32 * 8 + 4 * (size_t)(8 * D + 8 * S::kG + 16) +
-                        16 * (size_t)kMaxStages + 16;
+    const size_t tail = (kSplit == 2 ? (size_t)kPairs * 2 * 2 * 32 * S::kRBk * 16 : 0) +
+                        (size_t)(D / 16) * 32 * 8 + 4 * (size_t)(8 * D + 8 * S::kG + 16) +
+                        16 * (size_t)kMaxStages + 16 * (size_t)kPairs + 16;
     return 1024 + ring + tail;
 }
 
@@ -627,15 +783,16 @@ const int *attn_active_clusters() {
 // the smaller c on ties.
 template <int BITS, int D, int GROUP>
 int attn_pick_cluster(int64_t KV, int64_t N) {
+    constexpr int SR = Shape<BITS, D, GROUP>::kStageRows;
     const int *n = attn_active_clusters<BITS, D, GROUP>();
-    const int64_t maxc = std::min<int64_t>(16, std::max<int64_t>(1, (N + kStageRows - 1) / kStageRows));
+    const int64_t maxc = std::min<int64_t>(16, std::max<int64_t>(1, (N + SR - 1) / SR));
     int best = 1;
     int64_t best_cost = INT64_MAX;
     for (int c = 1; c <= maxc; ++c) {
         if (n[c] < 1) continue;
         const int64_t waves = (KV + n[c] - 1) / n[c];
-        const int64_t block = ((N + c - 1) / c + kTile - 1) / kTile * kTile;
-        const int64_t cost = waves * ((block + kStageRows - 1) / kStageRows);
+        const int64_t block = ((N + c - 1) / c + 15) / 16 * 16;
+        const int64_t cost = waves * ((block + SR - 1) / SR);
         if (cost < best_cost) {
             best_cost = cost;
             best = c;
@@ -674,8 +831,8 @@ cudaError_t attn_run(const AttnLaunch &L, AttnPlan *plan) {
     prm.N = (int)L.N;
     prm.nrep = (int)(L.H / L.KV);
     prm.csize = C;
-    prm.block = (int)(((L.N + C - 1) / C + kTile - 1) / kTile * kTile);
-    const int nst = (prm.block + kStageRows - 1) / kStageRows;
+    prm.block = (int)(((L.N + C - 1) / C + 15) / 16 * 16);
+    const int nst = (prm.block + S::kStageRows - 1) / S::kStageRows;
     prm.stages = std::max(1, std::min(attn_max_stages<BITS, D, GROUP>(), nst));
     prm.bf16 = L.dtype == AQ_BF16;
     if (plan) {
@@ -689,9 +846,9 @@ cudaError_t attn_run(const AttnLaunch &L, AttnPlan *plan) {
                                                  : CU_TENSOR_MAP_SWIZZLE_32B;
     CUtensorMap m[6];
     if (!tmap_2d(&m[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, L.kw, S::kRB, rows, S::kRB, S::kW,
-                 kStageRows, swz) ||
+                 S::kStageRows, swz) ||
         !tmap_2d(&m[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, L.vw, S::kRB, rows, S::kRB, S::kW,
-                 kStageRows, swz))
+                 S::kStageRows, swz))
         return cudaErrorInvalidValue;
     const void *sp[4] = {L.ks, L.kb, L.vs, L.vb};
     for (int i = 0; i < 4; ++i) {
@@ -708,13 +865,15 @@ cudaError_t attn_run(const AttnLaunch &L, AttnPlan *plan) {
     cfg.blockDim = dim3(kAttnThreads, 1, 1);
     cfg.dynamicSmemBytes = attn_smem_t<BITS, D, GROUP>(prm.stages, prm.nrep);
     cfg.stream = L.stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, prm, m[0], m[1], m[2], m[3], m[4], m[5]);
 }
 

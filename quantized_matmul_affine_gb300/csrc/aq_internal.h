@@ -47,6 +47,7 @@ enum : uint32_t {
     ERR_GEMV_DRAIN = 0x0303,
     ERR_ATTN_FULL = 0x0104,
     ERR_ATTN_EMPTY = 0x0204,
+    ERR_ATTN_PAIR = 0x0304,
 };
 
 // Each returns cudaSuccess, or the launch error.  `supported` reports
