@@ -169,8 +169,10 @@ aq_status aq_quantize_ex(int dtype, const void *w_dev, int64_t N, int64_t K, int
  *   o[h] = softmax(q[h] . Kd[kv]^T) . Vd[kv],   kv = h / (H / KV),
  * Kd, Vd the caches dequantised as scale * code + bias per group of
  * group_size values along the head dimension.  This is the operator of the
- * pages' fused decode kernel (fused-decode-kernel.ts); the query is used as
- * given (a 1/sqrt(D) factor, if wanted, is folded into q by the caller).
+ * fused decode kernel of the mlx-bun 0.0.4 page
+ * (src/model/fused-decode-kernel.ts); the query is used as given (a
+ * 1/sqrt(D) factor, if wanted, is folded into q by the caller, as the
+ * pages' kernel expects a pre-scaled query).
  *   dtype         AQ_F16 or AQ_BF16: the type of q and o.
  *   q_dev         [H][D], device.
  *   k_words_dev   uint32 [KV][N][D*bits/32], device, 16-byte aligned: row

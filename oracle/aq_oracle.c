@@ -364,8 +364,9 @@ int oracle_quantize(const float *w, int64_t N, int64_t K, int bits, uint8_t *cod
  * with Kd, Vd the caches dequantised as scale * q + bias per group of
  * `group` values along d (rows [KV][N], D values each, packed as the weight
  * format: K*B/32 words per row, LSB-first).  This is the operator of the
- * pages' fused decode kernel (fused-decode-kernel.ts: L = 1, quantised K
- * and V, grouped-query heads), taken as its plain definition in fp64; the
+ * fused decode kernel of the mlx-bun 0.0.4 page
+ * (src/model/fused-decode-kernel.ts: L = 1, quantised K and V,
+ * grouped-query heads), taken as its plain definition in fp64; the
  * query is used as given (any 1/sqrt(D) is the caller's).  Also returned,
  * for the tolerance: smag[h][n] = sum_d |q*Kd| and vmag[h][d] =
  * sum_n p * |Vd|.

@@ -2,8 +2,8 @@
 //   o[h] = softmax(q[h] . Kd[kv]^T) . Vd[kv],   kv = h / (H / KV),
 // with K and V stored in the affine format (4 or 8 bits, one fp16 scale and
 // bias per group of 32/64/128 values along the head dimension).  The
-// operator of the mlx-bun fused decode kernel (@mlx-bun/inference 1.0.0,
-// fused-decode-kernel.ts: flash-decoding split over the cached rows, the
+// operator of the fused decode kernel of the mlx-bun 0.0.4 page
+// (src/model/fused-decode-kernel.ts: flash-decoding split over the cached rows, the
 // scores taken in the factored form scale * sum(q * code) + bias * sum(q),
 // an online softmax per row block, a deterministic merge of the blocks).
 //

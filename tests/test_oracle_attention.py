@@ -2,9 +2,9 @@
 
 The oracle computes o = softmax(q . Kd^T) . Vd per query head in fp64, head
 h reading KV head h / (H/KV), K and V dequantised as scale * q + bias per
-group along d (the operator of the mlx-bun fused decode kernel,
-fused-decode-kernel.ts).  The tests tie it to an mpmath evaluation at 50
-digits over an independent bit-by-bit unpacker, to closed forms (one token,
+group along d (the operator of the fused decode kernel of the mlx-bun
+0.0.4 page, src/model/fused-decode-kernel.ts).  The tests tie it to an
+mpmath evaluation at 50 digits over an independent bit-by-bit unpacker, to closed forms (one token,
 a zero query), and to invariants (token order, a constant shift of every
 score of a head, the grouped-query head mapping), so a wrong head index,
 group index, missing max subtraction or normalisation fails one of them.
