@@ -290,7 +290,9 @@ aq_status aq_matmul_ex(int dtype, const void *x_dev, const uint32_t *Wq_dev,
         !aligned(biases_dev, 2) || !aligned(out_dev, 2))
         return AQ_ERR_MISALIGNED;
     if (!generic_supported_g(a, group_size)) return AQ_ERR_UNSUPPORTED;
-    if (generic_launch_g(a, group_size) != cudaSuccess) return AQ_ERR_CUDA;
+    const cudaError_t e = segv_supported(a, group_size) ? segv_launch(a, group_size)
+                                                         : generic_launch_g(a, group_size);
+    if (e != cudaSuccess) return AQ_ERR_CUDA;
     g_calls[AQ_VARIANT_GENERIC].fetch_add(1, std::memory_order_relaxed);
     return AQ_OK;
 }

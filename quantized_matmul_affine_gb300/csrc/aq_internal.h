@@ -80,6 +80,9 @@ cudaError_t quantize_launch(int dtype, const void *w, int64_t N, int64_t K, int 
 cudaError_t quantize_launch_g(int dtype, const void *w, int64_t N, int64_t K, int bits, int group,
                               uint32_t *words, void *scales, void *biases, cudaStream_t stream);
 bool generic_supported_g(const MatmulArgs &a, int group);
+// The small-M kernel of the other widths and group sizes (aq_segv.cu).
+bool segv_supported(const MatmulArgs &a, int group);
+cudaError_t segv_launch(const MatmulArgs &a, int group);
 bool attention_supported(int64_t H, int64_t KV, int64_t N, int64_t D, int bits, int group);
 // The launch geometry aq_attention_decode would use (snprintf semantics).
 int attention_describe(int64_t H, int64_t KV, int64_t N, int64_t D, int bits, int group,

@@ -102,3 +102,21 @@ def test_quantize_ex_bit_exact(bits, group, dtype):
     np.testing.assert_array_equal(s.cpu().numpy().view(np.uint16), sb)
     np.testing.assert_array_equal(b.cpu().numpy().view(np.uint16), bb)
     np.testing.assert_array_equal(Wq.cpu().numpy().view(np.uint32), oracle.pack_g(codes, bits))
+
+
+@pytest.mark.parametrize("bits,group", [(2, 32), (3, 128), (5, 64), (6, 32), (8, 128)])
+@pytest.mark.parametrize("M,N,K", [(2, 1001, 4096), (8, 33, 2048), (9, 64, 1024),
+                                   (32, 40, 512), (33, 17, 256), (1, 3, 32 * 33)])
+def test_matmul_ex_small_m_shapes(M, N, K, bits, group):
+    # row blocks of 1/2/4/8 activation rows, a long row, ragged N, and M = 33
+    # (past the small-M kernel: the plain kernel)
+    if K % group:
+        pytest.skip("K not a multiple of the group")
+    codes, s, b, x_bits = _problem(bits, group, M, N, K, "bf16", seed=bits + group + M + N)
+    Wq = aq.aq_pack(torch.from_numpy(codes).cuda(), bits)
+    y = aq.aq_matmul_ex(_x(x_bits, "bf16"), Wq, torch.from_numpy(s).cuda(),
+                        torch.from_numpy(b).cuda(), bits, group)
+    torch.cuda.synchronize()
+    y_ref, bound = oracle.matmul_g(workloads.to_f64(x_bits, "bf16"), oracle.pack_g(codes, bits),
+                                   s, b, bits, group, threads=8)
+    assert_within_tolerance(y_to_f64(y, "bf16"), y_ref, bound, f"bits={bits} group={group}")
