@@ -190,6 +190,58 @@ def device_problem(p, copies, torch, aq):
     return x, ws
 
 
+def gpu_comparisons(p, ws, x, torch, l2, stream):
+    """Context, not targets: (1) torch.matmul (cuBLAS) on the weights
+    dequantised once to x's dtype; (2) "expand": dequantise the packed words
+    with torch ops on every call, then torch.matmul (4-bit only).  Both
+    cold-L2 over rotating copies, CUDA events around CUDA-graph replays."""
+    dt = x.dtype
+    G = p.K // 64
+    s0 = ws[0][1].float().view(p.N, G, 1)
+    b0 = ws[0][2].float().view(p.N, G, 1)
+    codes = torch.from_numpy(p.codes).cuda().float().view(p.N, G, 64)
+    w0 = (codes * s0 + b0).view(p.N, p.K).to(dt)
+    del codes
+    dbytes = p.N * p.K * 2
+    dcopies = max(2, -(-2 * l2 // dbytes) + 1)
+    dense = [w0] + [w0.clone() for _ in range(dcopies - 1)]
+    shifts = torch.arange(0, 32, 4, device="cuda", dtype=torch.int32)
+
+    def expand(c):
+        Wq, sc, bi = ws[c % len(ws)]
+        q = (Wq.view(torch.int32).view(p.N, p.K // 8, 1) >> shifts) & 15
+        w = q.view(p.N, G, 64).to(dt) * sc.view(p.N, G, 1).to(dt) + bi.view(p.N, G, 1).to(dt)
+        return torch.matmul(x, w.view(p.N, p.K).t())
+
+    def timed(body, calls=128):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            body(0)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(calls):
+                    body(i)
+            g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(4):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / (4 * calls)
+
+    out = {"dense_matmul_us": round(timed(lambda i: torch.matmul(x, dense[i % dcopies].t())), 3),
+           "expand_then_matmul_us": round(timed(expand), 3) if p.bits == 4 else None,
+           "note": "context only: torch.matmul (cuBLAS) on weights dequantised once to "
+                   f"{'bf16' if dt == torch.bfloat16 else 'fp16'} ({dcopies} copies, cold L2); "
+                   "expand = torch-op dequantise of the packed words every call, then "
+                   "torch.matmul"}
+    del dense, w0
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import quantized_matmul_affine_gb300 as aq
@@ -304,8 +356,13 @@ def run_ours(args, rank, world, local_rank):
         aq.aq_matmul_host(x_host, *ws[i % copies], p.bits, y_host, x_dev, y_dev, stream=stream)
     torch.cuda.synchronize()
     e2e_us = reduce_max((time.perf_counter() - t0) * 1e6 / e2e_steps, "cuda")
-    return finish(args, p, name, idx, world, aq, variant, copies, wbytes, l2, chunk, us_call,
-                  value, us_hot, e2e_us, clocks, bytes_call, flops_call)
+    comp = None
+    if not args.no_compare:
+        comp = gpu_comparisons(p, ws, x, torch, l2, stream)
+    line, p = finish(args, p, name, idx, world, aq, variant, copies, wbytes, l2, chunk, us_call,
+                     value, us_hot, e2e_us, clocks, bytes_call, flops_call)
+    line["gpu_comparisons"] = comp
+    return line, p
 
 
 def finish(args, p, name, idx, world, aq, variant, copies, wbytes, l2, chunk, us_call, value,
@@ -938,6 +995,8 @@ def main():
     ap.add_argument("--all", action="store_true", help="one line per workload (not the default)")
     ap.add_argument("--quick", action="store_true",
                     help="timed region only: skip the hot-L2, end-to-end and CPU legs")
+    ap.add_argument("--no-compare", action="store_true",
+                    help="skip the torch.matmul comparison leg of the default workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
