@@ -85,11 +85,11 @@ def peaks():
         return 6800.0, 1900.0, "fallback"
 
 
-def traffic_record():
-    """dram bytes per launch from the committed ncu summary, if the kernel
+def traffic_record(fname="traffic.txt"):
+    """dram bytes per launch from a committed ncu summary, if the kernel
     source it was taken on is unchanged (source hash recorded beside it)."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    path = os.path.join(ROOT, "profiles", fname)
     try:
         rec = {}
         for line in open(path):
@@ -879,6 +879,10 @@ def run_attention(args, rank, world, local_rank):
     e2e_us = reduce_max((time.perf_counter() - t0) * 1e6 / n_e2e, "cuda")
     hbm, _, src = peaks()
     by = cbytes + 2 * 2 * H * D
+    rec = traffic_record("traffic_attention.txt")
+    attn_traffic = None
+    if rec.get("workload") == args.workload and "dram_bytes_per_launch" in rec:
+        attn_traffic = float(rec["dram_bytes_per_launch"])
     achieved = by / (us * 1e-6) / 1e9
     return {
         "metric": ATTN_METRIC,
@@ -896,7 +900,7 @@ def run_attention(args, rank, world, local_rank):
                    "launch": aq.aq_attention_describe(H, KV, N, D, bits, group),
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm,
-                     "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
+                     "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": attn_traffic,
                      "peak_source": f"{src} (MEASURED_PEAKS.json)" if src == "measured"
                      else "fallback",
                      "algorithmic_bytes_per_launch": by},

@@ -780,13 +780,13 @@ const int *attn_active_clusters() {
 }
 
 // Cluster size: the c minimising (waves of clusters) x (stages per CTA),
-// the smaller c on ties.
+// the smaller c on ties; 0 when no size can run (no device).
 template <int BITS, int D, int GROUP>
 int attn_pick_cluster(int64_t KV, int64_t N) {
     constexpr int SR = Shape<BITS, D, GROUP>::kStageRows;
     const int *n = attn_active_clusters<BITS, D, GROUP>();
     const int64_t maxc = std::min<int64_t>(16, std::max<int64_t>(1, (N + SR - 1) / SR));
-    int best = 1;
+    int best = 0;
     int64_t best_cost = INT64_MAX;
     for (int c = 1; c <= maxc; ++c) {
         if (n[c] < 1) continue;
@@ -820,6 +820,7 @@ template <int BITS, int D, int GROUP>
 cudaError_t attn_run(const AttnLaunch &L, AttnPlan *plan) {
     using S = Shape<BITS, D, GROUP>;
     const int C = attn_pick_cluster<BITS, D, GROUP>(L.KV, L.N);
+    if (C < 1) return cudaErrorNoDevice;
     AttnParams prm;
     prm.q = L.q;
     prm.out = L.out;

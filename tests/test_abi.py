@@ -172,3 +172,16 @@ def test_gemv_plan(M, N, K, bits, want):
     assert d.startswith("gemv ") and want in d, d
     smem = int(d.split("smem=")[1])
     assert smem <= (112 if M <= 8 else 227) * 1024
+
+
+def test_attention_describe_host_checks():
+    # argument checks need no device; without one the geometry is refused
+    import torch
+    assert aq.aq_attention_describe(3, 2, 100, 64, 4, 64) == "invalid arguments"
+    assert aq.aq_attention_describe(4, 2, 100, 96, 4, 32) == "unsupported"
+    assert aq.aq_attention_describe(4, 2, 100, 64, 3, 64) == "unsupported"
+    d = aq.aq_attention_describe(16, 8, 8192, 256, 4, 64)
+    if not torch.cuda.is_available():
+        assert d == "no device"
+    else:
+        assert d.startswith("attn cluster=")
