@@ -12,10 +12,15 @@ total exceeds twice the L2 size (every call reads its weights from HBM).
 
 widths:I times aq_matmul_ex on other code widths and group sizes;
 attention:I times aq_attention_decode (decode attention over a quantised KV
-cache).
-layerstep:I times one decoder-layer step (seven projections; I = 0/1 fused or
-not at M = 1, 2/3 at M = 8).  quantize:I times the float -> affine quantiser (aq_quantize) on the weight
-shapes of workloads.QUANTIZE_WORKLOADS instead of the matmul.
+cache).  layerstep:I times one decoder-layer step (seven projections; I = 0/1
+fused or not at M = 1, 2/3 at M = 8).  quantize:I times the float -> affine
+quantiser (aq_quantize) on the weight shapes of
+workloads.QUANTIZE_WORKLOADS instead of the matmul.
+
+The matmul workloads also carry `gpu_comparisons` (context, not targets):
+torch.matmul (cuBLAS) on the weights dequantised once, and a torch-op
+dequantise of the packed words followed by torch.matmul on every call
+(--no-compare skips them).
 
 Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs an
 independent replica on its own GPU ("replicas only": the method needs no
