@@ -93,6 +93,8 @@ def _check(H, KV, N, D, bits, group, dtype, seed, qscale=2.0, ramp=0.0):
     (2, 1, 16, 128, 4, 128, "bf16"),      # one full tile
     (16, 2, 2053, 256, 4, 64, "fp16"),    # eight query heads over 256 dims
     (8, 8, 129, 128, 4, 32, "bf16"),      # one row past a stage
+    (8, 1, 1000, 256, 8, 32, "fp16"),     # eight heads, 8-bit 256-byte rows, groups of 32
+    (16, 2, 700, 256, 8, 64, "bf16"),
 ])
 def test_attention_parity(H, KV, N, D, bits, group, dtype):
     _check(H, KV, N, D, bits, group, dtype, seed=H + KV + N + D + bits + group)

@@ -120,3 +120,21 @@ def test_matmul_ex_small_m_shapes(M, N, K, bits, group):
     y_ref, bound = oracle.matmul_g(workloads.to_f64(x_bits, "bf16"), oracle.pack_g(codes, bits),
                                    s, b, bits, group, threads=8)
     assert_within_tolerance(y_to_f64(y, "bf16"), y_ref, bound, f"bits={bits} group={group}")
+
+
+def test_matmul_ex_unaligned_x_takes_the_plain_kernel():
+    # x 2-byte aligned only: the small-M kernel stages x with 16-byte loads,
+    # so the call runs on the plain kernel, with the same results
+    M, N, K, bits, group = 3, 70, 512, 5, 64
+    codes, s, b, x_bits = _problem(bits, group, M, N, K, "fp16", seed=77)
+    flat = torch.zeros(M * K + 1, dtype=torch.int16, device="cuda")
+    flat[1:] = torch.from_numpy(np.ascontiguousarray(x_bits).view(np.int16).reshape(-1)).cuda()
+    x = flat[1:].view(M, K).view(torch.float16)
+    assert x.data_ptr() % 16 != 0
+    Wq = aq.aq_pack(torch.from_numpy(codes).cuda(), bits)
+    y = aq.aq_matmul_ex(x, Wq, torch.from_numpy(s).cuda(), torch.from_numpy(b).cuda(), bits,
+                        group)
+    torch.cuda.synchronize()
+    y_ref, bound = oracle.matmul_g(workloads.to_f64(x_bits, "fp16"), oracle.pack_g(codes, bits),
+                                   s, b, bits, group)
+    assert_within_tolerance(y_to_f64(y, "fp16"), y_ref, bound, "unaligned x")
