@@ -57,7 +57,6 @@ namespace {
 constexpr int kWarps = 8;               // warps per CTA
 constexpr int kThreads = kWarps * 32;
 constexpr int kGroupsPerStage = 8;      // 512 values of K per stage
-constexpr int kMaxSlots = 6;            // deepest per-warp ring
 constexpr int kMaxCluster = 16;
 
 template <int B>
