@@ -184,7 +184,7 @@ aq_status aq_quantize_ex(int dtype, const void *w_dev, int64_t N, int64_t K, int
  *   v_words_dev, v_scales_dev, v_biases_dev  the same for V.
  *   out_dev       o [H][D], device, caller-allocated.
  * Served: bits 4 or 8, group_size 32/64/128 (D % group_size == 0), D in
- * {64, 128, 256}, H/KV in {1, 2, 4, 8}, any N >= 1.  Scores are fp32; the
+ * {64, 128, 256, 512}, H/KV in {1, 2, 4, 8}, any N >= 1.  Scores are fp32; the
  * probabilities times the value scales enter the value product as fp16
  * (relative error 2^-11 per term); o is rounded once.  The rows of a KV
  * head are split over the CTAs of one thread-block cluster and merged in

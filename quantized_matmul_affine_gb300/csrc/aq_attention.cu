@@ -51,13 +51,6 @@ __device__ uint32_t g_attn_error;
 
 namespace {
 
-// kSplit = 2 gives each tile to a pair of warps, each taking half of the head
-// dimension (more warps, but partial scores cross shared memory every tile);
-// measured slower on GB300 than one warp per tile, so kSplit = 1.
-constexpr int kSplit = 1;
-constexpr int kPairs = kSplit == 2 ? 6 : 8;          // warp tiles per stage
-constexpr int kCWarps = kSplit * kPairs;             // consumer warps
-constexpr int kAttnThreads = (kCWarps + 1) * 32;     // + the TMA producer warp
 constexpr int kMaxStages = 8;
 constexpr int kRingBudget = 160 * 1024;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -75,6 +68,14 @@ struct AttnParams {
 
 template <int BITS, int D, int GROUP>
 struct Shape {
+    // kSplit = 2 gives each tile to a pair of warps, each taking half of the
+    // head dimension (partial scores cross shared memory every tile).  It
+    // measured slower than one warp per tile up to D = 256, so only D = 512
+    // takes it: there one warp would need 128 accumulator registers.
+    static constexpr int kSplit = D == 512 ? 2 : 1;
+    static constexpr int kPairs = kSplit == 2 ? 6 : 8;  // warp tiles per stage
+    static constexpr int kCWarps = kSplit * kPairs;     // consumer warps
+    static constexpr int kThreads = (kCWarps + 1) * 32; // + the TMA producer warp
     static constexpr int kRB = D * BITS / 8;            // bytes of one cached row
     static constexpr int kW = kRB < 128 ? kRB : 128;    // TMA box width = swizzle span
     static constexpr int kBoxes = kRB / kW;
@@ -153,8 +154,9 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+template <int NWARPS>
 __device__ __forceinline__ void consumer_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kCWarps * 32) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(NWARPS * 32) : "memory");
 }
 
 __device__ __forceinline__ float4 ld_dsmem_v4(uint32_t addr) {
@@ -182,13 +184,15 @@ __device__ __forceinline__ void attn_record(volatile int *flag, uint32_t *err, u
 }
 
 template <int BITS, int D, int GROUP>
-__global__ void __launch_bounds__(kAttnThreads, 1)
+__global__ void __launch_bounds__(Shape<BITS, D, GROUP>::kThreads, 1)
     attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tm_kw,
                 const __grid_constant__ CUtensorMap tm_vw, const __grid_constant__ CUtensorMap tm_ks,
                 const __grid_constant__ CUtensorMap tm_kb, const __grid_constant__ CUtensorMap tm_vs,
                 const __grid_constant__ CUtensorMap tm_vb) {
     using S = Shape<BITS, D, GROUP>;
     constexpr int G = S::kG, RB = S::kRBk, SR = S::kStageRows;
+    constexpr int kSplit = S::kSplit, kPairs = S::kPairs, kCWarps = S::kCWarps;
+    constexpr int kAttnThreads = S::kThreads;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *ring = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -306,7 +310,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             if (lane == 0) qsc[h] = pow2i(24 - e) * kLog2e;
         }
-        consumer_sync();
+        consumer_sync<kCWarps>();
         // B fragments of q' for k-step k, lane (hg, tt): head hg, the k of
         // thread tt's code registers 2s and 2s+1 (both halves)
         for (int e = threadIdx.x; e < (D / 16) * 32; e += kCWarps * 32) {
@@ -334,7 +338,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             qfrag[e] = make_uint2(r[0], r[1]);
         }
         const float qsc0 = qsc[2 * t], qsc1 = qsc[2 * t + 1];
-        consumer_sync();
+        consumer_sync<kCWarps>();
 
         // ------------------------------------------------------------ main loop
         // warps w and w + kPairs share a tile when split
@@ -608,7 +612,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 bt[1][gg] += __shfl_xor_sync(~0u, bt[1][gg], off);
             }
         }
-        consumer_sync();  // every warp is done with the ring
+        consumer_sync<kCWarps>();  // every warp is done with the ring
         float *wm = reinterpret_cast<float *>(ring);       // [pairs][nrep]
         float *wl = wm + kPairs * nrep;                    // [pairs][nrep]
         float *wo = wl + kPairs * nrep;                    // [pairs][nrep][D]
@@ -733,6 +737,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 template <int BITS, int D, int GROUP>
 size_t attn_smem_t(int stages, int nrep) {
     using S = Shape<BITS, D, GROUP>;
+    constexpr int kSplit = S::kSplit, kPairs = S::kPairs;
     const size_t merge =
         (4 * (size_t)nrep * ((kPairs + 1) * D + 3 * kPairs + 2) + 1023) & ~(size_t)1023;
     const size_t ring = std::max((size_t)stages * S::kStageBytes, merge);
@@ -761,7 +766,7 @@ const int *attn_active_clusters() {
         for (int c = 1; c <= 16; ++c) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3((unsigned)(c * 8), 1, 1);
-            cfg.blockDim = dim3(kAttnThreads, 1, 1);
+            cfg.blockDim = dim3(Shape<BITS, D, GROUP>::kThreads, 1, 1);
             cfg.dynamicSmemBytes = smem;
             cudaLaunchAttribute attr[1];
             attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -863,7 +868,7 @@ cudaError_t attn_run(const AttnLaunch &L, AttnPlan *plan) {
     attn_active_clusters<BITS, D, GROUP>();  // sets the kernel attributes
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(L.KV * C), 1, 1);
-    cfg.blockDim = dim3(kAttnThreads, 1, 1);
+    cfg.blockDim = dim3(S::kThreads, 1, 1);
     cfg.dynamicSmemBytes = attn_smem_t<BITS, D, GROUP>(prm.stages, prm.nrep);
     cfg.stream = L.stream;
     cudaLaunchAttribute attr[2];
@@ -894,7 +899,8 @@ cudaError_t attn_dim(int64_t D, int group, const AttnLaunch &L, AttnPlan *c) {
     switch (D) {
         case 64: return attn_group<BITS, 64>(group, L, c);
         case 128: return attn_group<BITS, 128>(group, L, c);
-        default: return attn_group<BITS, 256>(group, L, c);
+        case 256: return attn_group<BITS, 256>(group, L, c);
+        default: return attn_group<BITS, 512>(group, L, c);
     }
 }
 
@@ -908,7 +914,7 @@ bool attention_supported(int64_t H, int64_t KV, int64_t N, int64_t D, int bits, 
     if (H < 1 || KV < 1 || H % KV != 0 || N < 1) return false;
     const int64_t nrep = H / KV;
     if (nrep != 1 && nrep != 2 && nrep != 4 && nrep != 8) return false;
-    if (D != 64 && D != 128 && D != 256) return false;
+    if (D != 64 && D != 128 && D != 256 && D != 512) return false;
     if (bits != 4 && bits != 8) return false;
     if (group != 32 && group != 64 && group != 128) return false;
     if (D % group != 0) return false;

@@ -95,6 +95,10 @@ def _check(H, KV, N, D, bits, group, dtype, seed, qscale=2.0, ramp=0.0):
     (8, 8, 129, 128, 4, 32, "bf16"),      # one row past a stage
     (8, 1, 1000, 256, 8, 32, "fp16"),     # eight heads, 8-bit 256-byte rows, groups of 32
     (16, 2, 700, 256, 8, 64, "bf16"),
+    (8, 2, 1000, 512, 4, 64, "bf16"),     # 512 dimensions: a warp pair per tile
+    (8, 8, 333, 512, 8, 128, "fp16"),     # 512-byte rows, one-stage ring
+    (16, 2, 1500, 512, 4, 32, "bf16"),    # eight heads, sixteen groups per row
+    (2, 2, 97, 512, 8, 32, "bf16"),
 ])
 def test_attention_parity(H, KV, N, D, bits, group, dtype):
     _check(H, KV, N, D, bits, group, dtype, seed=H + KV + N + D + bits + group)
