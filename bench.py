@@ -803,7 +803,7 @@ ATTN_METRIC = ("µs/call and effective HBM GB/s (fraction of roofline), decode a
 # name -> list of (H, KV, N, D, bits, group, q dtype)
 ATTN_WORKLOADS = {"attention": [(16, 8, 8192, 256, 4, 64, "bf16"), (16, 8, 2048, 256, 4, 64, "bf16"),
                                 (16, 8, 32768, 256, 4, 64, "bf16"), (16, 8, 8192, 256, 8, 64, "bf16"),
-                                (32, 8, 8192, 128, 4, 64, "bf16")]}
+                                (32, 8, 8192, 128, 4, 64, "bf16"), (16, 8, 8192, 512, 4, 64, "bf16")]}
 
 
 def run_attention(args, rank, world, local_rank):
