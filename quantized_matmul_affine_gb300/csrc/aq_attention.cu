@@ -14,16 +14,19 @@
 //     merged in rank order through distributed shared memory - no global
 //     scratch, no second launch.  The cluster size is picked from the
 //     driver's count of co-resident clusters.
-//   * A producer warp streams 256-row stages (128 when a row is 256 bytes)
-//     of K and V codes (2-D TMA,
-//     swizzled so that the fragment reads below are free of bank conflicts)
-//     and their scales and biases (1-D TMA) into a shared-memory ring.
+//   * A producer warp streams stages of one tile per consumer warp (or warp
+//     pair): 256 rows, 128 when a row is 256 bytes, 96 at D = 512.  K and V
+//     codes arrive by 2-D TMA (swizzled so that the fragment reads below are
+//     free of bank conflicts), their scales and biases by 1-D TMA, into a
+//     shared-memory ring.
 //   * Each of 8 consumer warps takes a tile of two 16-row blocks of a stage
-//     (one block when a row is 256 bytes).  Scores on the tensor cores, per
-//     block S[16 rows][8 heads] = codes x q', the codes as the exact fp16
-//     subnormals code * 2^-24 (or 2^-20 where a nibble sits
-//     at bit 4), q' = q * 2^e per head in fp16; one m16n8k16 chain per group,
-//     then s = scale * sum(q code) + bias * sum(q) in fp32.
+//     (one block when a row is 256 bytes or more); at D = 512, 12 consumer
+//     warps take 6 tiles in pairs, each warp half of the head dimension.
+//     Scores on the tensor cores, per block S[16 rows][8 heads] =
+//     codes x q', the codes as the exact fp16 subnormals code * 2^-24 (or
+//     2^-20 where a nibble sits at bit 4), q' = q * 2^e per head in fp16;
+//     one m16n8k16 chain per group, then s = scale * sum(q code) +
+//     bias * sum(q) in fp32.
 //   * Online softmax in base 2 on the fragment; the probabilities, times the
 //     value scale of their row and group (and 2^ev, a per-warp power of two
 //     lowered as larger scales appear, which keeps them in the fp16 range
