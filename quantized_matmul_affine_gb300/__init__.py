@@ -114,6 +114,41 @@ def _dev(t: torch.Tensor, name: str) -> int:
     return t.data_ptr()
 
 
+def _nbytes(t: torch.Tensor) -> int:
+    return t.numel() * t.element_size()
+
+
+def _sized(t: torch.Tensor, name: str, nbytes: int, dtype=None) -> None:
+    """The library reads or writes exactly nbytes through t's pointer: a
+    buffer of another size (or dtype) is refused here, before any launch."""
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if _nbytes(t) != nbytes:
+        raise ValueError(f"{name} holds {_nbytes(t)} bytes; this call uses {nbytes}")
+
+
+_ACT = (torch.float16, torch.bfloat16)
+
+
+def _check_weights(Wq, scales, biases, N: int, K: int, bits: int, group: int,
+                   tag: str = "") -> None:
+    """Sizes of one packed weight matrix; checked only when the arguments are
+    otherwise valid (the library reports invalid ones with its own status)."""
+    if bits not in (2, 3, 4, 5, 6, 8) or group not in (32, 64, 128) or K <= 0 or N <= 0:
+        return
+    if K % group or (K * bits) % 32:
+        return
+    _sized(Wq, f"Wq{tag}", N * K * bits // 8)
+    _sized(scales, f"scales{tag}", 2 * N * (K // group), torch.float16)
+    _sized(biases, f"biases{tag}", 2 * N * (K // group), torch.float16)
+
+
+def _check_out(out, name: str, numel: int, dtype) -> None:
+    if out.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {out.dtype}")
+    _sized(out, name, numel * out.element_size())
+
+
 def aq_status_string(status: int) -> str:
     return load().aq_status_string(status).decode()
 
@@ -134,6 +169,8 @@ def aq_pack(codes: torch.Tensor, bits: int, words: Optional[torch.Tensor] = None
         raise ValueError("codes must be uint8")
     if words is None:
         words = torch.empty((N, K * bits // 32), dtype=torch.int32, device=codes.device)
+    elif bits in (2, 3, 4, 5, 6, 8) and K % 32 == 0:
+        _sized(words, "words", N * K * bits // 8)
     _check(load().aq_pack(_dev(codes, "codes"), N, K, bits, _dev(words, "words"),
                           _stream(stream)), "aq_pack")
     return words
@@ -173,8 +210,11 @@ def _mm(variant: int, dtype: int, x, Wq, scales, biases, bits, out, stream) -> t
     K = x.shape[-1]
     M = x.numel() // K if K else 0
     N = scales.shape[0]
+    if bits in (3, 4):
+        _check_weights(Wq, scales, biases, N, K, bits, 64)
     if out is None:
         out = torch.empty((*x.shape[:-1], N), dtype=x.dtype, device=x.device)
+    _check_out(out, "out", M * N, x.dtype)
     _check(load().aq_matmul_variant(variant, dtype, _dev(x, "x"), _dev(Wq, "Wq"),
                                     _dev(scales, "scales"), _dev(biases, "biases"), M, N, K,
                                     bits, _dev(out, "out"), _stream(stream)), "aq_matmul")
@@ -194,12 +234,16 @@ def aq_matmul_bf16(x, Wq, scales, biases, bits, out=None, stream=None) -> torch.
 def aq_matmul_ex(x, Wq, scales, biases, bits, group_size, out=None, stream=None):
     """Any code width of 2/3/4/5/6/8 bits and group size of 32/64/128; the
     dtype follows x (fp16 or bf16)."""
+    if x.dtype not in _ACT:
+        raise ValueError("x must be float16 or bfloat16")
     dtype = AQ_BF16 if x.dtype == torch.bfloat16 else AQ_F16
     K = x.shape[-1]
     M = x.numel() // K if K else 0
     N = scales.shape[0]
+    _check_weights(Wq, scales, biases, N, K, bits, group_size)
     if out is None:
         out = torch.empty((*x.shape[:-1], N), dtype=x.dtype, device=x.device)
+    _check_out(out, "out", M * N, x.dtype)
     _check(load().aq_matmul_ex(dtype, _dev(x, "x"), _dev(Wq, "Wq"), _dev(scales, "scales"),
                                _dev(biases, "biases"), M, N, K, bits, group_size,
                                _dev(out, "out"), _stream(stream)), "aq_matmul_ex")
@@ -210,11 +254,19 @@ def aq_attention_decode(q, k, v, bits, group_size, out=None, stream=None) -> tor
     """Decode attention over a quantised KV cache.  q [H, D] (fp16 or bf16);
     k and v are (words [KV, N, D*bits/32] int32, scales [KV, N, D/group] fp16,
     biases [KV, N, D/group] fp16).  Returns o [H, D] in q's dtype."""
+    if q.dtype not in _ACT:
+        raise ValueError("q must be float16 or bfloat16")
     dtype = AQ_BF16 if q.dtype == torch.bfloat16 else AQ_F16
     H, D = q.shape
     KV, N = k[0].shape[0], k[0].shape[1]
+    if bits in (4, 8) and group_size in (32, 64, 128) and D > 0 and D % group_size == 0:
+        for side, (w, sc, bi) in (("k", k), ("v", v)):
+            _sized(w, f"{side}_words", KV * N * D * bits // 8)
+            _sized(sc, f"{side}_scales", 2 * KV * N * (D // group_size), torch.float16)
+            _sized(bi, f"{side}_biases", 2 * KV * N * (D // group_size), torch.float16)
     if out is None:
         out = torch.empty((H, D), dtype=q.dtype, device=q.device)
+    _check_out(out, "out", H * D, q.dtype)
     _check(load().aq_attention_decode(dtype, _dev(q, "q"), _dev(k[0], "k_words"),
                                       _dev(k[1], "k_scales"), _dev(k[2], "k_biases"),
                                       _dev(v[0], "v_words"), _dev(v[1], "v_scales"),
@@ -244,8 +296,15 @@ def aq_matmul_multi(x, weights, bits, outs=None, stream=None) -> list:
     K = x.shape[-1]
     M = x.numel() // K if K else 0
     Ns = [w[1].shape[0] for w in weights]
+    if bits in (3, 4):
+        for j, (w, n) in enumerate(zip(weights, Ns)):
+            _check_weights(w[0], w[1], w[2], n, K, bits, 64, f"[{j}]")
     if outs is None:
         outs = [torch.empty((*x.shape[:-1], n), dtype=x.dtype, device=x.device) for n in Ns]
+    if len(outs) != P:
+        raise ValueError("one output per projection")
+    for j, (o, n) in enumerate(zip(outs, Ns)):
+        _check_out(o, f"outs[{j}]", M * n, x.dtype)
     ptr_arr = ctypes.c_void_p * max(P, 1)
     Wp = ptr_arr(*[_dev(w[0], "Wq") for w in weights])
     Sp = ptr_arr(*[_dev(w[1], "scales") for w in weights])
@@ -267,8 +326,12 @@ def aq_matmul_gate_up(x, gate, up, bits, out=None, stream=None) -> torch.Tensor:
     K = x.shape[-1]
     M = x.numel() // K if K else 0
     N = gate[1].shape[0]
+    if bits in (3, 4):
+        _check_weights(gate[0], gate[1], gate[2], N, K, bits, 64, " (gate)")
+        _check_weights(up[0], up[1], up[2], N, K, bits, 64, " (up)")
     if out is None:
         out = torch.empty((*x.shape[:-1], N), dtype=x.dtype, device=x.device)
+    _check_out(out, "out", M * N, x.dtype)
     _check(load().aq_matmul_gate_up(dtype, _dev(x, "x"), _dev(gate[0], "Wq"),
                                     _dev(gate[1], "scales"), _dev(gate[2], "biases"),
                                     _dev(up[0], "Wq"), _dev(up[1], "scales"),
@@ -292,6 +355,11 @@ def aq_matmul_host(x_host: torch.Tensor, Wq, scales, biases, bits, out_host: tor
     K = x_host.shape[-1]
     M = x_host.numel() // K
     N = scales.shape[0]
+    if bits in (3, 4):
+        _check_weights(Wq, scales, biases, N, K, bits, 64)
+    _check_out(out_host, "out_host", M * N, x_host.dtype)
+    _check_out(x_dev, "x_dev", M * K, x_host.dtype)
+    _check_out(out_dev, "out_dev", M * N, x_host.dtype)
     _check(load().aq_matmul_host(dtype, x_host.data_ptr(), _dev(Wq, "Wq"),
                                  _dev(scales, "scales"), _dev(biases, "biases"), M, N, K, bits,
                                  out_host.data_ptr(), _dev(x_dev, "x_dev"),
