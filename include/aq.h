@@ -1,6 +1,9 @@
 /*
  * aq.h — C ABI of libaq: y = x . W^T over MLX-style affine group-64 weights
- * at 3 or 4 bits, on one NVIDIA GB300 (sm_103a).
+ * at 3 or 4 bits, on one NVIDIA GB300 (sm_103a).  Around it: packing and the
+ * float -> affine quantiser, several projections of one x per call (q/k/v,
+ * gate/up with SiLU), other code widths and group sizes, and decode
+ * attention over a KV cache stored in the same format.
  *
  * Weight format (mlx-bun pages, @mlx-bun/inference 1.0.0,
  * kernels/quantization/affine-split-mma.ts helper affine_unit and
@@ -33,10 +36,12 @@
  *     call after call (fixed-order reductions, no atomics on data).
  *   - Consecutive matmul calls on one stream overlap (programmatic dependent
  *     launch): a call may start reading its Wq, scales and biases while the
- *     previous matmul call on the stream is still running, and reads x and
- *     writes out only after that call has finished.  So out_dev of a matmul
- *     call must not alias Wq_dev, scales_dev or biases_dev of the next
- *     matmul call on the same stream; everything else follows stream order.
+ *     previous call on the stream is still running, and reads x and writes
+ *     out only after that call has finished.  So the output of a matmul or
+ *     attention call must not alias Wq_dev, scales_dev or biases_dev of the
+ *     next matmul call on the same stream; everything else follows stream
+ *     order (aq_attention_decode reads nothing before the previous call has
+ *     finished).
  */
 #ifndef AQ_H
 #define AQ_H
