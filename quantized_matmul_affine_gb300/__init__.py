@@ -256,6 +256,8 @@ def aq_attention_decode(q, k, v, bits, group_size, out=None, stream=None) -> tor
     biases [KV, N, D/group] fp16).  Returns o [H, D] in q's dtype."""
     if q.dtype not in _ACT:
         raise ValueError("q must be float16 or bfloat16")
+    if q.dim() != 2 or len(k) != 3 or len(v) != 3 or any(t.dim() != 3 for t in (*k, *v)):
+        raise ValueError("q must be [H, D]; k and v (words, scales, biases), each [KV, N, ...]")
     dtype = AQ_BF16 if q.dtype == torch.bfloat16 else AQ_F16
     H, D = q.shape
     KV, N = k[0].shape[0], k[0].shape[1]

@@ -76,3 +76,11 @@ def test_pack_checks_the_words_buffer():
     codes = torch.zeros((4, 64), dtype=torch.uint8)
     with pytest.raises(ValueError, match="words holds"):
         aq.aq_pack(codes, 3, words=torch.zeros((4, 5), dtype=torch.int32))
+
+
+def test_attention_wants_three_dimensional_caches():
+    q = torch.zeros((4, 64), dtype=torch.bfloat16)
+    flat = (torch.zeros((20, 8), dtype=torch.int32), torch.zeros((20, 2), dtype=torch.float16),
+            torch.zeros((20, 2), dtype=torch.float16))
+    with pytest.raises(ValueError, match=r"\[KV, N"):
+        aq.aq_attention_decode(q, flat, flat, 4, 32)
