@@ -307,12 +307,21 @@ int aq_select(int64_t M, int64_t N, int64_t K, int bits, int dtype);
 int aq_describe(int64_t M, int64_t N, int64_t K, int bits, int dtype, char *buf, int buflen);
 
 /*
- * aq_stats — per-variant call counters since load (or the last reset).
+ * aq_stats — per-variant call counters since load (or the last
+ * aq_stats_reset), so a caller or a test can assert which kernel actually
+ * ran.  This follows the dispatch counter of the mlx-bun 0.0.4 page
+ * (src/model/fused-decode-kernel.ts, fusedKernelCalls, which a gate test
+ * reads to confirm the fused kernel ran), kept per variant here.
  *   calls  host array of n uint64; element v receives the number of calls
- *          that launched variant v (n may be less than AQ_NUM_VARIANTS).
- *   reset  non-zero: set the counters to zero after reading.
+ *          that launched variant v (n may be less than AQ_NUM_VARIANTS;
+ *          variants past n are not reported).
+ * Errors: AQ_ERR_INVALID_ARG if n < 0, or calls is NULL while n > 0.
+ * Counting is on the host at launch time (atomic, thread-safe).
  */
-aq_status aq_stats(uint64_t *calls, int n, int reset);
+aq_status aq_stats(uint64_t *calls, int n);
+
+/* aq_stats_reset — set every counter of aq_stats to zero. */
+void aq_stats_reset(void);
 
 /*
  * aq_device_error — read the device-side error word that kernels set when a
@@ -325,12 +334,22 @@ aq_status aq_device_error(uint32_t *code, int clear);
 
 /*
  * aq_free — release library-held resources (cached device attributes and
- * kernel configuration state).  The library holds no device allocations;
- * calling aq_free is optional and the library stays usable afterwards.
+ * kernel configuration state).  The pages' host wrapper (affineSplitMma in
+ * affine-split-mma.ts) borrows its inputs and returns an array the caller
+ * owns, so nothing the caller passes is ever freed by the library; this
+ * call releases only what the library keeps for itself.  It holds no device
+ * allocations; calling aq_free is optional and the library stays usable
+ * afterwards (state is rebuilt on the next call).
  */
 void aq_free(void);
 
-/* Human-readable name of a status code (static storage, never NULL). */
+/*
+ * aq_status_string — human-readable name of a status code (static storage,
+ * never NULL; "unknown status" for values outside aq_status).  The pages'
+ * host wrapper reports a bad call by throwing with a message (affineSplitMma
+ * throws "no rows" for M < 1); a C ABI returns the status instead and this
+ * gives its text.
+ */
 const char *aq_status_string(aq_status status);
 
 /* Human-readable name of a variant ("generic", "qmv", "tc", "gemv", "tcw"); "?" if unknown. */

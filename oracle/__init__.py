@@ -71,6 +71,8 @@ def _load() -> ctypes.CDLL:
             lib.oracle_quantize_g.argtypes = [p, i64, i64, i32, i32, p, p, p]
             lib.oracle_attention.argtypes = [p, p, p, p, p, p, p, i64, i64, i64, i64, i32, i32,
                                              p, p, p]
+            lib.oracle_gate_up_cols.argtypes = [p, p, p, p, p, p, p, i64, i64, i64, i32, p, i64,
+                                                p, p, p, p, p, p]
             lib.oracle_f32_to_f16.argtypes = [ctypes.c_float]
             lib.oracle_f32_to_f16.restype = ctypes.c_uint16
             lib.oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
@@ -78,7 +80,7 @@ def _load() -> ctypes.CDLL:
             for f in ("oracle_pack", "oracle_unpack", "oracle_dequant", "oracle_matmul",
                       "oracle_matmul_cols", "oracle_matmul_threads", "oracle_quantize",
                       "oracle_pack_g", "oracle_unpack_g", "oracle_dequant_g", "oracle_matmul_g",
-                      "oracle_quantize_g", "oracle_attention"):
+                      "oracle_quantize_g", "oracle_attention", "oracle_gate_up_cols"):
                 getattr(lib, f).restype = i32
             _lib = lib
     return _lib
@@ -172,6 +174,39 @@ def matmul_cols(x: np.ndarray, words: np.ndarray, scales: np.ndarray, biases: np
     _check(_load().oracle_matmul_cols(_ptr(x), _ptr(words), _ptr(s), _ptr(b), M, N, K, bits,
                                       _ptr(c), len(c), _ptr(y), _ptr(bound)), "matmul_cols")
     return y, bound
+
+
+def gate_up(x: np.ndarray, gate, up, bits: int, cols: Optional[Sequence[int]] = None):
+    """h = silu(g) * u with g = x . dequant(W_gate)^T, u = x . dequant(W_up)^T
+    and silu(g) = g / (1 + exp(-g)), all in float64 (the gate/up epilogue of
+    the mlx-bun 0.4.0 -> 1.0.0 page, src/model/trellis-shared-m.ts).
+
+    gate, up: (words, scales, biases) each, laid out as for matmul().  cols:
+    output columns to compute (all when None).  Returns a dict of [M, ncols]
+    arrays: h, g, u, silu (= silu(g)), bound_g, bound_u (sum_k |x*w| of each
+    product, for the tolerance)."""
+    x = _f64(x)
+    wg, sg, bg = gate
+    wu, su, bu = up
+    wg = np.ascontiguousarray(wg, dtype=np.uint32)
+    wu = np.ascontiguousarray(wu, dtype=np.uint32)
+    sg, bg, su, bu = _f64(sg), _f64(bg), _f64(su), _f64(bu)
+    M, K = x.shape
+    N = wg.shape[0]
+    if wu.shape != wg.shape:
+        raise ValueError("gate and up weights differ in shape")
+    if cols is None:
+        c, ncols, cp = None, N, None
+    else:
+        c = np.ascontiguousarray(cols, dtype=np.int64)
+        ncols, cp = len(c), _ptr(c)
+    out = {k: np.zeros((M, ncols), np.float64)
+           for k in ("h", "g", "u", "silu", "bound_g", "bound_u")}
+    _check(_load().oracle_gate_up_cols(
+        _ptr(x), _ptr(wg), _ptr(sg), _ptr(bg), _ptr(wu), _ptr(su), _ptr(bu), M, N, K, bits,
+        cp, ncols, *(_ptr(out[k]) for k in ("h", "g", "u", "silu", "bound_g", "bound_u"))),
+        "gate_up")
+    return out
 
 
 def tolerance(bound: np.ndarray) -> np.ndarray:

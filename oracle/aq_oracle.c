@@ -199,6 +199,52 @@ int oracle_matmul_cols(const double *x, const uint32_t *words, const double *sca
 }
 
 /*
+ * Gated MLP input of a decoder layer, h = silu(g) * u, where
+ *   g[m][n] = sum_k x[m][k] * w_gate[n][k]   (oracle_element on the gate weights)
+ *   u[m][n] = sum_k x[m][k] * w_up[n][k]     (oracle_element on the up weights)
+ *   silu(g) = g * sigmoid(g) = g / (1 + exp(-g)).
+ * The mlx-bun 0.4.0 -> 1.0.0 page (src/model/trellis-shared-m.ts, the gate/up
+ * kernel's epilogue) forms sigmoid(gate) = 1 / (1 + exp(-gate)), multiplies
+ * it by gate and the result by up.  The pages round gate, up, the sigmoid and
+ * the product to the activation type at every step; the operator itself is
+ * the exact value, computed here in double precision from the exact fp64
+ * products.  Columns: cols[j] for j < ncols, or every column 0..N-1 in order
+ * when cols is NULL (ncols must then be N).  Outputs are [M][ncols]; any of
+ * g, u, silu, bound_g, bound_u may be NULL.
+ */
+int oracle_gate_up_cols(const double *x, const uint32_t *wg, const double *sg, const double *bg,
+                        const uint32_t *wu, const double *su, const double *bu, int64_t M,
+                        int64_t N, int64_t K, int bits, const int64_t *cols, int64_t ncols,
+                        double *h, double *g, double *u, double *silu, double *bound_g,
+                        double *bound_u) {
+    if (!valid_shape(N, K, bits) || M < 0 || ncols < 0) return 1;
+    if (cols == NULL && ncols != N) return 1;
+    const int64_t wpr = oracle_words_per_row(K, bits);
+    const int64_t G = K / ORACLE_GROUP;
+    for (int64_t j = 0; j < ncols; ++j)
+        if (cols != NULL && (cols[j] < 0 || cols[j] >= N)) return 1;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t j = 0; j < ncols; ++j) {
+            const int64_t n = cols != NULL ? cols[j] : j;
+            const int64_t o = m * ncols + j;
+            double gv, uv, gb, ub;
+            oracle_element(x + m * K, wg + n * wpr, sg + n * G, bg + n * G, K, bits,
+                           ORACLE_GROUP, &gv, &gb);
+            oracle_element(x + m * K, wu + n * wpr, su + n * G, bu + n * G, K, bits,
+                           ORACLE_GROUP, &uv, &ub);
+            const double sig = 1.0 / (1.0 + exp(-gv));
+            const double sv = gv * sig;
+            h[o] = sv * uv;
+            if (g) g[o] = gv;
+            if (u) u[o] = uv;
+            if (silu) silu[o] = sv;
+            if (bound_g) bound_g[o] = gb;
+            if (bound_u) bound_u[o] = ub;
+        }
+    return 0;
+}
+
+/*
  * Row-parallel form of oracle_matmul: output columns are dealt out to
  * nthreads POSIX threads in contiguous blocks.  Every element is computed by
  * exactly the same oracle_element call, so the result is identical to the

@@ -25,7 +25,8 @@ __all__ = [
     "AQ_VARIANT_TC", "AQ_VARIANT_GEMV", "AQ_VARIANT_TCW", "AQ_NUM_VARIANTS", "aq_pack", "aq_quantize",
     "aq_quantize_bf16", "aq_matmul", "aq_matmul_bf16", "aq_matmul_multi", "aq_matmul_gate_up",
     "aq_matmul_ex", "aq_quantize_ex", "aq_attention_decode", "aq_attention_describe",
-    "aq_matmul_variant", "aq_matmul_host", "aq_select", "aq_describe", "aq_stats", "aq_device_error",
+    "aq_matmul_variant", "aq_matmul_host", "aq_select", "aq_describe", "aq_stats", "aq_stats_reset",
+    "aq_device_error",
     "aq_free", "aq_status_string", "aq_variant_name", "aq_version", "lib_path", "load",
 ]
 
@@ -78,7 +79,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "aq_select": ([i64, i64, i64, i32, i32], i32),
         "aq_describe": ([i64, i64, i64, i32, i32, p, i32], i32),
         "aq_attention_describe": ([i64, i64, i64, i64, i32, i32, p, i32], i32),
-        "aq_stats": ([p, i32, i32], i32),
+        "aq_stats": ([p, i32], i32),
+        "aq_stats_reset": ([], None),
         "aq_device_error": ([u32p, i32], i32),
         "aq_free": ([], None),
         "aq_status_string": ([i32], ctypes.c_char_p),
@@ -388,10 +390,16 @@ def aq_attention_describe(H: int, KV: int, N: int, D: int, bits: int, group_size
 
 
 def aq_stats(reset: bool = False) -> List[int]:
+    """Calls per variant (aq_stats); reset=True also calls aq_stats_reset."""
     buf = (ctypes.c_uint64 * AQ_NUM_VARIANTS)()
-    _check(load().aq_stats(ctypes.cast(buf, ctypes.c_void_p), AQ_NUM_VARIANTS, int(reset)),
-           "aq_stats")
+    _check(load().aq_stats(ctypes.cast(buf, ctypes.c_void_p), AQ_NUM_VARIANTS), "aq_stats")
+    if reset:
+        aq_stats_reset()
     return list(buf)
+
+
+def aq_stats_reset() -> None:
+    load().aq_stats_reset()
 
 
 def aq_device_error(clear: bool = False) -> int:

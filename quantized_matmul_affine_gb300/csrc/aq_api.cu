@@ -453,13 +453,14 @@ int aq_attention_describe(int64_t H, int64_t KV, int64_t N, int64_t D, int bits,
     return attention_describe(H, KV, N, D, bits, group_size, buf, buflen);
 }
 
-aq_status aq_stats(uint64_t *calls, int n, int reset) {
+aq_status aq_stats(uint64_t *calls, int n) {
     if (n < 0 || (n > 0 && !calls)) return AQ_ERR_INVALID_ARG;
-    for (int v = 0; v < AQ_NUM_VARIANTS; ++v) {
-        const uint64_t c = reset ? g_calls[v].exchange(0) : g_calls[v].load();
-        if (v < n) calls[v] = c;
-    }
+    for (int v = 0; v < AQ_NUM_VARIANTS && v < n; ++v) calls[v] = g_calls[v].load();
     return AQ_OK;
+}
+
+void aq_stats_reset(void) {
+    for (auto &c : g_calls) c.store(0);
 }
 
 aq_status aq_device_error(uint32_t *code, int clear) {

@@ -63,3 +63,19 @@ def matmul_examples():
         biases = np.array([[float(v) for v in r.split(",")] for r in biases.split(";")])
         yield (name, int(bits), K, codes, scales, biases, x_from_rule(xrule, K),
                np.array([float(v) for v in y.split(";")]))
+
+
+
+def gate_up_examples():
+    """(name, bits, K, gate, up, x, h): gate and up are (codes [1, K], scales
+    [1, K/64], biases [1, K/64]) with one scale and one bias for every group."""
+    for (name, bits, K, gcodes, gs, gb, ucodes, us, ub, xrule,
+         h) in _lines("gate_up_examples.txt"):
+        K = int(K)
+        G = K // 64
+
+        def w(codes, sc, bi):
+            return (codes_from_rule(codes, K)[None, :], np.full((1, G), float(sc)),
+                    np.full((1, G), float(bi)))
+        yield (name, int(bits), K, w(gcodes, gs, gb), w(ucodes, us, ub), x_from_rule(xrule, K),
+               float(h))

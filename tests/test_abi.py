@@ -92,9 +92,52 @@ def test_pack_validation():
 
 def test_stats_interface():
     lib = _raw()
-    assert lib.aq_stats(None, -1, 0) == 1
-    assert lib.aq_stats(None, 0, 0) == 0
+    assert lib.aq_stats(None, -1) == 1
+    assert lib.aq_stats(None, 0) == 0
     assert len(aq.aq_stats()) == aq.AQ_NUM_VARIANTS
+    aq.aq_stats_reset()
+    assert aq.aq_stats() == [0] * aq.AQ_NUM_VARIANTS
+
+
+def _declaration(name):
+    text = open(os.path.join(ROOT, "include", "aq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    m = re.search(r"([A-Za-z_][A-Za-z0-9_ \*]*?)\b" + name + r"\s*\(([^)]*)\)\s*;", text)
+    assert m, name
+    ret = " ".join(m.group(1).split())
+    params = [" ".join(p.split()) for p in m.group(2).split(",")]
+    return ret, params
+
+
+# The boundary's signatures as the scope table of the build fixes them
+# (parameter names aside): return type and parameter types in order.
+@pytest.mark.parametrize("name,ret,types", [
+    ("aq_pack", "aq_status", ["const uint8_t *", "int64_t", "int64_t", "int", "uint32_t *",
+                              "void *"]),
+    ("aq_matmul", "aq_status", ["const void *", "const uint32_t *", "const void *",
+                                "const void *", "int64_t", "int64_t", "int64_t", "int", "void *",
+                                "void *"]),
+    ("aq_matmul_bf16", "aq_status", ["const void *", "const uint32_t *", "const void *",
+                                     "const void *", "int64_t", "int64_t", "int64_t", "int",
+                                     "void *", "void *"]),
+    ("aq_free", "void", ["void"]),
+    ("aq_status_string", "const char *", ["aq_status"]),
+    ("aq_stats", "aq_status", ["uint64_t *", "int"]),
+    ("aq_stats_reset", "void", ["void"]),
+])
+def test_boundary_signatures(name, ret, types):
+    r, params = _declaration(name)
+    assert r.replace(" *", " *") == ret or r == ret.replace(" *", "*"), (name, r)
+    got = []
+    for p in params:
+        if p == "void":
+            got.append("void")
+            continue
+        # drop the parameter name: the last identifier
+        t = re.sub(r"\s*\b[A-Za-z_][A-Za-z0-9_]*$", "", p)
+        got.append(" ".join(t.replace("*", " * ").split()).replace(" *", " *"))
+    norm = [" ".join(t.replace("*", " * ").split()) for t in types]
+    assert got == norm, (name, got)
 
 
 # The dispatch rule, on the shapes of the workloads (alignment assumed).

@@ -10,7 +10,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 def test_reference_arm_line():
     out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "3",
-                          "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=300)
+                          "--warmup", "3", "--ref-budget", "3"], cwd=ROOT, capture_output=True, text=True, timeout=300)
     assert out.returncode == 0, out.stderr[-2000:]
     lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
     assert len(lines) == 1

@@ -4,7 +4,8 @@ through the C ABI.
 aq_matmul_multi: every projection's y within the matmul tolerance
 |y - y_ref| <= 2e-3 * sum_k |x_k w_nk| + 1e-5.
 
-aq_matmul_gate_up: h = silu(g) * u with g, u the gate and up products.  With
+aq_matmul_gate_up: h = silu(g) * u with g, u the gate and up products, against
+oracle.gate_up (the float64 operator, pinned in tests/test_oracle_gate_up.py).  With
 tg, tu the matmul tolerances of g and u and |silu'| <= 1.1,
 |h - h_ref| <= 1.1 tg (|u| + tu) + (|silu(g)| + 1.1 tg) tu, plus one rounding
 of h to the output type (2^-8 relative for bf16, 2^-11 for fp16).
@@ -92,16 +93,12 @@ def test_multi_matches_single_calls_bitwise():
         assert torch.equal(y.view(torch.int16), z.view(torch.int16))
 
 
-def _silu(g):
-    return g / (1.0 + np.exp(-g))
-
-
 def _check_gate_up(h, pg, pu, x_bits, dtype, cols=None):
-    g, bg = _ref(pg, x_bits, dtype, cols)
-    u, bu = _ref(pu, x_bits, dtype, cols)
-    tg, tu = oracle.tolerance(bg), oracle.tolerance(bu)
-    s = _silu(g)
-    h_ref = s * u
+    x = workloads.to_f64(x_bits, dtype)
+    r = oracle.gate_up(x, (oracle.pack(pg.codes, pg.bits), pg.scales, pg.biases),
+                       (oracle.pack(pu.codes, pu.bits), pu.scales, pu.biases), pg.bits, cols)
+    h_ref, u, s = r["h"], r["u"], r["silu"]
+    tg, tu = oracle.tolerance(r["bound_g"]), oracle.tolerance(r["bound_u"])
     e1 = 1.1 * tg * (np.abs(u) + tu) + (np.abs(s) + 1.1 * tg) * tu
     rnd = 2.0**-8 if dtype == "bf16" else 2.0**-11
     tol = e1 + rnd * (np.abs(h_ref) + e1) + 1e-7
