@@ -4,6 +4,12 @@ Each .cu file is compiled in parallel, then linked into
 quantized_matmul_affine_gb300/_build/libaq.so (the CUDA runtime is linked
 statically, so the library loads on machines without a GPU driver; kernels
 need one to run).  Usage: ``python -m quantized_matmul_affine_gb300.build``.
+
+The same sources are also built, in the same pool, into
+_build/test/libaq_test.so with AQ_TEST_HOOKS defined and the pipeline wait
+limit cut to 1 ms: a test-only library in which a producer can be told to
+withhold the copies of its first stage (aq_test_withhold), so that a test
+can watch a bounded wait give up.  The package never loads it.
 """
 from __future__ import annotations
 
@@ -18,6 +24,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libaq.so")
+TEST_BUILD = os.path.join(BUILD, "test")
+TEST_LIB = os.path.join(TEST_BUILD, "libaq_test.so")
+TEST_FLAGS = ["-DAQ_TEST_HOOKS=1", "-DAQ_WAIT_LIMIT_NS=1000000ull"]
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -41,43 +50,51 @@ def _deps():
         glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    if not force and up_to_date():
+    """Build libaq.so (and the test-only libaq_test.so) unless up to date."""
+    targets = [(LIB, BUILD, [])]
+    if extra_flags is None:
+        targets.append((TEST_LIB, TEST_BUILD, TEST_FLAGS))
+    targets = [t for t in targets if force or not up_to_date(t[0])]
+    if not targets:
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
-    flags = NVCC_FLAGS + list(extra_flags or [])
-    objs = []
-    jobs = []
-    for src in _sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        objs.append(obj)
-        jobs.append([cc] + flags + ["-c", src, "-o", obj])
+    jobs, links = [], []
+    for lib, out_dir, defs in targets:
+        os.makedirs(out_dir, exist_ok=True)
+        flags = NVCC_FLAGS + defs + list(extra_flags or [])
+        objs = []
+        for src in _sources():
+            obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
+            objs.append(obj)
+            jobs.append([cc] + flags + ["-c", src, "-o", obj])
+        links.append((lib, objs))
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
         return cmd, r
 
-    with concurrent.futures.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
+    with concurrent.futures.ThreadPoolExecutor(max_workers=max(4, os.cpu_count() or 4)) as ex:
         for cmd, r in ex.map(run, jobs):
             if verbose or r.returncode != 0:
                 sys.stderr.write(r.stdout + r.stderr)
             if r.returncode != 0:
                 raise RuntimeError("nvcc failed: " + " ".join(cmd))
-    tmp = LIB + f".tmp{os.getpid()}"
-    link = [cc] + ARCH + ["-shared", "-Xcompiler", "-fPIC", "-o", tmp] + objs
-    r = subprocess.run(link, capture_output=True, text=True)
-    if r.returncode != 0:
-        sys.stderr.write(r.stdout + r.stderr)
-        raise RuntimeError("link failed")
-    os.replace(tmp, LIB)
+    for lib, objs in links:
+        tmp = lib + f".tmp{os.getpid()}"
+        link = [cc] + ARCH + ["-shared", "-Xcompiler", "-fPIC", "-o", tmp] + objs
+        r = subprocess.run(link, capture_output=True, text=True)
+        if r.returncode != 0:
+            sys.stderr.write(r.stdout + r.stderr)
+            raise RuntimeError("link failed")
+        os.replace(tmp, lib)
     return LIB
 
 

@@ -21,9 +21,10 @@ namespace {
 std::atomic<uint64_t> g_calls[AQ_NUM_VARIANTS];
 std::atomic<int> g_sms_cache[64];
 
-// Largest M that the small-M kernel takes under the automatic rule, from
-// timings of both kernels on GB300 (see the dispatch table in the design
-// notes).  AQ_QMV_MAX_M overrides it for experiments.
+// Largest M that the streaming small-M kernel takes under the automatic rule
+// when the resident kernel does not apply: past 16 rows the tensor-core
+// kernel measured faster on GB300.  AQ_QMV_MAX_M overrides it for
+// experiments.
 int qmv_max_m() {
     static const int v = [] {
         const char *e = std::getenv("AQ_QMV_MAX_M");
@@ -34,6 +35,10 @@ int qmv_max_m() {
 }
 
 }  // namespace
+
+#ifdef AQ_TEST_HOOKS
+int g_test_withhold = 0;
+#endif
 
 int num_sms() {
     int dev = 0;
@@ -504,5 +509,11 @@ const char *aq_variant_name(int variant) {
 }
 
 const char *aq_version(void) { return "aq 0.1.0 (sm_103a)"; }
+
+#ifdef AQ_TEST_HOOKS
+// Test builds only: make a producer withhold the copies of its first stage
+// (see g_test_withhold), so that a test can watch a bounded wait run out.
+void aq_test_withhold(int what) { aq::g_test_withhold = what; }
+#endif
 
 }  // extern "C"

@@ -254,6 +254,9 @@ cudaError_t launch_plan(const MatmulArgs &a, GemvPlan &pl, const uint32_t *const
         maps.b[j] = maps.b[0];
     }
     pl.prm.err = gemv::error_word();
+#ifdef AQ_TEST_HOOKS
+    pl.prm.withhold = g_test_withhold == 1;
+#endif
     if (!pl.prm.err) return cudaErrorInvalidValue;
     using gemv::launch_blocks;
     if (pl.mp) {

@@ -108,6 +108,9 @@ struct GemvParams {
     uint32_t off_xst;       // staged x: box inside a ring slot
     int x_rows;             // staged x: rows per group in the box (= M)
     uint32_t stage_tx;      // bytes one stage brings in
+#ifdef AQ_TEST_HOOKS
+    int withhold;           // test builds only: the producer skips its first stage
+#endif
 };
 
 // Several projections of the same x in one launch (kernels instantiated
@@ -403,7 +406,13 @@ __global__ void __launch_bounds__(kGemvThreads, MB > 1 ? 1 : 2)
                         tm = map_of(pass);
                     }
                 uint8_t *dst = smem + (size_t)slot * p.slot_bytes;
-                if (lane == 3) {
+#ifdef AQ_TEST_HOOKS
+                const bool withheld = p.withhold && it == 0;  // nothing completes full[0]
+#else
+                constexpr bool withheld = false;
+#endif
+                if (withheld) {
+                } else if (lane == 3) {
                     tma_load_3d(dst + p.off_xst, tm, 0, 0, s * p.sg, &full[slot]);
                 } else if (lane == 0) {
                     mbar_arrive_expect_tx(&full[slot], p.stage_tx);
@@ -428,10 +437,8 @@ __global__ void __launch_bounds__(kGemvThreads, MB > 1 ? 1 : 2)
             // Copies still in flight must land before the CTA may exit.
             if (lane == 0)
                 for (int j = std::max(0, it - p.ring); j < it; ++j)
-                    if (!mbar_wait_sleep(&full[j % p.ring], (j / p.ring) & 1, 512)) {
-                        gemv_record(flag, p.err, ERR_GEMV_DRAIN);
-                        break;
-                    }
+                    if (!mbar_wait_sleep(&full[j % p.ring], (j / p.ring) & 1, 512))
+                        gemv_record(flag, p.err, ERR_GEMV_DRAIN);  // and wait for the others
         }
         return;
     }

@@ -95,6 +95,13 @@ cudaError_t generic_launch_g(const MatmulArgs &a, int group);
 cudaError_t pack_launch(const uint8_t *codes, int64_t N, int64_t K, int bits, uint32_t *words,
                         cudaStream_t stream);
 
+#ifdef AQ_TEST_HOOKS
+// Test builds only (never in libaq.so): which producer withholds the copies
+// of its first stage, so that the waits on them run out (1 = the resident
+// small-M kernel, 2 = the large-M tensor-core kernel, 0 = none).
+extern int g_test_withhold;
+#endif
+
 // Device error words, one per translation unit that owns bounded waits.
 cudaError_t gemv_read_error(uint32_t *code, bool clear);
 cudaError_t qmv_read_error(uint32_t *code, bool clear);

@@ -76,6 +76,9 @@ struct TcParams {
     // through distributed shared memory.
     int rounds, tail;
     uint32_t off_b, off_raw, off_bar, tmem_cols;
+#ifdef AQ_TEST_HOOKS
+    int withhold;  // test builds only: the x producer skips its first stage
+#endif
 };
 
 __device__ __forceinline__ void tc_record(volatile int *flag, uint32_t code) {
@@ -98,6 +101,18 @@ __device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile
     }
     tc_record(flag, code);
     return false;
+}
+
+// Bounded wait used while winding down: no error is recorded (it only makes
+// sure that copies or MMAs already issued have finished before the CTA
+// releases its shared and tensor memory).
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1; it < (1u << 31); ++it) {
+        if (mbar_try_wait(bar, parity)) return;
+        if ((it & 255u) == 0u && globaltimer_ns() - t0 > AQ_WAIT_LIMIT_NS) return;
+    }
 }
 
 __device__ __forceinline__ float h_at(const uint4 &v, int j) {
@@ -186,7 +201,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     uint64_t *ab_empty = bars + 2 * kStages;
     uint64_t *acc_full = bars + 3 * kStages;
     uint64_t *acc_empty = acc_full + 2;
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(acc_empty + 2);
+    uint64_t *drain = acc_empty + 2;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -220,6 +236,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], 4);
         }
+        mbar_init(drain, 1);
         *flag = 0;
         fence_mbar_init();
     }
@@ -250,6 +267,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     const int slot = it % kStages;
                     const uint32_t ph = (it / kStages) & 1u;
                     if (it >= kStages && !tc_wait(&ab_empty[slot], ph ^ 1u, flag, 0x0102)) goto tma_done;
+#ifdef AQ_TEST_HOOKS
+                    if (p.withhold && it == 0) continue;  // nothing will complete b_full[0]
+#endif
                     mbar_arrive_expect_tx(&b_full[slot], BM * 128);
 #pragma unroll
                     for (int h = 0; h < BM / kNI; ++h)
@@ -257,7 +277,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                                     m0 + h * kNI, &b_full[slot]);
                 }
             }
-        tma_done:;
+        tma_done:
+            // Wind-down: the loads issued for the last stages land before
+            // the CTA goes on (earlier ones were consumed by the MMAs).
+            for (uint32_t j = it > (uint32_t)kStages ? it - kStages : 0u; j < it; ++j)
+                drain_wait(&b_full[j % kStages], (j / kStages) & 1u);
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------------
@@ -272,6 +296,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const uint64_t b_desc0 = sw128_desc(smem_u32(b_ring));
         uint32_t it = 0, ti = 0;
         int tile, gb, ge;
+        bool issued = false;  // warp-uniform
         for (int u = 0; unit_of(u, tile, gb, ge); ++u, ++ti) {
             const uint32_t b = ti % kAcc, use = ti / kAcc;
             const bool free = ti < (uint32_t)kAcc ||
@@ -290,6 +315,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     break;
                 }
                 tc_fence_after();
+                issued = true;
                 if (lane == 0) {
                     const uint64_t ad = a_desc0 + (uint64_t)((uint32_t)(slot * kATileBytes) >> 4);
                     const uint64_t bd = b_desc0 + (uint64_t)((uint32_t)(slot * BM * 128) >> 4);
@@ -306,6 +332,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             }
             if (!ok) break;
             if (lane == 0) tc_commit(&acc_full[b]);
+            __syncwarp();
+        }
+        // Wind-down: every MMA issued has completed (it reads the rings and
+        // writes tensor memory) before the CTA goes on.
+        if (issued) {
+            if (lane == 0) tc_commit(drain);
+            __syncwarp();
+            drain_wait(drain, 0);
             __syncwarp();
         }
     } else if (warp < kWarpDq) {
@@ -461,14 +495,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         cp_async_wait<0>();
     }
 
+    // Copies and MMAs issued have completed (the producers and the MMA
+    // warp drained them, with bounded waits), so shared and tensor memory
+    // may be reused or released from here on, error or not.
     __syncthreads();
-    if (*flag) {
-        // A wait gave up: let copies and MMAs already issued finish before
-        // the tensor memory and shared memory are released.
-        const uint64_t t0 = globaltimer_ns();
-        while (globaltimer_ns() - t0 < 1000000ull) {
-        }
-    }
     if (p.tail > 0 && ((int)blockIdx.x >> 1) < p.tail) {
         // The split tail tile: rank 1 hands its half of the accumulator to
         // rank 0 through distributed shared memory, up to 256 columns at a
@@ -599,7 +629,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     uint64_t *b_full = bars + kWStages;
     uint64_t *ab_empty = bars + 2 * kWStages;
     uint64_t *acc_full = bars + 3 * kWStages;
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(acc_full + 1);
+    uint64_t *drain = acc_full + 1;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -616,6 +647,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             mbar_init(&ab_empty[s], 1);
         }
         mbar_init(acc_full, 1);
+        mbar_init(drain, 1);
         *flag = 0;
         fence_mbar_init();
     }
@@ -632,13 +664,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (warp == kWarpTma) {
         if (lane == 0) {
             grid_dependency_wait();  // x belongs to the stream order
-            for (int i = 0; i < ns; ++i) {
+            int i = 0;
+            for (; i < ns; ++i) {
                 const int slot = i % kWStages;
                 const uint32_t ph = (i / kWStages) & 1u;
                 if (i >= kWStages && !tc_wait(&ab_empty[slot], ph ^ 1u, flag, 0x0702)) break;
                 mbar_arrive_expect_tx(&a_full[slot], kWATile);
                 tma_load_2d(a_ring + slot * kWATile, &tmap_x, 64 * (g0 + i), 0, &a_full[slot]);
             }
+            // Wind-down: the loads issued for the last stages land first.
+            for (int j = i > kWStages ? i - kWStages : 0; j < i; ++j)
+                drain_wait(&a_full[j % kWStages], (uint32_t)(j / kWStages) & 1u);
         }
     } else if (warp == kWarpMma) {
         // D[x row][weight row] += x . W^T: 4 x (M=128, N=256, K=16) per stage
@@ -646,7 +682,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                                ((uint32_t)(kWRows >> 3) << 17) | ((uint32_t)(kWXRows >> 4) << 24);
         const uint64_t a_desc0 = sw128_desc(smem_u32(a_ring));
         const uint64_t b_desc0 = sw128_desc(smem_u32(b_ring));
-        bool ok = true;
+        bool ok = true, issued = false;  // both warp-uniform
         for (int i = 0; i < ns; ++i) {
             const int slot = i % kWStages;
             const uint32_t ph = (i / kWStages) & 1u;
@@ -657,6 +693,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 break;
             }
             tc_fence_after();
+            issued = true;
             if (lane == 0) {
                 const uint64_t ad = a_desc0 + (uint64_t)((uint32_t)(slot * kWATile) >> 4);
                 const uint64_t bd = b_desc0 + (uint64_t)((uint32_t)(slot * kWBTile) >> 4);
@@ -669,6 +706,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
         if (ok && lane == 0) tc_commit(acc_full);
         __syncwarp();
+        // Wind-down: every MMA issued has completed before the CTA goes on.
+        if (issued) {
+            if (lane == 0) tc_commit(drain);
+            __syncwarp();
+            drain_wait(drain, 0);
+            __syncwarp();
+        }
     } else if (warp < kWarpDq) {
         // Epilogue: TMEM lane = x row m = 32q + lane, column = weight row.
         const int q = warp & 3;
@@ -781,14 +825,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         cp_async_wait<0>();
     }
 
+    // Copies and MMAs issued have completed (the producers and the MMA
+    // warp drained them, with bounded waits), so shared and tensor memory
+    // may be reused or released from here on, error or not.
     __syncthreads();
-    if (*flag) {
-        // A wait gave up: let copies and MMAs already issued finish before
-        // the tensor memory and shared memory are released.
-        const uint64_t t0 = globaltimer_ns();
-        while (globaltimer_ns() - t0 < 1000000ull) {
-        }
-    }
     if (S > 1) {
         // Every CTA of the cluster reaches both barriers, error or not.
         // Rank r adds its share of the tile's M x 256 elements over all
@@ -857,7 +897,7 @@ bool tc_plan(const MatmulArgs &a, TcPlan &pl) {
     off += (size_t)kDqWarps * kRawSlots * raw_slot;
     off = (off + 15) / 16 * 16;
     q.off_bar = (uint32_t)off;
-    off += (3 * kStages + 4) * 8 + 16;
+    off += (3 * kStages + 5) * 8 + 16;
     pl.smem = off + 1024;  // room to align the base to 1024 bytes
     if (pl.smem > kSmemLimitTc) return false;
     q.tmem_cols = pl.BM >= 256 ? 512 : pl.BM == 128 ? 256 : 128;
@@ -865,6 +905,9 @@ bool tc_plan(const MatmulArgs &a, TcPlan &pl) {
     q.scales = static_cast<const __half *>(a.scales);
     q.biases = static_cast<const __half *>(a.biases);
     q.y = a.out;
+#ifdef AQ_TEST_HOOKS
+    q.withhold = g_test_withhold == 2;
+#endif
     const int total = q.n_tiles * q.m_tiles;
     int grid = std::min(total, num_sms());
     q.rounds = (total + grid - 1) / grid;
@@ -952,7 +995,7 @@ bool tcw_plan(const MatmulArgs &a, TcwPlan &pl) {
     off += (size_t)kDqWarps * kWRawSlots * raw_slot;
     off = (off + 15) / 16 * 16;
     q.off_bar = (uint32_t)off;
-    off += (3 * kWStages + 1) * 8 + 16;
+    off += (3 * kWStages + 2) * 8 + 16;
     pl.smem = off + 1024;  // room to align the base to 1024 bytes
     if (pl.smem > kSmemLimitTc) return false;
     if ((size_t)kWXRows * kWPitch * 4 > (size_t)kWStages * (kWATile + kWBTile)) return false;

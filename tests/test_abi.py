@@ -34,6 +34,16 @@ def test_library_exports_every_declared_symbol():
     assert not missing, missing
 
 
+def test_test_hook_only_in_the_test_library():
+    # the wait-expiry hook (tests/test_gpu_waits.py) exists only in the
+    # separately built test library, never in libaq.so
+    from quantized_matmul_affine_gb300 import build
+    prod = ctypes.CDLL(aq.lib_path())
+    assert not hasattr(prod, "aq_test_withhold")
+    if build.up_to_date(build.TEST_LIB):
+        assert hasattr(ctypes.CDLL(build.TEST_LIB), "aq_test_withhold")
+
+
 def test_binding_has_the_same_names():
     for n in header_functions():
         assert hasattr(aq, n), n
