@@ -12,18 +12,23 @@
 //   * A = 128 weight rows x 64 k (one group) per stage, dequantised by eight
 //     warps into shared memory as bf16 (x bf16) or fp16 (x fp16) in the
 //     128-byte-swizzled K-major layout the tensor core reads directly;
-//   * B = BM activation rows x 64 k of x, loaded by TMA (tensor map, 128-byte
-//     swizzle) - x is never converted;
-//   * one thread issues tcgen05.mma (M=128, N=BM, K=16) x4 per stage into an
-//     fp32 accumulator in tensor memory; two accumulators alternate so the
-//     epilogue of one tile overlaps the main loop of the next;
+//   * B = x^T, loaded by TMA (tensor map, 128-byte swizzle) in sub-tiles of
+//     min(BM, 256) activation rows x 64 k - x is never converted;
+//   * one thread issues tcgen05.mma (M=128, N=min(BM,256), K=16) x4 per
+//     sub-tile into fp32 accumulators in tensor memory.  A and B have rings
+//     of their own: each B sub-tile is released as soon as its four MMAs
+//     complete (a 512-row x tile is two sub-tiles sharing one A tile) and
+//     each A tile after its last; two accumulators alternate (x tiles up to
+//     256 rows) so the epilogue of one tile overlaps the main loop of the
+//     next;
 //   * four epilogue warps read the accumulator with tcgen05.ld, round to the
 //     output type and store y; persistent CTAs (one per SM) walk the tiles.
 //
 // Roles (448 threads): warp 0 TMA producer, warp 1 MMA issuer and tensor
 // memory owner, warps 2-5 epilogue, warps 6-13 dequantisation (each streams
-// its 16 weight rows through a two-slot cp.async ring).  Every mbarrier wait
-// is bounded; a wait that gives up records an error and the CTA winds down.
+// its 16 weight rows through a cp.async ring of 256-k super-stages).  Every
+// mbarrier wait is bounded; a wait that gives up records an error and the
+// CTA winds down after the copies and MMAs it issued have completed.
 #include "aq_internal.h"
 #include "aq_ptx.cuh"
 
@@ -45,13 +50,20 @@ constexpr int kWarpTma = 0, kWarpMma = 1, kWarpDq = 6, kDqWarps = 8;  // warps 2
 constexpr int kGroups = 4;    // groups per raw super-stage (256 k)
 constexpr int kATileBytes = 128 * 128;
 
-// A/B pipeline depth by x tile width.  The ring has to cover the round trip
-// dequantise -> MMA -> commit -> reuse.
-constexpr int stages_for(int BM) { return BM <= 64 ? 5 : BM <= 128 ? 4 : BM <= 256 ? 3 : 2; }
+// Ring depths by x tile width.  The x tiles come from L2 by TMA in
+// sub-tiles of min(BM, 256) rows x 64 k (8 to 32 KB), each in a slot of its
+// own and released as soon as its four MMAs complete, so that about a
+// microsecond of load latency stays covered at the MMA rate.  A tiles (128
+// weight rows x 64 k, 16 KB) have a ring of their own: a tile's slot comes
+// back one MMA completion plus one dequantisation after its last use, which
+// three or more slots keep off the critical path.
+constexpr int b_slots_for(int BM) { return BM >= 256 ? 4 : BM == 128 ? 5 : 8; }
+constexpr int a_slots_for(int BM) { return BM >= 256 ? 3 : BM == 128 ? 4 : 5; }
+constexpr int ni_for(int BM) { return BM > 256 ? 256 : BM; }
 // Raw super-stages per dequant warp; all but one are in flight while the
 // warp dequantises, so that the weight stream keeps enough bytes in flight
-// to cover the HBM latency (about 55 KB per SM at four slots).
-constexpr int raw_slots_for(int BM) { return BM <= 128 ? 4 : BM <= 256 ? 3 : 2; }
+// to cover the HBM latency.
+constexpr int raw_slots_for(int BM) { return BM <= 128 ? 3 : 2; }
 
 template <int B>
 struct Raw {
@@ -165,6 +177,81 @@ __device__ __forceinline__ uint4 dequant8(uint32_t u, float s, float bb, uint32_
     return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
+// ---------------------------------------------------------------------------
+// Dequantisation of the large-M kernel.  A code q at bit p of a 32-bit word,
+// with 12 <= p and p + bits <= 23, becomes the exact float 2^(23-p) + q once
+// the word is masked to the code and OR-ed with the exponent of 2^(23-p)
+// (the pages' mantissa trick, here with the code at one of a few mantissa
+// positions so that one shift serves two codes).  Then w = (2^E + q) s +
+// (b - 2^E s) in one fp32 fma per value, two values per packed fma; the bias
+// term b - 2^E s is rounded to fp32 once per group (error <= 2^-24 * 2^E s,
+// at most 2^-13 s here), and w is rounded once to the operand type.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kExp11 = 0x45000000u;  // 2048.0f: code at bit 12
+constexpr uint32_t kExp8 = 0x43800000u;   // 256.0f: code at bit 15
+constexpr uint32_t kExp7 = 0x43000000u;   // 128.0f: code at bit 16
+constexpr uint32_t kExp5 = 0x42000000u;   // 32.0f: code at bit 18
+
+__device__ __forceinline__ float code_at(uint32_t t, uint32_t mask, uint32_t expo) {
+    return __uint_as_float((t & mask) | expo);
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack_out(float2 w) {
+    if constexpr (BF16) {
+        return bf16x2(w.x, w.y);
+    } else {
+        return pack_half2(w.x, w.y);
+    }
+}
+
+// Per-group constants of one weight row: the scale and the bias terms of the
+// code positions used (4-bit: codes at bits 16 and 12 alternate, so every
+// pair takes (b - 128 s, b - 2048 s); 3-bit: pairs take (b - 2048 s,
+// b - 256 s) or (b - 32 s, b - 2048 s)).
+struct GroupConst {
+    float2 s2, p1, p2;
+};
+
+template <int B>
+__device__ __forceinline__ GroupConst group_const(float s, float b) {
+    GroupConst c;
+    c.s2 = make_float2(s, s);
+    const float b11 = fmaf(-2048.f, s, b);
+    if constexpr (B == 4) {
+        c.p1 = make_float2(fmaf(-128.f, s, b), b11);
+        c.p2 = c.p1;
+    } else {
+        c.p1 = make_float2(b11, fmaf(-256.f, s, b));
+        c.p2 = make_float2(fmaf(-32.f, s, b), b11);
+    }
+    return c;
+}
+
+// Eight codes (code i at bits B*i of u; 3-bit: bits 24-31 ignored) -> four
+// packed output pairs (k, k+1).
+template <int B, bool BF16>
+__device__ __forceinline__ uint4 dq8(uint32_t u, const GroupConst &c) {
+    float2 f01, f23, f45, f67;
+    if constexpr (B == 4) {
+        const uint32_t t1 = u << 8, t2 = u >> 8, t3 = prmt(u, u, 0x1032u);  // t3: u rotated by 16
+        f01 = make_float2(code_at(t3, 0x000F0000u, kExp7), code_at(t1, 0x0000F000u, kExp11));
+        f23 = make_float2(code_at(t1, 0x000F0000u, kExp7), code_at(u, 0x0000F000u, kExp11));
+        f45 = make_float2(code_at(u, 0x000F0000u, kExp7), code_at(t2, 0x0000F000u, kExp11));
+        f67 = make_float2(code_at(t2, 0x000F0000u, kExp7), code_at(t3, 0x0000F000u, kExp11));
+    } else {
+        const uint32_t ta = u << 12, tb = u << 3, td = u >> 9;
+        f01 = make_float2(code_at(ta, 0x00007000u, kExp11), code_at(ta, 0x00038000u, kExp8));
+        f23 = make_float2(code_at(ta, 0x001C0000u, kExp5), code_at(tb, 0x00007000u, kExp11));
+        f45 = make_float2(code_at(u, 0x00007000u, kExp11), code_at(u, 0x00038000u, kExp8));
+        f67 = make_float2(code_at(u, 0x001C0000u, kExp5), code_at(td, 0x00007000u, kExp11));
+    }
+    return make_uint4(pack_out<BF16>(__ffma2_rn(f01, c.s2, c.p1)),
+                      pack_out<BF16>(__ffma2_rn(f23, c.s2, c.p2)),
+                      pack_out<BF16>(__ffma2_rn(f45, c.s2, c.p1)),
+                      pack_out<BF16>(__ffma2_rn(f67, c.s2, c.p2)));
+}
+
 template <typename T>
 __device__ __forceinline__ T cvt_out(float v);
 template <>
@@ -181,13 +268,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tmap_x) {
     using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
     using R = Raw<B>;
-    constexpr int kStages = stages_for(BM);
+    constexpr int kA = a_slots_for(BM);
+    constexpr int kB = b_slots_for(BM);
     constexpr int kRawSlots = raw_slots_for(BM);
     // A 512-row x tile is two N = 256 MMAs per k-step into one 512-column
     // accumulator (each weight tile dequantised once for 512 x rows); the
     // narrower tiles double-buffer their accumulator.
-    constexpr int kNI = BM > 256 ? 256 : BM;  // N of one MMA
-    constexpr int kAcc = BM > 256 ? 1 : 2;    // accumulators in tensor memory
+    constexpr int kNI = ni_for(BM);  // N of one MMA = rows of one B sub-tile
+    constexpr int kH = BM / kNI;     // B sub-tiles per stage
+    constexpr int kBTile = kNI * 128;
+    constexpr int kAcc = BM > 256 ? 1 : 2;  // accumulators in tensor memory
     extern __shared__ uint8_t smem_dyn[];
     // Align to 1024 bytes by an offset from the __shared__ array itself, so
     // that every access below stays a shared-memory access (32-bit address).
@@ -197,9 +287,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     uint8_t *raw = smem + p.off_raw;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.off_bar);
     uint64_t *a_full = bars;
-    uint64_t *b_full = bars + kStages;
-    uint64_t *ab_empty = bars + 2 * kStages;
-    uint64_t *acc_full = bars + 3 * kStages;
+    uint64_t *a_empty = a_full + kA;
+    uint64_t *b_full = a_empty + kA;
+    uint64_t *b_empty = b_full + kB;
+    uint64_t *acc_full = b_empty + kB;
     uint64_t *acc_empty = acc_full + 2;
     uint64_t *drain = acc_empty + 2;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
@@ -227,10 +318,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kA; ++s) {
             mbar_init(&a_full[s], kDqWarps);
+            mbar_init(&a_empty[s], 1);
+        }
+        for (int s = 0; s < kB; ++s) {
             mbar_init(&b_full[s], 1);
-            mbar_init(&ab_empty[s], 1);
+            mbar_init(&b_empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
@@ -255,79 +349,94 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
     if (warp == kWarpTma) {
         // ------------------------------------------------------------------
-        // x tiles: BM rows x 64 k per stage, 128-byte swizzled, by TMA.
+        // x sub-tiles: kNI rows x 64 k, 128-byte swizzled, by TMA; kH of
+        // them per stage, each into its own slot of the B ring.
         // ------------------------------------------------------------------
         if (lane == 0) {
             grid_dependency_wait();
-            uint32_t it = 0;
+            uint32_t bi = 0;
             int tile, gb, ge;
             for (int u = 0; unit_of(u, tile, gb, ge); ++u) {
                 const int m0 = (tile % p.m_tiles) * BM;
-                for (int g = gb; g < ge; ++g, ++it) {
-                    const int slot = it % kStages;
-                    const uint32_t ph = (it / kStages) & 1u;
-                    if (it >= kStages && !tc_wait(&ab_empty[slot], ph ^ 1u, flag, 0x0102)) goto tma_done;
-#ifdef AQ_TEST_HOOKS
-                    if (p.withhold && it == 0) continue;  // nothing will complete b_full[0]
-#endif
-                    mbar_arrive_expect_tx(&b_full[slot], BM * 128);
+                for (int g = gb; g < ge; ++g) {
 #pragma unroll
-                    for (int h = 0; h < BM / kNI; ++h)
-                        tma_load_2d(b_ring + slot * (BM * 128) + h * kNI * 128, &tmap_x, 64 * g,
-                                    m0 + h * kNI, &b_full[slot]);
+                    for (int h = 0; h < kH; ++h) {
+                        const int slot = bi % kB;
+                        const uint32_t ph = (bi / kB) & 1u;
+                        if (bi >= kB && !tc_wait(&b_empty[slot], ph ^ 1u, flag, 0x0102))
+                            goto tma_done;
+#ifdef AQ_TEST_HOOKS
+                        if (p.withhold && bi == 0) {  // nothing will complete b_full[0]
+                            ++bi;
+                            continue;
+                        }
+#endif
+                        mbar_arrive_expect_tx(&b_full[slot], kBTile);
+                        tma_load_2d(b_ring + slot * kBTile, &tmap_x, 64 * g, m0 + h * kNI,
+                                    &b_full[slot]);
+                        ++bi;
+                    }
                 }
             }
         tma_done:
-            // Wind-down: the loads issued for the last stages land before
+            // Wind-down: the loads issued for the last sub-tiles land before
             // the CTA goes on (earlier ones were consumed by the MMAs).
-            for (uint32_t j = it > (uint32_t)kStages ? it - kStages : 0u; j < it; ++j)
-                drain_wait(&b_full[j % kStages], (j / kStages) & 1u);
+            for (uint32_t j = bi > (uint32_t)kB ? bi - kB : 0u; j < bi; ++j)
+                drain_wait(&b_full[j % kB], (j / kB) & 1u);
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------------
-        // MMA issue: 4 x (128 x BM x 16) per stage into accumulator b.  The
-        // whole warp walks the stages (converged, waits taken by every lane
-        // and agreed on); lane 0 issues.  Descriptors: those of slot 0,
-        // k-step 0, plus the byte offset of the slot and k-step over 16.
+        // MMA issue: per stage, for each B sub-tile h, 4 x (128 x kNI x 16)
+        // into columns [h kNI, (h+1) kNI) of accumulator b, then release the
+        // sub-tile; after the last, release the A tile.  The whole warp
+        // walks the stages (converged, waits taken by every lane and agreed
+        // on); lane 0 issues.  Descriptors: those of slot 0, k-step 0, plus
+        // the byte offset of the slot and k-step over 16.
         // ------------------------------------------------------------------
         const uint32_t idesc = (1u << 4) | ((BF16 ? 1u : 0u) << 7) | ((BF16 ? 1u : 0u) << 10) |
                                ((uint32_t)(kNI >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
         const uint64_t a_desc0 = sw128_desc(smem_u32(a_ring));
         const uint64_t b_desc0 = sw128_desc(smem_u32(b_ring));
-        uint32_t it = 0, ti = 0;
+        uint32_t ai = 0, bi = 0, ti = 0;
         int tile, gb, ge;
-        bool issued = false;  // warp-uniform
-        for (int u = 0; unit_of(u, tile, gb, ge); ++u, ++ti) {
+        bool ok = true, issued = false;  // both warp-uniform
+        for (int u = 0; ok && unit_of(u, tile, gb, ge); ++u, ++ti) {
             const uint32_t b = ti % kAcc, use = ti / kAcc;
             const bool free = ti < (uint32_t)kAcc ||
                               tc_wait(&acc_empty[b], (use & 1u) ^ 1u, flag, 0x0202);
             if (!__all_sync(0xffffffffu, free)) break;
             tc_fence_after();
             const uint32_t d = tmem + b * BM;
-            bool ok = true;
-            for (int g = gb; g < ge; ++g, ++it) {
-                const int slot = it % kStages;
-                const uint32_t ph = (it / kStages) & 1u;
-                const bool got = tc_wait(&a_full[slot], ph, flag, 0x0302) &&
-                                 tc_wait(&b_full[slot], ph, flag, 0x0402);
-                if (!__all_sync(0xffffffffu, got)) {
+            for (int g = gb; ok && g < ge; ++g, ++ai) {
+                const int as = ai % kA;
+                const bool got_a = tc_wait(&a_full[as], (ai / kA) & 1u, flag, 0x0302);
+                if (!__all_sync(0xffffffffu, got_a)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                issued = true;
-                if (lane == 0) {
-                    const uint64_t ad = a_desc0 + (uint64_t)((uint32_t)(slot * kATileBytes) >> 4);
-                    const uint64_t bd = b_desc0 + (uint64_t)((uint32_t)(slot * BM * 128) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
+                for (int h = 0; h < kH; ++h, ++bi) {
+                    const int bs = bi % kB;
+                    const bool got_b = tc_wait(&b_full[bs], (bi / kB) & 1u, flag, 0x0402);
+                    if (!__all_sync(0xffffffffu, got_b)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issued = true;
+                    if (lane == 0) {
+                        const uint64_t ad = a_desc0 + (uint64_t)((uint32_t)(as * kATileBytes) >> 4);
+                        const uint64_t bd = b_desc0 + (uint64_t)((uint32_t)(bs * kBTile) >> 4);
 #pragma unroll
-                        for (int h = 0; h < BM / kNI; ++h)
-                            tc_mma_f16(d + h * kNI, ad + 2 * kk,
-                                       bd + 2 * kk + (uint64_t)((uint32_t)(h * kNI * 128) >> 4),
-                                       idesc, (g != gb || kk != 0) ? 1u : 0u);
-                    tc_commit(&ab_empty[slot]);
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc_mma_f16(d + h * kNI, ad + 2 * kk, bd + 2 * kk, idesc,
+                                       (g != gb || kk != 0) ? 1u : 0u);
+                        tc_commit(&b_empty[bs]);
+                    }
+                    __syncwarp();
                 }
+                if (!ok) break;
+                if (lane == 0) tc_commit(&a_empty[as]);
                 __syncwarp();
             }
             if (!ok) break;
@@ -454,15 +563,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             const uint8_t *rowp = slotp + rl * R::kRowPitch;
 #pragma unroll 1
             for (int j = 0; j < kGroups; ++j, ++it) {
-                const int slot = it % kStages;
-                const uint32_t ph = (it / kStages) & 1u;
-                if (it >= kStages && !tc_wait(&ab_empty[slot], ph ^ 1u, flag, 0x0602)) {
+                const int slot = it % kA;
+                const uint32_t ph = (it / kA) & 1u;
+                if (it >= kA && !tc_wait(&a_empty[slot], ph ^ 1u, flag, 0x0602)) {
                     ok = false;
                     break;
                 }
-                const float s = h_at(sv, j), bsc = h_at(bv, j);
-                const float bb = fmaf(-128.f, s, bsc);
-                const uint32_t s2 = h2_at(sv, j), b2 = h2_at(bv, j);
+                const GroupConst gc = group_const<B>(h_at(sv, j), h_at(bv, j));
                 uint32_t u[4];  // 8 codes per entry, this lane's chunks 4h..4h+3
                 if constexpr (B == 4) {
                     const uint4 w = *reinterpret_cast<const uint4 *>(rowp + j * 32 + h * 16);  // 4 words
@@ -482,7 +589,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int chunk = 4 * h + c;  // k = 8*chunk .. 8*chunk+7
-                    const uint4 v = dequant8<B, BF16>(u[c], s, bb, s2, b2);
+                    const uint4 v = dq8<B, BF16>(u[c], gc);
                     *reinterpret_cast<uint4 *>(arow_p + ((chunk ^ (arow & 7)) << 4)) = v;
                 }
                 fence_proxy_async_smem();
@@ -507,7 +614,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         // barrier, error or not.
         constexpr int kCh = BM < 256 ? BM : 256;  // columns per hand-over
         constexpr int kXP = kCh + 4;              // floats per row of the buffer
-        static_assert(128 * kXP * 4 <= kStages * (kATileBytes + BM * 128), "hand-over buffer");
+        static_assert(128 * kXP * 4 <= kA * kATileBytes + kB * kBTile, "hand-over buffer");
         const int r = (int)blockIdx.x & 1;
         const int tile = p.rounds * (int)gridDim.x + ((int)blockIdx.x >> 1);
         int nfull = 0;  // whole tiles this CTA took before the tail
@@ -888,16 +995,16 @@ bool tc_plan(const MatmulArgs &a, TcPlan &pl) {
     q.m_tiles = (int)((a.M + pl.BM - 1) / pl.BM);
     if ((int64_t)q.n_tiles * q.m_tiles > INT32_MAX) return false;
     const int raw_slot = a.bits == 4 ? Raw<4>::kSlotBytes : Raw<3>::kSlotBytes;
-    const int kStages = stages_for(pl.BM);
+    const int kA = a_slots_for(pl.BM), kB = b_slots_for(pl.BM);
     const int kRawSlots = raw_slots_for(pl.BM);
-    size_t off = (size_t)kStages * kATileBytes;
+    size_t off = (size_t)kA * kATileBytes;
     q.off_b = (uint32_t)off;
-    off += (size_t)kStages * pl.BM * 128;
+    off += (size_t)kB * ni_for(pl.BM) * 128;
     q.off_raw = (uint32_t)off;
     off += (size_t)kDqWarps * kRawSlots * raw_slot;
     off = (off + 15) / 16 * 16;
     q.off_bar = (uint32_t)off;
-    off += (3 * kStages + 5) * 8 + 16;
+    off += (2 * kA + 2 * kB + 5) * 8 + 16;
     pl.smem = off + 1024;  // room to align the base to 1024 bytes
     if (pl.smem > kSmemLimitTc) return false;
     q.tmem_cols = pl.BM >= 256 ? 512 : pl.BM == 128 ? 256 : 128;
@@ -1096,8 +1203,10 @@ int tc_describe(const MatmulArgs &a, char *buf, int len) {
     TcPlan pl;
     if (!tc_plan(a, pl)) return snprintf(buf, len, "tc: unsupported");
     return snprintf(buf, len,
-                    "tc bm=%d stages=%d tiles=%dx%d grid=%d rounds=%d split=%d smem=%zu tmem=%u",
-                    pl.BM, stages_for(pl.BM), pl.prm.n_tiles, pl.prm.m_tiles, pl.grid,
+                    "tc bm=%d a_slots=%d b_slots=%d raw_slots=%d tiles=%dx%d grid=%d rounds=%d "
+                    "split=%d smem=%zu tmem=%u",
+                    pl.BM, a_slots_for(pl.BM), b_slots_for(pl.BM), raw_slots_for(pl.BM),
+                    pl.prm.n_tiles, pl.prm.m_tiles, pl.grid,
                     pl.prm.rounds, pl.prm.tail, pl.smem, pl.prm.tmem_cols);
 }
 
