@@ -561,40 +561,62 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             const uint4 sv = make_uint4(sv2.x, sv2.y, 0u, 0u);
             const uint4 bv = make_uint4(bv2.x, bv2.y, 0u, 0u);
             const uint8_t *rowp = slotp + rl * R::kRowPitch;
+            // kPair groups (A stages) at a time: with a deep enough A ring,
+            // two groups give the ALUs twice the independent work and one
+            // fence serves both; a shallow ring keeps one.
+            constexpr int kPair = kA >= 4 ? 2 : 1;
 #pragma unroll 1
-            for (int j = 0; j < kGroups; ++j, ++it) {
-                const int slot = it % kA;
-                const uint32_t ph = (it / kA) & 1u;
-                if (it >= kA && !tc_wait(&a_empty[slot], ph ^ 1u, flag, 0x0602)) {
+            for (int j = 0; j < kGroups; j += kPair, it += kPair) {
+                bool free2 = true;
+#pragma unroll
+                for (int e = 0; e < kPair; ++e) {
+                    const uint32_t ie = it + e;
+                    if (ie >= (uint32_t)kA &&
+                        !tc_wait(&a_empty[ie % kA], ((ie / kA) & 1u) ^ 1u, flag, 0x0602))
+                        free2 = false;
+                }
+                if (!free2) {
                     ok = false;
                     break;
                 }
-                const GroupConst gc = group_const<B>(h_at(sv, j), h_at(bv, j));
-                uint32_t u[4];  // 8 codes per entry, this lane's chunks 4h..4h+3
-                if constexpr (B == 4) {
-                    const uint4 w = *reinterpret_cast<const uint4 *>(rowp + j * 32 + h * 16);  // 4 words
-                    u[0] = w.x;
-                    u[1] = w.y;
-                    u[2] = w.z;
-                    u[3] = w.w;
-                } else {
-                    const uint32_t *wp = reinterpret_cast<const uint32_t *>(rowp + j * 24 + h * 12);
-                    const uint32_t w0 = wp[0], w1 = wp[1], w2 = wp[2];
-                    u[0] = w0;
-                    u[1] = __funnelshift_r(w0, w1, 24);
-                    u[2] = __funnelshift_r(w1, w2, 16);
-                    u[3] = w2 >> 8;
-                }
-                uint8_t *arow_p = a_ring + slot * kATileBytes + arow * 128;
+                uint32_t u[kPair][4];  // 8 codes per entry, this lane's chunks 4h..4h+3
+                GroupConst gc[kPair];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int chunk = 4 * h + c;  // k = 8*chunk .. 8*chunk+7
-                    const uint4 v = dq8<B, BF16>(u[c], gc);
-                    *reinterpret_cast<uint4 *>(arow_p + ((chunk ^ (arow & 7)) << 4)) = v;
+                for (int e = 0; e < kPair; ++e) {
+                    gc[e] = group_const<B>(h_at(sv, j + e), h_at(bv, j + e));
+                    if constexpr (B == 4) {
+                        const uint4 w =
+                            *reinterpret_cast<const uint4 *>(rowp + (j + e) * 32 + h * 16);
+                        u[e][0] = w.x;
+                        u[e][1] = w.y;
+                        u[e][2] = w.z;
+                        u[e][3] = w.w;
+                    } else {
+                        const uint32_t *wp =
+                            reinterpret_cast<const uint32_t *>(rowp + (j + e) * 24 + h * 12);
+                        const uint32_t w0 = wp[0], w1 = wp[1], w2 = wp[2];
+                        u[e][0] = w0;
+                        u[e][1] = __funnelshift_r(w0, w1, 24);
+                        u[e][2] = __funnelshift_r(w1, w2, 16);
+                        u[e][3] = w2 >> 8;
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < kPair; ++e) {
+                    uint8_t *arow_p = a_ring + ((it + e) % kA) * kATileBytes + arow * 128;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int chunk = 4 * h + c;  // k = 8*chunk .. 8*chunk+7
+                        const uint4 v = dq8<B, BF16>(u[e][c], gc[e]);
+                        *reinterpret_cast<uint4 *>(arow_p + ((chunk ^ (arow & 7)) << 4)) = v;
+                    }
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&a_full[slot]);
+                if (lane == 0) {
+#pragma unroll
+                    for (int e = 0; e < kPair; ++e) mbar_arrive(&a_full[(it + e) % kA]);
+                }
             }
             __syncwarp();
             advance(cu, ctile, cgb, cge, cvalid, css);
