@@ -131,54 +131,14 @@ __device__ __forceinline__ float h_at(const uint4 &v, int j) {
     const uint32_t w = j < 2 ? v.x : j < 4 ? v.y : j < 6 ? v.z : v.w;
     return __half2float(__ushort_as_half((unsigned short)((j & 1) ? (w >> 16) : (w & 0xFFFFu))));
 }
-__device__ __forceinline__ uint32_t h2_at(const uint4 &v, int j) {  // (h_j, h_j) as half2 bits
-    const uint32_t w = j < 2 ? v.x : j < 4 ? v.y : j < 6 ? v.z : v.w;
-    return prmt(w, 0u, (j & 1) ? 0x3232u : 0x1010u);
-}
 
 __device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// 8 codes (code i at bit bi*i of u) -> 8 dequantised values as 4 packed pairs.
-// bf16: w = fma(128 + q, s, b - 128 s) in fp32 (the code placed in the
-// mantissa of 128.0f), rounded once to bf16.  fp16: (q_lo, q_hi) exact as
-// halves, then one half2 fma with (s, s) and (b, b).
-template <int BITS, bool BF16>
-__device__ __forceinline__ uint4 dequant8(uint32_t u, float s, float bb, uint32_t s2, uint32_t b2) {
-    uint32_t out[4];
-    if constexpr (BF16) {
-        float f[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int sh = 16 - BITS * i;  // move code i to bit 16
-            const uint32_t t = sh >= 0 ? (u << sh) : (u >> (-sh));
-            const uint32_t m = ((1u << BITS) - 1u) << 16;
-            f[i] = fmaf(__uint_as_float((t & m) | 0x43000000u), s, bb);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) out[i] = bf16x2(f[2 * i], f[2 * i + 1]);
-    } else {
-        const __half2 magic = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            // code 2i to bit 0, code 2i+1 to bit 16
-            const uint32_t v = u >> (2 * BITS * i);
-            const uint32_t msk = (1u << BITS) - 1u;
-            const uint32_t pr = (v & msk) | ((v << (16 - BITS)) & (msk << 16));
-            const uint32_t qq = pr | 0x64006400u;  // halves 1024 + code
-            __half2 q = __hsub2(*reinterpret_cast<const __half2 *>(&qq), magic);
-            __half2 w = __hfma2(q, *reinterpret_cast<const __half2 *>(&s2),
-                                *reinterpret_cast<const __half2 *>(&b2));
-            out[i] = *reinterpret_cast<uint32_t *>(&w);
-        }
-    }
-    return make_uint4(out[0], out[1], out[2], out[3]);
-}
-
 // ---------------------------------------------------------------------------
-// Dequantisation of the large-M kernel.  A code q at bit p of a 32-bit word,
+// Dequantisation of the tensor-core kernels.  A code q at bit p of a 32-bit word,
 // with 12 <= p and p + bits <= 23, becomes the exact float 2^(23-p) + q once
 // the word is masked to the code and OR-ed with the exponent of 2^(23-p)
 // (the pages' mantissa trick, here with the code at one of a few mantissa
@@ -919,9 +879,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                         break;
                     }
                 }
-                const float sc = h_at(sv, j), bsc = h_at(bv, j);
-                const float bb = fmaf(-128.f, sc, bsc);
-                const uint32_t s2 = h2_at(sv, j), b2 = h2_at(bv, j);
+                const GroupConst gc = group_const<B>(h_at(sv, j), h_at(bv, j));
                 uint32_t u[8];  // 8 codes per entry
                 if constexpr (B == 4) {
                     const uint4 w0 = *reinterpret_cast<const uint4 *>(rowp + j * 32);
@@ -942,7 +900,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 uint8_t *brow = b_ring + slot * kWBTile + row * 128;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {  // k = 8c .. 8c+7
-                    const uint4 v = dequant8<B, BF16>(u[c], sc, bb, s2, b2);
+                    const uint4 v = dq8<B, BF16>(u[c], gc);
                     *reinterpret_cast<uint4 *>(brow + ((c ^ (row & 7)) << 4)) = v;
                 }
                 fence_proxy_async_smem();
