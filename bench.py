@@ -10,7 +10,8 @@ configuration measured in the same invocation:
     split3    3-bit 10240 x 5120, M in {1, 9, 16, 32, 64}, fp16
     layer     the seven 4-bit projections of a 5120-hidden decoder layer,
               M = 1, bf16, and the whole layer step (fused calls)
-    prefill   4-bit 28672 x 8192, M in {128, 512}, bf16
+    prefill   4-bit 28672 x 8192, M in {128, 512}, bf16 (and M = 256 beside
+              them: the middle of the tensor-core range)
 
 One step is one library call (one pass of the hot path over one batch of
 activations).  The headline's timed region holds exactly `--steps` calls,
@@ -76,7 +77,7 @@ PER_CONFIG_REGIONS = 5
 SUSTAIN_S = 0.6               # replays after a headline region, for the clock record
 PER_CONFIG_SPECS = (["small:0", "decode:0"] + [f"split3:{i}" for i in range(5)]
                     + [f"layer:{i}" for i in range(7)] + ["layerstep:0", "prefill:0",
-                                                          "prefill:1"])
+                                                          "prefill:2", "prefill:1"])
 
 
 def reduce_max(value: float, device: str = "cpu") -> float:

@@ -109,21 +109,6 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity,
 // completion counted in bytes on an mbarrier.  Addresses 16-byte aligned,
 // size a multiple of 16.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint64_t policy_evict_first() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-
-__device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes,
-                                         uint64_t *bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
-        "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst_smem)),
-        "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
-}
-
 __device__ __forceinline__ void bulk_g2s_plain(void *dst_smem, const void *src_gmem,
                                                uint32_t bytes, uint64_t *bar) {
     asm volatile(

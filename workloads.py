@@ -18,7 +18,7 @@ decode     4      4096 x 4096, M=1                        bf16
 split3     3      10240 x 5120, M in {1,9,16,32,64}       fp16
 layer      4      seven projections of a 5120-hidden      bf16
                   decoder layer (q,k,v,o,gate,up,down), M=1
-prefill    4      28672 x 8192, M in {128,512}            bf16
+prefill    4      28672 x 8192, M in {128,512,256}        bf16
 =========  =====  ======================================  ====================
 
 Codes are uniform over [0, 2^bits).  Scales are |N(0,1)|*c + 1e-3 with
@@ -155,7 +155,7 @@ WORKLOADS: Dict[str, List[Tuple[int, int, int, int, str, int]]] = {
     "decode": [(4, 4096, 4096, 1, "bf16", 1)],
     "split3": [(3, 10240, 5120, m, "fp16", 2) for m in (1, 9, 16, 32, 64)],
     "layer": [(4, n, k, 1, "bf16", 30 + p) for p, (_, n, k) in enumerate(LAYER_PROJECTIONS)],
-    "prefill": [(4, 28672, 8192, m, "bf16", 4) for m in (128, 512)],
+    "prefill": [(4, 28672, 8192, m, "bf16", 4) for m in (128, 512, 256)],
 }
 
 
