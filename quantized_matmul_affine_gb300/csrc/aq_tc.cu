@@ -657,12 +657,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 // ---------------------------------------------------------------------------
 // "tcw": the same tensor-core path with the roles swapped, for M <= 128.
 //
-// A tcgen05.mma of kind::f16 costs about the same time for any N up to 256
-// (measured on GB300: ~118 cycles for N = 16..128, 128 for N = 256), so with
-// the weights as the 128-row A operand a narrow x tile leaves most of each
-// instruction unused.  Here the x tile is A (128 rows, rows past M read as
-// zero) and a 256-row weight tile is B (N = 256): twice the weights per
-// instruction.  A weight tile's K range is split over the CTAs of a cluster
+// A chain of tcgen05.mma instructions of kind::f16 into one accumulator
+// advances at about the same rate for any N up to 256 (measured on GB300:
+// ~118 cycles an instruction for N = 16..128, 128 for N = 256), so with the
+// weights as the 128-row A operand a narrow x tile leaves most of each
+// instruction's time unused.  Here the x tile is A (128 rows, rows past M
+// read as zero) and a 256-row weight tile is B (N = 256): twice the weights
+// per instruction.  A weight tile's K range is split over the CTAs of a cluster
 // (up to 8) so that narrow outputs still fill the SMs; the partial tiles are
 // added in rank order through distributed shared memory (deterministic).
 //
