@@ -876,7 +876,8 @@ WIDTHS_METRIC = ("µs/call and effective HBM GB/s (fraction of roofline), other 
 WIDTH_WORKLOADS = {"widths": [(8, 64, 4096, 4096, 1, "bf16"), (2, 32, 4096, 4096, 1, "bf16"),
                               (6, 128, 4096, 4096, 1, "bf16"), (4, 128, 4096, 4096, 1, "bf16"),
                               (8, 32, 4096, 4096, 16, "fp16"), (8, 64, 4096, 4096, 64, "bf16"),
-                              (8, 64, 8192, 8192, 256, "bf16"), (5, 32, 8192, 8192, 256, "fp16")]}
+                              (8, 64, 8192, 8192, 256, "bf16"), (5, 32, 8192, 8192, 256, "fp16"),
+                              (3, 64, 10240, 5120, 256, "fp16")]}
 
 
 def run_widths(args, rank, world, local_rank, sampler):

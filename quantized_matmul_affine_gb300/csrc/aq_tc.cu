@@ -65,14 +65,23 @@ constexpr int ni_for(int BM) { return BM > 256 ? 256 : BM; }
 // to cover the HBM latency.
 constexpr int raw_slots_for(int BM) { return BM <= 128 ? 3 : 2; }
 
+// Raw super-stage of one dequantising warp: 16 rows x 4 groups of codes,
+// then their scales and biases.  The row pitch puts the rows in distinct
+// banks for the dequantising loads: 4-bit rows (16-byte loads, a quarter
+// warp at a time) 40 words apart; 3-bit rows (4-byte loads, two lanes a
+// row 3 words apart) 26 words apart, which is not a multiple of 16 bytes,
+// so 3-bit rows are copied in 8-byte pieces (at a 32-word pitch all 16 rows
+// of a load fell in the same banks).
 template <int B>
 struct Raw {
     static constexpr int kGroupBytes = 8 * B;
     static constexpr int kRowBytes = kGroups * kGroupBytes;  // 128 / 96
-    static constexpr int kChunksPerRow = kRowBytes / 16;    // 8 / 6
-    static constexpr int kRowPitch = kRowBytes + 32;         // 160 / 128: rows in distinct banks
+    static constexpr int kChunkBytes = B == 3 ? 8 : 16;      // cp.async piece
+    static constexpr int kChunksPerRow = kRowBytes / kChunkBytes;  // 8 / 12
+    static constexpr int kRowPitch = B == 3 ? 104 : kRowBytes + 32;  // 160 / 104
     static constexpr int kSbOff = 16 * kRowPitch;  // scales[16][4] then biases[16][4]
     static constexpr int kSlotBytes = kSbOff + 2 * 16 * 8;
+    static_assert(kRowPitch % kChunkBytes == 0 && kSbOff % 16 == 0, "raw slot alignment");
 };
 
 struct TcParams {
@@ -450,7 +459,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const int dw = warp - kWarpDq;
         uint8_t *ring = raw + dw * kRawSlots * R::kSlotBytes;
         const int64_t row_bytes = (int64_t)p.K * B / 8;
-        // copy plan: kChunks 16-byte pieces of 16 rows per super-stage + s/b
+        // copy plan: kChunks pieces of 16 rows per super-stage + s/b
         constexpr int kChunks = R::kChunksPerRow / 2;
         uint32_t roff[kChunks], doff[kChunks];
 #pragma unroll
@@ -458,7 +467,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             const int c = lane + 32 * i;
             const int r = c / R::kChunksPerRow, col = c % R::kChunksPerRow;
             roff[i] = (uint32_t)r;
-            doff[i] = (uint32_t)(r * R::kRowPitch + col * 16);
+            doff[i] = (uint32_t)(r * R::kRowPitch + col * R::kChunkBytes);
             roff[i] |= (uint32_t)col << 8;
         }
         const int nlast = p.N - 1;
@@ -470,8 +479,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             for (int i = 0; i < kChunks; ++i) {
                 const int r = roff[i] & 0xFF, col = roff[i] >> 8;
                 const int64_t n = min(n0 + r, nlast);
-                cp_async16(dst + doff[i],
-                           reinterpret_cast<const uint8_t *>(p.Wq) + n * row_bytes + kb + col * 16, 16u);
+                const uint8_t *src = reinterpret_cast<const uint8_t *>(p.Wq) + n * row_bytes + kb +
+                                     col * R::kChunkBytes;
+                if constexpr (R::kChunkBytes == 16)
+                    cp_async16(dst + doff[i], src, 16u);
+                else
+                    cp_async8(dst + doff[i], src);
             }
             const int sr = lane & 15;
             const int64_t n = min(n0 + sr, nlast);
@@ -681,11 +694,16 @@ constexpr int kWATile = kWXRows * 128;       // 16 KB
 constexpr int kWBTile = kWRows * 128;        // 32 KB
 constexpr int kWPitch = kWRows + 4;          // partial tile: floats per x row
 
+// Raw super-stage of one tcw dequantising warp: 32 rows (one per lane) x 4
+// groups, then scales and biases.  Rows 36 (4-bit) or 28 (3-bit) words
+// apart: the dequantising loads are 16 bytes wide (3-bit: two groups, 48
+// bytes, at a time) and a quarter warp's eight rows fall in distinct banks.
 template <int B>
 struct RawW {
     static constexpr int kGroupBytes = 8 * B;
     static constexpr int kRowBytes = kGroups * kGroupBytes;  // 128 / 96
-    static constexpr int kRowPitch = kRowBytes + 16;         // 144 / 112: rows in distinct banks
+    static constexpr int kChunksPerRow = kRowBytes / 16;    // 8 / 6
+    static constexpr int kRowPitch = kRowBytes + 16;         // 144 / 112
     static constexpr int kSbOff = 32 * kRowPitch;            // scales[32][4], then biases[32][4]
     static constexpr int kSlotBytes = kSbOff + 2 * 32 * 8;
 };
@@ -841,14 +859,21 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const int64_t row_bytes = (int64_t)p.K * B / 8;
         const int row = 32 * dw + lane;
         const int64_t n = min(n0 + row, p.N - 1);  // rows past N repeat the last (never stored)
-        const uint8_t *wrow = reinterpret_cast<const uint8_t *>(p.Wq) + n * row_bytes;
+        const uint8_t *wrow0 = reinterpret_cast<const uint8_t *>(p.Wq);
         const int nss = ns / kGroups;  // super-stages (4 groups each)
         auto issue = [&](int ss, int slot) {
             uint8_t *dst = ring + slot * R::kSlotBytes;
             const int64_t kb = (int64_t)(g0 + ss * kGroups) * R::kGroupBytes;
+            // consecutive lanes copy consecutive 16-byte pieces of a row
 #pragma unroll
-            for (int c = 0; c < R::kRowBytes / 16; ++c)
-                cp_async16(dst + lane * R::kRowPitch + c * 16, wrow + kb + c * 16, 16u);
+            for (int i = 0; i < R::kChunksPerRow; ++i) {
+                const int c = lane + 32 * i;
+                const int r = c / R::kChunksPerRow, col = c % R::kChunksPerRow;
+                cp_async16(dst + r * R::kRowPitch + col * 16,
+                           wrow0 + (int64_t)min(n0 + 32 * dw + r, p.N - 1) * row_bytes + kb +
+                               col * 16,
+                           16u);
+            }
             cp_async8(dst + R::kSbOff + lane * 8, p.scales + n * p.G + g0 + ss * kGroups);
             cp_async8(dst + R::kSbOff + 256 + lane * 8, p.biases + n * p.G + g0 + ss * kGroups);
         };
@@ -859,7 +884,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         int it = 0;  // stage counter (matches the MMA's)
         bool ok = true;
         for (int ss = 0; ss < nss && ok; ++ss) {
-            if (ss + kWRawSlots - 1 < nss) issue(ss + kWRawSlots - 1, (ss + kWRawSlots - 1) % kWRawSlots);
+            if (ss + kWRawSlots - 1 < nss)
+                issue(ss + kWRawSlots - 1, (ss + kWRawSlots - 1) % kWRawSlots);
             cp_async_commit();
             cp_async_wait<kWRawSlots - 1>();
             __syncwarp();
@@ -869,7 +895,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             const uint4 sv = make_uint4(sv2.x, sv2.y, 0u, 0u);
             const uint4 bv = make_uint4(bv2.x, bv2.y, 0u, 0u);
             const uint8_t *rowp = slotp + lane * R::kRowPitch;
-#pragma unroll 1
+            uint32_t w3[12];  // 3-bit: the codes of two groups
+            (void)w3;
+#pragma unroll
             for (int j = 0; j < kGroups; ++j, ++it) {
                 const int slot = it % kWStages;
                 const uint32_t ph = (it / kWStages) & 1u;
@@ -888,10 +916,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     u[0] = w0.x; u[1] = w0.y; u[2] = w0.z; u[3] = w0.w;
                     u[4] = w1.x; u[5] = w1.y; u[6] = w1.z; u[7] = w1.w;
                 } else {
-                    const uint32_t *wp = reinterpret_cast<const uint32_t *>(rowp + j * 24);
+                    // groups j and j+1 (48 bytes) are loaded together at even j
+                    if ((j & 1) == 0) {
+                        const uint4 *wp = reinterpret_cast<const uint4 *>(rowp + j * 24);
+                        const uint4 q0 = wp[0], q1 = wp[1], q2 = wp[2];
+                        w3[0] = q0.x, w3[1] = q0.y, w3[2] = q0.z, w3[3] = q0.w;
+                        w3[4] = q1.x, w3[5] = q1.y, w3[6] = q1.z, w3[7] = q1.w;
+                        w3[8] = q2.x, w3[9] = q2.y, w3[10] = q2.z, w3[11] = q2.w;
+                    }
+                    const uint32_t *wv = w3 + 6 * (j & 1);
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const uint32_t w0 = wp[3 * h], w1 = wp[3 * h + 1], w2 = wp[3 * h + 2];
+                        const uint32_t w0 = wv[3 * h], w1 = wv[3 * h + 1], w2 = wv[3 * h + 2];
                         u[4 * h] = w0;
                         u[4 * h + 1] = __funnelshift_r(w0, w1, 24);
                         u[4 * h + 2] = __funnelshift_r(w1, w2, 16);
