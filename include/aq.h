@@ -149,11 +149,13 @@ aq_status aq_matmul_bf16(const void *x_dev, const uint32_t *Wq_dev, const void *
  * 128).  Wq_dev is the same LSB-first stream (aq_pack), scales and biases
  * fp16 [N][K/group_size]; dtype AQ_F16 or AQ_BF16 for x and y.  3 and 4 bits
  * at groups of 64 run exactly as aq_matmul / aq_matmul_bf16 (the fast
- * kernels); everything else runs on CUDA cores: at M <= 32 with x 16-byte
- * aligned (and the staged rows of x within 200 KB of shared memory) the
- * small-M segment kernel, otherwise the plain kernel; aq_stats counts both
- * under AQ_VARIANT_GENERIC.  Tolerance, ownership and errors as aq_matmul,
- * with K % group_size == 0 in place of K % 64 == 0.
+ * kernels).  Otherwise: for M > 32 with K % 512 == 0 and x, Wq, scales and
+ * biases 16-byte aligned, the tensor-core kernel with a dequantisation for
+ * any width (counted under AQ_VARIANT_TC); at M <= 32 with x 16-byte aligned
+ * (and the staged rows of x within 200 KB of shared memory) the small-M
+ * segment kernel; anything else the plain kernel (both counted under
+ * AQ_VARIANT_GENERIC).  Tolerance, ownership and errors as aq_matmul, with
+ * K % group_size == 0 in place of K % 64 == 0.
  */
 aq_status aq_matmul_ex(int dtype, const void *x_dev, const uint32_t *Wq_dev,
                        const void *scales_dev, const void *biases_dev, int64_t M, int64_t N,

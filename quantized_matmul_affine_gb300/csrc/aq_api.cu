@@ -295,10 +295,21 @@ aq_status aq_matmul_ex(int dtype, const void *x_dev, const uint32_t *Wq_dev,
         !aligned(biases_dev, 2) || !aligned(out_dev, 2))
         return AQ_ERR_MISALIGNED;
     if (!generic_supported_g(a, group_size)) return AQ_ERR_UNSUPPORTED;
-    const cudaError_t e = segv_supported(a, group_size) ? segv_launch(a, group_size)
-                                                         : generic_launch_g(a, group_size);
+    // Past 32 rows the product is a contraction: the tensor-core kernel with
+    // the general-width dequantisation, where its shape and alignment rules
+    // hold; up to 32 rows the segment kernel; else the plain kernel.
+    int variant;
+    cudaError_t e;
+    if (M > 32 && tc_supported_g(a, group_size)) {
+        variant = AQ_VARIANT_TC;
+        e = tc_launch_g(a, group_size);
+    } else {
+        variant = AQ_VARIANT_GENERIC;
+        e = segv_supported(a, group_size) ? segv_launch(a, group_size)
+                                          : generic_launch_g(a, group_size);
+    }
     if (e != cudaSuccess) return AQ_ERR_CUDA;
-    g_calls[AQ_VARIANT_GENERIC].fetch_add(1, std::memory_order_relaxed);
+    g_calls[variant].fetch_add(1, std::memory_order_relaxed);
     return AQ_OK;
 }
 

@@ -73,6 +73,10 @@ bool tcw_supported(const MatmulArgs &a);
 cudaError_t tcw_launch(const MatmulArgs &a);
 int tcw_describe(const MatmulArgs &a, char *buf, int len);
 cudaError_t tc_launch(const MatmulArgs &a);
+// The tensor-core kernel for other code widths (2..8 bits) and group sizes
+// (32/64/128): K % 512 == 0, x, Wq, scales and biases 16-byte aligned.
+bool tc_supported_g(const MatmulArgs &a, int group);
+cudaError_t tc_launch_g(const MatmulArgs &a, int group);
 int tc_describe(const MatmulArgs &a, char *buf, int len);
 
 cudaError_t quantize_launch(int dtype, const void *w, int64_t N, int64_t K, int bits,

@@ -84,6 +84,61 @@ struct Raw {
     static_assert(kRowPitch % kChunkBytes == 0 && kSbOff % 16 == 0, "raw slot alignment");
 };
 
+// Raw super-stage of the general-width path (any code width B, groups of
+// 32, 64 or 128): 16 rows x 256 k of codes (32B bytes a row), then up to 8
+// scales and 8 biases a row.  Row pitches chosen so that the dequantising
+// loads of 16 rows (two lanes a row) fall in distinct banks, or in two.
+template <int B>
+struct RawG {
+    static constexpr int kGroupBytes = 8 * B;                // 64 k of one row
+    static constexpr int kRowBytes = kGroups * kGroupBytes;  // 256 k
+    static constexpr int kChunkBytes = 16;
+    static constexpr int kChunksPerRow = kRowBytes / 16;
+    static constexpr int kRowPitch = kRowBytes + (B == 4 ? 32 : 16);
+    static constexpr int kSbOff = 16 * kRowPitch;  // scales[16][8] then biases[16][8]
+    static constexpr int kSlotBytes = kSbOff + 2 * 16 * 16;
+    static_assert(kRowPitch % 16 == 0 && kSbOff % 16 == 0, "raw slot alignment");
+};
+// Raw slots per dequantising warp on the general-width path (as many as
+// shared memory holds next to 64 KB of A tiles and 80 KB of x tiles).
+constexpr int raw_slots_g(int B) { return B >= 6 ? 2 : 3; }
+
+// The 32 codes of one lane (B words, code i at bits [iB, iB+B) of the
+// little-endian stream) and the float 2048 + q of code i: the code moved to
+// mantissa bit 12 under the exponent of 2^11 (exact for q < 2^11).
+template <int B>
+__device__ __forceinline__ void load_codes(const uint8_t *p, uint32_t (&w)[B]) {
+    if constexpr (B == 2) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(p);
+        w[0] = v.x, w[1] = v.y;
+    } else if constexpr (B == 4 || B == 8) {
+#pragma unroll
+        for (int i = 0; i < B / 4; ++i) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(p + 16 * i);
+            w[4 * i] = v.x, w[4 * i + 1] = v.y, w[4 * i + 2] = v.z, w[4 * i + 3] = v.w;
+        }
+    } else if constexpr (B == 6) {
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+            const uint2 v = *reinterpret_cast<const uint2 *>(p + 8 * i);
+            w[2 * i] = v.x, w[2 * i + 1] = v.y;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < B; ++i) w[i] = reinterpret_cast<const uint32_t *>(p)[i];
+    }
+}
+template <int B>
+__device__ __forceinline__ float code_f(const uint32_t (&w)[B], int i) {
+    const int bit = i * B, wd = bit >> 5, off = bit & 31;
+    uint32_t t;
+    if (off + B <= 32)
+        t = off >= 12 ? (w[wd] >> (off - 12)) : (w[wd] << (12 - off));
+    else
+        t = __funnelshift_r(w[wd], w[wd + 1], off) << 12;
+    return __uint_as_float((t & (((1u << B) - 1u) << 12)) | 0x45000000u);
+}
+
 struct TcParams {
     const uint32_t *Wq;
     const __half *scales;
@@ -97,6 +152,7 @@ struct TcParams {
     // through distributed shared memory.
     int rounds, tail;
     uint32_t off_b, off_raw, off_bar, tmem_cols;
+    int lg, NG;  // general-width path: log2 of the group size, groups per row
 #ifdef AQ_TEST_HOOKS
     int withhold;  // test builds only: the x producer skips its first stage
 #endif
@@ -232,14 +288,16 @@ __device__ __forceinline__ __nv_bfloat16 cvt_out<__nv_bfloat16>(float v) {
 
 }  // namespace
 
-template <int B, bool BF16, int BM>
+template <int B, bool BF16, int BM, bool GEN>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tmap_x) {
     using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-    using R = Raw<B>;
+    // GEN: any code width and group size (32/64/128, p.lg), codes decoded at
+    // compile-time bit offsets; otherwise 3/4 bits at groups of 64.
+    using R = typename std::conditional<GEN, RawG<B>, Raw<B>>::type;
     constexpr int kA = a_slots_for(BM);
     constexpr int kB = b_slots_for(BM);
-    constexpr int kRawSlots = raw_slots_for(BM);
+    constexpr int kRawSlots = GEN ? raw_slots_g(B) : raw_slots_for(BM);
     // A 512-row x tile is two N = 256 MMAs per k-step into one 512-column
     // accumulator (each weight tile dequantised once for 512 x rows); the
     // narrower tiles double-buffer their accumulator.
@@ -489,7 +547,20 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             const int sr = lane & 15;
             const int64_t n = min(n0 + sr, nlast);
             const __half *base = (lane < 16) ? p.scales : p.biases;
-            cp_async8(dst + R::kSbOff + (lane >> 4) * 128 + sr * 8, base + n * p.G + ss * kGroups);
+            if constexpr (GEN) {
+                // 256 >> lg scales (or biases) of this row: 16, 8 or 4 bytes
+                uint8_t *sd = dst + R::kSbOff + (lane >> 4) * 256 + sr * 16;
+                const __half *src = base + n * p.NG + ss * (256 >> p.lg);
+                if (p.lg == 5)
+                    cp_async16(sd, src, 16u);
+                else if (p.lg == 6)
+                    cp_async8(sd, src);
+                else
+                    cp_async4(sd, src);
+            } else {
+                cp_async8(dst + R::kSbOff + (lane >> 4) * 128 + sr * 8,
+                          base + n * p.G + ss * kGroups);
+            }
         };
         // flat sequence of (unit, super-stage) for this CTA: the one being
         // dequantised (c...) and the next one to issue (n...)
@@ -529,10 +600,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             cp_async_wait<kRawSlots - 1>();
             __syncwarp();
             const uint8_t *slotp = ring + (cnt % kRawSlots) * R::kSlotBytes;
-            const uint2 sv2 = *reinterpret_cast<const uint2 *>(slotp + R::kSbOff + rl * 8);
-            const uint2 bv2 = *reinterpret_cast<const uint2 *>(slotp + R::kSbOff + 128 + rl * 8);
-            const uint4 sv = make_uint4(sv2.x, sv2.y, 0u, 0u);
-            const uint4 bv = make_uint4(bv2.x, bv2.y, 0u, 0u);
+            uint4 sv, bv;  // this row's scales and biases of the super-stage
+            if constexpr (GEN) {
+                sv = *reinterpret_cast<const uint4 *>(slotp + R::kSbOff + rl * 16);
+                bv = *reinterpret_cast<const uint4 *>(slotp + R::kSbOff + 256 + rl * 16);
+            } else {
+                const uint2 sv2 = *reinterpret_cast<const uint2 *>(slotp + R::kSbOff + rl * 8);
+                const uint2 bv2 =
+                    *reinterpret_cast<const uint2 *>(slotp + R::kSbOff + 128 + rl * 8);
+                sv = make_uint4(sv2.x, sv2.y, 0u, 0u);
+                bv = make_uint4(bv2.x, bv2.y, 0u, 0u);
+            }
             const uint8_t *rowp = slotp + rl * R::kRowPitch;
             // kPair groups (A stages) at a time: with a deep enough A ring,
             // two groups give the ALUs twice the independent work and one
@@ -552,6 +630,35 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     ok = false;
                     break;
                 }
+                if constexpr (GEN) {
+                    // this lane's 32 codes of stage j+e: one group (its index
+                    // within the super-stage from the group size), w = (2048
+                    // + q) s + (b - 2048 s) two at a time
+#pragma unroll
+                    for (int e = 0; e < kPair; ++e) {
+                        const int gi = (64 * (j + e) + 32 * h) >> p.lg;
+                        const float sc = h_at(sv, gi), bc = h_at(bv, gi);
+                        const float2 s2 = make_float2(sc, sc);
+                        const float pb = fmaf(-2048.f, sc, bc);
+                        const float2 p2 = make_float2(pb, pb);
+                        uint32_t w[B];
+                        load_codes<B>(rowp + (j + e) * R::kGroupBytes + h * 4 * B, w);
+                        uint8_t *arow_p = a_ring + ((it + e) % kA) * kATileBytes + arow * 128;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            uint32_t o[4];
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const int i0 = 8 * c + 2 * q;
+                                const float2 f = make_float2(code_f<B>(w, i0), code_f<B>(w, i0 + 1));
+                                o[q] = pack_out<BF16>(__ffma2_rn(f, s2, p2));
+                            }
+                            const int chunk = 4 * h + c;  // k = 8*chunk .. 8*chunk+7
+                            *reinterpret_cast<uint4 *>(arow_p + ((chunk ^ (arow & 7)) << 4)) =
+                                make_uint4(o[0], o[1], o[2], o[3]);
+                        }
+                    }
+                } else {
                 uint32_t u[kPair][4];  // 8 codes per entry, this lane's chunks 4h..4h+3
                 GroupConst gc[kPair];
 #pragma unroll
@@ -583,6 +690,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                         const uint4 v = dq8<B, BF16>(u[e][c], gc[e]);
                         *reinterpret_cast<uint4 *>(arow_p + ((chunk ^ (arow & 7)) << 4)) = v;
                     }
+                }
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -997,12 +1105,18 @@ struct TcPlan {
     int grid;
 };
 
-bool tc_plan(const MatmulArgs &a, TcPlan &pl) {
+// group: 0 for the 3/4-bit group-64 format, else the group size of the
+// general-width path (32, 64 or 128; x tiles of at most 128 rows).
+bool tc_plan(const MatmulArgs &a, TcPlan &pl, int group = 0) {
     if (a.K % 512 != 0 || a.M < 1 || a.N < 1) return false;
     if (a.M > INT32_MAX / 2 || a.N > INT32_MAX / 2 || a.K > INT32_MAX / 2) return false;
+    const bool gen = group != 0;
+    if (gen && group != 32 && group != 64 && group != 128) return false;
+    if (!gen && a.bits != 3 && a.bits != 4) return false;
     // Past 256 rows, 512-row x tiles: each weight tile is dequantised once
     // for 512 rows (two N = 256 MMAs per k-step).
     pl.BM = a.M <= 64 ? 64 : a.M <= 128 ? 128 : a.M <= 256 ? 256 : 512;
+    if (gen) pl.BM = std::min(pl.BM, 128);
     TcParams &q = pl.prm;
     q.M = (int)a.M;
     q.N = (int)a.N;
@@ -1011,9 +1125,28 @@ bool tc_plan(const MatmulArgs &a, TcPlan &pl) {
     q.n_tiles = (int)((a.N + 127) / 128);
     q.m_tiles = (int)((a.M + pl.BM - 1) / pl.BM);
     if ((int64_t)q.n_tiles * q.m_tiles > INT32_MAX) return false;
-    const int raw_slot = a.bits == 4 ? Raw<4>::kSlotBytes : Raw<3>::kSlotBytes;
+    int raw_slot = a.bits == 4 ? Raw<4>::kSlotBytes : Raw<3>::kSlotBytes;
+    int kRawSlots = raw_slots_for(pl.BM);
+    if (gen) {
+        switch (a.bits) {
+            case 2: raw_slot = RawG<2>::kSlotBytes; break;
+            case 3: raw_slot = RawG<3>::kSlotBytes; break;
+            case 4: raw_slot = RawG<4>::kSlotBytes; break;
+            case 5: raw_slot = RawG<5>::kSlotBytes; break;
+            case 6: raw_slot = RawG<6>::kSlotBytes; break;
+            case 8: raw_slot = RawG<8>::kSlotBytes; break;
+            default: return false;
+        }
+        kRawSlots = raw_slots_g(a.bits);
+        int lg = 0;
+        while ((1 << lg) < group) ++lg;
+        q.lg = lg;
+        q.NG = (int)(a.K / group);
+    } else {
+        q.lg = 6;
+        q.NG = (int)(a.K / 64);
+    }
     const int kA = a_slots_for(pl.BM), kB = b_slots_for(pl.BM);
-    const int kRawSlots = raw_slots_for(pl.BM);
     size_t off = (size_t)kA * kATileBytes;
     q.off_b = (uint32_t)off;
     off += (size_t)kB * ni_for(pl.BM) * 128;
@@ -1038,23 +1171,31 @@ bool tc_plan(const MatmulArgs &a, TcPlan &pl) {
     q.tail = 0;
     // Tiles left over after whole rounds, when they fill at most half of the
     // grid, are split in two K halves over CTA pairs (clusters of two)
-    // instead of running a half-empty round.
+    // instead of running a half-empty round; so are all tiles when there are
+    // at most half as many as SMs.
     const int g2 = grid & ~1;
-    if (g2 >= 2 && q.G % (2 * kGroups) == 0) {
-        const int full = total / g2, rem = total - full * g2;
-        if (rem > 0 && rem <= g2 / 2) {
-            grid = g2;
-            q.rounds = full;
-            q.tail = rem;
+    if (q.G % (2 * kGroups) == 0) {
+        if (2 * total <= num_sms()) {
+            // few tiles: every one split in two K halves
+            grid = 2 * total;
+            q.rounds = 0;
+            q.tail = total;
+        } else if (g2 >= 2) {
+            const int full = total / g2, rem = total - full * g2;
+            if (rem > 0 && rem <= g2 / 2) {
+                grid = g2;
+                q.rounds = full;
+                q.tail = rem;
+            }
         }
     }
     pl.grid = grid;
     return true;
 }
 
-template <int B, bool BF16, int BM>
+template <int B, bool BF16, int BM, bool GEN>
 cudaError_t tc_launch_t(const TcPlan &pl, const CUtensorMap &tm, cudaStream_t stream) {
-    auto kern = tc_kernel<B, BF16, BM>;
+    auto kern = tc_kernel<B, BF16, BM, GEN>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -1082,11 +1223,21 @@ cudaError_t tc_launch_t(const TcPlan &pl, const CUtensorMap &tm, cudaStream_t st
 template <int B, bool BF16>
 cudaError_t tc_launch_bm(const TcPlan &pl, const CUtensorMap &tm, cudaStream_t s) {
     switch (pl.BM) {
-        case 64: return tc_launch_t<B, BF16, 64>(pl, tm, s);
-        case 128: return tc_launch_t<B, BF16, 128>(pl, tm, s);
-        case 256: return tc_launch_t<B, BF16, 256>(pl, tm, s);
-        default: return tc_launch_t<B, BF16, 512>(pl, tm, s);
+        case 64: return tc_launch_t<B, BF16, 64, false>(pl, tm, s);
+        case 128: return tc_launch_t<B, BF16, 128, false>(pl, tm, s);
+        case 256: return tc_launch_t<B, BF16, 256, false>(pl, tm, s);
+        default: return tc_launch_t<B, BF16, 512, false>(pl, tm, s);
     }
+}
+
+// General-width path: x tiles of 64 or 128 rows.
+template <int B>
+cudaError_t tc_launch_g_bits(const TcPlan &pl, const CUtensorMap &tm, bool bf16, cudaStream_t s) {
+    if (bf16)
+        return pl.BM == 64 ? tc_launch_t<B, true, 64, true>(pl, tm, s)
+                           : tc_launch_t<B, true, 128, true>(pl, tm, s);
+    return pl.BM == 64 ? tc_launch_t<B, false, 64, true>(pl, tm, s)
+                       : tc_launch_t<B, false, 128, true>(pl, tm, s);
 }
 
 // The swapped-role kernel's plan: 256-row weight tiles; the K range of a
@@ -1199,16 +1350,43 @@ bool tc_supported(const MatmulArgs &a) {
     return tc_plan(a, pl);
 }
 
+static bool tc_x_map(const MatmulArgs &a, const TcPlan &pl, CUtensorMap *tm) {
+    return tmap_2d(tm, a.dtype == AQ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                   a.x, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.K * 2, 64u,
+                   (uint32_t)std::min(pl.BM, 256), CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool tc_supported_g(const MatmulArgs &a, int group) {
+    if (!aligned(a.x, 16) || !aligned(a.Wq, 16) || !aligned(a.scales, 16) ||
+        !aligned(a.biases, 16))
+        return false;
+    TcPlan pl;
+    return tc_plan(a, pl, group);
+}
+
+cudaError_t tc_launch_g(const MatmulArgs &a, int group) {
+    TcPlan pl;
+    if (!tc_plan(a, pl, group)) return cudaErrorInvalidValue;
+    CUtensorMap tm;
+    if (!tc_x_map(a, pl, &tm)) return cudaErrorInvalidValue;
+    const bool bf16 = a.dtype == AQ_BF16;
+    switch (a.bits) {
+        case 2: return tc_launch_g_bits<2>(pl, tm, bf16, a.stream);
+        case 3: return tc_launch_g_bits<3>(pl, tm, bf16, a.stream);
+        case 4: return tc_launch_g_bits<4>(pl, tm, bf16, a.stream);
+        case 5: return tc_launch_g_bits<5>(pl, tm, bf16, a.stream);
+        case 6: return tc_launch_g_bits<6>(pl, tm, bf16, a.stream);
+        case 8: return tc_launch_g_bits<8>(pl, tm, bf16, a.stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 cudaError_t tc_launch(const MatmulArgs &a) {
     TcPlan pl;
     if (!tc_plan(a, pl)) return cudaErrorInvalidValue;
     CUtensorMap tm;
-    if (!tmap_2d(&tm, a.dtype == AQ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                 a.x, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.K * 2, 64u,
-                 (uint32_t)std::min(pl.BM, 256),
-                 CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
+    if (!tc_x_map(a, pl, &tm)) return cudaErrorInvalidValue;
     if (a.bits == 3)
         return a.dtype == AQ_BF16 ? tc_launch_bm<3, true>(pl, tm, a.stream)
                                   : tc_launch_bm<3, false>(pl, tm, a.stream);

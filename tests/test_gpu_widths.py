@@ -67,6 +67,49 @@ def test_matmul_ex_parity(M, N, K, bits, group, dtype):
     assert_within_tolerance(y_to_f64(y, dtype), y_ref, bound, f"bits={bits} group={group}")
 
 
+# Past 32 rows (K % 512 == 0, aligned operands): the tensor-core kernel with
+# the general-width dequantisation.  64-row and 128-row x tiles, several x
+# tiles, ragged N and M, and N = 20000 (157 weight tiles: one round over the
+# SMs plus five tiles split in K over pairs of CTAs).
+TC_SHAPES = [(33, 300, 1024), (64, 700, 2048), (100, 129, 512), (256, 520, 1024),
+             (40, 20000, 512)]
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("group", GROUPS)
+@pytest.mark.parametrize("bits", WIDTHS)
+@pytest.mark.parametrize("M,N,K", TC_SHAPES)
+def test_matmul_ex_tensor_core(M, N, K, bits, group, dtype):
+    if bits in (3, 4) and group == 64:
+        pytest.skip("the 3/4-bit group-64 format runs as aq_matmul")
+    codes, s, b, x_bits = _problem(bits, group, M, N, K, dtype, seed=bits * 7 + group + M + N)
+    Wq = aq.aq_pack(torch.from_numpy(codes).cuda(), bits)
+    st, bt = torch.from_numpy(s).cuda(), torch.from_numpy(b).cuda()
+    x = _x(x_bits, dtype)
+    torch.cuda.synchronize()
+    aq.aq_stats(reset=True)
+    y = aq.aq_matmul_ex(x, Wq, st, bt, bits, group)
+    torch.cuda.synchronize()
+    calls = aq.aq_stats()
+    assert calls[aq.AQ_VARIANT_TC] == 1 and calls[aq.AQ_VARIANT_GENERIC] == 0, calls
+    y_ref, bound = oracle.matmul_g(workloads.to_f64(x_bits, dtype), oracle.pack_g(codes, bits),
+                                   s, b, bits, group, threads=8)
+    assert_within_tolerance(y_to_f64(y, dtype), y_ref, bound, f"bits={bits} group={group}")
+    assert aq.aq_device_error() == 0
+
+
+def test_matmul_ex_tensor_core_is_deterministic():
+    M, N, K, bits, group = 200, 20000, 512, 5, 32
+    codes, s, b, x_bits = _problem(bits, group, M, N, K, "bf16", seed=99)
+    Wq = aq.aq_pack(torch.from_numpy(codes).cuda(), bits)
+    st, bt = torch.from_numpy(s).cuda(), torch.from_numpy(b).cuda()
+    x = _x(x_bits, "bf16")
+    y1 = aq.aq_matmul_ex(x, Wq, st, bt, bits, group)
+    y2 = aq.aq_matmul_ex(x, Wq, st, bt, bits, group)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
 def test_matmul_ex_at_the_format_is_aq_matmul():
     # 4 bits, groups of 64: the same kernels and bits as aq_matmul_bf16
     p = workloads.make_problem("t", 4, 300, 2048, 3, "bf16", seed=8)
