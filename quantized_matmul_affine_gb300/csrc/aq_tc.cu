@@ -57,7 +57,10 @@ constexpr int kATileBytes = 128 * 128;
 // weight rows x 64 k, 16 KB) have a ring of their own: a tile's slot comes
 // back one MMA completion plus one dequantisation after its last use, which
 // three or more slots keep off the critical path.
-constexpr int b_slots_for(int BM) { return BM >= 256 ? 4 : BM == 128 ? 5 : 8; }
+constexpr int b_slots_for(int BM, bool gen = false) {
+    // the general-width path's raw rings are larger: three 32 KB x slots
+    return BM >= 256 ? (gen ? 3 : 4) : BM == 128 ? 5 : 8;
+}
 constexpr int a_slots_for(int BM) { return BM >= 256 ? 3 : BM == 128 ? 4 : 5; }
 constexpr int ni_for(int BM) { return BM > 256 ? 256 : BM; }
 // Raw super-stages per dequant warp; all but one are in flight while the
@@ -296,7 +299,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // compile-time bit offsets; otherwise 3/4 bits at groups of 64.
     using R = typename std::conditional<GEN, RawG<B>, Raw<B>>::type;
     constexpr int kA = a_slots_for(BM);
-    constexpr int kB = b_slots_for(BM);
+    constexpr int kB = b_slots_for(BM, GEN);
     constexpr int kRawSlots = GEN ? raw_slots_g(B) : raw_slots_for(BM);
     // A 512-row x tile is two N = 256 MMAs per k-step into one 512-column
     // accumulator (each weight tile dequantised once for 512 x rows); the
@@ -1116,7 +1119,7 @@ bool tc_plan(const MatmulArgs &a, TcPlan &pl, int group = 0) {
     // Past 256 rows, 512-row x tiles: each weight tile is dequantised once
     // for 512 rows (two N = 256 MMAs per k-step).
     pl.BM = a.M <= 64 ? 64 : a.M <= 128 ? 128 : a.M <= 256 ? 256 : 512;
-    if (gen) pl.BM = std::min(pl.BM, 128);
+    if (gen) pl.BM = std::min(pl.BM, 256);
     TcParams &q = pl.prm;
     q.M = (int)a.M;
     q.N = (int)a.N;
@@ -1146,7 +1149,7 @@ bool tc_plan(const MatmulArgs &a, TcPlan &pl, int group = 0) {
         q.lg = 6;
         q.NG = (int)(a.K / 64);
     }
-    const int kA = a_slots_for(pl.BM), kB = b_slots_for(pl.BM);
+    const int kA = a_slots_for(pl.BM), kB = b_slots_for(pl.BM, gen);
     size_t off = (size_t)kA * kATileBytes;
     q.off_b = (uint32_t)off;
     off += (size_t)kB * ni_for(pl.BM) * 128;
@@ -1230,14 +1233,18 @@ cudaError_t tc_launch_bm(const TcPlan &pl, const CUtensorMap &tm, cudaStream_t s
     }
 }
 
-// General-width path: x tiles of 64 or 128 rows.
+// General-width path: x tiles of 64, 128 or 256 rows.
+template <int B, bool BF16>
+cudaError_t tc_launch_g_bm(const TcPlan &pl, const CUtensorMap &tm, cudaStream_t s) {
+    switch (pl.BM) {
+        case 64: return tc_launch_t<B, BF16, 64, true>(pl, tm, s);
+        case 128: return tc_launch_t<B, BF16, 128, true>(pl, tm, s);
+        default: return tc_launch_t<B, BF16, 256, true>(pl, tm, s);
+    }
+}
 template <int B>
 cudaError_t tc_launch_g_bits(const TcPlan &pl, const CUtensorMap &tm, bool bf16, cudaStream_t s) {
-    if (bf16)
-        return pl.BM == 64 ? tc_launch_t<B, true, 64, true>(pl, tm, s)
-                           : tc_launch_t<B, true, 128, true>(pl, tm, s);
-    return pl.BM == 64 ? tc_launch_t<B, false, 64, true>(pl, tm, s)
-                       : tc_launch_t<B, false, 128, true>(pl, tm, s);
+    return bf16 ? tc_launch_g_bm<B, true>(pl, tm, s) : tc_launch_g_bm<B, false>(pl, tm, s);
 }
 
 // The swapped-role kernel's plan: 256-row weight tiles; the K range of a
