@@ -877,7 +877,8 @@ WIDTH_WORKLOADS = {"widths": [(8, 64, 4096, 4096, 1, "bf16"), (2, 32, 4096, 4096
                               (6, 128, 4096, 4096, 1, "bf16"), (4, 128, 4096, 4096, 1, "bf16"),
                               (8, 32, 4096, 4096, 16, "fp16"), (8, 64, 4096, 4096, 64, "bf16"),
                               (8, 64, 8192, 8192, 256, "bf16"), (5, 32, 8192, 8192, 256, "fp16"),
-                              (3, 64, 10240, 5120, 256, "fp16")]}
+                              (3, 64, 10240, 5120, 256, "fp16"), (8, 32, 4096, 4096, 4, "fp16"),
+                              (8, 32, 4096, 4096, 8, "fp16"), (5, 64, 4096, 4096, 16, "bf16")]}
 
 
 def run_widths(args, rank, world, local_rank, sampler):

@@ -10,15 +10,19 @@
 //     row: exactly B consecutive words of the LSB-first stream (32 B bits),
 //     never straddling a group (groups are multiples of 32).  The decode of a
 //     segment is unrolled at compile time (the shifts and word indices are
-//     constants); each code becomes a float as (2^23 | q) - 2^23, two
-//     full-rate operations.
+//     constants): each code is moved to the top B bits of a float mantissa
+//     under the exponent of 2^B, which is the float 2^B + q exactly (one
+//     shift and one logic operation), and the 2^B * sum(x) this adds to a
+//     segment's sum is taken out with the segment sums of x.
 //   * The block's activation rows (up to MB) sit in shared memory as fp32,
-//     rows interleaved per code ([segment][j][m], a pad per segment), so a
-//     lane reads the MB values of its code j with one or two vector loads and
-//     the 32 lanes' segments fall on distinct banks; the per-segment sums of
-//     x for the bias term are taken while staging (16-byte loads, four in
-//     flight).  The grid is persistent over the output rows, so a block
-//     stages x once for several rows.
+//     rows interleaved per code ([segment][j][m], 4 floats of pad per
+//     segment), so a lane reads the values of four codes (MB = 1), two codes
+//     (MB = 2) or one code (MB >= 4) with 16-byte loads and the 32 lanes'
+//     segments fall on distinct banks; the products are paired fp32 fmas.
+//     The per-segment sums of x for the bias term are taken while staging
+//     (16-byte loads, four in flight).  The grid is persistent over the
+//     output rows, so a block stages x once for several rows; the weights of
+//     a warp's first row are requested before x is staged.
 //   * Per segment: sum(x q) over 32 codes for each row, then
 //     acc += scale * sum(x q) + bias * sum(x); a fixed xor-butterfly reduces
 //     the lanes; lane 0 rounds once to x's dtype.
@@ -47,17 +51,22 @@ __device__ __forceinline__ float ld_act(const T *p) {
         return __half2float(*p);
 }
 
-// Code j of a 32-code segment held in w[0..B-1] (LSB-first), as a float.
-template <int B, int J>
-__device__ __forceinline__ float seg_code(const uint32_t (&w)[B]) {
-    constexpr int bit = J * B, wi = bit / 32, sh = bit % 32;
-    constexpr uint32_t mask = (1u << B) - 1u;
+// Code j of a 32-code segment held in w[0..B-1] (LSB-first), as the float
+// 2^B + q: the code moved to mantissa bits [23-B, 23) under the exponent of
+// 2^B.  j is a constant once the callers' loops are unrolled.
+template <int B>
+__device__ __forceinline__ float seg_code_rt(const uint32_t (&w)[B], int j) {
+    const int bit = j * B, wi = bit >> 5, sh = bit & 31, top = 23 - B;
+    const uint32_t mask = ((1u << B) - 1u) << top;
+    const uint32_t expo = (uint32_t)(127 + B) << 23;
     uint32_t v;
-    if constexpr (sh + B <= 32)
-        v = (w[wi] >> sh) & mask;
+    if (sh + B > 32)
+        v = __funnelshift_r(w[wi], w[wi + 1], sh) << top;
+    else if (sh <= top)
+        v = w[wi] << (top - sh);
     else
-        v = __funnelshift_r(w[wi], w[wi + 1], sh) & mask;
-    return __uint_as_float(v | 0x4B000000u) - 8388608.0f;
+        v = w[wi] >> (sh - top);
+    return __uint_as_float((v & mask) | expo);
 }
 
 // The block's activation rows for code j of segment sg: MB consecutive
@@ -88,29 +97,41 @@ __device__ __forceinline__ XRow<MB> ld_xrow(const float *p) {
     return r;
 }
 
-template <int B, int MB, int J>
-struct SegDot {
-    // d[m] += sum_{j >= J} x[m][j] * code_j
-    __device__ __forceinline__ static void run(const uint32_t (&w)[B], const float *xs,
-                                               float (&d)[MB]) {
-        const float q = seg_code<B, J>(w);
-        const XRow<MB> xr = ld_xrow<MB>(xs + J * MB);
-#pragma unroll
-        for (int m = 0; m < MB; ++m) d[m] = fmaf(xr.v[m], q, d[m]);
-        SegDot<B, MB, J + 1>::run(w, xs, d);
-    }
-};
+// d[m] (as float2 pairs) += sum_j x[m][j] * (2^B + q_j) over the segment's
+// 32 codes: the x values of a 16-byte load (4 codes at MB = 1, 2 at MB = 2,
+// one code's 4 rows at MB >= 4) times the codes, two products a packed fma.
 template <int B, int MB>
-struct SegDot<B, MB, 32> {
-    __device__ __forceinline__ static void run(const uint32_t (&)[B], const float *,
-                                               float (&)[MB]) {}
-};
+__device__ __forceinline__ void seg_dot(const uint32_t (&w)[B], const float *xs,
+                                        float2 (&d)[MB == 1 ? 1 : MB / 2]) {
+#pragma unroll
+    for (int v = 0; v < 8 * MB; ++v) {  // 16-byte vectors of the segment
+        const float4 xv = *reinterpret_cast<const float4 *>(xs + 4 * v);
+        if constexpr (MB == 1) {
+            const int j = 4 * v;
+            d[0] = __ffma2_rn(make_float2(xv.x, xv.y),
+                              make_float2(seg_code_rt<B>(w, j), seg_code_rt<B>(w, j + 1)), d[0]);
+            d[0] = __ffma2_rn(make_float2(xv.z, xv.w),
+                              make_float2(seg_code_rt<B>(w, j + 2), seg_code_rt<B>(w, j + 3)),
+                              d[0]);
+        } else if constexpr (MB == 2) {
+            const float q0 = seg_code_rt<B>(w, 2 * v), q1 = seg_code_rt<B>(w, 2 * v + 1);
+            d[0] = __ffma2_rn(make_float2(xv.x, xv.y), make_float2(q0, q0), d[0]);
+            d[0] = __ffma2_rn(make_float2(xv.z, xv.w), make_float2(q1, q1), d[0]);
+        } else {
+            const int j = v / (MB / 4), m0 = 4 * (v % (MB / 4));
+            const float q = seg_code_rt<B>(w, j);
+            d[m0 / 2] = __ffma2_rn(make_float2(xv.x, xv.y), make_float2(q, q), d[m0 / 2]);
+            d[m0 / 2 + 1] = __ffma2_rn(make_float2(xv.z, xv.w), make_float2(q, q), d[m0 / 2 + 1]);
+        }
+    }
+}
 
-// Floats per segment in shared memory: 32 codes x MB rows plus a pad that
-// puts the 32 lanes' segments on distinct banks (8- or 16-byte slots).
+// Floats per segment in shared memory: 32 codes x MB rows plus a pad of 4
+// that keeps the segments 16-byte aligned and puts the 32 lanes' segments on
+// distinct banks for 16-byte loads.
 template <int MB>
 __host__ __device__ constexpr int seg_stride() {
-    return 32 * MB + (MB == 1 ? 1 : MB == 2 ? 2 : 4);
+    return 32 * MB + 4;
 }
 
 template <int B, int MB, typename T>
@@ -125,6 +146,41 @@ __global__ void __launch_bounds__(kSegWarps * 32)
     float *ss = sm + nseg * SS;             // [MB][nseg]  sum of x over a segment
     const int m0 = blockIdx.y * MB;
     const int rows = min(MB, M - m0);
+    const int lane = threadIdx.x & 31;
+    const int G = K >> gshift;
+    constexpr int kD = MB == 1 ? 1 : MB / 2;  // float2 accumulators of a segment
+
+    // This warp's first row's first segments are brought into L2 before x
+    // is staged (they do not depend on it), so that their HBM latency
+    // overlaps the staging without holding registers.
+    int n = blockIdx.x * kSegWarps + (threadIdx.x >> 5);
+    if (n < N) {
+        const uint32_t *row = Wq + (size_t)n * nseg * B;
+#pragma unroll
+        for (int u = 0; u < kSegUnroll; ++u) {
+            const int sg = min(lane + 32 * u, nseg - 1);
+            prefetch_l2(row + (size_t)sg * B);
+        }
+        if (lane == 0) {
+            prefetch_l2(scales + (size_t)n * G);
+            prefetch_l2(biases + (size_t)n * G);
+        }
+    }
+    uint32_t w[kSegUnroll][B];
+    float sc[kSegUnroll], bi[kSegUnroll];
+    auto load_batch = [&](int nn, int s0) {
+        const uint32_t *row = Wq + (size_t)nn * nseg * B;
+#pragma unroll
+        for (int u = 0; u < kSegUnroll; ++u) {
+            const int sg = min(s0 + 32 * u, nseg - 1);  // past the row: re-read, unused
+#pragma unroll
+            for (int i = 0; i < B; ++i) w[u][i] = __ldg(row + (size_t)sg * B + i);
+            const int g = (sg * 32) >> gshift;
+            sc[u] = __half2float(scales[(size_t)nn * G + g]);
+            bi[u] = __half2float(biases[(size_t)nn * G + g]);
+        }
+    };
+
     // the block's activation rows: 8 values (16 bytes) per thread and step,
     // four steps' loads in flight; lanes 4j..4j+3 hold one segment and sum it
     {
@@ -165,40 +221,32 @@ __global__ void __launch_bounds__(kSegWarps * 32)
     }
     __syncthreads();
 
-    const int lane = threadIdx.x & 31;
-    const int G = K >> gshift;
-    for (int n = blockIdx.x * kSegWarps + (threadIdx.x >> 5); n < N;
-         n += gridDim.x * kSegWarps) {
-        const uint32_t *row = Wq + (size_t)n * nseg * B;
-        const __half *srow = scales + (size_t)n * G;
-        const __half *brow = biases + (size_t)n * G;
+    constexpr float kOff = (float)(1 << B);  // each code reads as 2^B + q
+    for (; n < N; n += gridDim.x * kSegWarps) {
         float acc[MB];
 #pragma unroll
         for (int m = 0; m < MB; ++m) acc[m] = 0.f;
 
         for (int s0 = lane; s0 < nseg; s0 += 32 * kSegUnroll) {
-            uint32_t w[kSegUnroll][B];
-            float sc[kSegUnroll], bi[kSegUnroll];
-#pragma unroll
-            for (int u = 0; u < kSegUnroll; ++u) {
-                const int sg = min(s0 + 32 * u, nseg - 1);  // past the row: re-read, unused
-#pragma unroll
-                for (int i = 0; i < B; ++i) w[u][i] = __ldg(row + (size_t)sg * B + i);
-                const int g = (sg * 32) >> gshift;
-                sc[u] = __half2float(srow[g]);
-                bi[u] = __half2float(brow[g]);
-            }
+            load_batch(n, s0);
 #pragma unroll
             for (int u = 0; u < kSegUnroll; ++u) {
                 const int sg = s0 + 32 * u;
                 if (sg >= nseg) break;
-                float d[MB];
+                float2 d[kD];
 #pragma unroll
-                for (int m = 0; m < MB; ++m) d[m] = 0.f;
-                SegDot<B, MB, 0>::run(w[u], xs + sg * SS, d);
+                for (int i = 0; i < kD; ++i) d[i] = make_float2(0.f, 0.f);
+                seg_dot<B, MB>(w[u], xs + sg * SS, d);
 #pragma unroll
-                for (int m = 0; m < MB; ++m)
-                    acc[m] = fmaf(sc[u], d[m], fmaf(bi[u], ss[m * nseg + sg], acc[m]));
+                for (int m = 0; m < MB; ++m) {
+                    float dm;
+                    if constexpr (MB == 1)
+                        dm = d[0].x + d[0].y;
+                    else
+                        dm = (m & 1) ? d[m / 2].y : d[m / 2].x;
+                    const float sx = ss[m * nseg + sg];
+                    acc[m] = fmaf(sc[u], fmaf(-kOff, sx, dm), fmaf(bi[u], sx, acc[m]));
+                }
             }
         }
 #pragma unroll
@@ -220,8 +268,7 @@ __global__ void __launch_bounds__(kSegWarps * 32)
 inline int segv_rows(int64_t M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
 
 inline size_t segv_smem(int mb, int64_t K) {
-    const int ss = 32 * mb + (mb == 1 ? 1 : mb == 2 ? 2 : 4);
-    return (size_t)(K / 32) * (size_t)(ss + mb) * sizeof(float);
+    return (size_t)(K / 32) * (size_t)(32 * mb + 4 + mb) * sizeof(float);  // x, then sums
 }
 
 template <int B, int MB, typename T>
