@@ -149,7 +149,7 @@ aq_status aq_matmul_bf16(const void *x_dev, const uint32_t *Wq_dev, const void *
  * 128).  Wq_dev is the same LSB-first stream (aq_pack), scales and biases
  * fp16 [N][K/group_size]; dtype AQ_F16 or AQ_BF16 for x and y.  3 and 4 bits
  * at groups of 64 run exactly as aq_matmul / aq_matmul_bf16 (the fast
- * kernels).  Otherwise: for M > 32 with K % 512 == 0 and x, Wq, scales and
+ * kernels).  Otherwise: for M > 4 with K % 512 == 0 and x, Wq, scales and
  * biases 16-byte aligned, the tensor-core kernel with a dequantisation for
  * any width (counted under AQ_VARIANT_TC); at M <= 32 with x 16-byte aligned
  * (and the staged rows of x within 200 KB of shared memory) the small-M

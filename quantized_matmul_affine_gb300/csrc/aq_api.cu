@@ -295,12 +295,15 @@ aq_status aq_matmul_ex(int dtype, const void *x_dev, const uint32_t *Wq_dev,
         !aligned(biases_dev, 2) || !aligned(out_dev, 2))
         return AQ_ERR_MISALIGNED;
     if (!generic_supported_g(a, group_size)) return AQ_ERR_UNSUPPORTED;
-    // Past 32 rows the product is a contraction: the tensor-core kernel with
-    // the general-width dequantisation, where its shape and alignment rules
-    // hold; up to 32 rows the segment kernel; else the plain kernel.
+    // Past 4 rows the tensor-core kernel with the general-width
+    // dequantisation, where its shape and alignment rules hold (measured at
+    // 4096 x 4096, 8 bits: 20.8 us at 4 to 16 rows against 19.3 / 33.2 /
+    // 56.5 us on the segment kernel at 4 / 8 / 16 rows, which re-reads the
+    // staged x per output row); otherwise up to 32 rows the segment kernel;
+    // else the plain kernel.
     int variant;
     cudaError_t e;
-    if (M > 32 && tc_supported_g(a, group_size)) {
+    if (M > 4 && tc_supported_g(a, group_size)) {
         variant = AQ_VARIANT_TC;
         e = tc_launch_g(a, group_size);
     } else {
