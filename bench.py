@@ -25,11 +25,13 @@ max(--steps, 200) calls.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload small|decode|split3:I|layer:I|prefill:I|quantize:I|
-                                layerstep:I|widths:I|attention:I] [--all]
+                                layerstep:I|widths:I|attention:I|attnws:I] [--all]
 
 --workload times one workload alone (no per_config).  widths:I times
 aq_matmul_ex on other code widths and group sizes; attention:I times
-aq_attention_decode (decode attention over a quantised KV cache);
+aq_attention_decode (decode attention over a quantised KV cache), attnws:I
+the same shapes through aq_attention_decode_ws (a workspace: several
+clusters a KV head);
 layerstep:I times one decoder-layer step (seven projections; I = 0/1 fused or
 not at M = 1, 2/3 at M = 8); quantize:I times the float -> affine quantiser.
 
@@ -981,6 +983,9 @@ ATTN_METRIC = ("µs/call and effective HBM GB/s (fraction of roofline), decode a
 ATTN_WORKLOADS = {"attention": [(16, 8, 8192, 256, 4, 64, "bf16"), (16, 8, 2048, 256, 4, 64, "bf16"),
                                 (16, 8, 32768, 256, 4, 64, "bf16"), (16, 8, 8192, 256, 8, 64, "bf16"),
                                 (32, 8, 8192, 128, 4, 64, "bf16"), (16, 8, 8192, 512, 4, 64, "bf16")]}
+# the same shapes through aq_attention_decode_ws (a workspace: several
+# clusters a KV head)
+ATTN_WORKLOADS["attnws"] = list(ATTN_WORKLOADS["attention"])
 
 
 def run_attention(args, rank, world, local_rank, sampler):
@@ -1005,6 +1010,16 @@ def run_attention(args, rank, world, local_rank, sampler):
                 torch.from_numpy(s).cuda().view(KV, N, G), torch.from_numpy(b).cuda().view(KV, N, G))
 
     k0, v0 = cache(), cache()
+    ws_mode = name == "attnws"
+    ws_bytes = aq.aq_attention_workspace_bytes(H, KV, N, D, bits, group) if ws_mode else 0
+    ws = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device="cuda") if ws_mode else None
+
+    def attend(qq, cc, out):
+        if ws_mode:
+            aq.aq_attention_decode_ws(qq, *cc, bits, group, workspace=ws, out=out, stream=stream)
+        else:
+            aq.aq_attention_decode(qq, *cc, bits, group, out=out, stream=stream)
+
     tdt = torch.bfloat16 if dt == "bf16" else torch.float16
     qb = workloads.make_x(H, D, dt, seed=71)
     q = torch.from_numpy(qb.view(np.int16)).cuda().view(tdt)
@@ -1017,7 +1032,7 @@ def run_attention(args, rank, world, local_rank, sampler):
 
     def call(i):
         c = i % copies
-        aq.aq_attention_decode(q, *caches[c], bits, group, out=outs[c], stream=stream)
+        attend(q, caches[c], outs[c])
 
     with torch.cuda.stream(stream):
         call(0)
@@ -1039,8 +1054,7 @@ def run_attention(args, rank, world, local_rank, sampler):
     with torch.cuda.stream(stream):
         for i in range(n_e2e):
             q_dev.copy_(q_host, non_blocking=True)
-            aq.aq_attention_decode(q_dev, *caches[i % copies], bits, group, out=outs[0],
-                                   stream=stream)
+            attend(q_dev, caches[i % copies], outs[0])
             o_host.copy_(outs[0], non_blocking=True)
             stream.synchronize()
     e2e_us = reduce_max((time.perf_counter() - t0) * 1e6 / n_e2e, "cuda")
@@ -1064,7 +1078,8 @@ def run_attention(args, rank, world, local_rank, sampler):
                    "l2": f"cold: {copies} rotating cache copies > 2x L2 ({l2 / 1e6:.0f} MB)",
                    "timing": f"CUDA events on the launching stream around {steps} calls "
                              f"replayed from CUDA graphs of {timer.chunk}",
-                   "launch": aq.aq_attention_describe(H, KV, N, D, bits, group),
+                   "launch": (aq.aq_attention_describe_ws(H, KV, N, D, bits, group, ws_bytes)
+                              if ws_mode else aq.aq_attention_describe(H, KV, N, D, bits, group)),
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm,
                      "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": attn_traffic,
@@ -1072,7 +1087,9 @@ def run_attention(args, rank, world, local_rank, sampler):
                      "algorithmic_bytes_per_launch": by},
         "e2e": {"value": round(whole_job_us_per_call(e2e_us, world), 3), "unit": "us/call",
                 "h2d_bytes_per_step": 2 * H * D, "d2h_bytes_per_step": 2 * H * D,
-                "path": "pinned q -> device, aq_attention_decode, o -> pinned host, sync"},
+                "path": "pinned q -> device, "
+                        + ("aq_attention_decode_ws" if ws_mode else "aq_attention_decode")
+                        + ", o -> pinned host, sync"},
         "gpu_launches": steps,
         "clocks": clocks,
     }

@@ -46,6 +46,7 @@
 #ifndef AQ_H
 #define AQ_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -218,6 +219,59 @@ aq_status aq_attention_decode(int dtype, const void *q_dev, const uint32_t *k_wo
  */
 int aq_attention_describe(int64_t H, int64_t KV, int64_t N, int64_t D, int bits, int group_size,
                           char *buf, int buflen);
+
+/*
+ * aq_attention_workspace_bytes — the workspace aq_attention_decode_ws needs
+ * to spread each KV head's rows over several thread-block clusters (the
+ * pages' kernel splits the rows of a head into blocks merged afterwards:
+ * src/model/fused-decode-kernel.ts, the flash-decoding split and its
+ * deterministic merge).  Returns 0 when one cluster per KV head is the best
+ * plan for these sizes on the current device, or for arguments
+ * aq_attention_decode would refuse.
+ */
+size_t aq_attention_workspace_bytes(int64_t H, int64_t KV, int64_t N, int64_t D, int bits,
+                                    int group_size);
+
+/*
+ * aq_attention_decode_ws — aq_attention_decode with a caller-provided
+ * workspace, so that a KV head's rows may span several clusters and the
+ * kernel may hold every SM (one cluster per KV head can hold only as many
+ * CTAs as the largest co-resident cluster).  Each cluster merges its CTAs in
+ * rank order through distributed shared memory and writes its partial
+ * (max, sum, unnormalised o per query head) to the workspace; the cluster
+ * that arrives last at a per-KV-head counter (one atomic add per cluster, no
+ * waiting) adds the partials in cluster order, writes o, and sets the
+ * counter back to zero.  The result is deterministic (fixed merge order)
+ * but not bit-identical to aq_attention_decode's (another split).
+ *   workspace_dev    device, 256-byte aligned, workspace_bytes long,
+ *                    owned by the caller.  Its first KV 32-bit words (the
+ *                    counters) must be zero before the first call (e.g.
+ *                    allocate it zeroed); every call leaves them zero.  The
+ *                    rest needs no initial value.
+ *   workspace_bytes  at least aq_attention_workspace_bytes(...) to get the
+ *                    several-cluster plan; any smaller size (0 with a NULL
+ *                    workspace) runs the one-cluster plan, as
+ *                    aq_attention_decode.
+ * Calls that may overlap (other streams, or the same workspace in flight)
+ * must use distinct workspaces.  Other arguments, results and errors as
+ * aq_attention_decode; AQ_ERR_INVALID_ARG also for workspace_bytes > 0 with
+ * a NULL workspace, AQ_ERR_MISALIGNED for a workspace not 256-byte aligned.
+ */
+aq_status aq_attention_decode_ws(int dtype, const void *q_dev, const uint32_t *k_words_dev,
+                                 const void *k_scales_dev, const void *k_biases_dev,
+                                 const uint32_t *v_words_dev, const void *v_scales_dev,
+                                 const void *v_biases_dev, int64_t H, int64_t KV, int64_t N,
+                                 int64_t D, int bits, int group_size, void *out_dev,
+                                 void *workspace_dev, size_t workspace_bytes, void *stream);
+
+/*
+ * aq_attention_describe_ws — aq_attention_describe for
+ * aq_attention_decode_ws with a workspace of workspace_bytes: with a
+ * workspace the line also names "clusters_per_kv_head=K workspace=W" (the
+ * grid is KV x C x K CTAs, W the bytes the plan uses).
+ */
+int aq_attention_describe_ws(int64_t H, int64_t KV, int64_t N, int64_t D, int bits,
+                             int group_size, size_t workspace_bytes, char *buf, int buflen);
 
 /* Largest number of projections aq_matmul_multi takes in one call. */
 #define AQ_MAX_PROJ 4

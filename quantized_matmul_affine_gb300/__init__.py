@@ -25,6 +25,7 @@ __all__ = [
     "AQ_VARIANT_TC", "AQ_VARIANT_GEMV", "AQ_VARIANT_TCW", "AQ_NUM_VARIANTS", "aq_pack", "aq_quantize",
     "aq_quantize_bf16", "aq_matmul", "aq_matmul_bf16", "aq_matmul_multi", "aq_matmul_gate_up",
     "aq_matmul_ex", "aq_quantize_ex", "aq_attention_decode", "aq_attention_describe",
+    "aq_attention_workspace_bytes", "aq_attention_decode_ws", "aq_attention_describe_ws",
     "aq_matmul_variant", "aq_matmul_host", "aq_select", "aq_describe", "aq_stats", "aq_stats_reset",
     "aq_device_error",
     "aq_free", "aq_status_string", "aq_variant_name", "aq_version", "lib_path", "load",
@@ -62,6 +63,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         raise ImportError(f"libaq.so not built at {path}")
     lib = ctypes.CDLL(path)
     p, i64, i32, u32p = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+    sz = ctypes.c_size_t
     sig = {
         "aq_pack": ([p, i64, i64, i32, p, p], i32),
         "aq_quantize": ([p, i64, i64, i32, p, p, p, p], i32),
@@ -79,6 +81,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "aq_select": ([i64, i64, i64, i32, i32], i32),
         "aq_describe": ([i64, i64, i64, i32, i32, p, i32], i32),
         "aq_attention_describe": ([i64, i64, i64, i64, i32, i32, p, i32], i32),
+        "aq_attention_workspace_bytes": ([i64, i64, i64, i64, i32, i32], sz),
+        "aq_attention_decode_ws": ([i32, p, p, p, p, p, p, p, i64, i64, i64, i64, i32, i32, p, p,
+                                    sz, p], i32),
+        "aq_attention_describe_ws": ([i64, i64, i64, i64, i32, i32, sz, p, i32], i32),
         "aq_stats": ([p, i32], i32),
         "aq_stats_reset": ([], None),
         "aq_device_error": ([u32p, i32], i32),
@@ -252,10 +258,7 @@ def aq_matmul_ex(x, Wq, scales, biases, bits, group_size, out=None, stream=None)
     return out
 
 
-def aq_attention_decode(q, k, v, bits, group_size, out=None, stream=None) -> torch.Tensor:
-    """Decode attention over a quantised KV cache.  q [H, D] (fp16 or bf16);
-    k and v are (words [KV, N, D*bits/32] int32, scales [KV, N, D/group] fp16,
-    biases [KV, N, D/group] fp16).  Returns o [H, D] in q's dtype."""
+def _attention_args(q, k, v, bits, group_size, out):
     if q.dtype not in _ACT:
         raise ValueError("q must be float16 or bfloat16")
     if q.dim() != 2 or len(k) != 3 or len(v) != 3 or any(t.dim() != 3 for t in (*k, *v)):
@@ -271,11 +274,44 @@ def aq_attention_decode(q, k, v, bits, group_size, out=None, stream=None) -> tor
     if out is None:
         out = torch.empty((H, D), dtype=q.dtype, device=q.device)
     _check_out(out, "out", H * D, q.dtype)
-    _check(load().aq_attention_decode(dtype, _dev(q, "q"), _dev(k[0], "k_words"),
-                                      _dev(k[1], "k_scales"), _dev(k[2], "k_biases"),
-                                      _dev(v[0], "v_words"), _dev(v[1], "v_scales"),
-                                      _dev(v[2], "v_biases"), H, KV, N, D, bits, group_size,
+    ptrs = (_dev(q, "q"), _dev(k[0], "k_words"), _dev(k[1], "k_scales"), _dev(k[2], "k_biases"),
+            _dev(v[0], "v_words"), _dev(v[1], "v_scales"), _dev(v[2], "v_biases"))
+    return dtype, ptrs, (H, KV, N, D), out
+
+
+def aq_attention_decode(q, k, v, bits, group_size, out=None, stream=None) -> torch.Tensor:
+    """Decode attention over a quantised KV cache.  q [H, D] (fp16 or bf16);
+    k and v are (words [KV, N, D*bits/32] int32, scales [KV, N, D/group] fp16,
+    biases [KV, N, D/group] fp16).  Returns o [H, D] in q's dtype."""
+    dtype, ptrs, (H, KV, N, D), out = _attention_args(q, k, v, bits, group_size, out)
+    _check(load().aq_attention_decode(dtype, *ptrs, H, KV, N, D, bits, group_size,
                                       _dev(out, "out"), _stream(stream)), "aq_attention_decode")
+    return out
+
+
+def aq_attention_workspace_bytes(H: int, KV: int, N: int, D: int, bits: int,
+                                 group_size: int) -> int:
+    """Workspace bytes for aq_attention_decode_ws's several-cluster plan (0:
+    one cluster per KV head is best, or the sizes are refused)."""
+    return int(load().aq_attention_workspace_bytes(H, KV, N, D, bits, group_size))
+
+
+def aq_attention_decode_ws(q, k, v, bits, group_size, workspace=None, out=None,
+                           stream=None) -> torch.Tensor:
+    """aq_attention_decode with a workspace (a uint8 device tensor whose
+    first KV 32-bit words are zero before the first call; every call leaves
+    them zero).  workspace=None allocates a zeroed one of the size the plan
+    needs for this call."""
+    dtype, ptrs, (H, KV, N, D), out = _attention_args(q, k, v, bits, group_size, out)
+    if workspace is None:
+        n = aq_attention_workspace_bytes(H, KV, N, D, bits, group_size)
+        workspace = torch.zeros(max(n, 1), dtype=torch.uint8, device=q.device)
+    if workspace.dtype != torch.uint8 or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous uint8 tensor")
+    _check(load().aq_attention_decode_ws(dtype, *ptrs, H, KV, N, D, bits, group_size,
+                                         _dev(out, "out"), _dev(workspace, "workspace"),
+                                         workspace.numel(), _stream(stream)),
+           "aq_attention_decode_ws")
     return out
 
 
@@ -386,6 +422,16 @@ def aq_attention_describe(H: int, KV: int, N: int, D: int, bits: int, group_size
     device for its count of co-resident clusters)."""
     buf = ctypes.create_string_buffer(256)
     load().aq_attention_describe(H, KV, N, D, bits, group_size, ctypes.addressof(buf), 256)
+    return buf.value.decode()
+
+
+def aq_attention_describe_ws(H: int, KV: int, N: int, D: int, bits: int, group_size: int,
+                             workspace_bytes: int) -> str:
+    """The launch geometry of aq_attention_decode_ws with a workspace of
+    workspace_bytes."""
+    buf = ctypes.create_string_buffer(256)
+    load().aq_attention_describe_ws(H, KV, N, D, bits, group_size, workspace_bytes,
+                                    ctypes.addressof(buf), 256)
     return buf.value.decode()
 
 

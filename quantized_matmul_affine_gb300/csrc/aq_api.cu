@@ -336,6 +336,41 @@ aq_status aq_attention_decode(int dtype, const void *q_dev, const uint32_t *k_wo
     if (!attention_supported(H, KV, N, D, bits, group_size)) return AQ_ERR_UNSUPPORTED;
     if (attention_launch(dtype, q_dev, k_words_dev, k_scales_dev, k_biases_dev, v_words_dev,
                          v_scales_dev, v_biases_dev, H, KV, N, D, bits, group_size, out_dev,
+                         nullptr, 0, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return AQ_ERR_CUDA;
+    return AQ_OK;
+}
+
+size_t aq_attention_workspace_bytes(int64_t H, int64_t KV, int64_t N, int64_t D, int bits,
+                                    int group_size) {
+    if (H < 1 || KV < 1 || N < 1 || H % KV != 0) return 0;
+    if (!attention_supported(H, KV, N, D, bits, group_size)) return 0;
+    return attention_workspace_bytes(H, KV, N, D, bits, group_size);
+}
+
+aq_status aq_attention_decode_ws(int dtype, const void *q_dev, const uint32_t *k_words_dev,
+                                 const void *k_scales_dev, const void *k_biases_dev,
+                                 const uint32_t *v_words_dev, const void *v_scales_dev,
+                                 const void *v_biases_dev, int64_t H, int64_t KV, int64_t N,
+                                 int64_t D, int bits, int group_size, void *out_dev,
+                                 void *workspace_dev, size_t workspace_bytes, void *stream) {
+    if (dtype != AQ_F16 && dtype != AQ_BF16) return AQ_ERR_INVALID_ARG;
+    if (!q_dev || !k_words_dev || !k_scales_dev || !k_biases_dev || !v_words_dev ||
+        !v_scales_dev || !v_biases_dev || !out_dev || (workspace_bytes > 0 && !workspace_dev))
+        return AQ_ERR_INVALID_ARG;
+    if (H < 1 || KV < 1 || N < 1 || D < 1 || H % KV != 0) return AQ_ERR_INVALID_ARG;
+    if ((bits != 4 && bits != 8) ||
+        (group_size != 32 && group_size != 64 && group_size != 128) || D % group_size != 0)
+        return AQ_ERR_INVALID_ARG;
+    if (!aligned(q_dev, 2) || !aligned(out_dev, 2) || !aligned(k_words_dev, 16) ||
+        !aligned(v_words_dev, 16) || !aligned(k_scales_dev, 16) || !aligned(k_biases_dev, 16) ||
+        !aligned(v_scales_dev, 16) || !aligned(v_biases_dev, 16) ||
+        !aligned(workspace_dev, 256))
+        return AQ_ERR_MISALIGNED;
+    if (!attention_supported(H, KV, N, D, bits, group_size)) return AQ_ERR_UNSUPPORTED;
+    if (attention_launch(dtype, q_dev, k_words_dev, k_scales_dev, k_biases_dev, v_words_dev,
+                         v_scales_dev, v_biases_dev, H, KV, N, D, bits, group_size, out_dev,
+                         workspace_bytes > 0 ? workspace_dev : nullptr, workspace_bytes,
                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return AQ_ERR_CUDA;
     return AQ_OK;
@@ -469,7 +504,16 @@ int aq_attention_describe(int64_t H, int64_t KV, int64_t N, int64_t D, int bits,
     if (H < 1 || KV < 1 || N < 1 || H % KV != 0) return snprintf(buf, buflen, "invalid arguments");
     if (!attention_supported(H, KV, N, D, bits, group_size))
         return snprintf(buf, buflen, "unsupported");
-    return attention_describe(H, KV, N, D, bits, group_size, buf, buflen);
+    return attention_describe(H, KV, N, D, bits, group_size, 0, buf, buflen);
+}
+
+int aq_attention_describe_ws(int64_t H, int64_t KV, int64_t N, int64_t D, int bits,
+                             int group_size, size_t workspace_bytes, char *buf, int buflen) {
+    if (!buf || buflen < 1) return -1;
+    if (H < 1 || KV < 1 || N < 1 || H % KV != 0) return snprintf(buf, buflen, "invalid arguments");
+    if (!attention_supported(H, KV, N, D, bits, group_size))
+        return snprintf(buf, buflen, "unsupported");
+    return attention_describe(H, KV, N, D, bits, group_size, workspace_bytes, buf, buflen);
 }
 
 aq_status aq_stats(uint64_t *calls, int n) {

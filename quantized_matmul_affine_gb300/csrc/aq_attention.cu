@@ -64,9 +64,15 @@ struct AttnParams {
     uint32_t *err;
     int KV, N, nrep;
     int block;          // cached rows per CTA (multiple of 16)
-    int csize;          // CTAs per cluster (one KV head)
+    int csize;          // CTAs per cluster
+    int nclus;          // clusters per KV head (> 1 only with a workspace)
     int stages;         // ring depth
     int bf16;
+    // workspace (nclus > 1): per (KV head, cluster, query head) the
+    // cluster's max and sum (log2 units) and its unnormalised o, and one
+    // arrival counter per KV head (zero between calls)
+    float *ws_m, *ws_l, *ws_o;
+    unsigned *cnt;
 };
 
 template <int BITS, int D, int GROUP>
@@ -214,9 +220,10 @@ __global__ void __launch_bounds__(Shape<BITS, D, GROUP>::kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, t = lane & 3;
-    const int kv = (int)blockIdx.x / p.csize;
+    const int kv = (int)blockIdx.x / (p.csize * p.nclus);
+    const int clus = ((int)blockIdx.x / p.csize) % p.nclus;
     const int rank = (int)blockIdx.x % p.csize;
-    const int n0 = rank * p.block;
+    const int n0 = (clus * p.csize + rank) * p.block;
     const int n1 = min(p.N, n0 + p.block);
     const int nst = n1 > n0 ? (n1 - n0 + SR - 1) / SR : 0;
     const int nrep = p.nrep;
@@ -684,19 +691,22 @@ __global__ void __launch_bounds__(Shape<BITS, D, GROUP>::kThreads, 1)
     }
     __syncthreads();
 
-    // the cluster's CTAs, in rank order; rank r writes its share of o
+    // the cluster's CTAs, in rank order; rank r writes its share of o (or,
+    // with several clusters a KV head, of the cluster's partial result)
     const int C = p.csize;
     if (C > 1) cluster_sync();
     const int total4 = nrep * D / 4;
     const int chunk4 = (total4 + C - 1) / C;
     const uint32_t bm = smem_u32(cm), bl = smem_u32(cl), bo = smem_u32(co);
+    const size_t wpart = (size_t)(kv * p.nclus + clus) * nrep;  // (head, cluster) partials
     for (int i4 = rank * chunk4 + (int)threadIdx.x; i4 < min(total4, (rank + 1) * chunk4);
          i4 += kAttnThreads) {
         const int j = (4 * i4) / D, d = 4 * i4 - j * D;
-        float L = 0.f;
+        float L = 0.f, M = -INFINITY;
         float4 Ov = make_float4(0.f, 0.f, 0.f, 0.f);
         if (C == 1) {
             L = cl[j];
+            M = cm[j];
             Ov = reinterpret_cast<const float4 *>(co)[i4];
         } else {
             // every rank's (max, sum, o) loaded at once, then folded in rank order
@@ -709,7 +719,6 @@ __global__ void __launch_bounds__(Shape<BITS, D, GROUP>::kThreads, 1)
                     lr[rr] = ld_dsmem_f32(map_to_rank(bl + 4u * j, (uint32_t)rr));
                     orr[rr] = ld_dsmem_v4(map_to_rank(bo + 16u * (uint32_t)i4, (uint32_t)rr));
                 }
-            float M = -INFINITY;
 #pragma unroll
             for (int rr = 0; rr < 16; ++rr)
                 if (rr < C) M = fmaxf(M, mr[rr]);
@@ -724,6 +733,14 @@ __global__ void __launch_bounds__(Shape<BITS, D, GROUP>::kThreads, 1)
                     Ov.w = fmaf(orr[rr].w, g, Ov.w);
                 }
         }
+        if (p.nclus > 1) {
+            reinterpret_cast<float4 *>(p.ws_o + (wpart + j) * D)[d / 4] = Ov;
+            if (d == 0) {
+                p.ws_m[wpart + j] = M;
+                p.ws_l[wpart + j] = L;
+            }
+            continue;
+        }
         const float inv[4] = {Ov.x / L, Ov.y / L, Ov.z / L, Ov.w / L};
         const size_t oi = (size_t)(kv * nrep + j) * D + d;
 #pragma unroll
@@ -734,7 +751,54 @@ __global__ void __launch_bounds__(Shape<BITS, D, GROUP>::kThreads, 1)
                 static_cast<__half *>(p.out)[oi + k] = __float2half_rn(inv[k]);
         }
     }
+    if (p.nclus > 1) __threadfence();  // the partials are visible GPU-wide before the count
     if (C > 1) cluster_sync();  // keep this CTA's results until every rank has read them
+    if (p.nclus == 1) return;
+
+    // Several clusters a KV head: the cluster that arrives last (one atomic
+    // count a cluster, no waiting) adds the clusters' partials in cluster
+    // order, writes o and sets the count back to zero for the next call.
+    __shared__ int s_last;
+    if (rank != 0) return;
+    __syncthreads();  // the cluster barrier above covered every rank's writes
+    if (threadIdx.x == 0) {
+        const unsigned old = atomicAdd(&p.cnt[kv], 1u);
+        s_last = old == (unsigned)(p.nclus - 1);
+        __threadfence();
+    }
+    __syncthreads();
+    if (!s_last) return;
+    for (int i4 = (int)threadIdx.x; i4 < total4; i4 += kAttnThreads) {
+        const int j = (4 * i4) / D, d = 4 * i4 - j * D;
+        const size_t w0 = (size_t)kv * p.nclus * nrep + j;  // cluster c at w0 + c * nrep
+        float M = -INFINITY;
+        for (int c = 0; c < p.nclus; ++c) M = fmaxf(M, __ldcg(p.ws_m + w0 + (size_t)c * nrep));
+        float L = 0.f;
+        float4 Ov = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c = 0; c < p.nclus; ++c) {
+            const float mc = __ldcg(p.ws_m + w0 + (size_t)c * nrep);
+            if (mc == -INFINITY) continue;  // a cluster with no rows adds nothing
+            const float g = exp2f(mc - M);
+            L = fmaf(__ldcg(p.ws_l + w0 + (size_t)c * nrep), g, L);
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(
+                                        p.ws_o + (w0 + (size_t)c * nrep) * D) +
+                                    d / 4);
+            Ov.x = fmaf(v.x, g, Ov.x);
+            Ov.y = fmaf(v.y, g, Ov.y);
+            Ov.z = fmaf(v.z, g, Ov.z);
+            Ov.w = fmaf(v.w, g, Ov.w);
+        }
+        const float inv[4] = {Ov.x / L, Ov.y / L, Ov.z / L, Ov.w / L};
+        const size_t oi = (size_t)(kv * nrep + j) * D + d;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (p.bf16)
+                static_cast<__nv_bfloat16 *>(p.out)[oi + k] = __float2bfloat16_rn(inv[k]);
+            else
+                static_cast<__half *>(p.out)[oi + k] = __float2half_rn(inv[k]);
+        }
+    }
+    if (threadIdx.x == 0) p.cnt[kv] = 0u;
 }
 
 template <int BITS, int D, int GROUP>
@@ -787,31 +851,61 @@ const int *attn_active_clusters() {
     return n;
 }
 
-// Cluster size: the c minimising (waves of clusters) x (stages per CTA),
-// the smaller c on ties; 0 when no size can run (no device).
+// Workspace of a plan with k clusters a KV head (k > 1): the arrival
+// counters, then the partial maxima, sums and o, each 256-byte aligned.
+struct AttnWs {
+    size_t off_m, off_l, off_o, bytes;
+};
+inline AttnWs attn_ws_layout(int64_t KV, int k, int64_t nrep, int64_t D) {
+    auto up = [](size_t b) { return (b + 255) / 256 * 256; };
+    AttnWs w;
+    const size_t parts = (size_t)(KV * k * nrep);
+    w.off_m = up((size_t)KV * sizeof(unsigned));
+    w.off_l = w.off_m + up(parts * sizeof(float));
+    w.off_o = w.off_l + up(parts * sizeof(float));
+    w.bytes = w.off_o + parts * (size_t)D * sizeof(float);
+    return w;
+}
+
+struct AttnPick {
+    int c, k;  // CTAs a cluster, clusters a KV head
+};
+
+// Cluster size c and clusters per KV head k: the pair minimising
+// (waves of clusters) x (stages per CTA), plus, for k > 1, the cost of the
+// merge across clusters (the partials through global memory, an atomic,
+// one CTA's second merge: measured ~2-3 us, about the time of 2.3 stages of
+// 64 KB, so charged as 2.3 x 64 KB / stage bytes stages); among equals the
+// smaller k, then the smaller c.  k > 1 only when ws_bytes holds its
+// workspace.  {0, 0} when no size can run (no device).
 template <int BITS, int D, int GROUP>
-int attn_pick_cluster(int64_t KV, int64_t N) {
+AttnPick attn_pick(int64_t KV, int64_t N, int64_t nrep, size_t ws_bytes) {
     constexpr int SR = Shape<BITS, D, GROUP>::kStageRows;
     const int *n = attn_active_clusters<BITS, D, GROUP>();
     const int64_t maxc = std::min<int64_t>(16, std::max<int64_t>(1, (N + SR - 1) / SR));
-    int best = 0;
-    int64_t best_cost = INT64_MAX;
-    for (int c = 1; c <= maxc; ++c) {
-        if (n[c] < 1) continue;
-        const int64_t waves = (KV + n[c] - 1) / n[c];
-        const int64_t block = ((N + c - 1) / c + 15) / 16 * 16;
-        const int64_t cost = waves * ((block + SR - 1) / SR);
-        if (cost < best_cost) {
-            best_cost = cost;
-            best = c;
+    const int64_t maxct = std::max<int64_t>(1, (N + 15) / 16);  // CTAs of at least 16 rows
+    AttnPick best = {0, 0};
+    double best_cost = 1e300;
+    for (int k = 1; k <= 16; ++k) {
+        if (k > 1 && attn_ws_layout(KV, k, nrep, D).bytes > ws_bytes) break;
+        for (int c = 1; c <= maxc; ++c) {
+            if (n[c] < 1 || (int64_t)k * c > maxct) continue;
+            const int64_t waves = (KV * k + n[c] - 1) / n[c];
+            const int64_t block = ((N + (int64_t)k * c - 1) / ((int64_t)k * c) + 15) / 16 * 16;
+            const double merge = 2.3 * 65536.0 / (double)Shape<BITS, D, GROUP>::kStageBytes;
+            const double cost = (double)(waves * ((block + SR - 1) / SR)) + (k > 1 ? merge : 0.0);
+            if (cost < best_cost) {
+                best_cost = cost;
+                best = {c, k};
+            }
         }
     }
     return best;
 }
 
 struct AttnPlan {
-    int cluster, block, stages;
-    size_t smem;
+    int cluster, block, stages, nclus;
+    size_t smem, ws_bytes;
 };
 
 struct AttnLaunch {
@@ -822,12 +916,15 @@ struct AttnLaunch {
     void *out;
     int64_t H, KV, N;
     cudaStream_t stream;
+    void *ws;         // workspace, 256-byte aligned (may be null)
+    size_t ws_bytes;  // its size (0: one cluster a KV head)
 };
 
 template <int BITS, int D, int GROUP>
 cudaError_t attn_run(const AttnLaunch &L, AttnPlan *plan) {
     using S = Shape<BITS, D, GROUP>;
-    const int C = attn_pick_cluster<BITS, D, GROUP>(L.KV, L.N);
+    const AttnPick pk = attn_pick<BITS, D, GROUP>(L.KV, L.N, L.H / L.KV, L.ws ? L.ws_bytes : 0);
+    const int C = pk.c;
     if (C < 1) return cudaErrorNoDevice;
     AttnParams prm;
     prm.q = L.q;
@@ -840,12 +937,21 @@ cudaError_t attn_run(const AttnLaunch &L, AttnPlan *plan) {
     prm.N = (int)L.N;
     prm.nrep = (int)(L.H / L.KV);
     prm.csize = C;
-    prm.block = (int)(((L.N + C - 1) / C + 15) / 16 * 16);
+    prm.nclus = pk.k;
+    const int64_t ctas = (int64_t)C * pk.k;  // CTAs a KV head
+    prm.block = (int)(((L.N + ctas - 1) / ctas + 15) / 16 * 16);
     const int nst = (prm.block + S::kStageRows - 1) / S::kStageRows;
     prm.stages = std::max(1, std::min(attn_max_stages<BITS, D, GROUP>(), nst));
     prm.bf16 = L.dtype == AQ_BF16;
+    const AttnWs wl = attn_ws_layout(L.KV, pk.k, prm.nrep, D);
+    uint8_t *wsb = static_cast<uint8_t *>(L.ws);
+    prm.cnt = pk.k > 1 ? reinterpret_cast<unsigned *>(wsb) : nullptr;
+    prm.ws_m = pk.k > 1 ? reinterpret_cast<float *>(wsb + wl.off_m) : nullptr;
+    prm.ws_l = pk.k > 1 ? reinterpret_cast<float *>(wsb + wl.off_l) : nullptr;
+    prm.ws_o = pk.k > 1 ? reinterpret_cast<float *>(wsb + wl.off_o) : nullptr;
     if (plan) {
-        *plan = {C, prm.block, prm.stages, attn_smem_t<BITS, D, GROUP>(prm.stages, prm.nrep)};
+        *plan = {C, prm.block, prm.stages, pk.k,
+                 attn_smem_t<BITS, D, GROUP>(prm.stages, prm.nrep), pk.k > 1 ? wl.bytes : 0};
         return cudaSuccess;
     }
 
@@ -870,7 +976,7 @@ cudaError_t attn_run(const AttnLaunch &L, AttnPlan *plan) {
     auto kern = attn_kernel<BITS, D, GROUP>;
     attn_active_clusters<BITS, D, GROUP>();  // sets the kernel attributes
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(L.KV * C), 1, 1);
+    cfg.gridDim = dim3((unsigned)(L.KV * C * pk.k), 1, 1);
     cfg.blockDim = dim3(S::kThreads, 1, 1);
     cfg.dynamicSmemBytes = attn_smem_t<BITS, D, GROUP>(prm.stages, prm.nrep);
     cfg.stream = L.stream;
@@ -926,22 +1032,44 @@ bool attention_supported(int64_t H, int64_t KV, int64_t N, int64_t D, int bits, 
 }
 
 int attention_describe(int64_t H, int64_t KV, int64_t N, int64_t D, int bits, int group,
-                       char *buf, int len) {
+                       size_t ws_bytes, char *buf, int len) {
     AttnLaunch L = {};
     L.H = H;
     L.KV = KV;
     L.N = N;
+    L.ws = ws_bytes ? reinterpret_cast<void *>(256) : nullptr;  // planning only
+    L.ws_bytes = ws_bytes;
     AttnPlan pl = {};
     if (attn_dispatch(D, bits, group, L, &pl) != cudaSuccess) return snprintf(buf, len, "no device");
-    return snprintf(buf, len, "attn cluster=%d block=%d stages=%d smem=%zu grid=%lld", pl.cluster,
-                    pl.block, pl.stages, pl.smem, (long long)(KV * pl.cluster));
+    if (ws_bytes == 0)
+        return snprintf(buf, len, "attn cluster=%d block=%d stages=%d smem=%zu grid=%lld",
+                        pl.cluster, pl.block, pl.stages, pl.smem, (long long)(KV * pl.cluster));
+    return snprintf(buf, len,
+                    "attn cluster=%d block=%d stages=%d smem=%zu grid=%lld "
+                    "clusters_per_kv_head=%d workspace=%zu",
+                    pl.cluster, pl.block, pl.stages, pl.smem,
+                    (long long)(KV * pl.cluster * pl.nclus), pl.nclus, pl.ws_bytes);
+}
+
+size_t attention_workspace_bytes(int64_t H, int64_t KV, int64_t N, int64_t D, int bits,
+                                 int group) {
+    AttnLaunch L = {};
+    L.H = H;
+    L.KV = KV;
+    L.N = N;
+    L.ws = reinterpret_cast<void *>(256);  // planning only: any size allowed
+    L.ws_bytes = (size_t)1 << 40;
+    AttnPlan pl = {};
+    if (attn_dispatch(D, bits, group, L, &pl) != cudaSuccess) return 0;
+    return pl.ws_bytes;
 }
 
 cudaError_t attention_launch(int dtype, const void *q, const uint32_t *kw, const void *ks,
                              const void *kb, const uint32_t *vw, const void *vs, const void *vb,
                              int64_t H, int64_t KV, int64_t N, int64_t D, int bits, int group,
-                             void *out, cudaStream_t stream) {
-    const AttnLaunch L = {dtype, q, kw, vw, ks, kb, vs, vb, out, H, KV, N, stream};
+                             void *out, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    const AttnLaunch L = {dtype, q,  kw, vw, ks, kb, vs, vb, out, H, KV, N, stream,
+                          ws,    ws_bytes};
     return attn_dispatch(D, bits, group, L, nullptr);
 }
 

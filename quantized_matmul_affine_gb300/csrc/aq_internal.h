@@ -88,13 +88,20 @@ bool generic_supported_g(const MatmulArgs &a, int group);
 bool segv_supported(const MatmulArgs &a, int group);
 cudaError_t segv_launch(const MatmulArgs &a, int group);
 bool attention_supported(int64_t H, int64_t KV, int64_t N, int64_t D, int bits, int group);
-// The launch geometry aq_attention_decode would use (snprintf semantics).
+// The launch geometry aq_attention_decode (ws_bytes 0) or
+// aq_attention_decode_ws (a workspace of ws_bytes) would use (snprintf
+// semantics).
 int attention_describe(int64_t H, int64_t KV, int64_t N, int64_t D, int bits, int group,
-                       char *buf, int len);
+                       size_t ws_bytes, char *buf, int len);
+// Workspace bytes that let the attention kernel spread a KV head over
+// several clusters (0 when one cluster a KV head is the best plan).
+size_t attention_workspace_bytes(int64_t H, int64_t KV, int64_t N, int64_t D, int bits,
+                                 int group);
+// ws: a workspace of ws_bytes (256-byte aligned; its counters zero), or null.
 cudaError_t attention_launch(int dtype, const void *q, const uint32_t *kw, const void *ks,
                              const void *kb, const uint32_t *vw, const void *vs, const void *vb,
                              int64_t H, int64_t KV, int64_t N, int64_t D, int bits, int group,
-                             void *out, cudaStream_t stream);
+                             void *out, void *ws, size_t ws_bytes, cudaStream_t stream);
 cudaError_t generic_launch_g(const MatmulArgs &a, int group);
 cudaError_t pack_launch(const uint8_t *codes, int64_t N, int64_t K, int bits, uint32_t *words,
                         cudaStream_t stream);

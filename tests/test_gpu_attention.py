@@ -57,14 +57,24 @@ def _case(H, KV, N, D, bits, group, dtype, seed, qscale=2.0, ramp=0.0):
     return (kc, ks, kb), (vc, vs, vb), q_bits
 
 
-def _check(H, KV, N, D, bits, group, dtype, seed, qscale=2.0, ramp=0.0):
+def _check(H, KV, N, D, bits, group, dtype, seed, qscale=2.0, ramp=0.0, workspace=False):
+    """workspace=True: aq_attention_decode_ws with a zeroed workspace of the
+    size its plan wants; returns that workspace (its counters checked zero)."""
     (kc, ks, kb), (vc, vs, vb), q_bits = _case(H, KV, N, D, bits, group, dtype, seed, qscale,
                                                ramp)
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
     q = torch.from_numpy(q_bits.view(np.int16)).cuda().view(tdt)
-    o = aq.aq_attention_decode(q, _dev_cache(kc, ks, kb, KV, N, D, bits),
-                               _dev_cache(vc, vs, vb, KV, N, D, bits), bits, group)
+    kd, vd = _dev_cache(kc, ks, kb, KV, N, D, bits), _dev_cache(vc, vs, vb, KV, N, D, bits)
+    ws = None
+    if workspace:
+        n = aq.aq_attention_workspace_bytes(H, KV, N, D, bits, group)
+        ws = torch.zeros(max(n, 1), dtype=torch.uint8, device="cuda")
+        o = aq.aq_attention_decode_ws(q, kd, vd, bits, group, workspace=ws)
+    else:
+        o = aq.aq_attention_decode(q, kd, vd, bits, group)
     torch.cuda.synchronize()
+    if ws is not None and ws.numel() >= 4 * KV:  # a several-cluster plan: its counters
+        assert int(ws[:4 * KV].view(torch.int32).abs().sum()) == 0, "counters not back to zero"
     got = workloads.to_f64(o.view(torch.int16).cpu().numpy().view(np.uint16), dtype)
     ref, smag, vmag = oracle.attention(workloads.to_f64(q_bits, dtype), oracle.pack_g(kc, bits),
                                        ks, kb, oracle.pack_g(vc, bits), vs, vb, KV, N, bits, group)
@@ -78,6 +88,7 @@ def _check(H, KV, N, D, bits, group, dtype, seed, qscale=2.0, ramp=0.0):
     bad = np.argwhere(~(np.abs(got - ref) <= tol))
     assert bad.size == 0, [(int(h), int(d), float(got[h, d]), float(ref[h, d]), float(tol[h, d]))
                            for h, d in bad[:4]]
+    return ws
 
 
 @pytest.mark.parametrize("H,KV,N,D,bits,group,dtype", [
@@ -147,3 +158,64 @@ def test_attention_deterministic():
     outs = [aq.aq_attention_decode(q, k, v, 4, 64).clone() for _ in range(3)]
     for o in outs[1:]:
         assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+
+
+# aq_attention_decode_ws: a KV head's rows over several clusters, partials
+# merged by the cluster that arrives last (counters in the workspace).
+@pytest.mark.parametrize("H,KV,N,D,bits,group,dtype", [
+    (16, 8, 32768, 256, 4, 64, "bf16"),   # the 32k workload shape: four clusters a head
+    (16, 8, 8192, 256, 4, 64, "bf16"),    # the 8k workload shape
+    (16, 8, 2048, 256, 4, 64, "bf16"),
+    (16, 8, 8192, 256, 8, 64, "bf16"),
+    (32, 8, 8192, 128, 4, 64, "bf16"),
+    (16, 8, 8192, 512, 4, 64, "bf16"),    # warp pairs
+    (8, 2, 5000, 128, 4, 32, "fp16"),     # few KV heads: many clusters a head
+    (4, 1, 20000, 64, 8, 64, "fp16"),
+    (8, 8, 300, 128, 4, 128, "bf16"),     # few rows: one cluster a head
+])
+def test_attention_ws_parity(H, KV, N, D, bits, group, dtype):
+    _check(H, KV, N, D, bits, group, dtype, seed=3 * H + KV + N + D + bits + group,
+           workspace=True)
+
+
+def test_attention_ws_plan_spreads_the_heads():
+    # 8 KV heads of 32768 rows: one cluster per head holds at most ~12 CTAs;
+    # with a workspace the plan takes several clusters a head
+    n = aq.aq_attention_workspace_bytes(16, 8, 32768, 256, 4, 64)
+    assert n > 0
+    d = aq.aq_attention_describe_ws(16, 8, 32768, 256, 4, 64, n)
+    fields = dict(kv.split("=") for kv in d.split()[1:])
+    assert int(fields["clusters_per_kv_head"]) > 1 and int(fields["workspace"]) <= n
+    assert int(fields["grid"]) == 8 * int(fields["cluster"]) * int(fields["clusters_per_kv_head"])
+    assert int(fields["grid"]) > 8 * int(dict(kv.split("=") for kv in aq.aq_attention_describe(
+        16, 8, 32768, 256, 4, 64).split()[1:])["cluster"])
+    # too small a workspace: the one-cluster plan
+    d1 = aq.aq_attention_describe_ws(16, 8, 32768, 256, 4, 64, 64)
+    assert "clusters_per_kv_head=1" in d1
+
+
+def test_attention_ws_deterministic_and_reusable():
+    H, KV, N, D, bits, group = 16, 8, 32768, 256, 4, 64
+    (kc, ks, kb), (vc, vs, vb), q_bits = _case(H, KV, N, D, bits, group, "bf16", seed=5)
+    q = torch.from_numpy(q_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    kd, vd = _dev_cache(kc, ks, kb, KV, N, D, bits), _dev_cache(vc, vs, vb, KV, N, D, bits)
+    n = aq.aq_attention_workspace_bytes(H, KV, N, D, bits, group)
+    ws = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    outs = [aq.aq_attention_decode_ws(q, kd, vd, bits, group, workspace=ws) for _ in range(3)]
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+    assert int(ws[:4 * KV].view(torch.int32).abs().sum()) == 0
+
+
+def test_attention_ws_small_workspace_runs_one_cluster():
+    _check(16, 8, 4096, 256, 4, 64, "bf16", seed=12)  # reference for the shape
+    H, KV, N, D, bits, group = 16, 8, 4096, 256, 4, 64
+    (kc, ks, kb), (vc, vs, vb), q_bits = _case(H, KV, N, D, bits, group, "bf16", seed=12)
+    q = torch.from_numpy(q_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    kd, vd = _dev_cache(kc, ks, kb, KV, N, D, bits), _dev_cache(vc, vs, vb, KV, N, D, bits)
+    o1 = aq.aq_attention_decode(q, kd, vd, bits, group)
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")  # too small for several clusters
+    o2 = aq.aq_attention_decode_ws(q, kd, vd, bits, group, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
