@@ -265,6 +265,34 @@ aq_status aq_attention_decode_ws(int dtype, const void *q_dev, const uint32_t *k
                                  void *workspace_dev, size_t workspace_bytes, void *stream);
 
 /*
+ * aq_attention_decode_static — aq_attention_decode_ws without a caller
+ * workspace: the several-cluster plan's workspace is a fixed array of
+ * AQ_ATTENTION_STATIC_SCRATCH_BYTES in device memory the library owns, so
+ * the call allocates nothing, for hosts that cannot allocate device memory
+ * per call (a C caller with no device allocator of its own, a decode loop
+ * that must not synchronise on cudaMalloc).  The pages have no counterpart
+ * (their kernel sums the blocks through a framework array); this is an
+ * interface of this library only.
+ *   Arguments, results and errors as aq_attention_decode, and the same plan
+ *   and results as aq_attention_decode_ws given a workspace of
+ *   aq_attention_workspace_bytes(...): AQ_ERR_UNSUPPORTED (nothing queued)
+ *   also when that workspace is larger than the array.
+ *   The array is zero at module load and every call leaves its counters
+ *   zero.  Its device address is looked up once per device on the first
+ *   call that needs it (cudaGetSymbolAddress): make that first call outside
+ *   stream capture.  One array per device: calls that may overlap in time
+ *   on one device (other streams, other host threads) share it and race; the
+ *   caller serialises them.
+ */
+#define AQ_ATTENTION_STATIC_SCRATCH_BYTES 1048576
+aq_status aq_attention_decode_static(int dtype, const void *q_dev, const uint32_t *k_words_dev,
+                                     const void *k_scales_dev, const void *k_biases_dev,
+                                     const uint32_t *v_words_dev, const void *v_scales_dev,
+                                     const void *v_biases_dev, int64_t H, int64_t KV, int64_t N,
+                                     int64_t D, int bits, int group_size, void *out_dev,
+                                     void *stream);
+
+/*
  * aq_attention_describe_ws — aq_attention_describe for
  * aq_attention_decode_ws with a workspace of workspace_bytes: with a
  * workspace the line also names "clusters_per_kv_head=K workspace=W" (the

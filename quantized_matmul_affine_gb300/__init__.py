@@ -26,6 +26,7 @@ __all__ = [
     "aq_quantize_bf16", "aq_matmul", "aq_matmul_bf16", "aq_matmul_multi", "aq_matmul_gate_up",
     "aq_matmul_ex", "aq_quantize_ex", "aq_attention_decode", "aq_attention_describe",
     "aq_attention_workspace_bytes", "aq_attention_decode_ws", "aq_attention_describe_ws",
+    "aq_attention_decode_static",
     "aq_matmul_variant", "aq_matmul_host", "aq_select", "aq_describe", "aq_stats", "aq_stats_reset",
     "aq_device_error",
     "aq_free", "aq_status_string", "aq_variant_name", "aq_version", "lib_path", "load",
@@ -85,6 +86,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "aq_attention_decode_ws": ([i32, p, p, p, p, p, p, p, i64, i64, i64, i64, i32, i32, p, p,
                                     sz, p], i32),
         "aq_attention_describe_ws": ([i64, i64, i64, i64, i32, i32, sz, p, i32], i32),
+        "aq_attention_decode_static": ([i32, p, p, p, p, p, p, p, i64, i64, i64, i64, i32, i32, p,
+                                        p], i32),
         "aq_stats": ([p, i32], i32),
         "aq_stats_reset": ([], None),
         "aq_device_error": ([u32p, i32], i32),
@@ -286,6 +289,17 @@ def aq_attention_decode(q, k, v, bits, group_size, out=None, stream=None) -> tor
     dtype, ptrs, (H, KV, N, D), out = _attention_args(q, k, v, bits, group_size, out)
     _check(load().aq_attention_decode(dtype, *ptrs, H, KV, N, D, bits, group_size,
                                       _dev(out, "out"), _stream(stream)), "aq_attention_decode")
+    return out
+
+
+def aq_attention_decode_static(q, k, v, bits, group_size, out=None, stream=None) -> torch.Tensor:
+    """aq_attention_decode_ws with the library's own fixed scratch instead of
+    a workspace (nothing allocated per call); calls on one device must not
+    overlap in time."""
+    dtype, ptrs, (H, KV, N, D), out = _attention_args(q, k, v, bits, group_size, out)
+    _check(load().aq_attention_decode_static(dtype, *ptrs, H, KV, N, D, bits, group_size,
+                                             _dev(out, "out"), _stream(stream)),
+           "aq_attention_decode_static")
     return out
 
 

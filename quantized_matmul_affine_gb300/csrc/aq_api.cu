@@ -341,6 +341,38 @@ aq_status aq_attention_decode(int dtype, const void *q_dev, const uint32_t *k_wo
     return AQ_OK;
 }
 
+aq_status aq_attention_decode_static(int dtype, const void *q_dev, const uint32_t *k_words_dev,
+                                     const void *k_scales_dev, const void *k_biases_dev,
+                                     const uint32_t *v_words_dev, const void *v_scales_dev,
+                                     const void *v_biases_dev, int64_t H, int64_t KV, int64_t N,
+                                     int64_t D, int bits, int group_size, void *out_dev,
+                                     void *stream) {
+    if (dtype != AQ_F16 && dtype != AQ_BF16) return AQ_ERR_INVALID_ARG;
+    if (!q_dev || !k_words_dev || !k_scales_dev || !k_biases_dev || !v_words_dev ||
+        !v_scales_dev || !v_biases_dev || !out_dev)
+        return AQ_ERR_INVALID_ARG;
+    if (H < 1 || KV < 1 || N < 1 || D < 1 || H % KV != 0) return AQ_ERR_INVALID_ARG;
+    if ((bits != 4 && bits != 8) ||
+        (group_size != 32 && group_size != 64 && group_size != 128) || D % group_size != 0)
+        return AQ_ERR_INVALID_ARG;
+    if (!aligned(q_dev, 2) || !aligned(out_dev, 2) || !aligned(k_words_dev, 16) ||
+        !aligned(v_words_dev, 16) || !aligned(k_scales_dev, 16) || !aligned(k_biases_dev, 16) ||
+        !aligned(v_scales_dev, 16) || !aligned(v_biases_dev, 16))
+        return AQ_ERR_MISALIGNED;
+    if (!attention_supported(H, KV, N, D, bits, group_size)) return AQ_ERR_UNSUPPORTED;
+    // the plan aq_attention_decode_ws takes with a workspace of the size it
+    // asks for; refused (nothing queued) when that is larger than the scratch
+    const size_t need = attention_workspace_bytes(H, KV, N, D, bits, group_size);
+    if (need > (size_t)AQ_ATTENTION_STATIC_SCRATCH_BYTES) return AQ_ERR_UNSUPPORTED;
+    void *scratch = need > 0 ? attention_static_scratch() : nullptr;
+    if (need > 0 && !scratch) return AQ_ERR_CUDA;
+    if (attention_launch(dtype, q_dev, k_words_dev, k_scales_dev, k_biases_dev, v_words_dev,
+                         v_scales_dev, v_biases_dev, H, KV, N, D, bits, group_size, out_dev,
+                         scratch, need, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return AQ_ERR_CUDA;
+    return AQ_OK;
+}
+
 size_t aq_attention_workspace_bytes(int64_t H, int64_t KV, int64_t N, int64_t D, int bits,
                                     int group_size) {
     if (H < 1 || KV < 1 || N < 1 || H % KV != 0) return 0;

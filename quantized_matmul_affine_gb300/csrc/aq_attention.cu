@@ -1073,6 +1073,31 @@ cudaError_t attention_launch(int dtype, const void *q, const uint32_t *kw, const
     return attn_dispatch(D, bits, group, L, nullptr);
 }
 
+// Scratch for aq_attention_decode_static: the workspace of the several-
+// cluster plan in device memory the library owns, for callers that cannot
+// allocate per call (plain C hosts without a device allocator at hand, or
+// decode loops that must not pay for a synchronising cudaMalloc each step).
+// Zero-initialised at module load; the counters at its start are zero again
+// after every call.  One array per device context, so calls that overlap in
+// time on one device (two streams) would share it and race.
+static __device__ __align__(256) uint8_t g_attn_scratch[AQ_ATTENTION_STATIC_SCRATCH_BYTES];
+
+// The device address of g_attn_scratch for the current device, looked up
+// once per device (cudaGetSymbolAddress); nullptr if the lookup fails.
+void *attention_static_scratch() {
+    static std::mutex mu;
+    static void *addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
 cudaError_t attn_read_error(uint32_t *code, bool clear) {
     cudaError_t e = cudaMemcpyFromSymbol(code, g_attn_error, sizeof(uint32_t));
     if (e != cudaSuccess || !clear) return e;

@@ -97,6 +97,9 @@ int attention_describe(int64_t H, int64_t KV, int64_t N, int64_t D, int bits, in
 // several clusters (0 when one cluster a KV head is the best plan).
 size_t attention_workspace_bytes(int64_t H, int64_t KV, int64_t N, int64_t D, int bits,
                                  int group);
+// The library's static attention scratch on the current device (its
+// address looked up once per device), or nullptr.
+void *attention_static_scratch();
 // ws: a workspace of ws_bytes (256-byte aligned; its counters zero), or null.
 cudaError_t attention_launch(int dtype, const void *q, const uint32_t *kw, const void *ks,
                              const void *kb, const uint32_t *vw, const void *vs, const void *vb,
