@@ -58,10 +58,13 @@ constexpr int kATileBytes = 128 * 128;
 // back one MMA completion plus one dequantisation after its last use, which
 // three or more slots keep off the critical path.
 constexpr int b_slots_for(int BM, bool gen = false) {
-    // the general-width path's raw rings are larger: three 32 KB x slots
-    return BM >= 256 ? (gen ? 3 : 4) : BM == 128 ? 5 : 8;
+    // 256-row tiles: three 32 KB x slots, beside four A slots (3/4 bits) or
+    // the larger raw rings of the general-width path
+    return BM > 256 ? 4 : BM == 256 ? 3 : BM == 128 ? 5 : 8;
 }
-constexpr int a_slots_for(int BM) { return BM >= 256 ? 3 : BM == 128 ? 4 : 5; }
+constexpr int a_slots_for(int BM, bool gen = false) {
+    return BM > 256 ? 3 : BM == 256 ? (gen ? 3 : 4) : BM == 128 ? 4 : 5;
+}
 constexpr int ni_for(int BM) { return BM > 256 ? 256 : BM; }
 // Raw super-stages per dequant warp; all but one are in flight while the
 // warp dequantises, so that the weight stream keeps enough bytes in flight
@@ -298,7 +301,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // GEN: any code width and group size (32/64/128, p.lg), codes decoded at
     // compile-time bit offsets; otherwise 3/4 bits at groups of 64.
     using R = typename std::conditional<GEN, RawG<B>, Raw<B>>::type;
-    constexpr int kA = a_slots_for(BM);
+    constexpr int kA = a_slots_for(BM, GEN);
     constexpr int kB = b_slots_for(BM, GEN);
     constexpr int kRawSlots = GEN ? raw_slots_g(B) : raw_slots_for(BM);
     // A 512-row x tile is two N = 256 MMAs per k-step into one 512-column
@@ -1149,7 +1152,7 @@ bool tc_plan(const MatmulArgs &a, TcPlan &pl, int group = 0) {
         q.lg = 6;
         q.NG = (int)(a.K / 64);
     }
-    const int kA = a_slots_for(pl.BM), kB = b_slots_for(pl.BM, gen);
+    const int kA = a_slots_for(pl.BM, gen), kB = b_slots_for(pl.BM, gen);
     size_t off = (size_t)kA * kATileBytes;
     q.off_b = (uint32_t)off;
     off += (size_t)kB * ni_for(pl.BM) * 128;
