@@ -25,7 +25,8 @@
  *     stream).  Work is queued asynchronously; no entry point synchronises
  *     the device except aq_matmul_host (which synchronises `stream`) and
  *     aq_device_error.
- *   - The library allocates no device memory in any entry point.
+ *   - The library allocates no device memory in any entry point (the
+ *     fixed scratch of aq_attention_decode_static exists from module load).
  *   - Arguments are validated before anything is queued; a bad argument
  *     returns an error status and queues nothing.  Launch failures return
  *     AQ_ERR_CUDA.  Faults that happen later on the device surface at the
