@@ -60,7 +60,7 @@ constexpr int kATileBytes = 128 * 128;
 constexpr int b_slots_for(int BM, bool gen = false) {
     // 256-row tiles: three 32 KB x slots, beside four A slots (3/4 bits) or
     // the larger raw rings of the general-width path
-    return BM > 256 ? 4 : BM == 256 ? 3 : BM == 128 ? 5 : 8;
+    return BM > 256 ? 4 : BM == 256 ? 3 : BM == 128 ? 4 : 8;
 }
 constexpr int a_slots_for(int BM, bool gen = false) {
     return BM > 256 ? 3 : BM == 256 ? (gen ? 3 : 4) : BM == 128 ? 4 : 5;
@@ -311,6 +311,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     constexpr int kH = BM / kNI;     // B sub-tiles per stage
     constexpr int kBTile = kNI * 128;
     constexpr int kAcc = BM > 256 ? 1 : 2;  // accumulators in tensor memory
+    // 128-row x tiles take two stages per MMA step: one x barrier for both
+    // stages' sub-tiles, one wait for both A tiles, 8 MMAs, then one commit
+    // for each ring.  The issuing thread pays about 80 cycles for every
+    // barrier wait and 100 for every commit, which an N = 128 MMA (64
+    // cycles at the full rate) does not hide; measured on GB300, a round of
+    // 8 MMAs with two waits and two commits takes 889 cycles against 706
+    // for 4 MMAs with the same.
+    constexpr int kSP = BM == 128 ? 2 : 1;
+    constexpr int kBG = kB / kSP;  // x barriers (groups of kSP slots)
+    static_assert(kSP == 1 || (kH == 1 && kB % kSP == 0 && kA % 2 == 0), "stage pairs");
     extern __shared__ uint8_t smem_dyn[];
     // Align to 1024 bytes by an offset from the __shared__ array itself, so
     // that every access below stays a shared-memory access (32-bit address).
@@ -391,6 +401,24 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             int tile, gb, ge;
             for (int u = 0; unit_of(u, tile, gb, ge); ++u) {
                 const int m0 = (tile % p.m_tiles) * BM;
+                if constexpr (kSP == 2) {
+                    // the two stages' sub-tiles on one barrier
+                    for (int g = gb; g < ge; g += 2, ++bi) {
+                        const int slot = bi % kBG;
+                        const uint32_t ph = (bi / kBG) & 1u;
+                        if (bi >= kBG && !tc_wait(&b_empty[slot], ph ^ 1u, flag, 0x0102))
+                            goto tma_done;
+#ifdef AQ_TEST_HOOKS
+                        if (p.withhold && bi == 0) continue;  // nothing will complete b_full[0]
+#endif
+                        mbar_arrive_expect_tx(&b_full[slot], 2 * kBTile);
+#pragma unroll
+                        for (int e = 0; e < 2; ++e)
+                            tma_load_2d(b_ring + (2 * slot + e) * kBTile, &tmap_x, 64 * (g + e), m0,
+                                        &b_full[slot]);
+                    }
+                    continue;
+                }
                 for (int g = gb; g < ge; ++g) {
 #pragma unroll
                     for (int h = 0; h < kH; ++h) {
@@ -414,8 +442,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         tma_done:
             // Wind-down: the loads issued for the last sub-tiles land before
             // the CTA goes on (earlier ones were consumed by the MMAs).
-            for (uint32_t j = bi > (uint32_t)kB ? bi - kB : 0u; j < bi; ++j)
-                drain_wait(&b_full[j % kB], (j / kB) & 1u);
+            for (uint32_t j = bi > (uint32_t)kBG ? bi - kBG : 0u; j < bi; ++j)
+                drain_wait(&b_full[j % kBG], (j / kBG) & 1u);
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------------
@@ -440,6 +468,40 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             if (!__all_sync(0xffffffffu, free)) break;
             tc_fence_after();
             const uint32_t d = tmem + b * BM;
+            if constexpr (kSP == 2) {
+                for (int g = gb; ok && g < ge; g += 2, ai += 2, ++bi) {
+                    const uint32_t al = ai + 1;  // the pair's second A stage
+                    const bool got_a = tc_wait(&a_full[al % kA], (al / kA) & 1u, flag, 0x0302);
+                    if (!__all_sync(0xffffffffu, got_a)) {
+                        ok = false;
+                        break;
+                    }
+                    const int bs = bi % kBG;
+                    const bool got_b = tc_wait(&b_full[bs], (bi / kBG) & 1u, flag, 0x0402);
+                    if (!__all_sync(0xffffffffu, got_b)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issued = true;
+                    if (lane == 0) {
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const uint64_t ad = a_desc0 +
+                                (uint64_t)((uint32_t)(((ai + e) % kA) * kATileBytes) >> 4);
+                            const uint64_t bd =
+                                b_desc0 + (uint64_t)((uint32_t)((2 * bs + e) * kBTile) >> 4);
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                tc_mma_f16(d, ad + 2 * kk, bd + 2 * kk, idesc,
+                                           (g + e != gb || kk != 0) ? 1u : 0u);
+                        }
+                        tc_commit(&b_empty[bs]);
+                        tc_commit(&a_empty[al % kA]);  // frees both A slots
+                    }
+                    __syncwarp();
+                }
+            } else {
             for (int g = gb; ok && g < ge; ++g, ++ai) {
                 const int as = ai % kA;
                 const bool got_a = tc_wait(&a_full[as], (ai / kA) & 1u, flag, 0x0302);
@@ -471,6 +533,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 if (!ok) break;
                 if (lane == 0) tc_commit(&a_empty[as]);
                 __syncwarp();
+            }
             }
             if (!ok) break;
             if (lane == 0) tc_commit(&acc_full[b]);
@@ -622,15 +685,25 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             // two groups give the ALUs twice the independent work and one
             // fence serves both; a shallow ring keeps one.
             constexpr int kPair = kA >= 4 ? 2 : 1;
+            static_assert(kSP == 1 || kPair == 2, "stage pairs are dequantised together");
 #pragma unroll 1
             for (int j = 0; j < kGroups; j += kPair, it += kPair) {
                 bool free2 = true;
-#pragma unroll
-                for (int e = 0; e < kPair; ++e) {
-                    const uint32_t ie = it + e;
-                    if (ie >= (uint32_t)kA &&
-                        !tc_wait(&a_empty[ie % kA], ((ie / kA) & 1u) ^ 1u, flag, 0x0602))
+                if constexpr (kSP == 2) {
+                    // a pair's slots come back together (one commit after the
+                    // pair that last used them)
+                    const uint32_t il = it + 1;
+                    if (il >= (uint32_t)kA &&
+                        !tc_wait(&a_empty[il % kA], ((il / kA) & 1u) ^ 1u, flag, 0x0602))
                         free2 = false;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < kPair; ++e) {
+                        const uint32_t ie = it + e;
+                        if (ie >= (uint32_t)kA &&
+                            !tc_wait(&a_empty[ie % kA], ((ie / kA) & 1u) ^ 1u, flag, 0x0602))
+                            free2 = false;
+                    }
                 }
                 if (!free2) {
                     ok = false;
@@ -701,8 +774,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
+                    if constexpr (kSP == 2) {
+                        mbar_arrive(&a_full[(it + 1) % kA]);  // the MMA waits on the second
+                    } else {
 #pragma unroll
-                    for (int e = 0; e < kPair; ++e) mbar_arrive(&a_full[(it + e) % kA]);
+                        for (int e = 0; e < kPair; ++e) mbar_arrive(&a_full[(it + e) % kA]);
+                    }
                 }
             }
             __syncwarp();
