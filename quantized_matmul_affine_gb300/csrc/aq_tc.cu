@@ -63,7 +63,7 @@ constexpr int b_slots_for(int BM, bool gen = false) {
     return BM > 256 ? 4 : BM == 256 ? 3 : BM == 128 ? 4 : 8;
 }
 constexpr int a_slots_for(int BM, bool gen = false) {
-    return BM > 256 ? 3 : BM == 256 ? (gen ? 3 : 4) : BM == 128 ? 4 : 5;
+    return BM > 256 ? 3 : BM == 256 ? (gen ? 3 : 4) : 4;
 }
 constexpr int ni_for(int BM) { return BM > 256 ? 256 : BM; }
 // Raw super-stages per dequant warp; all but one are in flight while the
@@ -311,14 +311,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     constexpr int kH = BM / kNI;     // B sub-tiles per stage
     constexpr int kBTile = kNI * 128;
     constexpr int kAcc = BM > 256 ? 1 : 2;  // accumulators in tensor memory
-    // 128-row x tiles take two stages per MMA step: one x barrier for both
+    // x tiles of up to 128 rows take two stages per MMA step: one x barrier for both
     // stages' sub-tiles, one wait for both A tiles, 8 MMAs, then one commit
     // for each ring.  The issuing thread pays about 80 cycles for every
     // barrier wait and 100 for every commit, which an N = 128 MMA (64
     // cycles at the full rate) does not hide; measured on GB300, a round of
     // 8 MMAs with two waits and two commits takes 889 cycles against 706
     // for 4 MMAs with the same.
-    constexpr int kSP = BM == 128 ? 2 : 1;
+    constexpr int kSP = BM <= 128 ? 2 : 1;
     constexpr int kBG = kB / kSP;  // x barriers (groups of kSP slots)
     static_assert(kSP == 1 || (kH == 1 && kB % kSP == 0 && kA % 2 == 0), "stage pairs");
     extern __shared__ uint8_t smem_dyn[];
