@@ -145,6 +145,27 @@ __device__ __forceinline__ float code_f(const uint32_t (&w)[B], int i) {
     return __uint_as_float((t & (((1u << B) - 1u) << 12)) | 0x45000000u);
 }
 
+// x tiles of up to 128 rows (3/4-bit path) take the A tiles from tensor
+// memory: the dequantising warps write them with tcgen05.st and the MMAs read
+// them there, so that the dequantisation needs no shared-memory stores of A
+// and no proxy fence.  Eight A stages of 32 columns sit beside the two
+// accumulators.
+constexpr bool ta_for(int BM, bool gen) { return BM <= 128 && !gen; }
+constexpr int kATmemSlots = 8;
+constexpr int kRawSlotsTa = 3;
+
+// Raw super-stage of one dequantising warp when A is in tensor memory: the
+// 32 rows of its lane quarter, 4 groups.
+template <int B>
+struct RawT {
+    static constexpr int kGroupBytes = 8 * B;
+    static constexpr int kRowBytes = kGroups * kGroupBytes;  // 128 / 96
+    static constexpr int kChunksPerRow = kRowBytes / 16;    // 8 / 6
+    static constexpr int kRowPitch = kRowBytes + 16;         // 144 / 112: rows in distinct banks
+    static constexpr int kSbOff = 32 * kRowPitch;            // scales[32][4], then biases[32][4]
+    static constexpr int kSlotBytes = kSbOff + 2 * 32 * 8;
+};
+
 struct TcParams {
     const uint32_t *Wq;
     const __half *scales;
@@ -301,9 +322,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // GEN: any code width and group size (32/64/128, p.lg), codes decoded at
     // compile-time bit offsets; otherwise 3/4 bits at groups of 64.
     using R = typename std::conditional<GEN, RawG<B>, Raw<B>>::type;
-    constexpr int kA = a_slots_for(BM, GEN);
+    constexpr bool TA = ta_for(BM, GEN);
+    constexpr int kA = TA ? kATmemSlots : a_slots_for(BM, GEN);
     constexpr int kB = b_slots_for(BM, GEN);
-    constexpr int kRawSlots = GEN ? raw_slots_g(B) : raw_slots_for(BM);
+    constexpr int kRawSlots = TA ? kRawSlotsTa : GEN ? raw_slots_g(B) : raw_slots_for(BM);
     // A 512-row x tile is two N = 256 MMAs per k-step into one 512-column
     // accumulator (each weight tile dequantised once for 512 x rows); the
     // narrower tiles double-buffer their accumulator.
@@ -362,7 +384,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kA; ++s) {
-            mbar_init(&a_full[s], kDqWarps);
+            // tensor-memory A: one dequantising warp per lane quarter writes a stage
+            mbar_init(&a_full[s], TA ? 4 : kDqWarps);
             mbar_init(&a_empty[s], 1);
         }
         for (int s = 0; s < kB; ++s) {
@@ -487,14 +510,24 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     if (lane == 0) {
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
-                            const uint64_t ad = a_desc0 +
-                                (uint64_t)((uint32_t)(((ai + e) % kA) * kATileBytes) >> 4);
                             const uint64_t bd =
                                 b_desc0 + (uint64_t)((uint32_t)((2 * bs + e) * kBTile) >> 4);
+                            if constexpr (TA) {
+                                // A stage: 32 columns after the accumulators, 8 a k-step
+                                const uint32_t at =
+                                    tmem + (uint32_t)(2 * BM + ((ai + e) % kA) * 32);
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                tc_mma_f16(d, ad + 2 * kk, bd + 2 * kk, idesc,
-                                           (g + e != gb || kk != 0) ? 1u : 0u);
+                                for (int kk = 0; kk < 4; ++kk)
+                                    tc_mma_f16_ta(d, at + 8u * kk, bd + 2 * kk, idesc,
+                                                  (g + e != gb || kk != 0) ? 1u : 0u);
+                            } else {
+                                const uint64_t ad = a_desc0 +
+                                    (uint64_t)((uint32_t)(((ai + e) % kA) * kATileBytes) >> 4);
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk)
+                                    tc_mma_f16(d, ad + 2 * kk, bd + 2 * kk, idesc,
+                                               (g + e != gb || kk != 0) ? 1u : 0u);
+                            }
                         }
                         tc_commit(&b_empty[bs]);
                         tc_commit(&a_empty[al % kA]);  // frees both A slots
@@ -579,6 +612,146 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[b]);
         }
+    } else if constexpr (TA) {
+        // ------------------------------------------------------------------
+        // Dequantisation into tensor memory.  The warp's lane quarter q is
+        // the 32-row block q of each 128-row weight tile (thread = row); the
+        // two warps of a quarter take alternate 4-group super-stages.  Each
+        // stage (one group) is 64 values of the thread's row: eight words of
+        // codes, dequantised and written as 32 columns of the A stage.  The
+        // MMA warp takes stages in pairs: the pair's slots are waited for
+        // once and its second stage's arrival stands for both.
+        // ------------------------------------------------------------------
+        static_assert(kSP == 2 && kA % 2 == 0, "tensor-memory A is consumed in stage pairs");
+        using RT = RawT<B>;
+        const int dw = warp - kWarpDq;
+        const int q = warp & 3;
+        const int par = dw >> 2;
+        uint8_t *ring = raw + dw * kRawSlotsTa * RT::kSlotBytes;
+        const int64_t row_bytes = (int64_t)p.K * B / 8;
+        const int nlast = p.N - 1;
+        auto issue = [&](int tile, int ss, int slot) {
+            const int n0 = (tile / p.m_tiles) * 128 + 32 * q;
+            uint8_t *dst = ring + slot * RT::kSlotBytes;
+            const int64_t kb = (int64_t)ss * kGroups * RT::kGroupBytes;
+#pragma unroll
+            for (int i = 0; i < RT::kChunksPerRow; ++i) {
+                const int c = lane + 32 * i;
+                const int r = c / RT::kChunksPerRow, col = c % RT::kChunksPerRow;
+                const int64_t n = min(n0 + r, nlast);
+                cp_async16(dst + r * RT::kRowPitch + col * 16,
+                           reinterpret_cast<const uint8_t *>(p.Wq) + n * row_bytes + kb + col * 16,
+                           16u);
+            }
+            const int64_t n = min(n0 + lane, nlast);
+            cp_async8(dst + RT::kSbOff + lane * 8, p.scales + n * p.G + ss * kGroups);
+            cp_async8(dst + RT::kSbOff + 256 + lane * 8, p.biases + n * p.G + ss * kGroups);
+        };
+        // Cursor over the CTA's super-stages in order (gs counts them all);
+        // this warp takes those with gs % 2 == par.
+        struct Cur {
+            int u, tile, gb, ge, ss, gs;
+            bool valid;
+        };
+        auto cur_init = [&](Cur &c) {
+            c.u = c.ss = c.gs = 0;
+            c.valid = unit_of(0, c.tile, c.gb, c.ge);
+        };
+        auto cur_next = [&](Cur &c) {
+            do {
+                if (++c.ss == (c.ge - c.gb) / kGroups) {
+                    c.ss = 0;
+                    ++c.u;
+                    c.valid = unit_of(c.u, c.tile, c.gb, c.ge);
+                }
+                ++c.gs;
+            } while (c.valid && (c.gs & 1) != par);
+        };
+        Cur ic, cc;
+        cur_init(ic);
+        if (ic.valid && par == 1) cur_next(ic);
+        cc = ic;
+        int iss = 0;
+        // kRawSlotsTa - 1 super-stages ahead, one commit group each
+#pragma unroll 1
+        for (int pre = 0; pre < kRawSlotsTa - 1; ++pre) {
+            if (ic.valid) {
+                issue(ic.tile, ic.gb / kGroups + ic.ss, iss % kRawSlotsTa);
+                ++iss;
+                cur_next(ic);
+            }
+            cp_async_commit();
+        }
+        const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(2 * BM);
+        bool ok = true;
+        for (int cnt = 0; cc.valid && ok; ++cnt) {
+            if (ic.valid) {
+                issue(ic.tile, ic.gb / kGroups + ic.ss, iss % kRawSlotsTa);
+                ++iss;
+                cur_next(ic);
+            }
+            cp_async_commit();
+            cp_async_wait<kRawSlotsTa - 1>();
+            __syncwarp();
+            const uint8_t *slotp = ring + (cnt % kRawSlotsTa) * RT::kSlotBytes;
+            const uint2 sv2 = *reinterpret_cast<const uint2 *>(slotp + RT::kSbOff + lane * 8);
+            const uint2 bv2 = *reinterpret_cast<const uint2 *>(slotp + RT::kSbOff + 256 + lane * 8);
+            const uint4 sv = make_uint4(sv2.x, sv2.y, 0u, 0u);
+            const uint4 bv = make_uint4(bv2.x, bv2.y, 0u, 0u);
+            const uint8_t *rowp = slotp + lane * RT::kRowPitch;
+#pragma unroll 1
+            for (int j = 0; j < kGroups; ++j) {
+                const uint32_t it = 4u * (uint32_t)cc.gs + (uint32_t)j;  // the MMA's stage count
+                const int slot = (int)(it % kA);
+                if ((j & 1) == 0) {  // the pair's slots: freed by one commit
+                    const uint32_t il = it + 1;
+                    if (il >= (uint32_t)kA &&
+                        !tc_wait(&a_empty[il % kA], ((il / kA) & 1u) ^ 1u, flag, 0x0602)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+                const GroupConst gc = group_const<B>(h_at(sv, j), h_at(bv, j));
+                uint32_t u[8];  // 8 codes per entry, k = 8c .. 8c+7 of the stage
+                if constexpr (B == 4) {
+                    const uint4 w0 = *reinterpret_cast<const uint4 *>(rowp + 32 * j);
+                    const uint4 w1 = *reinterpret_cast<const uint4 *>(rowp + 32 * j + 16);
+                    u[0] = w0.x, u[1] = w0.y, u[2] = w0.z, u[3] = w0.w;
+                    u[4] = w1.x, u[5] = w1.y, u[6] = w1.z, u[7] = w1.w;
+                } else {
+                    const uint32_t *wp = reinterpret_cast<const uint32_t *>(rowp + 24 * j);
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const uint32_t x0 = wp[3 * hh], x1 = wp[3 * hh + 1], x2 = wp[3 * hh + 2];
+                        u[4 * hh + 0] = x0;
+                        u[4 * hh + 1] = __funnelshift_r(x0, x1, 24);
+                        u[4 * hh + 2] = __funnelshift_r(x1, x2, 16);
+                        u[4 * hh + 3] = x2 >> 8;
+                    }
+                }
+                uint32_t out[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 v = dq8<B, BF16>(u[c], gc);
+                    out[4 * c + 0] = v.x;
+                    out[4 * c + 1] = v.y;
+                    out[4 * c + 2] = v.z;
+                    out[4 * c + 3] = v.w;
+                }
+                tmem_st32(trow + (uint32_t)(slot * 32), out);
+                if (j & 1) {  // the pair is complete
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&a_full[slot]);
+                }
+            }
+            __syncwarp();
+            cur_next(cc);
+        }
+        cp_async_wait<0>();
+        tmem_wait_st();
     } else {
         // ------------------------------------------------------------------
         // Dequantisation: this warp's 16 rows of each 128-row weight tile.
@@ -800,7 +973,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         // barrier, error or not.
         constexpr int kCh = BM < 256 ? BM : 256;  // columns per hand-over
         constexpr int kXP = kCh + 4;              // floats per row of the buffer
-        static_assert(128 * kXP * 4 <= kA * kATileBytes + kB * kBTile, "hand-over buffer");
+        // the idle rings: A tiles (in shared memory unless TA), x tiles, raw codes
+        static_assert(128 * kXP * 4 <= (TA ? 0 : kA * kATileBytes) + kB * kBTile +
+                                           kDqWarps * kRawSlots *
+                                               (TA ? RawT<B>::kSlotBytes : R::kSlotBytes),
+                      "hand-over buffer");
         const int r = (int)blockIdx.x & 1;
         const int tile = p.rounds * (int)gridDim.x + ((int)blockIdx.x >> 1);
         int nfull = 0;  // whole tiles this CTA took before the tail
@@ -1208,8 +1385,10 @@ bool tc_plan(const MatmulArgs &a, TcPlan &pl, int group = 0) {
     q.n_tiles = (int)((a.N + 127) / 128);
     q.m_tiles = (int)((a.M + pl.BM - 1) / pl.BM);
     if ((int64_t)q.n_tiles * q.m_tiles > INT32_MAX) return false;
-    int raw_slot = a.bits == 4 ? Raw<4>::kSlotBytes : Raw<3>::kSlotBytes;
-    int kRawSlots = raw_slots_for(pl.BM);
+    const bool ta = ta_for(pl.BM, gen);
+    int raw_slot = ta ? (a.bits == 4 ? RawT<4>::kSlotBytes : RawT<3>::kSlotBytes)
+                      : (a.bits == 4 ? Raw<4>::kSlotBytes : Raw<3>::kSlotBytes);
+    int kRawSlots = ta ? kRawSlotsTa : raw_slots_for(pl.BM);
     if (gen) {
         switch (a.bits) {
             case 2: raw_slot = RawG<2>::kSlotBytes; break;
@@ -1229,8 +1408,8 @@ bool tc_plan(const MatmulArgs &a, TcPlan &pl, int group = 0) {
         q.lg = 6;
         q.NG = (int)(a.K / 64);
     }
-    const int kA = a_slots_for(pl.BM, gen), kB = b_slots_for(pl.BM, gen);
-    size_t off = (size_t)kA * kATileBytes;
+    const int kA = ta ? kATmemSlots : a_slots_for(pl.BM, gen), kB = b_slots_for(pl.BM, gen);
+    size_t off = ta ? 0 : (size_t)kA * kATileBytes;  // A tiles in shared memory
     q.off_b = (uint32_t)off;
     off += (size_t)kB * ni_for(pl.BM) * 128;
     q.off_raw = (uint32_t)off;
@@ -1240,7 +1419,7 @@ bool tc_plan(const MatmulArgs &a, TcPlan &pl, int group = 0) {
     off += (2 * kA + 2 * kB + 5) * 8 + 16;
     pl.smem = off + 1024;  // room to align the base to 1024 bytes
     if (pl.smem > kSmemLimitTc) return false;
-    q.tmem_cols = pl.BM >= 256 ? 512 : pl.BM == 128 ? 256 : 128;
+    q.tmem_cols = (pl.BM >= 256 || ta) ? 512 : pl.BM == 128 ? 256 : 128;
     q.Wq = a.Wq;
     q.scales = static_cast<const __half *>(a.scales);
     q.biases = static_cast<const __half *>(a.biases);
