@@ -60,7 +60,7 @@ constexpr int kATileBytes = 128 * 128;
 constexpr int b_slots_for(int BM, bool gen = false) {
     // 256-row tiles: three 32 KB x slots, beside four A slots (3/4 bits) or
     // the larger raw rings of the general-width path
-    return BM > 256 ? 4 : BM == 256 ? 3 : BM == 128 ? 4 : 8;
+    return BM > 256 ? 4 : BM == 256 ? (gen ? 3 : 4) : BM == 128 ? 4 : 8;
 }
 constexpr int a_slots_for(int BM, bool gen = false) {
     return BM > 256 ? 3 : BM == 256 ? (gen ? 3 : 4) : 4;
@@ -150,9 +150,11 @@ __device__ __forceinline__ float code_f(const uint32_t (&w)[B], int i) {
 // them there, so that the dequantisation needs no shared-memory stores of A
 // and no proxy fence.  Eight A stages of 32 columns sit beside the two
 // accumulators.
-constexpr bool ta_for(int BM, bool gen) { return BM <= 128 && !gen; }
+constexpr bool ta_for(int BM, bool gen) { return BM <= 256 && !gen; }
 constexpr int kATmemSlots = 8;
-constexpr int kRawSlotsTa = 3;
+// raw super-stages per dequantising warp with A in tensor memory (256-row x
+// tiles: two, beside four 32 KB x slots)
+constexpr int raw_slots_ta(int BM) { return BM == 256 ? 2 : 3; }
 
 // Raw super-stage of one dequantising warp when A is in tensor memory: the
 // 32 rows of its lane quarter, 4 groups.
@@ -325,14 +327,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     constexpr bool TA = ta_for(BM, GEN);
     constexpr int kA = TA ? kATmemSlots : a_slots_for(BM, GEN);
     constexpr int kB = b_slots_for(BM, GEN);
-    constexpr int kRawSlots = TA ? kRawSlotsTa : GEN ? raw_slots_g(B) : raw_slots_for(BM);
+    constexpr int kRawSlots = TA ? raw_slots_ta(BM) : GEN ? raw_slots_g(B) : raw_slots_for(BM);
     // A 512-row x tile is two N = 256 MMAs per k-step into one 512-column
     // accumulator (each weight tile dequantised once for 512 x rows); the
     // narrower tiles double-buffer their accumulator.
     constexpr int kNI = ni_for(BM);  // N of one MMA = rows of one B sub-tile
     constexpr int kH = BM / kNI;     // B sub-tiles per stage
     constexpr int kBTile = kNI * 128;
-    constexpr int kAcc = BM > 256 ? 1 : 2;  // accumulators in tensor memory
+    // accumulators in tensor memory: one of 512 columns, two of up to 256, or
+    // one of 256 beside 256-row tensor-memory A stages
+    constexpr int kAcc = (BM > 256 || (BM == 256 && TA)) ? 1 : 2;
     // x tiles of up to 128 rows take two stages per MMA step: one x barrier for both
     // stages' sub-tiles, one wait for both A tiles, 8 MMAs, then one commit
     // for each ring.  The issuing thread pays about 80 cycles for every
@@ -340,7 +344,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // cycles at the full rate) does not hide; measured on GB300, a round of
     // 8 MMAs with two waits and two commits takes 889 cycles against 706
     // for 4 MMAs with the same.
-    constexpr int kSP = BM <= 128 ? 2 : 1;
+    constexpr int kSP = (BM <= 128 || TA) ? 2 : 1;
     constexpr int kBG = kB / kSP;  // x barriers (groups of kSP slots)
     static_assert(kSP == 1 || (kH == 1 && kB % kSP == 0 && kA % 2 == 0), "stage pairs");
     extern __shared__ uint8_t smem_dyn[];
@@ -515,7 +519,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                             if constexpr (TA) {
                                 // A stage: 32 columns after the accumulators, 8 a k-step
                                 const uint32_t at =
-                                    tmem + (uint32_t)(2 * BM + ((ai + e) % kA) * 32);
+                                    tmem + (uint32_t)(kAcc * BM + ((ai + e) % kA) * 32);
 #pragma unroll
                                 for (int kk = 0; kk < 4; ++kk)
                                     tc_mma_f16_ta(d, at + 8u * kk, bd + 2 * kk, idesc,
@@ -627,6 +631,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const int dw = warp - kWarpDq;
         const int q = warp & 3;
         const int par = dw >> 2;
+        constexpr int kRawSlotsTa = raw_slots_ta(BM);
         uint8_t *ring = raw + dw * kRawSlotsTa * RT::kSlotBytes;
         const int64_t row_bytes = (int64_t)p.K * B / 8;
         const int nlast = p.N - 1;
@@ -682,7 +687,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             }
             cp_async_commit();
         }
-        const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(2 * BM);
+        const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(kAcc * BM);
         bool ok = true;
         for (int cnt = 0; cc.valid && ok; ++cnt) {
             if (ic.valid) {
@@ -1388,7 +1393,7 @@ bool tc_plan(const MatmulArgs &a, TcPlan &pl, int group = 0) {
     const bool ta = ta_for(pl.BM, gen);
     int raw_slot = ta ? (a.bits == 4 ? RawT<4>::kSlotBytes : RawT<3>::kSlotBytes)
                       : (a.bits == 4 ? Raw<4>::kSlotBytes : Raw<3>::kSlotBytes);
-    int kRawSlots = ta ? kRawSlotsTa : raw_slots_for(pl.BM);
+    int kRawSlots = ta ? raw_slots_ta(pl.BM) : raw_slots_for(pl.BM);
     if (gen) {
         switch (a.bits) {
             case 2: raw_slot = RawG<2>::kSlotBytes; break;
