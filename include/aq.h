@@ -72,9 +72,12 @@ typedef enum aq_variant {
     AQ_VARIANT_AUTO = -1,   /* the dispatch rule picks */
     AQ_VARIANT_GENERIC = 0, /* plain-load CUDA-core kernel: any K % 64 == 0, any alignment */
     AQ_VARIANT_QMV = 1,     /* small-M: bulk-async staged weights, warp MMA, factored dequant */
-    AQ_VARIANT_TC = 2,      /* large-M: tcgen05 MMA with TMEM accumulators */
+    AQ_VARIANT_TC = 2,      /* M > 32: tcgen05 MMA with TMEM accumulators; with fewer
+                               weight tiles than SMs, a tile's K range shared over the
+                               CTAs of a cluster */
     AQ_VARIANT_GEMV = 3,    /* M <= 32: one resident CTA per SM, TMA weight ring, warp MMA */
-    AQ_VARIANT_TCW = 4,     /* M <= 128: tcgen05 MMA with x as the 128-row operand and 256-row
+    AQ_VARIANT_TCW = 4,     /* M <= 128 (explicit only: the dispatch rule prefers TC):
+                               tcgen05 MMA with x as the 128-row operand and 256-row
                                weight tiles, K split over a cluster */
     AQ_NUM_VARIANTS = 5
 } aq_variant;

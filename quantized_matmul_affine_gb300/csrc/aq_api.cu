@@ -38,6 +38,7 @@ int qmv_max_m() {
 
 #ifdef AQ_TEST_HOOKS
 int g_test_withhold = 0;
+int g_test_cluster_split = 0;
 #endif
 
 int num_sms() {
@@ -107,26 +108,20 @@ static int gemv_max_m() {
 // 32000x4096; 128256x4096 and 57344x8192: 18-23% slower).
 static bool gemv_for_m1(const MatmulArgs &a) { return a.N <= 128ll * num_sms(); }
 
-// 33..128 activation rows go to the swapped-role tensor-core kernel when the
-// 128-row weight tiles of the tc kernel would leave the SMs short of work
-// (fewer than 0.6 x SMs tiles): its K split recruits the idle SMs.  Both are
-// bound by the dequantisation (~16-18 codes per ns per SM measured on
-// GB300), so with enough tiles tc's full grid wins (GB300, M = 64/128:
-// 10240x5120 3-bit 31.7 against 40.0 us, 5120x13824 72.5 against 101.6,
-// 4096x4096 25.2 against 30.7; 13824x5120 48.8 against 42.5, 28672x8192
-// 156 against 130).
-static bool tcw_first(const MatmulArgs &a) {
-    const int64_t tc_tiles = (a.N + 127) / 128;
-    return tc_tiles * 5 < (int64_t)num_sms() * 3;
-}
+// Past 32 activation rows the tensor-core kernel takes every shape: with
+// fewer weight tiles than SMs it shares tiles among the CTAs of a cluster
+// (the clustered K split), which left the swapped-role kernel (still
+// available as AQ_VARIANT_TCW) behind on every shape measured (GB300, us:
+// 10240x5120 3-bit at M = 33/64/128: 25.6/25.7/28.0 against 27.8/29.6/33.7;
+// 4096x4096 at 64/128: 13.1/14.2 against 24.0/28.7; 5120x13824 at 64: 30.6
+// against 64.0; 5120x5120 at 128: 17.6 against 39.4; 1024x5120 at 64: 11.5
+// against 15.2; 13824x5120 at 128: 30.4 against 43.0).
 
 // The dispatch rule.  Returns the variant for the arguments (alignment
 // included), never AQ_VARIANT_AUTO.
 static int choose(const MatmulArgs &a) {
     const bool gemv_first = a.M > 1 || gemv_for_m1(a);
     if (a.M <= gemv_max_m() && gemv_first && gemv_supported(a)) return AQ_VARIANT_GEMV;
-    if (a.M > gemv_max_m() && a.M <= 128 && tcw_first(a) && tcw_supported(a))
-        return AQ_VARIANT_TCW;
     const bool qmv = qmv_supported(a);
     const bool tc = tc_supported(a);
     if (qmv && (a.M <= qmv_max_m() || !tc)) return AQ_VARIANT_QMV;
@@ -604,6 +599,30 @@ const char *aq_version(void) { return "aq 0.1.0 (sm_103a)"; }
 // Test builds only: make a producer withhold the copies of its first stage
 // (see g_test_withhold), so that a test can watch a bounded wait run out.
 void aq_test_withhold(int what) { aq::g_test_withhold = what; }
+// Test builds only: force the tensor-core kernel's clustered K split to
+// `ctas` CTAs sharing `tiles` tiles where that plan is valid (ctas = -1:
+// never split this way; 0: the planner's choice).
+void aq_test_cluster_split(int ctas, int tiles) {
+    aq::g_test_cluster_split = ctas < 0 ? -1 : (ctas << 8) | (tiles & 255);
+}
+// Test builds only: co-resident clusters of 1..8 CTAs of the tensor-core
+// kernel, as the planner sees them (out[c] for c = 1..8).
+void aq_test_active_clusters(int *out) {
+    const int *n = aq::tc_active_clusters_for_tests();
+    for (int c = 1; c <= 8; ++c) out[c] = n[c];
+}
+// Test builds only: the tensor-core kernel's plan for these sizes, whatever
+// the dispatch rule would pick.
+int aq_test_describe_tc(int64_t M, int64_t N, int64_t K, int bits, int dtype, char *buf,
+                        int buflen) {
+    if (!buf || buflen < 1) return -1;
+    const uintptr_t fake = 0x100000;
+    aq::MatmulArgs a = aq::make_args(dtype, (const void *)fake, (const uint32_t *)fake,
+                                     (const void *)fake, (const void *)fake, M, N, K, bits,
+                                     (void *)fake, nullptr);
+    if (aq::check_args(a) != AQ_OK) return snprintf(buf, buflen, "invalid arguments");
+    return aq::tc_describe(a, buf, buflen);
+}
 #endif
 
 }  // extern "C"

@@ -114,6 +114,11 @@ cudaError_t pack_launch(const uint8_t *codes, int64_t N, int64_t K, int bits, ui
 // of its first stage, so that the waits on them run out (1 = the resident
 // small-M kernel, 2 = the large-M tensor-core kernel, 0 = none).
 extern int g_test_withhold;
+// Test builds only: the tensor-core kernel's clustered K split, forced to
+// (CTAs << 8) | tiles a cluster where that plan is valid (-1: never; 0: the
+// planner's choice).
+extern int g_test_cluster_split;
+const int *tc_active_clusters_for_tests();
 #endif
 
 // Device error words, one per translation unit that owns bounded waits.

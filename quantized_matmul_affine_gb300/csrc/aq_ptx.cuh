@@ -156,6 +156,16 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
     return v;
 }
 
+// 16 bytes (16-byte aligned address).
+__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 // ---------------------------------------------------------------------------
 // Warp MMA m16n8k16, fp16 inputs, fp32 accumulate.
 // ---------------------------------------------------------------------------

@@ -180,6 +180,13 @@ struct TcParams {
     // cluster (cluster c takes tile rounds * grid + c), added at the end
     // through distributed shared memory.
     int rounds, tail;
+    // Few tiles (fewer than SMs, x tiles of at most 128 rows): instead, a
+    // cluster of cl_ctas CTAs shares cl_tiles < cl_ctas consecutive tiles
+    // (cluster c from tile c * cl_tiles); the cluster's K stages, tile after
+    // tile, are dealt out in even runs of whole super-stages, so a CTA holds
+    // partial accumulators of one or two tiles, added at the end in rank
+    // (that is K) order through distributed shared memory.  0 when unused.
+    int cl_ctas, cl_tiles;
     uint32_t off_b, off_raw, off_bar, tmem_cols;
     int lg, NG;  // general-width path: log2 of the group size, groups per row
 #ifdef AQ_TEST_HOOKS
@@ -315,6 +322,20 @@ __device__ __forceinline__ __nv_bfloat16 cvt_out<__nv_bfloat16>(float v) {
     return __float2bfloat16_rn(v);
 }
 
+// Clustered K split: the run [s, e) of the cluster's stages (in groups, from
+// the cluster's first tile t0) that CTA `cta` takes.  Runs are whole
+// 4-group super-stages, as even as that allows.
+// (32-bit arithmetic: with K below 2^30 and clusters of at most 8, (r + 1) *
+// w4 stays below 2^28.)
+__device__ __forceinline__ void cl_range(const TcParams &p, int G, int total, int cta, int &s,
+                                         int &e, int &t0) {
+    const int C = p.cl_ctas, r = cta % C;
+    t0 = (cta / C) * p.cl_tiles;
+    const int w4 = min(p.cl_tiles, total - t0) * (G / 4);
+    s = 4 * (r * w4 / C);
+    e = 4 * ((r + 1) * w4 / C);
+}
+
 }  // namespace
 
 template <int B, bool BF16, int BM, bool GEN>
@@ -369,7 +390,23 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const int total = p.n_tiles * p.m_tiles;
     const int G = p.G;
     // Unit u of this CTA: its tile and K range [gb, ge) in groups.
+    // Clustered K split: this CTA's run [cl_s, cl_e) of its cluster's
+    // stages (in groups from the cluster's first tile cl_t0), which starts
+    // in the cluster's tile cl_ts.
+    int cl_s = 0, cl_e = 0, cl_t0 = 0, cl_ts = 0;
+    if (p.cl_ctas > 0) {
+        cl_range(p, G, total, (int)blockIdx.x, cl_s, cl_e, cl_t0);
+        cl_ts = cl_s / G;
+    }
     auto unit_of = [&](int u, int &tile, int &gb, int &ge) -> bool {
+        if (p.cl_ctas > 0) {
+            const int tt = cl_ts + u;  // the cluster's tile of unit u
+            if (cl_s >= cl_e || tt * G >= cl_e) return false;
+            tile = cl_t0 + tt;
+            gb = u == 0 ? cl_s - tt * G : 0;
+            ge = min(G, cl_e - tt * G);
+            return true;
+        }
         if (u < p.rounds) {
             tile = (int)blockIdx.x + u * (int)gridDim.x;
             gb = 0;
@@ -1034,6 +1071,126 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
         tc_fence_before();
     }
+    if constexpr (BM <= 128) {
+        if (p.cl_ctas > 0) {
+            // Clustered K split.  (1) The epilogue warps copy each of the
+            // CTA's one or two partial accumulators into the idle ring as
+            // [BM][128] floats (unit i at i * BM * 128).  (2) After a cluster
+            // barrier, the contributors of each tile (consecutive ranks) share
+            // its outputs evenly; each output is the sum of the contributors'
+            // partials in rank order, read through distributed shared memory,
+            // then stored to y.  (3) A last cluster barrier keeps every
+            // partial readable until all sums are done.  Every CTA takes both
+            // barriers, error or not.
+            static_assert(2 * BM * 128 * 4 <= (TA ? 0 : kA * kATileBytes) + kB * kBTile +
+                                                  kDqWarps * kRawSlots *
+                                                      (TA ? RawT<B>::kSlotBytes : R::kSlotBytes),
+                          "partial tiles");
+            const int C = p.cl_ctas;
+            const int r = (int)blockIdx.x % C;
+            const int cbase = (int)blockIdx.x - r;  // the cluster's first CTA
+            float *part = reinterpret_cast<float *>(smem);
+            tc_fence_after();
+            if (warp > kWarpMma) {
+                // warps 2..13: lane quarter warp % 4, column blocks of 16
+                // dealt out over the quarter's three warps
+                const int q = warp & 3, h = (warp - kWarpMma - 1) >> 2;
+                const int row = 32 * q + lane;
+                int tile, gb, ge;
+                constexpr int kBlk = (BM / 16 + 2) / 3;  // column blocks a warp, at most
+                for (int i = 0; i < 2 && unit_of(i, tile, gb, ge); ++i) {
+                    const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(i % kAcc) * BM;
+                    float *dst = part + i * BM * 128 + row;
+                    uint32_t v[kBlk][16];
+#pragma unroll
+                    for (int bk = 0; bk < kBlk; ++bk)
+                        if (16 * h + 48 * bk < BM) tmem_ld16(ta + (uint32_t)(16 * h + 48 * bk), v[bk]);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int bk = 0; bk < kBlk; ++bk) {
+                        const int c0 = 16 * h + 48 * bk;
+                        if (c0 >= BM) continue;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) dst[(c0 + j) * 128] = __uint_as_float(v[bk][j]);
+                    }
+                }
+            }
+            tc_fence_before();
+            cluster_sync();
+            grid_dependency_wait();  // every thread below stores y
+            T *y = static_cast<T *>(p.y);
+            // lane k < C: the run of the cluster's rank k
+            int k_s = 0, k_e = 0;
+            if (lane < C) {
+                int t0;
+                cl_range(p, G, total, cbase + lane, k_s, k_e, t0);
+            }
+            int tile, gb, ge;
+            for (int i = 0; i < 2 && unit_of(i, tile, gb, ge); ++i) {
+                // contributors ra..rb: the ranks whose runs meet this tile;
+                // src[k]: contributor k's partial of it, as a cluster address
+                // (this CTA's own partial is read from its shared memory)
+                int ra = -1, rb = -1;
+                uint32_t src[8];
+                const int lo = (tile - cl_t0) * G, hi = lo + G;
+                for (int k = 0; k < C; ++k) {
+                    const int s = __shfl_sync(0xffffffffu, k_s, k), e = __shfl_sync(0xffffffffu, k_e, k);
+                    if (s < hi && e > lo) {
+                        if (ra < 0) ra = k;
+                        rb = k;
+                        const int sl = tile - cl_t0 - s / G;  // its unit index of this tile
+                        src[k] = map_to_rank(smem_u32(part) + (uint32_t)(sl * BM * 128 * 4),
+                                             (uint32_t)k);
+                    }
+                }
+                // this CTA's share: 16-byte chunks [c0, c1) of the tile's
+                // [BM][128] floats, up to four a thread in flight per step
+                const int nc = rb - ra + 1, me = r - ra;
+                constexpr int E4 = BM * 32;
+                const int c0 = me * E4 / nc, c1 = (me + 1) * E4 / nc;
+                const int n0 = (tile / p.m_tiles) * 128, m0 = (tile % p.m_tiles) * BM;
+                const float4 *own = reinterpret_cast<const float4 *>(part) + i * E4;
+                for (int c = c0 + (int)threadIdx.x; c < c1; c += 4 * kThreadsTc) {
+                    const int nj = min(4, (c1 - 1 - c) / kThreadsTc + 1);  // valid chunks
+                    float4 acc[4];
+                    for (int k = ra; k <= rb; ++k) {
+                        float4 w[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int cj = c + j * kThreadsTc;
+                            if (j < nj)
+                                w[j] = k == r ? own[cj] : ld_dsmem_v4(src[k] + 16u * (uint32_t)cj);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            if (j >= nj) continue;
+                            if (k == ra) {
+                                acc[j] = w[j];
+                            } else {
+                                acc[j].x += w[j].x;
+                                acc[j].y += w[j].y;
+                                acc[j].z += w[j].z;
+                                acc[j].w += w[j].w;
+                            }
+                        }
+                    }
+                    if (*flag) continue;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int cj = c + j * kThreadsTc;
+                        const int m = m0 + cj / 32, n = n0 + 4 * (cj & 31);
+                        if (j >= nj || m >= p.M) continue;
+                        T *yr = y + (size_t)m * p.N;
+                        if (n < p.N) yr[n] = cvt_out<T>(acc[j].x);
+                        if (n + 1 < p.N) yr[n + 1] = cvt_out<T>(acc[j].y);
+                        if (n + 2 < p.N) yr[n + 2] = cvt_out<T>(acc[j].z);
+                        if (n + 3 < p.N) yr[n + 3] = cvt_out<T>(acc[j].w);
+                    }
+                }
+            }
+            cluster_sync();
+        }
+    }
     if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, p.tmem_cols);
@@ -1370,6 +1527,41 @@ struct TcPlan {
     int grid;
 };
 
+// Co-resident clusters of 1..8 CTAs when each CTA has an SM to itself (every
+// tc plan does: its shared memory is over half an SM's), queried once.
+const int *tc_active_clusters() {
+    static int n[9];
+    static std::once_flag once;
+    std::call_once(once, [] {
+        auto kern = tc_kernel<4, true, 64, false>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimitTc);
+        for (int c = 1; c <= 8; ++c) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)c, 1, 1);
+            cfg.blockDim = dim3(kThreadsTc, 1, 1);
+            cfg.dynamicSmemBytes = kSmemLimitTc;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = (unsigned)c;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int k = 0;
+            if (cudaOccupancyMaxActiveClusters(&k, kern, &cfg) != cudaSuccess) k = 0;
+            n[c] = k;
+        }
+        cudaGetLastError();
+    });
+    return n;
+}
+
+// The clustered K split's fixed cost (partials through shared memory, two
+// cluster barriers, the sums), in stages of one group: measured on GB300 at
+// about 2-3.6 us when a cluster shares one tile and 7-9 us when it shares
+// several (two partial tiles a CTA), against ~0.37 us a stage.
+constexpr int cluster_split_stages(int tiles) { return tiles == 1 ? 8 : 20; }
+
 // group: 0 for the 3/4-bit group-64 format, else the group size of the
 // general-width path (32, 64 or 128; x tiles of at most 128 rows).
 bool tc_plan(const MatmulArgs &a, TcPlan &pl, int group = 0) {
@@ -1456,6 +1648,51 @@ bool tc_plan(const MatmulArgs &a, TcPlan &pl, int group = 0) {
             }
         }
     }
+    // Fewer tiles than SMs, x tiles of at most 128 rows (two accumulators,
+    // room for two partial tiles in the idle rings): a clustered K split
+    // when its longest run of stages, plus its fixed cost, is shorter than
+    // the plan above.  The clusters must all be resident at once.
+    q.cl_ctas = q.cl_tiles = 0;
+    const bool cl_room = pl.BM <= 128 && q.off_bar >= (uint32_t)(2 * pl.BM * 128 * 4);
+    auto cl_valid = [&](int C, int T) {
+        const int clusters = (total + T - 1) / T;
+        const int last = total - (clusters - 1) * T;
+        // all clusters resident at once; every CTA gets a run
+        return clusters <= tc_active_clusters()[C] && last * (q.G / 4) >= C;
+    };
+    if (cl_room && total < num_sms()) {
+        const int G = q.G;
+        int best = q.rounds * G + (q.tail > 0 ? G / 2 : 0);
+        for (int C = 2; C <= 8; ++C) {
+            for (int T = 1; T < C; ++T) {
+                if (!cl_valid(C, T)) continue;
+                const int cost = 4 * ((T * (G / 4) + C - 1) / C) + cluster_split_stages(T);
+                if (cost < best) {
+                    best = cost;
+                    q.cl_ctas = C;
+                    q.cl_tiles = T;
+                }
+            }
+        }
+    }
+#ifdef AQ_TEST_HOOKS
+    if (g_test_cluster_split < 0) {
+        q.cl_ctas = q.cl_tiles = 0;
+    } else if (g_test_cluster_split > 0) {
+        const int C = g_test_cluster_split >> 8, T = g_test_cluster_split & 255;
+        if (cl_room && C >= 2 && C <= 8 && T >= 1 && T < C && cl_valid(C, T)) {
+            q.cl_ctas = C;
+            q.cl_tiles = T;
+        }
+    }
+#endif
+    {
+        if (q.cl_ctas > 0) {
+            q.rounds = 0;
+            q.tail = 0;
+            grid = (total + q.cl_tiles - 1) / q.cl_tiles * q.cl_ctas;
+        }
+    }
     pl.grid = grid;
     return true;
 }
@@ -1479,7 +1716,8 @@ cudaError_t tc_launch_t(const TcPlan &pl, const CUtensorMap &tm, cudaStream_t st
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = pl.prm.tail > 0 ? 2u : 1u;
+    attr[1].val.clusterDim.x = pl.prm.cl_ctas > 0 ? (unsigned)pl.prm.cl_ctas
+                                                   : pl.prm.tail > 0 ? 2u : 1u;
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -1670,11 +1908,16 @@ int tc_describe(const MatmulArgs &a, char *buf, int len) {
     if (!tc_plan(a, pl)) return snprintf(buf, len, "tc: unsupported");
     return snprintf(buf, len,
                     "tc bm=%d a_slots=%d b_slots=%d raw_slots=%d tiles=%dx%d grid=%d rounds=%d "
-                    "split=%d smem=%zu tmem=%u",
+                    "split=%d cluster_split=%dx%d smem=%zu tmem=%u",
                     pl.BM, a_slots_for(pl.BM), b_slots_for(pl.BM), raw_slots_for(pl.BM),
                     pl.prm.n_tiles, pl.prm.m_tiles, pl.grid,
-                    pl.prm.rounds, pl.prm.tail, pl.smem, pl.prm.tmem_cols);
+                    pl.prm.rounds, pl.prm.tail, pl.prm.cl_ctas, pl.prm.cl_tiles, pl.smem,
+                    pl.prm.tmem_cols);
 }
+
+#ifdef AQ_TEST_HOOKS
+const int *tc_active_clusters_for_tests() { return tc_active_clusters(); }
+#endif
 
 cudaError_t tc_read_error(uint32_t *code, bool clear) {
     cudaError_t e = cudaMemcpyFromSymbol(code, g_tc_error, sizeof(uint32_t));

@@ -160,8 +160,8 @@ def test_boundary_signatures(name, ret, types):
     (16, 10240, 5120, 3, aq.AQ_VARIANT_GEMV),
     (17, 10240, 5120, 3, aq.AQ_VARIANT_GEMV),
     (32, 10240, 5120, 3, aq.AQ_VARIANT_GEMV),
-    (33, 10240, 5120, 3, aq.AQ_VARIANT_TCW),    # 80 tc tiles < 0.6 x 152
-    (64, 5120, 13824, 4, aq.AQ_VARIANT_TCW),
+    (33, 10240, 5120, 3, aq.AQ_VARIANT_TC),     # 80 tiles: the clustered K split
+    (64, 5120, 13824, 4, aq.AQ_VARIANT_TC),
     (128, 13824, 5120, 4, aq.AQ_VARIANT_TC),    # 108 tc tiles
     (129, 4096, 4096, 4, aq.AQ_VARIANT_TC),
     (1, 5120, 13824, 4, aq.AQ_VARIANT_GEMV),
@@ -172,7 +172,7 @@ def test_boundary_signatures(name, ret, types):
     (1, 128256, 4096, 4, aq.AQ_VARIANT_QMV),
     (8, 13824, 5120, 4, aq.AQ_VARIANT_GEMV),
     (2, 28672, 8192, 4, aq.AQ_VARIANT_GEMV),   # two passes of 95 rows per CTA
-    (64, 10240, 5120, 3, aq.AQ_VARIANT_TCW),
+    (64, 10240, 5120, 3, aq.AQ_VARIANT_TC),
     (128, 28672, 8192, 4, aq.AQ_VARIANT_TC),
     (512, 28672, 8192, 4, aq.AQ_VARIANT_TC),
     (1, 100, 576, 4, aq.AQ_VARIANT_GENERIC),   # K % 512 != 0 -> generic
