@@ -1125,8 +1125,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 int t0;
                 cl_range(p, G, total, cbase + lane, k_s, k_e, t0);
             }
-            int tile, gb, ge;
-            for (int i = 0; i < 2 && unit_of(i, tile, gb, ge); ++i) {
+            // The sums are held in registers (rounded and packed, four
+            // outputs a 16-byte chunk) until every partial has been read:
+            // then the last cluster barrier orders only those reads, and the
+            // y stores follow it.
+            constexpr int E4 = BM * 32;                            // chunks a tile
+            constexpr int kJ = (E4 + kThreadsTc - 1) / kThreadsTc;  // a thread's, at most
+            uint2 outv[2][kJ];
+            int u_c0[2] = {0, 0}, u_c1[2] = {0, 0}, u_m0[2] = {0, 0}, u_n0[2] = {0, 0};
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                int tile, gb, ge;
+                if (!unit_of(i, tile, gb, ge)) break;
                 // contributors ra..rb: the ranks whose runs meet this tile;
                 // src[k]: contributor k's partial of it, as a cluster address
                 // (this CTA's own partial is read from its shared memory)
@@ -1144,26 +1154,31 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     }
                 }
                 // this CTA's share: 16-byte chunks [c0, c1) of the tile's
-                // [BM][128] floats, up to four a thread in flight per step
+                // [BM][128] floats; chunk c0 + threadIdx.x + jj * threads is
+                // this thread's jj-th, up to four in flight per step
                 const int nc = rb - ra + 1, me = r - ra;
-                constexpr int E4 = BM * 32;
                 const int c0 = me * E4 / nc, c1 = (me + 1) * E4 / nc;
-                const int n0 = (tile / p.m_tiles) * 128, m0 = (tile % p.m_tiles) * BM;
+                u_c0[i] = c0;
+                u_c1[i] = c1;
+                u_n0[i] = (tile / p.m_tiles) * 128;
+                u_m0[i] = (tile % p.m_tiles) * BM;
                 const float4 *own = reinterpret_cast<const float4 *>(part) + i * E4;
-                for (int c = c0 + (int)threadIdx.x; c < c1; c += 4 * kThreadsTc) {
-                    const int nj = min(4, (c1 - 1 - c) / kThreadsTc + 1);  // valid chunks
+#pragma unroll
+                for (int jb = 0; jb < kJ; jb += 4) {
+                    const int cb = c0 + (int)threadIdx.x + jb * kThreadsTc;
+                    if (cb >= c1) break;
                     float4 acc[4];
                     for (int k = ra; k <= rb; ++k) {
                         float4 w[4];
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            const int cj = c + j * kThreadsTc;
-                            if (j < nj)
+                            const int cj = cb + j * kThreadsTc;
+                            if (jb + j < kJ && cj < c1)
                                 w[j] = k == r ? own[cj] : ld_dsmem_v4(src[k] + 16u * (uint32_t)cj);
                         }
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            if (j >= nj) continue;
+                            if (jb + j >= kJ || cb + j * kThreadsTc >= c1) continue;
                             if (k == ra) {
                                 acc[j] = w[j];
                             } else {
@@ -1174,21 +1189,37 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                             }
                         }
                     }
-                    if (*flag) continue;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const int cj = c + j * kThreadsTc;
-                        const int m = m0 + cj / 32, n = n0 + 4 * (cj & 31);
-                        if (j >= nj || m >= p.M) continue;
-                        T *yr = y + (size_t)m * p.N;
-                        if (n < p.N) yr[n] = cvt_out<T>(acc[j].x);
-                        if (n + 1 < p.N) yr[n + 1] = cvt_out<T>(acc[j].y);
-                        if (n + 2 < p.N) yr[n + 2] = cvt_out<T>(acc[j].z);
-                        if (n + 3 < p.N) yr[n + 3] = cvt_out<T>(acc[j].w);
+                        if (jb + j < kJ)
+                            outv[i][jb + j] = make_uint2(pack_out<BF16>(make_float2(acc[j].x, acc[j].y)),
+                                                         pack_out<BF16>(make_float2(acc[j].z, acc[j].w)));
                     }
                 }
             }
             cluster_sync();
+            if (!*flag) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+#pragma unroll
+                    for (int jj = 0; jj < kJ; ++jj) {
+                        const int c = u_c0[i] + (int)threadIdx.x + jj * kThreadsTc;
+                        if (c >= u_c1[i]) continue;
+                        const int m = u_m0[i] + c / 32, n = u_n0[i] + 4 * (c & 31);
+                        if (m >= p.M || n >= p.N) continue;
+                        T *yr = y + (size_t)m * p.N + n;
+                        const uint2 v = outv[i][jj];
+                        if (n + 3 < p.N && (reinterpret_cast<uintptr_t>(yr) & 7u) == 0) {
+                            *reinterpret_cast<uint2 *>(yr) = v;
+                        } else {
+                            const uint16_t h[4] = {(uint16_t)(v.x & 0xFFFFu), (uint16_t)(v.x >> 16),
+                                                   (uint16_t)(v.y & 0xFFFFu), (uint16_t)(v.y >> 16)};
+                            uint16_t *yh = reinterpret_cast<uint16_t *>(yr);
+                            for (int e = 0; e < 4 && n + e < p.N; ++e) yh[e] = h[e];
+                        }
+                    }
+                }
+            }
         }
     }
     if (warp == kWarpMma) {
