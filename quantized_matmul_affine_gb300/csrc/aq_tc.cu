@@ -365,9 +365,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // cycles at the full rate) does not hide; measured on GB300, a round of
     // 8 MMAs with two waits and two commits takes 889 cycles against 706
     // for 4 MMAs with the same.
-    constexpr int kSP = (BM <= 128 || TA) ? 2 : 1;
+    // 64-row x tiles with A in tensor memory take four stages per step (one
+    // dequantising warp's super-stage): 16 MMAs between two waits and two
+    // commits, which the probe above puts at ~64 cycles an MMA (GB300, M =
+    // 64: 10240x5120 3-bit 25.0 -> 24.2 us, 5120x13824 30.6 -> 29.0).  At
+    // 128 rows the eight 16 KB x slots this needs leave two raw slots a warp,
+    // which cost the 4-bit weight stream more than the steps gain.
+    constexpr int kSP = (BM == 64 && TA) ? 4 : (BM <= 128 || TA) ? 2 : 1;
     constexpr int kBG = kB / kSP;  // x barriers (groups of kSP slots)
-    static_assert(kSP == 1 || (kH == 1 && kB % kSP == 0 && kA % 2 == 0), "stage pairs");
+    static_assert(kSP == 1 || (kH == 1 && kB % kSP == 0 && kA % kSP == 0 && kBG >= 2),
+                  "stage groups");
     extern __shared__ uint8_t smem_dyn[];
     // Align to 1024 bytes by an offset from the __shared__ array itself, so
     // that every access below stays a shared-memory access (32-bit address).
@@ -465,9 +472,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             int tile, gb, ge;
             for (int u = 0; unit_of(u, tile, gb, ge); ++u) {
                 const int m0 = (tile % p.m_tiles) * BM;
-                if constexpr (kSP == 2) {
-                    // the two stages' sub-tiles on one barrier
-                    for (int g = gb; g < ge; g += 2, ++bi) {
+                if constexpr (kSP >= 2) {
+                    // the group's kSP stages' sub-tiles on one barrier
+                    for (int g = gb; g < ge; g += kSP, ++bi) {
                         const int slot = bi % kBG;
                         const uint32_t ph = (bi / kBG) & 1u;
                         if (bi >= kBG && !tc_wait(&b_empty[slot], ph ^ 1u, flag, 0x0102))
@@ -475,11 +482,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #ifdef AQ_TEST_HOOKS
                         if (p.withhold && bi == 0) continue;  // nothing will complete b_full[0]
 #endif
-                        mbar_arrive_expect_tx(&b_full[slot], 2 * kBTile);
+                        mbar_arrive_expect_tx(&b_full[slot], kSP * kBTile);
 #pragma unroll
-                        for (int e = 0; e < 2; ++e)
-                            tma_load_2d(b_ring + (2 * slot + e) * kBTile, &tmap_x, 64 * (g + e), m0,
-                                        &b_full[slot]);
+                        for (int e = 0; e < kSP; ++e)
+                            tma_load_2d(b_ring + (kSP * slot + e) * kBTile, &tmap_x, 64 * (g + e),
+                                        m0, &b_full[slot]);
                     }
                     continue;
                 }
@@ -532,9 +539,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             if (!__all_sync(0xffffffffu, free)) break;
             tc_fence_after();
             const uint32_t d = tmem + b * BM;
-            if constexpr (kSP == 2) {
-                for (int g = gb; ok && g < ge; g += 2, ai += 2, ++bi) {
-                    const uint32_t al = ai + 1;  // the pair's second A stage
+            if constexpr (kSP >= 2) {
+                for (int g = gb; ok && g < ge; g += kSP, ai += kSP, ++bi) {
+                    const uint32_t al = ai + kSP - 1;  // the group's last A stage
                     const bool got_a = tc_wait(&a_full[al % kA], (al / kA) & 1u, flag, 0x0302);
                     if (!__all_sync(0xffffffffu, got_a)) {
                         ok = false;
@@ -550,9 +557,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     issued = true;
                     if (lane == 0) {
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
+                        for (int e = 0; e < kSP; ++e) {
                             const uint64_t bd =
-                                b_desc0 + (uint64_t)((uint32_t)((2 * bs + e) * kBTile) >> 4);
+                                b_desc0 + (uint64_t)((uint32_t)((kSP * bs + e) * kBTile) >> 4);
                             if constexpr (TA) {
                                 // A stage: 32 columns after the accumulators, 8 a k-step
                                 const uint32_t at =
@@ -571,7 +578,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                             }
                         }
                         tc_commit(&b_empty[bs]);
-                        tc_commit(&a_empty[al % kA]);  // frees both A slots
+                        tc_commit(&a_empty[al % kA]);  // frees the group's A slots
                     }
                     __syncwarp();
                 }
@@ -660,10 +667,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         // two warps of a quarter take alternate 4-group super-stages.  Each
         // stage (one group) is 64 values of the thread's row: eight words of
         // codes, dequantised and written as 32 columns of the A stage.  The
-        // MMA warp takes stages in pairs: the pair's slots are waited for
-        // once and its second stage's arrival stands for both.
+        // MMA warp takes stages in groups of kSP (2, or 4: a whole
+        // super-stage): the group's slots are waited for once and its last
+        // stage's arrival stands for all.
         // ------------------------------------------------------------------
-        static_assert(kSP == 2 && kA % 2 == 0, "tensor-memory A is consumed in stage pairs");
+        static_assert((kSP == 2 || kSP == 4) && kA % kSP == 0 && kGroups % kSP == 0,
+                      "tensor-memory A is consumed in groups of stages");
         using RT = RawT<B>;
         const int dw = warp - kWarpDq;
         const int q = warp & 3;
@@ -745,8 +754,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             for (int j = 0; j < kGroups; ++j) {
                 const uint32_t it = 4u * (uint32_t)cc.gs + (uint32_t)j;  // the MMA's stage count
                 const int slot = (int)(it % kA);
-                if ((j & 1) == 0) {  // the pair's slots: freed by one commit
-                    const uint32_t il = it + 1;
+                if (j % kSP == 0) {  // the group's slots: freed by one commit
+                    const uint32_t il = it + kSP - 1;
                     if (il >= (uint32_t)kA &&
                         !tc_wait(&a_empty[il % kA], ((il / kA) & 1u) ^ 1u, flag, 0x0602)) {
                         ok = false;
@@ -782,7 +791,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     out[4 * c + 3] = v.w;
                 }
                 tmem_st32(trow + (uint32_t)(slot * 32), out);
-                if (j & 1) {  // the pair is complete
+                if (j % kSP == kSP - 1) {  // the group is complete
                     tmem_wait_st();
                     tc_fence_before();
                     __syncwarp();
