@@ -1142,36 +1142,43 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             constexpr int kJ = (E4 + kThreadsTc - 1) / kThreadsTc;  // a thread's, at most
             uint2 outv[2][kJ];
             int u_c0[2] = {0, 0}, u_c1[2] = {0, 0}, u_m0[2] = {0, 0}, u_n0[2] = {0, 0};
+            // This CTA's share of the sums: an even run [q0, q1) of the
+            // cluster's 16-byte output chunks, tile after tile (E4 a tile,
+            // [BM][128] floats); with fewer tiles than CTAs a run meets at
+            // most two tiles.
+            const int te = min(p.cl_tiles, total - cl_t0) * E4;
+            const int q0 = r * te / C, q1 = (r + 1) * te / C;
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
-                int tile, gb, ge;
-                if (!unit_of(i, tile, gb, ge)) break;
+                const int qs = i == 0 ? q0 : (q0 / E4 + 1) * E4;  // segment i's start
+                if (qs >= q1) break;
+                const int tt = qs / E4, tile = cl_t0 + tt;
                 // contributors ra..rb: the ranks whose runs meet this tile;
                 // src[k]: contributor k's partial of it, as a cluster address
-                // (this CTA's own partial is read from its shared memory)
-                int ra = -1, rb = -1;
+                // (this CTA's own partial, if it has one, from its shared
+                // memory)
+                int ra = -1, rb = -1, own_sl = 0;
                 uint32_t src[8];
-                const int lo = (tile - cl_t0) * G, hi = lo + G;
+                const int lo = tt * G, hi = lo + G;
                 for (int k = 0; k < C; ++k) {
                     const int s = __shfl_sync(0xffffffffu, k_s, k), e = __shfl_sync(0xffffffffu, k_e, k);
                     if (s < hi && e > lo) {
                         if (ra < 0) ra = k;
                         rb = k;
-                        const int sl = tile - cl_t0 - s / G;  // its unit index of this tile
+                        const int sl = tt - s / G;  // its unit index of this tile
+                        if (k == r) own_sl = sl;
                         src[k] = map_to_rank(smem_u32(part) + (uint32_t)(sl * BM * 128 * 4),
                                              (uint32_t)k);
                     }
                 }
-                // this CTA's share: 16-byte chunks [c0, c1) of the tile's
-                // [BM][128] floats; chunk c0 + threadIdx.x + jj * threads is
-                // this thread's jj-th, up to four in flight per step
-                const int nc = rb - ra + 1, me = r - ra;
-                const int c0 = me * E4 / nc, c1 = (me + 1) * E4 / nc;
+                // chunks [c0, c1) of this tile; chunk c0 + threadIdx.x + jj *
+                // threads is this thread's jj-th, up to four in flight a step
+                const int c0 = qs - tt * E4, c1 = min(E4, q1 - tt * E4);
                 u_c0[i] = c0;
                 u_c1[i] = c1;
                 u_n0[i] = (tile / p.m_tiles) * 128;
                 u_m0[i] = (tile % p.m_tiles) * BM;
-                const float4 *own = reinterpret_cast<const float4 *>(part) + i * E4;
+                const float4 *own = reinterpret_cast<const float4 *>(part) + own_sl * E4;
 #pragma unroll
                 for (int jb = 0; jb < kJ; jb += 4) {
                     const int cb = c0 + (int)threadIdx.x + jb * kThreadsTc;
