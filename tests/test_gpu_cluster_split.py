@@ -176,6 +176,10 @@ def test_planner_choice_at_the_pages_shape(M):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     N, K, bits = 10240, 5120, 3
+    # 80 weight tiles on more SMs: the dispatch takes tc, whose planner
+    # shares the tiles' K ranges over clusters
+    plan = aq.aq_describe(M, N, K, bits, aq.AQ_F16)
+    assert plan.startswith("tc ") and "cluster_split=0x0" not in plan, plan
     p = workloads.make_problem("cs", bits, N, K, M, "fp16", seed=M + 5)
     codes, s, b, x = dev_tensors(p)
     Wq = aq.aq_pack(codes, bits)

@@ -47,6 +47,8 @@ def lib():
     L.aq_device_error.restype = i32
     L.aq_test_withhold.argtypes = [i32]
     L.aq_test_withhold.restype = None
+    L.aq_test_cluster_split.argtypes = [i32, i32]
+    L.aq_test_cluster_split.restype = None
     code = ctypes.c_uint32(0)
     assert L.aq_device_error(ctypes.addressof(code), 1) == 0
     yield L
@@ -95,3 +97,30 @@ def test_wait_runs_out_then_next_call_is_correct(lib, withhold, variant, shape, 
     assert_within_tolerance(y, y_ref, bound, f"after a withheld stage ({hex(code)})")
     assert _device_error(lib, clear=False) == 0
 
+
+@pytest.mark.parametrize("ctas,tiles", [(4, 3), (8, 1)])
+def test_wait_runs_out_under_the_clustered_split(lib, ctas, tiles):
+    # the same with the tensor-core kernel's K range shared over the CTAs of
+    # a cluster: every CTA still meets both cluster barriers after its wait
+    # gives up, stores nothing, and the next call (same plan) is correct
+    M, N, K = 64, 1000, 2048  # 8 tiles of 32 stages
+    p = workloads.make_problem("w", 4, N, K, M, "bf16", seed=M + N + ctas)
+    codes, s, b, x = dev_tensors(p)
+    Wq = aq.aq_pack(codes, 4)
+    torch.cuda.synchronize()
+    lib.aq_test_cluster_split(ctas, tiles)
+    try:
+        try:
+            lib.aq_test_withhold(2)
+            _call(lib, aq.AQ_VARIANT_TC, p, x, Wq, s, b)
+        finally:
+            lib.aq_test_withhold(0)
+        code = _device_error(lib, clear=True)
+        assert code != 0, "the withheld stage did not make a wait give up"
+        assert code & 0xFF == ERR_FAMILY_TC, hex(code)
+        y = y_to_f64(_call(lib, aq.AQ_VARIANT_TC, p, x, Wq, s, b), "bf16")
+    finally:
+        lib.aq_test_cluster_split(0, 0)
+    y_ref, bound = reference(p)
+    assert_within_tolerance(y, y_ref, bound, f"after a withheld stage ({hex(code)})")
+    assert _device_error(lib, clear=False) == 0
