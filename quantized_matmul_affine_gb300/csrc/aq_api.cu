@@ -112,10 +112,10 @@ static bool gemv_for_m1(const MatmulArgs &a) { return a.N <= 128ll * num_sms(); 
 // fewer weight tiles than SMs it shares tiles among the CTAs of a cluster
 // (the clustered K split), which left the swapped-role kernel (still
 // available as AQ_VARIANT_TCW) behind on every shape measured (GB300, us:
-// 10240x5120 3-bit at M = 33/64/128: 24.1/24.2/27.8 against 27.8/29.7/33.7;
-// 4096x4096 at 64/128: 12.7/14.5 against 24.0/28.7; 5120x13824 at 64: 29.0
-// against 64.0; 5120x5120 at 128: 17.8 against 39.4; 1024x5120 at 64: 11.1
-// against 15.2; 13824x5120 at 128: 30.4 against 43.0).
+// 10240x5120 3-bit at M = 33/64/128: 23.1/23.2/26.6 against 27.8/29.7/33.7;
+// 4096x4096 at 64/128: 12.0/14.0 against 24.2/29.0; 5120x13824 at 64: 28.3
+// against 64.0; 5120x5120 at 128: 17.3 against 39.4; 1024x5120 at 64: 9.8
+// against 15.1; 13824x5120 at 128: 30.5 against 43.2).
 
 // The dispatch rule.  Returns the variant for the arguments (alignment
 // included), never AQ_VARIANT_AUTO.

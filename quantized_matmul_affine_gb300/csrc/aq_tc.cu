@@ -349,6 +349,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     constexpr int kA = TA ? kATmemSlots : a_slots_for(BM, GEN);
     constexpr int kB = b_slots_for(BM, GEN);
     constexpr int kRawSlots = TA ? raw_slots_ta(BM) : GEN ? raw_slots_g(B) : raw_slots_for(BM);
+    constexpr int kRawSlotBytes = [] {
+        if constexpr (TA) return RawT<B>::kSlotBytes;
+        else return R::kSlotBytes;
+    }();
     // A 512-row x tile is two N = 256 MMAs per k-step into one 512-column
     // accumulator (each weight tile dequantised once for 512 x rows); the
     // narrower tiles double-buffer their accumulator.
@@ -392,6 +396,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     uint64_t *drain = acc_empty + 2;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    // Clustered K split: the CTA's two sum segments, worked out by an
+    // epilogue warp while the main loop runs (16 ints each: tile, chunk
+    // range, contributor ranks, this CTA's unit of the tile, and each
+    // contributor's partial as a cluster address).
+    int *cl_tab = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(bars) +
+                                          (2 * kA + 2 * kB + 5) * 8 + 16);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int total = p.n_tiles * p.m_tiles;
@@ -428,6 +438,55 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             return true;
         }
         return false;
+    };
+
+    // The clustered K split's sum segments (one warp, converged): this CTA
+    // sums an even run [q0, q1) of its cluster's 16-byte output chunks,
+    // tile after tile (BM * 32 a tile, [BM][128] floats); with fewer tiles
+    // than CTAs a run meets at most two tiles.  For each: the tile, the
+    // chunk range, the contributors ra..rb (the ranks whose runs meet the
+    // tile, in K order), this CTA's unit index of it (if a contributor) and
+    // each contributor's partial as a cluster address.
+    auto cl_fill_table = [&]() {
+        const int C = p.cl_ctas, r = (int)blockIdx.x % C, cbase = (int)blockIdx.x - r;
+        constexpr int E4 = BM * 32;
+        int k_s = 0, k_e = 0;  // lane k < C: the run of rank k
+        if (lane < C) {
+            int t0;
+            cl_range(p, G, total, cbase + lane, k_s, k_e, t0);
+        }
+        const int te = min(p.cl_tiles, total - cl_t0) * E4;
+        const int q0 = r * te / C, q1 = (r + 1) * te / C;
+        for (int i = 0; i < 2; ++i) {
+            int *t = cl_tab + 16 * i;
+            const int qs = i == 0 ? q0 : (q0 / E4 + 1) * E4;  // segment i's start
+            const int tt = qs / E4;
+            const int lo = tt * G, hi = lo + G;
+            int ra = -1, rb = -1, own_sl = 0;
+            uint32_t src_l = 0;  // lane k: contributor k's partial
+            for (int k = 0; k < C; ++k) {
+                const int sk = __shfl_sync(0xffffffffu, k_s, k), ek = __shfl_sync(0xffffffffu, k_e, k);
+                if (sk < hi && ek > lo) {
+                    if (ra < 0) ra = k;
+                    rb = k;
+                    const int sl = tt - sk / G;  // its unit index of this tile
+                    if (k == r) own_sl = sl;
+                    const uint32_t a = map_to_rank(smem_u32(smem) + (uint32_t)(sl * BM * 128 * 4),
+                                                   (uint32_t)k);
+                    if (lane == k) src_l = a;
+                }
+            }
+            if (lane < 8) t[8 + lane] = (int)src_l;
+            if (lane == 0) {
+                t[0] = qs < q1;
+                t[1] = cl_t0 + tt;
+                t[2] = qs - tt * E4;
+                t[3] = min(E4, q1 - tt * E4);
+                t[4] = ra;
+                t[5] = rb;
+                t[6] = own_sl;
+            }
+        }
     };
 
     if (threadIdx.x == 0) {
@@ -634,6 +693,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         // ------------------------------------------------------------------
         const int q = warp & 3;
         T *y = static_cast<T *>(p.y);
+        if constexpr (BM <= 128) {
+            if (p.cl_ctas > 0 && warp == kWarpMma + 1) cl_fill_table();
+        }
         grid_dependency_wait();
         uint32_t ti = 0;
         int tile, gb, ge;
@@ -1026,8 +1088,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         constexpr int kXP = kCh + 4;              // floats per row of the buffer
         // the idle rings: A tiles (in shared memory unless TA), x tiles, raw codes
         static_assert(128 * kXP * 4 <= (TA ? 0 : kA * kATileBytes) + kB * kBTile +
-                                           kDqWarps * kRawSlots *
-                                               (TA ? RawT<B>::kSlotBytes : R::kSlotBytes),
+                                           kDqWarps * kRawSlots * kRawSlotBytes,
                       "hand-over buffer");
         const int r = (int)blockIdx.x & 1;
         const int tile = p.rounds * (int)gridDim.x + ((int)blockIdx.x >> 1);
@@ -1082,22 +1143,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
     if constexpr (BM <= 128) {
         if (p.cl_ctas > 0) {
-            // Clustered K split.  (1) The epilogue warps copy each of the
-            // CTA's one or two partial accumulators into the idle ring as
-            // [BM][128] floats (unit i at i * BM * 128).  (2) After a cluster
-            // barrier, the contributors of each tile (consecutive ranks) share
-            // its outputs evenly; each output is the sum of the contributors'
-            // partials in rank order, read through distributed shared memory,
-            // then stored to y.  (3) A last cluster barrier keeps every
-            // partial readable until all sums are done.  Every CTA takes both
+            // Clustered K split.  (1) Warps 2..13 copy each of the CTA's one
+            // or two partial accumulators into the idle ring as [BM][128]
+            // floats (unit i at i * BM * 128).  (2) After a cluster barrier,
+            // each CTA sums its segments of the cluster's outputs (the table
+            // filled during the main loop): each output is the sum of its
+            // tile's partials in rank order, read through distributed shared
+            // memory.  (3) A last cluster barrier keeps every partial readable
+            // until all sums are done; then y is stored.  Every CTA takes both
             // barriers, error or not.
             static_assert(2 * BM * 128 * 4 <= (TA ? 0 : kA * kATileBytes) + kB * kBTile +
-                                                  kDqWarps * kRawSlots *
-                                                      (TA ? RawT<B>::kSlotBytes : R::kSlotBytes),
+                                                  kDqWarps * kRawSlots * kRawSlotBytes,
                           "partial tiles");
-            const int C = p.cl_ctas;
-            const int r = (int)blockIdx.x % C;
-            const int cbase = (int)blockIdx.x - r;  // the cluster's first CTA
+            const int r = (int)blockIdx.x % p.cl_ctas;
             float *part = reinterpret_cast<float *>(smem);
             tc_fence_after();
             if (warp > kWarpMma) {
@@ -1128,12 +1186,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             cluster_sync();
             grid_dependency_wait();  // every thread below stores y
             T *y = static_cast<T *>(p.y);
-            // lane k < C: the run of the cluster's rank k
-            int k_s = 0, k_e = 0;
-            if (lane < C) {
-                int t0;
-                cl_range(p, G, total, cbase + lane, k_s, k_e, t0);
-            }
             // The sums are held in registers (rounded and packed, four
             // outputs a 16-byte chunk) until every partial has been read:
             // then the last cluster barrier orders only those reads, and the
@@ -1142,38 +1194,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             constexpr int kJ = (E4 + kThreadsTc - 1) / kThreadsTc;  // a thread's, at most
             uint2 outv[2][kJ];
             int u_c0[2] = {0, 0}, u_c1[2] = {0, 0}, u_m0[2] = {0, 0}, u_n0[2] = {0, 0};
-            // This CTA's share of the sums: an even run [q0, q1) of the
-            // cluster's 16-byte output chunks, tile after tile (E4 a tile,
-            // [BM][128] floats); with fewer tiles than CTAs a run meets at
-            // most two tiles.
-            const int te = min(p.cl_tiles, total - cl_t0) * E4;
-            const int q0 = r * te / C, q1 = (r + 1) * te / C;
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
-                const int qs = i == 0 ? q0 : (q0 / E4 + 1) * E4;  // segment i's start
-                if (qs >= q1) break;
-                const int tt = qs / E4, tile = cl_t0 + tt;
-                // contributors ra..rb: the ranks whose runs meet this tile;
-                // src[k]: contributor k's partial of it, as a cluster address
-                // (this CTA's own partial, if it has one, from its shared
-                // memory)
-                int ra = -1, rb = -1, own_sl = 0;
-                uint32_t src[8];
-                const int lo = tt * G, hi = lo + G;
-                for (int k = 0; k < C; ++k) {
-                    const int s = __shfl_sync(0xffffffffu, k_s, k), e = __shfl_sync(0xffffffffu, k_e, k);
-                    if (s < hi && e > lo) {
-                        if (ra < 0) ra = k;
-                        rb = k;
-                        const int sl = tt - s / G;  // its unit index of this tile
-                        if (k == r) own_sl = sl;
-                        src[k] = map_to_rank(smem_u32(part) + (uint32_t)(sl * BM * 128 * 4),
-                                             (uint32_t)k);
-                    }
-                }
-                // chunks [c0, c1) of this tile; chunk c0 + threadIdx.x + jj *
-                // threads is this thread's jj-th, up to four in flight a step
-                const int c0 = qs - tt * E4, c1 = min(E4, q1 - tt * E4);
+                // segment i of the table filled during the main loop
+                const int *t = cl_tab + 16 * i;
+                if (!t[0]) break;
+                const int tile = t[1], c0 = t[2], c1 = t[3], ra = t[4], rb = t[5];
+                const int own_sl = t[6];
+                const int *src = t + 8;  // contributor k's partial, a cluster address
                 u_c0[i] = c0;
                 u_c1[i] = c1;
                 u_n0[i] = (tile / p.m_tiles) * 128;
@@ -1190,7 +1218,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                         for (int j = 0; j < 4; ++j) {
                             const int cj = cb + j * kThreadsTc;
                             if (jb + j < kJ && cj < c1)
-                                w[j] = k == r ? own[cj] : ld_dsmem_v4(src[k] + 16u * (uint32_t)cj);
+                                w[j] = k == r ? own[cj]
+                                              : ld_dsmem_v4((uint32_t)src[k] + 16u * (uint32_t)cj);
                         }
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
@@ -1660,7 +1689,7 @@ bool tc_plan(const MatmulArgs &a, TcPlan &pl, int group = 0) {
     off += (size_t)kDqWarps * kRawSlots * raw_slot;
     off = (off + 15) / 16 * 16;
     q.off_bar = (uint32_t)off;
-    off += (2 * kA + 2 * kB + 5) * 8 + 16;
+    off += (2 * kA + 2 * kB + 5) * 8 + 16 + 128;  // barriers, TMEM address, flag, sum table
     pl.smem = off + 1024;  // room to align the base to 1024 bytes
     if (pl.smem > kSmemLimitTc) return false;
     q.tmem_cols = (pl.BM >= 256 || ta) ? 512 : pl.BM == 128 ? 256 : 128;
